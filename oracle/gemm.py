@@ -1,0 +1,127 @@
+"""Reference block-scaled GEMM: D = out_round(epi(alpha * A_hat @ B_hat^T)), in float64.
+
+TEST INFRASTRUCTURE (part of the CPU oracle; see ``oracle/formats.py``).
+
+What it follows:
+* the operation and operand layouts of "Add Cutlass MxFp8 Block Scale Matrix
+  Multiplication" (``MxFp8GemmSm100``: A row-major M x K, B given as N x K
+  ("ColumnMajor" K x N), D row-major M x N, float accumulator, ``alpha_ptr`` in
+  the epilogue; its test compares against ``get_ref_results`` on the dequantised
+  operands);
+* the NVFP4 entry ``runNvfp4Gemm<T, kEnableSilu, kEnableBias>`` of "[QST]
+  Performance overhead: Frequent cuTensorMapEncodeTiled ...": a host float
+  alpha, an optional bias and an optional SiLU, output type T.
+
+The exact result of the method is a scaled dot product, so this is that
+definition written out: every element and scale is decoded through the explicit
+tables of ``formats``, the products are summed in float64 (``numpy.matmul`` is
+the library primitive for the sum), then
+
+    y = alpha * acc;  y = y + bias[n] (bias);  y = y / (1 + exp(-y)) (SiLU);
+    D = y rounded to nearest even in the output type.
+
+The scales are read from the swizzled buffers through ``layout.unswizzle`` so
+that the byte map of the scale layout is exercised end to end.
+"""
+
+import numpy as np
+
+from . import formats as F
+from . import layout as L
+from .quantize import MX_BLOCK, NV_BLOCK, unpack_e2m1
+
+MXFP8 = "mxfp8"
+NVFP4 = "nvfp4"
+BF16 = "bf16"
+F16 = "f16"
+
+
+def decode_operand(kind, codes, sf_buf, rows, K):
+    """Element codes + swizzled scales -> float64 [rows, K] holding element * block scale."""
+    if kind == MXFP8:
+        codes = np.asarray(codes, dtype=np.uint8).reshape(rows, K)
+        sf = L.unswizzle(sf_buf, rows, K // MX_BLOCK)
+        return F.decode_e4m3(codes) * np.repeat(F.decode_ue8m0(sf), MX_BLOCK, axis=1)
+    if kind == NVFP4:
+        codes = unpack_e2m1(np.asarray(codes, dtype=np.uint8).reshape(rows, K // 2), K)
+        sf = L.unswizzle(sf_buf, rows, K // NV_BLOCK)
+        return F.decode_e2m1(codes) * np.repeat(F.decode_ue4m3(sf), NV_BLOCK, axis=1)
+    raise ValueError(kind)
+
+
+def epilogue(acc, alpha, bias=None, silu=False):
+    """float64 accumulator -> float64 pre-rounding output (alpha, + bias[n], SiLU)."""
+    y = float(np.float32(alpha)) * np.asarray(acc, dtype=np.float64)
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)[None, :]
+    if silu:
+        with np.errstate(over="ignore"):
+            y = y * (1.0 / (1.0 + np.exp(-y)))
+    return y
+
+
+def round_out(y, out):
+    return F.round_to_bf16(y) if out == BF16 else F.round_to_f16(y)
+
+
+def out_bits(v, out):
+    return F.bf16_bits(v) if out == BF16 else F.f16_bits(v)
+
+
+def out_from_bits(bits, out):
+    return F.bf16_from_bits(bits) if out == BF16 else F.f16_from_bits(bits)
+
+
+def ulp_out(v, out):
+    return F.ulp_bf16(v) if out == BF16 else F.ulp_f16(v)
+
+
+def reference(kind, A, B, SFA, SFB, M, N, K, alpha=1.0, bias=None, silu=False, out=BF16,
+              rows=None):
+    """Reference D (float64 values, exactly representable in ``out``) and the pre-rounding y.
+
+    ``bias`` is a float64 vector of the (already rounded) bias values.  ``rows``
+    optionally selects a subset of output rows (for sampled checks of large
+    problems); the result then has len(rows) rows.
+    """
+    Ahat = decode_operand(kind, A, SFA, M, K)
+    if rows is not None:
+        Ahat = Ahat[np.asarray(rows)]
+    Bhat = decode_operand(kind, B, SFB, N, K)
+    acc = Ahat @ Bhat.T
+    y = epilogue(acc, alpha, bias, silu)
+    return round_out(y, out), y
+
+
+def abs_product_sum(kind, A, B, SFA, SFB, M, N, K, rows=None):
+    """sum_k |a_hat[m,k] * b_hat[n,k]| in float64 (the scale of the accumulation error)."""
+    Ahat = decode_operand(kind, A, SFA, M, K)
+    if rows is not None:
+        Ahat = Ahat[np.asarray(rows)]
+    Bhat = decode_operand(kind, B, SFB, N, K)
+    return np.abs(Ahat) @ np.abs(Bhat).T
+
+
+def tolerance(ref, got, abs_sum, alpha, silu, out):
+    """Per-element bound |alpha| * 2**-7 * sum|a b| (x 1.1 with SiLU) + 1 output ulp.
+
+    The ulp is taken at the larger of |ref| and |got|, so that the rounding of
+    either side to the output type is covered.
+    """
+    lip = 1.1 if silu else 1.0            # max |d silu / dy| = 1.0998...
+    mag = np.maximum(np.abs(ref), np.abs(got))
+    return abs(float(np.float32(alpha))) * 2.0 ** -7 * lip * abs_sum + ulp_out(mag, out)
+
+
+def gemm_naive(kind, A, B, SFA, SFB, M, N, K, alpha=1.0, bias=None, silu=False):
+    """Triple loop in plain Python floats (float64): the same definition, no library sum."""
+    Ahat = decode_operand(kind, A, SFA, M, K)
+    Bhat = decode_operand(kind, B, SFB, N, K)
+    acc = np.zeros((M, N), dtype=np.float64)
+    for m in range(M):
+        for n in range(N):
+            t = 0.0
+            for k in range(K):
+                t += float(Ahat[m, k]) * float(Bhat[n, k])
+            acc[m, n] = t
+    return epilogue(acc, alpha, bias, silu)

@@ -1,0 +1,162 @@
+"""Pins of the oracle GEMM and epilogue.
+
+* exact rational brute force on 4 x 4 x 32 (MXFP8) and 4 x 4 x 32 (NVFP4):
+  elements decoded by PyTorch's float8 decoders / the E2M1 value list, scales
+  read from the LINEAR (unswizzled) scale matrix, sums in Fractions;
+* one-hot rows select single decoded elements times their scales;
+* constant matrices give K * a * b * scales exactly;
+* A and B are not interchangeable (D[m, n] pairs row m of A with row n of B);
+* the triple loop and the library sum agree;
+* the epilogue: bias is per output column, SiLU(0) = 0 and SiLU(y) -> y for large y.
+"""
+
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import gemm as R
+from oracle import layout as L
+from oracle import quantize as Q
+from fp4_gemm_blackwell_gb300 import synth
+
+E2M1_LIST = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+
+
+def _torch_e4m3(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _torch_e8m0(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+
+
+def _e2m1_from_list(code):
+    v = E2M1_LIST[code & 7]
+    return -v if code & 8 else v
+
+
+def _mx_operands(rows, K, seed, scale_spread=6):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 256, size=(rows, K), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C                              # no NaN codes
+    sf = rng.integers(127 - scale_spread, 127 + scale_spread + 1, size=(rows, K // 32), dtype=np.uint8)
+    return codes, sf
+
+
+def _nv_operands(rows, K, seed):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, size=(rows, K), dtype=np.uint8)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sf = rng.integers(1, 127, size=(rows, K // 16), dtype=np.uint8)
+    return codes, packed, sf
+
+
+def test_mx_bruteforce_4x4x32_exact():
+    M = N = 4
+    K = 32 * 2
+    a, sfa = _mx_operands(M, K, 1)
+    b, sfb = _mx_operands(N, K, 2)
+    ad, bd = _torch_e4m3(a), _torch_e4m3(b)
+    sa, sb = _torch_e8m0(sfa), _torch_e8m0(sfb)
+    got, _ = R.reference(R.MXFP8, a, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K, out=R.BF16)
+    y = R.reference(R.MXFP8, a, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K, out=R.BF16)[1]
+    for m in range(M):
+        for n in range(N):
+            acc = sum(Fraction(ad[m, k]) * Fraction(sa[m, k // 32]) * Fraction(bd[n, k]) * Fraction(sb[n, k // 32])
+                      for k in range(K))
+            assert abs(Fraction(y[m, n]) - acc) <= abs(acc) * Fraction(1, 2 ** 50)
+    assert np.all(np.isfinite(got))
+
+
+def test_nv_bruteforce_4x4x32_exact():
+    M = N = 4
+    K = 32
+    ac, ap, sfa = _nv_operands(M, K, 3)
+    bc, bp, sfb = _nv_operands(N, K, 4)
+    sa, sb = _torch_e4m3(sfa), _torch_e4m3(sfb)
+    alpha = np.float32(0.375)
+    _, y = R.reference(R.NVFP4, ap, bp, L.swizzle(sfa), L.swizzle(sfb), M, N, K, alpha=alpha, out=R.F16)
+    for m in range(M):
+        for n in range(N):
+            acc = sum(Fraction(_e2m1_from_list(ac[m, k])) * Fraction(sa[m, k // 16]) *
+                      Fraction(_e2m1_from_list(bc[n, k])) * Fraction(sb[n, k // 16]) for k in range(K))
+            assert Fraction(y[m, n]) == Fraction(float(alpha)) * acc       # exact in float64 here
+
+
+def test_one_hot_rows_select_elements():
+    M, N, K = 8, 8, 64
+    b, sfb = _mx_operands(N, K, 5)
+    a = np.zeros((M, K), dtype=np.uint8)
+    sfa = np.full((M, K // 32), 127, dtype=np.uint8)                   # scale 1
+    picks = [3, 17, 32, 40, 63, 0, 31, 50]
+    for m, k in enumerate(picks):
+        a[m, k] = 0x38                                                 # E4M3 1.0
+    _, y = R.reference(R.MXFP8, a, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K)
+    bd = _torch_e4m3(b) * np.repeat(_torch_e8m0(sfb), 32, axis=1)
+    for m, k in enumerate(picks):
+        assert np.array_equal(y[m], bd[:, k])
+
+
+def test_constant_matrices_closed_form():
+    M, N, K = 16, 24, 256
+    a = np.full((M, K), 0x44, dtype=np.uint8)                          # E4M3 0x44 = 1.5 * 2^1 = 3
+    b = np.full((N, K), 0xBA, dtype=np.uint8)                          # -(1.25) = -1.25
+    sfa = np.full((M, K // 32), 129, dtype=np.uint8)                   # 4
+    sfb = np.full((N, K // 32), 124, dtype=np.uint8)                   # 1/8
+    _, y = R.reference(R.MXFP8, a, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K, alpha=2.0)
+    assert np.all(y == 2.0 * K * 3.0 * -1.25 * 4 * 0.125)
+    # NVFP4: element 0x3 = 1.5, 0xC = -2; scales 0x40 = 2 and 0x30 = 0.5
+    ap = np.full((M, K // 2), 0x33, dtype=np.uint8)
+    bp = np.full((N, K // 2), 0xCC, dtype=np.uint8)
+    _, y2 = R.reference(R.NVFP4, ap, bp, L.swizzle(np.full((M, K // 16), 0x40, np.uint8)),
+                        L.swizzle(np.full((N, K // 16), 0x30, np.uint8)), M, N, K)
+    assert np.all(y2 == K * 1.5 * -2.0 * 2.0 * 0.5)
+
+
+def test_operands_are_not_interchangeable():
+    M, N, K = 4, 6, 32
+    a, sfa = _mx_operands(M, K, 8)
+    b, sfb = _mx_operands(N, K, 9)
+    _, y = R.reference(R.MXFP8, a, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K)
+    ad = _torch_e4m3(a) * np.repeat(_torch_e8m0(sfa), 32, axis=1)
+    bd = _torch_e4m3(b) * np.repeat(_torch_e8m0(sfb), 32, axis=1)
+    assert y.shape == (M, N)
+    for m in range(M):
+        for n in range(N):
+            assert y[m, n] == pytest.approx(float(np.dot(ad[m], bd[n])), rel=1e-12, abs=1e-300)
+
+
+def test_naive_loop_matches_library_sum_with_epilogue():
+    M, N, K = 5, 7, 64
+    xa = synth.normal_rowscaled(M, K, 11)
+    xb = synth.normal_rowscaled(N, K, 12)
+    ap, sfa, sa = Q.quantize_nvfp4(xa)
+    bp, sfb, sb = Q.quantize_nvfp4(xb)
+    alpha = np.float32(sa * sb)
+    _, bias = synth.bias(N)
+    _, y = R.reference(R.NVFP4, ap, bp, L.swizzle(sfa), L.swizzle(sfb), M, N, K, alpha=alpha, bias=bias, silu=True)
+    y2 = R.gemm_naive(R.NVFP4, ap, bp, L.swizzle(sfa), L.swizzle(sfb), M, N, K, alpha=alpha, bias=bias, silu=True)
+    assert np.allclose(y, y2, rtol=1e-13, atol=1e-15)
+
+
+def test_epilogue_closed_forms():
+    acc = np.array([[0.0, 0.0, 50.0, -50.0]])
+    bias = np.array([0.0, 1.0, 0.0, 0.0])
+    y = R.epilogue(acc, 1.0, bias, silu=True)
+    assert y[0, 0] == 0.0
+    assert y[0, 1] == pytest.approx(1.0 / (1.0 + np.exp(-1.0)))
+    assert y[0, 2] == pytest.approx(50.0, rel=1e-20)
+    assert abs(y[0, 3]) < 1e-19
+    # bias goes with the output column
+    acc2 = np.zeros((3, 4))
+    y2 = R.epilogue(acc2, 1.0, np.arange(4.0), silu=False)
+    assert np.array_equal(y2, np.tile(np.arange(4.0), (3, 1)))
+
+
+def test_tolerance_covers_rounding_only_cases():
+    ref = np.array([1.0, 100.0])
+    tol = R.tolerance(ref, ref, np.zeros(2), 1.0, False, R.BF16)
+    assert np.array_equal(tol, F.ulp_bf16(ref))

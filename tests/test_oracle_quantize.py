@@ -1,0 +1,151 @@
+"""Pins of the oracle's quantisers: exact rational invariants and brute force.
+
+MXFP8: the scale exponent is the least e with amax <= 448 * 2**e (checked with
+exact fractions), and every element is the nearest E4M3 value of x / 2**e
+(exhaustive search).  NVFP4: hand-chosen inputs where every float32 step is
+exact, so the codes are known in closed form; the general case is checked
+element by element against an exhaustive nearest-value search of x / den.
+"""
+
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import formats as F
+from oracle import quantize as Q
+from fp4_gemm_blackwell_gb300 import synth
+
+
+def _nearest_brute(v, table, maxv, ncodes):
+    mag = min(abs(v), maxv)
+    best = None
+    for c in range(ncodes):
+        t = table[c]
+        if np.isnan(t) or t < 0 or (t == 0 and np.signbit(t)):
+            continue
+        d = abs(Fraction(mag) - Fraction(t))
+        if best is None or d < best[0] or (d == best[0] and c % 2 == 0):
+            best = (d, c)
+    return best[1]
+
+
+def test_mx_scale_exponent_is_minimal_exact():
+    rng = np.random.default_rng(0)
+    amax = np.concatenate([np.abs(rng.normal(0, 1, 500)) * 10.0 ** rng.integers(-30, 30, 500),
+                           [448.0, 448.0 * 2 ** 5, 448.0 * 2 ** -9, np.nextafter(448.0, 1e9, dtype=np.float32),
+                            np.nextafter(448.0, 0, dtype=np.float32), 1.0, 3.4e38]]).astype(np.float32)
+    for a in amax:
+        e = Q.mx_scale_exponent(a)
+        fa = Fraction(float(a))
+        assert fa <= 448 * Fraction(2) ** e
+        assert fa > 448 * Fraction(2) ** (e - 1)
+    vec = Q.mx_scale_exponents(amax.astype(np.float64))
+    assert list(vec) == [Q.mx_scale_exponent(a) for a in amax]
+    # boundaries: amax exactly 448 * 2^k gives e = k; one float32 ulp above gives k + 1
+    assert Q.mx_scale_exponent(448.0) == 0
+    assert Q.mx_scale_exponent(448.0 * 2 ** 3) == 3
+    assert Q.mx_scale_exponent(float(np.nextafter(np.float32(448.0), np.float32(1e9)))) == 1
+    assert Q.mx_scale_exponent(0.0) == -127
+    assert Q.mx_scale_exponent(1e-45) == -127                         # clamp
+
+
+def test_mx_quantiser_against_brute_force():
+    x = synth.normal(4, 96, seed=5) * np.float32(3.0)
+    x[1, :32] *= np.float32(1e-6)                                      # a small block
+    x[2, 32:64] = 0.0                                                  # an all-zero block
+    codes, scales = Q.quantize_mxfp8(x)
+    assert codes.shape == (4, 96) and scales.shape == (4, 3)
+    for r in range(4):
+        for b in range(3):
+            blk = x[r, 32 * b:32 * b + 32].astype(np.float64)
+            e = int(scales[r, b]) - 127
+            amax = np.max(np.abs(blk))
+            if amax == 0:
+                assert e == -127
+                assert np.all(codes[r, 32 * b:32 * b + 32] == 0)
+                continue
+            assert Fraction(amax) <= 448 * Fraction(2) ** e < 2 * Fraction(amax)
+            for j in range(32):
+                q = blk[j] * 2.0 ** -e
+                want = _nearest_brute(q, F.E4M3_VALUES, 448.0, 127)
+                if np.signbit(q):
+                    want |= 0x80
+                assert codes[r, 32 * b + j] == want
+
+
+def test_mx_block_max_maps_inside_range():
+    x = synth.normal(64, 256, seed=9) * np.float32(1000.0)
+    codes, scales = Q.quantize_mxfp8(x)
+    dec = F.decode_e4m3(codes).reshape(64, 8, 32)
+    assert np.all(np.abs(dec) <= 448.0)
+    # each block's largest magnitude lands in the top binade [256, 448]
+    assert np.all(np.max(np.abs(dec), axis=2) >= 224.0)
+
+
+def test_nv_closed_form_case():
+    # amax_tensor = 2688 -> s = 1 exactly; a block with amax 6 -> t = 1 -> scale 1.0 (code 0x38);
+    # den = 1, so every element is E2M1(x) directly, ties included.
+    row0 = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -5.0, 0.1, 0.3, 4.4, -6.0, 1.0],
+                    dtype=np.float32)
+    row1 = np.zeros(16, dtype=np.float32)
+    row1[0] = 2688.0
+    x = np.stack([row0, row1])
+    packed, sc, s = Q.quantize_nvfp4(x)
+    assert s == np.float32(1.0)
+    assert sc[0, 0] == 0x38
+    assert sc[1, 0] == 0x7E                                           # 2688 / 6 = 448 -> max UE4M3
+    codes = Q.unpack_e2m1(packed, 16)[0]
+    vals = F.decode_e2m1(codes)
+    assert list(vals) == [6.0, 0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, -0.0, -1.0, -4.0, 0.0, 0.5, 4.0, -6.0, 1.0]
+    # nibble order: element 0 in the low nibble
+    assert packed[0, 0] & 0xF == codes[0] and packed[0, 0] >> 4 == codes[1]
+
+
+def test_nv_quantiser_against_brute_force():
+    x = synth.normal_rowscaled(6, 64, seed=4)
+    packed, sc, s = Q.quantize_nvfp4(x)
+    assert s == np.float32(np.float32(np.max(np.abs(x))) / np.float32(2688.0))
+    codes = Q.unpack_e2m1(packed, 64)
+    d = np.float32(np.float32(6.0) * s)
+    for r in range(6):
+        for b in range(4):
+            blk = x[r, 16 * b:16 * b + 16]
+            t = np.float32(np.float32(np.max(np.abs(blk))) / d)
+            want_sc = _nearest_brute(float(t), F.E4M3_VALUES, 448.0, 127)
+            assert sc[r, b] == want_sc
+            den = np.float32(np.float32(F.E4M3_VALUES[want_sc]) * s)
+            for j in range(16):
+                q = float(np.float32(blk[j] / den))
+                want = _nearest_brute(q, F.E2M1_VALUES, 6.0, 8) | (0x8 if np.signbit(q) else 0)
+                assert codes[r, 16 * b + j] == want
+
+
+def test_nv_tensor_amax_block_gets_max_scale():
+    x = synth.normal_rowscaled(32, 128, seed=8)
+    packed, sc, s = Q.quantize_nvfp4(x)
+    r, c = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert sc[r, c // 16] == 0x7E
+
+
+def test_nv_all_zero_tensor():
+    packed, sc, s = Q.quantize_nvfp4(np.zeros((4, 32), dtype=np.float32))
+    assert s == 0 and not packed.any() and not sc.any()
+
+
+@pytest.mark.parametrize("kind", ["mx", "nv"])
+def test_dequantised_error_is_within_half_step(kind):
+    x = synth.normal(16, 128, seed=21)
+    if kind == "mx":
+        codes, scales = Q.quantize_mxfp8(x)
+        deq = F.decode_e4m3(codes) * np.repeat(F.decode_ue8m0(scales), 32, axis=1)
+        # E4M3 relative step 2^-3 in normal range: |err| <= 2^-4 * |x| + tiny subnormal step
+        step = np.repeat(F.decode_ue8m0(scales), 32, axis=1) * 2.0 ** -9
+        assert np.all(np.abs(deq - x) <= np.abs(x) * 2.0 ** -4 + step / 2 + 1e-30)
+    else:
+        packed, sc, s = Q.quantize_nvfp4(x)
+        codes = Q.unpack_e2m1(packed, 128)
+        scale = np.repeat(F.decode_ue4m3(sc), 16, axis=1) * float(s)
+        deq = F.decode_e2m1(codes) * scale
+        # E2M1 spacing is at most 2 (between 4 and 6), so |err| <= 1 * block scale, plus scale rounding
+        assert np.all(np.abs(deq - x) <= 1.0 * scale * 1.07 + 1e-30)
