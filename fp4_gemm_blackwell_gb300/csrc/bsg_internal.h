@@ -1,0 +1,70 @@
+// Internal declarations shared by the host side and the kernels of the block-scaled GEMM.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bsg {
+
+enum : int { KIND_MX = 0, KIND_NV = 1 };
+enum : int { OUT_F16 = 0, OUT_BF16 = 1 };
+enum : unsigned { F_BIAS = 1u, F_SILU = 2u, F_ALPHA_DEVICE = 4u };
+
+// Bits of the device status word (OR-ed in by a CTA that gives up a wait).
+enum : unsigned {
+  ST_TIMEOUT_PRODUCER = 1u << 0,
+  ST_TIMEOUT_MMA = 1u << 1,
+  ST_TIMEOUT_EPILOGUE = 1u << 2,
+  ST_TIMEOUT_DRAIN = 1u << 3,
+};
+
+// Kernel parameters, passed by value as a __grid_constant__ (the tensor maps must live in
+// parameter space for the TMA instructions).
+struct GemmParams {
+  CUtensorMap tmap_a;  // A codes: bytes, dims {K bytes, M}, box {128, 128}, 128-byte swizzle
+  CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N}, box {128, BN}, 128-byte swizzle
+  const uint8_t* sfa;  // swizzled 128x4 scale atoms of A
+  const uint8_t* sfb;
+  const void* bias;    // N values of the output type (flags & F_BIAS)
+  void* d;             // M x N output, row-major
+  const float* alpha_dev;
+  float* partial;      // split-K partial tiles (splits x tiles x 128 x BN floats)
+  unsigned* counters;  // split-K arrival counter per tile (0 between launches)
+  unsigned* status;    // device status word
+  unsigned long long wait_limit_ns;
+  float alpha;
+  int M, N, K;
+  unsigned flags;
+  int sfa_atoms_per_band;  // padded scale columns / 4 of A
+  int sfb_atoms_per_band;
+  int sfb_bands;           // padded rows / 128 of B
+  int num_m_tiles, num_n_tiles, num_k_tiles;
+  int num_tiles;
+  int splits;              // split-K factor (every split owns >= 1 k-tile)
+  int k_tiles_per_split;
+  int num_units;           // num_tiles * splits
+  int group_m;             // tile rasterisation: m-blocks per group
+  int debug_skip_first_load;  // test hook: the producer never loads its first stage
+};
+
+struct GemmKernelInfo {
+  const void* fn;
+  int smem_bytes;
+  int threads;
+  int bn;
+  int stages;
+};
+
+// Look up a kernel instantiation: tile width bn (128 or 256), out (OUT_*).
+bool gemm_kernel_info_mx(int bn, int out, GemmKernelInfo* info);
+bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info);
+
+// Quantisers (stream-ordered).  See bsg_quantize in include/bsgemm.h.
+cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               cudaStream_t s);
+cudaError_t launch_quantize_nv(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               float* global_scale, cudaStream_t s);
+
+}  // namespace bsg

@@ -1,0 +1,477 @@
+// Block-scaled GEMM kernel for sm_103a: D = alpha * (A . B^T) (+ bias[n]) (-> SiLU).
+//
+// One persistent CTA per SM, six warps with fixed roles:
+//   warp 0      TMA producer: A / B code tiles (128-byte swizzled) and the matching 128x4 scale
+//               atoms into a STAGES-deep shared-memory ring (mbarrier full / empty pairs);
+//   warp 1      owns tensor memory; one thread copies the scale atoms into TMEM (tcgen05.cp)
+//               and issues the block-scaled tcgen05.mma chain into an FP32 accumulator;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes 32*(w%4)..),
+//               alpha, bias, SiLU, FP16/BF16 rounding and stores; with split-K, FP32 partial
+//               tiles in the workspace and a deterministic reduction by the last split.
+// Tile 128 x BN x (128 bytes of K): MXFP8 = 128 E4M3 per row per stage (four K=32 MMAs, one
+// UE8M0 scale each), NVFP4 = 256 E2M1 per row per stage (four K=64 MMAs, four UE4M3 each).
+//
+// The operation, formats and the 1-SM 128-row tile follow "Add Cutlass MxFp8 Block Scale
+// Matrix Multiplication" (MxFp8GemmSm100, PerSmTileShape 128 x 256 x 256) and "[QST]
+// Performance overhead ..." (KernelConfigM128: 1-SM 128 x 256 tiles; runNvfp4Gemm with the
+// kEnableBias / kEnableSilu epilogue), re-derived for a persistent, warp-specialised schedule.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bsg_internal.h"
+#include "ptx.cuh"
+
+namespace bsg {
+
+template <int KIND, int BN>
+struct GemmCfg {
+  static_assert(BN == 128 || BN == 256, "tile width");
+  static constexpr int BM = 128;
+  static constexpr int BK_BYTES = 128;
+  static constexpr int K_TILE = KIND == KIND_MX ? 128 : 256;  // elements per k-tile
+  static constexpr int MMA_K = KIND == KIND_MX ? 32 : 64;     // elements per MMA
+  static constexpr int STEPS = K_TILE / MMA_K;                // MMAs per k-tile (4)
+  static constexpr int SF_ATOMS = KIND == KIND_MX ? 1 : 4;    // 128x4 atoms per band per k-tile
+  static constexpr int NB = BN / 128;                         // 128-row bands of B per tile
+  static constexpr int A_BYTES = BM * BK_BYTES;
+  static constexpr int B_BYTES = BN * BK_BYTES;
+  static constexpr int SFA_BYTES = SF_ATOMS * 512;
+  static constexpr int SFB_BYTES = NB * SF_ATOMS * 512;
+  static constexpr int STAGE_RAW = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
+  static constexpr int SMEM_LIMIT = 232448;  // 227 KB per CTA
+  static constexpr int AUX_BYTES = 1024;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - AUX_BYTES - 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;
+  static constexpr int NACC = BN <= 128 ? 2 : 1;             // accumulator buffers in TMEM
+  static constexpr int SFA_COLS = 4 * SF_ATOMS;
+  static constexpr int SFB_COLS = 4 * SF_ATOMS * NB;
+  static constexpr int SF_SLOT_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int SF_COL0 = NACC * BN;
+  static constexpr int TMEM_USED = SF_COL0 + 2 * SF_SLOT_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int THREADS = 192;
+  // Instruction descriptor (block-scaled kinds): [4,6) B scale id, [7,10) A type,
+  // [10,13) B type, [15]/[16] A/B major (0 = K), [17,23) N >> 3, [23] scale type
+  // (1 = UE8M0, 0 = UE4M3), [24,29) M >> 4, [29,31) A scale id.
+  static constexpr uint32_t IDESC =
+      (KIND == KIND_MX ? ((0u << 7) | (0u << 10) | (1u << 23))    // E4M3 x E4M3, UE8M0
+                       : ((1u << 7) | (1u << 10) | (0u << 23)))   // E2M1 x E2M1, UE4M3
+      | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+  static_assert(STAGES >= 2, "ring too shallow");
+  static_assert(STAGES <= 8, "barrier slots");
+  static_assert(TMEM_USED <= 512, "tensor memory");
+};
+
+struct UnitCoord {
+  int m_blk, n_blk, split, tile, kt0, kt1;
+};
+
+__device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u) {
+  UnitCoord c;
+  c.split = u % p.splits;
+  c.tile = u / p.splits;
+  const int per_group = p.group_m * p.num_n_tiles;
+  const int g = c.tile / per_group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.num_m_tiles - first_m, p.group_m);
+  const int r = c.tile - g * per_group;
+  c.m_blk = first_m + r % gm;
+  c.n_blk = r / gm;
+  c.kt0 = c.split * p.k_tiles_per_split;
+  c.kt1 = min(c.kt0 + p.k_tiles_per_split, p.num_k_tiles);
+  return c;
+}
+
+// Bounded mbarrier wait.  Gives up when another role flagged an abort, or after the
+// plan's time limit (then flags the abort and records `who` in the status word).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             const GemmParams& p, unsigned who) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+      *abort_flag = 1;
+      atomicOr(p.status, who);
+      return false;
+    }
+  }
+}
+
+// Named-barrier AND over `nthreads` threads: every participant gets the same answer.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "barrier.cta.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (OUT == OUT_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <int OUT>
+__device__ __forceinline__ float out_to_float(uint16_t bits) {
+  if constexpr (OUT == OUT_BF16) {
+    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+  } else {
+    return __half2float(__ushort_as_half(bits));
+  }
+}
+
+// Epilogue of 32 consecutive columns n0.. of output row m held by this thread.
+template <int OUT>
+__device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0, const float* v,
+                                              float alpha) {
+  if (m >= p.M) return;
+  uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int n = n0 + 8 * g;
+    if (n >= p.N) break;  // N % 16 == 0: groups of 8 are whole
+    float y[8];
+    if (p.flags & F_BIAS) {
+      const uint4 braw =
+          __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias) + n));
+      const uint16_t* b = reinterpret_cast<const uint16_t*>(&braw);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = __fmaf_rn(alpha, v[8 * g + i], out_to_float<OUT>(b[i]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(alpha, v[8 * g + i]);
+    }
+    if (p.flags & F_SILU) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = y[i] / (1.0f + __expf(-y[i]));
+    }
+    uint4 o;
+    o.x = pack2<OUT>(y[0], y[1]);
+    o.y = pack2<OUT>(y[2], y[3]);
+    o.z = pack2<OUT>(y[4], y[5]);
+    o.w = pack2<OUT>(y[6], y[7]);
+    *reinterpret_cast<uint4*>(drow + n) = o;
+  }
+}
+
+template <int KIND, int BN, int OUT>
+__global__ void __launch_bounds__(192, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = GemmCfg<KIND, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+  const uint32_t smem0 = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint8_t* aux = smem + C::STAGES * C::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(aux);
+  // barrier slots: full[0..7], empty[8..15], tmem_full[16..17], tmem_empty[18..19], drain[20]
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + 8 + s); };
+  auto bar_tfull = [&](int a) { return smem_u32(bars + 16 + a); };
+  auto bar_tempty = [&](int a) { return smem_u32(bars + 18 + a); };
+  const uint32_t bar_drain = smem_u32(bars + 20);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 21);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 22);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(bars + 23);
+
+  auto stage_a = [&](int s) { return smem0 + s * C::STAGE_BYTES; };
+  auto stage_b = [&](int s) { return smem0 + s * C::STAGE_BYTES + C::A_BYTES; };
+  auto stage_sfa = [&](int s) { return smem0 + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES; };
+  auto stage_sfb = [&](int s) {
+    return smem0 + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES + C::SFA_BYTES;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull(a), 1);
+      mbar_init(bar_tempty(a), 128);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    prefetch_tmap(&p.tmap_a);
+    prefetch_tmap(&p.tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool first = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        const UnitCoord c = decode_unit(p, u);
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          const int k_rem = p.K - kt * C::K_TILE;
+          const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
+          const int sf_atoms = KIND == KIND_MX ? 1 : steps;
+          int bands = 0;
+#pragma unroll
+          for (int rb = 0; rb < C::NB; ++rb) bands += (c.n_blk * C::NB + rb < p.sfb_bands) ? 1 : 0;
+          const uint32_t bytes = C::A_BYTES + C::B_BYTES + (1 + bands) * sf_atoms * 512;
+          if (first && p.debug_skip_first_load) {
+            // test hook: leave this stage unfilled so that the MMA warp's wait runs out
+          } else {
+            const uint32_t fb = bar_full(stage);
+            mbar_arrive_expect_tx(fb, bytes);
+            tma_load_2d(stage_a(stage), &p.tmap_a, fb, kt * C::BK_BYTES, c.m_blk * C::BM);
+            tma_load_2d(stage_b(stage), &p.tmap_b, fb, kt * C::BK_BYTES, c.n_blk * BN);
+            const uint8_t* sa = p.sfa + (static_cast<size_t>(c.m_blk) * p.sfa_atoms_per_band +
+                                         static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
+            bulk_load(stage_sfa(stage), sa, sf_atoms * 512, fb);
+#pragma unroll
+            for (int rb = 0; rb < C::NB; ++rb) {
+              const int band = c.n_blk * C::NB + rb;
+              if (band < p.sfb_bands) {
+                const uint8_t* sb = p.sfb + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
+                                             static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
+                bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512, sb, sf_atoms * 512, fb);
+              }
+            }
+          }
+          first = false;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      int slot = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        const UnitCoord c = decode_unit(p, u);
+        if (!wait_bounded(bar_tempty(acc), acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          if (!wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int k_rem = p.K - kt * C::K_TILE;
+          const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
+          const uint32_t sfa_t = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
+          const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+          const uint32_t sa = stage_a(stage), sb = stage_b(stage);
+          const uint32_t ssfa = stage_sfa(stage), ssfb = stage_sfb(stage);
+          if constexpr (KIND == KIND_MX) {
+            tc_cp_sf_atom(sfa_t, sdesc_sf_atom(ssfa));
+#pragma unroll
+            for (int rb = 0; rb < C::NB; ++rb)
+              tc_cp_sf_atom(sfb_t + 4 * rb, sdesc_sf_atom(ssfb + rb * 512));
+            for (int j = 0; j < steps; ++j) {
+              const uint32_t idesc = C::IDESC | (static_cast<uint32_t>(j) << 4) |
+                                     (static_cast<uint32_t>(j) << 29);
+              tc_mma_mxf8(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
+                          idesc, sfa_t, sfb_t, (kt > c.kt0 || j > 0) ? 1u : 0u);
+            }
+          } else {
+            for (int j = 0; j < steps; ++j) {
+              tc_cp_sf_atom(sfa_t + 4 * j, sdesc_sf_atom(ssfa + 512 * j));
+#pragma unroll
+              for (int rb = 0; rb < C::NB; ++rb)
+                tc_cp_sf_atom(sfb_t + 4 * C::NB * j + 4 * rb,
+                              sdesc_sf_atom(ssfb + rb * C::SF_ATOMS * 512 + 512 * j));
+            }
+            for (int j = 0; j < steps; ++j) {
+              tc_mma_nvf4(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
+                          C::IDESC, sfa_t + 4 * j, sfb_t + 4 * C::NB * j,
+                          (kt > c.kt0 || j > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(bar_empty(stage));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          slot ^= 1;
+        }
+        if (!ok) break;
+        tc_commit(bar_tfull(acc));
+        if (C::NACC == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // let every tensor-core operation issued so far finish before TMEM is released
+        tc_commit(bar_drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar_drain, 0)) {
+          if (globaltimer_ns() - t0 > 10000000ull) {
+            atomicOr(p.status, ST_TIMEOUT_DRAIN);
+            break;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;       // accumulator row = TMEM lane
+    const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+      const UnitCoord c = decode_unit(p, u);
+      bool ok = wait_bounded(bar_tfull(acc), acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
+      ok = named_bar_and(1, 128, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+      const int m = c.m_blk * C::BM + row;
+      const int nbase = c.n_blk * BN;
+      if (p.splits == 1) {
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + ch * 32, r);
+          tmem_ld_wait();
+          if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar_tempty(acc));
+          }
+          store_chunk32<OUT>(p, m, nbase + ch * 32, reinterpret_cast<const float*>(r), alpha);
+        }
+      } else {
+        float4* part = reinterpret_cast<float4*>(
+            p.partial + (static_cast<size_t>(c.split) * p.num_tiles + c.tile) * (C::BM * BN));
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + ch * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float4 v4 = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                    __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+            __stcg(part + (ch * 8 + g) * C::BM + row, v4);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_tempty(acc));
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 64) {
+          const unsigned old = atomicAdd(p.counters + c.tile, 1u);
+          const int last = (old == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+          if (last) p.counters[c.tile] = 0u;  // ready for the next launch
+          *last_flag = last;
+        }
+        named_bar_sync(1, 128);
+        if (*last_flag) {
+          __threadfence();
+          const float4* base = reinterpret_cast<const float4*>(
+              p.partial + static_cast<size_t>(c.tile) * (C::BM * BN));
+          const size_t split_stride = static_cast<size_t>(p.num_tiles) * (C::BM * BN) / 4;
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            for (int s = 0; s < p.splits; ++s) {
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                const float4 t = __ldcg(base + s * split_stride + (ch * 8 + g) * C::BM + row);
+                v[4 * g] += t.x;
+                v[4 * g + 1] += t.y;
+                v[4 * g + 2] += t.z;
+                v[4 * g + 3] += t.w;
+              }
+            }
+            store_chunk32<OUT>(p, m, nbase + ch * 32, v, alpha);
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+      if (C::NACC == 2) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      } else {
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // give copies that were already in flight time to land before the CTA's smem goes away
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int KIND, int BN, int OUT>
+bool fill_kernel_info(GemmKernelInfo* info) {
+  using C = GemmCfg<KIND, BN>;
+  info->fn = reinterpret_cast<const void*>(&bsg_gemm_kernel<KIND, BN, OUT>);
+  info->smem_bytes = C::SMEM_BYTES;
+  info->threads = C::THREADS;
+  info->bn = BN;
+  info->stages = C::STAGES;
+  return true;
+}
+
+}  // namespace bsg

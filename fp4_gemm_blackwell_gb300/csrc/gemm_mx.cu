@@ -1,0 +1,14 @@
+// MXFP8 (E4M3 elements, UE8M0 per-32 scales) instantiations of the block-scaled GEMM kernel.
+#include "gemm_kernel.cuh"
+
+namespace bsg {
+
+bool gemm_kernel_info_mx(int bn, int out, GemmKernelInfo* info) {
+  if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_MX, 128, OUT_F16>(info);
+  if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 128, OUT_BF16>(info);
+  if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_MX, 256, OUT_F16>(info);
+  if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 256, OUT_BF16>(info);
+  return false;
+}
+
+}  // namespace bsg

@@ -1,0 +1,14 @@
+// NVFP4 (E2M1 elements, UE4M3 per-16 scales) instantiations of the block-scaled GEMM kernel.
+#include "gemm_kernel.cuh"
+
+namespace bsg {
+
+bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info) {
+  if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_NV, 128, OUT_F16>(info);
+  if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 128, OUT_BF16>(info);
+  if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_NV, 256, OUT_F16>(info);
+  if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 256, OUT_BF16>(info);
+  return false;
+}
+
+}  // namespace bsg

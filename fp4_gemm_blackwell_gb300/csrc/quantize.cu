@@ -1,0 +1,210 @@
+// Quantisers: row-major float32 -> block-scaled codes + swizzled 128x4 scale atoms.
+//
+// MXFP8 ("Add Cutlass MxFp8 Block Scale Matrix Multiplication", test step
+// pytorch_mxfp8_quantize with block size 32, then linear_to_swizzled_128_4): per 32-element
+// K-block, scale 2^e with e the least integer such that amax <= 448 * 2^e, elements E4M3 of
+// x * 2^-e rounded to nearest even with saturation.
+// NVFP4 (the Nvf4 kernels of "[QST] Performance overhead ..."): s = amax / 2688 per tensor,
+// per 16-element block UE4M3(amax_blk / (6 s)), elements E2M1(x / (scale * s)); each step one
+// float32 operation rounded to nearest even.
+//
+// One thread per (row, block) of the PADDED scale matrix, so every byte of the swizzled scale
+// buffer, padding included, is written by the call.
+#include <cstdint>
+
+#include "bsg_internal.h"
+#include "ptx.cuh"
+
+namespace bsg {
+
+// Byte offset of scale (r, c) in the swizzled buffer (cols4 = padded scale columns / 4).
+__device__ __forceinline__ size_t sf_swizzle_offset(int r, int c, int cols4) {
+  const size_t atom = static_cast<size_t>(r >> 7) * cols4 + (c >> 2);
+  return atom * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+// e = least integer with a <= 448 * 2^e, clamped to [-127, 127], for finite a >= 0.
+// With a = (1 + f) 2^(E-127) (E the biased exponent field) and 448 = 1.75 * 2^8:
+// a <= 448 * 2^e  <=>  e >= E - 135 when f <= 0.75, else e >= E - 134.
+__device__ __forceinline__ int mx_exponent(float a) {
+  const uint32_t bits = __float_as_uint(a);
+  const int E = static_cast<int>(bits >> 23);
+  const uint32_t frac = bits & 0x7FFFFFu;
+  if (E == 0) return -127;  // zero or subnormal: far below 448 * 2^-127
+  int e = E - 135 + (frac > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-e as float32 for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float exp2_neg(int e) {
+  const int be = 127 - e;
+  return be >= 1 ? __uint_as_float(static_cast<uint32_t>(be) << 23) : __uint_as_float(0x00400000u);
+}
+
+__global__ void __launch_bounds__(256) quantize_mx_kernel(const float* __restrict__ x, int rows, int K,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ sf, int rows_pad,
+                                                          int cols4) {
+  const int nblk = K / 32;
+  const int cols_pad = cols4 * 4;
+  const long long total = static_cast<long long>(rows_pad) * cols_pad;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / cols_pad);
+    const int c = static_cast<int>(i % cols_pad);
+    uint8_t code = 0;
+    if (r < rows && c < nblk) {
+      const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(r) * K + c * 32);
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 t = __ldg(src + j);
+        v[4 * j] = t.x;
+        v[4 * j + 1] = t.y;
+        v[4 * j + 2] = t.z;
+        v[4 * j + 3] = t.w;
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      const int e = mx_exponent(amax);
+      const float inv = exp2_neg(e);
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[4 * j], inv), __fmul_rn(v[4 * j + 1], inv));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[4 * j + 2], inv), __fmul_rn(v[4 * j + 3], inv));
+        w[j] = lo | (hi << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(codes + static_cast<size_t>(r) * K + c * 32);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      code = static_cast<uint8_t>(e + 127);
+    }
+    sf[sf_swizzle_offset(r, c, cols4)] = code;
+  }
+}
+
+// amax(|x|) into *amax_bits (float bits; non-negative floats order like unsigned integers).
+__global__ void __launch_bounds__(256) amax_kernel(const float* __restrict__ x, long long n,
+                                                   unsigned* __restrict__ amax_bits) {
+  float m = 0.0f;
+  const long long n4 = n / 4;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 t = __ldg(x4 + i);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(t.x), fabsf(t.y)), fmaxf(fabsf(t.z), fabsf(t.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wmax[8];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = 0.0f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) b = fmaxf(b, wmax[w]);
+    atomicMax(amax_bits, __float_as_uint(b));
+  }
+}
+
+// E4M3 code with the sign bit clear -> exact float value.
+__device__ __forceinline__ float ue4m3_value(uint32_t code) {
+  const uint32_t e = (code >> 3) & 0xFu, m = code & 7u;
+  if (e == 0) return static_cast<float>(m) * 0x1p-9f;
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+__global__ void __launch_bounds__(256) quantize_nv_kernel(const float* __restrict__ x, int rows, int K,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ sf, int rows_pad,
+                                                          int cols4,
+                                                          const unsigned* __restrict__ amax_bits) {
+  const float amax = __uint_as_float(*amax_bits);
+  const float s = __fdiv_rn(amax, 2688.0f);
+  const float d = __fmul_rn(6.0f, s);
+  const int nblk = K / 16;
+  const int cols_pad = cols4 * 4;
+  const long long total = static_cast<long long>(rows_pad) * cols_pad;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / cols_pad);
+    const int c = static_cast<int>(i % cols_pad);
+    uint8_t code = 0;
+    if (r < rows && c < nblk) {
+      const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(r) * K + c * 16);
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 t = __ldg(src + j);
+        v[4 * j] = t.x;
+        v[4 * j + 1] = t.y;
+        v[4 * j + 2] = t.z;
+        v[4 * j + 3] = t.w;
+      }
+      float bmax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(v[j]));
+      const float t = (d != 0.0f) ? __fdiv_rn(bmax, d) : 0.0f;
+      const uint32_t sc = cvt_e4m3x2(t, 0.0f) & 0x7Fu;
+      const float den = __fmul_rn(ue4m3_value(sc), s);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float q0 = 0.0f, q1 = 0.0f;
+        if (den != 0.0f) {
+          q0 = __fdiv_rn(v[2 * j], den);
+          q1 = __fdiv_rn(v[2 * j + 1], den);
+        }
+        const uint32_t byte = cvt_e2m1x2(q0, q1) & 0xFFu;
+        if (j < 4) lo |= byte << (8 * j);
+        else hi |= byte << (8 * (j - 4));
+      }
+      *reinterpret_cast<uint2*>(codes + static_cast<size_t>(r) * (K / 2) + c * 8) = make_uint2(lo, hi);
+      code = static_cast<uint8_t>(sc);
+    }
+    sf[sf_swizzle_offset(r, c, cols4)] = code;
+  }
+}
+
+__global__ void nv_finalize_kernel(float* global_scale) {
+  const float amax = __uint_as_float(*reinterpret_cast<unsigned*>(global_scale));
+  *global_scale = __fdiv_rn(amax, 2688.0f);
+}
+
+static int grid_for(long long n, int threads) {
+  long long b = (n + threads - 1) / threads;
+  if (b < 1) b = 1;
+  if (b > 152 * 16) b = 152 * 16;
+  return static_cast<int>(b);
+}
+
+cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               cudaStream_t s) {
+  const int rows_pad = (rows + 127) / 128 * 128;
+  const int cols4 = (K / 32 + 3) / 4;
+  const long long total = static_cast<long long>(rows_pad) * cols4 * 4;
+  quantize_mx_kernel<<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_nv(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               float* global_scale, cudaStream_t s) {
+  const int rows_pad = (rows + 127) / 128 * 128;
+  const int cols4 = (K / 16 + 3) / 4;
+  const long long total = static_cast<long long>(rows_pad) * cols4 * 4;
+  cudaError_t e = cudaMemsetAsync(global_scale, 0, sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  const long long n = static_cast<long long>(rows) * K;
+  amax_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(global_scale));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  quantize_nv_kernel<<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4,
+                                                          reinterpret_cast<unsigned*>(global_scale));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  nv_finalize_kernel<<<1, 1, 0, s>>>(global_scale);
+  return cudaGetLastError();
+}
+
+}  // namespace bsg

@@ -1,0 +1,176 @@
+/*
+ * bsgemm.h -- block-scaled low-precision GEMM for GB300 (sm_103a), C ABI.
+ *
+ *     D = alpha * (A . B^T) (+ bias) (-> SiLU),  FP32 accumulation,  FP16 / BF16 output
+ *
+ * in two formats:
+ *   MXFP8  E4M3 elements, one UE8M0 scale per 32 K-elements
+ *          ("Add Cutlass MxFp8 Block Scale Matrix Multiplication": MxFp8GemmSm100,
+ *           ElementA/B = mx_float8_t<float_e4m3_t>, ElementSFA/SFB = float_ue8m0_t);
+ *   NVFP4  E2M1 elements (two per byte, element 2j in the low nibble of byte j), one
+ *          UE4M3 scale per 16 K-elements, plus a float global factor alpha
+ *          ("[QST] Performance overhead: Frequent cuTensorMapEncodeTiled and
+ *           cudaGetDriverEntryPoint calls during Blackwell GEMM loops": runNvfp4Gemm<T,
+ *           kEnableSilu, kEnableBias>(output, input_a, input_b, scales_a, scales_b, bias,
+ *           alpha, M, N, K, stream)).
+ *
+ * Layouts (the MxFp8GemmSm100 element/layout configuration):
+ *   A    M x K, row-major (K contiguous);  MXFP8 1 byte per element, NVFP4 K/2 bytes per row.
+ *   B    N x K, row-major (K contiguous) -- the "ColumnMajor" K x N operand of the page.
+ *   SFA  block scales of A in the swizzled 128x4 layout: rows padded to a multiple of 128,
+ *        scale columns (K/32 or K/16) padded to a multiple of 4, cut into 512-byte atoms of
+ *        128 rows x 4 columns stored band by band; inside an atom, scale (r, c) is at byte
+ *        (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4).  Padding bytes must be 0.
+ *        ("scales must be padded/swizzled to 128x4 blocks"; linear_to_swizzled_128_4.)
+ *   SFB  the same for B (N rows).
+ *   D    M x N, row-major, FP16 or BF16.   bias: N values of the output type.
+ *
+ * Ownership: the caller owns every device buffer and the stream.  The library owns the
+ * plan, its TMA tensor maps and its workspace (allocated in bsg_plan_create, freed in
+ * bsg_plan_destroy).  No call takes ownership of a caller pointer.
+ *
+ * Errors: every call returns a bsg_status; on failure bsg_last_error() holds a message
+ * (thread-local).  Nothing is thrown across the ABI.  Validation happens before any device
+ * work; an invalid argument never launches a kernel.  There is no CPU fallback: a device
+ * that is not compute capability 10.3 gets BSG_ERR_ARCH.
+ *
+ * Asynchrony: run calls enqueue on the given stream and return; faults of a kernel surface
+ * on a later synchronising call, and a kernel whose internal wait ran past its time limit
+ * reports BSG_ERR_DEVICE_TIMEOUT through bsg_plan_check_status().
+ */
+#ifndef BSGEMM_H_
+#define BSGEMM_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers (same type). */
+typedef struct CUstream_st* bsg_stream_t;
+
+typedef enum {
+  BSG_OK = 0,
+  BSG_ERR_INVALID_ARG = 1,   /* null pointer, null plan, bad enum, bad flags */
+  BSG_ERR_SHAPE = 2,         /* M, N, K out of range, K / N not a multiple of the block,
+                                or a buffer smaller than its shape needs */
+  BSG_ERR_ALIGNMENT = 3,     /* a pointer not 16-byte aligned */
+  BSG_ERR_SCALE_LAYOUT = 4,  /* scale buffer smaller than its padded 128x4 layout */
+  BSG_ERR_DTYPE = 5,         /* output type / format combination not supported */
+  BSG_ERR_ARCH = 6,          /* current device is not sm_103 */
+  BSG_ERR_CUDA = 7,          /* a CUDA runtime / driver call failed (message holds it) */
+  BSG_ERR_DEVICE_TIMEOUT = 8,/* a kernel's bounded internal wait expired */
+  BSG_ERR_NOMEM = 9          /* a host or device allocation failed */
+} bsg_status;
+
+typedef enum { BSG_MXFP8 = 0, BSG_NVFP4 = 1 } bsg_kind;
+typedef enum { BSG_OUT_F16 = 0, BSG_OUT_BF16 = 1 } bsg_out;
+
+/* Epilogue flags.  BIAS and SILU are the kEnableBias / kEnableSilu switches of
+ * runNvfp4Gemm; ALPHA_DEVICE reads alpha from device memory at run time, the
+ * fusion_args.alpha_ptr of the MXFP8 page. */
+enum {
+  BSG_F_BIAS = 1u,
+  BSG_F_SILU = 2u,
+  BSG_F_ALPHA_DEVICE = 4u
+};
+
+typedef struct bsg_plan_s* bsg_plan_t;
+
+/* One GEMM problem.  Pointers are device pointers, 16-byte aligned.
+ *   M >= 1, N >= 16, K >= 32, N % 16 == 0, K % 32 == 0 (the MXFP8 page validates
+ *   K % 16 and N % 16; K % 32 keeps every MXFP8 block whole and every NVFP4 row a
+ *   whole number of 16-byte units).  M, N, K <= 2^20.
+ *   bias is read only with BSG_F_BIAS; alpha_dev only with BSG_F_ALPHA_DEVICE (else the
+ *   host value alpha is used).  SILU is applied after alpha and bias:
+ *   D = silu(alpha * acc + bias[n]). */
+typedef struct {
+  bsg_kind kind;
+  bsg_out out;
+  unsigned flags;
+  int M, N, K;
+  const void* A;
+  const void* B;
+  const void* SFA;
+  const void* SFB;
+  const void* bias;
+  void* D;
+  float alpha;
+  const float* alpha_dev;
+} bsg_desc;
+
+/* Validate d, choose the kernel variant (tile shape, split-K), encode the TMA tensor
+ * maps once, allocate the plan's workspace and fill a launch configuration.  The plan
+ * refers to d's pointers; it does not copy or own the buffers.  The device current at
+ * this call is the plan's device.  Returns BSG_ERR_* without allocating on bad input.
+ * (Split-K and variant choice may be forced with the BSG_FORCE_BN / BSG_FORCE_SPLITS
+ * environment variables, read here.) */
+bsg_status bsg_plan_create(bsg_plan_t* plan, const bsg_desc* d);
+
+/* Enqueue the GEMM on `stream`: one kernel launch.  No tensor-map encoding, no driver
+ * entry-point lookup, no allocation, no host synchronisation, so it can be captured in a
+ * CUDA graph.  A plan may be in flight on one stream at a time (its split-K workspace is
+ * shared between its launches). */
+bsg_status bsg_plan_run(bsg_plan_t plan, bsg_stream_t stream);
+
+/* Free the plan and its workspace.  Call after its last launch has completed. */
+bsg_status bsg_plan_destroy(bsg_plan_t plan);
+
+/* Synchronise the plan's device and read the plan's device status word: BSG_OK, or
+ * BSG_ERR_DEVICE_TIMEOUT if a launch of this plan abandoned a wait.  Clears the word. */
+bsg_status bsg_plan_check_status(bsg_plan_t plan);
+
+/* Name of the kernel variant the plan chose, e.g. "mxfp8_bn256_s1" (owned by the plan). */
+const char* bsg_plan_variant(bsg_plan_t plan);
+
+/* One-shot calls: look the problem up in a process-wide plan cache (keyed on every
+ * argument and the device), create the plan on a miss, and run it.  After the first call
+ * with given arguments, a call costs a hash lookup and one launch. */
+bsg_status mxfp8_gemm(void* D, const void* A, const void* B, const void* SFA, const void* SFB,
+                      float alpha, int M, int N, int K, bsg_out out, bsg_stream_t stream);
+
+bsg_status nvfp4_gemm(void* D, const void* A, const void* B, const void* SFA, const void* SFB,
+                      const void* bias, float alpha, unsigned flags, int M, int N, int K,
+                      bsg_out out, bsg_stream_t stream);
+
+/* Drop every plan of the one-shot cache (after the work using them has completed). */
+bsg_status bsg_cache_clear(void);
+
+/* Bytes of the swizzled scale buffer of a rows x K operand: 128*ceil(rows/128) *
+ * 4*ceil((K/blk)/4), blk = 32 (MXFP8) or 16 (NVFP4).  0 for invalid arguments. */
+size_t bsg_sf_bytes(bsg_kind kind, int rows, int K);
+
+/* Quantise a row-major float32 matrix x (rows x K, device) on `stream`:
+ *   codes  rows x K bytes (MXFP8) or rows x K/2 bytes (NVFP4), device;
+ *   sf     bsg_sf_bytes(kind, rows, K) bytes, written whole (padding zero), device;
+ *   global_scale  NVFP4 only: device float receiving s = amax(|x|) / 2688 (it is used as
+ *          the amax accumulator while the call runs); ignored for MXFP8.
+ * MXFP8 per 32-block: e = least integer with amax <= 448 * 2^e (clamped to [-127, 127]),
+ * scale code e + 127, element = E4M3 round-to-nearest-even saturating of x * 2^-e.
+ * NVFP4: d = 6 s, block scale = UE4M3(amax_block / d), element = E2M1(x / (scale * s)),
+ * each step one float32 operation rounded to nearest even (0 where a divisor is 0).
+ * The GEMM factor of two NVFP4 operands is alpha = s_A * s_B.  The MXFP8 page's test
+ * quantises with pytorch_mxfp8_quantize and swizzles with linear_to_swizzled_128_4 before
+ * each GEMM.  rows >= 1, K >= 32, K % 32 == 0; x, codes, sf 16-byte aligned. */
+bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, void* codes, void* sf,
+                        float* global_scale, bsg_stream_t stream);
+
+/* Last error message of the calling thread ("" if none). */
+const char* bsg_last_error(void);
+
+/* Library version string. */
+const char* bsg_version(void);
+
+/* ---- test hooks (fault injection without a GPU fault) ----
+ * Set the plan's bounded-wait limit (nanoseconds, 0 keeps the default of 2 s) and, with
+ * skip_first_load != 0, make the producer of every CTA leave its first ring stage unfilled,
+ * so that the tensor-core warp's wait runs out, the kernel flags BSG_ERR_DEVICE_TIMEOUT in
+ * the plan's status word and returns cleanly.  For tests of the failure path only. */
+bsg_status bsg_plan_debug_set(bsg_plan_t plan, int skip_first_load, unsigned long long wait_limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSGEMM_H_ */
