@@ -1,0 +1,555 @@
+// C ABI of the block-scaled GEMM library: validation, plans, tensor maps, launch, plan cache.
+//
+// The pages' host path ("[QST] Performance overhead: Frequent cuTensorMapEncodeTiled and
+// cudaGetDriverEntryPoint calls ...", runNvfp4Gemm; and the runGemm launcher of "Add Cutlass
+// MxFp8 Block Scale Matrix Multiplication") allocates a workspace, checks the arguments and
+// encodes the TMA descriptors on EVERY call, then launches.  Here all of that happens once,
+// in bsg_plan_create; bsg_plan_run is a single cudaLaunchKernelExC.  The driver entry points
+// are resolved once per process.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+
+#include "bsg_internal.h"
+#include "bsgemm.h"
+
+#define BSG_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr uint32_t kPlanMagic = 0xB5C0FFEEu;
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kMaxDim = 1 << 20;
+
+thread_local std::string g_err;
+
+bsg_status fail(bsg_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+bsg_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(BSG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- driver entry points
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
+std::once_flag g_driver_once;
+
+bool load_driver_entry_points() {
+  std::call_once(g_driver_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    fn = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 3020, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_addr_range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(fn);
+    cudaGetLastError();
+  });
+  return g_encode != nullptr;
+}
+
+// ---------------------------------------------------------------- device info
+struct DeviceInfo {
+  int major = 0, minor = 0, sms = 0;
+};
+std::mutex g_dev_mutex;
+std::unordered_map<int, DeviceInfo> g_dev;
+
+bsg_status current_device(int* dev, DeviceInfo* info) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_dev_mutex);
+  auto it = g_dev.find(*dev);
+  if (it == g_dev.end()) {
+    DeviceInfo di;
+    if ((e = cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    it = g_dev.emplace(*dev, di).first;
+  }
+  // bind the device's primary context to this thread so that the driver calls below see it
+  if ((e = cudaSetDevice(*dev)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  *info = it->second;
+  if (info->major != 10 || info->minor != 3)
+    return fail(BSG_ERR_ARCH, "device %d is compute capability %d.%d; this library runs on sm_103 only",
+                *dev, info->major, info->minor);
+  return BSG_OK;
+}
+
+// [p, p + need) must lie inside one device allocation.
+bsg_status check_range(const void* p, size_t need, bsg_status code, const char* name) {
+  if (g_addr_range == nullptr) return BSG_OK;  // no way to check: trust the caller
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  const CUresult r = g_addr_range(&base, &size, reinterpret_cast<CUdeviceptr>(p));
+  if (r != CUDA_SUCCESS)
+    return fail(BSG_ERR_INVALID_ARG, "%s (%p) is not a device allocation (driver error %d)", name, p,
+                static_cast<int>(r));
+  const size_t avail = static_cast<size_t>(base + size - reinterpret_cast<CUdeviceptr>(p));
+  if (need > avail)
+    return fail(code, "%s needs %zu bytes but its allocation holds %zu from that address", name, need,
+                avail);
+  return BSG_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t sf_bytes_of(int kind, int rows, int K) {
+  const int blk = kind == bsg::KIND_MX ? 32 : 16;
+  const size_t rp = (static_cast<size_t>(rows) + 127) / 128 * 128;
+  const size_t cp = (static_cast<size_t>(K / blk) + 3) / 4 * 4;
+  return rp * cp;
+}
+
+size_t code_row_bytes(int kind, int K) { return kind == bsg::KIND_MX ? K : K / 2; }
+
+bsg_status validate_desc(const bsg_desc* d) {
+  if (d == nullptr) return fail(BSG_ERR_INVALID_ARG, "descriptor is null");
+  if (d->kind != BSG_MXFP8 && d->kind != BSG_NVFP4) return fail(BSG_ERR_INVALID_ARG, "unknown kind %d", d->kind);
+  if (d->out != BSG_OUT_F16 && d->out != BSG_OUT_BF16)
+    return fail(BSG_ERR_DTYPE, "unsupported output type %d (FP16 or BF16 only)", d->out);
+  if (d->flags & ~(BSG_F_BIAS | BSG_F_SILU | BSG_F_ALPHA_DEVICE))
+    return fail(BSG_ERR_INVALID_ARG, "unknown flag bits 0x%x", d->flags);
+  if (d->M < 1 || d->N < 16 || d->K < 32 || d->M > kMaxDim || d->N > kMaxDim || d->K > kMaxDim)
+    return fail(BSG_ERR_SHAPE, "shape M=%d N=%d K=%d out of range (M>=1, N>=16, K>=32, each <= 2^20)",
+                d->M, d->N, d->K);
+  if (d->N % 16) return fail(BSG_ERR_SHAPE, "N=%d is not a multiple of 16", d->N);
+  if (d->K % 32) return fail(BSG_ERR_SHAPE, "K=%d is not a multiple of 32", d->K);
+  if (!d->A || !d->B || !d->SFA || !d->SFB || !d->D) return fail(BSG_ERR_INVALID_ARG, "null operand pointer");
+  if ((d->flags & BSG_F_BIAS) && !d->bias) return fail(BSG_ERR_INVALID_ARG, "BIAS set but bias is null");
+  if ((d->flags & BSG_F_ALPHA_DEVICE) && !d->alpha_dev)
+    return fail(BSG_ERR_INVALID_ARG, "ALPHA_DEVICE set but alpha_dev is null");
+  if (!aligned16(d->A) || !aligned16(d->B) || !aligned16(d->SFA) || !aligned16(d->SFB) || !aligned16(d->D) ||
+      ((d->flags & BSG_F_BIAS) && !aligned16(d->bias)))
+    return fail(BSG_ERR_ALIGNMENT, "operand pointers must be 16-byte aligned");
+  if ((d->flags & BSG_F_ALPHA_DEVICE) && (reinterpret_cast<uintptr_t>(d->alpha_dev) & 3u))
+    return fail(BSG_ERR_ALIGNMENT, "alpha_dev must be 4-byte aligned");
+  return BSG_OK;
+}
+
+bsg_status validate_ranges(const bsg_desc* d) {
+  const size_t rb = code_row_bytes(d->kind, d->K);
+  bsg_status s;
+  if ((s = check_range(d->A, rb * d->M, BSG_ERR_SHAPE, "A")) != BSG_OK) return s;
+  if ((s = check_range(d->B, rb * d->N, BSG_ERR_SHAPE, "B")) != BSG_OK) return s;
+  if ((s = check_range(d->SFA, sf_bytes_of(d->kind, d->M, d->K), BSG_ERR_SCALE_LAYOUT, "SFA")) != BSG_OK) return s;
+  if ((s = check_range(d->SFB, sf_bytes_of(d->kind, d->N, d->K), BSG_ERR_SCALE_LAYOUT, "SFB")) != BSG_OK) return s;
+  if ((s = check_range(d->D, static_cast<size_t>(d->M) * d->N * 2, BSG_ERR_SHAPE, "D")) != BSG_OK) return s;
+  if ((d->flags & BSG_F_BIAS) && (s = check_range(d->bias, static_cast<size_t>(d->N) * 2, BSG_ERR_SHAPE, "bias")) != BSG_OK)
+    return s;
+  if ((d->flags & BSG_F_ALPHA_DEVICE) && (s = check_range(d->alpha_dev, 4, BSG_ERR_SHAPE, "alpha_dev")) != BSG_OK)
+    return s;
+  return BSG_OK;
+}
+
+}  // namespace
+
+struct bsg_plan_s {
+  uint32_t magic;
+  bsg_desc desc;
+  bsg::GemmParams params;
+  bsg::GemmKernelInfo info;
+  int device;
+  int grid;
+  void* workspace;
+  char variant[64];
+};
+
+namespace {
+
+std::mutex g_attr_mutex;
+std::unordered_set<const void*> g_attr_done;
+
+bsg_status ensure_smem_attr(const bsg::GemmKernelInfo& info, int device) {
+  std::lock_guard<std::mutex> lk(g_attr_mutex);
+  const void* key = reinterpret_cast<const char*>(info.fn) + device;  // per (kernel, device)
+  if (g_attr_done.count(key)) return BSG_OK;
+  cudaError_t e = cudaFuncSetAttribute(info.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, info.smem_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  g_attr_done.insert(key);
+  return BSG_OK;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == 0) return dflt;
+  return std::atoi(v);
+}
+
+// Tile width, split-K: 256-wide tiles when they alone give every SM a tile; otherwise
+// 128-wide tiles (double-buffered accumulator) and, if that still leaves SMs idle, split K so
+// that tiles x splits is close to the SM count.  Every split owns at least one k-tile.
+void choose_variant(const bsg_desc* d, int sms, int* bn, int* splits, int* kps) {
+  const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
+  const int nkt = (d->K + k_tile - 1) / k_tile;
+  const long long mt = (d->M + 127) / 128;
+  const long long t256 = mt * ((d->N + 255) / 256);
+  const long long t128 = mt * ((d->N + 127) / 128);
+  int b, s;
+  if (t256 >= sms) {
+    b = 256;
+    s = 1;
+  } else {
+    b = 128;
+    s = t128 >= sms ? 1 : static_cast<int>(std::max<long long>(1, std::min<long long>(nkt, sms / t128)));
+  }
+  const int fb = env_int("BSG_FORCE_BN", 0);
+  if (fb == 128 || fb == 256) b = fb;
+  const int fs = env_int("BSG_FORCE_SPLITS", 0);
+  if (fs >= 1) s = std::min(fs, nkt);
+  int k = (nkt + s - 1) / s;
+  s = (nkt + k - 1) / k;
+  *bn = b;
+  *splits = s;
+  *kps = k;
+}
+
+bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, uint64_t rows,
+                          uint32_t box_rows, const char* name) {
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(BSG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with driver error %d", name, static_cast<int>(r));
+  return BSG_OK;
+}
+
+bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
+  if (out == nullptr) return fail(BSG_ERR_INVALID_ARG, "plan output pointer is null");
+  *out = nullptr;
+  bsg_status s = validate_desc(d);
+  if (s != BSG_OK) return s;
+  int dev = 0;
+  DeviceInfo di;
+  if ((s = current_device(&dev, &di)) != BSG_OK) return s;
+  if (!load_driver_entry_points())
+    return fail(BSG_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled from the driver");
+  if ((s = validate_ranges(d)) != BSG_OK) return s;
+
+  int bn, splits, kps;
+  choose_variant(d, di.sms, &bn, &splits, &kps);
+  bsg::GemmKernelInfo info{};
+  const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
+  const bool found = d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(bn, out_t, &info)
+                                          : bsg::gemm_kernel_info_nv(bn, out_t, &info);
+  if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
+  if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
+
+  bsg_plan_s* p = new (std::nothrow) bsg_plan_s();
+  if (p == nullptr) return fail(BSG_ERR_NOMEM, "host allocation of the plan failed");
+  p->magic = kPlanMagic;
+  p->desc = *d;
+  p->info = info;
+  p->device = dev;
+  p->workspace = nullptr;
+  bsg::GemmParams& g = p->params;
+  std::memset(&g, 0, sizeof(g));
+  const size_t rb = code_row_bytes(d->kind, d->K);
+  if ((s = encode_operand(&g.tmap_a, d->A, rb, d->M, 128, "A")) != BSG_OK ||
+      (s = encode_operand(&g.tmap_b, d->B, rb, d->N, static_cast<uint32_t>(bn), "B")) != BSG_OK) {
+    delete p;
+    return s;
+  }
+  const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
+  const int blk = d->kind == BSG_MXFP8 ? 32 : 16;
+  g.sfa = static_cast<const uint8_t*>(d->SFA);
+  g.sfb = static_cast<const uint8_t*>(d->SFB);
+  g.bias = d->bias;
+  g.d = d->D;
+  g.alpha_dev = d->alpha_dev;
+  g.wait_limit_ns = kDefaultWaitLimitNs;
+  g.alpha = d->alpha;
+  g.M = d->M;
+  g.N = d->N;
+  g.K = d->K;
+  g.flags = d->flags;
+  g.sfa_atoms_per_band = (d->K / blk + 3) / 4;
+  g.sfb_atoms_per_band = g.sfa_atoms_per_band;
+  g.sfb_bands = (d->N + 127) / 128;
+  g.num_m_tiles = (d->M + 127) / 128;
+  g.num_n_tiles = (d->N + bn - 1) / bn;
+  g.num_k_tiles = (d->K + k_tile - 1) / k_tile;
+  g.num_tiles = g.num_m_tiles * g.num_n_tiles;
+  g.splits = splits;
+  g.k_tiles_per_split = kps;
+  g.num_units = g.num_tiles * splits;
+  g.group_m = 16;
+  g.debug_skip_first_load = 0;
+
+  // workspace: [status word | per-tile counters | split-K partial tiles]
+  const size_t cnt_off = 256;
+  const size_t part_off = cnt_off + (static_cast<size_t>(g.num_tiles) * 4 + 255) / 256 * 256;
+  const size_t part_bytes = splits > 1 ? static_cast<size_t>(splits) * g.num_tiles * 128 * bn * 4 : 0;
+  const size_t ws_bytes = part_off + part_bytes;
+  cudaError_t e = cudaMalloc(&p->workspace, ws_bytes);
+  if (e != cudaSuccess) {
+    delete p;
+    cudaGetLastError();
+    return fail(BSG_ERR_NOMEM, "cudaMalloc of a %zu-byte workspace failed", ws_bytes);
+  }
+  e = cudaMemset(p->workspace, 0, part_off);
+  if (e != cudaSuccess) {
+    cudaFree(p->workspace);
+    delete p;
+    return cuda_fail(e, "cudaMemset(workspace)");
+  }
+  char* ws = static_cast<char*>(p->workspace);
+  g.status = reinterpret_cast<unsigned*>(ws);
+  g.counters = reinterpret_cast<unsigned*>(ws + cnt_off);
+  g.partial = splits > 1 ? reinterpret_cast<float*>(ws + part_off) : nullptr;
+  p->grid = std::min(g.num_units, di.sms);
+  std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
+                bn, splits, info.stages, p->grid);
+  if (env_int("BSG_LOG", 0))
+    std::fprintf(stderr, "[bsgemm] plan M=%d N=%d K=%d -> %s\n", d->M, d->N, d->K, p->variant);
+  *out = p;
+  return BSG_OK;
+}
+
+bool plan_ok(bsg_plan_t p) { return p != nullptr && p->magic == kPlanMagic; }
+
+bsg_status plan_launch(bsg_plan_t p, const bsg::GemmParams& params, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(p->grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(p->info.threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(p->info.smem_bytes);
+  cfg.stream = stream;
+  void* args[] = {const_cast<bsg::GemmParams*>(&params)};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, p->info.fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
+  return BSG_OK;
+}
+
+}  // namespace
+
+// ==================================================================== exported C ABI
+
+BSG_API const char* bsg_last_error(void) { return g_err.c_str(); }
+
+BSG_API const char* bsg_version(void) { return "bsgemm 0.1 (sm_103a)"; }
+
+BSG_API size_t bsg_sf_bytes(bsg_kind kind, int rows, int K) {
+  if ((kind != BSG_MXFP8 && kind != BSG_NVFP4) || rows < 1 || K < 32 || K % 32) return 0;
+  return sf_bytes_of(kind, rows, K);
+}
+
+BSG_API bsg_status bsg_plan_create(bsg_plan_t* plan, const bsg_desc* d) { return plan_create(plan, d); }
+
+BSG_API bsg_status bsg_plan_run(bsg_plan_t plan, bsg_stream_t stream) {
+  if (!plan_ok(plan)) return fail(BSG_ERR_INVALID_ARG, "invalid plan handle");
+  return plan_launch(plan, plan->params, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BSG_API bsg_status bsg_plan_destroy(bsg_plan_t plan) {
+  if (!plan_ok(plan)) return fail(BSG_ERR_INVALID_ARG, "invalid plan handle");
+  plan->magic = 0;
+  cudaError_t e = cudaSuccess;
+  if (plan->workspace) e = cudaFree(plan->workspace);
+  delete plan;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+  return BSG_OK;
+}
+
+BSG_API bsg_status bsg_plan_check_status(bsg_plan_t plan) {
+  if (!plan_ok(plan)) return fail(BSG_ERR_INVALID_ARG, "invalid plan handle");
+  int cur = 0;
+  cudaGetDevice(&cur);
+  cudaError_t e = cudaSetDevice(plan->device);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  unsigned word = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&word, plan->params.status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != 0) e = cudaMemset(plan->params.status, 0, sizeof(word));
+  cudaSetDevice(cur);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the plan status word");
+  if (word != 0)
+    return fail(BSG_ERR_DEVICE_TIMEOUT, "a launch of this plan gave up a wait (status 0x%x:%s%s%s%s)", word,
+                (word & bsg::ST_TIMEOUT_PRODUCER) ? " producer" : "", (word & bsg::ST_TIMEOUT_MMA) ? " mma" : "",
+                (word & bsg::ST_TIMEOUT_EPILOGUE) ? " epilogue" : "", (word & bsg::ST_TIMEOUT_DRAIN) ? " drain" : "");
+  return BSG_OK;
+}
+
+BSG_API const char* bsg_plan_variant(bsg_plan_t plan) {
+  if (!plan_ok(plan)) return "";
+  return plan->variant;
+}
+
+BSG_API bsg_status bsg_plan_debug_set(bsg_plan_t plan, int skip_first_load, unsigned long long wait_limit_ns) {
+  if (!plan_ok(plan)) return fail(BSG_ERR_INVALID_ARG, "invalid plan handle");
+  plan->params.debug_skip_first_load = skip_first_load ? 1 : 0;
+  plan->params.wait_limit_ns = wait_limit_ns ? wait_limit_ns : kDefaultWaitLimitNs;
+  return BSG_OK;
+}
+
+// ---------------------------------------------------------------- one-shot plan cache
+namespace {
+
+struct CacheKey {
+  int kind, out, M, N, K, device;
+  unsigned flags;
+  const void *A, *B, *SFA, *SFB, *bias, *D;
+  bool operator==(const CacheKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
+};
+
+struct CacheKeyHash {
+  size_t operator()(const CacheKey& k) const {
+    const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+    uint64_t h = 1469598103934665603ull;  // FNV-1a over the key bytes
+    for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ b[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+
+std::mutex g_cache_mutex;
+std::unordered_map<CacheKey, bsg_plan_t, CacheKeyHash> g_cache;
+
+bsg_status cached_run(const bsg_desc& d, cudaStream_t stream) {
+  const bsg_status vs = validate_desc(&d);  // before any CUDA call
+  if (vs != BSG_OK) return vs;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  CacheKey key;
+  std::memset(&key, 0, sizeof(key));  // padding bytes take part in the hash
+  key.kind = d.kind;
+  key.out = d.out;
+  key.M = d.M;
+  key.N = d.N;
+  key.K = d.K;
+  key.device = dev;
+  key.flags = d.flags;
+  key.A = d.A;
+  key.B = d.B;
+  key.SFA = d.SFA;
+  key.SFB = d.SFB;
+  key.bias = (d.flags & BSG_F_BIAS) ? d.bias : nullptr;
+  key.D = d.D;
+  bsg_plan_t plan = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_cache_mutex);
+    auto it = g_cache.find(key);
+    if (it != g_cache.end()) {
+      plan = it->second;
+    } else {
+      bsg_status s = plan_create(&plan, &d);
+      if (s != BSG_OK) return s;
+      g_cache.emplace(key, plan);
+    }
+  }
+  if (plan->params.alpha == d.alpha) return plan_launch(plan, plan->params, stream);
+  bsg::GemmParams params = plan->params;  // alpha is not part of the key
+  params.alpha = d.alpha;
+  return plan_launch(plan, params, stream);
+}
+
+}  // namespace
+
+BSG_API bsg_status mxfp8_gemm(void* D, const void* A, const void* B, const void* SFA, const void* SFB,
+                              float alpha, int M, int N, int K, bsg_out out, bsg_stream_t stream) {
+  bsg_desc d;
+  std::memset(&d, 0, sizeof(d));
+  d.kind = BSG_MXFP8;
+  d.out = out;
+  d.flags = 0;
+  d.M = M;
+  d.N = N;
+  d.K = K;
+  d.A = A;
+  d.B = B;
+  d.SFA = SFA;
+  d.SFB = SFB;
+  d.D = D;
+  d.alpha = alpha;
+  return cached_run(d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BSG_API bsg_status nvfp4_gemm(void* D, const void* A, const void* B, const void* SFA, const void* SFB,
+                              const void* bias, float alpha, unsigned flags, int M, int N, int K, bsg_out out,
+                              bsg_stream_t stream) {
+  if (flags & BSG_F_ALPHA_DEVICE)
+    return fail(BSG_ERR_INVALID_ARG, "nvfp4_gemm takes a host alpha; use a plan for a device alpha");
+  bsg_desc d;
+  std::memset(&d, 0, sizeof(d));
+  d.kind = BSG_NVFP4;
+  d.out = out;
+  d.flags = flags;
+  d.M = M;
+  d.N = N;
+  d.K = K;
+  d.A = A;
+  d.B = B;
+  d.SFA = SFA;
+  d.SFB = SFB;
+  d.bias = bias;
+  d.D = D;
+  d.alpha = alpha;
+  return cached_run(d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BSG_API bsg_status bsg_cache_clear(void) {
+  std::lock_guard<std::mutex> lk(g_cache_mutex);
+  bsg_status r = BSG_OK;
+  for (auto& kv : g_cache) {
+    const bsg_status s = bsg_plan_destroy(kv.second);
+    if (s != BSG_OK) r = s;
+  }
+  g_cache.clear();
+  return r;
+}
+
+// ---------------------------------------------------------------- quantiser
+BSG_API bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, void* codes, void* sf,
+                                float* global_scale, bsg_stream_t stream) {
+  if (kind != BSG_MXFP8 && kind != BSG_NVFP4) return fail(BSG_ERR_INVALID_ARG, "unknown kind %d", kind);
+  if (rows < 1 || K < 32 || K % 32 || rows > kMaxDim || K > kMaxDim)
+    return fail(BSG_ERR_SHAPE, "quantise shape rows=%d K=%d (rows>=1, K>=32, K%%32==0, each <= 2^20)", rows, K);
+  if (!x || !codes || !sf || (kind == BSG_NVFP4 && !global_scale))
+    return fail(BSG_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf) ||
+      (kind == BSG_NVFP4 && (reinterpret_cast<uintptr_t>(global_scale) & 3u)))
+    return fail(BSG_ERR_ALIGNMENT, "x, codes and sf must be 16-byte aligned, global_scale 4-byte aligned");
+  int dev = 0;
+  DeviceInfo di;
+  bsg_status s = current_device(&dev, &di);
+  if (s != BSG_OK) return s;
+  load_driver_entry_points();
+  if ((s = check_range(x, static_cast<size_t>(rows) * K * 4, BSG_ERR_SHAPE, "x")) != BSG_OK ||
+      (s = check_range(codes, code_row_bytes(kind, K) * rows, BSG_ERR_SHAPE, "codes")) != BSG_OK ||
+      (s = check_range(sf, sf_bytes_of(kind, rows, K), BSG_ERR_SCALE_LAYOUT, "sf")) != BSG_OK ||
+      (kind == BSG_NVFP4 && (s = check_range(global_scale, 4, BSG_ERR_SHAPE, "global_scale")) != BSG_OK))
+    return s;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      kind == BSG_MXFP8
+          ? bsg::launch_quantize_mx(x, rows, K, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(sf), st)
+          : bsg::launch_quantize_nv(x, rows, K, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(sf),
+                                    global_scale, st);
+  if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
+  return BSG_OK;
+}

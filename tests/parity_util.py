@@ -1,0 +1,101 @@
+"""Helpers of the GPU parity tests: oracle-quantised operands in, library GEMM out, oracle compare.
+
+The operands of every GEMM parity case are quantised by the ORACLE on the CPU and uploaded;
+the CUDA path's own quantiser is checked separately (bit-exact) so that no oracle input or
+expected value ever comes from the CUDA path.
+"""
+
+import numpy as np
+import torch
+
+import fp4_gemm_blackwell_gb300 as bsg
+from fp4_gemm_blackwell_gb300 import synth
+from oracle import gemm as R
+from oracle import layout as L
+from oracle import quantize as Q
+
+KIND = {"mxfp8": bsg.BSG_MXFP8, "nvfp4": bsg.BSG_NVFP4}
+OUT = {"bf16": bsg.BSG_OUT_BF16, "f16": bsg.BSG_OUT_F16}
+
+
+def dev(a, dtype=torch.uint8):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+def oracle_operand(kind, x):
+    """float32 matrix -> (codes uint8 2-D, swizzled scale buffer, global scale or None) by the oracle."""
+    if kind == "mxfp8":
+        codes, sf = Q.quantize_mxfp8(x)
+        return codes, L.swizzle(sf), None
+    packed, sf, s = Q.quantize_nvfp4(x)
+    return packed, L.swizzle(sf), s
+
+
+def make_problem(kind, M, N, K, seed_a=synth.SEED_A, seed_b=synth.SEED_B, rowscaled=None):
+    gen = synth.normal_rowscaled if (rowscaled if rowscaled is not None else kind == "nvfp4") else synth.normal
+    xa = gen(M, K, seed_a)
+    xb = gen(N, K, seed_b)
+    a, sfa, sa = oracle_operand(kind, xa)
+    b, sfb, sb = oracle_operand(kind, xb)
+    alpha = np.float32(1.0) if kind == "mxfp8" else np.float32(np.float32(sa) * np.float32(sb))
+    return dict(kind=kind, M=M, N=N, K=K, A=a, B=b, SFA=sfa, SFB=sfb, alpha=alpha)
+
+
+class DeviceProblem:
+    """Device copies of a problem's operands plus an output buffer with canary margins."""
+
+    CANARY = 0x7BAD
+
+    def __init__(self, prob, out="bf16", bias=False, silu=False, margin=256):
+        self.prob, self.out = prob, out
+        M, N = prob["M"], prob["N"]
+        self.A, self.B = dev(prob["A"]), dev(prob["B"])
+        self.SFA, self.SFB = dev(prob["SFA"]), dev(prob["SFB"])
+        self.flags = (bsg.BSG_F_BIAS if bias else 0) | (bsg.BSG_F_SILU if silu else 0)
+        self.bias_vals = None
+        self.bias = None
+        if bias:
+            bits, vals = synth.bias(N, out=out)
+            self.bias = dev(bits.view(np.int16)).view(torch.int16)
+            self.bias_vals = vals
+        self.margin = margin
+        self.Dbuf = torch.full((M * N + 2 * margin,), self.CANARY, dtype=torch.int16, device="cuda")
+        self.D = self.Dbuf[margin:margin + M * N]
+
+    def plan(self, alpha_dev=None):
+        p = self.prob
+        flags = self.flags | (bsg.BSG_F_ALPHA_DEVICE if alpha_dev is not None else 0)
+        return bsg.Plan(KIND[p["kind"]], OUT[self.out], p["M"], p["N"], p["K"], self.A, self.B, self.SFA,
+                        self.SFB, self.D, alpha=float(p["alpha"]), flags=flags, bias=self.bias,
+                        alpha_dev=alpha_dev)
+
+    def result(self):
+        torch.cuda.synchronize()
+        buf = self.Dbuf.cpu().numpy().view(np.uint16)
+        m = self.margin
+        assert np.all(buf[:m] == self.CANARY) and np.all(buf[-m:] == self.CANARY), "output canary overwritten"
+        bits = buf[m:-m].reshape(self.prob["M"], self.prob["N"])
+        return R.out_from_bits(bits, self.out)
+
+
+def reference(prob, out, bias_vals=None, silu=False, rows=None):
+    p = prob
+    ref, _ = R.reference(p["kind"], p["A"], p["B"], p["SFA"], p["SFB"], p["M"], p["N"], p["K"],
+                         alpha=p["alpha"], bias=bias_vals, silu=silu, out=out, rows=rows)
+    abs_sum = R.abs_product_sum(p["kind"], p["A"], p["B"], p["SFA"], p["SFB"], p["M"], p["N"], p["K"], rows=rows)
+    return ref, abs_sum
+
+
+def assert_parity(got, prob, out, bias_vals=None, silu=False, rows=None):
+    """Element-wise |got - ref| <= |alpha| 2^-7 sum|a b| (x1.1 with SiLU) + 1 output ulp."""
+    ref, abs_sum = reference(prob, out, bias_vals, silu, rows)
+    if rows is not None:
+        got = got[np.asarray(rows)]
+    tol = R.tolerance(ref, got, abs_sum, prob["alpha"], silu, out)
+    err = np.abs(got - ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        detail = ", ".join("(%d,%d) got %r ref %r tol %.3g" % (i, j, got[i, j], ref[i, j], tol[i, j]) for i, j in idx)
+        raise AssertionError("%d of %d outputs outside tolerance: %s" % (bad.sum(), bad.size, detail))
+    return float(np.max(err / np.maximum(tol, 1e-300)))

@@ -1,0 +1,104 @@
+"""The C-ABI library builds, loads and exports every entry point its header declares;
+host-side validation rejects bad arguments before touching a device (runs without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp4_gemm_blackwell_gb300 as bsg
+from fp4_gemm_blackwell_gb300 import build as B
+
+HEADER = os.path.join(B.INCLUDE, "bsgemm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return bsg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    for want in ["bsg_plan_create", "bsg_plan_run", "bsg_plan_destroy", "bsg_plan_check_status",
+                 "mxfp8_gemm", "nvfp4_gemm", "bsg_sf_bytes", "bsg_quantize", "bsg_last_error"]:
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_version_and_sf_bytes(L):
+    assert "sm_103a" in bsg.bsg_version()
+    # rows padded to 128, scale columns to 4 (MXFP8 block 32, NVFP4 block 16)
+    assert bsg.bsg_sf_bytes(bsg.BSG_MXFP8, 256, 256) == 256 * 8
+    assert bsg.bsg_sf_bytes(bsg.BSG_MXFP8, 8000, 8192) == 8064 * 256
+    assert bsg.bsg_sf_bytes(bsg.BSG_NVFP4, 8000, 8192) == 8064 * 512
+    assert bsg.bsg_sf_bytes(bsg.BSG_NVFP4, 1, 32) == 128 * 4
+    assert bsg.bsg_sf_bytes(bsg.BSG_MXFP8, 1, 160) == 128 * 8
+    assert bsg.bsg_sf_bytes(bsg.BSG_MXFP8, 0, 32) == 0
+    assert bsg.bsg_sf_bytes(bsg.BSG_MXFP8, 4, 48) == 0
+    assert bsg.bsg_sf_bytes(7, 4, 64) == 0
+
+
+def _plan_status(L, **kw):
+    base = dict(kind=0, out=1, flags=0, M=128, N=128, K=128, A=16, B=32, SFA=48, SFB=64, bias=None,
+                D=80, alpha=1.0, alpha_dev=None)
+    base.update(kw)
+    d = bsg.BsgDesc(base["kind"], base["out"], base["flags"], base["M"], base["N"], base["K"], base["A"],
+                    base["B"], base["SFA"], base["SFB"], base["bias"], base["D"], base["alpha"], base["alpha_dev"])
+    h = ctypes.c_void_p()
+    st = L.bsg_plan_create(ctypes.byref(h), ctypes.byref(d))
+    assert h.value is None
+    return st
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kind=5), 1), (dict(out=3), 5), (dict(flags=8), 1),
+    (dict(M=0), 2), (dict(N=8), 2), (dict(N=120), 2), (dict(K=48), 2), (dict(K=16), 2),
+    (dict(M=1 << 21), 2), (dict(A=None), 1), (dict(D=None), 1), (dict(flags=1), 1),
+    (dict(flags=4), 1), (dict(A=24), 3), (dict(SFB=72), 3), (dict(flags=1, bias=88), 3),
+])
+def test_invalid_descriptors_are_rejected_before_device_work(L, kw, status):
+    assert _plan_status(L, **kw) == status
+    assert bsg.bsg_last_error() != ""
+
+
+def test_null_handles(L):
+    assert L.bsg_plan_create(None, None) == 1
+    assert L.bsg_plan_run(None, None) == 1
+    assert L.bsg_plan_destroy(None) == 1
+    assert L.bsg_plan_check_status(None) == 1
+    assert L.bsg_plan_variant(None) == b""
+    with pytest.raises(bsg.BsgError) as e:
+        bsg.bsg_plan_run(None, 0)
+    assert e.value.name == "BSG_ERR_INVALID_ARG"
+
+
+@pytest.mark.parametrize("args,status", [
+    ((7, 16, 128, 128, 32, 48, 64), 1),        # kind
+    ((0, 16, 0, 128, 32, 48, 64), 2),          # rows
+    ((0, 16, 128, 48, 32, 48, 64), 2),         # K % 32
+    ((0, None, 128, 128, 32, 48, 64), 1),      # null x
+    ((1, 16, 128, 128, 32, 48, None), 1),      # NVFP4 needs global_scale
+    ((0, 20, 128, 128, 32, 48, 64), 3),        # misaligned x
+])
+def test_quantize_validation(L, args, status):
+    kind, x, rows, K, codes, sf, gs = args
+    assert L.bsg_quantize(kind, x, rows, K, codes, sf, gs, None) == status
+
+
+def test_one_shot_validation(L):
+    # N not a multiple of 16 and a device alpha through the host-alpha call are refused
+    assert L.mxfp8_gemm(16, 32, 48, 64, 80, ctypes.c_float(1.0), 128, 120, 128, 1, None) == 2
+    assert L.nvfp4_gemm(16, 32, 48, 64, 80, None, ctypes.c_float(1.0), 4, 128, 128, 128, 1, None) == 1
