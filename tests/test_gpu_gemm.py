@@ -1,0 +1,127 @@
+"""GPU block-scaled GEMM (through the C ABI) against the CPU oracle, element by element.
+
+Bound per output element: |alpha| * 2^-7 * sum_k |a_k b_k| (x 1.1 with SiLU) + 1 output ulp.
+Operands are quantised by the oracle; the output buffer carries canaries on both sides.
+"""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import fp4_gemm_blackwell_gb300 as bsg
+import parity_util as P
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "mxfp8_test_shapes.txt")
+
+
+def golden_shapes():
+    shapes = []
+    for line in open(GOLDEN):
+        t = line.split()
+        if len(t) == 3 and all(s.isdigit() for s in t):
+            shapes.append(tuple(int(s) for s in t))
+    return shapes
+
+
+def run_case(kind, M, N, K, out="bf16", bias=False, silu=False, env=None, monkeypatch=None, rows=None):
+    if env:
+        for k, v in env.items():
+            monkeypatch.setenv(k, str(v))
+    prob = P.make_problem(kind, M, N, K)
+    dp = P.DeviceProblem(prob, out=out, bias=bias, silu=silu)
+    with dp.plan() as plan:
+        variant = plan.variant
+        plan.run()
+        plan.check_status()
+        got = dp.result()
+    P.assert_parity(got, prob, out, dp.bias_vals, silu, rows=rows)
+    return variant
+
+
+@pytest.mark.parametrize("out", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", golden_shapes())
+def test_mxfp8_page_shapes(shape, out):
+    run_case("mxfp8", *shape, out=out)
+
+
+@pytest.mark.parametrize("out", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", golden_shapes())
+def test_nvfp4_page_shapes_bias_silu(shape, out):
+    run_case("nvfp4", *shape, out=out, bias=True, silu=True)
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("M,N,K", [(200, 144, 160), (130, 272, 96), (1, 512, 1024), (16, 4096, 256),
+                                   (300, 400, 608)])
+def test_ragged_shapes(kind, M, N, K):
+    run_case(kind, M, N, K, bias=(kind == "nvfp4"), silu=(kind == "nvfp4"))
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("bn,splits", [(128, 1), (256, 1), (128, 3), (256, 2), (128, 7)])
+def test_forced_variants(kind, bn, splits, monkeypatch):
+    v = run_case(kind, 384, 768, 1792, env={"BSG_FORCE_BN": bn, "BSG_FORCE_SPLITS": splits},
+                 monkeypatch=monkeypatch, bias=True, silu=True)
+    assert "_bn%d_s%d_" % (bn, splits) in v
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_persistent_multi_tile_per_cta(kind):
+    # 16 x 10 = 160 tiles of 128 x 256 on 152 SMs: some CTAs run two tiles
+    v = run_case(kind, 2048, 2560, 512)
+    assert "_bn256_s1_" in v
+
+
+def test_device_alpha_and_repeat_runs():
+    prob = P.make_problem("nvfp4", 256, 512, 512)
+    dp = P.DeviceProblem(prob, out="bf16", bias=True, silu=True)
+    alpha = torch.tensor([float(prob["alpha"])], dtype=torch.float32, device="cuda")
+    with dp.plan(alpha_dev=alpha) as plan:
+        for _ in range(3):
+            plan.run()
+        plan.check_status()
+        P.assert_parity(dp.result(), prob, "bf16", dp.bias_vals, True)
+
+
+def test_one_shot_calls_match_oracle():
+    bsg.bsg_cache_clear()
+    for kind in ("mxfp8", "nvfp4"):
+        prob = P.make_problem(kind, 192, 256, 384)
+        dp = P.DeviceProblem(prob, out="bf16", bias=(kind == "nvfp4"), silu=(kind == "nvfp4"))
+        for _ in range(2):                       # second call is a plan-cache hit
+            if kind == "mxfp8":
+                bsg.mxfp8_gemm(dp.D, dp.A, dp.B, dp.SFA, dp.SFB, float(prob["alpha"]), 192, 256, 384,
+                               bsg.BSG_OUT_BF16)
+            else:
+                bsg.nvfp4_gemm(dp.D, dp.A, dp.B, dp.SFA, dp.SFB, dp.bias, float(prob["alpha"]), dp.flags,
+                               192, 256, 384, bsg.BSG_OUT_BF16)
+            P.assert_parity(dp.result(), prob, "bf16", dp.bias_vals, kind == "nvfp4")
+    bsg.bsg_cache_clear()
+
+
+def test_undersized_scale_buffer_is_rejected():
+    prob = P.make_problem("mxfp8", 256, 256, 256)
+    dp = P.DeviceProblem(prob)
+    small = torch.zeros(128, dtype=torch.uint8, device="cuda")
+    with pytest.raises(bsg.BsgError) as e:
+        bsg.bsg_plan_create(bsg.BSG_MXFP8, bsg.BSG_OUT_BF16, 256, 256, 256, dp.A, dp.B, small[16:], dp.SFB, dp.D)
+    assert e.value.name == "BSG_ERR_SCALE_LAYOUT"
+
+
+def test_wait_timeout_reports_status_and_context_survives():
+    prob = P.make_problem("mxfp8", 256, 256, 256)
+    dp = P.DeviceProblem(prob)
+    with dp.plan() as plan:
+        bsg.bsg_plan_debug_set(plan.handle, 1, 50_000_000)       # 50 ms limit, first stage never loaded
+        plan.run()
+        with pytest.raises(bsg.BsgError) as e:
+            plan.check_status()
+        assert e.value.name == "BSG_ERR_DEVICE_TIMEOUT"
+        bsg.bsg_plan_debug_set(plan.handle, 0, 0)
+        plan.run()
+        plan.check_status()
+        P.assert_parity(dp.result(), prob, "bf16")

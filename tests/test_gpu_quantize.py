@@ -1,0 +1,80 @@
+"""GPU quantisers (bsg_quantize through the C ABI) against the CPU oracle: bit-exact codes,
+bit-exact swizzled scale buffers (padding included) and the NVFP4 global scale."""
+
+import numpy as np
+import pytest
+import torch
+
+import fp4_gemm_blackwell_gb300 as bsg
+from fp4_gemm_blackwell_gb300 import synth
+from oracle import formats as F
+from oracle import layout as L
+from oracle import quantize as Q
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_quantize(kind, x):
+    rows, K = x.shape
+    k = bsg.BSG_MXFP8 if kind == "mxfp8" else bsg.BSG_NVFP4
+    xd = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+    nb = rows * K if kind == "mxfp8" else rows * K // 2
+    codes = torch.full((nb,), 0xCD, dtype=torch.uint8, device="cuda")
+    sf = torch.full((bsg.bsg_sf_bytes(k, rows, K),), 0xAB, dtype=torch.uint8, device="cuda")
+    gs = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    bsg.bsg_quantize(k, xd, rows, K, codes, sf, gs)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), sf.cpu().numpy(), gs.item()
+
+
+def check(kind, x):
+    codes, sf, gs = gpu_quantize(kind, x)
+    if kind == "mxfp8":
+        oc, osf = Q.quantize_mxfp8(x)
+    else:
+        oc, osf, s = Q.quantize_nvfp4(x)
+        assert np.float32(gs) == s
+    assert np.array_equal(codes, oc.ravel()), "codes differ at %s" % np.flatnonzero(codes != oc.ravel())[:8]
+    want = L.swizzle(osf)
+    assert np.array_equal(sf, want), "scales differ at %s" % np.flatnonzero(sf != want)[:8]
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("rows,K", [(1, 32), (128, 256), (200, 96), (129, 160), (256, 4096), (1000, 512)])
+def test_quantiser_matches_oracle(kind, rows, K):
+    gen = synth.normal if kind == "mxfp8" else synth.normal_rowscaled
+    check(kind, gen(rows, K, seed=rows + K))
+
+
+def test_mx_ties_extremes_and_signs():
+    pos = F.E4M3_VALUES[:0x7F]
+    mids = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)             # every E4M3 tie
+    rows = []
+    for i in range(0, len(mids), 31):
+        blk = np.zeros(32, dtype=np.float32)
+        blk[0] = 448.0                                                 # amax 448 -> scale 2^0
+        chunk = mids[i:i + 31]
+        blk[1:1 + len(chunk)] = chunk * np.where(np.arange(len(chunk)) % 2, -1, 1)
+        rows.append(blk)
+    special = np.zeros(32, dtype=np.float32)                          # an all-zero block
+    tiny = np.full(32, 1e-41, dtype=np.float32)                       # subnormal amax
+    huge = np.linspace(-3e38, 3e38, 32).astype(np.float32)
+    neg_small = np.array([-1e-9] * 16 + [1.0] * 16, dtype=np.float32)  # negatives that round to -0
+    x = np.stack(rows + [special, tiny, huge, neg_small])
+    check("mxfp8", x)
+
+
+def test_nv_closed_form_ties_and_zero_tensor():
+    # s = 2688 / 2688 = 1; the block with amax 6 has scale 1, so elements are E2M1(x) directly
+    row0 = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -5.0, 0.1, 0.3, 4.4, -6.0, 1.0] * 2,
+                    dtype=np.float32)
+    row1 = np.zeros(32, dtype=np.float32)
+    row1[0] = 2688.0
+    check("nvfp4", np.stack([row0, row1]))
+    check("nvfp4", np.zeros((3, 64), dtype=np.float32))
+
+
+def test_full_size_operand_rows():
+    # an 8192 x 8192 NVFP4 operand and an 8000-row MXFP8 operand, compared whole
+    check("nvfp4", synth.normal_rowscaled(8192, 8192, seed=1))
+    check("mxfp8", synth.normal(8000, 8192, seed=0))
