@@ -106,9 +106,13 @@ def test_one_shot_calls_match_oracle():
 def test_undersized_scale_buffer_is_rejected():
     prob = P.make_problem("mxfp8", 256, 256, 256)
     dp = P.DeviceProblem(prob)
-    small = torch.zeros(128, dtype=torch.uint8, device="cuda")
+    # the caching allocator sub-allocates large segments: take the last 512 bytes of a fresh
+    # 64 MiB segment, so that the 2048-byte scale buffer would run past the allocation's end
+    torch.cuda.empty_cache()
+    seg = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    tail = seg[(64 << 20) - 512:]
     with pytest.raises(bsg.BsgError) as e:
-        bsg.bsg_plan_create(bsg.BSG_MXFP8, bsg.BSG_OUT_BF16, 256, 256, 256, dp.A, dp.B, small[16:], dp.SFB, dp.D)
+        bsg.bsg_plan_create(bsg.BSG_MXFP8, bsg.BSG_OUT_BF16, 256, 256, 256, dp.A, dp.B, tail, dp.SFB, dp.D)
     assert e.value.name == "BSG_ERR_SCALE_LAYOUT"
 
 
