@@ -1,0 +1,617 @@
+"""Benchmark of the block-scaled GEMM library on GB300.
+
+Headline workload (one step = one GEMM through the library's plan, operands already
+quantised and resident in HBM):
+    NVFP4 GEMM M=128, N=4096, K=4096, BF16 bias + SiLU, BF16 out (skinny M, HBM-bound).
+Metric: block-scaled GEMM TFLOPS (2*M*N*K per step); extras in the same JSON line give
+the roofline of the dominant kernel, the host microseconds per call against the kernel
+time, the end-to-end number through the C ABI with host buffers, the other workloads
+(MXFP8 256^3, MXFP8 8192^3 FP16/BF16, NVFP4 8192^3 and 8000x8192x8192, the launch loop)
+and the CPU oracle timed on this machine's host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--quick]
+
+Inputs rotate over enough copies that the operands of a step are not in L2 from the
+previous use (the copies together exceed the 129 MB L2).  Timed regions are bracketed by
+torch.cuda.synchronize (and a barrier with N > 1) and measured with CUDA events on the
+stream the kernels are launched on.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+M1, N1, K1 = 128, 4096, 4096          # the headline workload
+L2_BYTES = 129 * 1024 * 1024
+SM_COUNT_DEFAULT = 152
+
+
+# ---------------------------------------------------------------- peaks and clocks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# dense tensor rate of each operand type relative to bf16 (nominal GB300: bf16 2.25, fp8 4.5, fp4 13.5 PF)
+NOMINAL_RATIO = {"fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while a region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            t = [x.strip() for x in line.split(",")]
+            if len(t) < 8:
+                continue
+            try:
+                sm.append(float(t[0]))
+                smax.append(float(t[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, t[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp4_gemm_blackwell_gb300", "csrc")
+    for name in ("gemm_kernel.cuh", "ptx.cuh", "bsg_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """dram read+write bytes per launch from a committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel + "|" + workload]
+    except Exception:
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- operands
+class Operands:
+    """One quantised operand on the device, made by the library's own quantiser."""
+
+    def __init__(self, bsg, kind, rows, K, seed):
+        from fp4_gemm_blackwell_gb300 import synth
+        gen = synth.normal if kind == "mxfp8" else synth.normal_rowscaled
+        x = torch.from_numpy(gen(rows, K, seed)).cuda()
+        k = bsg.BSG_MXFP8 if kind == "mxfp8" else bsg.BSG_NVFP4
+        self.codes = torch.empty(rows * K if kind == "mxfp8" else rows * K // 2, dtype=torch.uint8, device="cuda")
+        self.sf = torch.empty(bsg.bsg_sf_bytes(k, rows, K), dtype=torch.uint8, device="cuda")
+        gs = torch.zeros(1, dtype=torch.float32, device="cuda")
+        bsg.bsg_quantize(k, x, rows, K, self.codes, self.sf, gs)
+        torch.cuda.synchronize()
+        self.s = float(gs.item()) if kind == "nvfp4" else 1.0
+        del x
+
+    def clone(self):
+        c = Operands.__new__(Operands)
+        c.codes, c.sf, c.s = self.codes.clone(), self.sf.clone(), self.s
+        return c
+
+
+class Problem:
+    """R device copies of one GEMM problem (operands, bias, output) with a plan per copy."""
+
+    def __init__(self, bsg, kind, M, N, K, out="bf16", bias=False, silu=False, copies=1, seeds=(0, 1)):
+        from fp4_gemm_blackwell_gb300 import synth
+        self.kind, self.M, self.N, self.K, self.out = kind, M, N, K, out
+        a = Operands(bsg, kind, M, K, seeds[0])
+        b = Operands(bsg, kind, N, K, seeds[1])
+        self.alpha = float(np.float32(np.float32(a.s) * np.float32(b.s)))
+        self.flags = (bsg.BSG_F_BIAS if bias else 0) | (bsg.BSG_F_SILU if silu else 0)
+        bias_t = None
+        if bias:
+            bits, _ = synth.bias(N, out=out)
+            bias_t = torch.from_numpy(bits.view(np.int16)).cuda()
+        out_t = bsg.BSG_OUT_BF16 if out == "bf16" else bsg.BSG_OUT_F16
+        k = bsg.BSG_MXFP8 if kind == "mxfp8" else bsg.BSG_NVFP4
+        self.sets, self.plans = [], []
+        for i in range(copies):
+            ai, bi = (a, b) if i == 0 else (a.clone(), b.clone())
+            bt = None if bias_t is None else (bias_t if i == 0 else bias_t.clone())
+            d = torch.empty(M * N, dtype=torch.int16, device="cuda")
+            self.sets.append((ai, bi, bt, d))
+            self.plans.append(bsg.Plan(k, out_t, M, N, K, ai.codes, bi.codes, ai.sf, bi.sf, d,
+                                       alpha=self.alpha, flags=self.flags, bias=bt))
+        self.variant = self.plans[0].variant
+
+    def flops(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def algorithmic_bytes(self):
+        """Bytes one launch must move at least: codes + scales of A and B, bias, output."""
+        cb = 1 if self.kind == "mxfp8" else 0.5
+        blk = 32 if self.kind == "mxfp8" else 16
+        sf = lambda rows: ((rows + 127) // 128 * 128) * ((self.K // blk + 3) // 4 * 4)
+        b = self.M * self.K * cb + self.N * self.K * cb + sf(self.M) + sf(self.N) + self.M * self.N * 2
+        if self.flags & 1:
+            b += self.N * 2
+        return int(b)
+
+    def close(self):
+        for p in self.plans:
+            p.close()
+        self.plans = []
+
+
+def copies_to_exceed_l2(bytes_per_copy):
+    return max(1, min(64, int(np.ceil(1.5 * L2_BYTES / max(bytes_per_copy, 1)))))
+
+
+def graph_time(plans, steps, warmup, barrier=None):
+    """Capture `steps` launches (rotating over plans) in one CUDA graph and time one replay.
+
+    Returns (elapsed_ms, number of our kernel launches in the timed region)."""
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            plans[i % len(plans)].run(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(steps):
+            plans[i % len(plans)].run(stream)
+    with torch.cuda.stream(stream):
+        g.replay()                                   # one untimed replay (warm graph upload)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    ms = start.elapsed_time(end)
+    del g
+    return ms, steps
+
+
+def stream_time(plans, steps, warmup):
+    """Plain stream launches behind a device-side sleep, so that the queue is full when the
+    timed region starts: the events then measure back-to-back kernel execution."""
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            plans[i % len(plans)].run(stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(2e6) * max(1, steps // 50))
+        start.record(stream)
+        t0 = time.perf_counter()
+        for i in range(steps):
+            plans[i % len(plans)].run(stream)
+        host_s = time.perf_counter() - t0
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end), host_s * 1e6 / steps
+
+
+# ---------------------------------------------------------------- the headline step
+def headline(bsg, steps, warmup, barrier):
+    probe = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=1)
+    per_copy = probe.algorithmic_bytes()
+    probe.close()
+    copies = copies_to_exceed_l2(per_copy)
+    prob = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=copies)
+    ms, launches = graph_time(prob.plans, steps, warmup, barrier)
+    stream_ms, host_us = stream_time(prob.plans, min(steps, 1000), warmup)
+    out = dict(problem=prob, ms=ms, launches=launches, copies=copies, per_copy=per_copy,
+               stream_kernel_us=stream_ms * 1e3 / min(steps, 1000), host_us_per_run=host_us)
+    return out
+
+
+def e2e(bsg, steps):
+    """Same workload through the one-shot C-ABI call, host buffers in and out every step."""
+    from fp4_gemm_blackwell_gb300 import synth
+    prob = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=1)
+    a, b, bias_d, d = prob.sets[0]
+    prob.close()
+    host = [t.cpu().pin_memory() for t in (a.codes, a.sf, b.codes, b.sf, bias_d)]
+    dev_in = [a.codes, a.sf, b.codes, b.sf, bias_d]
+    d_host = torch.empty_like(d, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = d.numel() * d.element_size()
+    ptrs = [t.data_ptr() for t in dev_in] + [d.data_ptr()]
+    L = bsg.lib()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    flags = prob.flags
+
+    def step():
+        for dst, src in zip(dev_in, host):
+            dst.copy_(src, non_blocking=True)
+        st = L.nvfp4_gemm(ptrs[5], ptrs[0], ptrs[2], ptrs[1], ptrs[3], ptrs[4], prob.alpha, flags,
+                          M1, N1, K1, bsg.BSG_OUT_BF16, sp)
+        if st != 0:
+            raise bsg.BsgError(st, bsg.bsg_last_error())
+        d_host.copy_(d, non_blocking=True)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    bsg.bsg_cache_clear()
+    tflops = 2.0 * M1 * N1 * K1 * steps / dt / 1e12
+    return {"value": round(tflops, 4), "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(dt * 1e3 / steps, 4), "steps": steps,
+            "path": "nvfp4_gemm (C ABI, cached plan) + pinned H2D of A/SFA/B/SFB/bias + D2H of D"}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return rank, world, local, dist
+    torch.cuda.set_device(0)
+    return 0, 1, 0, None
+
+
+# ---------------------------------------------------------------- the other workloads
+def tensor_peak(peaks, kind):
+    return peaks["bf16_tflops"] * NOMINAL_RATIO["fp8" if kind == "mxfp8" else "fp4"]
+
+
+def big_config(bsg, peaks, kind, M, N, K, out, bias, silu, steps=20, warmup=3):
+    prob = Problem(bsg, kind, M, N, K, out=out, bias=bias, silu=silu, copies=1)
+    ms, _ = graph_time(prob.plans, steps, warmup)
+    us = ms * 1e3 / steps
+    tf = prob.flops() / (us * 1e-6) / 1e12
+    peak = tensor_peak(peaks, kind)
+    r = {"us": round(us, 2), "tflops": round(tf, 1), "peak_tflops": round(peak, 1),
+         "frac_of_peak": round(tf / peak, 4), "variant": prob.variant,
+         "l2": "single input set of %.0f MB" % (prob.algorithmic_bytes() / 2 ** 20)}
+    prob.close()
+    return r
+
+
+def small_config(bsg, peaks, steps=2000, warmup=20):
+    prob = Problem(bsg, "mxfp8", 256, 256, 256, copies=64)
+    ms, _ = graph_time(prob.plans, steps, warmup)
+    us = ms * 1e3 / steps
+    tf = prob.flops() / (us * 1e-6) / 1e12
+    r = {"us": round(us, 3), "tflops": round(tf, 2), "frac_of_peak": round(tf / tensor_peak(peaks, "mxfp8"), 5),
+         "variant": prob.variant, "l2": "64 rotating sets, L2-resident (17 MB)", "bound": "launch latency"}
+    prob.close()
+    return r
+
+
+def launch_loop(bsg, calls=1000):
+    """1000 NVFP4 GEMM calls cycling M in {1,16,128,1024} x (N,K) in {(4096,4096),(14336,4096),
+    (4096,14336)}, BF16 out: host time per call against device kernel time, (i) one-shot C-ABI
+    calls (cached plans) on a stream, (ii) the same 1000 calls captured once in a CUDA graph."""
+    shapes = [(m, n, k) for m in (1, 16, 128, 1024) for (n, k) in ((4096, 4096), (14336, 4096), (4096, 14336))]
+    ops_a, ops_b = {}, {}
+    for (m, n, k) in shapes:
+        if (m, k) not in ops_a:
+            ops_a[(m, k)] = Operands(bsg, "nvfp4", m, k, 0)
+        if (n, k) not in ops_b:
+            ops_b[(n, k)] = Operands(bsg, "nvfp4", n, k, 1)
+    L = bsg.lib()
+    calls_args = []
+    keep = []
+    for (m, n, k) in shapes:
+        a, b = ops_a[(m, k)], ops_b[(n, k)]
+        d = torch.empty(m * n, dtype=torch.int16, device="cuda")
+        keep.append(d)
+        alpha = float(np.float32(np.float32(a.s) * np.float32(b.s)))
+        calls_args.append((d.data_ptr(), a.codes.data_ptr(), b.codes.data_ptr(), a.sf.data_ptr(), b.sf.data_ptr(),
+                           None, alpha, 0, m, n, k, bsg.BSG_OUT_BF16))
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+
+    def issue(i):
+        st = L.nvfp4_gemm(*calls_args[i % len(calls_args)], sp)
+        if st != 0:
+            raise bsg.BsgError(st, bsg.bsg_last_error())
+
+    for i in range(len(shapes) * 3):            # plan-cache misses happen here, untimed
+        issue(i)
+    torch.cuda.synchronize()
+    # (i) stream: host enqueue time, then wall time to completion
+    t0 = time.perf_counter()
+    for i in range(calls):
+        issue(i)
+    host_stream = (time.perf_counter() - t0) * 1e6 / calls
+    torch.cuda.synchronize()
+    wall_stream = (time.perf_counter() - t0) * 1e6 / calls
+    # device time of the same 1000 kernels, back to back (graph replay timed with events)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(calls):
+            issue(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        t1 = time.perf_counter()
+        g.replay()
+        host_graph = (time.perf_counter() - t1) * 1e6 / calls
+        end.record(stream)
+    torch.cuda.synchronize()
+    kernel_us = start.elapsed_time(end) * 1e3 / calls
+    bsg.bsg_cache_clear()
+    del g
+    return {"calls": calls, "shapes": len(shapes), "kernel_us_per_call": round(kernel_us, 3),
+            "stream": {"host_us_per_call": round(host_stream, 3), "wall_us_per_call": round(wall_stream, 3),
+                       "host_over_kernel": round(host_stream / kernel_us, 3)},
+            "graph": {"host_us_per_call": round(host_graph, 4), "host_over_kernel": round(host_graph / kernel_us, 4)},
+            "note": "host time is the enqueue time through the Python ctypes binding"}
+
+
+# ---------------------------------------------------------------- the CPU oracle
+def oracle_problem():
+    """The headline problem's operands quantised by the CPU oracle (setup, untimed)."""
+    from fp4_gemm_blackwell_gb300 import synth
+    from oracle import layout as OL
+    from oracle import quantize as OQ
+    xa = synth.normal_rowscaled(M1, K1, synth.SEED_A)
+    xb = synth.normal_rowscaled(N1, K1, synth.SEED_B)
+    a, sfa, sa = OQ.quantize_nvfp4(xa)
+    b, sfb, sb = OQ.quantize_nvfp4(xb)
+    _, bias = synth.bias(N1)
+    return dict(A=a, B=b, sfa=sfa, sfb=sfb, SFA=OL.swizzle(sfa), SFB=OL.swizzle(sfb),
+                alpha=np.float32(np.float32(sa) * np.float32(sb)), bias=bias)
+
+
+def cpu_baseline(budget_s=10.0):
+    """The oracle as it stands (decode through its tables, FP64 GEMM, epilogue, rounding) on the
+    whole headline problem, repeated until about `budget_s` seconds of CPU work."""
+    from oracle import gemm as OG
+    p = oracle_problem()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        OG.reference(OG.NVFP4, p["A"], p["B"], p["SFA"], p["SFB"], M1, N1, K1, alpha=p["alpha"],
+                     bias=p["bias"], silu=True, out=OG.BF16)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    tf = reps * 2.0 * M1 * N1 * K1 / dt / 1e12
+    return {"value": round(tf, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d full NVFP4 M=128 N=4096 K=4096 problems (table decode, float64 numpy matmul, bias, "
+                      "SiLU, BF16 rounding) in %.1f s; numpy's BLAS uses all %d host threads"
+                      % (reps, dt, os.cpu_count())}
+
+
+def reference_arm(args):
+    """--impl reference: the CPU oracle is the reference implementation on this workload.  A step
+    is a bounded sample: a 128 x 16 block of the output over the full K."""
+    from oracle import gemm as OG
+    from oracle import layout as OL
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    p = oracle_problem()
+    cols = 16
+    B = p["B"][:cols]
+    SFB = OL.swizzle(p["sfb"][:cols])
+    bias = p["bias"][:cols]
+
+    def step():
+        OG.reference(OG.NVFP4, p["A"], B, p["SFA"], SFB, M1, cols, K1, alpha=p["alpha"], bias=bias, silu=True,
+                     out=OG.BF16)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    flops = 2.0 * M1 * cols * K1 * args.steps
+    tf = flops / dt / 1e12
+    sample = "per step a 128 x %d output block of NVFP4 M=128 N=4096 K=4096 (bias+SiLU, BF16) by the float64 oracle" % cols
+    line = {"impl": "reference", "metric": METRIC, "value": round(tf, 6), "unit": "TFLOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "M": M1, "N": N1, "K": K1},
+            "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(tf, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+CASES = {
+    "nvfp4_m128": ("nvfp4", M1, N1, K1, "bf16", True, True),
+    "mxfp8_256": ("mxfp8", 256, 256, 256, "bf16", False, False),
+    "mxfp8_8192": ("mxfp8", 8192, 8192, 8192, "bf16", False, False),
+    "mxfp8_8192_f16": ("mxfp8", 8192, 8192, 8192, "f16", False, False),
+    "nvfp4_8192": ("nvfp4", 8192, 8192, 8192, "bf16", True, True),
+    "nvfp4_8000": ("nvfp4", 8000, 8192, 8192, "bf16", True, True),
+}
+
+
+def case_arm(args):
+    """--case NAME: one workload, `steps` plain stream launches of its plan after `warmup`
+    (for profiler captures and quick timing); prints one JSON line."""
+    import __graft_entry__
+    import fp4_gemm_blackwell_gb300 as bsg
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    kind, M, N, K, out, bias, silu = CASES[args.case]
+    prob = Problem(bsg, kind, M, N, K, out=out, bias=bias, silu=silu, copies=1)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            prob.plans[0].run(stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            prob.plans[0].run(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    us = start.elapsed_time(end) * 1e3 / args.steps
+    prob.plans[0].check_status()
+    print(json.dumps({"case": args.case, "variant": prob.variant, "us_per_launch": round(us, 3),
+                      "tflops": round(prob.flops() / (us * 1e-6) / 1e12, 2),
+                      "gbs": round(prob.algorithmic_bytes() / (us * 1e-6) / 1e9, 1)}), flush=True)
+    prob.close()
+    return 0
+
+
+METRIC = "block-scaled GEMM TFLOPS & % tensor peak (MXFP8, NVFP4); host µs/call vs kernel"
+WORKLOAD = "nvfp4_gemm M=128 N=4096 K=4096, bf16 bias + SiLU, bf16 out"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline only (no other workloads, no CPU baseline)")
+    ap.add_argument("--case", choices=sorted(CASES), help="time one workload with plain launches and exit")
+    args = ap.parse_args()
+    if args.case:
+        return case_arm(args)
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import __graft_entry__
+    import fp4_gemm_blackwell_gb300 as bsg
+    rank, world, local, dist = dist_setup(args.gpus)
+    if rank == 0:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+    bsg.lib()
+    barrier = (lambda: dist.barrier()) if dist else None
+    peaks = load_peaks()
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    h = headline(bsg, args.steps, args.warmup, barrier)
+    clocks = sampler.stop() if rank == 0 else None
+    prob = h["problem"]
+    ms_max = h["ms"]
+    if dist:
+        t = torch.tensor([h["ms"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    total_flops = prob.flops() * args.steps * world
+    value = total_flops / (ms_max * 1e-3) / 1e12
+    kernel_us = h["ms"] * 1e3 / args.steps
+    achieved = prob.algorithmic_bytes() / (kernel_us * 1e-6) / 1e9
+    result = None
+    if rank == 0:
+        extras = {}
+        e2e_r = e2e(bsg, min(200, args.steps))
+        if not args.quick:
+            extras["mxfp8_256_bf16"] = small_config(bsg, peaks)
+            extras["mxfp8_8192_bf16"] = big_config(bsg, peaks, "mxfp8", 8192, 8192, 8192, "bf16", False, False)
+            extras["mxfp8_8192_f16"] = big_config(bsg, peaks, "mxfp8", 8192, 8192, 8192, "f16", False, False)
+            extras["nvfp4_8192_bias_silu_bf16"] = big_config(bsg, peaks, "nvfp4", 8192, 8192, 8192, "bf16", True, True)
+            extras["nvfp4_8000x8192x8192_bias_silu_bf16"] = big_config(bsg, peaks, "nvfp4", 8000, 8192, 8192, "bf16",
+                                                                       True, True)
+            extras["launch_loop_1000"] = launch_loop(bsg)
+        cpu = cpu_baseline() if not args.quick else None
+        result = {
+            "metric": METRIC, "value": round(value, 4), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32 accumulate", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M1, "N": N1, "K": K1, "variant": prob.variant,
+                       "l2": "inputs rotate over %d copies (%.0f MB > 129 MB L2)" % (h["copies"], h["copies"] * h["per_copy"] / 2 ** 20),
+                       "timing": "CUDA events around one CUDA-graph replay of the K plan launches",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": recorded_traffic("bsg_gemm_kernel<nvfp4,bn128>", "nvfp4_m128_n4096_k4096"),
+                         "algorithmic_bytes_per_launch": prob.algorithmic_bytes(),
+                         "kernel_us": round(kernel_us, 3), "peak_source": peaks["source"] + " hbm_gbs (burst copy)"},
+            "host_us_per_call": {"plan_run_stream": round(h["host_us_per_run"], 3),
+                                 "kernel_us_stream_back_to_back": round(h["stream_kernel_us"], 3)},
+            "clocks": clocks, "e2e": e2e_r, "gpu_launches": h["launches"], "cpu_baseline": cpu, "extras": extras,
+        }
+    prob.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
