@@ -159,8 +159,11 @@ __device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0
       for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(alpha, v[8 * g + i]);
     }
     if (p.flags & F_SILU) {
+      // y * sigmoid(y).  The reciprocal uses the fast division: an IEEE division takes a
+      // slow path whenever 1 + e^-y overflows (y < -88), which is common for long K.
+      // __fdividef(1, d) returns 0 for d > 2^126, the correctly rounded sigmoid there.
 #pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = y[i] / (1.0f + __expf(-y[i]));
+      for (int i = 0; i < 8; ++i) y[i] = y[i] * __fdividef(1.0f, 1.0f + __expf(-y[i]));
     }
     uint4 o;
     o.x = pack2<OUT>(y[0], y[1]);
