@@ -15,7 +15,7 @@ __all__ = [
     "BSG_F_ALPHA_DEVICE", "BsgError", "lib", "bsg_sf_bytes", "bsg_quantize", "bsg_plan_create",
     "bsg_plan_run", "bsg_plan_destroy", "bsg_plan_check_status", "bsg_plan_variant",
     "bsg_plan_debug_set", "mxfp8_gemm", "nvfp4_gemm", "bsg_cache_clear", "bsg_last_error",
-    "bsg_version", "Plan",
+    "bsg_version", "Plan", "bsg_gemm_noalloc",
 ]
 
 BSG_MXFP8, BSG_NVFP4 = 0, 1
@@ -71,6 +71,7 @@ def lib():
         "mxfp8_gemm": (st, [vp, vp, vp, vp, vp, f, i, i, i, i, vp]),
         "nvfp4_gemm": (st, [vp, vp, vp, vp, vp, vp, f, u, i, i, i, i, vp]),
         "bsg_cache_clear": (st, []),
+        "bsg_gemm_noalloc": (st, [ctypes.POINTER(BsgDesc), vp]),
         "bsg_sf_bytes": (ctypes.c_size_t, [i, i, i]),
         "bsg_quantize": (st, [i, vp, i, i, vp, vp, vp, vp]),
         "bsg_last_error": (ctypes.c_char_p, []),
@@ -159,6 +160,14 @@ def mxfp8_gemm(D, A, B, SFA, SFB, alpha, M, N, K, out, stream=None):
 def nvfp4_gemm(D, A, B, SFA, SFB, bias, alpha, flags, M, N, K, out, stream=None):
     _check(lib().nvfp4_gemm(_ptr(D), _ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(bias), alpha, flags,
                             M, N, K, out, _stream(stream)))
+
+
+def bsg_gemm_noalloc(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None,
+                     stream=None):
+    """Allocation-free GEMM (no device allocation; shares one static scratch array per GPU)."""
+    d = BsgDesc(kind, out, flags, M, N, K, _ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(bias), _ptr(D),
+                alpha, _ptr(alpha_dev))
+    _check(lib().bsg_gemm_noalloc(ctypes.byref(d), _stream(stream)))
 
 
 def bsg_cache_clear():

@@ -553,3 +553,124 @@ BSG_API bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, 
   if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
   return BSG_OK;
 }
+
+// ==================================================================== allocation-free GEMM
+// Some callers cannot allocate device memory at the point where they run a GEMM: code that
+// runs inside a custom allocator or memory-pool callback, an engine that forbids device
+// allocation after start-up so that its memory budget stays fixed, or a host environment
+// where the CUDA allocator is owned by someone else.  bsg_gemm_noalloc serves them: it runs
+// the same kernel as bsg_plan_run, but its status word, split-K counters and split-K partial
+// tiles live in the file-scope device array below (kNoAllocScratchBytes per GPU that loads
+// this library, held until the process exits) instead of a plan's cudaMalloc'ed workspace.
+
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr int kNoAllocMaxDevices = 64;
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+unsigned char* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on `dev` (current device); looked up once per device.
+bsg_status noalloc_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(BSG_ERR_INVALID_ARG, "device ordinal %d too large", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(allocation-free scratch)");
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return BSG_OK;
+}
+
+}  // namespace
+
+BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
+  bsg_status s = validate_desc(d);
+  if (s != BSG_OK) return s;
+  int dev = 0;
+  DeviceInfo di;
+  if ((s = current_device(&dev, &di)) != BSG_OK) return s;
+  if (!load_driver_entry_points())
+    return fail(BSG_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled from the driver");
+  if ((s = validate_ranges(d)) != BSG_OK) return s;
+
+  int bn, splits, kps;
+  choose_variant(d, di.sms, &bn, &splits, &kps);
+  bsg::GemmKernelInfo info{};
+  const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
+  const bool found = d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(bn, out_t, &info)
+                                          : bsg::gemm_kernel_info_nv(bn, out_t, &info);
+  if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
+
+  const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
+  const int blk = d->kind == BSG_MXFP8 ? 32 : 16;
+  const int num_m = (d->M + 127) / 128, num_n = (d->N + bn - 1) / bn;
+  const int num_tiles = num_m * num_n;
+  const size_t cnt_off = 256;
+  const size_t part_off = cnt_off + (static_cast<size_t>(num_tiles) * 4 + 255) / 256 * 256;
+  const size_t part_bytes = splits > 1 ? static_cast<size_t>(splits) * num_tiles * 128 * bn * 4 : 0;
+  if (part_off + part_bytes > kNoAllocScratchBytes)
+    return fail(BSG_ERR_SHAPE,
+                "this problem needs %zu bytes of scratch (split-K %d over %d tiles); the allocation-free "
+                "entry point has %zu; use a plan",
+                part_off + part_bytes, splits, num_tiles, kNoAllocScratchBytes);
+  unsigned char* scratch = nullptr;
+  if ((s = noalloc_scratch(dev, &scratch)) != BSG_OK) return s;
+  if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
+
+  bsg::GemmParams g;
+  std::memset(&g, 0, sizeof(g));
+  const size_t rb = code_row_bytes(d->kind, d->K);
+  if ((s = encode_operand(&g.tmap_a, d->A, rb, d->M, 128, "A")) != BSG_OK ||
+      (s = encode_operand(&g.tmap_b, d->B, rb, d->N, static_cast<uint32_t>(bn), "B")) != BSG_OK)
+    return s;
+  g.sfa = static_cast<const uint8_t*>(d->SFA);
+  g.sfb = static_cast<const uint8_t*>(d->SFB);
+  g.bias = d->bias;
+  g.d = d->D;
+  g.alpha_dev = d->alpha_dev;
+  g.wait_limit_ns = kDefaultWaitLimitNs;
+  g.alpha = d->alpha;
+  g.M = d->M;
+  g.N = d->N;
+  g.K = d->K;
+  g.flags = d->flags;
+  g.sfa_atoms_per_band = (d->K / blk + 3) / 4;
+  g.sfb_atoms_per_band = g.sfa_atoms_per_band;
+  g.sfb_bands = (d->N + 127) / 128;
+  g.num_m_tiles = num_m;
+  g.num_n_tiles = num_n;
+  g.num_k_tiles = (d->K + k_tile - 1) / k_tile;
+  g.num_tiles = num_tiles;
+  g.splits = splits;
+  g.k_tiles_per_split = kps;
+  g.num_units = num_tiles * splits;
+  g.group_m = 16;
+  g.debug_skip_first_load = 0;
+  g.status = reinterpret_cast<unsigned*>(scratch);
+  g.counters = reinterpret_cast<unsigned*>(scratch + cnt_off);
+  g.partial = splits > 1 ? reinterpret_cast<float*>(scratch + part_off) : nullptr;
+
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the status word and the split-K counters must start at zero; the partial tiles are
+  // written whole by their split before they are read
+  cudaError_t e = cudaMemsetAsync(scratch, 0, part_off, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(allocation-free scratch)");
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(g.num_units, di.sms)), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(info.threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(info.smem_bytes);
+  cfg.stream = st;
+  void* args[] = {&g};
+  e = cudaLaunchKernelExC(&cfg, info.fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
+  return BSG_OK;
+}

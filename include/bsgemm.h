@@ -134,6 +134,23 @@ bsg_status nvfp4_gemm(void* D, const void* A, const void* B, const void* SFA, co
                       const void* bias, float alpha, unsigned flags, int M, int N, int K,
                       bsg_out out, bsg_stream_t stream);
 
+/* Allocation-free GEMM.  The pages have no counterpart of this call.  It is for callers that
+ * cannot allocate device memory when they run a GEMM -- code running inside an allocator or
+ * memory-pool callback, engines that forbid device allocation after start-up to keep a fixed
+ * memory budget, hosts whose CUDA allocator belongs to someone else.  It computes exactly what
+ * bsg_plan_create + bsg_plan_run compute for `d` (same validation, same kernel), but allocates
+ * no device memory: no cudaMalloc, no cudaFree, no allocating library routine.  Its status
+ * word, split-K counters and split-K partial tiles live in one static device array of
+ * 16 MiB that every GPU loading this library holds until the process exits; a problem whose
+ * split-K partials would not fit is rejected with BSG_ERR_SHAPE (use a plan instead).
+ * The first call on a device looks up that array's device address (once per device, with
+ * that device current); make that first call before any stream capture.  Every call clears
+ * the counters and status word at its start on `stream`; all calls share the one array, so
+ * calls that overlap on the GPU (different streams, or concurrent host threads) race.
+ * A kernel that gives up a wait is not reported by this call (there is no plan to query).
+ * Each call encodes its tensor maps on the host, so it costs more host time than a plan. */
+bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream);
+
 /* Drop every plan of the one-shot cache (after the work using them has completed). */
 bsg_status bsg_cache_clear(void);
 
