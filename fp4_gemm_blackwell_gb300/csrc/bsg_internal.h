@@ -12,6 +12,11 @@ enum : int { KIND_MX = 0, KIND_NV = 1 };
 enum : int { OUT_F16 = 0, OUT_BF16 = 1 };
 enum : unsigned { F_BIAS = 1u, F_SILU = 2u, F_ALPHA_DEVICE = 4u };
 
+// How split-K partial tiles are combined: not split; FP32 partials in the plan's global
+// workspace, summed by the last split to arrive; or the splits of a tile form one thread-block
+// cluster and each CTA sums a slab of rows from the peers' shared memory (DSMEM).
+enum : int { SPLIT_NONE = 0, SPLIT_WORKSPACE = 1, SPLIT_CLUSTER = 2 };
+
 // Bits of the device status word (OR-ed in by a CTA that gives up a wait).
 enum : unsigned {
   ST_TIMEOUT_PRODUCER = 1u << 0,
@@ -43,6 +48,7 @@ struct GemmParams {
   int num_m_tiles, num_n_tiles, num_k_tiles;
   int num_tiles;
   int splits;              // split-K factor (every split owns >= 1 k-tile)
+  int split_mode;          // SPLIT_NONE, SPLIT_WORKSPACE or SPLIT_CLUSTER
   int k_tiles_per_split;
   int num_units;           // num_tiles * splits
   int group_m;             // tile rasterisation: m-blocks per group

@@ -5,7 +5,8 @@
 //               atoms into a STAGES-deep shared-memory ring (mbarrier full / empty pairs);
 //   warp 1      owns tensor memory; one thread copies the scale atoms into TMEM (tcgen05.cp)
 //               and issues the block-scaled tcgen05.mma chain into an FP32 accumulator;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes 32*(w%4)..),
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes 32*(w%4)..,
+//               warps 2..5 the first half of the columns, warps 6..9 the second half),
 //               alpha, bias, SiLU, FP16/BF16 rounding and stores; with split-K, FP32 partial
 //               tiles in the workspace and a deterministic reduction by the last split.
 // Tile 128 x BN x (128 bytes of K): MXFP8 = 128 E4M3 per row per stage (four K=32 MMAs, one
@@ -53,7 +54,9 @@ struct GemmCfg {
   static constexpr int SF_COL0 = NACC * BN;
   static constexpr int TMEM_USED = SF_COL0 + 2 * SF_SLOT_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
-  static constexpr int THREADS = 192;
+  static constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half the columns
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS;
   // Instruction descriptor (block-scaled kinds): [4,6) B scale id, [7,10) A type,
   // [10,13) B type, [15]/[16] A/B major (0 = K), [17,23) N >> 3, [23] scale type
   // (1 = UE8M0, 0 = UE4M3), [24,29) M >> 4, [29,31) A scale id.
@@ -137,6 +140,39 @@ __device__ __forceinline__ float out_to_float(uint16_t bits) {
   }
 }
 
+// alpha, bias[n + i], SiLU on W consecutive accumulator values of one row, rounded to the
+// output type and packed two per word.  Columns at or beyond N read no bias.
+template <int OUT, int W>
+__device__ __forceinline__ void epi_pack(const GemmParams& p, int n, const float* v, float alpha,
+                                         uint32_t* out) {
+  static_assert(W == 4 || W == 8, "group width");
+  float y[W];
+  if ((p.flags & F_BIAS) && n < p.N) {
+    uint16_t b[W];
+    if constexpr (W == 8) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias) + n));
+      *reinterpret_cast<uint4*>(b) = raw;
+    } else {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
+      *reinterpret_cast<uint2*>(b) = raw;
+    }
+#pragma unroll
+    for (int i = 0; i < W; ++i) y[i] = __fmaf_rn(alpha, v[i], out_to_float<OUT>(b[i]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < W; ++i) y[i] = __fmul_rn(alpha, v[i]);
+  }
+  if (p.flags & F_SILU) {
+    // y * sigmoid(y).  The reciprocal uses the fast division: an IEEE division takes a
+    // slow path whenever 1 + e^-y overflows (y < -88), which is common for long K.
+    // __fdividef(1, d) returns 0 for d > 2^126, the correctly rounded sigmoid there.
+#pragma unroll
+    for (int i = 0; i < W; ++i) y[i] = y[i] * __fdividef(1.0f, 1.0f + __expf(-y[i]));
+  }
+#pragma unroll
+  for (int i = 0; i < W / 2; ++i) out[i] = pack2<OUT>(y[2 * i], y[2 * i + 1]);
+}
+
 // Epilogue of 32 consecutive columns n0.. of output row m held by this thread.
 template <int OUT>
 __device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0, const float* v,
@@ -147,35 +183,57 @@ __device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0
   for (int g = 0; g < 4; ++g) {
     const int n = n0 + 8 * g;
     if (n >= p.N) break;  // N % 16 == 0: groups of 8 are whole
-    float y[8];
-    if (p.flags & F_BIAS) {
-      const uint4 braw =
-          __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias) + n));
-      const uint16_t* b = reinterpret_cast<const uint16_t*>(&braw);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = __fmaf_rn(alpha, v[8 * g + i], out_to_float<OUT>(b[i]));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(alpha, v[8 * g + i]);
-    }
-    if (p.flags & F_SILU) {
-      // y * sigmoid(y).  The reciprocal uses the fast division: an IEEE division takes a
-      // slow path whenever 1 + e^-y overflows (y < -88), which is common for long K.
-      // __fdividef(1, d) returns 0 for d > 2^126, the correctly rounded sigmoid there.
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = y[i] * __fdividef(1.0f, 1.0f + __expf(-y[i]));
-    }
     uint4 o;
-    o.x = pack2<OUT>(y[0], y[1]);
-    o.y = pack2<OUT>(y[2], y[3]);
-    o.z = pack2<OUT>(y[4], y[5]);
-    o.w = pack2<OUT>(y[6], y[7]);
+    epi_pack<OUT, 8>(p, n, v + 8 * g, alpha, reinterpret_cast<uint32_t*>(&o));
     *reinterpret_cast<uint4*>(drow + n) = o;
   }
 }
 
+// Split-K through a cluster: the splits of one tile are the CTAs of one cluster, each holding
+// its FP32 partial tile in shared memory as [128 rows][BN + 4] floats.  CTA `split` sums rows
+// [split * 128/S, (split + 1) * 128/S) over the S peers in split order (deterministic), applies
+// the epilogue and stores whole rows (each lane 4 consecutive columns per 128).
+template <int OUT, int BN>
+__device__ __forceinline__ void cluster_reduce(const GemmParams& p, uint32_t part_saddr, const UnitCoord& c,
+                                               float alpha, int ew, int lane) {
+  const int S = p.splits;
+  const int R = 128 / S;
+  for (int r = ew; r < R; r += 8) {
+    const int row = c.split * R + r;
+    const int m = c.m_blk * 128 + row;
+    if (m >= p.M) break;
+    uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+#pragma unroll
+    for (int h = 0; h < BN / 128; ++h) {
+      const int col = h * 128 + 4 * lane;
+      const uint32_t off = part_saddr + static_cast<uint32_t>((row * (BN + 4) + col) * 4);
+      float4 t[8];  // S <= 8: issue every peer's load, then sum in split order
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp)
+        if (sp < S) t[sp] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(sp)));
+      float4 acc = t[0];
+#pragma unroll
+      for (int sp = 1; sp < 8; ++sp) {
+        if (sp < S) {
+          acc.x += t[sp].x;
+          acc.y += t[sp].y;
+          acc.z += t[sp].z;
+          acc.w += t[sp].w;
+        }
+      }
+      const int n = c.n_blk * BN + col;
+      if (n < p.N) {  // N % 16 == 0: groups of 4 are whole
+        const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+        uint2 o;
+        epi_pack<OUT, 4>(p, n, v, alpha, reinterpret_cast<uint32_t*>(&o));
+        *reinterpret_cast<uint2*>(drow + n) = o;
+      }
+    }
+  }
+}
+
 template <int KIND, int BN, int OUT>
-__global__ void __launch_bounds__(192, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<KIND, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -211,7 +269,7 @@ __global__ void __launch_bounds__(192, 1) bsg_gemm_kernel(const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
-      mbar_init(bar_tempty(a), 128);
+      mbar_init(bar_tempty(a), C::EPI_THREADS);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -229,6 +287,11 @@ __global__ void __launch_bounds__(192, 1) bsg_gemm_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above touched only this CTA's own resources; from here on global memory is
+  // read and written, so wait for the preceding grid in the stream (programmatic dependent
+  // launch), and let the next grid start its launch while this one runs.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -362,39 +425,76 @@ __global__ void __launch_bounds__(192, 1) bsg_gemm_kernel(const __grid_constant_
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (warps 2..9)
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;       // accumulator row = TMEM lane
+    constexpr int HC = BN / 2;           // columns per thread
+    const int col0 = ((warp - 2) >> 2) * HC;
     const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
       const UnitCoord c = decode_unit(p, u);
       bool ok = wait_bounded(bar_tfull(acc), acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
-      ok = named_bar_and(1, 128, ok);
+      ok = named_bar_and(1, C::EPI_THREADS, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
       const int m = c.m_blk * C::BM + row;
       const int nbase = c.n_blk * BN;
-      if (p.splits == 1) {
-#pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+      if (p.split_mode == SPLIT_NONE) {
+        // Round the whole row segment into registers first and release the accumulator before
+        // storing, so the next tile's MMAs do not wait for the stores.
+        uint32_t packed[HC / 2];
+#pragma unroll
+        for (int ch = 0; ch < HC / 32; ++ch) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + ch * 32, r);
+          tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
           tmem_ld_wait();
-          if (ch == BN / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(bar_tempty(acc));
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[8 * g + i]);
+            epi_pack<OUT, 8>(p, nbase + col0 + ch * 32 + 8 * g, v, alpha, &packed[ch * 16 + 4 * g]);
           }
-          store_chunk32<OUT>(p, m, nbase + ch * 32, reinterpret_cast<const float*>(r), alpha);
         }
+        tc_fence_before();
+        mbar_arrive(bar_tempty(acc));
+        if (m < p.M) {
+          uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+#pragma unroll
+          for (int g = 0; g < HC / 8; ++g) {
+            const int n = nbase + col0 + 8 * g;
+            if (n < p.N)
+              *reinterpret_cast<uint4*>(drow + n) =
+                  make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+          }
+        }
+      } else if (p.split_mode == SPLIT_CLUSTER) {
+        // partial tile -> this CTA's shared memory (the ring is idle: the unit's MMAs are done)
+        float* part = reinterpret_cast<float*>(smem);
+#pragma unroll 1
+        for (int ch = 0; ch < HC / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
+          tmem_ld_wait();
+          float4* dst = reinterpret_cast<float4*>(part + row * (BN + 4) + col0 + ch * 32);
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            dst[g] = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                 __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+        }
+        tc_fence_before();
+        mbar_arrive(bar_tempty(acc));
       } else {
+        // FP32 partial tile -> workspace as float4 [chunk][8][128 rows] (coalesced per warp)
         float4* part = reinterpret_cast<float4*>(
             p.partial + (static_cast<size_t>(c.split) * p.num_tiles + c.tile) * (C::BM * BN));
+        const int ch0 = col0 / 32;
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+        for (int ch = ch0; ch < ch0 + HC / 32; ++ch) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(t_row + ch * 32, r);
           tmem_ld_wait();
@@ -408,21 +508,21 @@ __global__ void __launch_bounds__(192, 1) bsg_gemm_kernel(const __grid_constant_
         tc_fence_before();
         mbar_arrive(bar_tempty(acc));
         __threadfence();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, C::EPI_THREADS);
         if (threadIdx.x == 64) {
           const unsigned old = atomicAdd(p.counters + c.tile, 1u);
           const int last = (old == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
           if (last) p.counters[c.tile] = 0u;  // ready for the next launch
           *last_flag = last;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, C::EPI_THREADS);
         if (*last_flag) {
           __threadfence();
           const float4* base = reinterpret_cast<const float4*>(
               p.partial + static_cast<size_t>(c.tile) * (C::BM * BN));
           const size_t split_stride = static_cast<size_t>(p.num_tiles) * (C::BM * BN) / 4;
 #pragma unroll 1
-          for (int ch = 0; ch < BN / 32; ++ch) {
+          for (int ch = ch0; ch < ch0 + HC / 32; ++ch) {
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
@@ -439,7 +539,7 @@ __global__ void __launch_bounds__(192, 1) bsg_gemm_kernel(const __grid_constant_
             store_chunk32<OUT>(p, m, nbase + ch * 32, v, alpha);
           }
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, C::EPI_THREADS);
       }
       if (C::NACC == 2) {
         acc ^= 1;
@@ -448,6 +548,21 @@ __global__ void __launch_bounds__(192, 1) bsg_gemm_kernel(const __grid_constant_
         acc_phase ^= 1u;
       }
     }
+  }
+
+  // ------------------------------------------------------------ split-K through the cluster
+  if (p.split_mode == SPLIT_CLUSTER) {
+    // Every thread of every CTA takes part in both cluster barriers, aborted or not, so that no
+    // CTA leaves while a peer may still read its shared memory.
+    __syncwarp();
+    cluster_sync();  // all partial tiles of the cluster are in shared memory
+    if (warp >= 2) {
+      const UnitCoord c = decode_unit(p, blockIdx.x);
+      const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
+      cluster_reduce<OUT, BN>(p, smem0, c, alpha, warp - 2, lane);
+    }
+    __syncwarp();
+    cluster_sync();  // the peers are done reading this CTA's shared memory
   }
 
   // ------------------------------------------------------------ teardown

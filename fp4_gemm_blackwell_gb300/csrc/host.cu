@@ -173,6 +173,7 @@ struct bsg_plan_s {
   bsg::GemmKernelInfo info;
   int device;
   int grid;
+  int cluster;
   void* workspace;
   char variant[64];
 };
@@ -200,20 +201,28 @@ int env_int(const char* name, int dflt) {
 
 // Tile width, split-K: 256-wide tiles when they alone give every SM a tile; otherwise
 // 128-wide tiles (double-buffered accumulator) and, if that still leaves SMs idle, split K so
-// that tiles x splits is close to the SM count.  Every split owns at least one k-tile.
-void choose_variant(const bsg_desc* d, int sms, int* bn, int* splits, int* kps) {
+// that tiles x splits is close to the SM count.  Every split owns at least one k-tile.  Split
+// factors of 2, 4 and 8 combine their partial tiles inside a thread-block cluster (DSMEM);
+// other factors (only reachable by forcing) go through the plan's global workspace.
+struct Variant {
+  int bn, splits, kps, mode, cluster;
+};
+
+Variant choose_variant(const bsg_desc* d, int sms) {
   const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
   const int nkt = (d->K + k_tile - 1) / k_tile;
   const long long mt = (d->M + 127) / 128;
   const long long t256 = mt * ((d->N + 255) / 256);
   const long long t128 = mt * ((d->N + 127) / 128);
-  int b, s;
+  int b, s = 1;
   if (t256 >= sms) {
     b = 256;
-    s = 1;
   } else {
     b = 128;
-    s = t128 >= sms ? 1 : static_cast<int>(std::max<long long>(1, std::min<long long>(nkt, sms / t128)));
+    if (t128 < sms) {
+      const long long want = std::min<long long>(std::min<long long>(nkt, 8), sms / t128);
+      while (s * 2 <= want) s *= 2;
+    }
   }
   const int fb = env_int("BSG_FORCE_BN", 0);
   if (fb == 128 || fb == 256) b = fb;
@@ -221,9 +230,29 @@ void choose_variant(const bsg_desc* d, int sms, int* bn, int* splits, int* kps) 
   if (fs >= 1) s = std::min(fs, nkt);
   int k = (nkt + s - 1) / s;
   s = (nkt + k - 1) / k;
-  *bn = b;
-  *splits = s;
-  *kps = k;
+  Variant v;
+  v.bn = b;
+  v.splits = s;
+  v.kps = k;
+  const bool pow2 = s == 2 || s == 4 || s == 8;
+  v.mode = s == 1 ? bsg::SPLIT_NONE
+                  : (pow2 && env_int("BSG_SPLIT_WORKSPACE", 0) == 0 ? bsg::SPLIT_CLUSTER : bsg::SPLIT_WORKSPACE);
+  v.cluster = v.mode == bsg::SPLIT_CLUSTER ? s : 1;
+  return v;
+}
+
+// Workspace layout: [status word | per-tile counters | split-K partials (workspace mode)].
+struct WorkspaceLayout {
+  size_t cnt_off, part_off, part_bytes, total;
+};
+
+WorkspaceLayout workspace_layout(const Variant& v, int num_tiles) {
+  WorkspaceLayout w;
+  w.cnt_off = 256;
+  w.part_off = w.cnt_off + (static_cast<size_t>(num_tiles) * 4 + 255) / 256 * 256;
+  w.part_bytes = v.mode == bsg::SPLIT_WORKSPACE ? static_cast<size_t>(v.splits) * num_tiles * 128 * v.bn * 4 : 0;
+  w.total = w.part_off + w.part_bytes;
+  return w;
 }
 
 bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, uint64_t rows,
@@ -240,6 +269,76 @@ bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, u
   return BSG_OK;
 }
 
+// Kernel parameters of problem d under variant v (tensor maps encoded here), except the
+// workspace pointers.  Grid: persistent (<= #SMs) unless the splits form clusters, in which
+// case every unit is its own CTA.
+bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, int sms, int* grid) {
+  std::memset(g, 0, sizeof(*g));
+  const size_t rb = code_row_bytes(d->kind, d->K);
+  bsg_status s;
+  if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, 128, "A")) != BSG_OK ||
+      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.bn), "B")) != BSG_OK)
+    return s;
+  const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
+  const int blk = d->kind == BSG_MXFP8 ? 32 : 16;
+  g->sfa = static_cast<const uint8_t*>(d->SFA);
+  g->sfb = static_cast<const uint8_t*>(d->SFB);
+  g->bias = d->bias;
+  g->d = d->D;
+  g->alpha_dev = d->alpha_dev;
+  g->wait_limit_ns = kDefaultWaitLimitNs;
+  g->alpha = d->alpha;
+  g->M = d->M;
+  g->N = d->N;
+  g->K = d->K;
+  g->flags = d->flags;
+  g->sfa_atoms_per_band = (d->K / blk + 3) / 4;
+  g->sfb_atoms_per_band = g->sfa_atoms_per_band;
+  g->sfb_bands = (d->N + 127) / 128;
+  g->num_m_tiles = (d->M + 127) / 128;
+  g->num_n_tiles = (d->N + v.bn - 1) / v.bn;
+  g->num_k_tiles = (d->K + k_tile - 1) / k_tile;
+  g->num_tiles = g->num_m_tiles * g->num_n_tiles;
+  g->splits = v.splits;
+  g->split_mode = v.mode;
+  g->k_tiles_per_split = v.kps;
+  g->num_units = g->num_tiles * v.splits;
+  g->group_m = 16;
+  g->debug_skip_first_load = 0;
+  *grid = v.mode == bsg::SPLIT_CLUSTER ? g->num_units : std::min(g->num_units, sms);
+  return BSG_OK;
+}
+
+bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, int threads, int smem,
+                       int cluster, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  if (env_int("BSG_PDL", 1)) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  void* args[] = {const_cast<bsg::GemmParams*>(&params)};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
+  return BSG_OK;
+}
+
 bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   if (out == nullptr) return fail(BSG_ERR_INVALID_ARG, "plan output pointer is null");
   *out = nullptr;
@@ -252,12 +351,11 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
     return fail(BSG_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled from the driver");
   if ((s = validate_ranges(d)) != BSG_OK) return s;
 
-  int bn, splits, kps;
-  choose_variant(d, di.sms, &bn, &splits, &kps);
+  const Variant v = choose_variant(d, di.sms);
   bsg::GemmKernelInfo info{};
   const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
-  const bool found = d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(bn, out_t, &info)
-                                          : bsg::gemm_kernel_info_nv(bn, out_t, &info);
+  const bool found = d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, &info)
+                                          : bsg::gemm_kernel_info_nv(v.bn, out_t, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
 
@@ -268,52 +366,20 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   p->info = info;
   p->device = dev;
   p->workspace = nullptr;
+  p->cluster = v.cluster;
   bsg::GemmParams& g = p->params;
-  std::memset(&g, 0, sizeof(g));
-  const size_t rb = code_row_bytes(d->kind, d->K);
-  if ((s = encode_operand(&g.tmap_a, d->A, rb, d->M, 128, "A")) != BSG_OK ||
-      (s = encode_operand(&g.tmap_b, d->B, rb, d->N, static_cast<uint32_t>(bn), "B")) != BSG_OK) {
+  if ((s = fill_params(&g, d, v, di.sms, &p->grid)) != BSG_OK) {
     delete p;
     return s;
   }
-  const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
-  const int blk = d->kind == BSG_MXFP8 ? 32 : 16;
-  g.sfa = static_cast<const uint8_t*>(d->SFA);
-  g.sfb = static_cast<const uint8_t*>(d->SFB);
-  g.bias = d->bias;
-  g.d = d->D;
-  g.alpha_dev = d->alpha_dev;
-  g.wait_limit_ns = kDefaultWaitLimitNs;
-  g.alpha = d->alpha;
-  g.M = d->M;
-  g.N = d->N;
-  g.K = d->K;
-  g.flags = d->flags;
-  g.sfa_atoms_per_band = (d->K / blk + 3) / 4;
-  g.sfb_atoms_per_band = g.sfa_atoms_per_band;
-  g.sfb_bands = (d->N + 127) / 128;
-  g.num_m_tiles = (d->M + 127) / 128;
-  g.num_n_tiles = (d->N + bn - 1) / bn;
-  g.num_k_tiles = (d->K + k_tile - 1) / k_tile;
-  g.num_tiles = g.num_m_tiles * g.num_n_tiles;
-  g.splits = splits;
-  g.k_tiles_per_split = kps;
-  g.num_units = g.num_tiles * splits;
-  g.group_m = 16;
-  g.debug_skip_first_load = 0;
-
-  // workspace: [status word | per-tile counters | split-K partial tiles]
-  const size_t cnt_off = 256;
-  const size_t part_off = cnt_off + (static_cast<size_t>(g.num_tiles) * 4 + 255) / 256 * 256;
-  const size_t part_bytes = splits > 1 ? static_cast<size_t>(splits) * g.num_tiles * 128 * bn * 4 : 0;
-  const size_t ws_bytes = part_off + part_bytes;
-  cudaError_t e = cudaMalloc(&p->workspace, ws_bytes);
+  const WorkspaceLayout w = workspace_layout(v, g.num_tiles);
+  cudaError_t e = cudaMalloc(&p->workspace, w.total);
   if (e != cudaSuccess) {
     delete p;
     cudaGetLastError();
-    return fail(BSG_ERR_NOMEM, "cudaMalloc of a %zu-byte workspace failed", ws_bytes);
+    return fail(BSG_ERR_NOMEM, "cudaMalloc of a %zu-byte workspace failed", w.total);
   }
-  e = cudaMemset(p->workspace, 0, part_off);
+  e = cudaMemset(p->workspace, 0, w.part_off);
   if (e != cudaSuccess) {
     cudaFree(p->workspace);
     delete p;
@@ -321,11 +387,11 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   }
   char* ws = static_cast<char*>(p->workspace);
   g.status = reinterpret_cast<unsigned*>(ws);
-  g.counters = reinterpret_cast<unsigned*>(ws + cnt_off);
-  g.partial = splits > 1 ? reinterpret_cast<float*>(ws + part_off) : nullptr;
-  p->grid = std::min(g.num_units, di.sms);
-  std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
-                bn, splits, info.stages, p->grid);
+  g.counters = reinterpret_cast<unsigned*>(ws + w.cnt_off);
+  g.partial = w.part_bytes ? reinterpret_cast<float*>(ws + w.part_off) : nullptr;
+  static const char* kModeName[] = {"", "w", "c"};
+  std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
+                v.bn, v.splits, kModeName[v.mode], info.stages, p->grid);
   if (env_int("BSG_LOG", 0))
     std::fprintf(stderr, "[bsgemm] plan M=%d N=%d K=%d -> %s\n", d->M, d->N, d->K, p->variant);
   *out = p;
@@ -335,16 +401,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
 bool plan_ok(bsg_plan_t p) { return p != nullptr && p->magic == kPlanMagic; }
 
 bsg_status plan_launch(bsg_plan_t p, const bsg::GemmParams& params, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(p->grid), 1, 1);
-  cfg.blockDim = dim3(static_cast<unsigned>(p->info.threads), 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(p->info.smem_bytes);
-  cfg.stream = stream;
-  void* args[] = {const_cast<bsg::GemmParams*>(&params)};
-  const cudaError_t e = cudaLaunchKernelExC(&cfg, p->info.fn, args);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
-  return BSG_OK;
+  return launch_gemm(p->info.fn, params, p->grid, p->info.threads, p->info.smem_bytes, p->cluster, stream);
 }
 
 }  // namespace
@@ -601,76 +658,34 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
     return fail(BSG_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled from the driver");
   if ((s = validate_ranges(d)) != BSG_OK) return s;
 
-  int bn, splits, kps;
-  choose_variant(d, di.sms, &bn, &splits, &kps);
+  const Variant v = choose_variant(d, di.sms);
   bsg::GemmKernelInfo info{};
   const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
-  const bool found = d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(bn, out_t, &info)
-                                          : bsg::gemm_kernel_info_nv(bn, out_t, &info);
+  const bool found = d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, &info)
+                                          : bsg::gemm_kernel_info_nv(v.bn, out_t, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
-
-  const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
-  const int blk = d->kind == BSG_MXFP8 ? 32 : 16;
-  const int num_m = (d->M + 127) / 128, num_n = (d->N + bn - 1) / bn;
-  const int num_tiles = num_m * num_n;
-  const size_t cnt_off = 256;
-  const size_t part_off = cnt_off + (static_cast<size_t>(num_tiles) * 4 + 255) / 256 * 256;
-  const size_t part_bytes = splits > 1 ? static_cast<size_t>(splits) * num_tiles * 128 * bn * 4 : 0;
-  if (part_off + part_bytes > kNoAllocScratchBytes)
+  const int num_tiles = ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn);
+  const WorkspaceLayout w = workspace_layout(v, num_tiles);
+  if (w.total > kNoAllocScratchBytes)
     return fail(BSG_ERR_SHAPE,
                 "this problem needs %zu bytes of scratch (split-K %d over %d tiles); the allocation-free "
                 "entry point has %zu; use a plan",
-                part_off + part_bytes, splits, num_tiles, kNoAllocScratchBytes);
+                w.total, v.splits, num_tiles, kNoAllocScratchBytes);
   unsigned char* scratch = nullptr;
   if ((s = noalloc_scratch(dev, &scratch)) != BSG_OK) return s;
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
 
   bsg::GemmParams g;
-  std::memset(&g, 0, sizeof(g));
-  const size_t rb = code_row_bytes(d->kind, d->K);
-  if ((s = encode_operand(&g.tmap_a, d->A, rb, d->M, 128, "A")) != BSG_OK ||
-      (s = encode_operand(&g.tmap_b, d->B, rb, d->N, static_cast<uint32_t>(bn), "B")) != BSG_OK)
-    return s;
-  g.sfa = static_cast<const uint8_t*>(d->SFA);
-  g.sfb = static_cast<const uint8_t*>(d->SFB);
-  g.bias = d->bias;
-  g.d = d->D;
-  g.alpha_dev = d->alpha_dev;
-  g.wait_limit_ns = kDefaultWaitLimitNs;
-  g.alpha = d->alpha;
-  g.M = d->M;
-  g.N = d->N;
-  g.K = d->K;
-  g.flags = d->flags;
-  g.sfa_atoms_per_band = (d->K / blk + 3) / 4;
-  g.sfb_atoms_per_band = g.sfa_atoms_per_band;
-  g.sfb_bands = (d->N + 127) / 128;
-  g.num_m_tiles = num_m;
-  g.num_n_tiles = num_n;
-  g.num_k_tiles = (d->K + k_tile - 1) / k_tile;
-  g.num_tiles = num_tiles;
-  g.splits = splits;
-  g.k_tiles_per_split = kps;
-  g.num_units = num_tiles * splits;
-  g.group_m = 16;
-  g.debug_skip_first_load = 0;
+  int grid = 0;
+  if ((s = fill_params(&g, d, v, di.sms, &grid)) != BSG_OK) return s;
   g.status = reinterpret_cast<unsigned*>(scratch);
-  g.counters = reinterpret_cast<unsigned*>(scratch + cnt_off);
-  g.partial = splits > 1 ? reinterpret_cast<float*>(scratch + part_off) : nullptr;
+  g.counters = reinterpret_cast<unsigned*>(scratch + w.cnt_off);
+  g.partial = w.part_bytes ? reinterpret_cast<float*>(scratch + w.part_off) : nullptr;
 
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the status word and the split-K counters must start at zero; the partial tiles are
   // written whole by their split before they are read
-  cudaError_t e = cudaMemsetAsync(scratch, 0, part_off, st);
+  const cudaError_t e = cudaMemsetAsync(scratch, 0, w.part_off, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(allocation-free scratch)");
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(std::min(g.num_units, di.sms)), 1, 1);
-  cfg.blockDim = dim3(static_cast<unsigned>(info.threads), 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(info.smem_bytes);
-  cfg.stream = st;
-  void* args[] = {&g};
-  e = cudaLaunchKernelExC(&cfg, info.fn, args);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
-  return BSG_OK;
+  return launch_gemm(info.fn, g, grid, info.threads, info.smem_bytes, v.cluster, st);
 }

@@ -62,11 +62,31 @@ def test_ragged_shapes(kind, M, N, K):
 
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
-@pytest.mark.parametrize("bn,splits", [(128, 1), (256, 1), (128, 3), (256, 2), (128, 7)])
-def test_forced_variants(kind, bn, splits, monkeypatch):
-    v = run_case(kind, 384, 768, 1792, env={"BSG_FORCE_BN": bn, "BSG_FORCE_SPLITS": splits},
-                 monkeypatch=monkeypatch, bias=True, silu=True)
-    assert "_bn%d_s%d_" % (bn, splits) in v
+@pytest.mark.parametrize("bn,splits,mode", [(128, 1, ""), (256, 1, ""), (128, 3, "w"), (256, 2, "c"), (128, 7, "w"),
+                                            (128, 4, "c"), (128, 8, "c"), (256, 4, "w")])
+def test_forced_variants(kind, bn, splits, mode, monkeypatch):
+    env = {"BSG_FORCE_BN": bn, "BSG_FORCE_SPLITS": splits}
+    if mode == "w":
+        env["BSG_SPLIT_WORKSPACE"] = 1
+    K = 1792
+    v = run_case(kind, 384, 768, K, env=env, monkeypatch=monkeypatch, bias=True, silu=True)
+    # a split factor that does not divide the k-tiles evenly is rounded so every split is busy
+    nkt = K // (128 if kind == "mxfp8" else 256)
+    kps = -(-nkt // splits)
+    s = -(-nkt // kps)
+    m = "" if s == 1 else ("w" if mode == "w" or s not in (2, 4, 8) else "c")
+    assert "_bn%d_s%d%s_" % (bn, s, m) in v
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_cluster_split_ragged_rows(kind, monkeypatch):
+    # ragged M inside a cluster-reduced tile: each CTA's row slab is partly beyond M
+    v = run_case(kind, 77, 272, 2048, env={"BSG_FORCE_SPLITS": 4}, monkeypatch=monkeypatch, bias=True, silu=True)
+    assert "_s4c_" in v
+
+
+def test_pdl_off_matches(monkeypatch):
+    run_case("nvfp4", 256, 512, 1024, env={"BSG_PDL": 0}, monkeypatch=monkeypatch, bias=True, silu=True)
 
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])

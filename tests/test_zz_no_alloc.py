@@ -26,12 +26,15 @@ def _call_noalloc(dp, prob):
     return dp.result()
 
 
-@pytest.mark.parametrize("kind,M,N,K,epi", [
-    ("nvfp4", 128, 512, 4096, True),     # split-K: partial tiles and counters in the static array
-    ("mxfp8", 2048, 2560, 512, False),   # no split: status word and counters only
-    ("nvfp4", 300, 400, 608, True),      # ragged tiles
+@pytest.mark.parametrize("kind,M,N,K,epi,workspace", [
+    ("nvfp4", 128, 512, 4096, True, True),    # split-K through scratch: partial tiles and counters
+    ("nvfp4", 128, 512, 4096, True, False),   # split-K through a cluster: status word only
+    ("mxfp8", 2048, 2560, 512, False, False), # no split
+    ("nvfp4", 300, 400, 608, True, False),    # ragged tiles
 ])
-def test_noalloc_matches_plan_twice(kind, M, N, K, epi):
+def test_noalloc_matches_plan_twice(kind, M, N, K, epi, workspace, monkeypatch):
+    if workspace:
+        monkeypatch.setenv("BSG_SPLIT_WORKSPACE", "1")
     prob = P.make_problem(kind, M, N, K)
     dp = P.DeviceProblem(prob, out="bf16", bias=epi, silu=epi)
     with dp.plan() as plan:
@@ -50,6 +53,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch(monkeypatch):
     # 64 splits x 4 tiles x 64 KiB of partials = 16 MiB, beyond the 16 MiB array once the
     # counters are added
     monkeypatch.setenv("BSG_FORCE_SPLITS", "64")
+    monkeypatch.setenv("BSG_SPLIT_WORKSPACE", "1")
     prob = P.make_problem("nvfp4", 128, 512, 16384)
     dp = P.DeviceProblem(prob)
     with pytest.raises(bsg.BsgError) as e:
