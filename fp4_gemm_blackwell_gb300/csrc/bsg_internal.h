@@ -23,6 +23,7 @@ enum : unsigned {
   ST_TIMEOUT_MMA = 1u << 1,
   ST_TIMEOUT_EPILOGUE = 1u << 2,
   ST_TIMEOUT_DRAIN = 1u << 3,
+  ST_TIMEOUT_SCALES = 1u << 4,
 };
 
 // Kernel parameters, passed by value as a __grid_constant__ (the tensor maps must live in

@@ -52,11 +52,18 @@ struct GemmCfg {
   static constexpr int SFB_COLS = 4 * SF_ATOMS * NB;
   static constexpr int SF_SLOT_COLS = SFA_COLS + SFB_COLS;
   static constexpr int SF_COL0 = NACC * BN;
-  static constexpr int TMEM_USED = SF_COL0 + 2 * SF_SLOT_COLS;
+  // NVFP4 needs four scale atoms per band per k-tile; copying them with tcgen05.cp would take
+  // the tensor pipe longer than the MMAs, so four scale warps write them into a TMEM slot per
+  // ring stage with tcgen05.st.  MXFP8 copies its one atom per band with tcgen05.cp into two
+  // alternating slots.
+  static constexpr bool SF_ST = KIND == KIND_NV;
+  static constexpr int SF_SLOTS = SF_ST ? STAGES : 2;
+  static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half the columns
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int EPI_WARP0 = SF_ST ? 6 : 2;     // first epilogue warp
+  static constexpr int THREADS = 32 * EPI_WARP0 + EPI_THREADS;
   // Instruction descriptor (block-scaled kinds): [4,6) B scale id, [7,10) A type,
   // [10,13) B type, [15]/[16] A/B major (0 = K), [17,23) N >> 3, [23] scale type
   // (1 = UE8M0, 0 = UE4M3), [24,29) M >> 4, [29,31) A scale id.
@@ -189,51 +196,75 @@ __device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0
   }
 }
 
+// alpha (+ preloaded bias) and SiLU on 4 accumulator values, packed two per word.
+template <int OUT>
+__device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, const float4& a, uint2 braw, float alpha) {
+  const uint16_t* b = reinterpret_cast<const uint16_t*>(&braw);
+  float y[4] = {a.x, a.y, a.z, a.w};
+  const bool has_bias = (p.flags & F_BIAS) != 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] = has_bias ? __fmaf_rn(alpha, y[i], out_to_float<OUT>(b[i])) : __fmul_rn(alpha, y[i]);
+  if (p.flags & F_SILU) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = y[i] * __fdividef(1.0f, 1.0f + __expf(-y[i]));  // see epi_pack
+  }
+  return make_uint2(pack2<OUT>(y[0], y[1]), pack2<OUT>(y[2], y[3]));
+}
+
 // Split-K through a cluster: the splits of one tile are the CTAs of one cluster, each holding
 // its FP32 partial tile in shared memory as [128 rows][BN + 4] floats.  CTA `split` sums rows
 // [split * 128/S, (split + 1) * 128/S) over the S peers in split order (deterministic), applies
-// the epilogue and stores whole rows (each lane 4 consecutive columns per 128).
-template <int OUT, int BN>
-__device__ __forceinline__ void cluster_reduce(const GemmParams& p, uint32_t part_saddr, const UnitCoord& c,
-                                               float alpha, int ew, int lane) {
-  const int S = p.splits;
-  const int R = 128 / S;
-  for (int r = ew; r < R; r += 8) {
-    const int row = c.split * R + r;
-    const int m = c.m_blk * 128 + row;
-    if (m >= p.M) break;
-    uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+// the epilogue and stores whole rows (each lane 4 consecutive columns per 128).  The 8 epilogue
+// warps take 16/S rows each; all peer loads of a warp's rows are issued before any sum.
+template <int OUT, int BN, int S>
+__device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, uint32_t part_saddr, const UnitCoord& c,
+                                                 float alpha, int ew, int lane) {
+  constexpr int R = 128 / S;     // rows per CTA
+  constexpr int RW = R / 8;      // rows per warp
+#pragma unroll 1
+  for (int h = 0; h < BN / 128; ++h) {
+    const int col = h * 128 + 4 * lane;
+    const int n = c.n_blk * BN + col;
+    uint2 braw = make_uint2(0u, 0u);
+    if ((p.flags & F_BIAS) && n < p.N)
+      braw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
+    float4 t[RW][S];
 #pragma unroll
-    for (int h = 0; h < BN / 128; ++h) {
-      const int col = h * 128 + 4 * lane;
+    for (int r = 0; r < RW; ++r) {
+      const int row = c.split * R + ew + 8 * r;
       const uint32_t off = part_saddr + static_cast<uint32_t>((row * (BN + 4) + col) * 4);
-      float4 t[8];  // S <= 8: issue every peer's load, then sum in split order
 #pragma unroll
-      for (int sp = 0; sp < 8; ++sp)
-        if (sp < S) t[sp] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(sp)));
-      float4 acc = t[0];
+      for (int sp = 0; sp < S; ++sp) t[r][sp] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(sp)));
+    }
 #pragma unroll
-      for (int sp = 1; sp < 8; ++sp) {
-        if (sp < S) {
-          acc.x += t[sp].x;
-          acc.y += t[sp].y;
-          acc.z += t[sp].z;
-          acc.w += t[sp].w;
-        }
+    for (int r = 0; r < RW; ++r) {
+      const int row = c.split * R + ew + 8 * r;
+      const int m = c.m_blk * 128 + row;
+      float4 acc = t[r][0];
+#pragma unroll
+      for (int sp = 1; sp < S; ++sp) {
+        acc.x += t[r][sp].x;
+        acc.y += t[r][sp].y;
+        acc.z += t[r][sp].z;
+        acc.w += t[r][sp].w;
       }
-      const int n = c.n_blk * BN + col;
-      if (n < p.N) {  // N % 16 == 0: groups of 4 are whole
-        const float v[4] = {acc.x, acc.y, acc.z, acc.w};
-        uint2 o;
-        epi_pack<OUT, 4>(p, n, v, alpha, reinterpret_cast<uint32_t*>(&o));
-        *reinterpret_cast<uint2*>(drow + n) = o;
-      }
+      if (m < p.M && n < p.N)  // N % 16 == 0: groups of 4 are whole
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N + n) =
+            epi4_with_bias<OUT>(p, acc, braw, alpha);
     }
   }
 }
 
+template <int OUT, int BN>
+__device__ __forceinline__ void cluster_reduce(const GemmParams& p, uint32_t part_saddr, const UnitCoord& c,
+                                               float alpha, int ew, int lane) {
+  if (p.splits == 2) cluster_reduce_s<OUT, BN, 2>(p, part_saddr, c, alpha, ew, lane);
+  else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4>(p, part_saddr, c, alpha, ew, lane);
+  else cluster_reduce_s<OUT, BN, 8>(p, part_saddr, c, alpha, ew, lane);
+}
+
 template <int KIND, int BN, int OUT>
-__global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<KIND, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -251,6 +282,7 @@ __global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant_
   auto bar_tfull = [&](int a) { return smem_u32(bars + 16 + a); };
   auto bar_tempty = [&](int a) { return smem_u32(bars + 18 + a); };
   const uint32_t bar_drain = smem_u32(bars + 20);
+  auto bar_sfready = [&](int s) { return smem_u32(bars + 24 + s); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 22);
   volatile int* last_flag = reinterpret_cast<volatile int*>(bars + 23);
@@ -272,6 +304,8 @@ __global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant_
       mbar_init(bar_tempty(a), C::EPI_THREADS);
     }
     mbar_init(bar_drain, 1);
+    if (C::SF_ST)
+      for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_sfready(s), 128);
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -364,10 +398,14 @@ __global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant_
             ok = false;
             break;
           }
+          if (C::SF_ST && !wait_bounded(bar_sfready(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const int k_rem = p.K - kt * C::K_TILE;
           const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
-          const uint32_t sfa_t = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
+          const uint32_t sfa_t = tmem_base + C::SF_COL0 + (C::SF_ST ? stage : slot) * C::SF_SLOT_COLS;
           const uint32_t sfb_t = sfa_t + C::SFA_COLS;
           const uint32_t sa = stage_a(stage), sb = stage_b(stage);
           const uint32_t ssfa = stage_sfa(stage), ssfb = stage_sfb(stage);
@@ -383,13 +421,8 @@ __global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant_
                           idesc, sfa_t, sfb_t, (kt > c.kt0 || j > 0) ? 1u : 0u);
             }
           } else {
-            for (int j = 0; j < steps; ++j) {
-              tc_cp_sf_atom(sfa_t + 4 * j, sdesc_sf_atom(ssfa + 512 * j));
-#pragma unroll
-              for (int rb = 0; rb < C::NB; ++rb)
-                tc_cp_sf_atom(sfb_t + 4 * C::NB * j + 4 * rb,
-                              sdesc_sf_atom(ssfb + rb * C::SF_ATOMS * 512 + 512 * j));
-            }
+            (void)ssfa;
+            (void)ssfb;  // the scale warps have put this stage's scales in its TMEM slot
             for (int j = 0; j < steps; ++j) {
               tc_mma_nvf4(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
                           C::IDESC, sfa_t + 4 * j, sfb_t + 4 * C::NB * j,
@@ -424,12 +457,73 @@ __global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant_
         }
       }
     }
+  } else if (C::SF_ST && warp < C::EPI_WARP0) {
+    // ------------------------------------------------------------ scale warps (NVFP4, warps 2..5)
+    // Per stage, each warp writes its TMEM lane quarter of the stage's scale slot: for MMA j,
+    // column 4j + k of lane i holds the four UE4M3 scales of A row 32k + i (row i of atom j),
+    // and column 4*NB*j + 4b + k those of B row 128b + 32k + i -- the layout a 32x128b.warpx4
+    // copy of the same atoms produces.
+    const int q = warp & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      const UnitCoord c = decode_unit(p, u);
+      for (int kt = c.kt0; kt < c.kt1; ++kt) {
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
+        if (!ok) break;
+        const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
+        uint32_t a[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 v = lds_u4(stage_sfa(stage) + 512 * j + 16 * lane);
+          a[4 * j] = v.x;
+          a[4 * j + 1] = v.y;
+          a[4 * j + 2] = v.z;
+          a[4 * j + 3] = v.w;
+        }
+        tmem_st_32x32b_x16(slot, a);
+        if constexpr (C::NB == 2) {
+          uint32_t b[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int rb = 0; rb < 2; ++rb) {
+              const uint4 v = lds_u4(stage_sfb(stage) + rb * C::SF_ATOMS * 512 + 512 * j + 16 * lane);
+              b[(2 * j + rb) * 4] = v.x;
+              b[(2 * j + rb) * 4 + 1] = v.y;
+              b[(2 * j + rb) * 4 + 2] = v.z;
+              b[(2 * j + rb) * 4 + 3] = v.w;
+            }
+          }
+          tmem_st_32x32b_x32(slot + C::SFA_COLS, b);
+        } else {
+          uint32_t b[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = lds_u4(stage_sfb(stage) + 512 * j + 16 * lane);
+            b[4 * j] = v.x;
+            b[4 * j + 1] = v.y;
+            b[4 * j + 2] = v.z;
+            b[4 * j + 3] = v.w;
+          }
+          tmem_st_32x32b_x16(slot + C::SFA_COLS, b);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_sfready(stage));
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..9)
+    // ------------------------------------------------------------ epilogue (8 warps)
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;       // accumulator row = TMEM lane
     constexpr int HC = BN / 2;           // columns per thread
-    const int col0 = ((warp - 2) >> 2) * HC;
+    const int col0 = ((warp - C::EPI_WARP0) >> 2) * HC;
     const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -509,7 +603,7 @@ __global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant_
         mbar_arrive(bar_tempty(acc));
         __threadfence();
         named_bar_sync(1, C::EPI_THREADS);
-        if (threadIdx.x == 64) {
+        if (threadIdx.x == C::EPI_WARP0 * 32) {
           const unsigned old = atomicAdd(p.counters + c.tile, 1u);
           const int last = (old == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
           if (last) p.counters[c.tile] = 0u;  // ready for the next launch
@@ -556,10 +650,10 @@ __global__ void __launch_bounds__(320, 1) bsg_gemm_kernel(const __grid_constant_
     // CTA leaves while a peer may still read its shared memory.
     __syncwarp();
     cluster_sync();  // all partial tiles of the cluster are in shared memory
-    if (warp >= 2) {
+    if (warp >= C::EPI_WARP0) {
       const UnitCoord c = decode_unit(p, blockIdx.x);
       const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
-      cluster_reduce<OUT, BN>(p, smem0, c, alpha, warp - 2, lane);
+      cluster_reduce<OUT, BN>(p, smem0, c, alpha, warp - C::EPI_WARP0, lane);
     }
     __syncwarp();
     cluster_sync();  // the peers are done reading this CTA's shared memory

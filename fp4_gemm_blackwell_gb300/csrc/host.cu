@@ -446,9 +446,10 @@ BSG_API bsg_status bsg_plan_check_status(bsg_plan_t plan) {
   cudaSetDevice(cur);
   if (e != cudaSuccess) return cuda_fail(e, "reading the plan status word");
   if (word != 0)
-    return fail(BSG_ERR_DEVICE_TIMEOUT, "a launch of this plan gave up a wait (status 0x%x:%s%s%s%s)", word,
+    return fail(BSG_ERR_DEVICE_TIMEOUT, "a launch of this plan gave up a wait (status 0x%x:%s%s%s%s%s)", word,
                 (word & bsg::ST_TIMEOUT_PRODUCER) ? " producer" : "", (word & bsg::ST_TIMEOUT_MMA) ? " mma" : "",
-                (word & bsg::ST_TIMEOUT_EPILOGUE) ? " epilogue" : "", (word & bsg::ST_TIMEOUT_DRAIN) ? " drain" : "");
+                (word & bsg::ST_TIMEOUT_EPILOGUE) ? " epilogue" : "", (word & bsg::ST_TIMEOUT_DRAIN) ? " drain" : "",
+                (word & bsg::ST_TIMEOUT_SCALES) ? " scales" : "");
   return BSG_OK;
 }
 
