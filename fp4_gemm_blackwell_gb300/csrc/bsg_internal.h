@@ -31,6 +31,8 @@ enum : unsigned {
 struct GemmParams {
   CUtensorMap tmap_a;  // A codes: bytes, dims {K bytes, M}, box {128, 128}, 128-byte swizzle
   CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N}, box {128, BN}, 128-byte swizzle
+  CUtensorMap tmap_sfa;  // pair kernel: scale buffers as 128-byte rows (4 per atom), no swizzle
+  CUtensorMap tmap_sfb;
   const uint8_t* sfa;  // swizzled 128x4 scale atoms of A
   const uint8_t* sfb;
   const void* bias;    // N values of the output type (flags & F_BIAS)
@@ -46,6 +48,7 @@ struct GemmParams {
   int sfa_atoms_per_band;  // padded scale columns / 4 of A
   int sfb_atoms_per_band;
   int sfb_bands;           // padded rows / 128 of B
+  int sfa_bands;           // padded rows / 128 of A
   int num_m_tiles, num_n_tiles, num_k_tiles;
   int num_tiles;
   int splits;              // split-K factor (every split owns >= 1 k-tile)
@@ -67,6 +70,9 @@ struct GemmKernelInfo {
 // Look up a kernel instantiation: tile width bn (128 or 256), out (OUT_*).
 bool gemm_kernel_info_mx(int bn, int out, GemmKernelInfo* info);
 bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info);
+// CTA-pair kernels (256 x 256 pair tiles, launched in clusters of 2).
+bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info);
+bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info);
 
 // Quantisers (stream-ordered).  See bsg_quantize in include/bsgemm.h.
 cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,

@@ -113,6 +113,23 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
   }
 }
 
+// The same for barriers that threads of another CTA of the cluster arrive on (acquire at
+// cluster scope).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                     const GemmParams& p, unsigned who) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+      *abort_flag = 1;
+      atomicOr(p.status, who);
+      return false;
+    }
+  }
+}
+
 // Named-barrier AND over `nthreads` threads: every participant gets the same answer.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
   uint32_t r;
@@ -211,16 +228,18 @@ __device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, const float
   return make_uint2(pack2<OUT>(y[0], y[1]), pack2<OUT>(y[2], y[3]));
 }
 
-// Split-K through a cluster: the splits of one tile are the CTAs of one cluster, each holding
-// its FP32 partial tile in shared memory as [128 rows][BN + 4] floats.  CTA `split` sums rows
-// [split * 128/S, (split + 1) * 128/S) over the S peers in split order (deterministic), applies
-// the epilogue and stores whole rows (each lane 4 consecutive columns per 128).  The 8 epilogue
-// warps take 16/S rows each; all peer loads of a warp's rows are issued before any sum.
+// Split-K through a cluster: the splits of one tile are the CTAs of one cluster.  Each CTA
+// holds its FP32 partial tile in shared memory as [128 rows][BN + 4] floats, owns the row slab
+// [split * 128/S, (split + 1) * 128/S), and has pushed every other slab to the CTA that owns
+// it (bulk copies into that CTA's receive slots, [S - 1][128/S][BN + 4] floats after the
+// partial tile).  Here the owner sums its slab over the S splits in split order
+// (deterministic), from local shared memory only, applies the epilogue and stores whole rows
+// (each lane 4 consecutive columns per 128).  The 8 epilogue warps take 16/S rows each.
 template <int OUT, int BN, int S>
-__device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, uint32_t part_saddr, const UnitCoord& c,
-                                                 float alpha, int ew, int lane) {
-  constexpr int R = 128 / S;     // rows per CTA
-  constexpr int RW = R / 8;      // rows per warp
+__device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const float* part, const float* recv,
+                                                 const UnitCoord& c, float alpha, int ew, int lane) {
+  constexpr int R = 128 / S;
+  constexpr int RW = R / 8;
 #pragma unroll 1
   for (int h = 0; h < BN / 128; ++h) {
     const int col = h * 128 + 4 * lane;
@@ -228,26 +247,26 @@ __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, uint32_t p
     uint2 braw = make_uint2(0u, 0u);
     if ((p.flags & F_BIAS) && n < p.N)
       braw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
-    float4 t[RW][S];
 #pragma unroll
     for (int r = 0; r < RW; ++r) {
-      const int row = c.split * R + ew + 8 * r;
-      const uint32_t off = part_saddr + static_cast<uint32_t>((row * (BN + 4) + col) * 4);
+      const int rl = ew + 8 * r;  // row within the slab
+      const int row = c.split * R + rl;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int sp = 0; sp < S; ++sp) t[r][sp] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(sp)));
-    }
-#pragma unroll
-    for (int r = 0; r < RW; ++r) {
-      const int row = c.split * R + ew + 8 * r;
-      const int m = c.m_blk * 128 + row;
-      float4 acc = t[r][0];
-#pragma unroll
-      for (int sp = 1; sp < S; ++sp) {
-        acc.x += t[r][sp].x;
-        acc.y += t[r][sp].y;
-        acc.z += t[r][sp].z;
-        acc.w += t[r][sp].w;
+      for (int sp = 0; sp < S; ++sp) {
+        const float* src = sp == c.split ? part + row * (BN + 4)
+                                         : recv + ((sp < c.split ? sp : sp - 1) * R + rl) * (BN + 4);
+        const float4 t = *reinterpret_cast<const float4*>(src + col);
+        if (sp == 0) {
+          acc = t;
+        } else {
+          acc.x += t.x;
+          acc.y += t.y;
+          acc.z += t.z;
+          acc.w += t.w;
+        }
       }
+      const int m = c.m_blk * 128 + row;
       if (m < p.M && n < p.N)  // N % 16 == 0: groups of 4 are whole
         *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N + n) =
             epi4_with_bias<OUT>(p, acc, braw, alpha);
@@ -256,11 +275,11 @@ __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, uint32_t p
 }
 
 template <int OUT, int BN>
-__device__ __forceinline__ void cluster_reduce(const GemmParams& p, uint32_t part_saddr, const UnitCoord& c,
-                                               float alpha, int ew, int lane) {
-  if (p.splits == 2) cluster_reduce_s<OUT, BN, 2>(p, part_saddr, c, alpha, ew, lane);
-  else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4>(p, part_saddr, c, alpha, ew, lane);
-  else cluster_reduce_s<OUT, BN, 8>(p, part_saddr, c, alpha, ew, lane);
+__device__ __forceinline__ void cluster_reduce(const GemmParams& p, const float* part, const float* recv,
+                                               const UnitCoord& c, float alpha, int ew, int lane) {
+  if (p.splits == 2) cluster_reduce_s<OUT, BN, 2>(p, part, recv, c, alpha, ew, lane);
+  else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4>(p, part, recv, c, alpha, ew, lane);
+  else cluster_reduce_s<OUT, BN, 8>(p, part, recv, c, alpha, ew, lane);
 }
 
 template <int KIND, int BN, int OUT>
@@ -283,6 +302,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
   auto bar_tempty = [&](int a) { return smem_u32(bars + 18 + a); };
   const uint32_t bar_drain = smem_u32(bars + 20);
   auto bar_sfready = [&](int s) { return smem_u32(bars + 24 + s); };
+  const uint32_t bar_recv = smem_u32(bars + 32);  // split-K cluster: peers' slabs have landed
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 22);
   volatile int* last_flag = reinterpret_cast<volatile int*>(bars + 23);
@@ -301,11 +321,12 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
-      mbar_init(bar_tempty(a), C::EPI_THREADS);
+      mbar_init(bar_tempty(a), C::EPI_WARPS);  // one arrival per epilogue warp
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_recv, 1);
     if (C::SF_ST)
-      for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_sfready(s), 128);
+      for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_sfready(s), 4);  // one arrival per scale warp
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -320,6 +341,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Split-K cluster: announce that this CTA's barriers are initialised; the thread that later
+  // pushes slabs to the peers waits for the matching announcements.
+  if (p.split_mode == SPLIT_CLUSTER) cluster_arrive_relaxed();
+  bool cluster_waited = false;  // this thread has completed the start-up cluster arrival
   const uint32_t tmem_base = *tmem_slot;
   // Everything above touched only this CTA's own resources; from here on global memory is
   // read and written, so wait for the preceding grid in the stream (programmatic dependent
@@ -511,7 +536,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar_sfready(stage));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfready(stage));
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -555,7 +581,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
           }
         }
         tc_fence_before();
-        mbar_arrive(bar_tempty(acc));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty(acc));
         if (m < p.M) {
           uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
 #pragma unroll
@@ -581,7 +608,29 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
                                  __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
         }
         tc_fence_before();
-        mbar_arrive(bar_tempty(acc));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty(acc));
+        fence_proxy_async_smem();  // the partial tile is read next by bulk copies
+        cluster_wait();            // every CTA of the cluster has initialised its receive barrier
+        cluster_waited = true;
+        named_bar_sync(1, C::EPI_THREADS);
+        const int S = p.splits, R = 128 / S;
+        const uint32_t slab = static_cast<uint32_t>(R * (BN + 4) * 4);
+        const uint32_t recv0 = smem0 + 128 * (BN + 4) * 4;
+        if (threadIdx.x == C::EPI_WARP0 * 32) {
+          mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(S - 1) * slab);
+          for (int r = 0; r < S; ++r) {
+            if (r == c.split) continue;
+            const int slot = c.split < r ? c.split : c.split - 1;  // this CTA's slot at CTA r
+            bulk_copy_s2c(mapa_shared(recv0 + slot * slab, static_cast<uint32_t>(r)), smem0 + r * slab, slab,
+                          mapa_shared(bar_recv, static_cast<uint32_t>(r)));
+          }
+        }
+        const bool got = named_bar_and(1, C::EPI_THREADS,
+                                       wait_bounded_cluster(bar_recv, 0, abort_flag, p, ST_TIMEOUT_EPILOGUE));
+        if (got)
+          cluster_reduce<OUT, BN>(p, part, reinterpret_cast<const float*>(smem + 128 * (BN + 4) * 4), c, alpha,
+                                  warp - C::EPI_WARP0, lane);
       } else {
         // FP32 partial tile -> workspace as float4 [chunk][8][128 rows] (coalesced per warp)
         float4* part = reinterpret_cast<float4*>(
@@ -600,7 +649,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
           }
         }
         tc_fence_before();
-        mbar_arrive(bar_tempty(acc));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty(acc));
         __threadfence();
         named_bar_sync(1, C::EPI_THREADS);
         if (threadIdx.x == C::EPI_WARP0 * 32) {
@@ -644,19 +694,14 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
     }
   }
 
-  // ------------------------------------------------------------ split-K through the cluster
+  // ------------------------------------------------------------ split-K cluster: lifetime
   if (p.split_mode == SPLIT_CLUSTER) {
-    // Every thread of every CTA takes part in both cluster barriers, aborted or not, so that no
-    // CTA leaves while a peer may still read its shared memory.
+    // Every thread completes the start-up arrival (the epilogue warps did before pushing), then
+    // one full cluster barrier: a CTA leaves only after every CTA has received all its slabs,
+    // i.e. after every copy that reads this CTA's shared memory has completed.
+    if (!cluster_waited) cluster_wait();
     __syncwarp();
-    cluster_sync();  // all partial tiles of the cluster are in shared memory
-    if (warp >= C::EPI_WARP0) {
-      const UnitCoord c = decode_unit(p, blockIdx.x);
-      const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
-      cluster_reduce<OUT, BN>(p, smem0, c, alpha, warp - C::EPI_WARP0, lane);
-    }
-    __syncwarp();
-    cluster_sync();  // the peers are done reading this CTA's shared memory
+    cluster_sync();
   }
 
   // ------------------------------------------------------------ teardown

@@ -1,5 +1,5 @@
 // MXFP8 (E4M3 elements, UE8M0 per-32 scales) instantiations of the block-scaled GEMM kernel.
-#include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 
 namespace bsg {
 
@@ -8,6 +8,12 @@ bool gemm_kernel_info_mx(int bn, int out, GemmKernelInfo* info) {
   if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 128, OUT_BF16>(info);
   if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_MX, 256, OUT_F16>(info);
   if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 256, OUT_BF16>(info);
+  return false;
+}
+
+bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info) {
+  if (out == OUT_F16) return fill_pair_kernel_info<KIND_MX, OUT_F16>(info);
+  if (out == OUT_BF16) return fill_pair_kernel_info<KIND_MX, OUT_BF16>(info);
   return false;
 }
 

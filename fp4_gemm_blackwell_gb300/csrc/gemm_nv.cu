@@ -1,5 +1,5 @@
 // NVFP4 (E2M1 elements, UE4M3 per-16 scales) instantiations of the block-scaled GEMM kernel.
-#include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 
 namespace bsg {
 
@@ -8,6 +8,12 @@ bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info) {
   if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 128, OUT_BF16>(info);
   if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_NV, 256, OUT_F16>(info);
   if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 256, OUT_BF16>(info);
+  return false;
+}
+
+bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info) {
+  if (out == OUT_F16) return fill_pair_kernel_info<KIND_NV, OUT_F16>(info);
+  if (out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, OUT_BF16>(info);
   return false;
 }
 

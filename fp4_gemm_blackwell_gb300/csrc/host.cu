@@ -206,6 +206,7 @@ int env_int(const char* name, int dflt) {
 // other factors (only reachable by forcing) go through the plan's global workspace.
 struct Variant {
   int bn, splits, kps, mode, cluster;
+  bool pair;  // CTA-pair kernel: 256 x 256 tiles over 2-CTA clusters
 };
 
 Variant choose_variant(const bsg_desc* d, int sms) {
@@ -231,12 +232,30 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   int k = (nkt + s - 1) / s;
   s = (nkt + k - 1) / k;
   Variant v;
+  // The CTA-pair kernel (256 x 256 tiles over 2-CTA clusters) is selected only on request
+  // (BSG_FORCE_PAIR=1) for now: measured on GB300 it is slower than the 1-SM kernel at 8192^3
+  // (load delivery per k-tile and, for NVFP4, 12 scale copies per k-tile), see the design doc.
+  v.pair = false;
+  const int fp = env_int("BSG_FORCE_PAIR", -1);
+  if (fp == 0 || fp == 1) v.pair = fp == 1;
+  if (v.pair) {
+    v.bn = 256;
+    v.splits = 1;
+    v.kps = nkt;
+    v.mode = bsg::SPLIT_NONE;
+    v.cluster = 2;
+    return v;
+  }
   v.bn = b;
   v.splits = s;
   v.kps = k;
-  const bool pow2 = s == 2 || s == 4 || s == 8;
+  // A cluster split keeps the partial tile and the peers' row slabs in the ring's shared
+  // memory: 128 x (bn + 4) floats plus (s - 1) slabs of 128/s rows, which for 256-wide tiles
+  // only fits with s = 2.
+  const bool cluster_ok = (s == 2 || s == 4 || s == 8) && (b == 128 || s == 2);
   v.mode = s == 1 ? bsg::SPLIT_NONE
-                  : (pow2 && env_int("BSG_SPLIT_WORKSPACE", 0) == 0 ? bsg::SPLIT_CLUSTER : bsg::SPLIT_WORKSPACE);
+                  : (cluster_ok && env_int("BSG_SPLIT_WORKSPACE", 0) == 0 ? bsg::SPLIT_CLUSTER
+                                                                           : bsg::SPLIT_WORKSPACE);
   v.cluster = v.mode == bsg::SPLIT_CLUSTER ? s : 1;
   return v;
 }
@@ -269,6 +288,21 @@ bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, u
   return BSG_OK;
 }
 
+// Scale buffer (swizzled 128x4 atoms, contiguous) as 128-byte rows, 4 rows per atom; boxes of
+// `atoms` atoms.  Used by the CTA-pair kernel, whose loads must all be tensor copies.
+bsg_status encode_scales(CUtensorMap* m, const void* ptr, size_t bytes, uint32_t atoms, const char* name) {
+  cuuint64_t dims[2] = {128, bytes / 128};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 4 * atoms};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(BSG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with driver error %d", name, static_cast<int>(r));
+  return BSG_OK;
+}
+
 // Kernel parameters of problem d under variant v (tensor maps encoded here), except the
 // workspace pointers.  Grid: persistent (<= #SMs) unless the splits form clusters, in which
 // case every unit is its own CTA.
@@ -277,10 +311,16 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   const size_t rb = code_row_bytes(d->kind, d->K);
   bsg_status s;
   if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, 128, "A")) != BSG_OK ||
-      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.bn), "B")) != BSG_OK)
+      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn), "B")) != BSG_OK)
     return s;
   const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
   const int blk = d->kind == BSG_MXFP8 ? 32 : 16;
+  if (v.pair) {
+    const uint32_t atoms = d->kind == BSG_MXFP8 ? 1 : 4;
+    if ((s = encode_scales(&g->tmap_sfa, d->SFA, sf_bytes_of(d->kind, d->M, d->K), atoms, "SFA")) != BSG_OK ||
+        (s = encode_scales(&g->tmap_sfb, d->SFB, sf_bytes_of(d->kind, d->N, d->K), atoms, "SFB")) != BSG_OK)
+      return s;
+  }
   g->sfa = static_cast<const uint8_t*>(d->SFA);
   g->sfb = static_cast<const uint8_t*>(d->SFB);
   g->bias = d->bias;
@@ -295,7 +335,8 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->sfa_atoms_per_band = (d->K / blk + 3) / 4;
   g->sfb_atoms_per_band = g->sfa_atoms_per_band;
   g->sfb_bands = (d->N + 127) / 128;
-  g->num_m_tiles = (d->M + 127) / 128;
+  g->sfa_bands = (d->M + 127) / 128;
+  g->num_m_tiles = v.pair ? (d->M + 255) / 256 : (d->M + 127) / 128;
   g->num_n_tiles = (d->N + v.bn - 1) / v.bn;
   g->num_k_tiles = (d->K + k_tile - 1) / k_tile;
   g->num_tiles = g->num_m_tiles * g->num_n_tiles;
@@ -305,7 +346,8 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->num_units = g->num_tiles * v.splits;
   g->group_m = 16;
   g->debug_skip_first_load = 0;
-  *grid = v.mode == bsg::SPLIT_CLUSTER ? g->num_units : std::min(g->num_units, sms);
+  if (v.pair) *grid = 2 * std::min(g->num_units, sms / 2);
+  else *grid = v.mode == bsg::SPLIT_CLUSTER ? g->num_units : std::min(g->num_units, sms);
   return BSG_OK;
 }
 
@@ -354,8 +396,10 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   const Variant v = choose_variant(d, di.sms);
   bsg::GemmKernelInfo info{};
   const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
-  const bool found = d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, &info)
-                                          : bsg::gemm_kernel_info_nv(v.bn, out_t, &info);
+  const bool found = v.pair ? (d->kind == BSG_MXFP8 ? bsg::gemm_pair_kernel_info_mx(out_t, &info)
+                                                    : bsg::gemm_pair_kernel_info_nv(out_t, &info))
+                            : (d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, &info)
+                                                    : bsg::gemm_kernel_info_nv(v.bn, out_t, &info));
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
 
@@ -390,8 +434,12 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   g.counters = reinterpret_cast<unsigned*>(ws + w.cnt_off);
   g.partial = w.part_bytes ? reinterpret_cast<float*>(ws + w.part_off) : nullptr;
   static const char* kModeName[] = {"", "w", "c"};
-  std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
-                v.bn, v.splits, kModeName[v.mode], info.stages, p->grid);
+  if (v.pair)
+    std::snprintf(p->variant, sizeof(p->variant), "%s_pair256_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
+                  info.stages, p->grid);
+  else
+    std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
+                  v.bn, v.splits, kModeName[v.mode], info.stages, p->grid);
   if (env_int("BSG_LOG", 0))
     std::fprintf(stderr, "[bsgemm] plan M=%d N=%d K=%d -> %s\n", d->M, d->N, d->K, p->variant);
   *out = p;
@@ -662,8 +710,10 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
   const Variant v = choose_variant(d, di.sms);
   bsg::GemmKernelInfo info{};
   const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
-  const bool found = d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, &info)
-                                          : bsg::gemm_kernel_info_nv(v.bn, out_t, &info);
+  const bool found = v.pair ? (d->kind == BSG_MXFP8 ? bsg::gemm_pair_kernel_info_mx(out_t, &info)
+                                                    : bsg::gemm_pair_kernel_info_nv(out_t, &info))
+                            : (d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, &info)
+                                                    : bsg::gemm_kernel_info_nv(v.bn, out_t, &info));
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   const int num_tiles = ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn);
   const WorkspaceLayout w = workspace_layout(v, num_tiles);

@@ -74,7 +74,7 @@ def test_forced_variants(kind, bn, splits, mode, monkeypatch):
     nkt = K // (128 if kind == "mxfp8" else 256)
     kps = -(-nkt // splits)
     s = -(-nkt // kps)
-    m = "" if s == 1 else ("w" if mode == "w" or s not in (2, 4, 8) else "c")
+    m = "" if s == 1 else ("w" if mode == "w" or s not in (2, 4, 8) or (bn == 256 and s > 2) else "c")
     assert "_bn%d_s%d%s_" % (bn, s, m) in v
 
 
@@ -85,14 +85,42 @@ def test_cluster_split_ragged_rows(kind, monkeypatch):
     assert "_s4c_" in v
 
 
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("M,N,K,out", [(256, 256, 512, "bf16"), (300, 272, 1024, "f16"), (2048, 2560, 512, "bf16"),
+                                       (640, 768, 4096, "bf16")])
+def test_pair_kernel(kind, M, N, K, out, monkeypatch):
+    # CTA-pair kernel (256 x 256 tiles on 2-CTA clusters): ragged M and N, both outputs,
+    # more pair tiles than SM pairs (persistent loop)
+    v = run_case(kind, M, N, K, out=out, env={"BSG_FORCE_PAIR": 1}, monkeypatch=monkeypatch,
+                 bias=(kind == "nvfp4"), silu=(kind == "nvfp4"))
+    assert "_pair256_" in v
+
+
+def test_pair_wait_timeout_reports_status(monkeypatch):
+    monkeypatch.setenv("BSG_FORCE_PAIR", "1")
+    prob = P.make_problem("nvfp4", 512, 512, 1024)
+    dp = P.DeviceProblem(prob)
+    with dp.plan() as plan:
+        assert "_pair256_" in plan.variant
+        bsg.bsg_plan_debug_set(plan.handle, 1, 50_000_000)
+        plan.run()
+        with pytest.raises(bsg.BsgError) as e:
+            plan.check_status()
+        assert e.value.name == "BSG_ERR_DEVICE_TIMEOUT"
+        bsg.bsg_plan_debug_set(plan.handle, 0, 0)
+        plan.run()
+        plan.check_status()
+        P.assert_parity(dp.result(), prob, "bf16")
+
+
 def test_pdl_off_matches(monkeypatch):
     run_case("nvfp4", 256, 512, 1024, env={"BSG_PDL": 0}, monkeypatch=monkeypatch, bias=True, silu=True)
 
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
-def test_persistent_multi_tile_per_cta(kind):
-    # 16 x 10 = 160 tiles of 128 x 256 on 152 SMs: some CTAs run two tiles
-    v = run_case(kind, 2048, 2560, 512)
+def test_persistent_multi_tile_per_cta(kind, monkeypatch):
+    # 16 x 10 = 160 tiles of 128 x 256 on 152 SMs: some CTAs run two tiles (1-SM kernel)
+    v = run_case(kind, 2048, 2560, 512, env={"BSG_FORCE_PAIR": 0}, monkeypatch=monkeypatch)
     assert "_bn256_s1_" in v
 
 
