@@ -31,8 +31,6 @@ enum : unsigned {
 struct GemmParams {
   CUtensorMap tmap_a;  // A codes: bytes, dims {K bytes, M}, box {128, 128}, 128-byte swizzle
   CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N}, box {128, BN}, 128-byte swizzle
-  CUtensorMap tmap_sfa;  // pair kernel: scale buffers as 128-byte rows (4 per atom), no swizzle
-  CUtensorMap tmap_sfb;
   const uint8_t* sfa;  // swizzled 128x4 scale atoms of A
   const uint8_t* sfb;
   const void* bias;    // N values of the output type (flags & F_BIAS)
@@ -56,6 +54,11 @@ struct GemmParams {
   int k_tiles_per_split;
   int num_units;           // num_tiles * splits
   int group_m;             // tile rasterisation: m-blocks per group
+  // Multicast clusters: cm = cmn x cmm CTAs (1 = none) take a block of cmm m-tiles x cmn n-tiles;
+  // the cmn CTAs of one m-tile share (multicast) its A tile, the cmm CTAs of one n-tile its B tile.
+  int cm, cmn, cmm;
+  int num_m_groups;        // ceil(num_m_tiles / cmm)
+  int num_n_groups;        // ceil(num_n_tiles / cmn)
   int debug_skip_first_load;  // test hook: the producer never loads its first stage
 };
 
@@ -67,9 +70,11 @@ struct GemmKernelInfo {
   int stages;
 };
 
-// Look up a kernel instantiation: tile width bn (128 or 256), out (OUT_*).
+// Look up a kernel instantiation: tile width bn (32, 64, 128 or 256), out (OUT_*).
 bool gemm_kernel_info_mx(int bn, int out, GemmKernelInfo* info);
 bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info);
+bool gemm_kernel_info_mx_narrow(int bn, int out, GemmKernelInfo* info);  // bn 32 or 64
+bool gemm_kernel_info_nv_narrow(int bn, int out, GemmKernelInfo* info);
 // CTA-pair kernels (256 x 256 pair tiles, launched in clusters of 2).
 bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info);
 bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info);

@@ -1,14 +1,17 @@
 // Block-scaled GEMM kernel for sm_103a: D = alpha * (A . B^T) (+ bias[n]) (-> SiLU).
 //
-// One persistent CTA per SM, six warps with fixed roles:
-//   warp 0      TMA producer: A / B code tiles (128-byte swizzled) and the matching 128x4 scale
-//               atoms into a STAGES-deep shared-memory ring (mbarrier full / empty pairs);
-//   warp 1      owns tensor memory; one thread copies the scale atoms into TMEM (tcgen05.cp)
-//               and issues the block-scaled tcgen05.mma chain into an FP32 accumulator;
-//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes 32*(w%4)..,
-//               warps 2..5 the first half of the columns, warps 6..9 the second half),
-//               alpha, bias, SiLU, FP16/BF16 rounding and stores; with split-K, FP32 partial
-//               tiles in the workspace and a deterministic reduction by the last split.
+// One persistent CTA per SM, sixteen warps in four warpgroups with fixed roles:
+//   warp 0       TMA producer of the A / B code tiles (128-byte swizzled) into a STAGES-deep
+//                shared-memory ring (mbarrier full / empty pairs);
+//   warp 1       owns tensor memory and issues the block-scaled tcgen05.mma chain into an FP32
+//                accumulator;
+//   warp 2       TMA producer of the matching 128x4 scale atoms (same stages, same barriers);
+//   warps 4..7   scale warps: copy each stage's scale atoms into a TMEM slot (tcgen05.st);
+//   warps 8..15  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes 32*(w%4)..,
+//                warps 8..11 the first half of the columns, warps 12..15 the second half),
+//                alpha, bias, SiLU, FP16/BF16 rounding and stores; with split-K, FP32 partial
+//                tiles reduced inside a thread-block cluster or through the workspace.
+// Optional multicast clusters share the A tile across n-tiles and the B tile across m-tiles.
 // Tile 128 x BN x (128 bytes of K): MXFP8 = 128 E4M3 per row per stage (four K=32 MMAs, one
 // UE8M0 scale each), NVFP4 = 256 E2M1 per row per stage (four K=64 MMAs, four UE4M3 each).
 //
@@ -28,14 +31,14 @@ namespace bsg {
 
 template <int KIND, int BN>
 struct GemmCfg {
-  static_assert(BN == 128 || BN == 256, "tile width");
+  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "tile width");
   static constexpr int BM = 128;
   static constexpr int BK_BYTES = 128;
   static constexpr int K_TILE = KIND == KIND_MX ? 128 : 256;  // elements per k-tile
   static constexpr int MMA_K = KIND == KIND_MX ? 32 : 64;     // elements per MMA
   static constexpr int STEPS = K_TILE / MMA_K;                // MMAs per k-tile (4)
   static constexpr int SF_ATOMS = KIND == KIND_MX ? 1 : 4;    // 128x4 atoms per band per k-tile
-  static constexpr int NB = BN / 128;                         // 128-row bands of B per tile
+  static constexpr int NB = BN >= 128 ? BN / 128 : 1;         // 128-row scale bands of B per tile
   static constexpr int A_BYTES = BM * BK_BYTES;
   static constexpr int B_BYTES = BN * BK_BYTES;
   static constexpr int SFA_BYTES = SF_ATOMS * 512;
@@ -52,18 +55,28 @@ struct GemmCfg {
   static constexpr int SFB_COLS = 4 * SF_ATOMS * NB;
   static constexpr int SF_SLOT_COLS = SFA_COLS + SFB_COLS;
   static constexpr int SF_COL0 = NACC * BN;
-  // NVFP4 needs four scale atoms per band per k-tile; copying them with tcgen05.cp would take
-  // the tensor pipe longer than the MMAs, so four scale warps write them into a TMEM slot per
-  // ring stage with tcgen05.st.  MXFP8 copies its one atom per band with tcgen05.cp into two
-  // alternating slots.
-  static constexpr bool SF_ST = KIND == KIND_NV;
-  static constexpr int SF_SLOTS = SF_ST ? STAGES : 2;
+  // Scale atoms reach TMEM through four scale warps that write them into a TMEM slot per ring
+  // stage with tcgen05.st: a tcgen05.cp per atom would occupy the tensor pipe (about 84 cycles
+  // each, 3 per MXFP8 and 12 per NVFP4 k-tile of a 256-wide tile) next to 512 cycles of MMAs.
+  // Tiles narrower than a 128-row scale band use only a quarter or a half of each B atom, which
+  // the scale warps move to the slot's first columns (every scale address the MMA gets stays a
+  // multiple of four columns).
+  static constexpr int SF_SLOTS = STAGES;
   static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half the columns
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-  static constexpr int EPI_WARP0 = SF_ST ? 6 : 2;     // first epilogue warp
+  // Sixteen warps in four warpgroups: {A/B producer, MMA, scale producer, idle}, the four scale
+  // warps, and the eight epilogue warps.  With 16 warps the launch gives every thread 128
+  // registers; the first two warpgroups hand registers to the epilogue (setmaxnreg), whose
+  // 256-wide tiles need about 180.
+  static constexpr int SCALE_WARP0 = 4;
+  static constexpr int EPI_WARP0 = 8;  // first epilogue warp
   static constexpr int THREADS = 32 * EPI_WARP0 + EPI_THREADS;
+  static constexpr int REGS_CTRL = 56, REGS_SCALE = 80, REGS_EPI = 184;
+  // per SM sub-partition (one warp of each warpgroup): 56 + 80 + 2 x 184 <= 512 registers a lane
+  static_assert(REGS_CTRL + REGS_SCALE + 2 * REGS_EPI <= 512, "register split");
+  static_assert(THREADS == 512, "warpgroup layout");
   // Instruction descriptor (block-scaled kinds): [4,6) B scale id, [7,10) A type,
   // [10,13) B type, [15]/[16] A/B major (0 = K), [17,23) N >> 3, [23] scale type
   // (1 = UE8M0, 0 = UE4M3), [24,29) M >> 4, [29,31) A scale id.
@@ -80,17 +93,20 @@ struct UnitCoord {
   int m_blk, n_blk, split, tile, kt0, kt1;
 };
 
-__device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u) {
+// Unit u (a tile, or one split of a tile) -> tile coordinates and k range.  With a multicast
+// cluster, u numbers blocks of cmm x cmn tiles and `rank` (the CTA's rank in its cluster,
+// rn + cmn * rm) picks the tile of the block.
+__device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u, int rank) {
   UnitCoord c;
   c.split = u % p.splits;
   c.tile = u / p.splits;
-  const int per_group = p.group_m * p.num_n_tiles;
+  const int per_group = p.group_m * p.num_n_groups;
   const int g = c.tile / per_group;
   const int first_m = g * p.group_m;
-  const int gm = min(p.num_m_tiles - first_m, p.group_m);
+  const int gm = min(p.num_m_groups - first_m, p.group_m);
   const int r = c.tile - g * per_group;
-  c.m_blk = first_m + r % gm;
-  c.n_blk = r / gm;
+  c.m_blk = (first_m + r % gm) * p.cmm + rank / p.cmn;
+  c.n_blk = (r / gm) * p.cmn + rank % p.cmn;
   c.kt0 = c.split * p.k_tiles_per_split;
   c.kt1 = min(c.kt0 + p.k_tiles_per_split, p.num_k_tiles);
   return c;
@@ -220,7 +236,8 @@ __device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, const float
   float y[4] = {a.x, a.y, a.z, a.w};
   const bool has_bias = (p.flags & F_BIAS) != 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) y[i] = has_bias ? __fmaf_rn(alpha, y[i], out_to_float<OUT>(b[i])) : __fmul_rn(alpha, y[i]);
+  for (int i = 0; i < 4; ++i)
+    y[i] = has_bias ? __fmaf_rn(alpha, y[i], out_to_float<OUT>(b[i])) : __fmul_rn(alpha, y[i]);
   if (p.flags & F_SILU) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) y[i] = y[i] * __fdividef(1.0f, 1.0f + __expf(-y[i]));  // see epi_pack
@@ -282,6 +299,13 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, const float*
   else cluster_reduce_s<OUT, BN, 8>(p, part, recv, c, alpha, ew, lane);
 }
 
+// Word t of the result is word (t + r) % 4 of v (r uniform across the warp).
+__device__ __forceinline__ uint4 rotate_words(uint4 v, int r) {
+  if (r & 1) v = make_uint4(v.y, v.z, v.w, v.x);
+  if (r & 2) v = make_uint4(v.z, v.w, v.x, v.y);
+  return v;
+}
+
 template <int KIND, int BN, int OUT>
 __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<KIND, BN>;
@@ -316,8 +340,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_full(s), 2);  // the code producer and the scale producer
+      mbar_init(bar_empty(s), p.cmn + p.cmm - 1);  // one release per CTA this stage's copies reach
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
@@ -325,8 +349,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_recv, 1);
-    if (C::SF_ST)
-      for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_sfready(s), 4);  // one arrival per scale warp
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_sfready(s), 4);  // one arrival per scale warp
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -341,10 +364,24 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // Split-K cluster: announce that this CTA's barriers are initialised; the thread that later
-  // pushes slabs to the peers waits for the matching announcements.
-  if (p.split_mode == SPLIT_CLUSTER) cluster_arrive_relaxed();
-  bool cluster_waited = false;  // this thread has completed the start-up cluster arrival
+  // Split-K cluster: the peers push their row slabs into this CTA's ring memory, so one cluster
+  // barrier phase separates "every CTA's MMAs are done and its partial tile is in shared
+  // memory" (epilogue threads arrive then; the other threads when their role ends) from the
+  // pushes; a second phase at teardown keeps every CTA alive until its slabs have been read.
+  bool cluster_waited = false;  // this thread has completed the first phase
+  // Multicast cluster: no CTA may write into a peer's ring or arrive on its barriers before the
+  // peer has initialised them.
+  if (p.cm > 1) cluster_sync();
+  const int crank = p.cm > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int rn = crank % p.cmn, rm = crank / p.cmn;      // position in the cmm x cmn block
+  const int u0 = static_cast<int>(blockIdx.x) / p.cm;   // first unit of this CTA (or cluster)
+  const int ustep = static_cast<int>(gridDim.x) / p.cm;  // CTAs (clusters) of the grid
+  // CTAs sharing this CTA's A tile (same m-tile) and B tile (same n-tile)
+  uint32_t row_mask = 0, col_mask = 0;
+  for (int i = 0; i < p.cmn; ++i) row_mask |= 1u << (rm * p.cmn + i);
+  for (int i = 0; i < p.cmm; ++i) col_mask |= 1u << (rn + i * p.cmn);
+  const uint16_t amask = static_cast<uint16_t>(row_mask), bmask = static_cast<uint16_t>(col_mask);
+  const uint16_t cmask = static_cast<uint16_t>(row_mask | col_mask);
   const uint32_t tmem_base = *tmem_slot;
   // Everything above touched only this CTA's own resources; from here on global memory is
   // read and written, so wait for the preceding grid in the stream (programmatic dependent
@@ -352,187 +389,266 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
   griddep_wait();
   griddep_launch_dependents();
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      bool first = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const UnitCoord c = decode_unit(p, u);
-        for (int kt = c.kt0; kt < c.kt1; ++kt) {
-          if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
-            ok = false;
-            break;
-          }
-          const int k_rem = p.K - kt * C::K_TILE;
-          const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
-          const int sf_atoms = KIND == KIND_MX ? 1 : steps;
-          int bands = 0;
-#pragma unroll
-          for (int rb = 0; rb < C::NB; ++rb) bands += (c.n_blk * C::NB + rb < p.sfb_bands) ? 1 : 0;
-          const uint32_t bytes = C::A_BYTES + C::B_BYTES + (1 + bands) * sf_atoms * 512;
-          if (first && p.debug_skip_first_load) {
-            // test hook: leave this stage unfilled so that the MMA warp's wait runs out
-          } else {
-            const uint32_t fb = bar_full(stage);
-            mbar_arrive_expect_tx(fb, bytes);
-            tma_load_2d(stage_a(stage), &p.tmap_a, fb, kt * C::BK_BYTES, c.m_blk * C::BM);
-            tma_load_2d(stage_b(stage), &p.tmap_b, fb, kt * C::BK_BYTES, c.n_blk * BN);
-            const uint8_t* sa = p.sfa + (static_cast<size_t>(c.m_blk) * p.sfa_atoms_per_band +
-                                         static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
-            bulk_load(stage_sfa(stage), sa, sf_atoms * 512, fb);
-#pragma unroll
-            for (int rb = 0; rb < C::NB; ++rb) {
-              const int band = c.n_blk * C::NB + rb;
-              if (band < p.sfb_bands) {
-                const uint8_t* sb = p.sfb + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
-                                             static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
-                bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512, sb, sf_atoms * 512, fb);
+  // Roles by warpgroup; each warpgroup first sets its register budget (setmaxnreg is executed
+  // by all four warps of a warpgroup at the same instruction).
+  if (warp < C::SCALE_WARP0) {
+    setmaxnreg_dec<C::REGS_CTRL>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer: code tiles
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool first = true;
+        for (int u = u0; ok && u < p.num_units; u += ustep) {
+          const UnitCoord c = decode_unit(p, u, crank);
+          for (int kt = c.kt0; kt < c.kt1; ++kt) {
+            if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            if (first && p.debug_skip_first_load) {
+              // test hook: leave this stage unfilled so that the MMA warp's wait runs out
+            } else {
+              const uint32_t fb = bar_full(stage);
+              mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+              if (p.cmn > 1) {
+                // this CTA's slice of the A tile (the tensor map's box is 128/cmn rows), written
+                // into the same stage of every CTA that shares the m-tile
+                const int rows = C::BM / p.cmn;
+                tma_load_2d_mc(stage_a(stage) + rn * rows * C::BK_BYTES, &p.tmap_a, fb, kt * C::BK_BYTES,
+                               c.m_blk * C::BM + rn * rows, amask);
+              } else {
+                tma_load_2d(stage_a(stage), &p.tmap_a, fb, kt * C::BK_BYTES, c.m_blk * C::BM);
+              }
+              if (p.cmm > 1) {
+                // likewise a BN/cmm-row slice of the B tile for every CTA that shares the n-tile
+                const int rows = BN / p.cmm;
+                tma_load_2d_mc(stage_b(stage) + rm * rows * C::BK_BYTES, &p.tmap_b, fb, kt * C::BK_BYTES,
+                               c.n_blk * BN + rm * rows, bmask);
+              } else {
+                tma_load_2d(stage_b(stage), &p.tmap_b, fb, kt * C::BK_BYTES, c.n_blk * BN);
               }
             }
+            first = false;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          first = false;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+        }
+        if (ok && p.cm > 1) {
+          // Wait until every consumer of the cluster has released the last fill of each stage:
+          // no peer's release may arrive at this CTA's barriers after it has exited.
+          for (int i = 0; i < C::STAGES; ++i) {
+            if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) break;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      int slot = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-        const UnitCoord c = decode_unit(p, u);
-        if (!wait_bounded(bar_tempty(acc), acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kt = c.kt0; kt < c.kt1; ++kt) {
-          if (!wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
-            ok = false;
-            break;
+    } else if (warp == 2) {
+      // ------------------------------------------------------------ TMA producer: scale atoms
+      // A second issuing thread: each copy instruction holds its thread for a hundred-odd cycles,
+      // so the scale copies run beside the code-tile copies, into the same stage and barrier.
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool first = true;
+        for (int u = u0; ok && u < p.num_units; u += ustep) {
+          const UnitCoord c = decode_unit(p, u, crank);
+          const int band0 = c.n_blk * BN / 128;    // first scale band of the B tile
+          const bool a_band = c.m_blk < p.sfa_bands;  // false only for a cluster's m-tile beyond M
+          int bands = 0;
+#pragma unroll
+          for (int rb = 0; rb < C::NB; ++rb) bands += (band0 + rb < p.sfb_bands) ? 1 : 0;
+          for (int kt = c.kt0; kt < c.kt1; ++kt) {
+            if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            const int k_rem = p.K - kt * C::K_TILE;
+            const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
+            const int sf_atoms = KIND == KIND_MX ? 1 : steps;
+            if (first && p.debug_skip_first_load) {
+              // test hook (see the code producer)
+            } else {
+              const uint32_t fb = bar_full(stage);
+              mbar_arrive_expect_tx(fb, static_cast<uint32_t>(((a_band ? 1 : 0) + bands) * sf_atoms * 512));
+              if (a_band) {
+                const uint8_t* sa = p.sfa + (static_cast<size_t>(c.m_blk) * p.sfa_atoms_per_band +
+                                             static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
+                bulk_load(stage_sfa(stage), sa, sf_atoms * 512, fb);
+              }
+#pragma unroll
+              for (int rb = 0; rb < C::NB; ++rb) {
+                const int band = band0 + rb;
+                if (band < p.sfb_bands) {
+                  const uint8_t* sb = p.sfb + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
+                                               static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
+                  bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512, sb, sf_atoms * 512, fb);
+                }
+              }
+            }
+            first = false;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          if (C::SF_ST && !wait_bounded(bar_sfready(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int u = u0; ok && u < p.num_units; u += ustep) {
+          const UnitCoord c = decode_unit(p, u, crank);
+          if (!wait_bounded(bar_tempty(acc), acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int k_rem = p.K - kt * C::K_TILE;
-          const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
-          const uint32_t sfa_t = tmem_base + C::SF_COL0 + (C::SF_ST ? stage : slot) * C::SF_SLOT_COLS;
-          const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-          const uint32_t sa = stage_a(stage), sb = stage_b(stage);
-          const uint32_t ssfa = stage_sfa(stage), ssfb = stage_sfb(stage);
-          if constexpr (KIND == KIND_MX) {
-            tc_cp_sf_atom(sfa_t, sdesc_sf_atom(ssfa));
-#pragma unroll
-            for (int rb = 0; rb < C::NB; ++rb)
-              tc_cp_sf_atom(sfb_t + 4 * rb, sdesc_sf_atom(ssfb + rb * 512));
-            for (int j = 0; j < steps; ++j) {
-              const uint32_t idesc = C::IDESC | (static_cast<uint32_t>(j) << 4) |
-                                     (static_cast<uint32_t>(j) << 29);
-              tc_mma_mxf8(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
-                          idesc, sfa_t, sfb_t, (kt > c.kt0 || j > 0) ? 1u : 0u);
+          const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
+          for (int kt = c.kt0; kt < c.kt1; ++kt) {
+            if (!wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
+              ok = false;
+              break;
             }
+            if (!wait_bounded(bar_sfready(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int k_rem = p.K - kt * C::K_TILE;
+            const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
+            // the scale warps have put this stage's scales in its TMEM slot
+            const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS;
+            const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+            const uint32_t sa = stage_a(stage), sb = stage_b(stage);
+            if constexpr (KIND == KIND_MX) {
+              for (int j = 0; j < steps; ++j) {
+                const uint32_t idesc = C::IDESC | (static_cast<uint32_t>(j) << 4) |
+                                       (static_cast<uint32_t>(j) << 29);
+                tc_mma_mxf8(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
+                            idesc, sfa_t, sfb_t, (kt > c.kt0 || j > 0) ? 1u : 0u);
+              }
+            } else {
+              for (int j = 0; j < steps; ++j) {
+                tc_mma_nvf4(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
+                            C::IDESC, sfa_t + 4 * j, sfb_t + 4 * C::NB * j,
+                            (kt > c.kt0 || j > 0) ? 1u : 0u);
+              }
+            }
+            if (p.cm > 1)
+              tc_commit_mc(bar_empty(stage), cmask);  // every CTA whose copies reach this stage
+            else
+              tc_commit(bar_empty(stage));
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar_tfull(acc));
+          if (C::NACC == 2) {
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
           } else {
-            (void)ssfa;
-            (void)ssfb;  // the scale warps have put this stage's scales in its TMEM slot
-            for (int j = 0; j < steps; ++j) {
-              tc_mma_nvf4(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
-                          C::IDESC, sfa_t + 4 * j, sfb_t + 4 * C::NB * j,
-                          (kt > c.kt0 || j > 0) ? 1u : 0u);
+            acc_phase ^= 1u;
+          }
+        }
+        if (!ok) {
+          // let every tensor-core operation issued so far finish before TMEM is released
+          tc_commit(bar_drain);
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar_drain, 0)) {
+            if (globaltimer_ns() - t0 > 10000000ull) {
+              atomicOr(p.status, ST_TIMEOUT_DRAIN);
+              break;
             }
-          }
-          tc_commit(bar_empty(stage));
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          slot ^= 1;
-        }
-        if (!ok) break;
-        tc_commit(bar_tfull(acc));
-        if (C::NACC == 2) {
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
-        } else {
-          acc_phase ^= 1u;
-        }
-      }
-      if (!ok) {
-        // let every tensor-core operation issued so far finish before TMEM is released
-        tc_commit(bar_drain);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_drain, 0)) {
-          if (globaltimer_ns() - t0 > 10000000ull) {
-            atomicOr(p.status, ST_TIMEOUT_DRAIN);
-            break;
           }
         }
       }
     }
-  } else if (C::SF_ST && warp < C::EPI_WARP0) {
-    // ------------------------------------------------------------ scale warps (NVFP4, warps 2..5)
-    // Per stage, each warp writes its TMEM lane quarter of the stage's scale slot: for MMA j,
-    // column 4j + k of lane i holds the four UE4M3 scales of A row 32k + i (row i of atom j),
-    // and column 4*NB*j + 4b + k those of B row 128b + 32k + i -- the layout a 32x128b.warpx4
-    // copy of the same atoms produces.
+  } else if (warp < C::EPI_WARP0) {
+    setmaxnreg_dec<C::REGS_SCALE>();
+    // ------------------------------------------------------------ scale warps (warps 4..7)
+    // Per stage, each warp writes its TMEM lane quarter of the stage's scale slot with the layout
+    // a 32x128b.warpx4 copy of the atoms produces: lane i, column 4j + k holds the four scales
+    // (one 32-bit word of the atom's row i) of A row 32k + i of atom j, and the B columns follow
+    // (4*NB per atom).  A tile narrower than its 128-row band uses words jq.. of each B atom
+    // row, jq = its first 32-row quarter of the band: they are rotated to the front.
     const int q = warp & 3;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-      const UnitCoord c = decode_unit(p, u);
+    for (int u = u0; ok && u < p.num_units; u += ustep) {
+      const UnitCoord c = decode_unit(p, u, crank);
+      const int jq = BN < 128 ? (c.n_blk * BN % 128) / 32 : 0;
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
         ok = __all_sync(0xffffffffu, wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
         if (!ok) break;
         const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
-        uint32_t a[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 v = lds_u4(stage_sfa(stage) + 512 * j + 16 * lane);
-          a[4 * j] = v.x;
-          a[4 * j + 1] = v.y;
-          a[4 * j + 2] = v.z;
-          a[4 * j + 3] = v.w;
-        }
-        tmem_st_32x32b_x16(slot, a);
-        if constexpr (C::NB == 2) {
-          uint32_t b[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-#pragma unroll
-            for (int rb = 0; rb < 2; ++rb) {
-              const uint4 v = lds_u4(stage_sfb(stage) + rb * C::SF_ATOMS * 512 + 512 * j + 16 * lane);
-              b[(2 * j + rb) * 4] = v.x;
-              b[(2 * j + rb) * 4 + 1] = v.y;
-              b[(2 * j + rb) * 4 + 2] = v.z;
-              b[(2 * j + rb) * 4 + 3] = v.w;
-            }
-          }
-          tmem_st_32x32b_x32(slot + C::SFA_COLS, b);
+        if constexpr (KIND == KIND_MX && C::NB == 1) {
+          // one atom per operand: A words as they are, B words rotated
+          const uint4 va = lds_u4(stage_sfa(stage) + 16 * lane);
+          const uint4 vb = rotate_words(lds_u4(stage_sfb(stage) + 16 * lane), jq);
+          const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+          tmem_st_32x32b_x8(slot, w);
+        } else if constexpr (KIND == KIND_MX) {
+          // one A atom, two B atoms (bands)
+          const uint4 va = lds_u4(stage_sfa(stage) + 16 * lane);
+          const uint4 vb0 = lds_u4(stage_sfb(stage) + 16 * lane);
+          const uint4 vb1 = lds_u4(stage_sfb(stage) + 512 + 16 * lane);
+          const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+          const uint32_t wb[8] = {vb0.x, vb0.y, vb0.z, vb0.w, vb1.x, vb1.y, vb1.z, vb1.w};
+          tmem_st_32x32b_x4(slot, wa);
+          tmem_st_32x32b_x8(slot + C::SFA_COLS, wb);
         } else {
-          uint32_t b[16];
+          uint32_t a[16];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint4 v = lds_u4(stage_sfb(stage) + 512 * j + 16 * lane);
-            b[4 * j] = v.x;
-            b[4 * j + 1] = v.y;
-            b[4 * j + 2] = v.z;
-            b[4 * j + 3] = v.w;
+            const uint4 v = lds_u4(stage_sfa(stage) + 512 * j + 16 * lane);
+            a[4 * j] = v.x;
+            a[4 * j + 1] = v.y;
+            a[4 * j + 2] = v.z;
+            a[4 * j + 3] = v.w;
           }
-          tmem_st_32x32b_x16(slot + C::SFA_COLS, b);
+          tmem_st_32x32b_x16(slot, a);
+          if constexpr (C::NB == 2) {
+            uint32_t b[32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+              for (int rb = 0; rb < 2; ++rb) {
+                const uint4 v = lds_u4(stage_sfb(stage) + rb * C::SF_ATOMS * 512 + 512 * j + 16 * lane);
+                b[(2 * j + rb) * 4] = v.x;
+                b[(2 * j + rb) * 4 + 1] = v.y;
+                b[(2 * j + rb) * 4 + 2] = v.z;
+                b[(2 * j + rb) * 4 + 3] = v.w;
+              }
+            }
+            tmem_st_32x32b_x32(slot + C::SFA_COLS, b);
+          } else {
+            uint32_t b[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 v = rotate_words(lds_u4(stage_sfb(stage) + 512 * j + 16 * lane), jq);
+              b[4 * j] = v.x;
+              b[4 * j + 1] = v.y;
+              b[4 * j + 2] = v.z;
+              b[4 * j + 3] = v.w;
+            }
+            tmem_st_32x32b_x16(slot + C::SFA_COLS, b);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -545,7 +661,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (8 warps)
+    setmaxnreg_inc<C::REGS_EPI>();
+    // ------------------------------------------------------------ epilogue (warps 8..15)
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;       // accumulator row = TMEM lane
     constexpr int HC = BN / 2;           // columns per thread
@@ -553,8 +670,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
     const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-      const UnitCoord c = decode_unit(p, u);
+    for (int u = u0; u < p.num_units; u += ustep) {
+      const UnitCoord c = decode_unit(p, u, crank);
       bool ok = wait_bounded(bar_tfull(acc), acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
       ok = named_bar_and(1, C::EPI_THREADS, ok);
       if (!ok) break;
@@ -567,17 +684,30 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
         // Round the whole row segment into registers first and release the accumulator before
         // storing, so the next tile's MMAs do not wait for the stores.
         uint32_t packed[HC / 2];
-#pragma unroll
-        for (int ch = 0; ch < HC / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
+        if constexpr (HC == 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(t_row + col0, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 0; g < 2; ++g) {
             float v[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[8 * g + i]);
-            epi_pack<OUT, 8>(p, nbase + col0 + ch * 32 + 8 * g, v, alpha, &packed[ch * 16 + 4 * g]);
+            epi_pack<OUT, 8>(p, nbase + col0 + 8 * g, v, alpha, &packed[4 * g]);
+          }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < HC / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              float v[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[8 * g + i]);
+              epi_pack<OUT, 8>(p, nbase + col0 + ch * 32 + 8 * g, v, alpha, &packed[ch * 16 + 4 * g]);
+            }
           }
         }
         tc_fence_before();
@@ -593,97 +723,100 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
                   make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
           }
         }
-      } else if (p.split_mode == SPLIT_CLUSTER) {
-        // partial tile -> this CTA's shared memory (the ring is idle: the unit's MMAs are done)
-        float* part = reinterpret_cast<float*>(smem);
+      } else if constexpr (BN >= 128) {  // split-K is planned for 128- and 256-wide tiles only
+        if (p.split_mode == SPLIT_CLUSTER) {
+          // partial tile -> this CTA's shared memory (the ring is idle: the unit's MMAs are done)
+          float* part = reinterpret_cast<float*>(smem);
 #pragma unroll 1
-        for (int ch = 0; ch < HC / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
-          tmem_ld_wait();
-          float4* dst = reinterpret_cast<float4*>(part + row * (BN + 4) + col0 + ch * 32);
+          for (int ch = 0; ch < HC / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
+            tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(part + row * (BN + 4) + col0 + ch * 32);
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            dst[g] = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                 __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty(acc));
-        fence_proxy_async_smem();  // the partial tile is read next by bulk copies
-        cluster_wait();            // every CTA of the cluster has initialised its receive barrier
-        cluster_waited = true;
-        named_bar_sync(1, C::EPI_THREADS);
-        const int S = p.splits, R = 128 / S;
-        const uint32_t slab = static_cast<uint32_t>(R * (BN + 4) * 4);
-        const uint32_t recv0 = smem0 + 128 * (BN + 4) * 4;
-        if (threadIdx.x == C::EPI_WARP0 * 32) {
-          mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(S - 1) * slab);
-          for (int r = 0; r < S; ++r) {
-            if (r == c.split) continue;
-            const int slot = c.split < r ? c.split : c.split - 1;  // this CTA's slot at CTA r
-            bulk_copy_s2c(mapa_shared(recv0 + slot * slab, static_cast<uint32_t>(r)), smem0 + r * slab, slab,
-                          mapa_shared(bar_recv, static_cast<uint32_t>(r)));
+            for (int g = 0; g < 8; ++g)
+              dst[g] = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                   __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
           }
-        }
-        const bool got = named_bar_and(1, C::EPI_THREADS,
-                                       wait_bounded_cluster(bar_recv, 0, abort_flag, p, ST_TIMEOUT_EPILOGUE));
-        if (got)
-          cluster_reduce<OUT, BN>(p, part, reinterpret_cast<const float*>(smem + 128 * (BN + 4) * 4), c, alpha,
-                                  warp - C::EPI_WARP0, lane);
-      } else {
-        // FP32 partial tile -> workspace as float4 [chunk][8][128 rows] (coalesced per warp)
-        float4* part = reinterpret_cast<float4*>(
-            p.partial + (static_cast<size_t>(c.split) * p.num_tiles + c.tile) * (C::BM * BN));
-        const int ch0 = col0 / 32;
-#pragma unroll 1
-        for (int ch = ch0; ch < ch0 + HC / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + ch * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            float4 v4 = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                    __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
-            __stcg(part + (ch * 8 + g) * C::BM + row, v4);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty(acc));
+          fence_proxy_async_smem();  // the partial tile is read next by bulk copies
+          cluster_arrive();          // this CTA's ring is idle and its partial tile complete
+          cluster_wait();            // ... and so are all the peers'
+          cluster_waited = true;
+          named_bar_sync(1, C::EPI_THREADS);
+          const int S = p.splits, R = 128 / S;
+          const uint32_t slab = static_cast<uint32_t>(R * (BN + 4) * 4);
+          const uint32_t recv0 = smem0 + 128 * (BN + 4) * 4;
+          if (threadIdx.x == C::EPI_WARP0 * 32) {
+            mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(S - 1) * slab);
+            for (int r = 0; r < S; ++r) {
+              if (r == c.split) continue;
+              const int slot = c.split < r ? c.split : c.split - 1;  // this CTA's slot at CTA r
+              bulk_copy_s2c(mapa_shared(recv0 + slot * slab, static_cast<uint32_t>(r)), smem0 + r * slab, slab,
+                            mapa_shared(bar_recv, static_cast<uint32_t>(r)));
+            }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty(acc));
-        __threadfence();
-        named_bar_sync(1, C::EPI_THREADS);
-        if (threadIdx.x == C::EPI_WARP0 * 32) {
-          const unsigned old = atomicAdd(p.counters + c.tile, 1u);
-          const int last = (old == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
-          if (last) p.counters[c.tile] = 0u;  // ready for the next launch
-          *last_flag = last;
-        }
-        named_bar_sync(1, C::EPI_THREADS);
-        if (*last_flag) {
-          __threadfence();
-          const float4* base = reinterpret_cast<const float4*>(
-              p.partial + static_cast<size_t>(c.tile) * (C::BM * BN));
-          const size_t split_stride = static_cast<size_t>(p.num_tiles) * (C::BM * BN) / 4;
+          const bool got = named_bar_and(1, C::EPI_THREADS,
+                                         wait_bounded_cluster(bar_recv, 0, abort_flag, p, ST_TIMEOUT_EPILOGUE));
+          if (got)
+            cluster_reduce<OUT, BN>(p, part, reinterpret_cast<const float*>(smem + 128 * (BN + 4) * 4), c, alpha,
+                                    warp - C::EPI_WARP0, lane);
+        } else {
+          // FP32 partial tile -> workspace as float4 [chunk][8][128 rows] (coalesced per warp)
+          float4* part = reinterpret_cast<float4*>(
+              p.partial + (static_cast<size_t>(c.split) * p.num_tiles + c.tile) * (C::BM * BN));
+          const int ch0 = col0 / 32;
 #pragma unroll 1
           for (int ch = ch0; ch < ch0 + HC / 32; ++ch) {
-            float v[32];
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + ch * 32, r);
+            tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-            for (int s = 0; s < p.splits; ++s) {
-#pragma unroll
-              for (int g = 0; g < 8; ++g) {
-                const float4 t = __ldcg(base + s * split_stride + (ch * 8 + g) * C::BM + row);
-                v[4 * g] += t.x;
-                v[4 * g + 1] += t.y;
-                v[4 * g + 2] += t.z;
-                v[4 * g + 3] += t.w;
-              }
+            for (int g = 0; g < 8; ++g) {
+              float4 v4 = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                      __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+              __stcg(part + (ch * 8 + g) * C::BM + row, v4);
             }
-            store_chunk32<OUT>(p, m, nbase + ch * 32, v, alpha);
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty(acc));
+          __threadfence();
+          named_bar_sync(1, C::EPI_THREADS);
+          if (threadIdx.x == C::EPI_WARP0 * 32) {
+            const unsigned old = atomicAdd(p.counters + c.tile, 1u);
+            const int last = (old == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+            if (last) p.counters[c.tile] = 0u;  // ready for the next launch
+            *last_flag = last;
+          }
+          named_bar_sync(1, C::EPI_THREADS);
+          if (*last_flag) {
+            __threadfence();
+            const float4* base = reinterpret_cast<const float4*>(
+                p.partial + static_cast<size_t>(c.tile) * (C::BM * BN));
+            const size_t split_stride = static_cast<size_t>(p.num_tiles) * (C::BM * BN) / 4;
+#pragma unroll 1
+            for (int ch = ch0; ch < ch0 + HC / 32; ++ch) {
+              float v[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+              for (int s = 0; s < p.splits; ++s) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                  const float4 t = __ldcg(base + s * split_stride + (ch * 8 + g) * C::BM + row);
+                  v[4 * g] += t.x;
+                  v[4 * g + 1] += t.y;
+                  v[4 * g + 2] += t.z;
+                  v[4 * g + 3] += t.w;
+                }
+              }
+              store_chunk32<OUT>(p, m, nbase + ch * 32, v, alpha);
+            }
+          }
+          named_bar_sync(1, C::EPI_THREADS);
         }
-        named_bar_sync(1, C::EPI_THREADS);
       }
       if (C::NACC == 2) {
         acc ^= 1;
@@ -696,10 +829,17 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
 
   // ------------------------------------------------------------ split-K cluster: lifetime
   if (p.split_mode == SPLIT_CLUSTER) {
-    // Every thread completes the start-up arrival (the epilogue warps did before pushing), then
-    // one full cluster barrier: a CTA leaves only after every CTA has received all its slabs,
-    // i.e. after every copy that reads this CTA's shared memory has completed.
-    if (!cluster_waited) cluster_wait();
+    // Every thread completes the first phase (the epilogue threads did before pushing), then
+    // a second one: a CTA leaves only after every CTA has received all its slabs, i.e. after
+    // every copy that reads this CTA's shared memory has completed.
+    if (!cluster_waited) {
+      cluster_arrive_relaxed();
+      cluster_wait();
+    }
+    __syncwarp();
+    cluster_sync();
+  } else if (p.cm > 1) {
+    // multicast cluster: leave together, once no CTA issues further copies into the others
     __syncwarp();
     cluster_sync();
   }

@@ -1,0 +1,15 @@
+// MXFP8 (E4M3 elements, UE8M0 per-32 scales) instantiations of the block-scaled GEMM kernel with
+// 32- and 64-wide tiles (few row tiles: every SM gets a tile without splitting K).
+#include "gemm_kernel.cuh"
+
+namespace bsg {
+
+bool gemm_kernel_info_mx_narrow(int bn, int out, GemmKernelInfo* info) {
+  if (bn == 32 && out == OUT_F16) return fill_kernel_info<KIND_MX, 32, OUT_F16>(info);
+  if (bn == 32 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 32, OUT_BF16>(info);
+  if (bn == 64 && out == OUT_F16) return fill_kernel_info<KIND_MX, 64, OUT_F16>(info);
+  if (bn == 64 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 64, OUT_BF16>(info);
+  return false;
+}
+
+}  // namespace bsg

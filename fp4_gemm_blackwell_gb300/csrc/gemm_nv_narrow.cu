@@ -1,0 +1,15 @@
+// NVFP4 (E2M1 elements, UE4M3 per-16 scales) instantiations of the block-scaled GEMM kernel with
+// 32- and 64-wide tiles (few row tiles: every SM gets a tile without splitting K).
+#include "gemm_kernel.cuh"
+
+namespace bsg {
+
+bool gemm_kernel_info_nv_narrow(int bn, int out, GemmKernelInfo* info) {
+  if (bn == 32 && out == OUT_F16) return fill_kernel_info<KIND_NV, 32, OUT_F16>(info);
+  if (bn == 32 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 32, OUT_BF16>(info);
+  if (bn == 64 && out == OUT_F16) return fill_kernel_info<KIND_NV, 64, OUT_F16>(info);
+  if (bn == 64 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 64, OUT_BF16>(info);
+  return false;
+}
+
+}  // namespace bsg

@@ -9,14 +9,18 @@
 // KernelTmaWarpSpecialized2SmNvf4Sm100; "Add Cutlass MxFp8 Block Scale Matrix
 // Multiplication": MmaTileShape 256 x 256 x 256 over a cluster, PerSmTileShape 128 x 256).
 //
-// Warps (both CTAs): 0 TMA producer, 1 TMEM owner / MMA issuer (the leader's lane 0 issues
-// the pair's scale copies and MMAs), 2..9 epilogue.
-// Synchronisation without per-stage thread handshakes between the CTAs: both CTAs' TMA loads
-// of a stage complete on the leader's `full` barrier (the leader posts the byte count of both);
-// the leader's tcgen05.commit is multicast to both CTAs' `empty` and `tmem_full` barriers; the
-// scale atoms go to each CTA's own TMEM through pairwise tcgen05.cp (each CTA holds A's and
-// both of B's 128-row scale bands in its own shared memory); each epilogue warp arrives on the
-// leader's `tmem_empty` once per tile.
+// Sixteen warps per CTA in four warpgroups (register budgets set with setmaxnreg):
+//   warp 0       TMA producer of the A / B code tiles with the pair form of the copy,
+//                completing on the leader's `full` barrier (the leader posts both CTAs' bytes);
+//   warp 1       TMEM owner; the leader's lane 0 issues the pair's MMAs;
+//   warp 2       TMA producer of the CTA's scale atoms (A's 128 rows, both 128-row bands of
+//                B), completing on its own `sf_full` barrier;
+//   warps 4..7   scale warps: copy each stage's scale atoms into the CTA's own TMEM slot
+//                (tcgen05.st) and arrive on the leader's `full` barrier (the peer's through a
+//                multicast tcgen05.commit);
+//   warps 8..15  epilogue of the CTA's 128 rows; each warp arrives on the leader's
+//                `tmem_empty` once per tile (the peer's through a multicast tcgen05.commit).
+// The leader's tcgen05.commit is multicast to both CTAs' `empty` and `tmem_full` barriers.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -47,12 +51,16 @@ struct PairCfg {
   static constexpr int SFB_COLS = 8 * SF_ATOMS;  // B's 256 rows
   static constexpr int SF_SLOT_COLS = SFA_COLS + SFB_COLS;
   static constexpr int SF_COL0 = BN;             // one 256-column accumulator first
-  static constexpr int TMEM_USED = SF_COL0 + 2 * SF_SLOT_COLS;
+  static constexpr int TMEM_USED = SF_COL0 + STAGES * SF_SLOT_COLS;
   static constexpr int TMEM_COLS = 512;
+  static constexpr int SCALE_WARP0 = 4;
+  static constexpr int EPI_WARP0 = 8;
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-  static constexpr int EPI_WARP0 = 2;
   static constexpr int THREADS = 32 * EPI_WARP0 + EPI_THREADS;
+  static constexpr int REGS_CTRL = 56, REGS_SCALE = 80, REGS_EPI = 184;
+  static_assert(REGS_CTRL + REGS_SCALE + 2 * REGS_EPI <= 512, "register split");
+  static_assert(THREADS == 512, "warpgroup layout");
   static constexpr uint32_t IDESC =
       (KIND == KIND_MX ? ((0u << 7) | (0u << 10) | (1u << 23)) : ((1u << 7) | (1u << 10) | (0u << 23))) |
       (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
@@ -77,14 +85,18 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
 
   uint8_t* aux = smem + C::STAGES * C::STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(aux);
-  // slots: full[0..7], empty[8..15], tmem_full 16, tmem_empty 17, drain 18
+  // slots: full[0..7], empty[8..15], sf_full[16..23], tmem_full 32, tmem_empty 33, drain 34,
+  // tmem address 35, abort flag 36.  The leader's `full` completes when both CTAs' code tiles
+  // have landed and both CTAs' scale warps have filled their TMEM slots: one wait per k-tile
+  // for the MMA issuer.
   auto bar_full = [&](int s) { return smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return smem_u32(bars + 8 + s); };
-  const uint32_t bar_tfull = smem_u32(bars + 16);
-  const uint32_t bar_tempty = smem_u32(bars + 17);
-  const uint32_t bar_drain = smem_u32(bars + 18);
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 19);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
+  auto bar_sf_full = [&](int s) { return smem_u32(bars + 16 + s); };
+  const uint32_t bar_tfull = smem_u32(bars + 32);
+  const uint32_t bar_tempty = smem_u32(bars + 33);
+  const uint32_t bar_drain = smem_u32(bars + 34);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 35);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 36);
 
   auto stage_a = [&](int s) { return smem0 + s * C::STAGE_BYTES; };
   auto stage_b = [&](int s) { return smem0 + s * C::STAGE_BYTES + C::A_BYTES; };
@@ -93,8 +105,10 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar_full(s), 1);   // the leader's producer arrives (with both CTAs' bytes)
-      mbar_init(bar_empty(s), 1);  // the leader's multicast commit
+      // the leader's producer (with both CTAs' code bytes) and the scale warps of both CTAs
+      mbar_init(bar_full(s), 1 + 8);
+      mbar_init(bar_empty(s), 1);    // the leader's multicast commit
+      mbar_init(bar_sf_full(s), 1);  // this CTA's producer (scale bytes)
     }
     mbar_init(bar_tfull, 1);
     mbar_init(bar_tempty, 2 * C::EPI_WARPS);  // one arrival per epilogue warp of each CTA
@@ -104,8 +118,6 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     prefetch_tmap(&p.tmap_a);
     prefetch_tmap(&p.tmap_b);
-    prefetch_tmap(&p.tmap_sfa);
-    prefetch_tmap(&p.tmap_sfb);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
@@ -122,125 +134,232 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
   const int pair0 = blockIdx.x >> 1;
   const int pairs = gridDim.x >> 1;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (each CTA)
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      bool first = true;
-      for (int u = pair0; ok && u < p.num_units; u += pairs) {
-        const UnitCoord c = decode_unit(p, u);
-        const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
-        for (int kt = c.kt0; kt < c.kt1; ++kt) {
-          if (!wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
-            ok = false;
-            break;
-          }
-          // The pair's stage is one transaction on the leader's barrier: A, B and the scale
-          // atoms of both CTAs, whole boxes (bands past the scale buffers read as zeros).
-          const uint32_t fb = mapa_shared(bar_full(stage), leader);
-          if (first && p.debug_skip_first_load) {
-            // test hook: leave this stage unfilled so that the waits downstream run out
-          } else {
-            if (is_leader) mbar_arrive_expect_tx(bar_full(stage), 2 * C::STAGE_RAW);
-            tma_load_2d_pair(stage_a(stage), &p.tmap_a, fb, kt * C::BK_BYTES, m_blk * C::BM);
-            tma_load_2d_pair(stage_b(stage), &p.tmap_b, fb, kt * C::BK_BYTES,
-                             c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128);
-            tma_load_2d_pair(stage_sfa(stage), &p.tmap_sfa, fb, 0,
-                             (m_blk * p.sfa_atoms_per_band + kt * C::SF_ATOMS) * 4);
-#pragma unroll
-            for (int rb = 0; rb < 2; ++rb)
-              tma_load_2d_pair(stage_sfb(stage) + rb * C::SF_ATOMS * 512, &p.tmap_sfb, fb, 0,
-                               ((c.n_blk * 2 + rb) * p.sfb_atoms_per_band + kt * C::SF_ATOMS) * 4);
-          }
-          first = false;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+  if (warp < C::SCALE_WARP0) {
+    setmaxnreg_dec<C::REGS_CTRL>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer (each CTA)
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool first = true;
+        for (int u = pair0; ok && u < p.num_units; u += pairs) {
+          const UnitCoord c = decode_unit(p, u, 0);
+          const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
+          for (int kt = c.kt0; kt < c.kt1; ++kt) {
+            if (!wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            if (first && p.debug_skip_first_load) {
+              // test hook: leave this stage unfilled so that the waits downstream run out
+            } else {
+              // code tiles of both CTAs: one transaction on the leader's barrier
+              const uint32_t fb = mapa_shared(bar_full(stage), leader);
+              if (is_leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (C::A_BYTES + C::B_BYTES));
+              tma_load_2d_pair(stage_a(stage), &p.tmap_a, fb, kt * C::BK_BYTES, m_blk * C::BM);
+              tma_load_2d_pair(stage_b(stage), &p.tmap_b, fb, kt * C::BK_BYTES,
+                               c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128);
+            }
+            first = false;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader, lane 0)
-    if (is_leader && lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t acc_phase = 0;
-      int slot = 0;
-      bool ok = true;
-      for (int u = pair0; ok && u < p.num_units; u += pairs) {
-        const UnitCoord c = decode_unit(p, u);
-        if (!wait_bounded_cluster(bar_tempty, acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
-          ok = false;
-          break;
+    } else if (warp == 2) {
+      // ---------------------------------------------------------- TMA producer: scale atoms
+      // A second issuing thread (each copy instruction holds its thread for a hundred-odd
+      // cycles): this CTA's scale atoms, on its own barrier.
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool first = true;
+        for (int u = pair0; ok && u < p.num_units; u += pairs) {
+          const UnitCoord c = decode_unit(p, u, 0);
+          const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
+          const bool a_band = m_blk < p.sfa_bands;  // false for the pair's second m-tile past M
+          int bands = 0;
+#pragma unroll
+          for (int rb = 0; rb < 2; ++rb) bands += (c.n_blk * 2 + rb < p.sfb_bands) ? 1 : 0;
+          for (int kt = c.kt0; kt < c.kt1; ++kt) {
+            if (!wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            const int k_rem = p.K - kt * C::K_TILE;
+            const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
+            const int sf_atoms = KIND == KIND_MX ? 1 : steps;
+            if (first && p.debug_skip_first_load) {
+              // test hook (see the code producer)
+            } else {
+              const uint32_t sb = bar_sf_full(stage);
+              mbar_arrive_expect_tx(sb, static_cast<uint32_t>(((a_band ? 1 : 0) + bands) * sf_atoms * 512));
+              if (a_band)
+                bulk_load(stage_sfa(stage),
+                          p.sfa + (static_cast<size_t>(m_blk) * p.sfa_atoms_per_band +
+                                   static_cast<size_t>(kt) * C::SF_ATOMS) * 512,
+                          sf_atoms * 512, sb);
+#pragma unroll
+              for (int rb = 0; rb < 2; ++rb) {
+                const int band = c.n_blk * 2 + rb;
+                if (band < p.sfb_bands)
+                  bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512,
+                            p.sfb + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
+                                     static_cast<size_t>(kt) * C::SF_ATOMS) * 512,
+                            sf_atoms * 512, sb);
+              }
+            }
+            first = false;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
         }
-        tc_fence_after();
-        for (int kt = c.kt0; kt < c.kt1; ++kt) {
-          if (!wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer (leader, lane 0)
+      if (is_leader && lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int u = pair0; ok && u < p.num_units; u += pairs) {
+          const UnitCoord c = decode_unit(p, u, 0);
+          if (!wait_bounded_cluster(bar_tempty, acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int k_rem = p.K - kt * C::K_TILE;
-          const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
-          const uint32_t sfa_t = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-          const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-          const uint32_t sa = stage_a(stage), sb = stage_b(stage);
-          const uint32_t ssfa = stage_sfa(stage), ssfb = stage_sfb(stage);
-          if constexpr (KIND == KIND_MX) {
-            tc_cp_sf_atom_pair(sfa_t, sdesc_sf_atom(ssfa));
-            tc_cp_sf_atom_pair(sfb_t, sdesc_sf_atom(ssfb));
-            tc_cp_sf_atom_pair(sfb_t + 4, sdesc_sf_atom(ssfb + 512));
-            for (int j = 0; j < steps; ++j) {
-              const uint32_t idesc = C::IDESC | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
-              tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j), idesc,
-                               sfa_t, sfb_t, (kt > c.kt0 || j > 0) ? 1u : 0u);
+          for (int kt = c.kt0; kt < c.kt1; ++kt) {
+            if (!wait_bounded_cluster(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
+              ok = false;
+              break;
             }
-          } else {
-            for (int j = 0; j < steps; ++j) {
-              tc_cp_sf_atom_pair(sfa_t + 4 * j, sdesc_sf_atom(ssfa + 512 * j));
-              tc_cp_sf_atom_pair(sfb_t + 8 * j, sdesc_sf_atom(ssfb + 512 * j));
-              tc_cp_sf_atom_pair(sfb_t + 8 * j + 4, sdesc_sf_atom(ssfb + C::SF_ATOMS * 512 + 512 * j));
+            tc_fence_after();
+            const int k_rem = p.K - kt * C::K_TILE;
+            const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
+            // the scale warps of both CTAs have put this stage's scales in their TMEM slots
+            const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS;
+            const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+            const uint32_t sa = stage_a(stage), sb = stage_b(stage);
+            if constexpr (KIND == KIND_MX) {
+              for (int j = 0; j < steps; ++j) {
+                const uint32_t idesc = C::IDESC | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
+                tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j), idesc,
+                                 sfa_t, sfb_t, (kt > c.kt0 || j > 0) ? 1u : 0u);
+              }
+            } else {
+              for (int j = 0; j < steps; ++j)
+                tc_mma_nvf4_pair(tmem_base, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
+                                 C::IDESC, sfa_t + 4 * j, sfb_t + 8 * j, (kt > c.kt0 || j > 0) ? 1u : 0u);
             }
-            for (int j = 0; j < steps; ++j)
-              tc_mma_nvf4_pair(tmem_base, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j), C::IDESC,
-                               sfa_t + 4 * j, sfb_t + 8 * j, (kt > c.kt0 || j > 0) ? 1u : 0u);
+            tc_commit_pair_mc(bar_empty(stage), pair_mask);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          tc_commit_pair_mc(bar_empty(stage), pair_mask);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          slot ^= 1;
+          if (!ok) break;
+          tc_commit_pair_mc(bar_tfull, pair_mask);
+          acc_phase ^= 1u;
         }
-        if (!ok) break;
-        tc_commit_pair_mc(bar_tfull, pair_mask);
-        acc_phase ^= 1u;
-      }
-      if (!ok) {
-        tc_commit_pair_mc(bar_drain, static_cast<uint16_t>(1u << rank));
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_drain, 0)) {
-          if (globaltimer_ns() - t0 > 10000000ull) {
-            atomicOr(p.status, ST_TIMEOUT_DRAIN);
-            break;
+        if (!ok) {
+          tc_commit_pair_mc(bar_drain, static_cast<uint16_t>(1u << rank));
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar_drain, 0)) {
+            if (globaltimer_ns() - t0 > 10000000ull) {
+              atomicOr(p.status, ST_TIMEOUT_DRAIN);
+              break;
+            }
           }
         }
       }
     }
+  } else if (warp < C::EPI_WARP0) {
+    setmaxnreg_dec<C::REGS_SCALE>();
+    // ------------------------------------------------------------ scale warps (each CTA)
+    // The layout a 32x128b.warpx4 copy of the atoms produces, per stage slot: lane i, column
+    // 4j + k holds the four scales of A row 32k + i of atom j (this CTA's 128 rows), and column
+    // 8j + 4b + k those of B row 128b + 32k + i (the pair tile's 256 rows).
+    const int q = warp & 3;
+    const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = pair0; ok && u < p.num_units; u += pairs) {
+      const UnitCoord c = decode_unit(p, u, 0);
+      for (int kt = c.kt0; kt < c.kt1; ++kt) {
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
+        if (!ok) break;
+        const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
+        if constexpr (KIND == KIND_MX) {
+          const uint4 va = lds_u4(stage_sfa(stage) + 16 * lane);
+          const uint4 vb0 = lds_u4(stage_sfb(stage) + 16 * lane);
+          const uint4 vb1 = lds_u4(stage_sfb(stage) + 512 + 16 * lane);
+          const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+          const uint32_t wb[8] = {vb0.x, vb0.y, vb0.z, vb0.w, vb1.x, vb1.y, vb1.z, vb1.w};
+          tmem_st_32x32b_x4(slot, wa);
+          tmem_st_32x32b_x8(slot + C::SFA_COLS, wb);
+        } else {
+          uint32_t a[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = lds_u4(stage_sfa(stage) + 512 * j + 16 * lane);
+            a[4 * j] = v.x;
+            a[4 * j + 1] = v.y;
+            a[4 * j + 2] = v.z;
+            a[4 * j + 3] = v.w;
+          }
+          tmem_st_32x32b_x16(slot, a);
+          uint32_t b[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int rb = 0; rb < 2; ++rb) {
+              const uint4 v = lds_u4(stage_sfb(stage) + rb * C::SF_ATOMS * 512 + 512 * j + 16 * lane);
+              b[(2 * j + rb) * 4] = v.x;
+              b[(2 * j + rb) * 4 + 1] = v.y;
+              b[(2 * j + rb) * 4 + 2] = v.z;
+              b[(2 * j + rb) * 4 + 3] = v.w;
+            }
+          }
+          tmem_st_32x32b_x32(slot + C::SFA_COLS, b);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          // The peer signals through the tensor-core commit path, which arrives on the leader's
+          // barrier without holding this thread for the cluster round trip that a remote
+          // mbarrier arrive takes (its stores to TMEM are complete: tcgen05.wait::st above).
+          if (is_leader)
+            mbar_arrive(bar_full(stage));
+          else
+            tc_commit_pair_mc(bar_full(stage), leader_mask);
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   } else {
+    setmaxnreg_inc<C::REGS_EPI>();
     // ------------------------------------------------------------ epilogue (each CTA, 8 warps)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     constexpr int HC = C::BN / 2;
     const int col0 = ((warp - C::EPI_WARP0) >> 2) * HC;
     const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
-    const uint32_t leader_tempty = mapa_shared(bar_tempty, leader);
+    const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
     uint32_t acc_phase = 0;
     for (int u = pair0; u < p.num_units; u += pairs) {
-      const UnitCoord c = decode_unit(p, u);
+      const UnitCoord c = decode_unit(p, u, 0);
       bool ok = wait_bounded_cluster(bar_tfull, acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
       ok = named_bar_and(1, C::EPI_THREADS, ok);
       if (!ok) break;
@@ -264,7 +383,13 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(leader_tempty);
+      // the accumulator rows of this warp are read (tcgen05.wait::ld above): release them
+      if (lane == 0) {
+        if (is_leader)
+          mbar_arrive(bar_tempty);
+        else
+          tc_commit_pair_mc(bar_tempty, leader_mask);
+      }
       if (m < p.M) {
         uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
 #pragma unroll

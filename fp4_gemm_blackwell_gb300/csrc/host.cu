@@ -193,6 +193,43 @@ bsg_status ensure_smem_attr(const bsg::GemmKernelInfo& info, int device) {
   return BSG_OK;
 }
 
+// CTAs of `info`'s kernel that can be resident at once when launched in clusters of `cluster`
+// (the SM count for cluster <= 1; clusters must fit in a GPC, which can leave SMs over).
+std::mutex g_occ_mutex;
+std::unordered_map<std::string, int> g_occ_cache;
+
+bsg_status resident_ctas(const bsg::GemmKernelInfo& info, int cluster, int sms, int device, int* out) {
+  *out = sms;
+  if (cluster <= 1) return BSG_OK;
+  char key[96];
+  std::snprintf(key, sizeof(key), "%p/%d/%d", info.fn, cluster, device);
+  std::lock_guard<std::mutex> lk(g_occ_mutex);
+  auto it = g_occ_cache.find(key);
+  if (it != g_occ_cache.end()) {
+    *out = it->second;
+    return BSG_OK;
+  }
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster * sms), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(info.threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(info.smem_bytes);
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, info.fn, &cfg);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+  if (clusters < 1) return fail(BSG_ERR_CUDA, "no cluster of %d CTAs of this kernel fits on the device", cluster);
+  *out = std::min(sms, clusters * cluster);
+  g_occ_cache[key] = *out;
+  return BSG_OK;
+}
+
 int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (v == nullptr || *v == 0) return dflt;
@@ -200,13 +237,17 @@ int env_int(const char* name, int dflt) {
 }
 
 // Tile width, split-K: 256-wide tiles when they alone give every SM a tile; otherwise
-// 128-wide tiles (double-buffered accumulator) and, if that still leaves SMs idle, split K so
-// that tiles x splits is close to the SM count.  Every split owns at least one k-tile.  Split
-// factors of 2, 4 and 8 combine their partial tiles inside a thread-block cluster (DSMEM);
-// other factors (only reachable by forcing) go through the plan's global workspace.
+// 128-wide tiles (double-buffered accumulator).  If that still leaves SMs idle, narrower tiles
+// (64 or 32 columns) when they give at least three quarters of the SMs a tile -- the A tile all
+// of them share is then multicast to clusters of cm CTAs that take adjacent n-tiles, and K is
+// not split -- else split K so that tiles x splits is close to the SM count.  Every split owns
+// at least one k-tile.  Split factors of 2, 4 and 8 combine their partial tiles inside a
+// thread-block cluster (DSMEM); other factors (only reachable by forcing) go through the
+// plan's global workspace.
 struct Variant {
   int bn, splits, kps, mode, cluster;
-  bool pair;  // CTA-pair kernel: 256 x 256 tiles over 2-CTA clusters
+  int cmn, cmm;  // multicast cluster: cmm m-tiles x cmn n-tiles (A shared along n, B along m)
+  bool pair;     // CTA-pair kernel: 256 x 256 tiles over 2-CTA clusters
 };
 
 Variant choose_variant(const bsg_desc* d, int sms) {
@@ -215,23 +256,32 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   const long long mt = (d->M + 127) / 128;
   const long long t256 = mt * ((d->N + 255) / 256);
   const long long t128 = mt * ((d->N + 127) / 128);
+  const long long t64 = mt * ((d->N + 63) / 64);
+  const long long t32 = mt * ((d->N + 31) / 32);
   int b, s = 1;
   if (t256 >= sms) {
     b = 256;
+  } else if (t128 >= sms) {
+    b = 128;
+  } else if (4 * t64 >= 3LL * sms) {
+    b = 64;
+  } else if (4 * t32 >= 3LL * sms) {
+    b = 32;
   } else {
     b = 128;
-    if (t128 < sms) {
-      const long long want = std::min<long long>(std::min<long long>(nkt, 8), sms / t128);
-      while (s * 2 <= want) s *= 2;
-    }
+    const long long want = std::min<long long>(std::min<long long>(nkt, 8), sms / t128);
+    while (s * 2 <= want) s *= 2;
   }
   const int fb = env_int("BSG_FORCE_BN", 0);
-  if (fb == 128 || fb == 256) b = fb;
+  if (fb == 32 || fb == 64 || fb == 128 || fb == 256) b = fb;
   const int fs = env_int("BSG_FORCE_SPLITS", 0);
   if (fs >= 1) s = std::min(fs, nkt);
+  if (b < 128) s = 1;  // narrow tiles never split K
   int k = (nkt + s - 1) / s;
   s = (nkt + k - 1) / k;
   Variant v;
+  v.cmn = 1;
+  v.cmm = 1;
   // The CTA-pair kernel (256 x 256 tiles over 2-CTA clusters) is selected only on request
   // (BSG_FORCE_PAIR=1) for now: measured on GB300 it is slower than the 1-SM kernel at 8192^3
   // (load delivery per k-tile and, for NVFP4, 12 scale copies per k-tile), see the design doc.
@@ -249,6 +299,25 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   v.bn = b;
   v.splits = s;
   v.kps = k;
+  // multicast cluster (split-K off): A shared by cmn n-tiles, B by cmm m-tiles; each at most the
+  // number of such tiles (power of two), and the cluster at most 8 CTAs
+  int cmn = b < 128 ? 4 : 1, cmm = 1;
+  const int fc = env_int("BSG_FORCE_CM", 0);
+  if (fc == 1 || fc == 2 || fc == 4 || fc == 8) cmn = fc;
+  const int fm = env_int("BSG_FORCE_CMM", 0);
+  if (fm == 1 || fm == 2 || fm == 4 || fm == 8) cmm = fm;
+  if (s > 1) cmn = cmm = 1;
+  const long long nt = (d->N + b - 1) / b;
+  while (cmn > 1 && cmn > nt) cmn /= 2;
+  while (cmm > 1 && cmm > mt) cmm /= 2;
+  while (cmn * cmm > 8) (cmn >= cmm ? cmn : cmm) /= 2;
+  if (cmn * cmm > 1) {
+    v.cmn = cmn;
+    v.cmm = cmm;
+    v.mode = bsg::SPLIT_NONE;
+    v.cluster = cmn * cmm;
+    return v;
+  }
   // A cluster split keeps the partial tile and the peers' row slabs in the ring's shared
   // memory: 128 x (bn + 4) floats plus (s - 1) slabs of 128/s rows, which for 256-wide tiles
   // only fits with s = 2.
@@ -288,39 +357,19 @@ bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, u
   return BSG_OK;
 }
 
-// Scale buffer (swizzled 128x4 atoms, contiguous) as 128-byte rows, 4 rows per atom; boxes of
-// `atoms` atoms.  Used by the CTA-pair kernel, whose loads must all be tensor copies.
-bsg_status encode_scales(CUtensorMap* m, const void* ptr, size_t bytes, uint32_t atoms, const char* name) {
-  cuuint64_t dims[2] = {128, bytes / 128};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, 4 * atoms};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(BSG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with driver error %d", name, static_cast<int>(r));
-  return BSG_OK;
-}
-
 // Kernel parameters of problem d under variant v (tensor maps encoded here), except the
 // workspace pointers.  Grid: persistent (<= #SMs) unless the splits form clusters, in which
 // case every unit is its own CTA.
-bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, int sms, int* grid) {
+bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, int sms, int resident_ctas,
+                       int* grid) {
   std::memset(g, 0, sizeof(*g));
   const size_t rb = code_row_bytes(d->kind, d->K);
   bsg_status s;
-  if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, 128, "A")) != BSG_OK ||
-      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn), "B")) != BSG_OK)
+  if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, static_cast<uint32_t>(128 / v.cmn), "A")) != BSG_OK ||
+      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn / v.cmm), "B")) != BSG_OK)
     return s;
   const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
   const int blk = d->kind == BSG_MXFP8 ? 32 : 16;
-  if (v.pair) {
-    const uint32_t atoms = d->kind == BSG_MXFP8 ? 1 : 4;
-    if ((s = encode_scales(&g->tmap_sfa, d->SFA, sf_bytes_of(d->kind, d->M, d->K), atoms, "SFA")) != BSG_OK ||
-        (s = encode_scales(&g->tmap_sfb, d->SFB, sf_bytes_of(d->kind, d->N, d->K), atoms, "SFB")) != BSG_OK)
-      return s;
-  }
   g->sfa = static_cast<const uint8_t*>(d->SFA);
   g->sfb = static_cast<const uint8_t*>(d->SFB);
   g->bias = d->bias;
@@ -343,10 +392,16 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->splits = v.splits;
   g->split_mode = v.mode;
   g->k_tiles_per_split = v.kps;
-  g->num_units = g->num_tiles * v.splits;
+  g->cmn = v.cmn;
+  g->cmm = v.cmm;
+  g->cm = v.cmn * v.cmm;
+  g->num_m_groups = (g->num_m_tiles + v.cmm - 1) / v.cmm;
+  g->num_n_groups = (g->num_n_tiles + v.cmn - 1) / v.cmn;
+  g->num_units = g->num_m_groups * g->num_n_groups * v.splits;
   g->group_m = 16;
   g->debug_skip_first_load = 0;
   if (v.pair) *grid = 2 * std::min(g->num_units, sms / 2);
+  else if (g->cm > 1) *grid = g->cm * std::min(g->num_units, resident_ctas / g->cm);
   else *grid = v.mode == bsg::SPLIT_CLUSTER ? g->num_units : std::min(g->num_units, sms);
   return BSG_OK;
 }
@@ -402,6 +457,8 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
                                                     : bsg::gemm_kernel_info_nv(v.bn, out_t, &info));
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
+  int resident = di.sms;
+  if ((s = resident_ctas(info, v.cmn * v.cmm, di.sms, dev, &resident)) != BSG_OK) return s;
 
   bsg_plan_s* p = new (std::nothrow) bsg_plan_s();
   if (p == nullptr) return fail(BSG_ERR_NOMEM, "host allocation of the plan failed");
@@ -412,7 +469,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   p->workspace = nullptr;
   p->cluster = v.cluster;
   bsg::GemmParams& g = p->params;
-  if ((s = fill_params(&g, d, v, di.sms, &p->grid)) != BSG_OK) {
+  if ((s = fill_params(&g, d, v, di.sms, resident, &p->grid)) != BSG_OK) {
     delete p;
     return s;
   }
@@ -434,12 +491,15 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   g.counters = reinterpret_cast<unsigned*>(ws + w.cnt_off);
   g.partial = w.part_bytes ? reinterpret_cast<float*>(ws + w.part_off) : nullptr;
   static const char* kModeName[] = {"", "w", "c"};
-  if (v.pair)
+  if (v.pair) {
     std::snprintf(p->variant, sizeof(p->variant), "%s_pair256_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
                   info.stages, p->grid);
-  else
-    std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
-                  v.bn, v.splits, kModeName[v.mode], info.stages, p->grid);
+  } else {
+    char mc[24] = "";
+    if (v.cmn * v.cmm > 1) std::snprintf(mc, sizeof(mc), v.cmm > 1 ? "_mc%dx%d" : "_mc%d", v.cmn, v.cmm);
+    std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
+                  v.bn, v.splits, kModeName[v.mode], mc, info.stages, p->grid);
+  }
   if (env_int("BSG_LOG", 0))
     std::fprintf(stderr, "[bsgemm] plan M=%d N=%d K=%d -> %s\n", d->M, d->N, d->K, p->variant);
   *out = p;
@@ -725,10 +785,12 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
   unsigned char* scratch = nullptr;
   if ((s = noalloc_scratch(dev, &scratch)) != BSG_OK) return s;
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
+  int resident = di.sms;
+  if ((s = resident_ctas(info, v.cmn * v.cmm, di.sms, dev, &resident)) != BSG_OK) return s;
 
   bsg::GemmParams g;
   int grid = 0;
-  if ((s = fill_params(&g, d, v, di.sms, &grid)) != BSG_OK) return s;
+  if ((s = fill_params(&g, d, v, di.sms, resident, &grid)) != BSG_OK) return s;
   g.status = reinterpret_cast<unsigned*>(scratch);
   g.counters = reinterpret_cast<unsigned*>(scratch + w.cnt_off);
   g.partial = w.part_bytes ? reinterpret_cast<float*>(scratch + w.part_off) : nullptr;

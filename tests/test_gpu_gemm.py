@@ -86,6 +86,58 @@ def test_cluster_split_ragged_rows(kind, monkeypatch):
 
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("bn", [32, 64])
+@pytest.mark.parametrize("cm", [1, 2, 4, 8])
+def test_narrow_tiles_multicast(kind, bn, cm, monkeypatch):
+    # 32- and 64-wide tiles (B scales taken from a quarter / half of each 128-row band), the A
+    # tile multicast over clusters of cm CTAs; N = 400 leaves the last tile half full and the
+    # last cluster with n-tiles wholly beyond N, M = 200 a ragged second m-tile
+    v = run_case(kind, 200, 400, 1792, env={"BSG_FORCE_BN": bn, "BSG_FORCE_CM": cm}, monkeypatch=monkeypatch,
+                 bias=True, silu=True)
+    nt = -(-400 // bn)
+    while cm > nt:  # a cluster never has more CTAs than there are n-tiles
+        cm //= 2
+    assert "_bn%d_s1%s_" % (bn, "" if cm == 1 else "_mc%d" % cm) in v
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_narrow_tiles_persistent_clusters(kind, monkeypatch):
+    # 8 x 128 tiles of 128 x 32 in clusters of 4: more cluster units than resident clusters
+    v = run_case(kind, 1024, 4096, 512, env={"BSG_FORCE_BN": 32, "BSG_FORCE_CM": 4}, monkeypatch=monkeypatch,
+                 out="f16", rows=np.arange(0, 1024, 7))
+    assert "_bn32_s1_mc4_" in v
+
+
+def test_skinny_default_is_narrow_multicast():
+    # the M = 128, N = 4096 shape gets 32-wide tiles, one per SM, without split-K
+    prob = P.make_problem("nvfp4", 128, 4096, 512)
+    dp = P.DeviceProblem(prob, out="bf16", bias=True, silu=True)
+    with dp.plan() as plan:
+        assert "_bn32_s1_mc4_" in plan.variant
+        plan.run()
+        plan.check_status()
+        P.assert_parity(dp.result(), prob, "bf16", dp.bias_vals, True)
+
+
+def test_multicast_wait_timeout_reports_status(monkeypatch):
+    monkeypatch.setenv("BSG_FORCE_BN", "32")
+    monkeypatch.setenv("BSG_FORCE_CM", "4")
+    prob = P.make_problem("nvfp4", 256, 1024, 1024)
+    dp = P.DeviceProblem(prob)
+    with dp.plan() as plan:
+        assert "_mc4_" in plan.variant
+        bsg.bsg_plan_debug_set(plan.handle, 1, 50_000_000)
+        plan.run()
+        with pytest.raises(bsg.BsgError) as e:
+            plan.check_status()
+        assert e.value.name == "BSG_ERR_DEVICE_TIMEOUT"
+        bsg.bsg_plan_debug_set(plan.handle, 0, 0)
+        plan.run()
+        plan.check_status()
+        P.assert_parity(dp.result(), prob, "bf16")
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("M,N,K,out", [(256, 256, 512, "bf16"), (300, 272, 1024, "f16"), (2048, 2560, 512, "bf16"),
                                        (640, 768, 4096, "bf16")])
 def test_pair_kernel(kind, M, N, K, out, monkeypatch):
