@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
   auto bar_tfull = [&](int a) { return smem_u32(bars + 16 + a); };
   auto bar_tempty = [&](int a) { return smem_u32(bars + 18 + a); };
   const uint32_t bar_drain = smem_u32(bars + 20);
-  auto bar_sfready = [&](int s) { return smem_u32(bars + 24 + s); };
+  auto bar_sf_full = [&](int s) { return smem_u32(bars + 24 + s); };  // scale atoms landed
   const uint32_t bar_recv = smem_u32(bars + 32);  // split-K cluster: peers' slabs have landed
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 22);
@@ -340,7 +340,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar_full(s), 2);  // the code producer and the scale producer
+      // the code producer (with its bytes) and the four scale warps once the stage's scales are
+      // in TMEM: one wait per k-tile for the MMA issuer
+      mbar_init(bar_full(s), 1 + 4);
       mbar_init(bar_empty(s), p.cmn + p.cmm - 1);  // one release per CTA this stage's copies reach
     }
     for (int a = 0; a < 2; ++a) {
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_recv, 1);
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_sfready(s), 4);  // one arrival per scale warp
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(bar_sf_full(s), 1);  // the scale producer
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -452,7 +454,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
     } else if (warp == 2) {
       // ------------------------------------------------------------ TMA producer: scale atoms
       // A second issuing thread: each copy instruction holds its thread for a hundred-odd cycles,
-      // so the scale copies run beside the code-tile copies, into the same stage and barrier.
+      // so the scale copies run beside the code-tile copies, into the same stage, completing on
+      // the stage's `sf_full` barrier, which the scale warps wait for; they in turn arrive on
+      // the stage's `full` barrier, so the MMA issuer waits once per k-tile.
       if (lane == 0) {
         int stage = 0;
         uint32_t phase = 0;
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
             if (first && p.debug_skip_first_load) {
               // test hook (see the code producer)
             } else {
-              const uint32_t fb = bar_full(stage);
+              const uint32_t fb = bar_sf_full(stage);
               mbar_arrive_expect_tx(fb, static_cast<uint32_t>(((a_band ? 1 : 0) + bands) * sf_atoms * 512));
               if (a_band) {
                 const uint8_t* sa = p.sfa + (static_cast<size_t>(c.m_blk) * p.sfa_atoms_per_band +
@@ -519,10 +523,6 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
           const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
             if (!wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
-              ok = false;
-              break;
-            }
-            if (!wait_bounded(bar_sfready(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
       const UnitCoord c = decode_unit(p, u, crank);
       const int jq = BN < 128 ? (c.n_blk * BN % 128) / 32 : 0;
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
-        ok = __all_sync(0xffffffffu, wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
         if (!ok) break;
         const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
         if constexpr (KIND == KIND_MX && C::NB == 1) {
@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfready(stage));
+        if (lane == 0) mbar_arrive(bar_full(stage));
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;

@@ -236,14 +236,17 @@ int env_int(const char* name, int dflt) {
   return std::atoi(v);
 }
 
-// Tile width, split-K: 256-wide tiles when they alone give every SM a tile; otherwise
-// 128-wide tiles (double-buffered accumulator).  If that still leaves SMs idle, narrower tiles
-// (64 or 32 columns) when they give at least three quarters of the SMs a tile -- the A tile all
-// of them share is then multicast to clusters of cm CTAs that take adjacent n-tiles, and K is
-// not split -- else split K so that tiles x splits is close to the SM count.  Every split owns
-// at least one k-tile.  Split factors of 2, 4 and 8 combine their partial tiles inside a
-// thread-block cluster (DSMEM); other factors (only reachable by forcing) go through the
-// plan's global workspace.
+// Kernel variant, from measurements on GB300 (NVFP4 and MXFP8, M from 1 to 8192):
+//  - M > 256 and at least a quarter as many 256 x 256 tiles as SMs: the CTA-pair kernel (its
+//    per-SM shared-memory traffic per MMA is two thirds of the 1-SM tile's);
+//  - else 1-SM tiles: 256 wide when they alone give every SM a tile, 128 wide when they give at
+//    least two thirds of the SMs one; otherwise, for K of at most four k-tiles, 32-wide tiles
+//    (more CTAs loading at once; split-K would cost more than it saves), and for longer K,
+//    128-wide tiles with K split so that tiles x splits fills at most one wave (2, 4 or 8
+//    splits reduce inside a thread-block cluster; other factors, only reachable by forcing,
+//    go through the plan's global workspace).
+// Multicast clusters (A shared along n, B along m) are available by forcing but never won a
+// measurement: the 1-SM tile is bound by shared-memory traffic, which multicast leaves as is.
 struct Variant {
   int bn, splits, kps, mode, cluster;
   int cmn, cmm;  // multicast cluster: cmm m-tiles x cmn n-tiles (A shared along n, B along m)
@@ -256,16 +259,17 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   const long long mt = (d->M + 127) / 128;
   const long long t256 = mt * ((d->N + 255) / 256);
   const long long t128 = mt * ((d->N + 127) / 128);
-  const long long t64 = mt * ((d->N + 63) / 64);
-  const long long t32 = mt * ((d->N + 31) / 32);
+  const long long pair_tiles = ((d->M + 255) / 256) * ((d->N + 255) / 256);
   int b, s = 1;
-  if (t256 >= sms) {
+  bool pair = false;
+  if (d->M > 256 && 4 * pair_tiles >= sms) {
+    pair = true;
     b = 256;
-  } else if (t128 >= sms) {
+  } else if (t256 >= sms) {
+    b = 256;
+  } else if (3 * t128 >= 2LL * sms) {
     b = 128;
-  } else if (4 * t64 >= 3LL * sms) {
-    b = 64;
-  } else if (4 * t32 >= 3LL * sms) {
+  } else if (nkt <= 4) {
     b = 32;
   } else {
     b = 128;
@@ -273,7 +277,10 @@ Variant choose_variant(const bsg_desc* d, int sms) {
     while (s * 2 <= want) s *= 2;
   }
   const int fb = env_int("BSG_FORCE_BN", 0);
-  if (fb == 32 || fb == 64 || fb == 128 || fb == 256) b = fb;
+  if (fb == 32 || fb == 64 || fb == 128 || fb == 256) {
+    b = fb;
+    pair = false;
+  }
   const int fs = env_int("BSG_FORCE_SPLITS", 0);
   if (fs >= 1) s = std::min(fs, nkt);
   if (b < 128) s = 1;  // narrow tiles never split K
@@ -282,10 +289,7 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   Variant v;
   v.cmn = 1;
   v.cmm = 1;
-  // The CTA-pair kernel (256 x 256 tiles over 2-CTA clusters) is selected only on request
-  // (BSG_FORCE_PAIR=1) for now: measured on GB300 it is slower than the 1-SM kernel at 8192^3
-  // (load delivery per k-tile and, for NVFP4, 12 scale copies per k-tile), see the design doc.
-  v.pair = false;
+  v.pair = pair && env_int("BSG_FORCE_SPLITS", 0) == 0;
   const int fp = env_int("BSG_FORCE_PAIR", -1);
   if (fp == 0 || fp == 1) v.pair = fp == 1;
   if (v.pair) {
@@ -301,7 +305,7 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   v.kps = k;
   // multicast cluster (split-K off): A shared by cmn n-tiles, B by cmm m-tiles; each at most the
   // number of such tiles (power of two), and the cluster at most 8 CTAs
-  int cmn = b < 128 ? 4 : 1, cmm = 1;
+  int cmn = 1, cmm = 1;
   const int fc = env_int("BSG_FORCE_CM", 0);
   if (fc == 1 || fc == 2 || fc == 4 || fc == 8) cmn = fc;
   const int fm = env_int("BSG_FORCE_CMM", 0);
