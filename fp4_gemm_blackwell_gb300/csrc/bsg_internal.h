@@ -54,6 +54,8 @@ struct GemmParams {
   int k_tiles_per_split;
   int num_units;           // num_tiles * splits
   int group_m;             // tile rasterisation: m-blocks per group
+  int ring_stages;         // shared-memory ring stages in use (the kernel's maximum, or fewer to
+                           // make room for split-K receive slots)
   // Multicast clusters: cm = cmn x cmm CTAs (1 = none) take a block of cmm m-tiles x cmn n-tiles;
   // the cmn CTAs of one m-tile share (multicast) its A tile, the cmm CTAs of one n-tile its B tile.
   int cm, cmn, cmm;
@@ -67,7 +69,8 @@ struct GemmKernelInfo {
   int smem_bytes;
   int threads;
   int bn;
-  int stages;
+  int stages;       // ring stages
+  int stage_bytes;  // bytes of one ring stage
 };
 
 // Look up a kernel instantiation: tile width bn (32, 64, 128 or 256), out (OUT_*).

@@ -245,58 +245,47 @@ __device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, const float
   return make_uint2(pack2<OUT>(y[0], y[1]), pack2<OUT>(y[2], y[3]));
 }
 
-// Split-K through a cluster: the splits of one tile are the CTAs of one cluster.  Each CTA
-// holds its FP32 partial tile in shared memory as [128 rows][BN + 4] floats, owns the row slab
-// [split * 128/S, (split + 1) * 128/S), and has pushed every other slab to the CTA that owns
-// it (bulk copies into that CTA's receive slots, [S - 1][128/S][BN + 4] floats after the
-// partial tile).  Here the owner sums its slab over the S splits in split order
-// (deterministic), from local shared memory only, applies the epilogue and stores whole rows
-// (each lane 4 consecutive columns per 128).  The 8 epilogue warps take 16/S rows each.
+// Split-K through a cluster, owner side: the S partial slabs of this CTA's 128/S rows are in
+// shared memory, slot sp = split sp, [128/S rows][BN + 4] floats each.  The owner sums them in
+// split order (deterministic), applies the epilogue and stores whole rows (each lane 4
+// consecutive columns per 128).  The 8 epilogue warps take 16/S rows each.
 template <int OUT, int BN, int S>
-__device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const float* part, const float* recv,
-                                                 const UnitCoord& c, float alpha, int ew, int lane) {
+__device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const float* slabs, const UnitCoord& c,
+                                                 float alpha, const uint2 (&braw)[BN / 128], int ew, int lane) {
   constexpr int R = 128 / S;
   constexpr int RW = R / 8;
-#pragma unroll 1
+#pragma unroll
   for (int h = 0; h < BN / 128; ++h) {
     const int col = h * 128 + 4 * lane;
     const int n = c.n_blk * BN + col;
-    uint2 braw = make_uint2(0u, 0u);
-    if ((p.flags & F_BIAS) && n < p.N)
-      braw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
 #pragma unroll
     for (int r = 0; r < RW; ++r) {
       const int rl = ew + 8 * r;  // row within the slab
-      const int row = c.split * R + rl;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc = *reinterpret_cast<const float4*>(slabs + rl * (BN + 4) + col);
 #pragma unroll
-      for (int sp = 0; sp < S; ++sp) {
-        const float* src = sp == c.split ? part + row * (BN + 4)
-                                         : recv + ((sp < c.split ? sp : sp - 1) * R + rl) * (BN + 4);
-        const float4 t = *reinterpret_cast<const float4*>(src + col);
-        if (sp == 0) {
-          acc = t;
-        } else {
-          acc.x += t.x;
-          acc.y += t.y;
-          acc.z += t.z;
-          acc.w += t.w;
-        }
+      for (int sp = 1; sp < S; ++sp) {
+        const float4 t = *reinterpret_cast<const float4*>(slabs + (sp * R + rl) * (BN + 4) + col);
+        acc.x += t.x;
+        acc.y += t.y;
+        acc.z += t.z;
+        acc.w += t.w;
       }
+      // slab row rl holds tile row (rl / LPO) * 32 + split * LPO + rl % LPO, LPO = 32 / S
+      const int row = (rl / (32 / S)) * 32 + c.split * (32 / S) + rl % (32 / S);
       const int m = c.m_blk * 128 + row;
       if (m < p.M && n < p.N)  // N % 16 == 0: groups of 4 are whole
         *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N + n) =
-            epi4_with_bias<OUT>(p, acc, braw, alpha);
+            epi4_with_bias<OUT>(p, acc, braw[h], alpha);
     }
   }
 }
 
 template <int OUT, int BN>
-__device__ __forceinline__ void cluster_reduce(const GemmParams& p, const float* part, const float* recv,
-                                               const UnitCoord& c, float alpha, int ew, int lane) {
-  if (p.splits == 2) cluster_reduce_s<OUT, BN, 2>(p, part, recv, c, alpha, ew, lane);
-  else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4>(p, part, recv, c, alpha, ew, lane);
-  else cluster_reduce_s<OUT, BN, 8>(p, part, recv, c, alpha, ew, lane);
+__device__ __forceinline__ void cluster_reduce(const GemmParams& p, const float* slabs, const UnitCoord& c,
+                                               float alpha, const uint2 (&braw)[BN / 128], int ew, int lane) {
+  if (p.splits == 2) cluster_reduce_s<OUT, BN, 2>(p, slabs, c, alpha, braw, ew, lane);
+  else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4>(p, slabs, c, alpha, braw, ew, lane);
+  else cluster_reduce_s<OUT, BN, 8>(p, slabs, c, alpha, braw, ew, lane);
 }
 
 // Word t of the result is word (t + r) % 4 of v (r uniform across the warp).
@@ -366,11 +355,12 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // Split-K cluster: the peers push their row slabs into this CTA's ring memory, so one cluster
-  // barrier phase separates "every CTA's MMAs are done and its partial tile is in shared
-  // memory" (epilogue threads arrive then; the other threads when their role ends) from the
-  // pushes; a second phase at teardown keeps every CTA alive until its slabs have been read.
-  bool cluster_waited = false;  // this thread has completed the first phase
+  // Split-K cluster: the peers store partial rows into this CTA's receive slots (shared memory
+  // past the ring stages in use), so every CTA announces at start-up that its barriers are
+  // initialised (fence.mbarrier_init above); a thread waits for the announcements before its
+  // first remote store, or at teardown.
+  bool cluster_waited = false;  // this thread has completed the start-up cluster barrier
+  if (p.split_mode == SPLIT_CLUSTER) cluster_arrive_relaxed();
   // Multicast cluster: no CTA may write into a peer's ring or arrive on its barriers before the
   // peer has initialised them.
   if (p.cm > 1) cluster_sync();
@@ -385,6 +375,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
   const uint16_t amask = static_cast<uint16_t>(row_mask), bmask = static_cast<uint16_t>(col_mask);
   const uint16_t cmask = static_cast<uint16_t>(row_mask | col_mask);
   const uint32_t tmem_base = *tmem_slot;
+  const int nst = p.ring_stages;  // ring stages in use (fewer than STAGES with a split-K cluster)
   // Everything above touched only this CTA's own resources; from here on global memory is
   // read and written, so wait for the preceding grid in the stream (programmatic dependent
   // launch), and let the next grid start its launch while this one runs.
@@ -433,7 +424,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
               }
             }
             first = false;
-            if (++stage == C::STAGES) {
+            if (++stage == nst) {
               stage = 0;
               phase ^= 1u;
             }
@@ -442,9 +433,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
         if (ok && p.cm > 1) {
           // Wait until every consumer of the cluster has released the last fill of each stage:
           // no peer's release may arrive at this CTA's barriers after it has exited.
-          for (int i = 0; i < C::STAGES; ++i) {
+          for (int i = 0; i < nst; ++i) {
             if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) break;
-            if (++stage == C::STAGES) {
+            if (++stage == nst) {
               stage = 0;
               phase ^= 1u;
             }
@@ -498,7 +489,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
               }
             }
             first = false;
-            if (++stage == C::STAGES) {
+            if (++stage == nst) {
               stage = 0;
               phase ^= 1u;
             }
@@ -551,7 +542,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
               tc_commit_mc(bar_empty(stage), cmask);  // every CTA whose copies reach this stage
             else
               tc_commit(bar_empty(stage));
-            if (++stage == C::STAGES) {
+            if (++stage == nst) {
               stage = 0;
               phase ^= 1u;
             }
@@ -654,7 +645,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_full(stage));
-        if (++stage == C::STAGES) {
+        if (++stage == nst) {
           stage = 0;
           phase ^= 1u;
         }
@@ -725,43 +716,58 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
         }
       } else if constexpr (BN >= 128) {  // split-K is planned for 128- and 256-wide tiles only
         if (p.split_mode == SPLIT_CLUSTER) {
-          // partial tile -> this CTA's shared memory (the ring is idle: the unit's MMAs are done)
-          float* part = reinterpret_cast<float*>(smem);
+          // Split-K through the cluster (one unit per CTA).  Row `row` of the tile belongs to
+          // split owner = lane / (32/S), so every warp holds rows of every owner.  Each thread
+          // streams its partial row from TMEM through registers into slot `split` of the owner's
+          // receive area: a peer's with st.async (counted on the peer's receive barrier), its own
+          // with plain stores.  The receive area, S slots of 128/S rows, lies past the ring
+          // stages in use, so peers write it while this CTA may still be running its MMAs.  Then
+          // all epilogue threads of the owner sum the S slots in split order (deterministic) and
+          // store whole rows.
+          const int S = p.splits, LPO = 32 / S, R = 128 / S;
+          const int owner = lane / LPO;
+          const int lr = q * LPO + lane % LPO;  // row within the owner's slab
+          const uint32_t slab_bytes = static_cast<uint32_t>(R * (BN + 4) * 4);
+          const uint32_t recv0 = smem0 + static_cast<uint32_t>(nst * C::STAGE_BYTES);
+          uint2 braw[BN / 128];  // bias of the columns this thread reduces, loaded early
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            const int n = nbase + h * 128 + 4 * lane;
+            braw[h] = make_uint2(0u, 0u);
+            if ((p.flags & F_BIAS) && n < p.N)
+              braw[h] = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
+          }
+          if (threadIdx.x == C::EPI_WARP0 * 32)
+            mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>((S - 1) * R * BN * 4));
+          cluster_wait();  // every CTA of the cluster has initialised its receive barrier
+          cluster_waited = true;
+          const uint32_t off = static_cast<uint32_t>(c.split) * slab_bytes +
+                               static_cast<uint32_t>((lr * (BN + 4) + col0) * 4);
+          const bool mine = owner == c.split;
+          const uint32_t dst = mine ? recv0 + off : mapa_shared(recv0 + off, static_cast<uint32_t>(owner));
+          const uint32_t rbar = mine ? 0u : mapa_shared(bar_recv, static_cast<uint32_t>(owner));
 #pragma unroll 1
           for (int ch = 0; ch < HC / 32; ++ch) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
             tmem_ld_wait();
-            float4* dst = reinterpret_cast<float4*>(part + row * (BN + 4) + col0 + ch * 32);
 #pragma unroll
-            for (int g = 0; g < 8; ++g)
-              dst[g] = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                   __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+            for (int g = 0; g < 8; ++g) {
+              const uint32_t a = dst + static_cast<uint32_t>((ch * 32 + 4 * g) * 4);
+              if (mine)
+                sts_u4(a, make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]));
+              else
+                st_async_v4(a, __uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]), rbar);
+            }
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(acc));
-          fence_proxy_async_smem();  // the partial tile is read next by bulk copies
-          cluster_arrive();          // this CTA's ring is idle and its partial tile complete
-          cluster_wait();            // ... and so are all the peers'
-          cluster_waited = true;
-          named_bar_sync(1, C::EPI_THREADS);
-          const int S = p.splits, R = 128 / S;
-          const uint32_t slab = static_cast<uint32_t>(R * (BN + 4) * 4);
-          const uint32_t recv0 = smem0 + 128 * (BN + 4) * 4;
-          if (threadIdx.x == C::EPI_WARP0 * 32) {
-            mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(S - 1) * slab);
-            for (int r = 0; r < S; ++r) {
-              if (r == c.split) continue;
-              const int slot = c.split < r ? c.split : c.split - 1;  // this CTA's slot at CTA r
-              bulk_copy_s2c(mapa_shared(recv0 + slot * slab, static_cast<uint32_t>(r)), smem0 + r * slab, slab,
-                            mapa_shared(bar_recv, static_cast<uint32_t>(r)));
-            }
-          }
           const bool got = named_bar_and(1, C::EPI_THREADS,
                                          wait_bounded_cluster(bar_recv, 0, abort_flag, p, ST_TIMEOUT_EPILOGUE));
           if (got)
-            cluster_reduce<OUT, BN>(p, part, reinterpret_cast<const float*>(smem + 128 * (BN + 4) * 4), c, alpha,
+            cluster_reduce<OUT, BN>(p, reinterpret_cast<const float*>(smem + nst * C::STAGE_BYTES), c, alpha, braw,
                                     warp - C::EPI_WARP0, lane);
         } else {
           // FP32 partial tile -> workspace as float4 [chunk][8][128 rows] (coalesced per warp)
@@ -829,15 +835,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
 
   // ------------------------------------------------------------ split-K cluster: lifetime
   if (p.split_mode == SPLIT_CLUSTER) {
-    // Every thread completes the first phase (the epilogue threads did before pushing), then
-    // a second one: a CTA leaves only after every CTA has received all its slabs, i.e. after
-    // every copy that reads this CTA's shared memory has completed.
-    if (!cluster_waited) {
-      cluster_arrive_relaxed();
-      cluster_wait();
-    }
-    __syncwarp();
-    cluster_sync();
+    // Every thread completes the start-up barrier (the epilogue threads did before storing).  No
+    // CTA needs to outlive another: a CTA leaves after its receive barrier saw every byte sent
+    // to it, and what it sent came from registers.
+    if (!cluster_waited) cluster_wait();
   } else if (p.cm > 1) {
     // multicast cluster: leave together, once no CTA issues further copies into the others
     __syncwarp();
@@ -868,6 +869,7 @@ bool fill_kernel_info(GemmKernelInfo* info) {
   info->threads = C::THREADS;
   info->bn = BN;
   info->stages = C::STAGES;
+  info->stage_bytes = C::STAGE_BYTES;
   return true;
 }
 

@@ -428,6 +428,7 @@ bool fill_pair_kernel_info(GemmKernelInfo* info) {
   info->threads = C::THREADS;
   info->bn = C::BN;
   info->stages = C::STAGES;
+  info->stage_bytes = C::STAGE_BYTES;
   return true;
 }
 

@@ -322,10 +322,9 @@ Variant choose_variant(const bsg_desc* d, int sms) {
     v.cluster = cmn * cmm;
     return v;
   }
-  // A cluster split keeps the partial tile and the peers' row slabs in the ring's shared
-  // memory: 128 x (bn + 4) floats plus (s - 1) slabs of 128/s rows, which for 256-wide tiles
-  // only fits with s = 2.
-  const bool cluster_ok = (s == 2 || s == 4 || s == 8) && (b == 128 || s == 2);
+  // A cluster split keeps 128 x (bn + 4) floats of partial rows in shared memory next to the
+  // ring, which leaves a 128-wide tile four stages and a 256-wide tile too few.
+  const bool cluster_ok = (s == 2 || s == 4 || s == 8) && b == 128;
   v.mode = s == 1 ? bsg::SPLIT_NONE
                   : (cluster_ok && env_int("BSG_SPLIT_WORKSPACE", 0) == 0 ? bsg::SPLIT_CLUSTER
                                                                            : bsg::SPLIT_WORKSPACE);
@@ -364,8 +363,8 @@ bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, u
 // Kernel parameters of problem d under variant v (tensor maps encoded here), except the
 // workspace pointers.  Grid: persistent (<= #SMs) unless the splits form clusters, in which
 // case every unit is its own CTA.
-bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, int sms, int resident_ctas,
-                       int* grid) {
+bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, const bsg::GemmKernelInfo& info,
+                       int sms, int resident_ctas, int* grid) {
   std::memset(g, 0, sizeof(*g));
   const size_t rb = code_row_bytes(d->kind, d->K);
   bsg_status s;
@@ -404,6 +403,15 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->num_units = g->num_m_groups * g->num_n_groups * v.splits;
   g->group_m = 16;
   g->debug_skip_first_load = 0;
+  g->ring_stages = info.stages;
+  if (v.mode == bsg::SPLIT_CLUSTER) {
+    // the split-K receive area, splits x (128 / splits) rows x (bn + 4) floats, takes the place
+    // of the last ring stages
+    const long long recv = 128LL * (v.bn + 4) * 4;
+    g->ring_stages = info.stages - static_cast<int>((recv + info.stage_bytes - 1) / info.stage_bytes);
+    if (g->ring_stages < 2)
+      return fail(BSG_ERR_SHAPE, "split-K cluster receive slots leave fewer than two ring stages");
+  }
   if (v.pair) *grid = 2 * std::min(g->num_units, sms / 2);
   else if (g->cm > 1) *grid = g->cm * std::min(g->num_units, resident_ctas / g->cm);
   else *grid = v.mode == bsg::SPLIT_CLUSTER ? g->num_units : std::min(g->num_units, sms);
@@ -473,7 +481,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   p->workspace = nullptr;
   p->cluster = v.cluster;
   bsg::GemmParams& g = p->params;
-  if ((s = fill_params(&g, d, v, di.sms, resident, &p->grid)) != BSG_OK) {
+  if ((s = fill_params(&g, d, v, info, di.sms, resident, &p->grid)) != BSG_OK) {
     delete p;
     return s;
   }
@@ -502,7 +510,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
     char mc[24] = "";
     if (v.cmn * v.cmm > 1) std::snprintf(mc, sizeof(mc), v.cmm > 1 ? "_mc%dx%d" : "_mc%d", v.cmn, v.cmm);
     std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
-                  v.bn, v.splits, kModeName[v.mode], mc, info.stages, p->grid);
+                  v.bn, v.splits, kModeName[v.mode], mc, g.ring_stages, p->grid);
   }
   if (env_int("BSG_LOG", 0))
     std::fprintf(stderr, "[bsgemm] plan M=%d N=%d K=%d -> %s\n", d->M, d->N, d->K, p->variant);
@@ -794,7 +802,7 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
 
   bsg::GemmParams g;
   int grid = 0;
-  if ((s = fill_params(&g, d, v, di.sms, resident, &grid)) != BSG_OK) return s;
+  if ((s = fill_params(&g, d, v, info, di.sms, resident, &grid)) != BSG_OK) return s;
   g.status = reinterpret_cast<unsigned*>(scratch);
   g.counters = reinterpret_cast<unsigned*>(scratch + w.cnt_off);
   g.partial = w.part_bytes ? reinterpret_cast<float*>(scratch + w.part_off) : nullptr;

@@ -62,7 +62,7 @@ def test_ragged_shapes(kind, M, N, K):
 
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
-@pytest.mark.parametrize("bn,splits,mode", [(128, 1, ""), (256, 1, ""), (128, 3, "w"), (256, 2, "c"), (128, 7, "w"),
+@pytest.mark.parametrize("bn,splits,mode", [(128, 1, ""), (256, 1, ""), (128, 3, "w"), (256, 2, "w"), (128, 7, "w"),
                                             (128, 4, "c"), (128, 8, "c"), (256, 4, "w")])
 def test_forced_variants(kind, bn, splits, mode, monkeypatch):
     env = {"BSG_FORCE_BN": bn, "BSG_FORCE_SPLITS": splits}
@@ -74,7 +74,7 @@ def test_forced_variants(kind, bn, splits, mode, monkeypatch):
     nkt = K // (128 if kind == "mxfp8" else 256)
     kps = -(-nkt // splits)
     s = -(-nkt // kps)
-    m = "" if s == 1 else ("w" if mode == "w" or s not in (2, 4, 8) or (bn == 256 and s > 2) else "c")
+    m = "" if s == 1 else ("w" if mode == "w" or s not in (2, 4, 8) or bn == 256 else "c")
     assert "_bn%d_s%d%s_" % (bn, s, m) in v
 
 
