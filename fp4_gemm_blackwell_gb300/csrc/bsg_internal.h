@@ -71,6 +71,7 @@ struct GemmKernelInfo {
   int bn;
   int stages;       // ring stages
   int stage_bytes;  // bytes of one ring stage
+  int kc;           // k-tiles (128 bytes of K) per ring stage
 };
 
 // Look up a kernel instantiation: tile width bn (32, 64, 128 or 256), out (OUT_*).
@@ -79,7 +80,7 @@ bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info);
 bool gemm_kernel_info_mx_narrow(int bn, int out, GemmKernelInfo* info);  // bn 32 or 64
 bool gemm_kernel_info_nv_narrow(int bn, int out, GemmKernelInfo* info);
 // CTA-pair kernels (256 x 256 pair tiles, launched in clusters of 2).
-bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info);
+bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info);  // BSG_PAIR_KC=1 or 2 (default 2)
 bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info);
 
 // Quantisers (stream-ordered).  See bsg_quantize in include/bsgemm.h.

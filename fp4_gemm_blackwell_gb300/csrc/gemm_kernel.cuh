@@ -870,6 +870,7 @@ bool fill_kernel_info(GemmKernelInfo* info) {
   info->bn = BN;
   info->stages = C::STAGES;
   info->stage_bytes = C::STAGE_BYTES;
+  info->kc = 1;
   return true;
 }
 

@@ -13,8 +13,8 @@ bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info) {
 }
 
 bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info) {
-  if (out == OUT_F16) return fill_pair_kernel_info<KIND_NV, OUT_F16>(info);
-  if (out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, OUT_BF16>(info);
+  if (out == OUT_F16) return fill_pair_kernel_info<KIND_NV, 1, OUT_F16>(info);
+  if (out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, 1, OUT_BF16>(info);
   return false;
 }
 

@@ -27,17 +27,20 @@
 
 namespace bsg {
 
-template <int KIND>
+// KC = k-tiles of 128 bytes of K per ring stage (one wait and one commit per stage).
+template <int KIND, int KC>
 struct PairCfg {
   static constexpr int BM = 128;  // A rows per CTA (pair tile: 256)
   static constexpr int BN = 256;  // pair tile width; each CTA loads 128 rows of B
   static constexpr int BK_BYTES = 128;
-  static constexpr int K_TILE = KIND == KIND_MX ? 128 : 256;
+  static constexpr int K_TILE = KC * (KIND == KIND_MX ? 128 : 256);  // elements per stage
   static constexpr int MMA_K = KIND == KIND_MX ? 32 : 64;
-  static constexpr int STEPS = K_TILE / MMA_K;
-  static constexpr int SF_ATOMS = KIND == KIND_MX ? 1 : 4;
-  static constexpr int A_BYTES = BM * BK_BYTES;
-  static constexpr int B_BYTES = 128 * BK_BYTES;
+  static constexpr int STEPS = K_TILE / MMA_K;                        // 4 MMAs per 128-byte slab
+  static constexpr int SF_ATOMS = KC * (KIND == KIND_MX ? 1 : 4);     // per 128-row band per stage
+  static constexpr int SLAB_A = BM * BK_BYTES;                        // one 128-byte k-slab of A
+  static constexpr int SLAB_B = 128 * BK_BYTES;
+  static constexpr int A_BYTES = KC * SLAB_A;
+  static constexpr int B_BYTES = KC * SLAB_B;
   static constexpr int SFA_BYTES = SF_ATOMS * 512;
   static constexpr int SFB_BYTES = 2 * SF_ATOMS * 512;  // both 128-row bands of the tile's B
   static constexpr int STAGE_RAW = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -65,12 +68,13 @@ struct PairCfg {
       (KIND == KIND_MX ? ((0u << 7) | (0u << 10) | (1u << 23)) : ((1u << 7) | (1u << 10) | (0u << 23))) |
       (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
   static_assert(STAGES >= 2 && STAGES <= 8, "ring");
+  static_assert(SF_ATOMS <= 4, "scale-warp stores");
   static_assert(TMEM_USED <= TMEM_COLS, "tensor memory");
 };
 
-template <int KIND, int OUT>
-__global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
-  using C = PairCfg<KIND>;
+template <int KIND, int KC, int OUT>
+__global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  using C = PairCfg<KIND, KC>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
@@ -157,9 +161,13 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
               // code tiles of both CTAs: one transaction on the leader's barrier
               const uint32_t fb = mapa_shared(bar_full(stage), leader);
               if (is_leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (C::A_BYTES + C::B_BYTES));
-              tma_load_2d_pair(stage_a(stage), &p.tmap_a, fb, kt * C::BK_BYTES, m_blk * C::BM);
-              tma_load_2d_pair(stage_b(stage), &p.tmap_b, fb, kt * C::BK_BYTES,
-                               c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128);
+#pragma unroll
+              for (int j = 0; j < KC; ++j) {  // slabs past K read as zeros (their MMAs are skipped)
+                const int x = (kt * KC + j) * C::BK_BYTES;
+                tma_load_2d_pair(stage_a(stage) + j * C::SLAB_A, &p.tmap_a, fb, x, m_blk * C::BM);
+                tma_load_2d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x,
+                                 c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128);
+              }
             }
             first = false;
             if (++stage == C::STAGES) {
@@ -192,7 +200,7 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
             }
             const int k_rem = p.K - kt * C::K_TILE;
             const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
-            const int sf_atoms = KIND == KIND_MX ? 1 : steps;
+            const int sf_atoms = KIND == KIND_MX ? (steps + 3) / 4 : steps;  // atoms K still covers
             if (first && p.debug_skip_first_load) {
               // test hook (see the code producer)
             } else {
@@ -247,16 +255,23 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
             const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS;
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
             const uint32_t sa = stage_a(stage), sb = stage_b(stage);
+            // MMA j reads 32 bytes of K at offset 32 (j % 4) of slab j / 4; its scales are in atom
+            // j / 4 (MXFP8, byte j % 4 of each word) or atom j (NVFP4)
             if constexpr (KIND == KIND_MX) {
               for (int j = 0; j < steps; ++j) {
-                const uint32_t idesc = C::IDESC | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
-                tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j), idesc,
-                                 sfa_t, sfb_t, (kt > c.kt0 || j > 0) ? 1u : 0u);
+                const uint32_t jj = static_cast<uint32_t>(j & 3), slab = static_cast<uint32_t>(j >> 2);
+                const uint32_t idesc = C::IDESC | (jj << 4) | (jj << 29);
+                tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + slab * C::SLAB_A + 32 * jj),
+                                 sdesc_kmajor_sw128(sb + slab * C::SLAB_B + 32 * jj), idesc, sfa_t + 4 * slab,
+                                 sfb_t + 8 * slab, (kt > c.kt0 || j > 0) ? 1u : 0u);
               }
             } else {
-              for (int j = 0; j < steps; ++j)
-                tc_mma_nvf4_pair(tmem_base, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
-                                 C::IDESC, sfa_t + 4 * j, sfb_t + 8 * j, (kt > c.kt0 || j > 0) ? 1u : 0u);
+              for (int j = 0; j < steps; ++j) {
+                const uint32_t jj = static_cast<uint32_t>(j & 3), slab = static_cast<uint32_t>(j >> 2);
+                tc_mma_nvf4_pair(tmem_base, sdesc_kmajor_sw128(sa + slab * C::SLAB_A + 32 * jj),
+                                 sdesc_kmajor_sw128(sb + slab * C::SLAB_B + 32 * jj), C::IDESC, sfa_t + 4 * j,
+                                 sfb_t + 8 * j, (kt > c.kt0 || j > 0) ? 1u : 0u);
+              }
             }
             tc_commit_pair_mc(bar_empty(stage), pair_mask);
             if (++stage == C::STAGES) {
@@ -284,8 +299,8 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
     setmaxnreg_dec<C::REGS_SCALE>();
     // ------------------------------------------------------------ scale warps (each CTA)
     // The layout a 32x128b.warpx4 copy of the atoms produces, per stage slot: lane i, column
-    // 4j + k holds the four scales of A row 32k + i of atom j (this CTA's 128 rows), and column
-    // 8j + 4b + k those of B row 128b + 32k + i (the pair tile's 256 rows).
+    // 4t + k holds the four scales of A row 32k + i of atom t (this CTA's 128 rows), and column
+    // 8t + 4b + k those of B row 128b + 32k + i (the pair tile's 256 rows).
     const int q = warp & 3;
     const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
     int stage = 0;
@@ -297,39 +312,26 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
         ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
         if (!ok) break;
         const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
-        if constexpr (KIND == KIND_MX) {
-          const uint4 va = lds_u4(stage_sfa(stage) + 16 * lane);
-          const uint4 vb0 = lds_u4(stage_sfb(stage) + 16 * lane);
-          const uint4 vb1 = lds_u4(stage_sfb(stage) + 512 + 16 * lane);
-          const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
-          const uint32_t wb[8] = {vb0.x, vb0.y, vb0.z, vb0.w, vb1.x, vb1.y, vb1.z, vb1.w};
-          tmem_st_32x32b_x4(slot, wa);
-          tmem_st_32x32b_x8(slot + C::SFA_COLS, wb);
-        } else {
-          uint32_t a[16];
+        constexpr int NA = C::SF_ATOMS;
+        uint32_t a[4 * NA], b[8 * NA];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 v = lds_u4(stage_sfa(stage) + 512 * j + 16 * lane);
-            a[4 * j] = v.x;
-            a[4 * j + 1] = v.y;
-            a[4 * j + 2] = v.z;
-            a[4 * j + 3] = v.w;
+        for (int t = 0; t < NA; ++t) {
+          const uint4 v = lds_u4(stage_sfa(stage) + 512 * t + 16 * lane);
+          a[4 * t] = v.x;
+          a[4 * t + 1] = v.y;
+          a[4 * t + 2] = v.z;
+          a[4 * t + 3] = v.w;
+#pragma unroll
+          for (int rb = 0; rb < 2; ++rb) {
+            const uint4 w = lds_u4(stage_sfb(stage) + rb * NA * 512 + 512 * t + 16 * lane);
+            b[(2 * t + rb) * 4] = w.x;
+            b[(2 * t + rb) * 4 + 1] = w.y;
+            b[(2 * t + rb) * 4 + 2] = w.z;
+            b[(2 * t + rb) * 4 + 3] = w.w;
           }
-          tmem_st_32x32b_x16(slot, a);
-          uint32_t b[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-#pragma unroll
-            for (int rb = 0; rb < 2; ++rb) {
-              const uint4 v = lds_u4(stage_sfb(stage) + rb * C::SF_ATOMS * 512 + 512 * j + 16 * lane);
-              b[(2 * j + rb) * 4] = v.x;
-              b[(2 * j + rb) * 4 + 1] = v.y;
-              b[(2 * j + rb) * 4 + 2] = v.z;
-              b[(2 * j + rb) * 4 + 3] = v.w;
-            }
-          }
-          tmem_st_32x32b_x32(slot + C::SFA_COLS, b);
         }
+        tmem_st_cols(slot, a);
+        tmem_st_cols(slot + C::SFA_COLS, b);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -420,10 +422,11 @@ __global__ void __launch_bounds__(PairCfg<KIND>::THREADS, 1) bsg_gemm_pair_kerne
   }
 }
 
-template <int KIND, int OUT>
+template <int KIND, int KC, int OUT>
 bool fill_pair_kernel_info(GemmKernelInfo* info) {
-  using C = PairCfg<KIND>;
-  info->fn = reinterpret_cast<const void*>(&bsg_gemm_pair_kernel<KIND, OUT>);
+  using C = PairCfg<KIND, KC>;
+  info->fn = reinterpret_cast<const void*>(&bsg_gemm_pair_kernel<KIND, KC, OUT>);
+  info->kc = KC;
   info->smem_bytes = C::SMEM_BYTES;
   info->threads = C::THREADS;
   info->bn = C::BN;

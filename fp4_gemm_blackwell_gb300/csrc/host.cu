@@ -390,11 +390,11 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->sfa_bands = (d->M + 127) / 128;
   g->num_m_tiles = v.pair ? (d->M + 255) / 256 : (d->M + 127) / 128;
   g->num_n_tiles = (d->N + v.bn - 1) / v.bn;
-  g->num_k_tiles = (d->K + k_tile - 1) / k_tile;
+  g->num_k_tiles = (d->K + k_tile * info.kc - 1) / (k_tile * info.kc);  // ring stages of K
   g->num_tiles = g->num_m_tiles * g->num_n_tiles;
   g->splits = v.splits;
   g->split_mode = v.mode;
-  g->k_tiles_per_split = v.kps;
+  g->k_tiles_per_split = info.kc == 1 ? v.kps : g->num_k_tiles;  // several k-tiles per stage: no split
   g->cmn = v.cmn;
   g->cmm = v.cmm;
   g->cm = v.cmn * v.cmm;

@@ -253,6 +253,16 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
       : "memory");
 }
 
+// tcgen05.st of N consecutive 32-bit columns (N = 4, 8, 16 or 32) of this warp's lane quarter.
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 4 || N == 8 || N == 16 || N == 32, "column count");
+  if constexpr (N == 4) tmem_st_32x32b_x4(taddr, r);
+  else if constexpr (N == 8) tmem_st_32x32b_x8(taddr, r);
+  else if constexpr (N == 16) tmem_st_32x32b_x16(taddr, r);
+  else tmem_st_32x32b_x32(taddr, r);
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
