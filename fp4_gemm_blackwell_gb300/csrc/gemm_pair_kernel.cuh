@@ -68,7 +68,7 @@ struct PairCfg {
       (KIND == KIND_MX ? ((0u << 7) | (0u << 10) | (1u << 23)) : ((1u << 7) | (1u << 10) | (0u << 23))) |
       (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
   static_assert(STAGES >= 2 && STAGES <= 8, "ring");
-  static_assert(SF_ATOMS <= 4, "scale-warp stores");
+  static_assert(SF_ATOMS <= 4 || SF_ATOMS % 4 == 0, "scale-warp stores");
   static_assert(TMEM_USED <= TMEM_COLS, "tensor memory");
 };
 
@@ -312,26 +312,31 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
         if (!ok) break;
         const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
+        // atoms in groups of up to four: 16 A columns and 32 B columns per group
         constexpr int NA = C::SF_ATOMS;
-        uint32_t a[4 * NA], b[8 * NA];
+        constexpr int GA = NA < 4 ? NA : 4;
 #pragma unroll
-        for (int t = 0; t < NA; ++t) {
-          const uint4 v = lds_u4(stage_sfa(stage) + 512 * t + 16 * lane);
-          a[4 * t] = v.x;
-          a[4 * t + 1] = v.y;
-          a[4 * t + 2] = v.z;
-          a[4 * t + 3] = v.w;
+        for (int g0 = 0; g0 < NA; g0 += GA) {
+          uint32_t a[4 * GA], b[8 * GA];
 #pragma unroll
-          for (int rb = 0; rb < 2; ++rb) {
-            const uint4 w = lds_u4(stage_sfb(stage) + rb * NA * 512 + 512 * t + 16 * lane);
-            b[(2 * t + rb) * 4] = w.x;
-            b[(2 * t + rb) * 4 + 1] = w.y;
-            b[(2 * t + rb) * 4 + 2] = w.z;
-            b[(2 * t + rb) * 4 + 3] = w.w;
+          for (int t = 0; t < GA; ++t) {
+            const uint4 v = lds_u4(stage_sfa(stage) + 512 * (g0 + t) + 16 * lane);
+            a[4 * t] = v.x;
+            a[4 * t + 1] = v.y;
+            a[4 * t + 2] = v.z;
+            a[4 * t + 3] = v.w;
+#pragma unroll
+            for (int rb = 0; rb < 2; ++rb) {
+              const uint4 w = lds_u4(stage_sfb(stage) + rb * NA * 512 + 512 * (g0 + t) + 16 * lane);
+              b[(2 * t + rb) * 4] = w.x;
+              b[(2 * t + rb) * 4 + 1] = w.y;
+              b[(2 * t + rb) * 4 + 2] = w.z;
+              b[(2 * t + rb) * 4 + 3] = w.w;
+            }
           }
+          tmem_st_cols(slot + 4 * g0, a);
+          tmem_st_cols(slot + C::SFA_COLS + 8 * g0, b);
         }
-        tmem_st_cols(slot, a);
-        tmem_st_cols(slot + C::SFA_COLS, b);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
