@@ -409,11 +409,24 @@ def launch_loop(bsg, calls=1000):
     kernel_us = start.elapsed_time(end) * 1e3 / calls
     bsg.bsg_cache_clear()
     del g
+    native = native_launch_loop()
     return {"calls": calls, "shapes": len(shapes), "kernel_us_per_call": round(kernel_us, 3),
+            "c_abi": native,
             "stream": {"host_us_per_call": round(host_stream, 3), "wall_us_per_call": round(wall_stream, 3),
                        "host_over_kernel": round(host_stream / kernel_us, 3)},
             "graph": {"host_us_per_call": round(host_graph, 4), "host_over_kernel": round(host_graph / kernel_us, 4)},
             "note": "host time is the enqueue time through the Python ctypes binding"}
+
+
+def native_launch_loop():
+    """The same loop from a compiled C++ caller (fp4_gemm_blackwell_gb300/bsg_launch_loop, built
+    with the library): the host cost of the C ABI itself, without the Python FFI."""
+    exe = os.path.join(ROOT, "fp4_gemm_blackwell_gb300", "bsg_launch_loop")
+    try:
+        r = subprocess.run([exe], stdout=subprocess.PIPE, stderr=subprocess.PIPE, timeout=300)
+        return json.loads(r.stdout.decode().strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: the Python-level loop above still stands
+        return {"error": str(e)[:200]}
 
 
 # ---------------------------------------------------------------- the CPU oracle

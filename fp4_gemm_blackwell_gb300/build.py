@@ -16,6 +16,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libbsgemm.so")
+# Programs built beside the library (csrc/*_main.cu, linked against it): the native
+# launch-overhead loop that bench.py runs.
+LAUNCH_LOOP = os.path.join(PKG, "bsg_launch_loop")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-I" + INCLUDE, "-I" + CSRC,
           "-Xcompiler", "-fPIC,-fvisibility=hidden"]
@@ -37,7 +40,7 @@ def build(verbose=False, force=False):
     nvcc = _nvcc()
     objdir = os.path.join(ROOT, "_build", platform.machine())
     os.makedirs(objdir, exist_ok=True)
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    sources = sorted(f for f in glob.glob(os.path.join(CSRC, "*.cu")) if not f.endswith("_main.cu"))
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(INCLUDE, "*.h"))
     hdr_time = _newest(headers)
@@ -69,6 +72,16 @@ def build(verbose=False, force=False):
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
         os.replace(tmp, LIB)
+    main_src = os.path.join(CSRC, "launch_loop_main.cu")
+    if force or not os.path.exists(LAUNCH_LOOP) or os.path.getmtime(LAUNCH_LOOP) < max(
+            os.path.getmtime(LIB), os.path.getmtime(main_src)):
+        cmd = [nvcc] + ARCH + ["-O3", "-std=c++17", "-I" + INCLUDE, "-o", LAUNCH_LOOP, main_src, "-L" + PKG,
+                               "-lbsgemm", "-Xlinker", "-rpath,$ORIGIN"]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+        if r.returncode != 0:
+            raise RuntimeError("launch loop build failed:\n" + r.stdout.decode(errors="replace"))
     return LIB
 
 

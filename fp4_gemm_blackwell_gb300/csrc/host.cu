@@ -176,6 +176,9 @@ struct bsg_plan_s {
   int cluster;
   void* workspace;
   char variant[64];
+  // launch configuration built once at plan creation (a run only sets the stream)
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attrs[2];
 };
 
 namespace {
@@ -418,11 +421,11 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   return BSG_OK;
 }
 
-bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, int threads, int smem,
-                       int cluster, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attrs[2];
+// Launch configuration: grid, block, dynamic shared memory, programmatic dependent launch
+// (unless BSG_PDL=0, read when the configuration is built) and the cluster shape.
+void make_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute (&attrs)[2], int grid, int threads, int smem,
+                        int cluster) {
+  std::memset(cfg, 0, sizeof(*cfg));
   int n = 0;
   if (env_int("BSG_PDL", 1)) {
     attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -436,16 +439,27 @@ bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, 
     attrs[n].val.clusterDim.z = 1;
     ++n;
   }
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = stream;
-  cfg.attrs = attrs;
-  cfg.numAttrs = n;
+  cfg->gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg->blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg->dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg->attrs = attrs;
+  cfg->numAttrs = n;
+}
+
+bsg_status launch_with(cudaLaunchConfig_t* cfg, const void* fn, const bsg::GemmParams& params, cudaStream_t stream) {
+  cfg->stream = stream;
   void* args[] = {const_cast<bsg::GemmParams*>(&params)};
-  const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  const cudaError_t e = cudaLaunchKernelExC(cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
   return BSG_OK;
+}
+
+bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, int threads, int smem,
+                       int cluster, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attrs[2];
+  make_launch_config(&cfg, attrs, grid, threads, smem, cluster);
+  return launch_with(&cfg, fn, params, stream);
 }
 
 bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
@@ -512,6 +526,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
     std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
                   v.bn, v.splits, kModeName[v.mode], mc, g.ring_stages, p->grid);
   }
+  make_launch_config(&p->cfg, p->attrs, p->grid, info.threads, info.smem_bytes, p->cluster);
   if (env_int("BSG_LOG", 0))
     std::fprintf(stderr, "[bsgemm] plan M=%d N=%d K=%d -> %s\n", d->M, d->N, d->K, p->variant);
   *out = p;
@@ -521,7 +536,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
 bool plan_ok(bsg_plan_t p) { return p != nullptr && p->magic == kPlanMagic; }
 
 bsg_status plan_launch(bsg_plan_t p, const bsg::GemmParams& params, cudaStream_t stream) {
-  return launch_gemm(p->info.fn, params, p->grid, p->info.threads, p->info.smem_bytes, p->cluster, stream);
+  return launch_with(&p->cfg, p->info.fn, params, stream);
 }
 
 }  // namespace
