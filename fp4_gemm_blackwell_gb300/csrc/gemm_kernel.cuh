@@ -247,45 +247,43 @@ __device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, const float
 
 // Split-K through a cluster, owner side: the S partial slabs of this CTA's 128/S rows are in
 // shared memory, slot sp = split sp, [128/S rows][BN + 4] floats each.  The owner sums them in
-// split order (deterministic), applies the epilogue and stores whole rows (each lane 4
-// consecutive columns per 128).  The 8 epilogue warps take 16/S rows each.
+// split order (deterministic), applies the epilogue and stores whole rows: epilogue thread t
+// takes column group c4 = t % (BN/4) (4 consecutive columns) of rows t / (BN/4), + 1024/BN, ...
 template <int OUT, int BN, int S>
 __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const float* slabs, const UnitCoord& c,
-                                                 float alpha, const uint2 (&braw)[BN / 128], int ew, int lane) {
+                                                 float alpha, uint2 braw, int t) {
   constexpr int R = 128 / S;
-  constexpr int RW = R / 8;
+  constexpr int C4 = BN / 4;          // column groups per row
+  constexpr int RP = 256 / C4;        // rows per pass of the 256 epilogue threads
+  const int c4 = t % C4;
+  const int col = 4 * c4;
+  const int n = c.n_blk * BN + col;
 #pragma unroll
-  for (int h = 0; h < BN / 128; ++h) {
-    const int col = h * 128 + 4 * lane;
-    const int n = c.n_blk * BN + col;
+  for (int rl = t / C4; rl < R; rl += RP) {
+    float4 acc = *reinterpret_cast<const float4*>(slabs + rl * (BN + 4) + col);
 #pragma unroll
-    for (int r = 0; r < RW; ++r) {
-      const int rl = ew + 8 * r;  // row within the slab
-      float4 acc = *reinterpret_cast<const float4*>(slabs + rl * (BN + 4) + col);
-#pragma unroll
-      for (int sp = 1; sp < S; ++sp) {
-        const float4 t = *reinterpret_cast<const float4*>(slabs + (sp * R + rl) * (BN + 4) + col);
-        acc.x += t.x;
-        acc.y += t.y;
-        acc.z += t.z;
-        acc.w += t.w;
-      }
-      // slab row rl holds tile row (rl / LPO) * 32 + split * LPO + rl % LPO, LPO = 32 / S
-      const int row = (rl / (32 / S)) * 32 + c.split * (32 / S) + rl % (32 / S);
-      const int m = c.m_blk * 128 + row;
-      if (m < p.M && n < p.N)  // N % 16 == 0: groups of 4 are whole
-        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N + n) =
-            epi4_with_bias<OUT>(p, acc, braw[h], alpha);
+    for (int sp = 1; sp < S; ++sp) {
+      const float4 v = *reinterpret_cast<const float4*>(slabs + (sp * R + rl) * (BN + 4) + col);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
     }
+    // slab row rl holds tile row (rl / LPO) * 32 + split * LPO + rl % LPO, LPO = 32 / S
+    const int row = (rl / (32 / S)) * 32 + c.split * (32 / S) + rl % (32 / S);
+    const int m = c.m_blk * 128 + row;
+    if (m < p.M && n < p.N)  // N % 16 == 0: groups of 4 are whole
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N + n) =
+          epi4_with_bias<OUT>(p, acc, braw, alpha);
   }
 }
 
 template <int OUT, int BN>
 __device__ __forceinline__ void cluster_reduce(const GemmParams& p, const float* slabs, const UnitCoord& c,
-                                               float alpha, const uint2 (&braw)[BN / 128], int ew, int lane) {
-  if (p.splits == 2) cluster_reduce_s<OUT, BN, 2>(p, slabs, c, alpha, braw, ew, lane);
-  else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4>(p, slabs, c, alpha, braw, ew, lane);
-  else cluster_reduce_s<OUT, BN, 8>(p, slabs, c, alpha, braw, ew, lane);
+                                               float alpha, uint2 braw, int t) {
+  if (p.splits == 2) cluster_reduce_s<OUT, BN, 2>(p, slabs, c, alpha, braw, t);
+  else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4>(p, slabs, c, alpha, braw, t);
+  else cluster_reduce_s<OUT, BN, 8>(p, slabs, c, alpha, braw, t);
 }
 
 // Word t of the result is word (t + r) % 4 of v (r uniform across the warp).
@@ -714,7 +712,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
                   make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
           }
         }
-      } else if constexpr (BN >= 128) {  // split-K is planned for 128- and 256-wide tiles only
+      } else if constexpr (BN >= 64) {  // split-K is planned for tiles 64 columns wide or more
         if (p.split_mode == SPLIT_CLUSTER) {
           // Split-K through the cluster (one unit per CTA).  Row `row` of the tile belongs to
           // split owner = lane / (32/S), so every warp holds rows of every owner.  Each thread
@@ -729,13 +727,12 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
           const int lr = q * LPO + lane % LPO;  // row within the owner's slab
           const uint32_t slab_bytes = static_cast<uint32_t>(R * (BN + 4) * 4);
           const uint32_t recv0 = smem0 + static_cast<uint32_t>(nst * C::STAGE_BYTES);
-          uint2 braw[BN / 128];  // bias of the columns this thread reduces, loaded early
-#pragma unroll
-          for (int h = 0; h < BN / 128; ++h) {
-            const int n = nbase + h * 128 + 4 * lane;
-            braw[h] = make_uint2(0u, 0u);
+          const int et = threadIdx.x - C::EPI_WARP0 * 32;  // epilogue thread index
+          uint2 braw = make_uint2(0u, 0u);  // bias of the columns this thread reduces, loaded early
+          {
+            const int n = nbase + 4 * (et % (BN / 4));
             if ((p.flags & F_BIAS) && n < p.N)
-              braw[h] = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
+              braw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
           }
           if (threadIdx.x == C::EPI_WARP0 * 32)
             mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>((S - 1) * R * BN * 4));
@@ -768,7 +765,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
                                          wait_bounded_cluster(bar_recv, 0, abort_flag, p, ST_TIMEOUT_EPILOGUE));
           if (got)
             cluster_reduce<OUT, BN>(p, reinterpret_cast<const float*>(smem + nst * C::STAGE_BYTES), c, alpha, braw,
-                                    warp - C::EPI_WARP0, lane);
+                                    et);
         } else {
           // FP32 partial tile -> workspace as float4 [chunk][8][128 rows] (coalesced per warp)
           float4* part = reinterpret_cast<float4*>(

@@ -275,18 +275,34 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   } else if (nkt <= 4) {
     b = 32;
   } else {
-    b = 128;
-    const long long want = std::min<long long>(std::min<long long>(nkt, 8), sms / t128);
-    while (s * 2 <= want) s *= 2;
+    // split-K: 128- or 64-wide tiles, s = the largest power of two <= min(k-tiles, 8,
+    // #SMs / tiles); pick the cheaper by a per-CTA cost in KB moved (measured weights): per
+    // k-tile 16 (A) + bn/8 (B) + 10 (control), plus 5 per KB of partial rows exchanged over
+    // DSMEM ((s-1)/s of a 128 x bn FP32 tile), which moves ~5x slower than TMA fills.
+    double best = 1e30;
+    for (int cb : {128, 64}) {
+      const long long tiles = mt * ((d->N + cb - 1) / cb);
+      const long long want = std::min<long long>(std::min<long long>(nkt, 8), std::max<long long>(1, sms / tiles));
+      int cs = 1;
+      while (cs * 2 <= want) cs *= 2;
+      const int kps = (nkt + cs - 1) / cs;
+      const double cost = kps * (16.0 + cb / 8.0 + 10.0) + 5.0 * (cs - 1) / cs * (cb / 2.0);
+      if (cost < best) {
+        best = cost;
+        b = cb;
+        s = cs;
+      }
+    }
   }
   const int fb = env_int("BSG_FORCE_BN", 0);
-  if (fb == 32 || fb == 64 || fb == 128 || fb == 256) {
-    b = fb;
-    pair = false;
-  }
   const int fs = env_int("BSG_FORCE_SPLITS", 0);
+  if (fb == 32 || fb == 64 || fb == 128 || fb == 256) {  // a forced width runs unsplit unless
+    b = fb;                                               // the splits are forced too
+    pair = false;
+    s = 1;
+  }
   if (fs >= 1) s = std::min(fs, nkt);
-  if (b < 128) s = 1;  // narrow tiles never split K
+  if (b < 64) s = 1;  // 32-wide tiles never split K
   int k = (nkt + s - 1) / s;
   s = (nkt + k - 1) / k;
   Variant v;
@@ -326,8 +342,8 @@ Variant choose_variant(const bsg_desc* d, int sms) {
     return v;
   }
   // A cluster split keeps 128 x (bn + 4) floats of partial rows in shared memory next to the
-  // ring, which leaves a 128-wide tile four stages and a 256-wide tile too few.
-  const bool cluster_ok = (s == 2 || s == 4 || s == 8) && b == 128;
+  // ring, which leaves 64- and 128-wide tiles enough stages and a 256-wide tile too few.
+  const bool cluster_ok = (s == 2 || s == 4 || s == 8) && (b == 64 || b == 128);
   v.mode = s == 1 ? bsg::SPLIT_NONE
                   : (cluster_ok && env_int("BSG_SPLIT_WORKSPACE", 0) == 0 ? bsg::SPLIT_CLUSTER
                                                                            : bsg::SPLIT_WORKSPACE);

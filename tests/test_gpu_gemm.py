@@ -79,6 +79,15 @@ def test_forced_variants(kind, bn, splits, mode, monkeypatch):
 
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("splits", [2, 4, 8])
+def test_cluster_split_64_wide(kind, splits, monkeypatch):
+    # 64-wide tiles split over K inside clusters; ragged M and N
+    v = run_case(kind, 200, 400, 4096, env={"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": splits}, monkeypatch=monkeypatch,
+                 bias=True, silu=True)
+    assert "_bn64_s%dc_" % splits in v
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 def test_cluster_split_ragged_rows(kind, monkeypatch):
     # ragged M inside a cluster-reduced tile: each CTA's row slab is partly beyond M
     v = run_case(kind, 77, 272, 2048, env={"BSG_FORCE_SPLITS": 4}, monkeypatch=monkeypatch, bias=True, silu=True)
@@ -110,7 +119,7 @@ def test_narrow_tiles_persistent_clusters(kind, monkeypatch):
 
 @pytest.mark.parametrize("M,N,K,expect", [
     (128, 4096, 512, "_bn32_s1_st"),      # short K: 32-wide tiles, no split
-    (128, 4096, 4096, "_bn128_s4c_"),     # long K, few tiles: split-K 4 in clusters
+    (128, 4096, 4096, "_bn64_s2c_"),      # long K, few tiles: 64-wide tiles, split-K 2 in clusters
     (128, 14336, 1024, "_bn128_s1_"),     # 112 tiles of 128: no split
     (1024, 4096, 1024, "_pair256_"),      # M > 256: CTA pairs
 ])
