@@ -637,7 +637,8 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": recorded_traffic("bsg_gemm_kernel<nvfp4,bn128>", "nvfp4_m128_n4096_k4096"),
+                         "traffic": recorded_traffic("bsg_gemm_kernel<nvfp4,%s>" % prob.variant.split("_")[1],
+                                                     "nvfp4_m128_n4096_k4096"),
                          "algorithmic_bytes_per_launch": prob.algorithmic_bytes(),
                          "kernel_us": round(kernel_us, 3), "peak_source": peaks["source"] + " hbm_gbs (burst copy)"},
             "host_us_per_call": {"plan_run_stream": round(h["host_us_per_run"], 3),
