@@ -74,11 +74,14 @@ struct GemmKernelInfo {
   int kc;           // k-tiles (128 bytes of K) per ring stage
 };
 
-// Look up a kernel instantiation: tile width bn (32, 64, 128 or 256), out (OUT_*).
-bool gemm_kernel_info_mx(int bn, int out, GemmKernelInfo* info);
-bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info);
+// Look up a kernel instantiation: tile width bn (32, 64, 128 or 256), out (OUT_*), kc k-slabs per
+// ring stage (1, or 2 for bn 64 and 128).
+bool gemm_kernel_info_mx(int bn, int out, int kc, GemmKernelInfo* info);
+bool gemm_kernel_info_nv(int bn, int out, int kc, GemmKernelInfo* info);
 bool gemm_kernel_info_mx_narrow(int bn, int out, GemmKernelInfo* info);  // bn 32 or 64
 bool gemm_kernel_info_nv_narrow(int bn, int out, GemmKernelInfo* info);
+bool gemm_kernel_info_mx_kc2(int bn, int out, GemmKernelInfo* info);     // bn 64 or 128
+bool gemm_kernel_info_nv_kc2(int bn, int out, GemmKernelInfo* info);
 // CTA-pair kernels (256 x 256 pair tiles, launched in clusters of 2).
 bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info);  // BSG_PAIR_KC=1 or 2 (default 2)
 bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info);

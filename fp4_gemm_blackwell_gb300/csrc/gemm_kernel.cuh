@@ -29,18 +29,22 @@
 
 namespace bsg {
 
-template <int KIND, int BN>
+// KC = k-slabs of 128 bytes of K per ring stage (one barrier wait and one commit per stage).
+template <int KIND, int BN, int KC>
 struct GemmCfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "tile width");
+  static_assert(KC == 1 || KC == 2, "k-slabs per stage");
   static constexpr int BM = 128;
   static constexpr int BK_BYTES = 128;
-  static constexpr int K_TILE = KIND == KIND_MX ? 128 : 256;  // elements per k-tile
-  static constexpr int MMA_K = KIND == KIND_MX ? 32 : 64;     // elements per MMA
-  static constexpr int STEPS = K_TILE / MMA_K;                // MMAs per k-tile (4)
-  static constexpr int SF_ATOMS = KIND == KIND_MX ? 1 : 4;    // 128x4 atoms per band per k-tile
-  static constexpr int NB = BN >= 128 ? BN / 128 : 1;         // 128-row scale bands of B per tile
-  static constexpr int A_BYTES = BM * BK_BYTES;
-  static constexpr int B_BYTES = BN * BK_BYTES;
+  static constexpr int K_TILE = KC * (KIND == KIND_MX ? 128 : 256);  // elements per stage
+  static constexpr int MMA_K = KIND == KIND_MX ? 32 : 64;            // elements per MMA
+  static constexpr int STEPS = K_TILE / MMA_K;                       // MMAs per stage (4 a slab)
+  static constexpr int SF_ATOMS = KC * (KIND == KIND_MX ? 1 : 4);    // 128x4 atoms per band per stage
+  static constexpr int NB = BN >= 128 ? BN / 128 : 1;                // 128-row scale bands of B per tile
+  static constexpr int SLAB_A = BM * BK_BYTES;                       // one 128-byte k-slab of A
+  static constexpr int SLAB_B = BN * BK_BYTES;
+  static constexpr int A_BYTES = KC * SLAB_A;
+  static constexpr int B_BYTES = KC * SLAB_B;
   static constexpr int SFA_BYTES = SF_ATOMS * 512;
   static constexpr int SFB_BYTES = NB * SF_ATOMS * 512;
   static constexpr int STAGE_RAW = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -87,6 +91,7 @@ struct GemmCfg {
   static_assert(STAGES >= 2, "ring too shallow");
   static_assert(STAGES <= 8, "barrier slots");
   static_assert(TMEM_USED <= 512, "tensor memory");
+  static_assert(SF_ATOMS <= 4 || SF_ATOMS % 4 == 0, "scale-warp stores");
 };
 
 struct UnitCoord {
@@ -293,9 +298,9 @@ __device__ __forceinline__ uint4 rotate_words(uint4 v, int r) {
   return v;
 }
 
-template <int KIND, int BN, int OUT>
-__global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<KIND, BN>;
+template <int KIND, int BN, int KC, int OUT>
+__global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = GemmCfg<KIND, BN, KC>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
@@ -403,22 +408,25 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
             } else {
               const uint32_t fb = bar_full(stage);
               mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
-              if (p.cmn > 1) {
-                // this CTA's slice of the A tile (the tensor map's box is 128/cmn rows), written
-                // into the same stage of every CTA that shares the m-tile
-                const int rows = C::BM / p.cmn;
-                tma_load_2d_mc(stage_a(stage) + rn * rows * C::BK_BYTES, &p.tmap_a, fb, kt * C::BK_BYTES,
-                               c.m_blk * C::BM + rn * rows, amask);
-              } else {
-                tma_load_2d(stage_a(stage), &p.tmap_a, fb, kt * C::BK_BYTES, c.m_blk * C::BM);
-              }
-              if (p.cmm > 1) {
-                // likewise a BN/cmm-row slice of the B tile for every CTA that shares the n-tile
-                const int rows = BN / p.cmm;
-                tma_load_2d_mc(stage_b(stage) + rm * rows * C::BK_BYTES, &p.tmap_b, fb, kt * C::BK_BYTES,
-                               c.n_blk * BN + rm * rows, bmask);
-              } else {
-                tma_load_2d(stage_b(stage), &p.tmap_b, fb, kt * C::BK_BYTES, c.n_blk * BN);
+#pragma unroll
+              for (int j = 0; j < KC; ++j) {  // k-slabs past K read as zeros (their MMAs are skipped)
+                const int x = (kt * KC + j) * C::BK_BYTES;
+                const uint32_t sa = stage_a(stage) + j * C::SLAB_A, sb = stage_b(stage) + j * C::SLAB_B;
+                if (p.cmn > 1) {
+                  // this CTA's slice of the A tile (the tensor map's box is 128/cmn rows), written
+                  // into the same stage of every CTA that shares the m-tile
+                  const int rows = C::BM / p.cmn;
+                  tma_load_2d_mc(sa + rn * rows * C::BK_BYTES, &p.tmap_a, fb, x, c.m_blk * C::BM + rn * rows, amask);
+                } else {
+                  tma_load_2d(sa, &p.tmap_a, fb, x, c.m_blk * C::BM);
+                }
+                if (p.cmm > 1) {
+                  // likewise a BN/cmm-row slice of the B tile for every CTA that shares the n-tile
+                  const int rows = BN / p.cmm;
+                  tma_load_2d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, bmask);
+                } else {
+                  tma_load_2d(sb, &p.tmap_b, fb, x, c.n_blk * BN);
+                }
               }
             }
             first = false;
@@ -465,7 +473,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
             }
             const int k_rem = p.K - kt * C::K_TILE;
             const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
-            const int sf_atoms = KIND == KIND_MX ? 1 : steps;
+            const int sf_atoms = KIND == KIND_MX ? (steps + 3) / 4 : steps;  // atoms K still covers
             if (first && p.debug_skip_first_load) {
               // test hook (see the code producer)
             } else {
@@ -522,18 +530,22 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
             const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS;
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
             const uint32_t sa = stage_a(stage), sb = stage_b(stage);
+            // MMA j reads 32 bytes of K at offset 32 (j % 4) of k-slab j / 4; its scales are in
+            // atom j / 4 (MXFP8, byte j % 4 of each word) or atom j (NVFP4)
             if constexpr (KIND == KIND_MX) {
               for (int j = 0; j < steps; ++j) {
-                const uint32_t idesc = C::IDESC | (static_cast<uint32_t>(j) << 4) |
-                                       (static_cast<uint32_t>(j) << 29);
-                tc_mma_mxf8(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
-                            idesc, sfa_t, sfb_t, (kt > c.kt0 || j > 0) ? 1u : 0u);
+                const uint32_t jj = static_cast<uint32_t>(j & 3), slab = static_cast<uint32_t>(j >> 2);
+                const uint32_t idesc = C::IDESC | (jj << 4) | (jj << 29);
+                tc_mma_mxf8(d_t, sdesc_kmajor_sw128(sa + slab * C::SLAB_A + 32 * jj),
+                            sdesc_kmajor_sw128(sb + slab * C::SLAB_B + 32 * jj), idesc, sfa_t + 4 * slab,
+                            sfb_t + 4 * C::NB * slab, (kt > c.kt0 || j > 0) ? 1u : 0u);
               }
             } else {
               for (int j = 0; j < steps; ++j) {
-                tc_mma_nvf4(d_t, sdesc_kmajor_sw128(sa + 32 * j), sdesc_kmajor_sw128(sb + 32 * j),
-                            C::IDESC, sfa_t + 4 * j, sfb_t + 4 * C::NB * j,
-                            (kt > c.kt0 || j > 0) ? 1u : 0u);
+                const uint32_t jj = static_cast<uint32_t>(j & 3), slab = static_cast<uint32_t>(j >> 2);
+                tc_mma_nvf4(d_t, sdesc_kmajor_sw128(sa + slab * C::SLAB_A + 32 * jj),
+                            sdesc_kmajor_sw128(sb + slab * C::SLAB_B + 32 * jj), C::IDESC, sfa_t + 4 * j,
+                            sfb_t + 4 * C::NB * j, (kt > c.kt0 || j > 0) ? 1u : 0u);
               }
             }
             if (p.cm > 1)
@@ -572,9 +584,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
     // ------------------------------------------------------------ scale warps (warps 4..7)
     // Per stage, each warp writes its TMEM lane quarter of the stage's scale slot with the layout
     // a 32x128b.warpx4 copy of the atoms produces: lane i, column 4j + k holds the four scales
-    // (one 32-bit word of the atom's row i) of A row 32k + i of atom j, and the B columns follow
-    // (4*NB per atom).  A tile narrower than its 128-row band uses words jq.. of each B atom
-    // row, jq = its first 32-row quarter of the band: they are rotated to the front.
+    // (one 32-bit word of the atom's row i) of A row 32k + i of atom j, and column
+    // 4*NB*j + 4b + k those of B row 128b + 32k + i.  A tile narrower than its 128-row band uses
+    // words jq.. of each B atom row, jq = its first 32-row quarter of the band: they are rotated
+    // to the front.
     const int q = warp & 3;
     int stage = 0;
     uint32_t phase = 0;
@@ -586,58 +599,30 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
         ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
         if (!ok) break;
         const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
-        if constexpr (KIND == KIND_MX && C::NB == 1) {
-          // one atom per operand: A words as they are, B words rotated
-          const uint4 va = lds_u4(stage_sfa(stage) + 16 * lane);
-          const uint4 vb = rotate_words(lds_u4(stage_sfb(stage) + 16 * lane), jq);
-          const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-          tmem_st_32x32b_x8(slot, w);
-        } else if constexpr (KIND == KIND_MX) {
-          // one A atom, two B atoms (bands)
-          const uint4 va = lds_u4(stage_sfa(stage) + 16 * lane);
-          const uint4 vb0 = lds_u4(stage_sfb(stage) + 16 * lane);
-          const uint4 vb1 = lds_u4(stage_sfb(stage) + 512 + 16 * lane);
-          const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
-          const uint32_t wb[8] = {vb0.x, vb0.y, vb0.z, vb0.w, vb1.x, vb1.y, vb1.z, vb1.w};
-          tmem_st_32x32b_x4(slot, wa);
-          tmem_st_32x32b_x8(slot + C::SFA_COLS, wb);
-        } else {
-          uint32_t a[16];
+        // atoms in groups of up to four: 4 A columns and 4 * NB B columns per atom
+        constexpr int NA = C::SF_ATOMS;
+        constexpr int GA = NA < 4 ? NA : 4;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 v = lds_u4(stage_sfa(stage) + 512 * j + 16 * lane);
-            a[4 * j] = v.x;
-            a[4 * j + 1] = v.y;
-            a[4 * j + 2] = v.z;
-            a[4 * j + 3] = v.w;
-          }
-          tmem_st_32x32b_x16(slot, a);
-          if constexpr (C::NB == 2) {
-            uint32_t b[32];
+        for (int g0 = 0; g0 < NA; g0 += GA) {
+          uint32_t a[4 * GA], b[4 * C::NB * GA];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+          for (int t = 0; t < GA; ++t) {
+            const uint4 v = lds_u4(stage_sfa(stage) + 512 * (g0 + t) + 16 * lane);
+            a[4 * t] = v.x;
+            a[4 * t + 1] = v.y;
+            a[4 * t + 2] = v.z;
+            a[4 * t + 3] = v.w;
 #pragma unroll
-              for (int rb = 0; rb < 2; ++rb) {
-                const uint4 v = lds_u4(stage_sfb(stage) + rb * C::SF_ATOMS * 512 + 512 * j + 16 * lane);
-                b[(2 * j + rb) * 4] = v.x;
-                b[(2 * j + rb) * 4 + 1] = v.y;
-                b[(2 * j + rb) * 4 + 2] = v.z;
-                b[(2 * j + rb) * 4 + 3] = v.w;
-              }
+            for (int rb = 0; rb < C::NB; ++rb) {
+              const uint4 w = rotate_words(lds_u4(stage_sfb(stage) + rb * NA * 512 + 512 * (g0 + t) + 16 * lane), jq);
+              b[(C::NB * t + rb) * 4] = w.x;
+              b[(C::NB * t + rb) * 4 + 1] = w.y;
+              b[(C::NB * t + rb) * 4 + 2] = w.z;
+              b[(C::NB * t + rb) * 4 + 3] = w.w;
             }
-            tmem_st_32x32b_x32(slot + C::SFA_COLS, b);
-          } else {
-            uint32_t b[16];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 v = rotate_words(lds_u4(stage_sfb(stage) + 512 * j + 16 * lane), jq);
-              b[4 * j] = v.x;
-              b[4 * j + 1] = v.y;
-              b[4 * j + 2] = v.z;
-              b[4 * j + 3] = v.w;
-            }
-            tmem_st_32x32b_x16(slot + C::SFA_COLS, b);
           }
+          tmem_st_cols(slot + 4 * g0, a);
+          tmem_st_cols(slot + C::SFA_COLS + 4 * C::NB * g0, b);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -858,16 +843,16 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1) bsg_gemm_kernel
   }
 }
 
-template <int KIND, int BN, int OUT>
+template <int KIND, int BN, int KC, int OUT>
 bool fill_kernel_info(GemmKernelInfo* info) {
-  using C = GemmCfg<KIND, BN>;
-  info->fn = reinterpret_cast<const void*>(&bsg_gemm_kernel<KIND, BN, OUT>);
+  using C = GemmCfg<KIND, BN, KC>;
+  info->fn = reinterpret_cast<const void*>(&bsg_gemm_kernel<KIND, BN, KC, OUT>);
   info->smem_bytes = C::SMEM_BYTES;
   info->threads = C::THREADS;
   info->bn = BN;
   info->stages = C::STAGES;
   info->stage_bytes = C::STAGE_BYTES;
-  info->kc = 1;
+  info->kc = KC;
   return true;
 }
 

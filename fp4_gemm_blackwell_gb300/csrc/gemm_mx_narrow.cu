@@ -5,10 +5,10 @@
 namespace bsg {
 
 bool gemm_kernel_info_mx_narrow(int bn, int out, GemmKernelInfo* info) {
-  if (bn == 32 && out == OUT_F16) return fill_kernel_info<KIND_MX, 32, OUT_F16>(info);
-  if (bn == 32 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 32, OUT_BF16>(info);
-  if (bn == 64 && out == OUT_F16) return fill_kernel_info<KIND_MX, 64, OUT_F16>(info);
-  if (bn == 64 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 64, OUT_BF16>(info);
+  if (bn == 32 && out == OUT_F16) return fill_kernel_info<KIND_MX, 32, 1, OUT_F16>(info);
+  if (bn == 32 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 32, 1, OUT_BF16>(info);
+  if (bn == 64 && out == OUT_F16) return fill_kernel_info<KIND_MX, 64, 1, OUT_F16>(info);
+  if (bn == 64 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 64, 1, OUT_BF16>(info);
   return false;
 }
 

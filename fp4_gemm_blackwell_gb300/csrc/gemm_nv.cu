@@ -3,12 +3,13 @@
 
 namespace bsg {
 
-bool gemm_kernel_info_nv(int bn, int out, GemmKernelInfo* info) {
+bool gemm_kernel_info_nv(int bn, int out, int kc, GemmKernelInfo* info) {
+  if (kc == 2) return gemm_kernel_info_nv_kc2(bn, out, info);
   if (bn < 128) return gemm_kernel_info_nv_narrow(bn, out, info);
-  if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_NV, 128, OUT_F16>(info);
-  if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 128, OUT_BF16>(info);
-  if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_NV, 256, OUT_F16>(info);
-  if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 256, OUT_BF16>(info);
+  if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_NV, 128, 1, OUT_F16>(info);
+  if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 128, 1, OUT_BF16>(info);
+  if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_NV, 256, 1, OUT_F16>(info);
+  if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 256, 1, OUT_BF16>(info);
   return false;
 }
 

@@ -253,6 +253,7 @@ int env_int(const char* name, int dflt) {
 struct Variant {
   int bn, splits, kps, mode, cluster;
   int cmn, cmm;  // multicast cluster: cmm m-tiles x cmn n-tiles (A shared along n, B along m)
+  int kc;        // 128-byte k-slabs per ring stage (1-SM kernel; kps counts ring stages)
   bool pair;     // CTA-pair kernel: 256 x 256 tiles over 2-CTA clusters
 };
 
@@ -277,8 +278,9 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   } else {
     // split-K: 128- or 64-wide tiles, s = the largest power of two <= min(k-tiles, 8,
     // #SMs / tiles); pick the cheaper by a per-CTA cost in KB moved (measured weights): per
-    // k-tile 16 (A) + bn/8 (B) + 10 (control), plus 5 per KB of partial rows exchanged over
-    // DSMEM ((s-1)/s of a 128 x bn FP32 tile), which moves ~5x slower than TMA fills.
+    // k-tile 16 (A) + bn/8 (B) + 10 / kc (control, per ring stage of kc k-slabs: two for
+    // 64-wide tiles, see below), plus 5 per KB of partial rows exchanged over DSMEM ((s-1)/s
+    // of a 128 x bn FP32 tile), which moves ~5x slower than TMA fills.
     double best = 1e30;
     for (int cb : {128, 64}) {
       const long long tiles = mt * ((d->N + cb - 1) / cb);
@@ -286,7 +288,8 @@ Variant choose_variant(const bsg_desc* d, int sms) {
       int cs = 1;
       while (cs * 2 <= want) cs *= 2;
       const int kps = (nkt + cs - 1) / cs;
-      const double cost = kps * (16.0 + cb / 8.0 + 10.0) + 5.0 * (cs - 1) / cs * (cb / 2.0);
+      const double ckc = (cb == 64 || cs == 1) ? 2.0 : 1.0;
+      const double cost = kps * (16.0 + cb / 8.0 + 10.0 / ckc) + 5.0 * (cs - 1) / cs * (cb / 2.0);
       if (cost < best) {
         best = cost;
         b = cb;
@@ -303,16 +306,26 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   }
   if (fs >= 1) s = std::min(fs, nkt);
   if (b < 64) s = 1;  // 32-wide tiles never split K
-  int k = (nkt + s - 1) / s;
-  s = (nkt + k - 1) / k;
+  // Two 128-byte k-slabs per ring stage halve the per-stage control (one barrier wait, one
+  // commit, one scale staging per 8 MMAs) where the ring keeps three stages of the doubled size:
+  // 64-wide tiles, and 128-wide tiles without a split-K receive area (measured: 128x4096x4096
+  // 9.1 -> 8.1 us with 64-wide split-K 2; 128-wide split-K 4, left with 2 stages, got slower).
+  int kc = (b == 64 || (b == 128 && s == 1)) ? 2 : 1;
+  const int fk = env_int("BSG_KC", 0);
+  if (fk == 1 || (fk == 2 && (b == 64 || b == 128))) kc = fk;
+  const int nst = (nkt + kc - 1) / kc;  // ring stages along K
+  int k = (nst + s - 1) / s;
+  s = (nst + k - 1) / k;
   Variant v;
   v.cmn = 1;
   v.cmm = 1;
+  v.kc = kc;
   v.pair = pair && env_int("BSG_FORCE_SPLITS", 0) == 0;
   const int fp = env_int("BSG_FORCE_PAIR", -1);
   if (fp == 0 || fp == 1) v.pair = fp == 1;
   if (v.pair) {
     v.bn = 256;
+    v.kc = 1;
     v.splits = 1;
     v.kps = nkt;
     v.mode = bsg::SPLIT_NONE;
@@ -413,7 +426,7 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->num_tiles = g->num_m_tiles * g->num_n_tiles;
   g->splits = v.splits;
   g->split_mode = v.mode;
-  g->k_tiles_per_split = info.kc == 1 ? v.kps : g->num_k_tiles;  // several k-tiles per stage: no split
+  g->k_tiles_per_split = v.pair ? g->num_k_tiles : v.kps;  // in ring stages
   g->cmn = v.cmn;
   g->cmm = v.cmm;
   g->cm = v.cmn * v.cmm;
@@ -495,8 +508,8 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
   const bool found = v.pair ? (d->kind == BSG_MXFP8 ? bsg::gemm_pair_kernel_info_mx(out_t, &info)
                                                     : bsg::gemm_pair_kernel_info_nv(out_t, &info))
-                            : (d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, &info)
-                                                    : bsg::gemm_kernel_info_nv(v.bn, out_t, &info));
+                            : (d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, v.kc, &info)
+                                                    : bsg::gemm_kernel_info_nv(v.bn, out_t, v.kc, &info));
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
   int resident = di.sms;
@@ -539,8 +552,8 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   } else {
     char mc[24] = "";
     if (v.cmn * v.cmm > 1) std::snprintf(mc, sizeof(mc), v.cmm > 1 ? "_mc%dx%d" : "_mc%d", v.cmn, v.cmm);
-    std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
-                  v.bn, v.splits, kModeName[v.mode], mc, g.ring_stages, p->grid);
+    std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s%s%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
+                  v.bn, v.splits, kModeName[v.mode], mc, v.kc == 2 ? "_kc2" : "", g.ring_stages, p->grid);
   }
   make_launch_config(&p->cfg, p->attrs, p->grid, info.threads, info.smem_bytes, p->cluster);
   if (env_int("BSG_LOG", 0))
@@ -815,8 +828,8 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
   const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
   const bool found = v.pair ? (d->kind == BSG_MXFP8 ? bsg::gemm_pair_kernel_info_mx(out_t, &info)
                                                     : bsg::gemm_pair_kernel_info_nv(out_t, &info))
-                            : (d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, &info)
-                                                    : bsg::gemm_kernel_info_nv(v.bn, out_t, &info));
+                            : (d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, v.kc, &info)
+                                                    : bsg::gemm_kernel_info_nv(v.bn, out_t, v.kc, &info));
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   const int num_tiles = ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn);
   const WorkspaceLayout w = workspace_layout(v, num_tiles);

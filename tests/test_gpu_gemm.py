@@ -71,7 +71,11 @@ def test_forced_variants(kind, bn, splits, mode, monkeypatch):
     K = 1792
     v = run_case(kind, 384, 768, K, env=env, monkeypatch=monkeypatch, bias=True, silu=True)
     # a split factor that does not divide the k-tiles evenly is rounded so every split is busy
-    nkt = K // (128 if kind == "mxfp8" else 256)
+    # (counted in ring stages: two k-tiles each for 64-wide and unsplit 128-wide tiles)
+    kc = 2 if (bn == 64 or (bn == 128 and splits == 1)) and os.environ.get("BSG_KC") != "1" else 1
+    if os.environ.get("BSG_KC") == "2" and bn in (64, 128):
+        kc = 2
+    nkt = -(-K // ((128 if kind == "mxfp8" else 256) * kc))
     kps = -(-nkt // splits)
     s = -(-nkt // kps)
     m = "" if s == 1 else ("w" if mode == "w" or s not in (2, 4, 8) or bn == 256 else "c")

@@ -52,6 +52,7 @@ def test_noalloc_matches_plan_twice(kind, M, N, K, epi, workspace, monkeypatch):
 def test_noalloc_rejects_problems_beyond_its_scratch(monkeypatch):
     # 64 splits x 4 tiles x 64 KiB of partials = 16 MiB, beyond the 16 MiB array once the
     # counters are added
+    monkeypatch.setenv("BSG_FORCE_BN", "128")
     monkeypatch.setenv("BSG_FORCE_SPLITS", "64")
     monkeypatch.setenv("BSG_SPLIT_WORKSPACE", "1")
     prob = P.make_problem("nvfp4", 128, 512, 16384)
