@@ -84,7 +84,7 @@ bool gemm_kernel_info_mx_kc2(int bn, int out, GemmKernelInfo* info);     // bn 6
 bool gemm_kernel_info_nv_kc2(int bn, int out, GemmKernelInfo* info);
 // CTA-pair kernels (256 x 256 pair tiles, launched in clusters of 2).
 bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info);  // BSG_PAIR_KC=1 or 2 (default 2)
-bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info);
+bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info);  // BSG_PAIR_KC=1 or 2 (default 2)
 
 // Quantisers (stream-ordered).  See bsg_quantize in include/bsgemm.h.
 cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,

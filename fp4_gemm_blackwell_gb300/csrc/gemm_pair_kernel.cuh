@@ -43,18 +43,26 @@ struct PairCfg {
   static constexpr int B_BYTES = KC * SLAB_B;
   static constexpr int SFA_BYTES = SF_ATOMS * 512;
   static constexpr int SFB_BYTES = 2 * SF_ATOMS * 512;  // both 128-row bands of the tile's B
-  static constexpr int STAGE_RAW = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  // SEP: the scale atoms have their own two-stage ring and two TMEM slots, apart from the code
+  // ring (NVFP4 with two k-slabs: 12 KB of atoms per stage would leave room for only two 76 KB
+  // stages, and 96 TMEM columns per slot for only two slots).  The scale warps release a scale
+  // stage once they have copied it; a TMEM slot is released by the MMAs' commit.
+  static constexpr bool SEP = KIND == KIND_NV && KC == 2;
+  static constexpr int SF_STAGE_BYTES = (SFA_BYTES + SFB_BYTES + 1023) / 1024 * 1024;
+  static constexpr int SF_STAGES = SEP ? 2 : 0;
+  static constexpr int STAGE_RAW = A_BYTES + B_BYTES + (SEP ? 0 : SFA_BYTES + SFB_BYTES);
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int AUX_BYTES = 1024;
-  static constexpr int STAGES_FIT = (SMEM_LIMIT - AUX_BYTES - 1024) / STAGE_BYTES;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - AUX_BYTES - 1024 - SF_STAGES * SF_STAGE_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + AUX_BYTES + 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + SF_STAGES * SF_STAGE_BYTES + AUX_BYTES + 1024;
   static constexpr int SFA_COLS = 4 * SF_ATOMS;  // per scale slot: A's 128 rows
   static constexpr int SFB_COLS = 8 * SF_ATOMS;  // B's 256 rows
   static constexpr int SF_SLOT_COLS = SFA_COLS + SFB_COLS;
   static constexpr int SF_COL0 = BN;             // one 256-column accumulator first
-  static constexpr int TMEM_USED = SF_COL0 + STAGES * SF_SLOT_COLS;
+  static constexpr int SF_SLOTS = SEP ? SF_STAGES : STAGES;
+  static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT_COLS;
   static constexpr int TMEM_COLS = 512;
   static constexpr int SCALE_WARP0 = 4;
   static constexpr int EPI_WARP0 = 8;
@@ -87,15 +95,20 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
   const bool is_leader = (rank & 1u) == 0;
   const uint16_t pair_mask = static_cast<uint16_t>(3u << leader);
 
-  uint8_t* aux = smem + C::STAGES * C::STAGE_BYTES;
+  const uint32_t sf0 = smem0 + C::STAGES * C::STAGE_BYTES;  // separate scale ring (SEP)
+  uint8_t* aux = smem + C::STAGES * C::STAGE_BYTES + C::SF_STAGES * C::SF_STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(aux);
   // slots: full[0..7], empty[8..15], sf_full[16..23], tmem_full 32, tmem_empty 33, drain 34,
-  // tmem address 35, abort flag 36.  The leader's `full` completes when both CTAs' code tiles
-  // have landed and both CTAs' scale warps have filled their TMEM slots: one wait per k-tile
-  // for the MMA issuer.
+  // tmem address 35, abort flag 36; with a separate scale ring also sf_empty[40..47],
+  // slot_free[48..55] and sfready[56..63].  Without it, the leader's `full` completes when both
+  // CTAs' code tiles have landed and both CTAs' scale warps have filled their TMEM slots: one
+  // wait per stage for the MMA issuer.
   auto bar_full = [&](int s) { return smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return smem_u32(bars + 8 + s); };
   auto bar_sf_full = [&](int s) { return smem_u32(bars + 16 + s); };
+  auto bar_sf_empty = [&](int t) { return smem_u32(bars + 40 + t); };   // scale stage copied (SEP)
+  auto bar_slot_free = [&](int t) { return smem_u32(bars + 48 + t); };  // TMEM slot read (SEP)
+  auto bar_sfready = [&](int t) { return smem_u32(bars + 56 + t); };    // TMEM slot filled (SEP)
   const uint32_t bar_tfull = smem_u32(bars + 32);
   const uint32_t bar_tempty = smem_u32(bars + 33);
   const uint32_t bar_drain = smem_u32(bars + 34);
@@ -104,15 +117,24 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
 
   auto stage_a = [&](int s) { return smem0 + s * C::STAGE_BYTES; };
   auto stage_b = [&](int s) { return smem0 + s * C::STAGE_BYTES + C::A_BYTES; };
-  auto stage_sfa = [&](int s) { return smem0 + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES; };
-  auto stage_sfb = [&](int s) { return smem0 + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES + C::SFA_BYTES; };
+  // scale atoms of stage s (SEP: of scale stage s)
+  auto stage_sfa = [&](int s) {
+    return C::SEP ? sf0 + s * C::SF_STAGE_BYTES : smem0 + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+  };
+  auto stage_sfb = [&](int s) { return stage_sfa(s) + C::SFA_BYTES; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      // the leader's producer (with both CTAs' code bytes) and the scale warps of both CTAs
-      mbar_init(bar_full(s), 1 + 8);
+      // the leader's producer (with both CTAs' code bytes) and, without a separate scale ring,
+      // the scale warps of both CTAs
+      mbar_init(bar_full(s), C::SEP ? 1 : 1 + 8);
       mbar_init(bar_empty(s), 1);    // the leader's multicast commit
       mbar_init(bar_sf_full(s), 1);  // this CTA's producer (scale bytes)
+    }
+    for (int t = 0; t < C::SF_STAGES; ++t) {
+      mbar_init(bar_sf_empty(t), 4);   // this CTA's scale warps
+      mbar_init(bar_slot_free(t), 1);  // the leader's multicast commit
+      mbar_init(bar_sfready(t), 8);    // the scale warps of both CTAs
     }
     mbar_init(bar_tfull, 1);
     mbar_init(bar_tempty, 2 * C::EPI_WARPS);  // one arrival per epilogue warp of each CTA
@@ -180,7 +202,9 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     } else if (warp == 2) {
       // ---------------------------------------------------------- TMA producer: scale atoms
       // A second issuing thread (each copy instruction holds its thread for a hundred-odd
-      // cycles): this CTA's scale atoms, on its own barrier.
+      // cycles): this CTA's scale atoms, on its own barrier; into the code ring's stages, or
+      // (SEP) into the scale ring, refilled once the scale warps have copied a stage.
+      constexpr int NR = C::SEP ? C::SF_STAGES : C::STAGES;
       if (lane == 0) {
         int stage = 0;
         uint32_t phase = 0;
@@ -194,7 +218,10 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
 #pragma unroll
           for (int rb = 0; rb < 2; ++rb) bands += (c.n_blk * 2 + rb < p.sfb_bands) ? 1 : 0;
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
-            if (!wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
+            const bool free_ = C::SEP ? wait_bounded(bar_sf_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)
+                                      : wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p,
+                                                             ST_TIMEOUT_PRODUCER);
+            if (!free_) {
               ok = false;
               break;
             }
@@ -222,7 +249,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
               }
             }
             first = false;
-            if (++stage == C::STAGES) {
+            if (++stage == NR) {
               stage = 0;
               phase ^= 1u;
             }
@@ -234,6 +261,8 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
       if (is_leader && lane == 0) {
         int stage = 0;
         uint32_t phase = 0;
+        int sst = 0;  // scale slot (SEP)
+        uint32_t sph = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int u = pair0; ok && u < p.num_units; u += pairs) {
@@ -244,7 +273,8 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
           }
           tc_fence_after();
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
-            if (!wait_bounded_cluster(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
+            if (!wait_bounded_cluster(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA) ||
+                (C::SEP && !wait_bounded_cluster(bar_sfready(sst), sph, abort_flag, p, ST_TIMEOUT_MMA))) {
               ok = false;
               break;
             }
@@ -252,7 +282,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
             const int k_rem = p.K - kt * C::K_TILE;
             const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
             // the scale warps of both CTAs have put this stage's scales in their TMEM slots
-            const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS;
+            const uint32_t sfa_t = tmem_base + C::SF_COL0 + (C::SEP ? sst : stage) * C::SF_SLOT_COLS;
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
             const uint32_t sa = stage_a(stage), sb = stage_b(stage);
             // MMA j reads 32 bytes of K at offset 32 (j % 4) of slab j / 4; its scales are in atom
@@ -278,6 +308,13 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
               stage = 0;
               phase ^= 1u;
             }
+            if constexpr (C::SEP) {
+              tc_commit_pair_mc(bar_slot_free(sst), pair_mask);  // this scale slot may be refilled
+              if (++sst == C::SF_STAGES) {
+                sst = 0;
+                sph ^= 1u;
+              }
+            }
           }
           if (!ok) break;
           tc_commit_pair_mc(bar_tfull, pair_mask);
@@ -301,6 +338,9 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     // The layout a 32x128b.warpx4 copy of the atoms produces, per stage slot: lane i, column
     // 4t + k holds the four scales of A row 32k + i of atom t (this CTA's 128 rows), and column
     // 8t + 4b + k those of B row 128b + 32k + i (the pair tile's 256 rows).
+    // With a separate scale ring (SEP) the stage index is the scale stage, which is also the TMEM
+    // slot: it is filled once the MMAs that read its previous contents have completed.
+    constexpr int NR = C::SEP ? C::SF_STAGES : C::STAGES;
     const int q = warp & 3;
     const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
     int stage = 0;
@@ -309,7 +349,9 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     for (int u = pair0; ok && u < p.num_units; u += pairs) {
       const UnitCoord c = decode_unit(p, u, 0);
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
-        ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES) &&
+                                         (!C::SEP || wait_bounded_cluster(bar_slot_free(stage), phase ^ 1u,
+                                                                          abort_flag, p, ST_TIMEOUT_SCALES)));
         if (!ok) break;
         const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
         // atoms in groups of up to four: 16 A columns and 32 B columns per group
@@ -344,12 +386,14 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
           // The peer signals through the tensor-core commit path, which arrives on the leader's
           // barrier without holding this thread for the cluster round trip that a remote
           // mbarrier arrive takes (its stores to TMEM are complete: tcgen05.wait::st above).
+          const uint32_t ready = C::SEP ? bar_sfready(stage) : bar_full(stage);
           if (is_leader)
-            mbar_arrive(bar_full(stage));
+            mbar_arrive(ready);
           else
-            tc_commit_pair_mc(bar_full(stage), leader_mask);
+            tc_commit_pair_mc(ready, leader_mask);
+          if (C::SEP) mbar_arrive(bar_sf_empty(stage));  // the scale stage may be refilled
         }
-        if (++stage == C::STAGES) {
+        if (++stage == NR) {
           stage = 0;
           phase ^= 1u;
         }
