@@ -87,7 +87,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
+        sm, smax, watts, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             t = [x.strip() for x in line.split(",")]
@@ -98,13 +98,17 @@ class ClockSampler:
                 smax.append(float(t[1]))
             except ValueError:
                 continue
+            try:
+                watts.append(float(t[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, t[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "power_w": statistics.median(watts) if watts else None, "samples": len(sm)}
 
 
 def kernel_source_hash():
@@ -554,17 +558,21 @@ def case_arm(args):
             prob.plans[0].run(stream)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    clocks.start()
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(args.steps):
             prob.plans[0].run(stream)
         end.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     us = start.elapsed_time(end) * 1e3 / args.steps
     prob.plans[0].check_status()
     print(json.dumps({"case": args.case, "variant": prob.variant, "us_per_launch": round(us, 3),
                       "tflops": round(prob.flops() / (us * 1e-6) / 1e12, 2),
-                      "gbs": round(prob.algorithmic_bytes() / (us * 1e-6) / 1e9, 1)}), flush=True)
+                      "gbs": round(prob.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
+                      "clocks": clk}), flush=True)
     prob.close()
     return 0
 

@@ -655,44 +655,50 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
       const int m = c.m_blk * C::BM + row;
       const int nbase = c.n_blk * BN;
       if (p.split_mode == SPLIT_NONE) {
-        // Round the whole row segment into registers first and release the accumulator before
-        // storing, so the next tile's MMAs do not wait for the stores.
-        uint32_t packed[HC / 2];
-        if constexpr (HC == 16) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(t_row + col0, r);
+        uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+        if constexpr (C::NACC == 1) {
+          // One accumulator: the whole row segment comes out of TMEM before any arithmetic and
+          // the accumulator is released at once, since the next tile's MMAs need all of it.
+          uint32_t r[HC];
+#pragma unroll
+          for (int ch = 0; ch < HC / 32; ++ch)
+            tmem_ld_32x32b_x32(t_row + col0 + ch * 32, reinterpret_cast<uint32_t(&)[32]>(r[32 * ch]));
           tmem_ld_wait();
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[8 * g + i]);
-            epi_pack<OUT, 8>(p, nbase + col0 + 8 * g, v, alpha, &packed[4 * g]);
-          }
-        } else {
-#pragma unroll
-          for (int ch = 0; ch < HC / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              float v[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[8 * g + i]);
-              epi_pack<OUT, 8>(p, nbase + col0 + ch * 32 + 8 * g, v, alpha, &packed[ch * 16 + 4 * g]);
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty(acc));
-        if (m < p.M) {
-          uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty(acc));
 #pragma unroll
           for (int g = 0; g < HC / 8; ++g) {
             const int n = nbase + col0 + 8 * g;
-            if (n < p.N)
+            uint32_t o[4];
+            epi_pack<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[8 * g]), alpha, o);
+            if (m < p.M && n < p.N) *reinterpret_cast<uint4*>(drow + n) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        } else {
+          // Two accumulators: the next tile's MMAs run in the other one, so the segment is
+          // rounded chunk by chunk (fewer live registers) and released before the stores.
+          uint32_t packed[HC / 2];
+#pragma unroll
+          for (int ch = 0; ch < (HC + 31) / 32; ++ch) {
+            constexpr int W = HC < 32 ? HC : 32;
+            uint32_t r[W];
+            if constexpr (W == 16)
+              tmem_ld_32x32b_x16(t_row + col0, r);
+            else
+              tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < W / 8; ++g)
+              epi_pack<OUT, 8>(p, nbase + col0 + ch * 32 + 8 * g, reinterpret_cast<const float*>(&r[8 * g]), alpha,
+                               &packed[ch * 16 + 4 * g]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty(acc));
+#pragma unroll
+          for (int g = 0; g < HC / 8; ++g) {
+            const int n = nbase + col0 + 8 * g;
+            if (m < p.M && n < p.N)
               *reinterpret_cast<uint4*>(drow + n) =
                   make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
           }

@@ -418,38 +418,29 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       const int m = (c.m_blk * 2 + static_cast<int>(rank & 1u)) * C::BM + row;
       const int nbase = c.n_blk * C::BN;
-      uint32_t packed[HC / 2];
+      // The whole row segment comes out of TMEM before any arithmetic and the accumulator is
+      // released at once: the next tile's MMAs need all of it, and holding it through the
+      // epilogue math stalled them for longer than the math itself takes.
+      uint32_t r[HC];
 #pragma unroll
-      for (int ch = 0; ch < HC / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float v[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[8 * g + i]);
-          epi_pack<OUT, 8>(p, nbase + col0 + ch * 32 + 8 * g, v, alpha, &packed[ch * 16 + 4 * g]);
-        }
-      }
+      for (int ch = 0; ch < HC / 32; ++ch)
+        tmem_ld_32x32b_x32(t_row + col0 + ch * 32, reinterpret_cast<uint32_t(&)[32]>(r[32 * ch]));
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      // the accumulator rows of this warp are read (tcgen05.wait::ld above): release them
       if (lane == 0) {
         if (is_leader)
           mbar_arrive(bar_tempty);
         else
           tc_commit_pair_mc(bar_tempty, leader_mask);
       }
-      if (m < p.M) {
-        uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+      uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
 #pragma unroll
-        for (int g = 0; g < HC / 8; ++g) {
-          const int n = nbase + col0 + 8 * g;
-          if (n < p.N)
-            *reinterpret_cast<uint4*>(drow + n) =
-                make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
-        }
+      for (int g = 0; g < HC / 8; ++g) {
+        const int n = nbase + col0 + 8 * g;
+        uint32_t o[4];
+        epi_pack<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[8 * g]), alpha, o);
+        if (m < p.M && n < p.N) *reinterpret_cast<uint4*>(drow + n) = make_uint4(o[0], o[1], o[2], o[3]);
       }
       acc_phase ^= 1u;
     }
