@@ -10,7 +10,7 @@ namespace bsg {
 
 enum : int { KIND_MX = 0, KIND_NV = 1 };
 enum : int { OUT_F16 = 0, OUT_BF16 = 1 };
-enum : unsigned { F_BIAS = 1u, F_SILU = 2u, F_ALPHA_DEVICE = 4u };
+enum : unsigned { F_BIAS = 1u, F_SILU = 2u, F_ALPHA_DEVICE = 4u, F_D32 = 8u /* D 32-byte aligned (set by the host) */ };
 
 // How split-K partial tiles are combined: not split; FP32 partials in the plan's global
 // workspace, summed by the last split to arrive; or the splits of a tile form one thread-block

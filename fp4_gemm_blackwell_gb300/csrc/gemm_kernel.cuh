@@ -185,6 +185,17 @@ __device__ __forceinline__ float out_to_float(uint16_t bits) {
   }
 }
 
+// 16 output values (8 packed words) of one row at d: one 32-byte store when D is 32-byte aligned
+// (a whole L2 sector per lane; n is a multiple of 16 and N % 16 == 0), else two 16-byte stores.
+__device__ __forceinline__ void st_out16(uint16_t* d, const uint32_t (&o)[8], bool wide) {
+  if (wide) {
+    st_global_v8(d, o);
+  } else {
+    reinterpret_cast<uint4*>(d)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(d)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // alpha, bias[n + i], SiLU on W consecutive accumulator values of one row, rounded to the
 // output type and packed two per word.  Columns at or beyond N read no bias.
 template <int OUT, int W>
@@ -667,12 +678,14 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(acc));
+          const bool wide = p.flags & F_D32;
 #pragma unroll
-          for (int g = 0; g < HC / 8; ++g) {
-            const int n = nbase + col0 + 8 * g;
-            uint32_t o[4];
-            epi_pack<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[8 * g]), alpha, o);
-            if (m < p.M && n < p.N) *reinterpret_cast<uint4*>(drow + n) = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int g = 0; g < HC / 16; ++g) {
+            const int n = nbase + col0 + 16 * g;
+            uint32_t o[8];
+            epi_pack<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[16 * g]), alpha, o);
+            epi_pack<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(&r[16 * g + 8]), alpha, o + 4);
+            if (m < p.M && n < p.N) st_out16(drow + n, o, wide);
           }
         } else {
           // Two accumulators: the next tile's MMAs run in the other one, so the segment is
@@ -695,12 +708,11 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(acc));
+          const bool wide = p.flags & F_D32;
 #pragma unroll
-          for (int g = 0; g < HC / 8; ++g) {
-            const int n = nbase + col0 + 8 * g;
-            if (m < p.M && n < p.N)
-              *reinterpret_cast<uint4*>(drow + n) =
-                  make_uint4(packed[4 * g], packed[4 * g + 1], packed[4 * g + 2], packed[4 * g + 3]);
+          for (int g = 0; g < HC / 16; ++g) {
+            const int n = nbase + col0 + 16 * g;
+            if (m < p.M && n < p.N) st_out16(drow + n, reinterpret_cast<const uint32_t(&)[8]>(packed[8 * g]), wide);
           }
         }
       } else if constexpr (BN >= 64) {  // split-K is planned for tiles 64 columns wide or more

@@ -415,7 +415,7 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->M = d->M;
   g->N = d->N;
   g->K = d->K;
-  g->flags = d->flags;
+  g->flags = d->flags | ((reinterpret_cast<uintptr_t>(d->D) & 31u) == 0 ? bsg::F_D32 : 0u);
   g->sfa_atoms_per_band = (d->K / blk + 3) / 4;
   g->sfb_atoms_per_band = g->sfa_atoms_per_band;
   g->sfb_bands = (d->N + 127) / 128;

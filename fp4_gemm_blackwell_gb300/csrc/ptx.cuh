@@ -78,8 +78,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// Tiled load for CTA pairs: the destination is this CTA's shared memory, the completion may
-// be counted on the pair leader's barrier (`bar` a shared::cluster address).
 // The same box delivered to every CTA of the cluster named in cta_mask, at this CTA's shared
 // memory offset `dst`, each completing on its own barrier at offset `bar`.
 __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
@@ -90,6 +88,8 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
       : "memory");
 }
+// Tiled load for CTA pairs: the destination is this CTA's shared memory, the completion may
+// be counted on the pair leader's barrier (`bar` a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
                                                  int32_t y) {
   asm volatile(
@@ -97,6 +97,13 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
       : "memory");
+}
+
+// 32-byte global store of eight words (the address 32-byte aligned): a whole L2 sector per lane.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // 1-D bulk load global -> shared (16-byte aligned addresses, size a multiple of 16).

@@ -156,6 +156,23 @@ def test_multicast_wait_timeout_reports_status(monkeypatch):
 
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("env", [{"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 128},
+                                 {"BSG_FORCE_BN": 64}, {"BSG_FORCE_BN": 32}])
+def test_output_only_16_byte_aligned(kind, env, monkeypatch):
+    # D 16 bytes past a 32-byte boundary: the epilogues fall back from 32-byte to 16-byte stores
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    prob = P.make_problem(kind, 300, 272, 512)
+    dp = P.DeviceProblem(prob, out="bf16", bias=True, silu=kind == "nvfp4", margin=8)
+    assert dp.D.data_ptr() % 32 == 16
+    with dp.plan() as plan:
+        plan.run()
+        plan.check_status()
+        got = dp.result()
+    P.assert_parity(got, prob, "bf16", dp.bias_vals, kind == "nvfp4")
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("M,N,K,out", [(256, 256, 512, "bf16"), (300, 272, 1024, "f16"), (2048, 2560, 512, "bf16"),
                                        (640, 768, 4096, "bf16")])
 def test_pair_kernel(kind, M, N, K, out, monkeypatch):
