@@ -738,37 +738,46 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
               braw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
           }
           if (threadIdx.x == C::EPI_WARP0 * 32)
-            mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>((S - 1) * R * BN * 4));
-          cluster_wait();  // every CTA of the cluster has initialised its receive barrier
-          cluster_waited = true;
-          const uint32_t off = static_cast<uint32_t>(c.split) * slab_bytes +
-                               static_cast<uint32_t>((lr * (BN + 4) + col0) * 4);
+            mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(S - 1) * slab_bytes);
+          // Partial rows leave TMEM into shared memory: this CTA's own rows into its receive slot
+          // `split`, every peer's rows into a staging slab of the ring (idle: the unit's MMAs have
+          // completed and no copy is pending), laid out as the peer's slot.  Then one bulk copy per
+          // peer moves a whole slab over DSMEM (complete-tx on the peer's receive barrier), which
+          // runs several times faster than per-thread remote stores.
           const bool mine = owner == c.split;
-          const uint32_t dst = mine ? recv0 + off : mapa_shared(recv0 + off, static_cast<uint32_t>(owner));
-          const uint32_t rbar = mine ? 0u : mapa_shared(bar_recv, static_cast<uint32_t>(owner));
+          const uint32_t dst = (mine ? recv0 + static_cast<uint32_t>(c.split) * slab_bytes
+                                     : smem0 + static_cast<uint32_t>(owner) * slab_bytes) +
+                               static_cast<uint32_t>((lr * (BN + 4) + col0) * 4);
 #pragma unroll 1
           for (int ch = 0; ch < HC / 32; ++ch) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const uint32_t a = dst + static_cast<uint32_t>((ch * 32 + 4 * g) * 4);
-              if (mine)
-                sts_u4(a, make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]));
-              else
-                st_async_v4(a, __uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]), rbar);
-            }
+            for (int g = 0; g < 8; ++g)
+              sts_u4(dst + static_cast<uint32_t>((ch * 32 + 4 * g) * 4),
+                     make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]));
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(acc));
+          fence_proxy_async_smem();  // the staging slabs are read by the bulk copies (async proxy)
+          named_bar_sync(1, C::EPI_THREADS);
+          cluster_wait();  // every CTA of the cluster has initialised its receive barrier
+          cluster_waited = true;
+          const bool sender = et < S && et != c.split;  // one thread per peer
+          if (sender) {
+            bulk_copy_s2c(mapa_shared(recv0 + static_cast<uint32_t>(c.split) * slab_bytes, static_cast<uint32_t>(et)),
+                          smem0 + static_cast<uint32_t>(et) * slab_bytes, slab_bytes,
+                          mapa_shared(bar_recv, static_cast<uint32_t>(et)));
+            bulk_commit_group();
+          }
           const bool got = named_bar_and(1, C::EPI_THREADS,
                                          wait_bounded_cluster(bar_recv, 0, abort_flag, p, ST_TIMEOUT_EPILOGUE));
           if (got)
             cluster_reduce<OUT, BN>(p, reinterpret_cast<const float*>(smem + nst * C::STAGE_BYTES), c, alpha, braw,
                                     et);
+          if (sender) bulk_wait_group0();  // the slab has reached the peer before this CTA may leave
         } else {
           // FP32 partial tile -> workspace as float4 [chunk][8][128 rows] (coalesced per warp)
           float4* part = reinterpret_cast<float4*>(

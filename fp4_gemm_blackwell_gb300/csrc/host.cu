@@ -443,6 +443,9 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
     g->ring_stages = info.stages - static_cast<int>((recv + info.stage_bytes - 1) / info.stage_bytes);
     if (g->ring_stages < 2)
       return fail(BSG_ERR_SHAPE, "split-K cluster receive slots leave fewer than two ring stages");
+    // the peers' partial rows are staged in the ring before their bulk copies
+    if (recv > static_cast<long long>(g->ring_stages) * info.stage_bytes)
+      return fail(BSG_ERR_SHAPE, "split-K cluster staging does not fit the ring");
   }
   if (v.pair) *grid = 2 * std::min(g->num_units, sms / 2);
   else if (g->cm > 1) *grid = g->cm * std::min(g->num_units, resident_ctas / g->cm);

@@ -399,6 +399,7 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // 16 bytes from registers into the shared memory of a CTA of the cluster (shared::cluster address
 // `dst`), counted as complete-tx bytes on that CTA's mbarrier `bar` (shared::cluster address).
 __device__ __forceinline__ void st_async_v4(uint32_t dst, float a, float b, float c, float d, uint32_t bar) {
