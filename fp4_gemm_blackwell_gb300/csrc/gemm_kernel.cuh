@@ -271,19 +271,30 @@ __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const floa
   constexpr int R = 128 / S;
   constexpr int C4 = BN / 4;          // column groups per row
   constexpr int RP = 256 / C4;        // rows per pass of the 256 epilogue threads
+  constexpr int NP = R / RP;          // passes (R is a multiple of RP for S <= 8)
+  static_assert(R % RP == 0 && NP >= 1, "reduction passes");
   const int c4 = t % C4;
   const int col = 4 * c4;
   const int n = c.n_blk * BN + col;
+  const int r0 = t / C4;
+  // every shared-memory read first (a fixed number of passes, so all of them are in flight
+  // together), then the sums in split order, the epilogue and the stores
+  float4 part[NP][S];
 #pragma unroll
-  for (int rl = t / C4; rl < R; rl += RP) {
-    float4 acc = *reinterpret_cast<const float4*>(slabs + rl * (BN + 4) + col);
+  for (int i = 0; i < NP; ++i)
+#pragma unroll
+    for (int sp = 0; sp < S; ++sp)
+      part[i][sp] = *reinterpret_cast<const float4*>(slabs + (sp * R + r0 + i * RP) * (BN + 4) + col);
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int rl = r0 + i * RP;
+    float4 acc = part[i][0];
 #pragma unroll
     for (int sp = 1; sp < S; ++sp) {
-      const float4 v = *reinterpret_cast<const float4*>(slabs + (sp * R + rl) * (BN + 4) + col);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+      acc.x += part[i][sp].x;
+      acc.y += part[i][sp].y;
+      acc.z += part[i][sp].z;
+      acc.w += part[i][sp].w;
     }
     // slab row rl holds tile row (rl / LPO) * 32 + split * LPO + rl % LPO, LPO = 32 / S
     const int row = (rl / (32 / S)) * 32 + c.split * (32 / S) + rl % (32 / S);
