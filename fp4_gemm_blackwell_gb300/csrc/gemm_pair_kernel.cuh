@@ -46,7 +46,8 @@ struct PairCfg {
   // SEP: the scale atoms have their own two-stage ring and two TMEM slots, apart from the code
   // ring (NVFP4 with two k-slabs: 12 KB of atoms per stage would leave room for only two 76 KB
   // stages, and 96 TMEM columns per slot for only two slots).  The scale warps release a scale
-  // stage once they have copied it; a TMEM slot is released by the MMAs' commit.
+  // stage once they have copied it; a TMEM slot is free again once the MMAs of the code stage
+  // that last used it have completed (that code stage's `empty` barrier).
   static constexpr bool SEP = KIND == KIND_NV && KC == 2;
   static constexpr int SF_STAGE_BYTES = (SFA_BYTES + SFB_BYTES + 1023) / 1024 * 1024;
   static constexpr int SF_STAGES = SEP ? 2 : 0;
@@ -99,16 +100,13 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
   uint8_t* aux = smem + C::STAGES * C::STAGE_BYTES + C::SF_STAGES * C::SF_STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(aux);
   // slots: full[0..7], empty[8..15], sf_full[16..23], tmem_full 32, tmem_empty 33, drain 34,
-  // tmem address 35, abort flag 36; with a separate scale ring also sf_empty[40..47],
-  // slot_free[48..55] and sfready[56..63].  Without it, the leader's `full` completes when both
-  // CTAs' code tiles have landed and both CTAs' scale warps have filled their TMEM slots: one
-  // wait per stage for the MMA issuer.
+  // tmem address 35, abort flag 36; with a separate scale ring also sf_empty[40..47].  The
+  // leader's `full` completes when both CTAs' code tiles have landed and both CTAs' scale warps
+  // have filled their TMEM slots: one wait per stage for the MMA issuer.
   auto bar_full = [&](int s) { return smem_u32(bars + s); };
   auto bar_empty = [&](int s) { return smem_u32(bars + 8 + s); };
   auto bar_sf_full = [&](int s) { return smem_u32(bars + 16 + s); };
-  auto bar_sf_empty = [&](int t) { return smem_u32(bars + 40 + t); };   // scale stage copied (SEP)
-  auto bar_slot_free = [&](int t) { return smem_u32(bars + 48 + t); };  // TMEM slot read (SEP)
-  auto bar_sfready = [&](int t) { return smem_u32(bars + 56 + t); };    // TMEM slot filled (SEP)
+  auto bar_sf_empty = [&](int t) { return smem_u32(bars + 40 + t); };  // scale stage copied (SEP)
   const uint32_t bar_tfull = smem_u32(bars + 32);
   const uint32_t bar_tempty = smem_u32(bars + 33);
   const uint32_t bar_drain = smem_u32(bars + 34);
@@ -127,15 +125,11 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     for (int s = 0; s < C::STAGES; ++s) {
       // the leader's producer (with both CTAs' code bytes) and, without a separate scale ring,
       // the scale warps of both CTAs
-      mbar_init(bar_full(s), C::SEP ? 1 : 1 + 8);
+      mbar_init(bar_full(s), 1 + 8);
       mbar_init(bar_empty(s), 1);    // the leader's multicast commit
       mbar_init(bar_sf_full(s), 1);  // this CTA's producer (scale bytes)
     }
-    for (int t = 0; t < C::SF_STAGES; ++t) {
-      mbar_init(bar_sf_empty(t), 4);   // this CTA's scale warps
-      mbar_init(bar_slot_free(t), 1);  // the leader's multicast commit
-      mbar_init(bar_sfready(t), 8);    // the scale warps of both CTAs
-    }
+    for (int t = 0; t < C::SF_STAGES; ++t) mbar_init(bar_sf_empty(t), 4);  // this CTA's scale warps
     mbar_init(bar_tfull, 1);
     mbar_init(bar_tempty, 2 * C::EPI_WARPS);  // one arrival per epilogue warp of each CTA
     mbar_init(bar_drain, 1);
@@ -261,8 +255,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
       if (is_leader && lane == 0) {
         int stage = 0;
         uint32_t phase = 0;
-        int sst = 0;  // scale slot (SEP)
-        uint32_t sph = 0;
+        int sst = 0;  // TMEM scale slot (SEP): the scale ring's stage
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int u = pair0; ok && u < p.num_units; u += pairs) {
@@ -273,8 +266,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
           }
           tc_fence_after();
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
-            if (!wait_bounded_cluster(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA) ||
-                (C::SEP && !wait_bounded_cluster(bar_sfready(sst), sph, abort_flag, p, ST_TIMEOUT_MMA))) {
+            if (!wait_bounded_cluster(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
@@ -309,11 +301,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
               phase ^= 1u;
             }
             if constexpr (C::SEP) {
-              tc_commit_pair_mc(bar_slot_free(sst), pair_mask);  // this scale slot may be refilled
-              if (++sst == C::SF_STAGES) {
-                sst = 0;
-                sph ^= 1u;
-              }
+              if (++sst == C::SF_STAGES) sst = 0;
             }
           }
           if (!ok) break;
@@ -339,19 +327,35 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     // 4t + k holds the four scales of A row 32k + i of atom t (this CTA's 128 rows), and column
     // 8t + 4b + k those of B row 128b + 32k + i (the pair tile's 256 rows).
     // With a separate scale ring (SEP) the stage index is the scale stage, which is also the TMEM
-    // slot: it is filled once the MMAs that read its previous contents have completed.
+    // slot: it is refilled once the MMAs that read its previous contents, those of the ring stage
+    // SF_STAGES back, have completed, which the leader's commit to that code stage's `empty`
+    // barrier (multicast to both CTAs) tells.  Either way the scale warps arrive on the code
+    // stage's `full` barrier, so the MMA issuer waits once per stage and commits once.
     constexpr int NR = C::SEP ? C::SF_STAGES : C::STAGES;
     const int q = warp & 3;
     const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
     int stage = 0;
     uint32_t phase = 0;
+    int cs = 0;                   // code stage of this k-stage (SEP)
+    int cs_old = 0, lag = 0;      // code stage SF_STAGES k-stages back, once there is one (SEP)
+    uint32_t ph_old = 0;
     bool ok = true;
     for (int u = pair0; ok && u < p.num_units; u += pairs) {
       const UnitCoord c = decode_unit(p, u, 0);
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
-        ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES) &&
-                                         (!C::SEP || wait_bounded_cluster(bar_slot_free(stage), phase ^ 1u,
-                                                                          abort_flag, p, ST_TIMEOUT_SCALES)));
+        bool got = wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES);
+        if constexpr (C::SEP) {
+          if (lag == C::SF_STAGES) {
+            got = got && wait_bounded_cluster(bar_empty(cs_old), ph_old, abort_flag, p, ST_TIMEOUT_SCALES);
+            if (++cs_old == C::STAGES) {
+              cs_old = 0;
+              ph_old ^= 1u;
+            }
+          } else {
+            ++lag;
+          }
+        }
+        ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
         const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
         // atoms in groups of up to four: 16 A columns and 32 B columns per group
@@ -386,13 +390,14 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
           // The peer signals through the tensor-core commit path, which arrives on the leader's
           // barrier without holding this thread for the cluster round trip that a remote
           // mbarrier arrive takes (its stores to TMEM are complete: tcgen05.wait::st above).
-          const uint32_t ready = C::SEP ? bar_sfready(stage) : bar_full(stage);
+          const uint32_t ready = C::SEP ? bar_full(cs) : bar_full(stage);
           if (is_leader)
             mbar_arrive(ready);
           else
             tc_commit_pair_mc(ready, leader_mask);
           if (C::SEP) mbar_arrive(bar_sf_empty(stage));  // the scale stage may be refilled
         }
+        if (C::SEP && ++cs == C::STAGES) cs = 0;
         if (++stage == NR) {
           stage = 0;
           phase ^= 1u;
