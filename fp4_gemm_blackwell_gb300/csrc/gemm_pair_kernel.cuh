@@ -343,27 +343,13 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     for (int u = pair0; ok && u < p.num_units; u += pairs) {
       const UnitCoord c = decode_unit(p, u, 0);
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
-        bool got = wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES);
-        if constexpr (C::SEP) {
-          if (lag == C::SF_STAGES) {
-            got = got && wait_bounded_cluster(bar_empty(cs_old), ph_old, abort_flag, p, ST_TIMEOUT_SCALES);
-            if (++cs_old == C::STAGES) {
-              cs_old = 0;
-              ph_old ^= 1u;
-            }
-          } else {
-            ++lag;
-          }
-        }
-        ok = __all_sync(0xffffffffu, got);
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
         if (!ok) break;
         const uint32_t slot = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS + (static_cast<uint32_t>(q * 32) << 16);
         // atoms in groups of up to four: 16 A columns and 32 B columns per group
         constexpr int NA = C::SF_ATOMS;
         constexpr int GA = NA < 4 ? NA : 4;
-#pragma unroll
-        for (int g0 = 0; g0 < NA; g0 += GA) {
-          uint32_t a[4 * GA], b[8 * GA];
+        auto load_group = [&](int g0, uint32_t (&a)[4 * GA], uint32_t (&b)[8 * GA]) {
 #pragma unroll
           for (int t = 0; t < GA; ++t) {
             const uint4 v = lds_u4(stage_sfa(stage) + 512 * (g0 + t) + 16 * lane);
@@ -380,6 +366,30 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
               b[(2 * t + rb) * 4 + 3] = w.w;
             }
           }
+        };
+        // The first group is read from shared memory before the TMEM slot is known to be free
+        // (SEP: the MMAs of the stage SF_STAGES back may still be reading it), so that only the
+        // stores into TMEM follow the MMAs' completion.
+        uint32_t a[4 * GA], b[8 * GA];
+        load_group(0, a, b);
+        if constexpr (C::SEP) {
+          if (lag == C::SF_STAGES) {
+            ok = __all_sync(0xffffffffu,
+                            wait_bounded_cluster(bar_empty(cs_old), ph_old, abort_flag, p, ST_TIMEOUT_SCALES));
+            if (!ok) break;
+            if (++cs_old == C::STAGES) {
+              cs_old = 0;
+              ph_old ^= 1u;
+            }
+          } else {
+            ++lag;
+          }
+        }
+        tmem_st_cols(slot, a);
+        tmem_st_cols(slot + C::SFA_COLS, b);
+#pragma unroll
+        for (int g0 = GA; g0 < NA; g0 += GA) {
+          load_group(g0, a, b);
           tmem_st_cols(slot + 4 * g0, a);
           tmem_st_cols(slot + C::SFA_COLS + 8 * g0, b);
         }
