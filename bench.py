@@ -382,6 +382,49 @@ def small_config(bsg, peaks, steps=2000, warmup=20):
     return r
 
 
+def quantiser(bsg, peaks, kind, rows, K, bf16, steps=50, warmup=5):
+    """bsg_quantize / bsg_quantize_bf16 on a rows x K activation (float32 or BF16), timed as one
+    CUDA-graph replay of `steps` calls.  Algorithmic bytes: the input once, the codes, the
+    swizzled scale buffer (and the 4-byte global scale); NVFP4 reads its input twice (tensor
+    amax, then the blocks), which the roofline counts as the kernel's own cost, not as bytes."""
+    import torch
+    from fp4_gemm_blackwell_gb300 import synth
+    k = bsg.BSG_MXFP8 if kind == "mxfp8" else bsg.BSG_NVFP4
+    x = synth.normal_rowscaled(rows, K, seed=0)
+    xd = (torch.from_numpy(synth.as_bf16_bits(x).view(np.int16)) if bf16 else torch.from_numpy(x)).cuda()
+    code_bytes = rows * K if kind == "mxfp8" else rows * K // 2
+    codes = torch.empty(code_bytes, dtype=torch.uint8, device="cuda")
+    sf_bytes = bsg.bsg_sf_bytes(k, rows, K)
+    sf = torch.empty(sf_bytes, dtype=torch.uint8, device="cuda")
+    gs = torch.empty(1, dtype=torch.float32, device="cuda")
+    fn = bsg.bsg_quantize_bf16 if bf16 else bsg.bsg_quantize
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn(k, xd, rows, K, codes, sf, gs, stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(steps):
+            fn(k, xd, rows, K, codes, sf, gs, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    us = start.elapsed_time(end) * 1e3 / steps
+    nbytes = xd.numel() * xd.element_size() + code_bytes + sf_bytes + (4 if kind == "nvfp4" else 0)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del g
+    return {"us": round(us, 2), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "algorithmic_bytes": nbytes, "input": "bf16" if bf16 else "f32", "shape": [rows, K],
+            "launches_per_call": 1 if kind == "mxfp8" else 3}
+
+
 def launch_loop(bsg, calls=1000):
     """1000 NVFP4 GEMM calls cycling M in {1,16,128,1024} x (N,K) in {(4096,4096),(14336,4096),
     (4096,14336)}, BF16 out: host time per call against device kernel time, (i) one-shot C-ABI
@@ -634,6 +677,10 @@ def main():
             extras["nvfp4_8000x8192x8192_bias_silu_bf16"] = big_config(bsg, peaks, "nvfp4", 8000, 8192, 8192, "bf16",
                                                                        True, True)
             extras["launch_loop_1000"] = launch_loop(bsg)
+            for kind in ("mxfp8", "nvfp4"):
+                for bf in (False, True):
+                    extras["quantize_%s_%s_8192x8192" % (kind, "bf16" if bf else "f32")] = quantiser(
+                        bsg, peaks, kind, 8192, 8192, bf)
         cpu = cpu_baseline() if not args.quick else None
         result = {
             "metric": METRIC, "value": round(value, 4), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,

@@ -12,7 +12,7 @@ import os
 
 __all__ = [
     "BSG_MXFP8", "BSG_NVFP4", "BSG_OUT_F16", "BSG_OUT_BF16", "BSG_F_BIAS", "BSG_F_SILU",
-    "BSG_F_ALPHA_DEVICE", "BsgError", "lib", "bsg_sf_bytes", "bsg_quantize", "bsg_plan_create",
+    "BSG_F_ALPHA_DEVICE", "BsgError", "lib", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_plan_create",
     "bsg_plan_run", "bsg_plan_destroy", "bsg_plan_check_status", "bsg_plan_variant",
     "bsg_plan_debug_set", "mxfp8_gemm", "nvfp4_gemm", "bsg_cache_clear", "bsg_last_error",
     "bsg_version", "Plan", "bsg_gemm_noalloc",
@@ -74,6 +74,7 @@ def lib():
         "bsg_gemm_noalloc": (st, [ctypes.POINTER(BsgDesc), vp]),
         "bsg_sf_bytes": (ctypes.c_size_t, [i, i, i]),
         "bsg_quantize": (st, [i, vp, i, i, vp, vp, vp, vp]),
+        "bsg_quantize_bf16": (st, [i, vp, i, i, vp, vp, vp, vp]),
         "bsg_last_error": (ctypes.c_char_p, []),
         "bsg_version": (ctypes.c_char_p, []),
     }
@@ -122,6 +123,12 @@ def bsg_sf_bytes(kind, rows, K):
 def bsg_quantize(kind, x, rows, K, codes, sf, global_scale=None, stream=None):
     _check(lib().bsg_quantize(kind, _ptr(x), rows, K, _ptr(codes), _ptr(sf), _ptr(global_scale),
                               _stream(stream)))
+
+
+def bsg_quantize_bf16(kind, x, rows, K, codes, sf, global_scale=None, stream=None):
+    """x: rows x K BF16 values (a torch.bfloat16 tensor or 16-bit integer bit patterns)."""
+    _check(lib().bsg_quantize_bf16(kind, _ptr(x), rows, K, _ptr(codes), _ptr(sf), _ptr(global_scale),
+                                   _stream(stream)))
 
 
 def bsg_plan_create(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None):

@@ -86,10 +86,15 @@ bool gemm_kernel_info_nv_kc2(int bn, int out, GemmKernelInfo* info);
 bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info);  // BSG_PAIR_KC=1 or 2 (default 2)
 bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info);  // BSG_PAIR_KC=1 or 2 (default 2)
 
-// Quantisers (stream-ordered).  See bsg_quantize in include/bsgemm.h.
+// Quantisers (stream-ordered).  See bsg_quantize / bsg_quantize_bf16 in include/bsgemm.h; the
+// uint16_t forms read BF16 bit patterns.
 cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
                                cudaStream_t s);
+cudaError_t launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               cudaStream_t s);
 cudaError_t launch_quantize_nv(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               float* global_scale, cudaStream_t s);
+cudaError_t launch_quantize_nv(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
                                float* global_scale, cudaStream_t s);
 
 }  // namespace bsg

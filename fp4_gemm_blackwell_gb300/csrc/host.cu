@@ -749,8 +749,11 @@ BSG_API bsg_status bsg_cache_clear(void) {
 }
 
 // ---------------------------------------------------------------- quantiser
-BSG_API bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, void* codes, void* sf,
-                                float* global_scale, bsg_stream_t stream) {
+// Shared by both quantiser entry points: validation, then the launch for element type T
+// (float32, or BF16 bit patterns as uint16_t).
+template <typename T>
+static bsg_status quantize_entry(bsg_kind kind, const T* x, int rows, int K, void* codes, void* sf,
+                                 float* global_scale, bsg_stream_t stream) {
   if (kind != BSG_MXFP8 && kind != BSG_NVFP4) return fail(BSG_ERR_INVALID_ARG, "unknown kind %d", kind);
   if (rows < 1 || K < 32 || K % 32 || rows > kMaxDim || K > kMaxDim)
     return fail(BSG_ERR_SHAPE, "quantise shape rows=%d K=%d (rows>=1, K>=32, K%%32==0, each <= 2^20)", rows, K);
@@ -764,7 +767,7 @@ BSG_API bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, 
   bsg_status s = current_device(&dev, &di);
   if (s != BSG_OK) return s;
   load_driver_entry_points();
-  if ((s = check_range(x, static_cast<size_t>(rows) * K * 4, BSG_ERR_SHAPE, "x")) != BSG_OK ||
+  if ((s = check_range(x, static_cast<size_t>(rows) * K * sizeof(T), BSG_ERR_SHAPE, "x")) != BSG_OK ||
       (s = check_range(codes, code_row_bytes(kind, K) * rows, BSG_ERR_SHAPE, "codes")) != BSG_OK ||
       (s = check_range(sf, sf_bytes_of(kind, rows, K), BSG_ERR_SCALE_LAYOUT, "sf")) != BSG_OK ||
       (kind == BSG_NVFP4 && (s = check_range(global_scale, 4, BSG_ERR_SHAPE, "global_scale")) != BSG_OK))
@@ -777,6 +780,16 @@ BSG_API bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, 
                                     global_scale, st);
   if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
   return BSG_OK;
+}
+
+BSG_API bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, void* codes, void* sf,
+                                float* global_scale, bsg_stream_t stream) {
+  return quantize_entry(kind, x, rows, K, codes, sf, global_scale, stream);
+}
+
+BSG_API bsg_status bsg_quantize_bf16(bsg_kind kind, const void* x, int rows, int K, void* codes, void* sf,
+                                     float* global_scale, bsg_stream_t stream) {
+  return quantize_entry(kind, static_cast<const uint16_t*>(x), rows, K, codes, sf, global_scale, stream);
 }
 
 // ==================================================================== allocation-free GEMM

@@ -1,4 +1,6 @@
-// Quantisers: row-major float32 -> block-scaled codes + swizzled 128x4 scale atoms.
+// Quantisers: row-major float32 or BF16 -> block-scaled codes + swizzled 128x4 scale atoms.
+// A BF16 input is widened to float32 exactly (its bits are the upper half of the float32's),
+// so it quantises to the same bytes as its float32 value.
 //
 // MXFP8 ("Add Cutlass MxFp8 Block Scale Matrix Multiplication", test step
 // pytorch_mxfp8_quantize with block size 32, then linear_to_swizzled_128_4): per 32-element
@@ -41,7 +43,36 @@ __device__ __forceinline__ float exp2_neg(int e) {
   return be >= 1 ? __uint_as_float(static_cast<uint32_t>(be) << 23) : __uint_as_float(0x00400000u);
 }
 
-__global__ void __launch_bounds__(256) quantize_mx_kernel(const float* __restrict__ x, int rows, int K,
+// N consecutive input elements as float32: float4 loads, or 16-byte loads of eight BF16 each.
+template <int N>
+__device__ __forceinline__ void load_f32(const float* p, float (&v)[N]) {
+  const float4* src = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int j = 0; j < N / 4; ++j) {
+    const float4 t = __ldg(src + j);
+    v[4 * j] = t.x;
+    v[4 * j + 1] = t.y;
+    v[4 * j + 2] = t.z;
+    v[4 * j + 3] = t.w;
+  }
+}
+template <int N>
+__device__ __forceinline__ void load_f32(const uint16_t* p, float (&v)[N]) {
+  const uint4* src = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int j = 0; j < N / 8; ++j) {
+    const uint4 t = __ldg(src + j);
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[8 * j + 2 * h] = __uint_as_float(w[h] << 16);
+      v[8 * j + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_mx_kernel(const T* __restrict__ x, int rows, int K,
                                                           uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ sf, int rows_pad,
                                                           int cols4) {
@@ -54,16 +85,8 @@ __global__ void __launch_bounds__(256) quantize_mx_kernel(const float* __restric
     const int c = static_cast<int>(i % cols_pad);
     uint8_t code = 0;
     if (r < rows && c < nblk) {
-      const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(r) * K + c * 32);
       float v[32];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 t = __ldg(src + j);
-        v[4 * j] = t.x;
-        v[4 * j + 1] = t.y;
-        v[4 * j + 2] = t.z;
-        v[4 * j + 3] = t.w;
-      }
+      load_f32(x + static_cast<size_t>(r) * K + c * 32, v);
       float amax = 0.0f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
@@ -86,15 +109,18 @@ __global__ void __launch_bounds__(256) quantize_mx_kernel(const float* __restric
 }
 
 // amax(|x|) into *amax_bits (float bits; non-negative floats order like unsigned integers).
-__global__ void __launch_bounds__(256) amax_kernel(const float* __restrict__ x, long long n,
+// n is a multiple of 32 (K % 32 == 0): eight elements per step.
+template <typename T>
+__global__ void __launch_bounds__(256) amax_kernel(const T* __restrict__ x, long long n,
                                                    unsigned* __restrict__ amax_bits) {
   float m = 0.0f;
-  const long long n4 = n / 4;
-  const float4* x4 = reinterpret_cast<const float4*>(x);
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+  const long long n8 = n / 8;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 t = __ldg(x4 + i);
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(t.x), fabsf(t.y)), fmaxf(fabsf(t.z), fabsf(t.w))));
+    float v[8];
+    load_f32(x + i * 8, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -115,7 +141,8 @@ __device__ __forceinline__ float ue4m3_value(uint32_t code) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-__global__ void __launch_bounds__(256) quantize_nv_kernel(const float* __restrict__ x, int rows, int K,
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_nv_kernel(const T* __restrict__ x, int rows, int K,
                                                           uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ sf, int rows_pad,
                                                           int cols4,
@@ -132,16 +159,8 @@ __global__ void __launch_bounds__(256) quantize_nv_kernel(const float* __restric
     const int c = static_cast<int>(i % cols_pad);
     uint8_t code = 0;
     if (r < rows && c < nblk) {
-      const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(r) * K + c * 16);
       float v[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 t = __ldg(src + j);
-        v[4 * j] = t.x;
-        v[4 * j + 1] = t.y;
-        v[4 * j + 2] = t.z;
-        v[4 * j + 3] = t.w;
-      }
+      load_f32(x + static_cast<size_t>(r) * K + c * 16, v);
       float bmax = 0.0f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(v[j]));
@@ -179,32 +198,50 @@ static int grid_for(long long n, int threads) {
   return static_cast<int>(b);
 }
 
-cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
-                               cudaStream_t s) {
+template <typename T>
+cudaError_t quantize_mx(const T* x, int rows, int K, uint8_t* codes, uint8_t* sf, cudaStream_t s) {
   const int rows_pad = (rows + 127) / 128 * 128;
   const int cols4 = (K / 32 + 3) / 4;
   const long long total = static_cast<long long>(rows_pad) * cols4 * 4;
-  quantize_mx_kernel<<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4);
+  quantize_mx_kernel<T><<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_nv(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
-                               float* global_scale, cudaStream_t s) {
+template <typename T>
+cudaError_t quantize_nv(const T* x, int rows, int K, uint8_t* codes, uint8_t* sf, float* global_scale,
+                        cudaStream_t s) {
   const int rows_pad = (rows + 127) / 128 * 128;
   const int cols4 = (K / 16 + 3) / 4;
   const long long total = static_cast<long long>(rows_pad) * cols4 * 4;
   cudaError_t e = cudaMemsetAsync(global_scale, 0, sizeof(float), s);
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(rows) * K;
-  amax_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(global_scale));
+  amax_kernel<T><<<grid_for(n / 8, 256), 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(global_scale));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  quantize_nv_kernel<<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4,
-                                                          reinterpret_cast<unsigned*>(global_scale));
+  quantize_nv_kernel<T><<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4,
+                                                             reinterpret_cast<unsigned*>(global_scale));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   nv_finalize_kernel<<<1, 1, 0, s>>>(global_scale);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               cudaStream_t s) {
+  return quantize_mx(x, rows, K, codes, sf, s);
+}
+cudaError_t launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               cudaStream_t s) {
+  return quantize_mx(x, rows, K, codes, sf, s);
+}
+cudaError_t launch_quantize_nv(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               float* global_scale, cudaStream_t s) {
+  return quantize_nv(x, rows, K, codes, sf, global_scale, s);
+}
+cudaError_t launch_quantize_nv(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                               float* global_scale, cudaStream_t s) {
+  return quantize_nv(x, rows, K, codes, sf, global_scale, s);
 }
 
 }  // namespace bsg

@@ -10,7 +10,9 @@ Recipe (the workloads of the block-scaled GEMM pages, drawn with a CPU
 * ``normal_rowscaled``: N(0, 1) times one U(0.5, 2) multiplier per row, drawn
   after the matrix from the same generator;
 * ``bias``: N(0, 1) * std, rounded to the output type (bf16 or f16), returned as
-  its 16-bit patterns and as float64 values.
+  its 16-bit patterns and as float64 values;
+* ``as_bf16_bits``: a float32 matrix rounded to BF16 (torch's round to nearest even),
+  returned as 16-bit patterns: the input of the BF16 quantiser.
 Seeds: A = 0, B = 1, bias = 2 unless a caller says otherwise.
 """
 
@@ -46,3 +48,8 @@ def bias(n, seed=SEED_BIAS, std=0.1, out="bf16"):
     t = b.to(torch.bfloat16 if out == "bf16" else torch.float16)
     bits = t.view(torch.int16).numpy().view(np.uint16).copy()
     return bits, t.to(torch.float64).numpy()
+
+
+def as_bf16_bits(x):
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()

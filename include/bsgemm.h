@@ -173,6 +173,16 @@ size_t bsg_sf_bytes(bsg_kind kind, int rows, int K);
 bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, void* codes, void* sf,
                         float* global_scale, bsg_stream_t stream);
 
+/* bsg_quantize for a row-major BF16 matrix x (rows x K 16-bit BF16 values, device, 16-byte
+ * aligned): each element is widened to float32 exactly (a BF16 value is the upper half of a
+ * float32) and quantised as bsg_quantize quantises that float32, so the codes, the scale
+ * buffer and the NVFP4 global scale are the bytes bsg_quantize writes for the widened matrix.
+ * It reads half the bytes: the activation quantiser in front of a GEMM whose input comes out
+ * of a BF16 layer (the MXFP8 page's test quantises its operands before every GEMM).  Same
+ * arguments, ownership, stream ordering and errors as bsg_quantize. */
+bsg_status bsg_quantize_bf16(bsg_kind kind, const void* x, int rows, int K, void* codes, void* sf,
+                             float* global_scale, bsg_stream_t stream);
+
 /* Last error message of the calling thread ("" if none). */
 const char* bsg_last_error(void);
 

@@ -181,6 +181,19 @@ def bf16_from_bits(bits):
     return b.view(np.float32).astype(np.float64)
 
 
+def decode_bf16(bits):
+    """BF16 bit patterns -> float64 values from the bit fields s|eeeeeeee|fffffff (bias 127):
+    e = 0 gives (f/128) 2^-126, e = 255 gives +-inf (f = 0) or NaN, otherwise (1 + f/128) 2^(e-127).
+    The input of the BF16 quantiser (each value is then an exact float32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    s = np.where((b >> 15) & 1, -1.0, 1.0)
+    e = (b >> 7) & 0xFF
+    f = (b & 0x7F).astype(np.float64)
+    mag = np.where(e == 0, np.ldexp(f / 128.0, -126), np.ldexp(1.0 + f / 128.0, np.clip(e, 1, 254) - 127))
+    mag = np.where(e == 255, np.where(f == 0, np.inf, np.nan), mag)
+    return s * mag
+
+
 def f16_from_bits(bits):
     return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
 

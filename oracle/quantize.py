@@ -117,6 +117,17 @@ def quantize_nvfp4(x, s=None):
     return packed, sc.astype(np.uint8), s
 
 
+def quantize_mxfp8_bf16(bits):
+    """BF16 bit patterns [rows, K] -> quantize_mxfp8 of their values (every BF16 value is a
+    float32, so the widening is exact and the recipe is the float32 one unchanged)."""
+    return quantize_mxfp8(F.decode_bf16(bits).astype(np.float32))
+
+
+def quantize_nvfp4_bf16(bits, s=None):
+    """BF16 bit patterns [rows, K] -> quantize_nvfp4 of their values (see quantize_mxfp8_bf16)."""
+    return quantize_nvfp4(F.decode_bf16(bits).astype(np.float32), s)
+
+
 def unpack_e2m1(packed, K):
     """uint8 [rows, K/2] -> E2M1 codes uint8 [rows, K] (low nibble first)."""
     packed = np.asarray(packed, dtype=np.uint8)

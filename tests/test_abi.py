@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for want in ["bsg_plan_create", "bsg_plan_run", "bsg_plan_destroy", "bsg_plan_check_status",
-                 "mxfp8_gemm", "nvfp4_gemm", "bsg_sf_bytes", "bsg_quantize", "bsg_last_error"]:
+                 "mxfp8_gemm", "nvfp4_gemm", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_last_error"]:
         assert want in names
 
 
@@ -96,6 +96,7 @@ def test_null_handles(L):
 def test_quantize_validation(L, args, status):
     kind, x, rows, K, codes, sf, gs = args
     assert L.bsg_quantize(kind, x, rows, K, codes, sf, gs, None) == status
+    assert L.bsg_quantize_bf16(kind, x, rows, K, codes, sf, gs, None) == status
 
 
 def test_one_shot_validation(L):

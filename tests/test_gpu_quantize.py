@@ -27,12 +27,26 @@ def gpu_quantize(kind, x):
     return codes.cpu().numpy(), sf.cpu().numpy(), gs.item()
 
 
-def check(kind, x):
-    codes, sf, gs = gpu_quantize(kind, x)
+def gpu_quantize_bf16(kind, bits):
+    rows, K = bits.shape
+    k = bsg.BSG_MXFP8 if kind == "mxfp8" else bsg.BSG_NVFP4
+    xd = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+    nb = rows * K if kind == "mxfp8" else rows * K // 2
+    codes = torch.full((nb,), 0xCD, dtype=torch.uint8, device="cuda")
+    sf = torch.full((bsg.bsg_sf_bytes(k, rows, K),), 0xAB, dtype=torch.uint8, device="cuda")
+    gs = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    bsg.bsg_quantize_bf16(k, xd, rows, K, codes, sf, gs)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), sf.cpu().numpy(), gs.item()
+
+
+def check(kind, x, bf16=False):
+    """x: float32 values, or (bf16=True) BF16 bit patterns."""
+    codes, sf, gs = gpu_quantize_bf16(kind, x) if bf16 else gpu_quantize(kind, x)
     if kind == "mxfp8":
-        oc, osf = Q.quantize_mxfp8(x)
+        oc, osf = Q.quantize_mxfp8_bf16(x) if bf16 else Q.quantize_mxfp8(x)
     else:
-        oc, osf, s = Q.quantize_nvfp4(x)
+        oc, osf, s = Q.quantize_nvfp4_bf16(x) if bf16 else Q.quantize_nvfp4(x)
         assert np.float32(gs) == s
     assert np.array_equal(codes, oc.ravel()), "codes differ at %s" % np.flatnonzero(codes != oc.ravel())[:8]
     want = L.swizzle(osf)
@@ -78,3 +92,44 @@ def test_full_size_operand_rows():
     # an 8192 x 8192 NVFP4 operand and an 8000-row MXFP8 operand, compared whole
     check("nvfp4", synth.normal_rowscaled(8192, 8192, seed=1))
     check("mxfp8", synth.normal(8000, 8192, seed=0))
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("rows,K", [(1, 32), (128, 256), (200, 96), (129, 160), (256, 4096), (1000, 512)])
+def test_bf16_quantiser_matches_oracle(kind, rows, K):
+    gen = synth.normal if kind == "mxfp8" else synth.normal_rowscaled
+    check(kind, synth.as_bf16_bits(gen(rows, K, seed=rows + K)), bf16=True)
+
+
+def test_bf16_ties_extremes_and_zero():
+    # every E4M3 tie (four fraction bits: exact in BF16) with amax 448, a zero block, the largest
+    # and smallest BF16 magnitudes; NVFP4 closed-form row and an all-zero tensor
+    pos = F.E4M3_VALUES[:0x7F]
+    mids = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)
+    rows = []
+    for i in range(0, len(mids), 31):
+        blk = np.zeros(32, dtype=np.float32)
+        blk[0] = 448.0
+        chunk = mids[i:i + 31]
+        blk[1:1 + len(chunk)] = chunk * np.where(np.arange(len(chunk)) % 2, -1, 1)
+        rows.append(blk)
+    rows.append(np.zeros(32, dtype=np.float32))
+    big = np.full(32, float.fromhex("0x1.fep127"), dtype=np.float32)
+    big[1::2] *= -1
+    rows.append(big)
+    rows.append(np.full(32, 2.0 ** -133, dtype=np.float32))
+    x = np.stack(rows)
+    bits = synth.as_bf16_bits(x)
+    assert np.array_equal(F.decode_bf16(bits).astype(np.float32), x)     # the values survive as BF16
+    check("mxfp8", bits, bf16=True)
+    row0 = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -5.0, 0.1, 0.3, 4.4, -6.0, 1.0] * 2,
+                    dtype=np.float32)
+    row1 = np.zeros(32, dtype=np.float32)
+    row1[0] = 2688.0
+    check("nvfp4", synth.as_bf16_bits(np.stack([row0, row1])), bf16=True)
+    check("nvfp4", np.zeros((3, 64), dtype=np.uint16), bf16=True)
+
+
+def test_bf16_full_size_operand():
+    check("nvfp4", synth.as_bf16_bits(synth.normal_rowscaled(8192, 8192, seed=1)), bf16=True)
+    check("mxfp8", synth.as_bf16_bits(synth.normal(8000, 8192, seed=0)), bf16=True)

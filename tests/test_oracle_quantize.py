@@ -149,3 +149,32 @@ def test_dequantised_error_is_within_half_step(kind):
         deq = F.decode_e2m1(codes) * scale
         # E2M1 spacing is at most 2 (between 4 and 6), so |err| <= 1 * block scale, plus scale rounding
         assert np.all(np.abs(deq - x) <= 1.0 * scale * 1.07 + 1e-30)
+
+
+def test_bf16_decode_exhaustive():
+    # every 16-bit pattern, against the float32 whose upper half it is (a reinterpretation by
+    # numpy, not the oracle's field decode): equal values, NaN exactly where the pattern is NaN
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = F.decode_bf16(bits)
+    want = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    # hand-checked patterns: 1, -2, the largest finite, the smallest subnormal, +-inf, -0
+    assert F.decode_bf16(np.array([0x3F80, 0xC000, 0x7F7F, 0x0001, 0x7F80, 0xFF80], np.uint16)).tolist() == [
+        1.0, -2.0, float.fromhex("0x1.fep127"), 2.0 ** -133, float("inf"), float("-inf")]
+    z = F.decode_bf16(np.array([0x8000], np.uint16))[0]
+    assert z == 0.0 and np.signbit(z)
+
+
+def test_bf16_quantisers_quantise_the_widened_values():
+    # the BF16 entry points apply the float32 recipe to the exactly widened values
+    x = synth.normal_rowscaled(8, 96, seed=3)
+    bits = synth.as_bf16_bits(x)
+    wide = (bits.astype(np.uint32) << 16).view(np.float32)
+    c0, s0 = Q.quantize_mxfp8_bf16(bits)
+    c1, s1 = Q.quantize_mxfp8(wide)
+    assert np.array_equal(c0, c1) and np.array_equal(s0, s1)
+    p0, t0, g0 = Q.quantize_nvfp4_bf16(bits)
+    p1, t1, g1 = Q.quantize_nvfp4(wide)
+    assert np.array_equal(p0, p1) and np.array_equal(t0, t1) and g0 == g1
