@@ -167,15 +167,28 @@ __global__ void __launch_bounds__(256) quantize_nv_kernel(const T* __restrict__ 
       const float t = (d != 0.0f) ? __fdiv_rn(bmax, d) : 0.0f;
       const uint32_t sc = cvt_e4m3x2(t, 0.0f) & 0x7Fu;
       const float den = __fmul_rn(ue4m3_value(sc), s);
+      // Element = E2M1(RN(x / den)), reached without a division per element: p = RN(x * RN(1/den))
+      // is within 2^-22.4 of x/den relative (and so of RN(x/den)), and E2M1 rounding is monotone,
+      // so when p (1 - 2^-21) and p (1 + 2^-21) round to the same code, that is the code of
+      // RN(x/den).  Pairs that straddle a rounding threshold, and blocks whose den or 1/den is
+      // not a normal float32, take the IEEE division.
+      const bool fast = den >= 0x1p-126f && den <= 0x1p126f;
+      const float inv = fast ? __frcp_rn(den) : 0.0f;
       uint32_t lo = 0, hi = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float q0 = 0.0f, q1 = 0.0f;
+        uint32_t byte = 0;
         if (den != 0.0f) {
-          q0 = __fdiv_rn(v[2 * j], den);
-          q1 = __fdiv_rn(v[2 * j + 1], den);
+          bool exact = !fast;
+          if (fast) {
+            const float p0 = __fmul_rn(v[2 * j], inv), p1 = __fmul_rn(v[2 * j + 1], inv);
+            const uint32_t below = cvt_e2m1x2(__fmul_rn(p0, 1.0f - 0x1p-21f), __fmul_rn(p1, 1.0f - 0x1p-21f)) & 0xFFu;
+            const uint32_t above = cvt_e2m1x2(__fmul_rn(p0, 1.0f + 0x1p-21f), __fmul_rn(p1, 1.0f + 0x1p-21f)) & 0xFFu;
+            byte = below;
+            exact = below != above;
+          }
+          if (exact) byte = cvt_e2m1x2(__fdiv_rn(v[2 * j], den), __fdiv_rn(v[2 * j + 1], den)) & 0xFFu;
         }
-        const uint32_t byte = cvt_e2m1x2(q0, q1) & 0xFFu;
         if (j < 4) lo |= byte << (8 * j);
         else hi |= byte << (8 * (j - 4));
       }

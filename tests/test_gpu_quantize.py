@@ -133,3 +133,40 @@ def test_bf16_ties_extremes_and_zero():
 def test_bf16_full_size_operand():
     check("nvfp4", synth.as_bf16_bits(synth.normal_rowscaled(8192, 8192, seed=1)), bf16=True)
     check("mxfp8", synth.as_bf16_bits(synth.normal(8000, 8192, seed=0)), bf16=True)
+
+
+def test_nv_elements_at_rounding_thresholds():
+    # One element of 2688 makes s = 1, so a block whose largest magnitude is 6 v (v a UE4M3 value)
+    # gets den = v exactly.  With v not a power of two, x / den and x * (1 / den) can round
+    # differently; elements RN(T v) and up to 3 float32 ulps either side, for every E2M1 rounding
+    # threshold T, check that the kernel's element codes are those of RN(x / den) exactly.
+    thresholds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    dens = [1.125, 1.375, 0.8125, 3.25, 0.5625, 7.0, 0.1171875, 13.0]
+    blocks = []
+    for v in dens:
+        cand = []
+        for T in thresholds:
+            base = np.float32(T * v)
+            lo = hi = base
+            cand.append(base)
+            for _ in range(3):
+                lo = np.nextafter(lo, np.float32(0))
+                hi = np.nextafter(hi, np.float32(1e30))
+                cand += [lo, hi]
+        cand = np.array(cand, dtype=np.float32)
+        cand[1::2] *= -1                                           # both signs
+        for i in range(0, len(cand), 15):
+            blk = np.zeros(16, dtype=np.float32)
+            blk[0] = np.float32(6.0 * v)                           # the block's largest magnitude
+            chunk = cand[i:i + 15]
+            blk[1:1 + len(chunk)] = chunk
+            blocks.append(blk)
+    if len(blocks) % 2:
+        blocks.append(np.zeros(16, dtype=np.float32))
+    x = np.concatenate(blocks).reshape(-1, 32)
+    big = np.zeros((1, 32), dtype=np.float32)
+    big[0, 0] = 2688.0                                             # tensor amax: s = 1
+    x = np.vstack([big, x])
+    _, _, s = Q.quantize_nvfp4(x)
+    assert s == np.float32(1.0)
+    check("nvfp4", x)
