@@ -12,7 +12,7 @@ import os
 
 __all__ = [
     "BSG_MXFP8", "BSG_NVFP4", "BSG_OUT_F16", "BSG_OUT_BF16", "BSG_F_BIAS", "BSG_F_SILU",
-    "BSG_F_ALPHA_DEVICE", "BsgError", "lib", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_plan_create",
+    "BSG_F_ALPHA_DEVICE", "BSG_F_C", "BSG_F_ALPHA_ROW", "BSG_F_ALPHA_COL", "BsgError", "lib", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_plan_create",
     "bsg_plan_run", "bsg_plan_destroy", "bsg_plan_check_status", "bsg_plan_variant",
     "bsg_plan_debug_set", "mxfp8_gemm", "nvfp4_gemm", "bsg_cache_clear", "bsg_last_error",
     "bsg_version", "Plan", "bsg_gemm_noalloc",
@@ -21,6 +21,7 @@ __all__ = [
 BSG_MXFP8, BSG_NVFP4 = 0, 1
 BSG_OUT_F16, BSG_OUT_BF16 = 0, 1
 BSG_F_BIAS, BSG_F_SILU, BSG_F_ALPHA_DEVICE = 1, 2, 4
+BSG_F_C, BSG_F_ALPHA_ROW, BSG_F_ALPHA_COL = 8, 16, 32
 
 STATUS_NAMES = {
     0: "BSG_OK", 1: "BSG_ERR_INVALID_ARG", 2: "BSG_ERR_SHAPE", 3: "BSG_ERR_ALIGNMENT",
@@ -45,6 +46,8 @@ class BsgDesc(ctypes.Structure):
         ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("SFA", ctypes.c_void_p),
         ("SFB", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("D", ctypes.c_void_p),
         ("alpha", ctypes.c_float), ("alpha_dev", ctypes.c_void_p),
+        ("C", ctypes.c_void_p), ("beta", ctypes.c_float), ("alpha_row", ctypes.c_void_p),
+        ("alpha_col", ctypes.c_void_p),
     ]
 
 
@@ -131,9 +134,10 @@ def bsg_quantize_bf16(kind, x, rows, K, codes, sf, global_scale=None, stream=Non
                                    _stream(stream)))
 
 
-def bsg_plan_create(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None):
+def bsg_plan_create(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None,
+                    C=None, beta=0.0, alpha_row=None, alpha_col=None):
     d = BsgDesc(kind, out, flags, M, N, K, _ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(bias), _ptr(D),
-                alpha, _ptr(alpha_dev))
+                alpha, _ptr(alpha_dev), _ptr(C), beta, _ptr(alpha_row), _ptr(alpha_col))
     h = ctypes.c_void_p()
     _check(lib().bsg_plan_create(ctypes.byref(h), ctypes.byref(d)))
     return h.value
@@ -170,10 +174,10 @@ def nvfp4_gemm(D, A, B, SFA, SFB, bias, alpha, flags, M, N, K, out, stream=None)
 
 
 def bsg_gemm_noalloc(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None,
-                     stream=None):
+                     stream=None, C=None, beta=0.0, alpha_row=None, alpha_col=None):
     """Allocation-free GEMM (no device allocation; shares one static scratch array per GPU)."""
     d = BsgDesc(kind, out, flags, M, N, K, _ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(bias), _ptr(D),
-                alpha, _ptr(alpha_dev))
+                alpha, _ptr(alpha_dev), _ptr(C), beta, _ptr(alpha_row), _ptr(alpha_col))
     _check(lib().bsg_gemm_noalloc(ctypes.byref(d), _stream(stream)))
 
 

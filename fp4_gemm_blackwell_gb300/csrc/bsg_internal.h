@@ -10,7 +10,15 @@ namespace bsg {
 
 enum : int { KIND_MX = 0, KIND_NV = 1 };
 enum : int { OUT_F16 = 0, OUT_BF16 = 1 };
-enum : unsigned { F_BIAS = 1u, F_SILU = 2u, F_ALPHA_DEVICE = 4u, F_D32 = 8u /* D 32-byte aligned (set by the host) */ };
+enum : unsigned {
+  F_BIAS = 1u,
+  F_SILU = 2u,
+  F_ALPHA_DEVICE = 4u,
+  F_C = 8u,
+  F_ALPHA_ROW = 16u,
+  F_ALPHA_COL = 32u,
+  F_D32 = 1u << 30  // D (and C) 32-byte aligned: set by the host, not a caller flag
+};
 
 // How split-K partial tiles are combined: not split; FP32 partials in the plan's global
 // workspace, summed by the last split to arrive; or the splits of a tile form one thread-block
@@ -35,12 +43,16 @@ struct GemmParams {
   const uint8_t* sfb;
   const void* bias;    // N values of the output type (flags & F_BIAS)
   void* d;             // M x N output, row-major
+  const void* c;       // M x N residual input, row-major, output type (flags & F_C)
+  const float* alpha_row;  // M factors (flags & F_ALPHA_ROW)
+  const float* alpha_col;  // N factors (flags & F_ALPHA_COL)
   const float* alpha_dev;
   float* partial;      // split-K partial tiles (splits x tiles x 128 x BN floats)
   unsigned* counters;  // split-K arrival counter per tile (0 between launches)
   unsigned* status;    // device status word
   unsigned long long wait_limit_ns;
   float alpha;
+  float beta;
   int M, N, K;
   unsigned flags;
   int sfa_atoms_per_band;  // padded scale columns / 4 of A

@@ -196,37 +196,140 @@ __device__ __forceinline__ void st_out16(uint16_t* d, const uint32_t (&o)[8], bo
   }
 }
 
-// alpha, bias[n + i], SiLU on W consecutive accumulator values of one row, rounded to the
-// output type and packed two per word.  Columns at or beyond N read no bias.
+// alpha * alpha_row[m]: the part of the epilogue factor shared by a whole output row.
+__device__ __forceinline__ float row_alpha(const GemmParams& p, float alpha, int m) {
+  return ((p.flags & F_ALPHA_ROW) && m < p.M) ? __fmul_rn(alpha, __ldg(p.alpha_row + m)) : alpha;
+}
+
+// y * sigmoid(y) in place.  The reciprocal uses the fast division: an IEEE division takes a slow
+// path whenever 1 + e^-y overflows (y < -88), which is common for long K; __fdividef(1, d)
+// returns 0 for d > 2^126, the correctly rounded sigmoid there.
+template <int W>
+__device__ __forceinline__ void silu_inplace(float (&y)[W]) {
+#pragma unroll
+  for (int i = 0; i < W; ++i) y[i] = y[i] * __fdividef(1.0f, 1.0f + __expf(-y[i]));
+}
+
+// W consecutive values of the bias (output type) at column n, as float32.
 template <int OUT, int W>
-__device__ __forceinline__ void epi_pack(const GemmParams& p, int n, const float* v, float alpha,
-                                         uint32_t* out) {
+__device__ __forceinline__ void load_bias(const GemmParams& p, int n, float (&b)[W]) {
+  uint16_t raw[W];
+  if constexpr (W == 8)
+    *reinterpret_cast<uint4*>(raw) = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias) + n));
+  else
+    *reinterpret_cast<uint2*>(raw) = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
+#pragma unroll
+  for (int i = 0; i < W; ++i) b[i] = out_to_float<OUT>(raw[i]);
+}
+
+// Epilogue of W consecutive accumulator values v of one output row, columns n..n+W-1:
+//   y = alpha * v[i] (+ bias[n+i]);  SiLU;  rounded to the output type and packed two per word.
+// Columns at or beyond N read no bias.  The path of every problem without C or per-column
+// factors (epi_pack_ext covers those).
+template <int OUT, int W>
+__device__ __forceinline__ void epi_pack(const GemmParams& p, int n, const float* v, float alpha, uint32_t* out) {
   static_assert(W == 4 || W == 8, "group width");
   float y[W];
   if ((p.flags & F_BIAS) && n < p.N) {
-    uint16_t b[W];
-    if constexpr (W == 8) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias) + n));
-      *reinterpret_cast<uint4*>(b) = raw;
-    } else {
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + n));
-      *reinterpret_cast<uint2*>(b) = raw;
-    }
+    float b[W];
+    load_bias<OUT, W>(p, n, b);
 #pragma unroll
-    for (int i = 0; i < W; ++i) y[i] = __fmaf_rn(alpha, v[i], out_to_float<OUT>(b[i]));
+    for (int i = 0; i < W; ++i) y[i] = __fmaf_rn(alpha, v[i], b[i]);
   } else {
 #pragma unroll
     for (int i = 0; i < W; ++i) y[i] = __fmul_rn(alpha, v[i]);
   }
-  if (p.flags & F_SILU) {
-    // y * sigmoid(y).  The reciprocal uses the fast division: an IEEE division takes a
-    // slow path whenever 1 + e^-y overflows (y < -88), which is common for long K.
-    // __fdividef(1, d) returns 0 for d > 2^126, the correctly rounded sigmoid there.
-#pragma unroll
-    for (int i = 0; i < W; ++i) y[i] = y[i] * __fdividef(1.0f, 1.0f + __expf(-y[i]));
-  }
+  if (p.flags & F_SILU) silu_inplace(y);
 #pragma unroll
   for (int i = 0; i < W / 2; ++i) out[i] = pack2<OUT>(y[2 * i], y[2 * i + 1]);
+}
+
+// The epilogue with the residual and per-column factors, on W values of row m at columns n..:
+//   y = alpha_m * alpha_col[n+i] * v[i] + bias[n+i] + beta * c[i];  SiLU;  packed.
+// alpha_m = row_alpha(alpha, m); c = the W values of C[m, n..] already loaded (cw: W/2 words of
+// two output-type values), read only with F_C.  Columns at or beyond N read nothing.
+template <int OUT, int W>
+__device__ __forceinline__ void epi_pack_ext(const GemmParams& p, int n, const float* v, float alpha_m,
+                                             const uint32_t* cw, uint32_t* out) {
+  static_assert(W == 4 || W == 8, "group width");
+  const bool in = n < p.N;
+  float a[W], y[W];
+#pragma unroll
+  for (int i = 0; i < W; ++i)
+    a[i] = ((p.flags & F_ALPHA_COL) && in) ? __fmul_rn(alpha_m, __ldg(p.alpha_col + n + i)) : alpha_m;
+  if ((p.flags & F_BIAS) && in) {
+    float b[W];
+    load_bias<OUT, W>(p, n, b);
+#pragma unroll
+    for (int i = 0; i < W; ++i) y[i] = __fmaf_rn(a[i], v[i], b[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < W; ++i) y[i] = __fmul_rn(a[i], v[i]);
+  }
+  if (p.flags & F_C) {
+    const uint16_t* c = reinterpret_cast<const uint16_t*>(cw);
+#pragma unroll
+    for (int i = 0; i < W; ++i) y[i] = __fmaf_rn(p.beta, out_to_float<OUT>(c[i]), y[i]);
+  }
+  if (p.flags & F_SILU) silu_inplace(y);
+#pragma unroll
+  for (int i = 0; i < W / 2; ++i) out[i] = pack2<OUT>(y[2 * i], y[2 * i + 1]);
+}
+
+// 16 consecutive values of C (output type) at row m, column n, as eight words: one 32-byte load
+// when C is 32-byte aligned (wide), else two 16-byte loads.  Plain loads: C may be D itself, and
+// every element is read by the thread that later stores it.
+__device__ __forceinline__ void load_c16(const GemmParams& p, int m, int n, bool wide, uint32_t (&w)[8]) {
+  const uint16_t* src = static_cast<const uint16_t*>(p.c) + static_cast<size_t>(m) * p.N + n;
+  if (wide) {
+    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(src)
+                 : "memory");
+  } else {
+    const uint4 a = reinterpret_cast<const uint4*>(src)[0];
+    const uint4 b = reinterpret_cast<const uint4*>(src)[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+}
+
+// A row segment of 16*G accumulator values r (row m, columns n0.., n0 a multiple of 16) through
+// the epilogue into D: the plain path, or (C / per-column factors) the extended one, which loads
+// C one group of 16 columns ahead of the arithmetic.  Rows at or beyond M and columns at or
+// beyond N are not stored.
+template <int OUT, int G>
+__device__ __forceinline__ void epilogue_row(const GemmParams& p, int m, int n0, const uint32_t* r, float alpha) {
+  uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+  const bool wide = p.flags & F_D32;
+  const bool row_in = m < p.M;
+  if (!(p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW))) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int n = n0 + 16 * g;
+      uint32_t o[8];
+      epi_pack<OUT, 8>(p, n, reinterpret_cast<const float*>(r + 16 * g), alpha, o);
+      epi_pack<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(r + 16 * g + 8), alpha, o + 4);
+      if (row_in && n < p.N) st_out16(drow + n, o, wide);
+    }
+    return;
+  }
+  const float alpha_m = row_alpha(p, alpha, m);
+  const bool has_c = (p.flags & F_C) && row_in;
+  uint32_t cnext[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (has_c && n0 < p.N) load_c16(p, m, n0, wide, cnext);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int n = n0 + 16 * g;
+    uint32_t ccur[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ccur[i] = cnext[i];
+    if (g + 1 < G && has_c && n + 16 < p.N) load_c16(p, m, n + 16, wide, cnext);
+    uint32_t o[8];
+    epi_pack_ext<OUT, 8>(p, n, reinterpret_cast<const float*>(r + 16 * g), alpha_m, ccur, o);
+    epi_pack_ext<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(r + 16 * g + 8), alpha_m, ccur + 4, o + 4);
+    if (row_in && n < p.N) st_out16(drow + n, o, wide);
+  }
 }
 
 // Epilogue of 32 consecutive columns n0.. of output row m held by this thread.
@@ -235,29 +338,54 @@ __device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0
                                               float alpha) {
   if (m >= p.M) return;
   uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+  const bool ext = p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW);
+  const float alpha_m = ext ? row_alpha(p, alpha, m) : alpha;
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const int n = n0 + 8 * g;
-    if (n >= p.N) break;  // N % 16 == 0: groups of 8 are whole
-    uint4 o;
-    epi_pack<OUT, 8>(p, n, v + 8 * g, alpha, reinterpret_cast<uint32_t*>(&o));
-    *reinterpret_cast<uint4*>(drow + n) = o;
+  for (int h = 0; h < 2; ++h) {
+    const int n = n0 + 16 * h;
+    if (n >= p.N) break;  // N % 16 == 0: groups of 16 are whole
+    uint32_t o[8];
+    if (ext) {
+      uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (p.flags & F_C) load_c16(p, m, n, (p.flags & F_D32) != 0, c);
+      epi_pack_ext<OUT, 8>(p, n, v + 16 * h, alpha_m, c, o);
+      epi_pack_ext<OUT, 8>(p, n + 8, v + 16 * h + 8, alpha_m, c + 4, o + 4);
+    } else {
+      epi_pack<OUT, 8>(p, n, v + 16 * h, alpha, o);
+      epi_pack<OUT, 8>(p, n + 8, v + 16 * h + 8, alpha, o + 4);
+    }
+    st_out16(drow + n, o, (p.flags & F_D32) != 0);
   }
 }
 
-// alpha (+ preloaded bias) and SiLU on 4 accumulator values, packed two per word.
-template <int OUT>
-__device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, const float4& a, uint2 braw, float alpha) {
+// The epilogue on 4 accumulator values of row m, columns n..n+3, with the bias preloaded
+// (braw); packed two per word.  EXT: the residual and per-column factors too (alpha_m is then
+// row_alpha(alpha, m)); without it, the plain path's arithmetic exactly.
+template <int OUT, bool EXT>
+__device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, int m, int n, const float4& a, uint2 braw,
+                                                float alpha_m) {
   const uint16_t* b = reinterpret_cast<const uint16_t*>(&braw);
   float y[4] = {a.x, a.y, a.z, a.w};
   const bool has_bias = (p.flags & F_BIAS) != 0;
+  if (!EXT || !(p.flags & F_ALPHA_COL)) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    y[i] = has_bias ? __fmaf_rn(alpha, y[i], out_to_float<OUT>(b[i])) : __fmul_rn(alpha, y[i]);
-  if (p.flags & F_SILU) {
+    for (int i = 0; i < 4; ++i)
+      y[i] = has_bias ? __fmaf_rn(alpha_m, y[i], out_to_float<OUT>(b[i])) : __fmul_rn(alpha_m, y[i]);
+  } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) y[i] = y[i] * __fdividef(1.0f, 1.0f + __expf(-y[i]));  // see epi_pack
+    for (int i = 0; i < 4; ++i) {
+      const float ai = __fmul_rn(alpha_m, __ldg(p.alpha_col + n + i));
+      y[i] = has_bias ? __fmaf_rn(ai, y[i], out_to_float<OUT>(b[i])) : __fmul_rn(ai, y[i]);
+    }
   }
+  if (EXT && (p.flags & F_C)) {
+    uint16_t c[4];
+    *reinterpret_cast<uint2*>(c) =
+        *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.c) + static_cast<size_t>(m) * p.N + n);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = __fmaf_rn(p.beta, out_to_float<OUT>(c[i]), y[i]);
+  }
+  if (p.flags & F_SILU) silu_inplace(y);
   return make_uint2(pack2<OUT>(y[0], y[1]), pack2<OUT>(y[2], y[3]));
 }
 
@@ -265,7 +393,7 @@ __device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, const float
 // shared memory, slot sp = split sp, [128/S rows][BN + 4] floats each.  The owner sums them in
 // split order (deterministic), applies the epilogue and stores whole rows: epilogue thread t
 // takes column group c4 = t % (BN/4) (4 consecutive columns) of rows t / (BN/4), + 1024/BN, ...
-template <int OUT, int BN, int S>
+template <int OUT, int BN, int S, bool EXT>
 __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const float* slabs, const UnitCoord& c,
                                                  float alpha, uint2 braw, int t) {
   constexpr int R = 128 / S;
@@ -301,16 +429,22 @@ __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const floa
     const int m = c.m_blk * 128 + row;
     if (m < p.M && n < p.N)  // N % 16 == 0: groups of 4 are whole
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N + n) =
-          epi4_with_bias<OUT>(p, acc, braw, alpha);
+          epi4_with_bias<OUT, EXT>(p, m, n, acc, braw, EXT ? row_alpha(p, alpha, m) : alpha);
   }
 }
 
 template <int OUT, int BN>
 __device__ __forceinline__ void cluster_reduce(const GemmParams& p, const float* slabs, const UnitCoord& c,
                                                float alpha, uint2 braw, int t) {
-  if (p.splits == 2) cluster_reduce_s<OUT, BN, 2>(p, slabs, c, alpha, braw, t);
-  else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4>(p, slabs, c, alpha, braw, t);
-  else cluster_reduce_s<OUT, BN, 8>(p, slabs, c, alpha, braw, t);
+  if (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW)) {
+    if (p.splits == 2) cluster_reduce_s<OUT, BN, 2, true>(p, slabs, c, alpha, braw, t);
+    else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4, true>(p, slabs, c, alpha, braw, t);
+    else cluster_reduce_s<OUT, BN, 8, true>(p, slabs, c, alpha, braw, t);
+  } else {
+    if (p.splits == 2) cluster_reduce_s<OUT, BN, 2, false>(p, slabs, c, alpha, braw, t);
+    else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4, false>(p, slabs, c, alpha, braw, t);
+    else cluster_reduce_s<OUT, BN, 8, false>(p, slabs, c, alpha, braw, t);
+  }
 }
 
 // Word t of the result is word (t + r) % 4 of v (r uniform across the warp).
@@ -689,32 +823,46 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(acc));
-          const bool wide = p.flags & F_D32;
-#pragma unroll
-          for (int g = 0; g < HC / 16; ++g) {
-            const int n = nbase + col0 + 16 * g;
-            uint32_t o[8];
-            epi_pack<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[16 * g]), alpha, o);
-            epi_pack<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(&r[16 * g + 8]), alpha, o + 4);
-            if (m < p.M && n < p.N) st_out16(drow + n, o, wide);
-          }
+          epilogue_row<OUT, HC / 16>(p, m, nbase + col0, r, alpha);
         } else {
           // Two accumulators: the next tile's MMAs run in the other one, so the segment is
           // rounded chunk by chunk (fewer live registers) and released before the stores.
           uint32_t packed[HC / 2];
-#pragma unroll
-          for (int ch = 0; ch < (HC + 31) / 32; ++ch) {
-            constexpr int W = HC < 32 ? HC : 32;
-            uint32_t r[W];
+          constexpr int W = HC < 32 ? HC : 32;
+          auto load_chunk = [&](int ch, uint32_t (&r)[W]) {
             if constexpr (W == 16)
               tmem_ld_32x32b_x16(t_row + col0, r);
             else
               tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
             tmem_ld_wait();
+          };
+          if (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW)) {
+            const float alpha_m = row_alpha(p, alpha, m);
 #pragma unroll
-            for (int g = 0; g < W / 8; ++g)
-              epi_pack<OUT, 8>(p, nbase + col0 + ch * 32 + 8 * g, reinterpret_cast<const float*>(&r[8 * g]), alpha,
-                               &packed[ch * 16 + 4 * g]);
+            for (int ch = 0; ch < (HC + 31) / 32; ++ch) {
+              uint32_t r[W];
+              load_chunk(ch, r);
+#pragma unroll
+              for (int h = 0; h < W / 16; ++h) {
+                const int n = nbase + col0 + ch * 32 + 16 * h;
+                uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if ((p.flags & F_C) && m < p.M && n < p.N) load_c16(p, m, n, (p.flags & F_D32) != 0, c);
+                epi_pack_ext<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[16 * h]), alpha_m, c,
+                                     &packed[ch * 16 + 8 * h]);
+                epi_pack_ext<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(&r[16 * h + 8]), alpha_m, c + 4,
+                                     &packed[ch * 16 + 8 * h + 4]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < (HC + 31) / 32; ++ch) {
+              uint32_t r[W];
+              load_chunk(ch, r);
+#pragma unroll
+              for (int g = 0; g < W / 8; ++g)
+                epi_pack<OUT, 8>(p, nbase + col0 + ch * 32 + 8 * g, reinterpret_cast<const float*>(&r[8 * g]), alpha,
+                                 &packed[ch * 16 + 4 * g]);
+            }
           }
           tc_fence_before();
           __syncwarp();

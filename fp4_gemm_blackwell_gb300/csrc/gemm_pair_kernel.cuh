@@ -449,16 +449,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         else
           tc_commit_pair_mc(bar_tempty, leader_mask);
       }
-      uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
-      const bool wide = p.flags & F_D32;
-#pragma unroll
-      for (int g = 0; g < HC / 16; ++g) {
-        const int n = nbase + col0 + 16 * g;
-        uint32_t o[8];
-        epi_pack<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[16 * g]), alpha, o);
-        epi_pack<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(&r[16 * g + 8]), alpha, o + 4);
-        if (m < p.M && n < p.N) st_out16(drow + n, o, wide);
-      }
+      epilogue_row<OUT, HC / 16>(p, m, nbase + col0, r, alpha);
       acc_phase ^= 1u;
     }
   }

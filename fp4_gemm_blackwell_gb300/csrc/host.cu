@@ -130,7 +130,7 @@ bsg_status validate_desc(const bsg_desc* d) {
   if (d->kind != BSG_MXFP8 && d->kind != BSG_NVFP4) return fail(BSG_ERR_INVALID_ARG, "unknown kind %d", d->kind);
   if (d->out != BSG_OUT_F16 && d->out != BSG_OUT_BF16)
     return fail(BSG_ERR_DTYPE, "unsupported output type %d (FP16 or BF16 only)", d->out);
-  if (d->flags & ~(BSG_F_BIAS | BSG_F_SILU | BSG_F_ALPHA_DEVICE))
+  if (d->flags & ~(BSG_F_BIAS | BSG_F_SILU | BSG_F_ALPHA_DEVICE | BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL))
     return fail(BSG_ERR_INVALID_ARG, "unknown flag bits 0x%x", d->flags);
   if (d->M < 1 || d->N < 16 || d->K < 32 || d->M > kMaxDim || d->N > kMaxDim || d->K > kMaxDim)
     return fail(BSG_ERR_SHAPE, "shape M=%d N=%d K=%d out of range (M>=1, N>=16, K>=32, each <= 2^20)",
@@ -146,6 +146,15 @@ bsg_status validate_desc(const bsg_desc* d) {
     return fail(BSG_ERR_ALIGNMENT, "operand pointers must be 16-byte aligned");
   if ((d->flags & BSG_F_ALPHA_DEVICE) && (reinterpret_cast<uintptr_t>(d->alpha_dev) & 3u))
     return fail(BSG_ERR_ALIGNMENT, "alpha_dev must be 4-byte aligned");
+  if ((d->flags & BSG_F_C) && !d->C) return fail(BSG_ERR_INVALID_ARG, "C set but C is null");
+  if ((d->flags & BSG_F_ALPHA_ROW) && !d->alpha_row)
+    return fail(BSG_ERR_INVALID_ARG, "ALPHA_ROW set but alpha_row is null");
+  if ((d->flags & BSG_F_ALPHA_COL) && !d->alpha_col)
+    return fail(BSG_ERR_INVALID_ARG, "ALPHA_COL set but alpha_col is null");
+  if ((d->flags & BSG_F_C) && !aligned16(d->C)) return fail(BSG_ERR_ALIGNMENT, "C must be 16-byte aligned");
+  if (((d->flags & BSG_F_ALPHA_ROW) && (reinterpret_cast<uintptr_t>(d->alpha_row) & 3u)) ||
+      ((d->flags & BSG_F_ALPHA_COL) && (reinterpret_cast<uintptr_t>(d->alpha_col) & 3u)))
+    return fail(BSG_ERR_ALIGNMENT, "alpha_row and alpha_col must be 4-byte aligned");
   return BSG_OK;
 }
 
@@ -160,6 +169,14 @@ bsg_status validate_ranges(const bsg_desc* d) {
   if ((d->flags & BSG_F_BIAS) && (s = check_range(d->bias, static_cast<size_t>(d->N) * 2, BSG_ERR_SHAPE, "bias")) != BSG_OK)
     return s;
   if ((d->flags & BSG_F_ALPHA_DEVICE) && (s = check_range(d->alpha_dev, 4, BSG_ERR_SHAPE, "alpha_dev")) != BSG_OK)
+    return s;
+  if ((d->flags & BSG_F_C) && (s = check_range(d->C, static_cast<size_t>(d->M) * d->N * 2, BSG_ERR_SHAPE, "C")) != BSG_OK)
+    return s;
+  if ((d->flags & BSG_F_ALPHA_ROW) &&
+      (s = check_range(d->alpha_row, static_cast<size_t>(d->M) * 4, BSG_ERR_SHAPE, "alpha_row")) != BSG_OK)
+    return s;
+  if ((d->flags & BSG_F_ALPHA_COL) &&
+      (s = check_range(d->alpha_col, static_cast<size_t>(d->N) * 4, BSG_ERR_SHAPE, "alpha_col")) != BSG_OK)
     return s;
   return BSG_OK;
 }
@@ -415,7 +432,14 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->M = d->M;
   g->N = d->N;
   g->K = d->K;
-  g->flags = d->flags | ((reinterpret_cast<uintptr_t>(d->D) & 31u) == 0 ? bsg::F_D32 : 0u);
+  // 32-byte stores (and loads of C) when D and, if read, C are 32-byte aligned
+  const bool d32 = (reinterpret_cast<uintptr_t>(d->D) & 31u) == 0 &&
+                   (!(d->flags & BSG_F_C) || (reinterpret_cast<uintptr_t>(d->C) & 31u) == 0);
+  g->flags = d->flags | (d32 ? bsg::F_D32 : 0u);
+  g->c = (d->flags & BSG_F_C) ? d->C : nullptr;
+  g->beta = d->beta;
+  g->alpha_row = (d->flags & BSG_F_ALPHA_ROW) ? d->alpha_row : nullptr;
+  g->alpha_col = (d->flags & BSG_F_ALPHA_COL) ? d->alpha_col : nullptr;
   g->sfa_atoms_per_band = (d->K / blk + 3) / 4;
   g->sfb_atoms_per_band = g->sfa_atoms_per_band;
   g->sfb_bands = (d->N + 127) / 128;

@@ -69,22 +69,32 @@ typedef enum { BSG_OUT_F16 = 0, BSG_OUT_BF16 = 1 } bsg_out;
 
 /* Epilogue flags.  BIAS and SILU are the kEnableBias / kEnableSilu switches of
  * runNvfp4Gemm; ALPHA_DEVICE reads alpha from device memory at run time, the
- * fusion_args.alpha_ptr of the MXFP8 page. */
+ * fusion_args.alpha_ptr of the MXFP8 page.  C adds beta * C[m,n] from a separate matrix
+ * (the MXFP8 page's LinearCombination epilogue with its C operand, there aliased to D);
+ * ALPHA_ROW / ALPHA_COL multiply alpha by alpha_row[m] / alpha_col[n] (per-row and
+ * per-column factors, e.g. per-token and per-channel global scales). */
 enum {
   BSG_F_BIAS = 1u,
   BSG_F_SILU = 2u,
-  BSG_F_ALPHA_DEVICE = 4u
+  BSG_F_ALPHA_DEVICE = 4u,
+  BSG_F_C = 8u,
+  BSG_F_ALPHA_ROW = 16u,
+  BSG_F_ALPHA_COL = 32u
 };
 
 typedef struct bsg_plan_s* bsg_plan_t;
 
-/* One GEMM problem.  Pointers are device pointers, 16-byte aligned.
+/* One GEMM problem.  Pointers are device pointers, 16-byte aligned (alpha_dev, alpha_row
+ * and alpha_col 4-byte aligned).
  *   M >= 1, N >= 16, K >= 32, N % 16 == 0, K % 32 == 0 (the MXFP8 page validates
  *   K % 16 and N % 16; K % 32 keeps every MXFP8 block whole and every NVFP4 row a
  *   whole number of 16-byte units).  M, N, K <= 2^20.
  *   bias is read only with BSG_F_BIAS; alpha_dev only with BSG_F_ALPHA_DEVICE (else the
- *   host value alpha is used).  SILU is applied after alpha and bias:
- *   D = silu(alpha * acc + bias[n]). */
+ *   host value alpha is used); C (M x N, row-major, the output type; it may be D itself)
+ *   and beta only with BSG_F_C; alpha_row (M floats) only with BSG_F_ALPHA_ROW; alpha_col
+ *   (N floats) only with BSG_F_ALPHA_COL.  With every flag set
+ *     D[m,n] = silu(alpha * alpha_row[m] * alpha_col[n] * acc[m,n] + bias[n] + beta * C[m,n]),
+ *   the factors multiplied in float32 in that order, each term added in float32. */
 typedef struct {
   bsg_kind kind;
   bsg_out out;
@@ -98,6 +108,10 @@ typedef struct {
   void* D;
   float alpha;
   const float* alpha_dev;
+  const void* C;
+  float beta;
+  const float* alpha_row;
+  const float* alpha_col;
 } bsg_desc;
 
 /* Validate d, choose the kernel variant (tile shape, split-K), encode the TMA tensor

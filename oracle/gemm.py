@@ -17,8 +17,13 @@ definition written out: every element and scale is decoded through the explicit
 tables of ``formats``, the products are summed in float64 (``numpy.matmul`` is
 the library primitive for the sum), then
 
-    y = alpha * acc;  y = y + bias[n] (bias);  y = y / (1 + exp(-y)) (SiLU);
+    y = alpha * alpha_row[m] * alpha_col[n] * acc;  y = y + bias[n] (bias);
+    y = y + beta * C[m, n] (C);  y = y / (1 + exp(-y)) (SiLU);
     D = y rounded to nearest even in the output type.
+
+The per-row / per-column factors and the C term are the next-step epilogue of the
+MXFP8 page's LinearCombination (alpha, beta and a C operand, there aliased to D),
+with C kept separate; their order is this library's documented reading.
 
 The scales are read from the swizzled buffers through ``layout.unswizzle`` so
 that the byte map of the scale layout is exercised end to end.
@@ -49,11 +54,26 @@ def decode_operand(kind, codes, sf_buf, rows, K):
     raise ValueError(kind)
 
 
-def epilogue(acc, alpha, bias=None, silu=False):
-    """float64 accumulator -> float64 pre-rounding output (alpha, + bias[n], SiLU)."""
-    y = float(np.float32(alpha)) * np.asarray(acc, dtype=np.float64)
+def effective_alpha(alpha, alpha_row=None, alpha_col=None):
+    """alpha * alpha_row[m] * alpha_col[n] in float64 (a scalar, a column, a row or a matrix);
+    every factor is a float32 value."""
+    a = np.float64(np.float32(alpha))
+    if alpha_row is not None:
+        a = a * np.asarray(alpha_row, dtype=np.float32).astype(np.float64)[:, None]
+    if alpha_col is not None:
+        a = a * np.asarray(alpha_col, dtype=np.float32).astype(np.float64)[None, :]
+    return a
+
+
+def epilogue(acc, alpha, bias=None, silu=False, C=None, beta=0.0, alpha_row=None, alpha_col=None):
+    """float64 accumulator -> float64 pre-rounding output (the factors, + bias[n], + beta C, SiLU).
+
+    ``C`` holds the float64 values of the residual input (exact in the output type)."""
+    y = effective_alpha(alpha, alpha_row, alpha_col) * np.asarray(acc, dtype=np.float64)
     if bias is not None:
         y = y + np.asarray(bias, dtype=np.float64)[None, :]
+    if C is not None:
+        y = y + np.float64(np.float32(beta)) * np.asarray(C, dtype=np.float64)
     if silu:
         with np.errstate(over="ignore"):
             y = y * (1.0 / (1.0 + np.exp(-y)))
@@ -77,19 +97,22 @@ def ulp_out(v, out):
 
 
 def reference(kind, A, B, SFA, SFB, M, N, K, alpha=1.0, bias=None, silu=False, out=BF16,
-              rows=None):
+              rows=None, C=None, beta=0.0, alpha_row=None, alpha_col=None):
     """Reference D (float64 values, exactly representable in ``out``) and the pre-rounding y.
 
-    ``bias`` is a float64 vector of the (already rounded) bias values.  ``rows``
-    optionally selects a subset of output rows (for sampled checks of large
-    problems); the result then has len(rows) rows.
+    ``bias`` is a float64 vector of the (already rounded) bias values, ``C`` the float64 M x N
+    values of the residual input.  ``rows`` optionally selects a subset of output rows (for
+    sampled checks of large problems); the result then has len(rows) rows.
     """
     Ahat = decode_operand(kind, A, SFA, M, K)
     if rows is not None:
-        Ahat = Ahat[np.asarray(rows)]
+        r = np.asarray(rows)
+        Ahat = Ahat[r]
+        C = None if C is None else np.asarray(C)[r]
+        alpha_row = None if alpha_row is None else np.asarray(alpha_row)[r]
     Bhat = decode_operand(kind, B, SFB, N, K)
     acc = Ahat @ Bhat.T
-    y = epilogue(acc, alpha, bias, silu)
+    y = epilogue(acc, alpha, bias, silu, C, beta, alpha_row, alpha_col)
     return round_out(y, out), y
 
 
@@ -105,15 +128,18 @@ def abs_product_sum(kind, A, B, SFA, SFB, M, N, K, rows=None):
 def tolerance(ref, got, abs_sum, alpha, silu, out):
     """Per-element bound |alpha| * 2**-7 * sum|a b| (x 1.1 with SiLU) + 1 output ulp.
 
-    The ulp is taken at the larger of |ref| and |got|, so that the rounding of
-    either side to the output type is covered.
+    ``alpha`` is the effective factor (a scalar, or ``effective_alpha`` with per-row /
+    per-column factors).  The ulp is taken at the larger of |ref| and |got|, so that the
+    rounding of either side to the output type is covered.
     """
     lip = 1.1 if silu else 1.0            # max |d silu / dy| = 1.0998...
     mag = np.maximum(np.abs(ref), np.abs(got))
-    return abs(float(np.float32(alpha))) * 2.0 ** -7 * lip * abs_sum + ulp_out(mag, out)
+    a = np.abs(np.asarray(alpha, dtype=np.float64)) if np.ndim(alpha) else abs(float(np.float32(alpha)))
+    return a * 2.0 ** -7 * lip * abs_sum + ulp_out(mag, out)
 
 
-def gemm_naive(kind, A, B, SFA, SFB, M, N, K, alpha=1.0, bias=None, silu=False):
+def gemm_naive(kind, A, B, SFA, SFB, M, N, K, alpha=1.0, bias=None, silu=False, C=None, beta=0.0,
+               alpha_row=None, alpha_col=None):
     """Triple loop in plain Python floats (float64): the same definition, no library sum."""
     Ahat = decode_operand(kind, A, SFA, M, K)
     Bhat = decode_operand(kind, B, SFB, N, K)
@@ -124,4 +150,4 @@ def gemm_naive(kind, A, B, SFA, SFB, M, N, K, alpha=1.0, bias=None, silu=False):
             for k in range(K):
                 t += float(Ahat[m, k]) * float(Bhat[n, k])
             acc[m, n] = t
-    return epilogue(acc, alpha, bias, silu)
+    return epilogue(acc, alpha, bias, silu, C, beta, alpha_row, alpha_col)

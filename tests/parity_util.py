@@ -46,7 +46,10 @@ class DeviceProblem:
 
     CANARY = 0x7BAD
 
-    def __init__(self, prob, out="bf16", bias=False, silu=False, margin=256):
+    def __init__(self, prob, out="bf16", bias=False, silu=False, margin=256, residual=None, beta=0.0,
+                 alpha_row=False, alpha_col=False):
+        """residual: None, "separate" (a C matrix of its own) or "inplace" (C is D, preloaded);
+        alpha_row / alpha_col: per-row / per-column factors drawn U(0.5, 2)."""
         self.prob, self.out = prob, out
         M, N = prob["M"], prob["N"]
         self.A, self.B = dev(prob["A"]), dev(prob["B"])
@@ -61,13 +64,39 @@ class DeviceProblem:
         self.margin = margin
         self.Dbuf = torch.full((M * N + 2 * margin,), self.CANARY, dtype=torch.int16, device="cuda")
         self.D = self.Dbuf[margin:margin + M * N]
+        rng = np.random.default_rng(M * 7 + N)
+        self.C = None
+        self.C_vals = None
+        self.beta = float(np.float32(beta))
+        if residual is not None:
+            bits, self.C_vals = synth_residual(M, N, out, seed=M + 3 * N)
+            self.flags |= bsg.BSG_F_C
+            if residual == "inplace":
+                self.D.copy_(dev(bits.reshape(-1).view(np.int16)).view(torch.int16))
+                self.C = self.D
+            else:
+                self.C = dev(bits.view(np.int16)).view(torch.int16)
+        self.alpha_row = self.alpha_row_vals = self.alpha_col = self.alpha_col_vals = None
+        if alpha_row:
+            self.alpha_row_vals = rng.uniform(0.5, 2.0, M).astype(np.float32)
+            self.alpha_row = dev(self.alpha_row_vals).view(torch.float32)
+            self.flags |= bsg.BSG_F_ALPHA_ROW
+        if alpha_col:
+            self.alpha_col_vals = rng.uniform(0.5, 2.0, N).astype(np.float32)
+            self.alpha_col = dev(self.alpha_col_vals).view(torch.float32)
+            self.flags |= bsg.BSG_F_ALPHA_COL
+
+    def epi_kwargs(self):
+        """The residual / factor arguments of the oracle reference for this problem."""
+        return dict(C=self.C_vals, beta=self.beta, alpha_row=self.alpha_row_vals, alpha_col=self.alpha_col_vals)
 
     def plan(self, alpha_dev=None):
         p = self.prob
         flags = self.flags | (bsg.BSG_F_ALPHA_DEVICE if alpha_dev is not None else 0)
         return bsg.Plan(KIND[p["kind"]], OUT[self.out], p["M"], p["N"], p["K"], self.A, self.B, self.SFA,
                         self.SFB, self.D, alpha=float(p["alpha"]), flags=flags, bias=self.bias,
-                        alpha_dev=alpha_dev)
+                        alpha_dev=alpha_dev, C=self.C, beta=self.beta, alpha_row=self.alpha_row,
+                        alpha_col=self.alpha_col)
 
     def result(self):
         torch.cuda.synchronize()
@@ -78,20 +107,33 @@ class DeviceProblem:
         return R.out_from_bits(bits, self.out)
 
 
-def reference(prob, out, bias_vals=None, silu=False, rows=None):
+def synth_residual(M, N, out, seed):
+    """A residual matrix C: N(0, 1) rounded to the output type (bits and float64 values)."""
+    bits, vals = synth.bias(M * N, seed=seed, std=1.0, out=out)
+    return bits.reshape(M, N), vals.reshape(M, N)
+
+
+def reference(prob, out, bias_vals=None, silu=False, rows=None, epi=None):
     p = prob
     ref, _ = R.reference(p["kind"], p["A"], p["B"], p["SFA"], p["SFB"], p["M"], p["N"], p["K"],
-                         alpha=p["alpha"], bias=bias_vals, silu=silu, out=out, rows=rows)
+                         alpha=p["alpha"], bias=bias_vals, silu=silu, out=out, rows=rows, **(epi or {}))
     abs_sum = R.abs_product_sum(p["kind"], p["A"], p["B"], p["SFA"], p["SFB"], p["M"], p["N"], p["K"], rows=rows)
     return ref, abs_sum
 
 
-def assert_parity(got, prob, out, bias_vals=None, silu=False, rows=None):
-    """Element-wise |got - ref| <= |alpha| 2^-7 sum|a b| (x1.1 with SiLU) + 1 output ulp."""
-    ref, abs_sum = reference(prob, out, bias_vals, silu, rows)
+def assert_parity(got, prob, out, bias_vals=None, silu=False, rows=None, epi=None):
+    """Element-wise |got - ref| <= |alpha_eff| 2^-7 sum|a b| (x1.1 with SiLU) + 1 output ulp, with
+    alpha_eff = alpha * alpha_row[m] * alpha_col[n] when the problem has those factors."""
+    ref, abs_sum = reference(prob, out, bias_vals, silu, rows, epi)
     if rows is not None:
         got = got[np.asarray(rows)]
-    tol = R.tolerance(ref, got, abs_sum, prob["alpha"], silu, out)
+    alpha = prob["alpha"]
+    if epi and (epi.get("alpha_row") is not None or epi.get("alpha_col") is not None):
+        ar = epi.get("alpha_row")
+        if ar is not None and rows is not None:
+            ar = np.asarray(ar)[np.asarray(rows)]
+        alpha = np.broadcast_to(R.effective_alpha(alpha, ar, epi.get("alpha_col")), ref.shape)
+    tol = R.tolerance(ref, got, abs_sum, alpha, silu, out)
     err = np.abs(got - ref)
     bad = ~(err <= tol)
     if bad.any():

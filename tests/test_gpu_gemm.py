@@ -155,6 +155,35 @@ def test_multicast_wait_timeout_reports_status(monkeypatch):
         P.assert_parity(dp.result(), prob, "bf16")
 
 
+EPI_FAMILIES = [{"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 128}, {"BSG_FORCE_BN": 64},
+                {"BSG_FORCE_BN": 32}, {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2},
+                {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 4}, {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3}]
+
+
+@pytest.mark.parametrize("env", EPI_FAMILIES)
+@pytest.mark.parametrize("kind,residual,beta,rows_f,cols_f,bias,silu", [
+    ("nvfp4", "separate", 0.5, True, True, True, True),      # every term at once
+    ("mxfp8", "inplace", -1.0, False, True, False, False),   # D += A B^T scaled per column, in place
+    ("nvfp4", None, 0.0, True, False, True, False),          # per-row factor alone
+])
+def test_residual_and_factor_epilogue(env, kind, residual, beta, rows_f, cols_f, bias, silu, monkeypatch):
+    # beta * C and alpha * alpha_row[m] * alpha_col[n] through every epilogue path: one and two
+    # TMEM accumulators, CTA pairs, split-K reduced in a cluster and through the workspace
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    prob = P.make_problem(kind, 300, 272, 2048)   # K: 2, 3 and 4 splits stay exact for both formats
+    dp = P.DeviceProblem(prob, out="bf16", bias=bias, silu=silu, residual=residual, beta=beta,
+                         alpha_row=rows_f, alpha_col=cols_f)
+    with dp.plan() as plan:
+        variant = plan.variant
+        plan.run()
+        plan.check_status()
+        got = dp.result()
+    if "BSG_FORCE_SPLITS" in env:
+        assert ("_s%d" % env["BSG_FORCE_SPLITS"]) in variant, variant
+    P.assert_parity(got, prob, "bf16", dp.bias_vals, silu, epi=dp.epi_kwargs())
+
+
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("env", [{"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 128},
                                  {"BSG_FORCE_BN": 64}, {"BSG_FORCE_BN": 32}])

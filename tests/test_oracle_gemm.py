@@ -7,7 +7,10 @@
 * constant matrices give K * a * b * scales exactly;
 * A and B are not interchangeable (D[m, n] pairs row m of A with row n of B);
 * the triple loop and the library sum agree;
-* the epilogue: bias is per output column, SiLU(0) = 0 and SiLU(y) -> y for large y.
+* the epilogue: bias is per output column, SiLU(0) = 0 and SiLU(y) -> y for large y;
+  the residual and per-row / per-column factors: a zero operand leaves bias + beta C exactly,
+  one-hot rows pick alpha * alpha_row[m] * alpha_col[n] times one decoded element, and C / the
+  row factor follow their row through a sampled-rows evaluation.
 """
 
 from fractions import Fraction
@@ -160,3 +163,49 @@ def test_tolerance_covers_rounding_only_cases():
     ref = np.array([1.0, 100.0])
     tol = R.tolerance(ref, ref, np.zeros(2), 1.0, False, R.BF16)
     assert np.array_equal(tol, F.ulp_bf16(ref))
+
+
+def test_residual_and_factor_closed_forms():
+    M, N, K = 3, 4, 32
+    zero = np.zeros((M, K), dtype=np.uint8)                             # E4M3 0 everywhere: acc = 0
+    b, sfb = _mx_operands(N, K, 21)
+    sfa = np.full((M, K // 32), 127, dtype=np.uint8)
+    C = np.array([[1.5, -2.0, 0.25, 8.0], [0.0, 3.0, -0.5, 1.0], [6.0, -7.0, 0.125, 2.0]])
+    bias = np.array([0.25, 0.5, -1.0, 0.0])
+    d, y = R.reference(R.MXFP8, zero, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K, bias=bias, C=C, beta=2.0,
+                       alpha_row=np.array([3.0, 5.0, 7.0], np.float32), alpha_col=np.ones(N, np.float32))
+    assert np.array_equal(y, bias[None, :] + 2.0 * C)                   # small dyadics: exact
+    assert np.array_equal(d, y)
+    # one-hot rows: D[m, n] = alpha * alpha_row[m] * alpha_col[n] * b_hat[n, k_m]
+    a = np.zeros((M, K), dtype=np.uint8)
+    picks = [0, 9, 31]
+    for m, k in enumerate(picks):
+        a[m, k] = 0x38                                                  # 1.0
+    ar = np.array([0.5, 2.0, -4.0], dtype=np.float32)
+    ac = np.array([1.0, 0.25, -2.0, 8.0], dtype=np.float32)
+    _, y2 = R.reference(R.MXFP8, a, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K, alpha=1.5, alpha_row=ar,
+                        alpha_col=ac)
+    bd = _torch_e4m3(b) * np.repeat(_torch_e8m0(sfb), 32, axis=1)
+    for m, k in enumerate(picks):
+        for n in range(N):
+            assert y2[m, n] == 1.5 * float(ar[m]) * float(ac[n]) * bd[n, k]
+    # sampled rows carry their own C row and row factor
+    _, y3 = R.reference(R.MXFP8, a, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K, alpha=1.5, alpha_row=ar,
+                        alpha_col=ac, C=C, beta=-1.0, rows=[2, 0])
+    full = R.reference(R.MXFP8, a, b, L.swizzle(sfa), L.swizzle(sfb), M, N, K, alpha=1.5, alpha_row=ar,
+                       alpha_col=ac, C=C, beta=-1.0)[1]
+    assert np.array_equal(y3, full[[2, 0]])
+
+
+def test_naive_loop_matches_with_residual_and_factors():
+    M, N, K = 4, 6, 64
+    xa = synth.normal_rowscaled(M, K, 13)
+    xb = synth.normal_rowscaled(N, K, 14)
+    ap, sfa, sa = Q.quantize_nvfp4(xa)
+    bp, sfb, sb = Q.quantize_nvfp4(xb)
+    rng = np.random.default_rng(15)
+    kw = dict(alpha=np.float32(sa * sb), bias=synth.bias(N)[1], silu=True, C=rng.normal(0, 1, (M, N)), beta=0.75,
+              alpha_row=rng.uniform(0.5, 2, M).astype(np.float32), alpha_col=rng.uniform(0.5, 2, N).astype(np.float32))
+    _, y = R.reference(R.NVFP4, ap, bp, L.swizzle(sfa), L.swizzle(sfb), M, N, K, **kw)
+    y2 = R.gemm_naive(R.NVFP4, ap, bp, L.swizzle(sfa), L.swizzle(sfb), M, N, K, **kw)
+    assert np.allclose(y, y2, rtol=1e-13, atol=1e-15)
