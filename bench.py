@@ -159,13 +159,24 @@ class Operands:
 class Problem:
     """R device copies of one GEMM problem (operands, bias, output) with a plan per copy."""
 
-    def __init__(self, bsg, kind, M, N, K, out="bf16", bias=False, silu=False, copies=1, seeds=(0, 1)):
+    def __init__(self, bsg, kind, M, N, K, out="bf16", bias=False, silu=False, copies=1, seeds=(0, 1),
+                 residual=False, factors=False):
+        """residual: beta * C from a separate M x N matrix per copy (beta = 1); factors: per-row
+        and per-column alpha vectors (U(0.5, 2))."""
         from fp4_gemm_blackwell_gb300 import synth
         self.kind, self.M, self.N, self.K, self.out = kind, M, N, K, out
+        self.residual, self.factors = residual, factors
         a = Operands(bsg, kind, M, K, seeds[0])
         b = Operands(bsg, kind, N, K, seeds[1])
         self.alpha = float(np.float32(np.float32(a.s) * np.float32(b.s)))
-        self.flags = (bsg.BSG_F_BIAS if bias else 0) | (bsg.BSG_F_SILU if silu else 0)
+        self.flags = ((bsg.BSG_F_BIAS if bias else 0) | (bsg.BSG_F_SILU if silu else 0) |
+                      (bsg.BSG_F_C if residual else 0) | (bsg.BSG_F_ALPHA_ROW | bsg.BSG_F_ALPHA_COL if factors else 0))
+        self.extra = []
+        cbits = synth.bias(M * N, seed=5, std=1.0, out=out)[0] if residual else None
+        g = torch.Generator(device="cpu")
+        g.manual_seed(6)
+        ar = (torch.rand(M, generator=g) * 1.5 + 0.5).cuda() if factors else None
+        ac = (torch.rand(N, generator=g) * 1.5 + 0.5).cuda() if factors else None
         bias_t = None
         if bias:
             bits, _ = synth.bias(N, out=out)
@@ -177,9 +188,12 @@ class Problem:
             ai, bi = (a, b) if i == 0 else (a.clone(), b.clone())
             bt = None if bias_t is None else (bias_t if i == 0 else bias_t.clone())
             d = torch.empty(M * N, dtype=torch.int16, device="cuda")
+            c = torch.from_numpy(cbits.view(np.int16)).cuda() if residual else None
+            self.extra.append(c)
             self.sets.append((ai, bi, bt, d))
             self.plans.append(bsg.Plan(k, out_t, M, N, K, ai.codes, bi.codes, ai.sf, bi.sf, d,
-                                       alpha=self.alpha, flags=self.flags, bias=bt))
+                                       alpha=self.alpha, flags=self.flags, bias=bt, C=c, beta=1.0,
+                                       alpha_row=ar, alpha_col=ac))
         self.variant = self.plans[0].variant
 
     def flops(self):
@@ -193,6 +207,10 @@ class Problem:
         b = self.M * self.K * cb + self.N * self.K * cb + sf(self.M) + sf(self.N) + self.M * self.N * 2
         if self.flags & 1:
             b += self.N * 2
+        if self.residual:
+            b += self.M * self.N * 2
+        if self.factors:
+            b += (self.M + self.N) * 4
         return int(b)
 
     def close(self):
@@ -358,8 +376,8 @@ def tensor_peak(peaks, kind):
     return peaks["bf16_tflops"] * NOMINAL_RATIO["fp8" if kind == "mxfp8" else "fp4"]
 
 
-def big_config(bsg, peaks, kind, M, N, K, out, bias, silu, steps=20, warmup=3):
-    prob = Problem(bsg, kind, M, N, K, out=out, bias=bias, silu=silu, copies=1)
+def big_config(bsg, peaks, kind, M, N, K, out, bias, silu, steps=20, warmup=3, residual=False, factors=False):
+    prob = Problem(bsg, kind, M, N, K, out=out, bias=bias, silu=silu, copies=1, residual=residual, factors=factors)
     ms, _ = graph_time(prob.plans, steps, warmup)
     us = ms * 1e3 / steps
     tf = prob.flops() / (us * 1e-6) / 1e12
@@ -367,6 +385,23 @@ def big_config(bsg, peaks, kind, M, N, K, out, bias, silu, steps=20, warmup=3):
     r = {"us": round(us, 2), "tflops": round(tf, 1), "peak_tflops": round(peak, 1),
          "frac_of_peak": round(tf / peak, 4), "variant": prob.variant,
          "l2": "single input set of %.0f MB" % (prob.algorithmic_bytes() / 2 ** 20)}
+    prob.close()
+    return r
+
+
+def skinny_config(bsg, peaks, steps=400, warmup=10, **epi):
+    """The headline shape (NVFP4 128 x 4096 x 4096, bias + SiLU) with extra epilogue terms,
+    inputs rotated over enough copies to exceed L2; kernel time and HBM roofline fraction."""
+    p1 = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=1, **epi)
+    cp = copies_to_exceed_l2(p1.algorithmic_bytes())
+    p1.close()
+    prob = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=cp, **epi)
+    ms, _ = graph_time(prob.plans, steps, warmup)
+    us = ms * 1e3 / steps
+    gbs = prob.algorithmic_bytes() / (us * 1e-6) / 1e9
+    r = {"us": round(us, 3), "tflops": round(prob.flops() / (us * 1e-6) / 1e12, 1), "gbs": round(gbs, 1),
+         "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": prob.algorithmic_bytes(),
+         "variant": prob.variant}
     prob.close()
     return r
 
@@ -676,6 +711,9 @@ def main():
             extras["nvfp4_8192_bias_silu_bf16"] = big_config(bsg, peaks, "nvfp4", 8192, 8192, 8192, "bf16", True, True)
             extras["nvfp4_8000x8192x8192_bias_silu_bf16"] = big_config(bsg, peaks, "nvfp4", 8000, 8192, 8192, "bf16",
                                                                        True, True)
+            extras["nvfp4_8192_bias_silu_residual_factors_bf16"] = big_config(
+                bsg, peaks, "nvfp4", 8192, 8192, 8192, "bf16", True, True, residual=True, factors=True)
+            extras["nvfp4_m128_residual_factors"] = skinny_config(bsg, peaks, residual=True, factors=True)
             extras["launch_loop_1000"] = launch_loop(bsg)
             for kind in ("mxfp8", "nvfp4"):
                 for bf in (False, True):
