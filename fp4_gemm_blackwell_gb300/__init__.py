@@ -47,7 +47,9 @@ class BsgDesc(ctypes.Structure):
         ("SFB", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("D", ctypes.c_void_p),
         ("alpha", ctypes.c_float), ("alpha_dev", ctypes.c_void_p),
         ("C", ctypes.c_void_p), ("beta", ctypes.c_float), ("alpha_row", ctypes.c_void_p),
-        ("alpha_col", ctypes.c_void_p),
+        ("alpha_col", ctypes.c_void_p), ("L", ctypes.c_int),
+        ("stride_A", ctypes.c_longlong), ("stride_B", ctypes.c_longlong), ("stride_SFA", ctypes.c_longlong),
+        ("stride_SFB", ctypes.c_longlong), ("stride_D", ctypes.c_longlong), ("stride_C", ctypes.c_longlong),
     ]
 
 
@@ -135,9 +137,13 @@ def bsg_quantize_bf16(kind, x, rows, K, codes, sf, global_scale=None, stream=Non
 
 
 def bsg_plan_create(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None,
-                    C=None, beta=0.0, alpha_row=None, alpha_col=None):
+                    C=None, beta=0.0, alpha_row=None, alpha_col=None, L=0, strides=None):
+    """strides (batched, L >= 2): dict of byte strides stride_A, stride_B, stride_SFA, stride_SFB,
+    stride_D and stride_C between consecutive problems."""
+    st = strides or {}
     d = BsgDesc(kind, out, flags, M, N, K, _ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(bias), _ptr(D),
-                alpha, _ptr(alpha_dev), _ptr(C), beta, _ptr(alpha_row), _ptr(alpha_col))
+                alpha, _ptr(alpha_dev), _ptr(C), beta, _ptr(alpha_row), _ptr(alpha_col), L,
+                *(st.get(k, 0) for k in ("stride_A", "stride_B", "stride_SFA", "stride_SFB", "stride_D", "stride_C")))
     h = ctypes.c_void_p()
     _check(lib().bsg_plan_create(ctypes.byref(h), ctypes.byref(d)))
     return h.value

@@ -37,8 +37,8 @@ enum : unsigned {
 // Kernel parameters, passed by value as a __grid_constant__ (the tensor maps must live in
 // parameter space for the TMA instructions).
 struct GemmParams {
-  CUtensorMap tmap_a;  // A codes: bytes, dims {K bytes, M}, box {128, 128}, 128-byte swizzle
-  CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N}, box {128, BN}, 128-byte swizzle
+  CUtensorMap tmap_a;  // A codes: bytes, dims {K bytes, M, batches}, box {128, 128, 1}, 128-byte swizzle
+  CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N, batches}, box {128, BN, 1}, 128-byte swizzle
   const uint8_t* sfa;  // swizzled 128x4 scale atoms of A
   const uint8_t* sfb;
   const void* bias;    // N values of the output type (flags & F_BIAS)
@@ -60,11 +60,15 @@ struct GemmParams {
   int sfb_bands;           // padded rows / 128 of B
   int sfa_bands;           // padded rows / 128 of A
   int num_m_tiles, num_n_tiles, num_k_tiles;
-  int num_tiles;
+  int num_tiles;           // tiles of all batch entries (the workspace's tile count)
+  int batches;             // L >= 1 problems of this shape, entry b at the strides below
+  int units_per_batch;     // num_m_groups * num_n_groups * splits
+  long long sfa_batch, sfb_batch;  // bytes between the scale buffers of consecutive entries
+  long long d_batch, c_batch;      // 16-bit elements between consecutive D (C) matrices
   int splits;              // split-K factor (every split owns >= 1 k-tile)
   int split_mode;          // SPLIT_NONE, SPLIT_WORKSPACE or SPLIT_CLUSTER
   int k_tiles_per_split;
-  int num_units;           // num_tiles * splits
+  int num_units;           // units_per_batch * batches
   int group_m;             // tile rasterisation: m-blocks per group
   int ring_stages;         // shared-memory ring stages in use (the kernel's maximum, or fewer to
                            // make room for split-K receive slots)
@@ -97,6 +101,21 @@ bool gemm_kernel_info_nv_kc2(int bn, int out, GemmKernelInfo* info);
 // CTA-pair kernels (256 x 256 pair tiles, launched in clusters of 2).
 bool gemm_pair_kernel_info_mx(int out, GemmKernelInfo* info);  // BSG_PAIR_KC=1 or 2 (default 2)
 bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info);  // BSG_PAIR_KC=1 or 2 (default 2)
+// The same lookups for the extended instantiations: the residual and per-row / per-column factor
+// epilogue and batch entries (chosen when a problem sets BSG_F_C, BSG_F_ALPHA_ROW or
+// BSG_F_ALPHA_COL, or has L > 1).
+bool gemm_kernel_info_mx_ext(int bn, int out, int kc, GemmKernelInfo* info);
+bool gemm_kernel_info_nv_ext(int bn, int out, int kc, GemmKernelInfo* info);
+bool gemm_kernel_info_mx_narrow_ext(int bn, int out, GemmKernelInfo* info);
+bool gemm_kernel_info_nv_narrow_ext(int bn, int out, GemmKernelInfo* info);
+bool gemm_kernel_info_mx_kc2_ext(int bn, int out, GemmKernelInfo* info);
+bool gemm_kernel_info_nv_kc2_ext(int bn, int out, GemmKernelInfo* info);
+bool gemm_pair_kernel_info_mx_ext(int out, GemmKernelInfo* info);
+bool gemm_pair_kernel_info_nv_ext(int out, GemmKernelInfo* info);
+
+// The kernel of variant (pair, bn, kc) for a problem's format, output type, epilogue flags and
+// batch count.
+bool find_kernel(int kind, int out, unsigned flags, int batches, bool pair, int bn, int kc, GemmKernelInfo* info);
 
 // Quantisers (stream-ordered).  See bsg_quantize / bsg_quantize_bf16 in include/bsgemm.h; the
 // uint16_t forms read BF16 bit patterns.

@@ -95,21 +95,32 @@ struct GemmCfg {
 };
 
 struct UnitCoord {
-  int m_blk, n_blk, split, tile, kt0, kt1;
+  int m_blk, n_blk, split, tile, kt0, kt1, batch;
 };
 
-// Unit u (a tile, or one split of a tile) -> tile coordinates and k range.  With a multicast
-// cluster, u numbers blocks of cmm x cmn tiles and `rank` (the CTA's rank in its cluster,
-// rn + cmn * rm) picks the tile of the block.
+// Unit u (a tile, or one split of a tile, of batch entry u / units_per_batch) -> tile
+// coordinates and k range.  With a multicast cluster, u numbers blocks of cmm x cmn tiles and
+// `rank` (the CTA's rank in its cluster, rn + cmn * rm) picks the tile of the block.  `tile` is
+// the tile's index over all entries (the workspace's).  Batch entries exist only in the EXT
+// instantiations; elsewhere c.batch is the constant 0 and every batch offset folds away.
+template <bool EXT>
 __device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u, int rank) {
   UnitCoord c;
+  c.batch = 0;
+  int tile0 = 0;  // tiles of the entries before this one
+  if (EXT && p.batches > 1) {
+    c.batch = u / p.units_per_batch;
+    u -= c.batch * p.units_per_batch;
+    tile0 = c.batch * (p.units_per_batch / p.splits);
+  }
   c.split = u % p.splits;
-  c.tile = u / p.splits;
+  const int t = u / p.splits;
+  c.tile = tile0 + t;
   const int per_group = p.group_m * p.num_n_groups;
-  const int g = c.tile / per_group;
+  const int g = t / per_group;
   const int first_m = g * p.group_m;
   const int gm = min(p.num_m_groups - first_m, p.group_m);
-  const int r = c.tile - g * per_group;
+  const int r = t - g * per_group;
   c.m_blk = (first_m + r % gm) * p.cmm + rank / p.cmn;
   c.n_blk = (r / gm) * p.cmn + rank % p.cmn;
   c.kt0 = c.split * p.k_tiles_per_split;
@@ -196,6 +207,14 @@ __device__ __forceinline__ void st_out16(uint16_t* d, const uint32_t (&o)[8], bo
   }
 }
 
+// Row m of D (C) of batch entry b.
+__device__ __forceinline__ uint16_t* d_row(const GemmParams& p, int b, int m) {
+  return static_cast<uint16_t*>(p.d) + static_cast<size_t>(b) * p.d_batch + static_cast<size_t>(m) * p.N;
+}
+__device__ __forceinline__ const uint16_t* c_row(const GemmParams& p, int b, int m) {
+  return static_cast<const uint16_t*>(p.c) + static_cast<size_t>(b) * p.c_batch + static_cast<size_t>(m) * p.N;
+}
+
 // alpha * alpha_row[m]: the part of the epilogue factor shared by a whole output row.
 __device__ __forceinline__ float row_alpha(const GemmParams& p, float alpha, int m) {
   return ((p.flags & F_ALPHA_ROW) && m < p.M) ? __fmul_rn(alpha, __ldg(p.alpha_row + m)) : alpha;
@@ -279,8 +298,8 @@ __device__ __forceinline__ void epi_pack_ext(const GemmParams& p, int n, const f
 // 16 consecutive values of C (output type) at row m, column n, as eight words: one 32-byte load
 // when C is 32-byte aligned (wide), else two 16-byte loads.  Plain loads: C may be D itself, and
 // every element is read by the thread that later stores it.
-__device__ __forceinline__ void load_c16(const GemmParams& p, int m, int n, bool wide, uint32_t (&w)[8]) {
-  const uint16_t* src = static_cast<const uint16_t*>(p.c) + static_cast<size_t>(m) * p.N + n;
+__device__ __forceinline__ void load_c16(const GemmParams& p, int b, int m, int n, bool wide, uint32_t (&w)[8]) {
+  const uint16_t* src = c_row(p, b, m) + n;
   if (wide) {
     asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
@@ -298,12 +317,13 @@ __device__ __forceinline__ void load_c16(const GemmParams& p, int m, int n, bool
 // the epilogue into D: the plain path, or (C / per-column factors) the extended one, which loads
 // C one group of 16 columns ahead of the arithmetic.  Rows at or beyond M and columns at or
 // beyond N are not stored.
-template <int OUT, int G>
-__device__ __forceinline__ void epilogue_row(const GemmParams& p, int m, int n0, const uint32_t* r, float alpha) {
-  uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+template <int OUT, int G, bool EXT>
+__device__ __forceinline__ void epilogue_row(const GemmParams& p, int b, int m, int n0, const uint32_t* r,
+                                             float alpha) {
+  uint16_t* drow = d_row(p, b, m);
   const bool wide = p.flags & F_D32;
   const bool row_in = m < p.M;
-  if (!(p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW))) {
+  if (!EXT || !(p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW))) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int n = n0 + 16 * g;
@@ -317,14 +337,14 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, int m, int n0,
   const float alpha_m = row_alpha(p, alpha, m);
   const bool has_c = (p.flags & F_C) && row_in;
   uint32_t cnext[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (has_c && n0 < p.N) load_c16(p, m, n0, wide, cnext);
+  if (has_c && n0 < p.N) load_c16(p, b, m, n0, wide, cnext);
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const int n = n0 + 16 * g;
     uint32_t ccur[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) ccur[i] = cnext[i];
-    if (g + 1 < G && has_c && n + 16 < p.N) load_c16(p, m, n + 16, wide, cnext);
+    if (g + 1 < G && has_c && n + 16 < p.N) load_c16(p, b, m, n + 16, wide, cnext);
     uint32_t o[8];
     epi_pack_ext<OUT, 8>(p, n, reinterpret_cast<const float*>(r + 16 * g), alpha_m, ccur, o);
     epi_pack_ext<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(r + 16 * g + 8), alpha_m, ccur + 4, o + 4);
@@ -333,12 +353,12 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, int m, int n0,
 }
 
 // Epilogue of 32 consecutive columns n0.. of output row m held by this thread.
-template <int OUT>
-__device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0, const float* v,
+template <int OUT, bool EXT>
+__device__ __forceinline__ void store_chunk32(const GemmParams& p, int b, int m, int n0, const float* v,
                                               float alpha) {
   if (m >= p.M) return;
-  uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
-  const bool ext = p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW);
+  uint16_t* drow = d_row(p, b, m);
+  const bool ext = EXT && (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW));
   const float alpha_m = ext ? row_alpha(p, alpha, m) : alpha;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -347,7 +367,7 @@ __device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0
     uint32_t o[8];
     if (ext) {
       uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (p.flags & F_C) load_c16(p, m, n, (p.flags & F_D32) != 0, c);
+      if (p.flags & F_C) load_c16(p, b, m, n, (p.flags & F_D32) != 0, c);
       epi_pack_ext<OUT, 8>(p, n, v + 16 * h, alpha_m, c, o);
       epi_pack_ext<OUT, 8>(p, n + 8, v + 16 * h + 8, alpha_m, c + 4, o + 4);
     } else {
@@ -362,26 +382,25 @@ __device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n0
 // (braw); packed two per word.  EXT: the residual and per-column factors too (alpha_m is then
 // row_alpha(alpha, m)); without it, the plain path's arithmetic exactly.
 template <int OUT, bool EXT>
-__device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, int m, int n, const float4& a, uint2 braw,
-                                                float alpha_m) {
-  const uint16_t* b = reinterpret_cast<const uint16_t*>(&braw);
+__device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, int b, int m, int n, const float4& a,
+                                                uint2 braw, float alpha_m) {
+  const uint16_t* bv = reinterpret_cast<const uint16_t*>(&braw);
   float y[4] = {a.x, a.y, a.z, a.w};
   const bool has_bias = (p.flags & F_BIAS) != 0;
   if (!EXT || !(p.flags & F_ALPHA_COL)) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      y[i] = has_bias ? __fmaf_rn(alpha_m, y[i], out_to_float<OUT>(b[i])) : __fmul_rn(alpha_m, y[i]);
+      y[i] = has_bias ? __fmaf_rn(alpha_m, y[i], out_to_float<OUT>(bv[i])) : __fmul_rn(alpha_m, y[i]);
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float ai = __fmul_rn(alpha_m, __ldg(p.alpha_col + n + i));
-      y[i] = has_bias ? __fmaf_rn(ai, y[i], out_to_float<OUT>(b[i])) : __fmul_rn(ai, y[i]);
+      y[i] = has_bias ? __fmaf_rn(ai, y[i], out_to_float<OUT>(bv[i])) : __fmul_rn(ai, y[i]);
     }
   }
   if (EXT && (p.flags & F_C)) {
     uint16_t c[4];
-    *reinterpret_cast<uint2*>(c) =
-        *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.c) + static_cast<size_t>(m) * p.N + n);
+    *reinterpret_cast<uint2*>(c) = *reinterpret_cast<const uint2*>(c_row(p, b, m) + n);
 #pragma unroll
     for (int i = 0; i < 4; ++i) y[i] = __fmaf_rn(p.beta, out_to_float<OUT>(c[i]), y[i]);
   }
@@ -428,15 +447,15 @@ __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const floa
     const int row = (rl / (32 / S)) * 32 + c.split * (32 / S) + rl % (32 / S);
     const int m = c.m_blk * 128 + row;
     if (m < p.M && n < p.N)  // N % 16 == 0: groups of 4 are whole
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N + n) =
-          epi4_with_bias<OUT, EXT>(p, m, n, acc, braw, EXT ? row_alpha(p, alpha, m) : alpha);
+      *reinterpret_cast<uint2*>(d_row(p, c.batch, m) + n) =
+          epi4_with_bias<OUT, EXT>(p, c.batch, m, n, acc, braw, EXT ? row_alpha(p, alpha, m) : alpha);
   }
 }
 
-template <int OUT, int BN>
+template <int OUT, int BN, bool EXT>
 __device__ __forceinline__ void cluster_reduce(const GemmParams& p, const float* slabs, const UnitCoord& c,
                                                float alpha, uint2 braw, int t) {
-  if (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW)) {
+  if (EXT && (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW))) {
     if (p.splits == 2) cluster_reduce_s<OUT, BN, 2, true>(p, slabs, c, alpha, braw, t);
     else if (p.splits == 4) cluster_reduce_s<OUT, BN, 4, true>(p, slabs, c, alpha, braw, t);
     else cluster_reduce_s<OUT, BN, 8, true>(p, slabs, c, alpha, braw, t);
@@ -454,7 +473,9 @@ __device__ __forceinline__ uint4 rotate_words(uint4 v, int r) {
   return v;
 }
 
-template <int KIND, int BN, int KC, int OUT>
+// EXT: the instantiation with the residual and per-row / per-column factor epilogue and batch
+// entries (single problems without those flags run the instantiation without their code).
+template <int KIND, int BN, int KC, int OUT, bool EXT>
 __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<KIND, BN, KC>;
   extern __shared__ uint8_t smem_raw[];
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         bool ok = true;
         bool first = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit(p, u, crank);
+          const UnitCoord c = decode_unit<EXT>(p, u, crank);
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
             if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
               ok = false;
@@ -572,16 +593,30 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
                   // this CTA's slice of the A tile (the tensor map's box is 128/cmn rows), written
                   // into the same stage of every CTA that shares the m-tile
                   const int rows = C::BM / p.cmn;
-                  tma_load_2d_mc(sa + rn * rows * C::BK_BYTES, &p.tmap_a, fb, x, c.m_blk * C::BM + rn * rows, amask);
+                  if (EXT && p.batches > 1)
+                    tma_load_3d_mc(sa + rn * rows * C::BK_BYTES, &p.tmap_a, fb, x, c.m_blk * C::BM + rn * rows, c.batch,
+                                   amask);
+                  else
+                    tma_load_2d_mc(sa + rn * rows * C::BK_BYTES, &p.tmap_a, fb, x, c.m_blk * C::BM + rn * rows, amask);
                 } else {
-                  tma_load_2d(sa, &p.tmap_a, fb, x, c.m_blk * C::BM);
+                  if (EXT && p.batches > 1)
+                    tma_load_3d(sa, &p.tmap_a, fb, x, c.m_blk * C::BM, c.batch);
+                  else
+                    tma_load_2d(sa, &p.tmap_a, fb, x, c.m_blk * C::BM);
                 }
                 if (p.cmm > 1) {
                   // likewise a BN/cmm-row slice of the B tile for every CTA that shares the n-tile
                   const int rows = BN / p.cmm;
-                  tma_load_2d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, bmask);
+                  if (EXT && p.batches > 1)
+                    tma_load_3d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, c.batch,
+                                   bmask);
+                  else
+                    tma_load_2d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, bmask);
                 } else {
-                  tma_load_2d(sb, &p.tmap_b, fb, x, c.n_blk * BN);
+                  if (EXT && p.batches > 1)
+                    tma_load_3d(sb, &p.tmap_b, fb, x, c.n_blk * BN, c.batch);
+                  else
+                    tma_load_2d(sb, &p.tmap_b, fb, x, c.n_blk * BN);
                 }
               }
             }
@@ -616,7 +651,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         bool ok = true;
         bool first = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit(p, u, crank);
+          const UnitCoord c = decode_unit<EXT>(p, u, crank);
           const int band0 = c.n_blk * BN / 128;    // first scale band of the B tile
           const bool a_band = c.m_blk < p.sfa_bands;  // false only for a cluster's m-tile beyond M
           int bands = 0;
@@ -636,7 +671,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
               const uint32_t fb = bar_sf_full(stage);
               mbar_arrive_expect_tx(fb, static_cast<uint32_t>(((a_band ? 1 : 0) + bands) * sf_atoms * 512));
               if (a_band) {
-                const uint8_t* sa = p.sfa + (static_cast<size_t>(c.m_blk) * p.sfa_atoms_per_band +
+                const uint8_t* sa = p.sfa + c.batch * p.sfa_batch + (static_cast<size_t>(c.m_blk) * p.sfa_atoms_per_band +
                                              static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
                 bulk_load(stage_sfa(stage), sa, sf_atoms * 512, fb);
               }
@@ -644,7 +679,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
               for (int rb = 0; rb < C::NB; ++rb) {
                 const int band = band0 + rb;
                 if (band < p.sfb_bands) {
-                  const uint8_t* sb = p.sfb + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
+                  const uint8_t* sb = p.sfb + c.batch * p.sfb_batch + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
                                                static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
                   bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512, sb, sf_atoms * 512, fb);
                 }
@@ -667,7 +702,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit(p, u, crank);
+          const UnitCoord c = decode_unit<EXT>(p, u, crank);
           if (!wait_bounded(bar_tempty(acc), acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
             ok = false;
             break;
@@ -749,7 +784,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     uint32_t phase = 0;
     bool ok = true;
     for (int u = u0; ok && u < p.num_units; u += ustep) {
-      const UnitCoord c = decode_unit(p, u, crank);
+      const UnitCoord c = decode_unit<EXT>(p, u, crank);
       const int jq = BN < 128 ? (c.n_blk * BN % 128) / 32 : 0;
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
         ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
@@ -801,7 +836,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = u0; u < p.num_units; u += ustep) {
-      const UnitCoord c = decode_unit(p, u, crank);
+      const UnitCoord c = decode_unit<EXT>(p, u, crank);
       bool ok = wait_bounded(bar_tfull(acc), acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
       ok = named_bar_and(1, C::EPI_THREADS, ok);
       if (!ok) break;
@@ -811,7 +846,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
       const int m = c.m_blk * C::BM + row;
       const int nbase = c.n_blk * BN;
       if (p.split_mode == SPLIT_NONE) {
-        uint16_t* drow = static_cast<uint16_t*>(p.d) + static_cast<size_t>(m) * p.N;
+        uint16_t* drow = d_row(p, c.batch, m);
         if constexpr (C::NACC == 1) {
           // One accumulator: the whole row segment comes out of TMEM before any arithmetic and
           // the accumulator is released at once, since the next tile's MMAs need all of it.
@@ -823,7 +858,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(acc));
-          epilogue_row<OUT, HC / 16>(p, m, nbase + col0, r, alpha);
+          epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, nbase + col0, r, alpha);
         } else {
           // Two accumulators: the next tile's MMAs run in the other one, so the segment is
           // rounded chunk by chunk (fewer live registers) and released before the stores.
@@ -836,7 +871,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
               tmem_ld_32x32b_x32(t_row + col0 + ch * 32, r);
             tmem_ld_wait();
           };
-          if (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW)) {
+          if (EXT && (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW))) {
             const float alpha_m = row_alpha(p, alpha, m);
 #pragma unroll
             for (int ch = 0; ch < (HC + 31) / 32; ++ch) {
@@ -845,11 +880,11 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
 #pragma unroll
               for (int h = 0; h < W / 16; ++h) {
                 const int n = nbase + col0 + ch * 32 + 16 * h;
-                uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if ((p.flags & F_C) && m < p.M && n < p.N) load_c16(p, m, n, (p.flags & F_D32) != 0, c);
-                epi_pack_ext<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[16 * h]), alpha_m, c,
+                uint32_t cw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if ((p.flags & F_C) && m < p.M && n < p.N) load_c16(p, c.batch, m, n, (p.flags & F_D32) != 0, cw);
+                epi_pack_ext<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[16 * h]), alpha_m, cw,
                                      &packed[ch * 16 + 8 * h]);
-                epi_pack_ext<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(&r[16 * h + 8]), alpha_m, c + 4,
+                epi_pack_ext<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(&r[16 * h + 8]), alpha_m, cw + 4,
                                      &packed[ch * 16 + 8 * h + 4]);
               }
             }
@@ -934,8 +969,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
           const bool got = named_bar_and(1, C::EPI_THREADS,
                                          wait_bounded_cluster(bar_recv, 0, abort_flag, p, ST_TIMEOUT_EPILOGUE));
           if (got)
-            cluster_reduce<OUT, BN>(p, reinterpret_cast<const float*>(smem + nst * C::STAGE_BYTES), c, alpha, braw,
-                                    et);
+            cluster_reduce<OUT, BN, EXT>(p, reinterpret_cast<const float*>(smem + nst * C::STAGE_BYTES), c, alpha,
+                                         braw, et);
           if (sender) bulk_wait_group0();  // the slab has reached the peer before this CTA may leave
         } else {
           // FP32 partial tile -> workspace as float4 [chunk][8][128 rows] (coalesced per warp)
@@ -986,7 +1021,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
                   v[4 * g + 3] += t.w;
                 }
               }
-              store_chunk32<OUT>(p, m, nbase + ch * 32, v, alpha);
+              store_chunk32<OUT, EXT>(p, c.batch, m, nbase + ch * 32, v, alpha);
             }
           }
           named_bar_sync(1, C::EPI_THREADS);
@@ -1029,10 +1064,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
   }
 }
 
-template <int KIND, int BN, int KC, int OUT>
+template <int KIND, int BN, int KC, int OUT, bool EXT = false>
 bool fill_kernel_info(GemmKernelInfo* info) {
   using C = GemmCfg<KIND, BN, KC>;
-  info->fn = reinterpret_cast<const void*>(&bsg_gemm_kernel<KIND, BN, KC, OUT>);
+  info->fn = reinterpret_cast<const void*>(&bsg_gemm_kernel<KIND, BN, KC, OUT, EXT>);
   info->smem_bytes = C::SMEM_BYTES;
   info->threads = C::THREADS;
   info->bn = BN;

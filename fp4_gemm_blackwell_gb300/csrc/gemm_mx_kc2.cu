@@ -2,13 +2,20 @@
 // two 128-byte k-slabs per ring stage (64- and 128-wide tiles).
 #include "gemm_kernel.cuh"
 
+// Instantiated twice: here without the residual / factor epilogue and batch entries, and by the
+// _ext twin of this file (which defines these two macros and includes it) with them.
+#ifndef BSG_INST_EXT
+#define BSG_INST_EXT false
+#define BSG_INST_NAME(f) f
+#endif
+
 namespace bsg {
 
-bool gemm_kernel_info_mx_kc2(int bn, int out, GemmKernelInfo* info) {
-  if (bn == 64 && out == OUT_F16) return fill_kernel_info<KIND_MX, 64, 2, OUT_F16>(info);
-  if (bn == 64 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 64, 2, OUT_BF16>(info);
-  if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_MX, 128, 2, OUT_F16>(info);
-  if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 128, 2, OUT_BF16>(info);
+bool BSG_INST_NAME(gemm_kernel_info_mx_kc2)(int bn, int out, GemmKernelInfo* info) {
+  if (bn == 64 && out == OUT_F16) return fill_kernel_info<KIND_MX, 64, 2, OUT_F16, BSG_INST_EXT>(info);
+  if (bn == 64 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 64, 2, OUT_BF16, BSG_INST_EXT>(info);
+  if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_MX, 128, 2, OUT_F16, BSG_INST_EXT>(info);
+  if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 128, 2, OUT_BF16, BSG_INST_EXT>(info);
   return false;
 }
 

@@ -3,25 +3,32 @@
 
 #include "gemm_pair_kernel.cuh"
 
+// Instantiated twice: here without the residual / factor epilogue and batch entries, and by the
+// _ext twin of this file (which defines these two macros and includes it) with them.
+#ifndef BSG_INST_EXT
+#define BSG_INST_EXT false
+#define BSG_INST_NAME(f) f
+#endif
+
 namespace bsg {
 
-bool gemm_kernel_info_nv(int bn, int out, int kc, GemmKernelInfo* info) {
-  if (kc == 2) return gemm_kernel_info_nv_kc2(bn, out, info);
-  if (bn < 128) return gemm_kernel_info_nv_narrow(bn, out, info);
-  if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_NV, 128, 1, OUT_F16>(info);
-  if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 128, 1, OUT_BF16>(info);
-  if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_NV, 256, 1, OUT_F16>(info);
-  if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 256, 1, OUT_BF16>(info);
+bool BSG_INST_NAME(gemm_kernel_info_nv)(int bn, int out, int kc, GemmKernelInfo* info) {
+  if (kc == 2) return BSG_INST_NAME(gemm_kernel_info_nv_kc2)(bn, out, info);
+  if (bn < 128) return BSG_INST_NAME(gemm_kernel_info_nv_narrow)(bn, out, info);
+  if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_NV, 128, 1, OUT_F16, BSG_INST_EXT>(info);
+  if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 128, 1, OUT_BF16, BSG_INST_EXT>(info);
+  if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_NV, 256, 1, OUT_F16, BSG_INST_EXT>(info);
+  if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 256, 1, OUT_BF16, BSG_INST_EXT>(info);
   return false;
 }
 
-bool gemm_pair_kernel_info_nv(int out, GemmKernelInfo* info) {
+bool BSG_INST_NAME(gemm_pair_kernel_info_nv)(int out, GemmKernelInfo* info) {
   const char* e = std::getenv("BSG_PAIR_KC");
   const int kc = (e != nullptr && std::atoi(e) == 1) ? 1 : 2;  // two k-slabs per stage unless forced
-  if (kc == 2 && out == OUT_F16) return fill_pair_kernel_info<KIND_NV, 2, OUT_F16>(info);
-  if (kc == 2 && out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, 2, OUT_BF16>(info);
-  if (out == OUT_F16) return fill_pair_kernel_info<KIND_NV, 1, OUT_F16>(info);
-  if (out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, 1, OUT_BF16>(info);
+  if (kc == 2 && out == OUT_F16) return fill_pair_kernel_info<KIND_NV, 2, OUT_F16, BSG_INST_EXT>(info);
+  if (kc == 2 && out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, 2, OUT_BF16, BSG_INST_EXT>(info);
+  if (out == OUT_F16) return fill_pair_kernel_info<KIND_NV, 1, OUT_F16, BSG_INST_EXT>(info);
+  if (out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, 1, OUT_BF16, BSG_INST_EXT>(info);
   return false;
 }
 

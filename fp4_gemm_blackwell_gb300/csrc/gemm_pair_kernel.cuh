@@ -81,7 +81,7 @@ struct PairCfg {
   static_assert(TMEM_USED <= TMEM_COLS, "tensor memory");
 };
 
-template <int KIND, int KC, int OUT>
+template <int KIND, int KC, int OUT, bool EXT>
 __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   using C = PairCfg<KIND, KC>;
   extern __shared__ uint8_t smem_raw[];
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         bool ok = true;
         bool first = true;
         for (int u = pair0; ok && u < p.num_units; u += pairs) {
-          const UnitCoord c = decode_unit(p, u, 0);
+          const UnitCoord c = decode_unit<EXT>(p, u, 0);
           const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
             if (!wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
@@ -180,9 +180,14 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
 #pragma unroll
               for (int j = 0; j < KC; ++j) {  // slabs past K read as zeros (their MMAs are skipped)
                 const int x = (kt * KC + j) * C::BK_BYTES;
-                tma_load_2d_pair(stage_a(stage) + j * C::SLAB_A, &p.tmap_a, fb, x, m_blk * C::BM);
-                tma_load_2d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x,
-                                 c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128);
+                const int yb = c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128;
+                if (EXT && p.batches > 1) {
+                  tma_load_3d_pair(stage_a(stage) + j * C::SLAB_A, &p.tmap_a, fb, x, m_blk * C::BM, c.batch);
+                  tma_load_3d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x, yb, c.batch);
+                } else {
+                  tma_load_2d_pair(stage_a(stage) + j * C::SLAB_A, &p.tmap_a, fb, x, m_blk * C::BM);
+                  tma_load_2d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x, yb);
+                }
               }
             }
             first = false;
@@ -205,7 +210,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         bool ok = true;
         bool first = true;
         for (int u = pair0; ok && u < p.num_units; u += pairs) {
-          const UnitCoord c = decode_unit(p, u, 0);
+          const UnitCoord c = decode_unit<EXT>(p, u, 0);
           const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
           const bool a_band = m_blk < p.sfa_bands;  // false for the pair's second m-tile past M
           int bands = 0;
@@ -229,7 +234,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
               mbar_arrive_expect_tx(sb, static_cast<uint32_t>(((a_band ? 1 : 0) + bands) * sf_atoms * 512));
               if (a_band)
                 bulk_load(stage_sfa(stage),
-                          p.sfa + (static_cast<size_t>(m_blk) * p.sfa_atoms_per_band +
+                          p.sfa + c.batch * p.sfa_batch + (static_cast<size_t>(m_blk) * p.sfa_atoms_per_band +
                                    static_cast<size_t>(kt) * C::SF_ATOMS) * 512,
                           sf_atoms * 512, sb);
 #pragma unroll
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
                 const int band = c.n_blk * 2 + rb;
                 if (band < p.sfb_bands)
                   bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512,
-                            p.sfb + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
+                            p.sfb + c.batch * p.sfb_batch + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
                                      static_cast<size_t>(kt) * C::SF_ATOMS) * 512,
                             sf_atoms * 512, sb);
               }
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int u = pair0; ok && u < p.num_units; u += pairs) {
-          const UnitCoord c = decode_unit(p, u, 0);
+          const UnitCoord c = decode_unit<EXT>(p, u, 0);
           if (!wait_bounded_cluster(bar_tempty, acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
             ok = false;
             break;
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     uint32_t ph_old = 0;
     bool ok = true;
     for (int u = pair0; ok && u < p.num_units; u += pairs) {
-      const UnitCoord c = decode_unit(p, u, 0);
+      const UnitCoord c = decode_unit<EXT>(p, u, 0);
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
         ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
         if (!ok) break;
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
     uint32_t acc_phase = 0;
     for (int u = pair0; u < p.num_units; u += pairs) {
-      const UnitCoord c = decode_unit(p, u, 0);
+      const UnitCoord c = decode_unit<EXT>(p, u, 0);
       bool ok = wait_bounded_cluster(bar_tfull, acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
       ok = named_bar_and(1, C::EPI_THREADS, ok);
       if (!ok) break;
@@ -449,7 +454,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         else
           tc_commit_pair_mc(bar_tempty, leader_mask);
       }
-      epilogue_row<OUT, HC / 16>(p, m, nbase + col0, r, alpha);
+      epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, nbase + col0, r, alpha);
       acc_phase ^= 1u;
     }
   }
@@ -470,10 +475,10 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
   }
 }
 
-template <int KIND, int KC, int OUT>
+template <int KIND, int KC, int OUT, bool EXT = false>
 bool fill_pair_kernel_info(GemmKernelInfo* info) {
   using C = PairCfg<KIND, KC>;
-  info->fn = reinterpret_cast<const void*>(&bsg_gemm_pair_kernel<KIND, KC, OUT>);
+  info->fn = reinterpret_cast<const void*>(&bsg_gemm_pair_kernel<KIND, KC, OUT, EXT>);
   info->kc = KC;
   info->smem_bytes = C::SMEM_BYTES;
   info->threads = C::THREADS;

@@ -137,6 +137,23 @@ bsg_status validate_desc(const bsg_desc* d) {
                 d->M, d->N, d->K);
   if (d->N % 16) return fail(BSG_ERR_SHAPE, "N=%d is not a multiple of 16", d->N);
   if (d->K % 32) return fail(BSG_ERR_SHAPE, "K=%d is not a multiple of 32", d->K);
+  if (d->L < 0 || d->L > 65535) return fail(BSG_ERR_SHAPE, "L=%d out of range (0..65535)", d->L);
+  if (d->L > 1) {
+    const long long rb = static_cast<long long>(code_row_bytes(d->kind, d->K));
+    const struct {
+      long long stride, need;
+      const char* name;
+    } st[] = {{d->stride_A, rb * d->M, "stride_A"},
+              {d->stride_B, rb * d->N, "stride_B"},
+              {d->stride_SFA, static_cast<long long>(sf_bytes_of(d->kind, d->M, d->K)), "stride_SFA"},
+              {d->stride_SFB, static_cast<long long>(sf_bytes_of(d->kind, d->N, d->K)), "stride_SFB"},
+              {d->stride_D, 2LL * d->M * d->N, "stride_D"},
+              {(d->flags & BSG_F_C) ? d->stride_C : 2LL * d->M * d->N, 2LL * d->M * d->N, "stride_C"}};
+    for (const auto& x : st)
+      if (x.stride % 16 || x.stride < x.need)
+        return fail(BSG_ERR_SHAPE, "%s=%lld must be a multiple of 16 and at least one entry (%lld bytes)", x.name,
+                    x.stride, x.need);
+  }
   if (!d->A || !d->B || !d->SFA || !d->SFB || !d->D) return fail(BSG_ERR_INVALID_ARG, "null operand pointer");
   if ((d->flags & BSG_F_BIAS) && !d->bias) return fail(BSG_ERR_INVALID_ARG, "BIAS set but bias is null");
   if ((d->flags & BSG_F_ALPHA_DEVICE) && !d->alpha_dev)
@@ -160,17 +177,26 @@ bsg_status validate_desc(const bsg_desc* d) {
 
 bsg_status validate_ranges(const bsg_desc* d) {
   const size_t rb = code_row_bytes(d->kind, d->K);
+  // bytes of L entries at `stride`, one entry being `one` bytes
+  const size_t L1 = d->L > 1 ? static_cast<size_t>(d->L - 1) : 0;
+  auto span = [&](long long stride, size_t one) { return L1 * static_cast<size_t>(stride) + one; };
   bsg_status s;
-  if ((s = check_range(d->A, rb * d->M, BSG_ERR_SHAPE, "A")) != BSG_OK) return s;
-  if ((s = check_range(d->B, rb * d->N, BSG_ERR_SHAPE, "B")) != BSG_OK) return s;
-  if ((s = check_range(d->SFA, sf_bytes_of(d->kind, d->M, d->K), BSG_ERR_SCALE_LAYOUT, "SFA")) != BSG_OK) return s;
-  if ((s = check_range(d->SFB, sf_bytes_of(d->kind, d->N, d->K), BSG_ERR_SCALE_LAYOUT, "SFB")) != BSG_OK) return s;
-  if ((s = check_range(d->D, static_cast<size_t>(d->M) * d->N * 2, BSG_ERR_SHAPE, "D")) != BSG_OK) return s;
+  if ((s = check_range(d->A, span(d->stride_A, rb * d->M), BSG_ERR_SHAPE, "A")) != BSG_OK) return s;
+  if ((s = check_range(d->B, span(d->stride_B, rb * d->N), BSG_ERR_SHAPE, "B")) != BSG_OK) return s;
+  if ((s = check_range(d->SFA, span(d->stride_SFA, sf_bytes_of(d->kind, d->M, d->K)), BSG_ERR_SCALE_LAYOUT, "SFA")) !=
+      BSG_OK)
+    return s;
+  if ((s = check_range(d->SFB, span(d->stride_SFB, sf_bytes_of(d->kind, d->N, d->K)), BSG_ERR_SCALE_LAYOUT, "SFB")) !=
+      BSG_OK)
+    return s;
+  if ((s = check_range(d->D, span(d->stride_D, static_cast<size_t>(d->M) * d->N * 2), BSG_ERR_SHAPE, "D")) != BSG_OK)
+    return s;
   if ((d->flags & BSG_F_BIAS) && (s = check_range(d->bias, static_cast<size_t>(d->N) * 2, BSG_ERR_SHAPE, "bias")) != BSG_OK)
     return s;
   if ((d->flags & BSG_F_ALPHA_DEVICE) && (s = check_range(d->alpha_dev, 4, BSG_ERR_SHAPE, "alpha_dev")) != BSG_OK)
     return s;
-  if ((d->flags & BSG_F_C) && (s = check_range(d->C, static_cast<size_t>(d->M) * d->N * 2, BSG_ERR_SHAPE, "C")) != BSG_OK)
+  if ((d->flags & BSG_F_C) &&
+      (s = check_range(d->C, span(d->stride_C, static_cast<size_t>(d->M) * d->N * 2), BSG_ERR_SHAPE, "C")) != BSG_OK)
     return s;
   if ((d->flags & BSG_F_ALPHA_ROW) &&
       (s = check_range(d->alpha_row, static_cast<size_t>(d->M) * 4, BSG_ERR_SHAPE, "alpha_row")) != BSG_OK)
@@ -278,9 +304,10 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
   const int nkt = (d->K + k_tile - 1) / k_tile;
   const long long mt = (d->M + 127) / 128;
-  const long long t256 = mt * ((d->N + 255) / 256);
-  const long long t128 = mt * ((d->N + 127) / 128);
-  const long long pair_tiles = ((d->M + 255) / 256) * ((d->N + 255) / 256);
+  const long long L = d->L > 1 ? d->L : 1;  // tiles of all batch entries compete for the SMs
+  const long long t256 = mt * ((d->N + 255) / 256) * L;
+  const long long t128 = mt * ((d->N + 127) / 128) * L;
+  const long long pair_tiles = ((d->M + 255) / 256) * ((d->N + 255) / 256) * L;
   int b, s = 1;
   bool pair = false;
   if (d->M > 256 && 4 * pair_tiles >= sms) {
@@ -300,7 +327,7 @@ Variant choose_variant(const bsg_desc* d, int sms) {
     // of a 128 x bn FP32 tile), which moves ~5x slower than TMA fills.
     double best = 1e30;
     for (int cb : {128, 64}) {
-      const long long tiles = mt * ((d->N + cb - 1) / cb);
+      const long long tiles = mt * ((d->N + cb - 1) / cb) * L;
       const long long want = std::min<long long>(std::min<long long>(nkt, 8), std::max<long long>(1, sms / tiles));
       int cs = 1;
       while (cs * 2 <= want) cs *= 2;
@@ -395,13 +422,16 @@ WorkspaceLayout workspace_layout(const Variant& v, int num_tiles) {
   return w;
 }
 
+// Tiled map of a row-major code matrix (2-D), or of `batches` > 1 of them `batch_bytes` apart (3-D:
+// the kernels load batched operands with the 3-D form of the copy, single ones with the 2-D form).
 bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, uint64_t rows,
-                          uint32_t box_rows, const char* name) {
-  cuuint64_t dims[2] = {row_bytes, rows};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                          uint32_t box_rows, uint64_t batches, uint64_t batch_bytes, const char* name) {
+  cuuint64_t dims[3] = {row_bytes, rows, batches};
+  cuuint64_t strides[2] = {row_bytes, batch_bytes};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t rank = batches > 1 ? 3 : 2;
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(ptr), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -417,9 +447,17 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   std::memset(g, 0, sizeof(*g));
   const size_t rb = code_row_bytes(d->kind, d->K);
   bsg_status s;
-  if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, static_cast<uint32_t>(128 / v.cmn), "A")) != BSG_OK ||
-      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn / v.cmm), "B")) != BSG_OK)
+  const int L = d->L > 1 ? d->L : 1;
+  if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, static_cast<uint32_t>(128 / v.cmn), L, d->stride_A, "A")) !=
+          BSG_OK ||
+      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn / v.cmm), L,
+                          d->stride_B, "B")) != BSG_OK)
     return s;
+  g->batches = L;
+  g->sfa_batch = L > 1 ? d->stride_SFA : 0;
+  g->sfb_batch = L > 1 ? d->stride_SFB : 0;
+  g->d_batch = L > 1 ? d->stride_D / 2 : 0;
+  g->c_batch = (L > 1 && (d->flags & BSG_F_C)) ? d->stride_C / 2 : 0;
   const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
   const int blk = d->kind == BSG_MXFP8 ? 32 : 16;
   g->sfa = static_cast<const uint8_t*>(d->SFA);
@@ -447,7 +485,7 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->num_m_tiles = v.pair ? (d->M + 255) / 256 : (d->M + 127) / 128;
   g->num_n_tiles = (d->N + v.bn - 1) / v.bn;
   g->num_k_tiles = (d->K + k_tile * info.kc - 1) / (k_tile * info.kc);  // ring stages of K
-  g->num_tiles = g->num_m_tiles * g->num_n_tiles;
+  g->num_tiles = g->num_m_tiles * g->num_n_tiles * L;  // over all entries
   g->splits = v.splits;
   g->split_mode = v.mode;
   g->k_tiles_per_split = v.pair ? g->num_k_tiles : v.kps;  // in ring stages
@@ -456,7 +494,8 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->cm = v.cmn * v.cmm;
   g->num_m_groups = (g->num_m_tiles + v.cmm - 1) / v.cmm;
   g->num_n_groups = (g->num_n_tiles + v.cmn - 1) / v.cmn;
-  g->num_units = g->num_m_groups * g->num_n_groups * v.splits;
+  g->units_per_batch = g->num_m_groups * g->num_n_groups * v.splits;
+  g->num_units = g->units_per_batch * L;
   g->group_m = 16;
   g->debug_skip_first_load = 0;
   g->ring_stages = info.stages;
@@ -518,6 +557,22 @@ bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, 
   return launch_with(&cfg, fn, params, stream);
 }
 
+}  // namespace
+
+namespace bsg {
+bool find_kernel(int kind, int out, unsigned flags, int batches, bool pair, int bn, int kc, GemmKernelInfo* info) {
+  const bool ext = (flags & (BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL)) != 0 || batches > 1;
+  if (pair) {
+    if (kind == KIND_MX) return ext ? gemm_pair_kernel_info_mx_ext(out, info) : gemm_pair_kernel_info_mx(out, info);
+    return ext ? gemm_pair_kernel_info_nv_ext(out, info) : gemm_pair_kernel_info_nv(out, info);
+  }
+  if (kind == KIND_MX) return ext ? gemm_kernel_info_mx_ext(bn, out, kc, info) : gemm_kernel_info_mx(bn, out, kc, info);
+  return ext ? gemm_kernel_info_nv_ext(bn, out, kc, info) : gemm_kernel_info_nv(bn, out, kc, info);
+}
+}  // namespace bsg
+
+namespace {
+
 bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   if (out == nullptr) return fail(BSG_ERR_INVALID_ARG, "plan output pointer is null");
   *out = nullptr;
@@ -533,10 +588,8 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   const Variant v = choose_variant(d, di.sms);
   bsg::GemmKernelInfo info{};
   const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
-  const bool found = v.pair ? (d->kind == BSG_MXFP8 ? bsg::gemm_pair_kernel_info_mx(out_t, &info)
-                                                    : bsg::gemm_pair_kernel_info_nv(out_t, &info))
-                            : (d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, v.kc, &info)
-                                                    : bsg::gemm_kernel_info_nv(v.bn, out_t, v.kc, &info));
+  const bool found = bsg::find_kernel(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, d->flags, d->L,
+                                      v.pair, v.bn, v.kc, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
   int resident = di.sms;
@@ -866,12 +919,10 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
   const Variant v = choose_variant(d, di.sms);
   bsg::GemmKernelInfo info{};
   const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
-  const bool found = v.pair ? (d->kind == BSG_MXFP8 ? bsg::gemm_pair_kernel_info_mx(out_t, &info)
-                                                    : bsg::gemm_pair_kernel_info_nv(out_t, &info))
-                            : (d->kind == BSG_MXFP8 ? bsg::gemm_kernel_info_mx(v.bn, out_t, v.kc, &info)
-                                                    : bsg::gemm_kernel_info_nv(v.bn, out_t, v.kc, &info));
+  const bool found = bsg::find_kernel(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, d->flags, d->L,
+                                      v.pair, v.bn, v.kc, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
-  const int num_tiles = ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn);
+  const int num_tiles = ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn) * (d->L > 1 ? d->L : 1);
   const WorkspaceLayout w = workspace_layout(v, num_tiles);
   if (w.total > kNoAllocScratchBytes)
     return fail(BSG_ERR_SHAPE,

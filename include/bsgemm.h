@@ -94,7 +94,12 @@ typedef struct bsg_plan_s* bsg_plan_t;
  *   and beta only with BSG_F_C; alpha_row (M floats) only with BSG_F_ALPHA_ROW; alpha_col
  *   (N floats) only with BSG_F_ALPHA_COL.  With every flag set
  *     D[m,n] = silu(alpha * alpha_row[m] * alpha_col[n] * acc[m,n] + bias[n] + beta * C[m,n]),
- *   the factors multiplied in float32 in that order, each term added in float32. */
+ *   the factors multiplied in float32 in that order, each term added in float32.
+ * Batched (the L of the MXFP8 page's {m, n, k, l} problem shape): L >= 2 independent problems
+ * of this shape in one launch, entry l at A + l*stride_A, B + l*stride_B, SFA + l*stride_SFA,
+ * SFB + l*stride_SFB, D + l*stride_D and (with C) C + l*stride_C (strides in bytes, multiples
+ * of 16, each at least one entry's size); bias, alpha, alpha_row and alpha_col are shared by all
+ * entries.  L = 0 or 1 is one problem (the strides are then ignored); L <= 65535. */
 typedef struct {
   bsg_kind kind;
   bsg_out out;
@@ -112,6 +117,8 @@ typedef struct {
   float beta;
   const float* alpha_row;
   const float* alpha_col;
+  int L;
+  long long stride_A, stride_B, stride_SFA, stride_SFB, stride_D, stride_C;
 } bsg_desc;
 
 /* Validate d, choose the kernel variant (tile shape, split-K), encode the TMA tensor

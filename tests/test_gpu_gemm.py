@@ -12,6 +12,8 @@ import torch
 
 import fp4_gemm_blackwell_gb300 as bsg
 import parity_util as P
+from fp4_gemm_blackwell_gb300 import synth
+from oracle import gemm as R
 
 pytestmark = pytest.mark.gpu
 
@@ -293,3 +295,72 @@ def test_wait_timeout_reports_status_and_context_survives():
         plan.run()
         plan.check_status()
         P.assert_parity(dp.result(), prob, "bf16")
+
+
+
+def _batched_buffers(kind, L, M, N, K, pad=256, residual=False):
+    """L problems quantised by the oracle, copied into single device buffers at strides of one
+    entry + pad bytes; D with canaries between the entries."""
+    probs = [P.make_problem(kind, M, N, K, seed_a=10 + l, seed_b=20 + l) for l in range(L)]
+    def pack(arrs):
+        one = max(a.size for a in arrs)
+        stride = (one + pad + 15) // 16 * 16
+        buf = np.full(L * stride, 0x5A, dtype=np.uint8)
+        for l, a in enumerate(arrs):
+            buf[l * stride:l * stride + a.size] = np.ascontiguousarray(a).view(np.uint8).ravel()
+        return P.dev(buf), stride
+    A, sA = pack([p["A"] for p in probs])
+    B, sB = pack([p["B"] for p in probs])
+    SFA, sSFA = pack([p["SFA"] for p in probs])
+    SFB, sSFB = pack([p["SFB"] for p in probs])
+    sD = (M * N * 2 + pad + 15) // 16 * 16
+    D = torch.full((L * sD // 2,), 0x7BAD, dtype=torch.int16, device="cuda")
+    C = Cvals = None
+    sC = 0
+    if residual:
+        sC = sD
+        bits = np.zeros(L * sC // 2, dtype=np.uint16)
+        Cvals = []
+        for l in range(L):
+            b, v = P.synth_residual(M, N, "bf16", seed=40 + l)
+            bits[l * sC // 2:l * sC // 2 + M * N] = b.ravel()
+            Cvals.append(v)
+        C = P.dev(bits.view(np.int16)).view(torch.int16)
+    strides = dict(stride_A=sA, stride_B=sB, stride_SFA=sSFA, stride_SFB=sSFB, stride_D=sD, stride_C=sC)
+    return probs, A, B, SFA, SFB, D, C, Cvals, strides
+
+
+@pytest.mark.parametrize("env", [{}, {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 128},
+                                 {"BSG_FORCE_BN": 32}, {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2},
+                                 {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3}, {"BSG_FORCE_BN": 32, "BSG_FORCE_CM": 4}])
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_batched(kind, env, monkeypatch):
+    # L = 3 problems of one shape in one launch (the L of the {m, n, k, l} problem shape), every
+    # kernel family; each entry against its own oracle result, nothing written between entries
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    L, M, N, K = 3, 200, 144, 1536
+    residual = kind == "nvfp4" and "BSG_FORCE_SPLITS" in env
+    probs, A, B, SFA, SFB, D, C, Cvals, strides = _batched_buffers(kind, L, M, N, K, residual=residual)
+    bias_bits, bias_vals = synth.bias(N, out="bf16")
+    bias = P.dev(bias_bits.view(np.int16)).view(torch.int16)
+    flags = bsg.BSG_F_BIAS | (bsg.BSG_F_SILU if kind == "nvfp4" else 0) | (bsg.BSG_F_C if residual else 0)
+    alphas = [float(p["alpha"]) for p in probs]
+    # alpha is shared by the batch: give every entry the same one by scaling with entry 0's
+    alpha = alphas[0]
+    with bsg.Plan(P.KIND[kind], P.OUT["bf16"], M, N, K, A, B, SFA, SFB, D, alpha=alpha, flags=flags, bias=bias,
+                  C=C, beta=0.5, L=L, strides=strides) as plan:
+        variant = plan.variant
+        plan.run()
+        plan.check_status()
+    torch.cuda.synchronize()
+    dall = D.cpu().numpy().view(np.uint16)
+    sD = strides["stride_D"] // 2
+    for l, p in enumerate(probs):
+        got = R.out_from_bits(dall[l * sD:l * sD + M * N].reshape(M, N), "bf16")
+        q = dict(p)
+        q["alpha"] = np.float32(alpha)
+        epi = dict(C=Cvals[l], beta=0.5) if residual else None
+        P.assert_parity(got, q, "bf16", bias_vals, kind == "nvfp4", epi=epi)
+        gap = dall[l * sD + M * N:(l + 1) * sD] if l + 1 < L else dall[l * sD + M * N:]
+        assert np.all(gap == 0x7BAD), "wrote past entry %d (%s)" % (l, variant)
