@@ -160,19 +160,27 @@ class Problem:
     """R device copies of one GEMM problem (operands, bias, output) with a plan per copy."""
 
     def __init__(self, bsg, kind, M, N, K, out="bf16", bias=False, silu=False, copies=1, seeds=(0, 1),
-                 residual=False, factors=False):
+                 residual=False, factors=False, L=1):
         """residual: beta * C from a separate M x N matrix per copy (beta = 1); factors: per-row
-        and per-column alpha vectors (U(0.5, 2))."""
+        and per-column alpha vectors (U(0.5, 2)); L > 1: a batch of L problems of this shape per
+        copy, entry l being rows l*M.. of one (L*M) x K operand A (likewise B), quantised as one
+        tensor (M and N multiples of 128, so every entry's scales start on a band)."""
         from fp4_gemm_blackwell_gb300 import synth
-        self.kind, self.M, self.N, self.K, self.out = kind, M, N, K, out
+        self.kind, self.M, self.N, self.K, self.out, self.L = kind, M, N, K, out, L
         self.residual, self.factors = residual, factors
-        a = Operands(bsg, kind, M, K, seeds[0])
-        b = Operands(bsg, kind, N, K, seeds[1])
+        if L > 1 and (M % 128 or N % 128):
+            raise ValueError("batched problems here need M and N multiples of 128")
+        a = Operands(bsg, kind, L * M, K, seeds[0])
+        b = Operands(bsg, kind, L * N, K, seeds[1])
         self.alpha = float(np.float32(np.float32(a.s) * np.float32(b.s)))
         self.flags = ((bsg.BSG_F_BIAS if bias else 0) | (bsg.BSG_F_SILU if silu else 0) |
                       (bsg.BSG_F_C if residual else 0) | (bsg.BSG_F_ALPHA_ROW | bsg.BSG_F_ALPHA_COL if factors else 0))
         self.extra = []
-        cbits = synth.bias(M * N, seed=5, std=1.0, out=out)[0] if residual else None
+        cbits = synth.bias(L * M * N, seed=5, std=1.0, out=out)[0] if residual else None
+        cb = 1 if kind == "mxfp8" else 2
+        strides = dict(stride_A=M * K // cb, stride_B=N * K // cb, stride_SFA=bsg.bsg_sf_bytes(
+            self._k(bsg), M, K), stride_SFB=bsg.bsg_sf_bytes(self._k(bsg), N, K), stride_D=2 * M * N,
+            stride_C=2 * M * N if residual else 0)
         g = torch.Generator(device="cpu")
         g.manual_seed(6)
         ar = (torch.rand(M, generator=g) * 1.5 + 0.5).cuda() if factors else None
@@ -187,28 +195,33 @@ class Problem:
         for i in range(copies):
             ai, bi = (a, b) if i == 0 else (a.clone(), b.clone())
             bt = None if bias_t is None else (bias_t if i == 0 else bias_t.clone())
-            d = torch.empty(M * N, dtype=torch.int16, device="cuda")
+            d = torch.empty(L * M * N, dtype=torch.int16, device="cuda")
             c = torch.from_numpy(cbits.view(np.int16)).cuda() if residual else None
             self.extra.append(c)
             self.sets.append((ai, bi, bt, d))
             self.plans.append(bsg.Plan(k, out_t, M, N, K, ai.codes, bi.codes, ai.sf, bi.sf, d,
                                        alpha=self.alpha, flags=self.flags, bias=bt, C=c, beta=1.0,
-                                       alpha_row=ar, alpha_col=ac))
+                                       alpha_row=ar, alpha_col=ac, L=L if L > 1 else 0,
+                                       strides=strides if L > 1 else None))
         self.variant = self.plans[0].variant
 
+    def _k(self, bsg):
+        return bsg.BSG_MXFP8 if self.kind == "mxfp8" else bsg.BSG_NVFP4
+
     def flops(self):
-        return 2.0 * self.M * self.N * self.K
+        return 2.0 * self.M * self.N * self.K * self.L
 
     def algorithmic_bytes(self):
-        """Bytes one launch must move at least: codes + scales of A and B, bias, output."""
+        """Bytes one launch must move at least: codes + scales of A and B, bias, output (of all
+        L entries; bias and factors are shared by the entries)."""
         cb = 1 if self.kind == "mxfp8" else 0.5
         blk = 32 if self.kind == "mxfp8" else 16
         sf = lambda rows: ((rows + 127) // 128 * 128) * ((self.K // blk + 3) // 4 * 4)
-        b = self.M * self.K * cb + self.N * self.K * cb + sf(self.M) + sf(self.N) + self.M * self.N * 2
+        b = self.L * (self.M * self.K * cb + self.N * self.K * cb + sf(self.M) + sf(self.N) + self.M * self.N * 2)
         if self.flags & 1:
             b += self.N * 2
         if self.residual:
-            b += self.M * self.N * 2
+            b += self.L * self.M * self.N * 2
         if self.factors:
             b += (self.M + self.N) * 4
         return int(b)
@@ -402,6 +415,23 @@ def skinny_config(bsg, peaks, steps=400, warmup=10, **epi):
     r = {"us": round(us, 3), "tflops": round(prob.flops() / (us * 1e-6) / 1e12, 1), "gbs": round(gbs, 1),
          "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": prob.algorithmic_bytes(),
          "variant": prob.variant}
+    prob.close()
+    return r
+
+
+def batched_config(bsg, peaks, L, steps=200, warmup=10):
+    """L problems of the headline shape (NVFP4 128 x 4096 x 4096, bias + SiLU) in one launch,
+    inputs rotated over enough copies to exceed L2."""
+    p1 = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=1, L=L)
+    cp = copies_to_exceed_l2(p1.algorithmic_bytes())
+    p1.close()
+    prob = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=cp, L=L)
+    ms, _ = graph_time(prob.plans, steps, warmup)
+    us = ms * 1e3 / steps
+    gbs = prob.algorithmic_bytes() / (us * 1e-6) / 1e9
+    r = {"L": L, "us": round(us, 3), "us_per_entry": round(us / L, 3),
+         "tflops": round(prob.flops() / (us * 1e-6) / 1e12, 1), "gbs": round(gbs, 1),
+         "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "variant": prob.variant, "copies": cp}
     prob.close()
     return r
 
@@ -618,6 +648,7 @@ CASES = {
     "mxfp8_8192_f16": ("mxfp8", 8192, 8192, 8192, "f16", False, False),
     "nvfp4_8192": ("nvfp4", 8192, 8192, 8192, "bf16", True, True),
     "nvfp4_8000": ("nvfp4", 8000, 8192, 8192, "bf16", True, True),
+    "nvfp4_m128_l8": ("nvfp4", M1, N1, K1, "bf16", True, True, 8),  # a batch of 8 entries
 }
 
 
@@ -628,8 +659,8 @@ def case_arm(args):
     import fp4_gemm_blackwell_gb300 as bsg
     __graft_entry__.build()
     torch.cuda.set_device(0)
-    kind, M, N, K, out, bias, silu = CASES[args.case]
-    prob = Problem(bsg, kind, M, N, K, out=out, bias=bias, silu=silu, copies=1)
+    kind, M, N, K, out, bias, silu, *batch = CASES[args.case]
+    prob = Problem(bsg, kind, M, N, K, out=out, bias=bias, silu=silu, copies=1, L=batch[0] if batch else 1)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -714,6 +745,8 @@ def main():
             extras["nvfp4_8192_bias_silu_residual_factors_bf16"] = big_config(
                 bsg, peaks, "nvfp4", 8192, 8192, 8192, "bf16", True, True, residual=True, factors=True)
             extras["nvfp4_m128_residual_factors"] = skinny_config(bsg, peaks, residual=True, factors=True)
+            for L in (2, 8):
+                extras["nvfp4_batched_l%d_m128_n4096_k4096" % L] = batched_config(bsg, peaks, L)
             extras["launch_loop_1000"] = launch_loop(bsg)
             for kind in ("mxfp8", "nvfp4"):
                 for bf in (False, True):
