@@ -436,6 +436,66 @@ def batched_config(bsg, peaks, L, steps=200, warmup=10):
     return r
 
 
+MOE_TOKENS = (97, 211, 64, 150, 128, 30, 180, 164)  # rows routed to each of 8 experts (1024 in all)
+
+
+def grouped_config(bsg, peaks, steps=200, warmup=10):
+    """Expert GEMMs of a mixture-of-experts layer: 8 groups (experts) of NVFP4 N=4096 x K=4096
+    weights, MOE_TOKENS rows each in the 128-row-aligned grouped layout (group_index on the
+    device, per-expert alpha_dev), bias + SiLU, BF16 out; one grouped launch per step, and for
+    comparison the same 8 problems as 8 plain launches.  Inputs rotate over enough copies to
+    exceed L2.  FLOPs and bytes count the routed rows only."""
+    from fp4_gemm_blackwell_gb300 import synth
+    G, N, K = len(MOE_TOKENS), N1, K1
+    gidx = []
+    for g, n in enumerate(MOE_TOKENS):
+        gidx += [g] * n + [-1] * (-n % 128)
+    M = len(gidx)
+    rows = sum(MOE_TOKENS)
+    cb = 2  # NVFP4: two elements per byte
+    per_copy = M * K // cb + G * N * K // cb + M * N * 2
+    cp = copies_to_exceed_l2(per_copy)
+    k = bsg.BSG_NVFP4
+    bits, _ = synth.bias(N, out="bf16")
+    bias_t = torch.from_numpy(bits.view(np.int16)).cuda()
+    gi = torch.tensor(gidx, dtype=torch.int32, device="cuda")
+    grouped, separate, keep = [], [], []
+    for i in range(cp):
+        a = Operands(bsg, "nvfp4", M, K, 10 + i)
+        b = Operands(bsg, "nvfp4", G * N, K, 20 + i)  # expert g: rows g*N.. of one operand
+        alpha = float(np.float32(np.float32(a.s) * np.float32(b.s)))
+        ad = torch.full((G,), alpha, dtype=torch.float32, device="cuda")
+        d = torch.empty(M * N, dtype=torch.int16, device="cuda")
+        keep += [a, b, ad, d]
+        strides = dict(stride_B=N * K // cb, stride_SFB=bsg.bsg_sf_bytes(k, N, K))
+        grouped.append(bsg.Plan(k, bsg.BSG_OUT_BF16, M, N, K, a.codes, b.codes, a.sf, b.sf, d,
+                                flags=bsg.BSG_F_GROUPED | bsg.BSG_F_ALPHA_DEVICE | bsg.BSG_F_BIAS | bsg.BSG_F_SILU,
+                                bias=bias_t, alpha_dev=ad, L=G, strides=strides, group_index=gi))
+        row0 = 0
+        for g, n in enumerate(MOE_TOKENS):  # the same rows as G plain problems
+            ab = a.codes.view(M, K // cb)[row0:row0 + n]
+            sfa = a.sf[row0 // 128 * bsg.bsg_sf_bytes(k, 128, K):]
+            separate.append(bsg.Plan(k, bsg.BSG_OUT_BF16, n, N, K, ab, b.codes.view(G * N, K // cb)[g * N:],
+                                     sfa, b.sf[g * bsg.bsg_sf_bytes(k, N, K):], d.view(M, N)[row0:],
+                                     alpha=alpha, flags=bsg.BSG_F_BIAS | bsg.BSG_F_SILU, bias=bias_t))
+            row0 += n + (-n % 128)
+    ms, _ = graph_time(grouped, steps, warmup)
+    us = ms * 1e3 / steps
+    ms_s, _ = graph_time(separate, steps * G, warmup * G)
+    us_s = ms_s * 1e3 / steps
+    flops = 2.0 * rows * N * K
+    nbytes = rows * K // cb + G * N * K // cb + bsg.bsg_sf_bytes(k, M, K) + G * bsg.bsg_sf_bytes(k, N, K) + \
+        rows * N * 2 + N * 2 + 4 * G
+    gbs = nbytes / (us * 1e-6) / 1e9
+    r = {"groups": G, "rows": list(MOE_TOKENS), "N": N, "K": K, "us": round(us, 3),
+         "tflops": round(flops / (us * 1e-6) / 1e12, 1), "gbs": round(gbs, 1),
+         "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes,
+         "variant": grouped[0].variant, "separate_launches_us": round(us_s, 3), "copies": cp}
+    for pl in grouped + separate:
+        pl.close()
+    return r
+
+
 def small_config(bsg, peaks, steps=2000, warmup=20):
     prob = Problem(bsg, "mxfp8", 256, 256, 256, copies=64)
     ms, _ = graph_time(prob.plans, steps, warmup)
@@ -747,6 +807,7 @@ def main():
             extras["nvfp4_m128_residual_factors"] = skinny_config(bsg, peaks, residual=True, factors=True)
             for L in (2, 8):
                 extras["nvfp4_batched_l%d_m128_n4096_k4096" % L] = batched_config(bsg, peaks, L)
+            extras["nvfp4_grouped_8x4096x4096_moe"] = grouped_config(bsg, peaks)
             extras["launch_loop_1000"] = launch_loop(bsg)
             for kind in ("mxfp8", "nvfp4"):
                 for bf in (False, True):

@@ -17,6 +17,7 @@ enum : unsigned {
   F_C = 8u,
   F_ALPHA_ROW = 16u,
   F_ALPHA_COL = 32u,
+  F_GROUPED = 64u,
   F_D32 = 1u << 30  // D (and C) 32-byte aligned: set by the host, not a caller flag
 };
 
@@ -38,7 +39,7 @@ enum : unsigned {
 // parameter space for the TMA instructions).
 struct GemmParams {
   CUtensorMap tmap_a;  // A codes: bytes, dims {K bytes, M, batches}, box {128, 128, 1}, 128-byte swizzle
-  CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N, batches}, box {128, BN, 1}, 128-byte swizzle
+  CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N, b_entries}, box {128, BN, 1}, 128-byte swizzle
   const uint8_t* sfa;  // swizzled 128x4 scale atoms of A
   const uint8_t* sfb;
   const void* bias;    // N values of the output type (flags & F_BIAS)
@@ -61,9 +62,12 @@ struct GemmParams {
   int sfa_bands;           // padded rows / 128 of A
   int num_m_tiles, num_n_tiles, num_k_tiles;
   int num_tiles;           // tiles of all batch entries (the workspace's tile count)
-  int batches;             // L >= 1 problems of this shape, entry b at the strides below
+  int batches;             // entries of A, SFA, D and C: L >= 1 problems of this shape at the strides
+                           // below (1 when grouped)
+  int b_entries;           // entries of B and SFB: L when batched, the G groups when grouped, else 1
+  const int* group_index;  // grouped (F_GROUPED): the group of each of the M rows, -1 = no group
   int units_per_batch;     // num_m_groups * num_n_groups * splits
-  long long sfa_batch, sfb_batch;  // bytes between the scale buffers of consecutive entries
+  long long sfa_batch, sfb_batch;  // bytes between the scale buffers of consecutive entries (groups)
   long long d_batch, c_batch;      // 16-bit elements between consecutive D (C) matrices
   int splits;              // split-K factor (every split owns >= 1 k-tile)
   int split_mode;          // SPLIT_NONE, SPLIT_WORKSPACE or SPLIT_CLUSTER

@@ -95,14 +95,18 @@ struct GemmCfg {
 };
 
 struct UnitCoord {
-  int m_blk, n_blk, split, tile, kt0, kt1, batch;
+  int m_blk, n_blk, split, tile, kt0, kt1;
+  int batch;  // entry of A, SFA, D and C
+  int bsel;   // entry of B, SFB and alpha_dev: the batch entry, or the tile's group when grouped
+  bool skip;  // grouped: the tile has no group (every role passes over it)
 };
 
 // Unit u (a tile, or one split of a tile, of batch entry u / units_per_batch) -> tile
 // coordinates and k range.  With a multicast cluster, u numbers blocks of cmm x cmn tiles and
 // `rank` (the CTA's rank in its cluster, rn + cmn * rm) picks the tile of the block.  `tile` is
-// the tile's index over all entries (the workspace's).  Batch entries exist only in the EXT
-// instantiations; elsewhere c.batch is the constant 0 and every batch offset folds away.
+// the tile's index over all entries (the workspace's).  Batch entries and groups exist only in
+// the EXT instantiations; elsewhere c.batch and c.bsel are the constant 0 and every entry offset
+// folds away.  Grouped (1-SM tiles, no multicast), the tile's group is that of its first row.
 template <bool EXT>
 __device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u, int rank) {
   UnitCoord c;
@@ -125,7 +129,28 @@ __device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u, int
   c.n_blk = (r / gm) * p.cmn + rank % p.cmn;
   c.kt0 = c.split * p.k_tiles_per_split;
   c.kt1 = min(c.kt0 + p.k_tiles_per_split, p.num_k_tiles);
+  c.bsel = c.batch;
+  c.skip = false;
+  if (EXT && p.group_index != nullptr) {
+    const int r0 = c.m_blk * 128;
+    const int grp = r0 < p.M ? __ldg(p.group_index + r0) : -1;
+    c.bsel = grp;
+    c.skip = grp < 0 || grp >= p.b_entries;
+  }
   return c;
+}
+
+// Whether output row m of unit c is stored: inside M and, grouped, in the unit's group.
+template <bool EXT>
+__device__ __forceinline__ bool row_live(const GemmParams& p, const UnitCoord& c, int m) {
+  if (m >= p.M) return false;
+  return !(EXT && p.group_index != nullptr) || __ldg(p.group_index + m) == c.bsel;
+}
+
+// The unit's alpha: the plan's, or (EXT, device alpha with several B entries) its entry's.
+template <bool EXT>
+__device__ __forceinline__ float unit_alpha(const GemmParams& p, const UnitCoord& c, float alpha) {
+  return (EXT && (p.flags & F_ALPHA_DEVICE) && p.b_entries > 1) ? __ldg(p.alpha_dev + c.bsel) : alpha;
 }
 
 // Bounded mbarrier wait.  Gives up when another role flagged an abort, or after the
@@ -315,14 +340,13 @@ __device__ __forceinline__ void load_c16(const GemmParams& p, int b, int m, int 
 
 // A row segment of 16*G accumulator values r (row m, columns n0.., n0 a multiple of 16) through
 // the epilogue into D: the plain path, or (C / per-column factors) the extended one, which loads
-// C one group of 16 columns ahead of the arithmetic.  Rows at or beyond M and columns at or
-// beyond N are not stored.
+// C one group of 16 columns ahead of the arithmetic.  The row is stored only if row_in
+// (row_live), and columns at or beyond N never.
 template <int OUT, int G, bool EXT>
-__device__ __forceinline__ void epilogue_row(const GemmParams& p, int b, int m, int n0, const uint32_t* r,
-                                             float alpha) {
+__device__ __forceinline__ void epilogue_row(const GemmParams& p, int b, int m, bool row_in, int n0,
+                                             const uint32_t* r, float alpha) {
   uint16_t* drow = d_row(p, b, m);
   const bool wide = p.flags & F_D32;
-  const bool row_in = m < p.M;
   if (!EXT || !(p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW))) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -354,9 +378,9 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, int b, int m, 
 
 // Epilogue of 32 consecutive columns n0.. of output row m held by this thread.
 template <int OUT, bool EXT>
-__device__ __forceinline__ void store_chunk32(const GemmParams& p, int b, int m, int n0, const float* v,
-                                              float alpha) {
-  if (m >= p.M) return;
+__device__ __forceinline__ void store_chunk32(const GemmParams& p, int b, int m, bool row_in, int n0,
+                                              const float* v, float alpha) {
+  if (!row_in) return;
   uint16_t* drow = d_row(p, b, m);
   const bool ext = EXT && (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW));
   const float alpha_m = ext ? row_alpha(p, alpha, m) : alpha;
@@ -446,7 +470,7 @@ __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const floa
     // slab row rl holds tile row (rl / LPO) * 32 + split * LPO + rl % LPO, LPO = 32 / S
     const int row = (rl / (32 / S)) * 32 + c.split * (32 / S) + rl % (32 / S);
     const int m = c.m_blk * 128 + row;
-    if (m < p.M && n < p.N)  // N % 16 == 0: groups of 4 are whole
+    if (row_live<EXT>(p, c, m) && n < p.N)  // N % 16 == 0: groups of 4 are whole
       *reinterpret_cast<uint2*>(d_row(p, c.batch, m) + n) =
           epi4_with_bias<OUT, EXT>(p, c.batch, m, n, acc, braw, EXT ? row_alpha(p, alpha, m) : alpha);
   }
@@ -575,6 +599,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         bool first = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
           const UnitCoord c = decode_unit<EXT>(p, u, crank);
+          if (EXT && c.skip) continue;
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
             if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
               ok = false;
@@ -607,14 +632,14 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
                 if (p.cmm > 1) {
                   // likewise a BN/cmm-row slice of the B tile for every CTA that shares the n-tile
                   const int rows = BN / p.cmm;
-                  if (EXT && p.batches > 1)
-                    tma_load_3d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, c.batch,
+                  if (EXT && p.b_entries > 1)
+                    tma_load_3d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, c.bsel,
                                    bmask);
                   else
                     tma_load_2d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, bmask);
                 } else {
-                  if (EXT && p.batches > 1)
-                    tma_load_3d(sb, &p.tmap_b, fb, x, c.n_blk * BN, c.batch);
+                  if (EXT && p.b_entries > 1)
+                    tma_load_3d(sb, &p.tmap_b, fb, x, c.n_blk * BN, c.bsel);
                   else
                     tma_load_2d(sb, &p.tmap_b, fb, x, c.n_blk * BN);
                 }
@@ -652,6 +677,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         bool first = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
           const UnitCoord c = decode_unit<EXT>(p, u, crank);
+          if (EXT && c.skip) continue;
           const int band0 = c.n_blk * BN / 128;    // first scale band of the B tile
           const bool a_band = c.m_blk < p.sfa_bands;  // false only for a cluster's m-tile beyond M
           int bands = 0;
@@ -679,7 +705,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
               for (int rb = 0; rb < C::NB; ++rb) {
                 const int band = band0 + rb;
                 if (band < p.sfb_bands) {
-                  const uint8_t* sb = p.sfb + c.batch * p.sfb_batch + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
+                  const uint8_t* sb = p.sfb + c.bsel * p.sfb_batch + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
                                                static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
                   bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512, sb, sf_atoms * 512, fb);
                 }
@@ -703,6 +729,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         bool ok = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
           const UnitCoord c = decode_unit<EXT>(p, u, crank);
+          if (EXT && c.skip) continue;
           if (!wait_bounded(bar_tempty(acc), acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
             ok = false;
             break;
@@ -785,6 +812,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     bool ok = true;
     for (int u = u0; ok && u < p.num_units; u += ustep) {
       const UnitCoord c = decode_unit<EXT>(p, u, crank);
+      if (EXT && c.skip) continue;
       const int jq = BN < 128 ? (c.n_blk * BN % 128) / 32 : 0;
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
         ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
@@ -832,11 +860,13 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     const int row = q * 32 + lane;       // accumulator row = TMEM lane
     constexpr int HC = BN / 2;           // columns per thread
     const int col0 = ((warp - C::EPI_WARP0) >> 2) * HC;
-    const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
+    const float alpha0 = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = u0; u < p.num_units; u += ustep) {
       const UnitCoord c = decode_unit<EXT>(p, u, crank);
+      if (EXT && c.skip) continue;
+      const float alpha = unit_alpha<EXT>(p, c, alpha0);
       bool ok = wait_bounded(bar_tfull(acc), acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
       ok = named_bar_and(1, C::EPI_THREADS, ok);
       if (!ok) break;
@@ -844,6 +874,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
       const int m = c.m_blk * C::BM + row;
+      const bool row_in = row_live<EXT>(p, c, m);
       const int nbase = c.n_blk * BN;
       if (p.split_mode == SPLIT_NONE) {
         uint16_t* drow = d_row(p, c.batch, m);
@@ -858,7 +889,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_tempty(acc));
-          epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, nbase + col0, r, alpha);
+          epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, row_in, nbase + col0, r, alpha);
         } else {
           // Two accumulators: the next tile's MMAs run in the other one, so the segment is
           // rounded chunk by chunk (fewer live registers) and released before the stores.
@@ -881,7 +912,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
               for (int h = 0; h < W / 16; ++h) {
                 const int n = nbase + col0 + ch * 32 + 16 * h;
                 uint32_t cw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if ((p.flags & F_C) && m < p.M && n < p.N) load_c16(p, c.batch, m, n, (p.flags & F_D32) != 0, cw);
+                if ((p.flags & F_C) && row_in && n < p.N) load_c16(p, c.batch, m, n, (p.flags & F_D32) != 0, cw);
                 epi_pack_ext<OUT, 8>(p, n, reinterpret_cast<const float*>(&r[16 * h]), alpha_m, cw,
                                      &packed[ch * 16 + 8 * h]);
                 epi_pack_ext<OUT, 8>(p, n + 8, reinterpret_cast<const float*>(&r[16 * h + 8]), alpha_m, cw + 4,
@@ -906,7 +937,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
 #pragma unroll
           for (int g = 0; g < HC / 16; ++g) {
             const int n = nbase + col0 + 16 * g;
-            if (m < p.M && n < p.N) st_out16(drow + n, reinterpret_cast<const uint32_t(&)[8]>(packed[8 * g]), wide);
+            if (row_in && n < p.N) st_out16(drow + n, reinterpret_cast<const uint32_t(&)[8]>(packed[8 * g]), wide);
           }
         }
       } else if constexpr (BN >= 64) {  // split-K is planned for tiles 64 columns wide or more
@@ -1021,7 +1052,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
                   v[4 * g + 3] += t.w;
                 }
               }
-              store_chunk32<OUT, EXT>(p, c.batch, m, nbase + ch * 32, v, alpha);
+              store_chunk32<OUT, EXT>(p, c.batch, m, row_in, nbase + ch * 32, v, alpha);
             }
           }
           named_bar_sync(1, C::EPI_THREADS);

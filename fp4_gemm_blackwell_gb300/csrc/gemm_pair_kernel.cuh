@@ -181,13 +181,14 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
               for (int j = 0; j < KC; ++j) {  // slabs past K read as zeros (their MMAs are skipped)
                 const int x = (kt * KC + j) * C::BK_BYTES;
                 const int yb = c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128;
-                if (EXT && p.batches > 1) {
+                if (EXT && p.batches > 1)
                   tma_load_3d_pair(stage_a(stage) + j * C::SLAB_A, &p.tmap_a, fb, x, m_blk * C::BM, c.batch);
-                  tma_load_3d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x, yb, c.batch);
-                } else {
+                else
                   tma_load_2d_pair(stage_a(stage) + j * C::SLAB_A, &p.tmap_a, fb, x, m_blk * C::BM);
+                if (EXT && p.b_entries > 1)
+                  tma_load_3d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x, yb, c.bsel);
+                else
                   tma_load_2d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x, yb);
-                }
               }
             }
             first = false;
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
                 const int band = c.n_blk * 2 + rb;
                 if (band < p.sfb_bands)
                   bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512,
-                            p.sfb + c.batch * p.sfb_batch + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
+                            p.sfb + c.bsel * p.sfb_batch + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
                                      static_cast<size_t>(kt) * C::SF_ATOMS) * 512,
                             sf_atoms * 512, sb);
               }
@@ -426,11 +427,12 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     const int row = q * 32 + lane;
     constexpr int HC = C::BN / 2;
     const int col0 = ((warp - C::EPI_WARP0) >> 2) * HC;
-    const float alpha = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
+    const float alpha0 = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
     const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
     uint32_t acc_phase = 0;
     for (int u = pair0; u < p.num_units; u += pairs) {
       const UnitCoord c = decode_unit<EXT>(p, u, 0);
+      const float alpha = unit_alpha<EXT>(p, c, alpha0);
       bool ok = wait_bounded_cluster(bar_tfull, acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
       ok = named_bar_and(1, C::EPI_THREADS, ok);
       if (!ok) break;
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         else
           tc_commit_pair_mc(bar_tempty, leader_mask);
       }
-      epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, nbase + col0, r, alpha);
+      epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, m < p.M, nbase + col0, r, alpha);
       acc_phase ^= 1u;
     }
   }

@@ -130,7 +130,8 @@ bsg_status validate_desc(const bsg_desc* d) {
   if (d->kind != BSG_MXFP8 && d->kind != BSG_NVFP4) return fail(BSG_ERR_INVALID_ARG, "unknown kind %d", d->kind);
   if (d->out != BSG_OUT_F16 && d->out != BSG_OUT_BF16)
     return fail(BSG_ERR_DTYPE, "unsupported output type %d (FP16 or BF16 only)", d->out);
-  if (d->flags & ~(BSG_F_BIAS | BSG_F_SILU | BSG_F_ALPHA_DEVICE | BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL))
+  if (d->flags &
+      ~(BSG_F_BIAS | BSG_F_SILU | BSG_F_ALPHA_DEVICE | BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL | BSG_F_GROUPED))
     return fail(BSG_ERR_INVALID_ARG, "unknown flag bits 0x%x", d->flags);
   if (d->M < 1 || d->N < 16 || d->K < 32 || d->M > kMaxDim || d->N > kMaxDim || d->K > kMaxDim)
     return fail(BSG_ERR_SHAPE, "shape M=%d N=%d K=%d out of range (M>=1, N>=16, K>=32, each <= 2^20)",
@@ -138,19 +139,29 @@ bsg_status validate_desc(const bsg_desc* d) {
   if (d->N % 16) return fail(BSG_ERR_SHAPE, "N=%d is not a multiple of 16", d->N);
   if (d->K % 32) return fail(BSG_ERR_SHAPE, "K=%d is not a multiple of 32", d->K);
   if (d->L < 0 || d->L > 65535) return fail(BSG_ERR_SHAPE, "L=%d out of range (0..65535)", d->L);
+  const bool grouped = (d->flags & BSG_F_GROUPED) != 0;
+  if (grouped) {
+    if (d->L < 1) return fail(BSG_ERR_SHAPE, "GROUPED needs L >= 1 groups");
+    if (!d->group_index) return fail(BSG_ERR_INVALID_ARG, "GROUPED set but group_index is null");
+    if (reinterpret_cast<uintptr_t>(d->group_index) & 3u)
+      return fail(BSG_ERR_ALIGNMENT, "group_index must be 4-byte aligned");
+  }
   if (d->L > 1) {
+    // batched: every operand has L entries; grouped: B and SFB have one per group
     const long long rb = static_cast<long long>(code_row_bytes(d->kind, d->K));
+    const long long dm = 2LL * d->M * d->N;
     const struct {
       long long stride, need;
       const char* name;
-    } st[] = {{d->stride_A, rb * d->M, "stride_A"},
-              {d->stride_B, rb * d->N, "stride_B"},
-              {d->stride_SFA, static_cast<long long>(sf_bytes_of(d->kind, d->M, d->K)), "stride_SFA"},
-              {d->stride_SFB, static_cast<long long>(sf_bytes_of(d->kind, d->N, d->K)), "stride_SFB"},
-              {d->stride_D, 2LL * d->M * d->N, "stride_D"},
-              {(d->flags & BSG_F_C) ? d->stride_C : 2LL * d->M * d->N, 2LL * d->M * d->N, "stride_C"}};
+      bool used;
+    } st[] = {{d->stride_A, rb * d->M, "stride_A", !grouped},
+              {d->stride_B, rb * d->N, "stride_B", true},
+              {d->stride_SFA, static_cast<long long>(sf_bytes_of(d->kind, d->M, d->K)), "stride_SFA", !grouped},
+              {d->stride_SFB, static_cast<long long>(sf_bytes_of(d->kind, d->N, d->K)), "stride_SFB", true},
+              {d->stride_D, dm, "stride_D", !grouped},
+              {d->stride_C, dm, "stride_C", !grouped && (d->flags & BSG_F_C)}};
     for (const auto& x : st)
-      if (x.stride % 16 || x.stride < x.need)
+      if (x.used && (x.stride % 16 || x.stride < x.need))
         return fail(BSG_ERR_SHAPE, "%s=%lld must be a multiple of 16 and at least one entry (%lld bytes)", x.name,
                     x.stride, x.need);
   }
@@ -177,26 +188,34 @@ bsg_status validate_desc(const bsg_desc* d) {
 
 bsg_status validate_ranges(const bsg_desc* d) {
   const size_t rb = code_row_bytes(d->kind, d->K);
-  // bytes of L entries at `stride`, one entry being `one` bytes
+  const bool grouped = (d->flags & BSG_F_GROUPED) != 0;
+  // bytes of L entries at `stride`, one entry being `one` bytes (A, SFA, D and C have one entry
+  // when grouped)
   const size_t L1 = d->L > 1 ? static_cast<size_t>(d->L - 1) : 0;
   auto span = [&](long long stride, size_t one) { return L1 * static_cast<size_t>(stride) + one; };
+  auto span_a = [&](long long stride, size_t one) { return grouped ? one : span(stride, one); };
   bsg_status s;
-  if ((s = check_range(d->A, span(d->stride_A, rb * d->M), BSG_ERR_SHAPE, "A")) != BSG_OK) return s;
+  if ((s = check_range(d->A, span_a(d->stride_A, rb * d->M), BSG_ERR_SHAPE, "A")) != BSG_OK) return s;
   if ((s = check_range(d->B, span(d->stride_B, rb * d->N), BSG_ERR_SHAPE, "B")) != BSG_OK) return s;
-  if ((s = check_range(d->SFA, span(d->stride_SFA, sf_bytes_of(d->kind, d->M, d->K)), BSG_ERR_SCALE_LAYOUT, "SFA")) !=
-      BSG_OK)
+  if ((s = check_range(d->SFA, span_a(d->stride_SFA, sf_bytes_of(d->kind, d->M, d->K)), BSG_ERR_SCALE_LAYOUT,
+                       "SFA")) != BSG_OK)
     return s;
   if ((s = check_range(d->SFB, span(d->stride_SFB, sf_bytes_of(d->kind, d->N, d->K)), BSG_ERR_SCALE_LAYOUT, "SFB")) !=
       BSG_OK)
     return s;
-  if ((s = check_range(d->D, span(d->stride_D, static_cast<size_t>(d->M) * d->N * 2), BSG_ERR_SHAPE, "D")) != BSG_OK)
+  if ((s = check_range(d->D, span_a(d->stride_D, static_cast<size_t>(d->M) * d->N * 2), BSG_ERR_SHAPE, "D")) != BSG_OK)
     return s;
   if ((d->flags & BSG_F_BIAS) && (s = check_range(d->bias, static_cast<size_t>(d->N) * 2, BSG_ERR_SHAPE, "bias")) != BSG_OK)
     return s;
-  if ((d->flags & BSG_F_ALPHA_DEVICE) && (s = check_range(d->alpha_dev, 4, BSG_ERR_SHAPE, "alpha_dev")) != BSG_OK)
+  // one alpha per entry (group) when there are several, else one
+  if ((d->flags & BSG_F_ALPHA_DEVICE) &&
+      (s = check_range(d->alpha_dev, 4 * (L1 + 1), BSG_ERR_SHAPE, "alpha_dev")) != BSG_OK)
     return s;
   if ((d->flags & BSG_F_C) &&
-      (s = check_range(d->C, span(d->stride_C, static_cast<size_t>(d->M) * d->N * 2), BSG_ERR_SHAPE, "C")) != BSG_OK)
+      (s = check_range(d->C, span_a(d->stride_C, static_cast<size_t>(d->M) * d->N * 2), BSG_ERR_SHAPE, "C")) != BSG_OK)
+    return s;
+  if (grouped &&
+      (s = check_range(d->group_index, static_cast<size_t>(d->M) * 4, BSG_ERR_SHAPE, "group_index")) != BSG_OK)
     return s;
   if ((d->flags & BSG_F_ALPHA_ROW) &&
       (s = check_range(d->alpha_row, static_cast<size_t>(d->M) * 4, BSG_ERR_SHAPE, "alpha_row")) != BSG_OK)
@@ -304,13 +323,15 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
   const int nkt = (d->K + k_tile - 1) / k_tile;
   const long long mt = (d->M + 127) / 128;
-  const long long L = d->L > 1 ? d->L : 1;  // tiles of all batch entries compete for the SMs
+  // tiles of all batch entries compete for the SMs; grouped rows are all in M already
+  const bool grouped = (d->flags & BSG_F_GROUPED) != 0;
+  const long long L = d->L > 1 && !grouped ? d->L : 1;
   const long long t256 = mt * ((d->N + 255) / 256) * L;
   const long long t128 = mt * ((d->N + 127) / 128) * L;
   const long long pair_tiles = ((d->M + 255) / 256) * ((d->N + 255) / 256) * L;
   int b, s = 1;
   bool pair = false;
-  if (d->M > 256 && 4 * pair_tiles >= sms) {
+  if (d->M > 256 && 4 * pair_tiles >= sms && !grouped) {
     pair = true;
     b = 256;
   } else if (t256 >= sms) {
@@ -367,6 +388,7 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   v.pair = pair && env_int("BSG_FORCE_SPLITS", 0) == 0;
   const int fp = env_int("BSG_FORCE_PAIR", -1);
   if (fp == 0 || fp == 1) v.pair = fp == 1;
+  if (grouped) v.pair = false;  // a 256-row pair tile could span two groups
   if (v.pair) {
     v.bn = 256;
     v.kc = 1;
@@ -386,7 +408,7 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   if (fc == 1 || fc == 2 || fc == 4 || fc == 8) cmn = fc;
   const int fm = env_int("BSG_FORCE_CMM", 0);
   if (fm == 1 || fm == 2 || fm == 4 || fm == 8) cmm = fm;
-  if (s > 1) cmn = cmm = 1;
+  if (s > 1 || grouped) cmn = cmm = 1;  // grouped: the m-tiles sharing a B tile could differ in group
   const long long nt = (d->N + b - 1) / b;
   while (cmn > 1 && cmn > nt) cmn /= 2;
   while (cmm > 1 && cmm > mt) cmm /= 2;
@@ -447,15 +469,19 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   std::memset(g, 0, sizeof(*g));
   const size_t rb = code_row_bytes(d->kind, d->K);
   bsg_status s;
-  const int L = d->L > 1 ? d->L : 1;
+  const bool grouped = (d->flags & BSG_F_GROUPED) != 0;
+  const int LB = d->L > 1 ? d->L : 1;  // entries of B and SFB (batch entries or groups)
+  const int L = grouped ? 1 : LB;      // entries of A, SFA, D and C
   if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, static_cast<uint32_t>(128 / v.cmn), L, d->stride_A, "A")) !=
           BSG_OK ||
-      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn / v.cmm), L,
+      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn / v.cmm), LB,
                           d->stride_B, "B")) != BSG_OK)
     return s;
   g->batches = L;
+  g->b_entries = LB;
+  g->group_index = grouped ? d->group_index : nullptr;
   g->sfa_batch = L > 1 ? d->stride_SFA : 0;
-  g->sfb_batch = L > 1 ? d->stride_SFB : 0;
+  g->sfb_batch = LB > 1 ? d->stride_SFB : 0;
   g->d_batch = L > 1 ? d->stride_D / 2 : 0;
   g->c_batch = (L > 1 && (d->flags & BSG_F_C)) ? d->stride_C / 2 : 0;
   const int k_tile = d->kind == BSG_MXFP8 ? 128 : 256;
@@ -561,7 +587,7 @@ bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, 
 
 namespace bsg {
 bool find_kernel(int kind, int out, unsigned flags, int batches, bool pair, int bn, int kc, GemmKernelInfo* info) {
-  const bool ext = (flags & (BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL)) != 0 || batches > 1;
+  const bool ext = (flags & (BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL | BSG_F_GROUPED)) != 0 || batches > 1;
   if (pair) {
     if (kind == KIND_MX) return ext ? gemm_pair_kernel_info_mx_ext(out, info) : gemm_pair_kernel_info_mx(out, info);
     return ext ? gemm_pair_kernel_info_nv_ext(out, info) : gemm_pair_kernel_info_nv(out, info);
@@ -922,7 +948,8 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
   const bool found = bsg::find_kernel(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, d->flags, d->L,
                                       v.pair, v.bn, v.kc, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
-  const int num_tiles = ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn) * (d->L > 1 ? d->L : 1);
+  const int num_tiles =
+      ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn) * (d->L > 1 && !(d->flags & BSG_F_GROUPED) ? d->L : 1);
   const WorkspaceLayout w = workspace_layout(v, num_tiles);
   if (w.total > kNoAllocScratchBytes)
     return fail(BSG_ERR_SHAPE,

@@ -72,14 +72,16 @@ typedef enum { BSG_OUT_F16 = 0, BSG_OUT_BF16 = 1 } bsg_out;
  * fusion_args.alpha_ptr of the MXFP8 page.  C adds beta * C[m,n] from a separate matrix
  * (the MXFP8 page's LinearCombination epilogue with its C operand, there aliased to D);
  * ALPHA_ROW / ALPHA_COL multiply alpha by alpha_row[m] / alpha_col[n] (per-row and
- * per-column factors, e.g. per-token and per-channel global scales). */
+ * per-column factors, e.g. per-token and per-channel global scales).  GROUPED makes the
+ * problem a grouped GEMM (see bsg_desc). */
 enum {
   BSG_F_BIAS = 1u,
   BSG_F_SILU = 2u,
   BSG_F_ALPHA_DEVICE = 4u,
   BSG_F_C = 8u,
   BSG_F_ALPHA_ROW = 16u,
-  BSG_F_ALPHA_COL = 32u
+  BSG_F_ALPHA_COL = 32u,
+  BSG_F_GROUPED = 64u
 };
 
 typedef struct bsg_plan_s* bsg_plan_t;
@@ -99,7 +101,20 @@ typedef struct bsg_plan_s* bsg_plan_t;
  * of this shape in one launch, entry l at A + l*stride_A, B + l*stride_B, SFA + l*stride_SFA,
  * SFB + l*stride_SFB, D + l*stride_D and (with C) C + l*stride_C (strides in bytes, multiples
  * of 16, each at least one entry's size); bias, alpha, alpha_row and alpha_col are shared by all
- * entries.  L = 0 or 1 is one problem (the strides are then ignored); L <= 65535. */
+ * entries, and with BSG_F_ALPHA_DEVICE alpha_dev holds one alpha per entry.  L = 0 or 1 is one
+ * problem (the strides are then ignored); L <= 65535.
+ * Grouped (BSG_F_GROUPED; a mixture-of-experts layer's expert GEMMs): L >= 1 groups share
+ * N and K; group g has its own B (B + g*stride_B, SFB + g*stride_SFB) and, with
+ * BSG_F_ALPHA_DEVICE, alpha_dev[g].  A, SFA, D and C hold the rows of every group: the M
+ * rows of one matrix each, and group_index (M int32, device memory, read when the kernel
+ * runs, so a preceding kernel may write it) gives each row's group, or -1 for a row that
+ * belongs to none (not computed into D, D left as it was).  Each 128-row block of rows
+ * (rows 128t .. 128t+127) must hold rows of at most one group plus rows of none; the group
+ * of a block is that of its first row.  A block whose first row has no group (or a group
+ * outside 0..L-1) is skipped whole, and a row whose group differs from its block's is not
+ * stored.  So each group's rows start on a multiple of 128 and are padded with -1 rows to the
+ * next one.  stride_A, stride_SFA, stride_D and stride_C are ignored.  Grouped problems run on
+ * 128-row tiles (no CTA pairs). */
 typedef struct {
   bsg_kind kind;
   bsg_out out;
@@ -119,6 +134,7 @@ typedef struct {
   const float* alpha_col;
   int L;
   long long stride_A, stride_B, stride_SFA, stride_SFB, stride_D, stride_C;
+  const int* group_index;
 } bsg_desc;
 
 /* Validate d, choose the kernel variant (tile shape, split-K), encode the TMA tensor

@@ -54,11 +54,12 @@ def test_version_and_sf_bytes(L):
 def _plan_status(L, **kw):
     base = dict(kind=0, out=1, flags=0, M=128, N=128, K=128, A=16, B=32, SFA=48, SFB=64, bias=None,
                 D=80, alpha=1.0, alpha_dev=None, C=None, beta=0.0, alpha_row=None, alpha_col=None, batches=0,
-                strides=(0, 0, 0, 0, 0, 0))
+                strides=(0, 0, 0, 0, 0, 0), group_index=None)
     base.update(kw)
     d = bsg.BsgDesc(base["kind"], base["out"], base["flags"], base["M"], base["N"], base["K"], base["A"],
                     base["B"], base["SFA"], base["SFB"], base["bias"], base["D"], base["alpha"], base["alpha_dev"],
-                    base["C"], base["beta"], base["alpha_row"], base["alpha_col"], base["batches"], *base["strides"])
+                    base["C"], base["beta"], base["alpha_row"], base["alpha_col"], base["batches"], *base["strides"],
+                    base["group_index"])
     h = ctypes.c_void_p()
     st = L.bsg_plan_create(ctypes.byref(h), ctypes.byref(d))
     assert h.value is None
@@ -70,13 +71,17 @@ def _plan_status(L, **kw):
     (dict(M=0), 2), (dict(N=8), 2), (dict(N=120), 2), (dict(K=48), 2), (dict(K=16), 2),
     (dict(M=1 << 21), 2), (dict(A=None), 1), (dict(D=None), 1), (dict(flags=1), 1),
     (dict(flags=4), 1), (dict(A=24), 3), (dict(SFB=72), 3), (dict(flags=1, bias=88), 3),
-    (dict(flags=64), 1), (dict(flags=8, C=104), 3), (dict(flags=16), 1), (dict(flags=32), 1),
+    (dict(flags=128), 1), (dict(flags=8, C=104), 3), (dict(flags=16), 1), (dict(flags=32), 1),
     (dict(flags=16, alpha_row=130), 3), (dict(flags=32, alpha_col=6), 3),
     # batched: L out of range; a stride below one entry; a stride not a multiple of 16
     (dict(batches=-1), 2), (dict(batches=70000), 2),
     (dict(batches=2, strides=(0, 16384, 2048, 2048, 32768, 0)), 2),
     (dict(batches=2, strides=(16384 + 8, 16384, 2048, 2048, 32768, 0)), 2),
     (dict(batches=2, strides=(16384, 16384, 2048, 2048, 32768 - 16, 0)), 2),
+    # grouped: no groups; no group_index; a misaligned group_index; a B stride below one expert
+    (dict(flags=64), 2), (dict(flags=64, batches=4), 1), (dict(flags=64, batches=4, group_index=6), 3),
+    (dict(flags=64, batches=4, group_index=256, strides=(0, 16384 - 16, 0, 2048, 0, 0)), 2),
+    (dict(flags=64, batches=4, group_index=256, strides=(0, 16384, 0, 512 - 16, 0, 0)), 2),
 ])
 def test_invalid_descriptors_are_rejected_before_device_work(L, kw, status):
     assert _plan_status(L, **kw) == status

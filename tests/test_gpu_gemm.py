@@ -364,3 +364,93 @@ def test_batched(kind, env, monkeypatch):
         P.assert_parity(got, q, "bf16", bias_vals, kind == "nvfp4", epi=epi)
         gap = dall[l * sD + M * N:(l + 1) * sD] if l + 1 < L else dall[l * sD + M * N:]
         assert np.all(gap == 0x7BAD), "wrote past entry %d (%s)" % (l, variant)
+
+
+def _grouped_layout(sizes, tail):
+    """Rows of groups of the given sizes, each starting on a multiple of 128 and padded with -1
+    rows to the next one, then `tail` rows of no group.  Returns (group_index, rows of each group)."""
+    idx, rows, at = [], [], 0
+    for g, n in enumerate(sizes):
+        pad = -n % 128
+        rows.append(list(range(at, at + n)))
+        idx += [g] * n + [-1] * pad
+        at += n + pad
+    idx += [-1] * tail
+    return np.array(idx, dtype=np.int32), rows
+
+
+@pytest.mark.parametrize("env", [{}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 128}, {"BSG_FORCE_BN": 32},
+                                 {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2},
+                                 {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3},
+                                 {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_CM": 4}])
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_grouped(kind, env, monkeypatch):
+    # Grouped GEMM (expert GEMMs of a mixture-of-experts layer): 4 groups of 200, 0, 37 and 128
+    # rows with their own B and alpha, in the 128-row-aligned layout; then a block whose first
+    # row names group 99 (skipped whole) and a ragged tail of no group.  One row inside group
+    # 3's block is marked group 2: it is not stored.  Each group against its own oracle result;
+    # every row of no stored group keeps the canary.  A forced CTA pair or multicast cluster
+    # must not apply to a grouped problem.
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    G, N, K = 4, 144, 1536
+    gidx, grows = _grouped_layout([200, 0, 37, 128], tail=0)
+    stray = grows[3][5]
+    gidx[stray] = 2
+    grows[3].remove(stray)
+    skip_block = np.zeros(128, dtype=np.int32)
+    skip_block[0] = 99
+    gidx = np.concatenate([gidx, skip_block, np.full(60, -1, dtype=np.int32)])
+    M = len(gidx)
+    gen = synth.normal_rowscaled if kind == "nvfp4" else synth.normal
+    a, sfa, sa = P.oracle_operand(kind, gen(M, K, 31))
+    bs = [P.oracle_operand(kind, gen(N, K, 40 + g)) for g in range(G)]
+    if kind == "nvfp4":
+        alphas = [np.float32(np.float32(sa) * np.float32(s)) for _, _, s in bs]
+    else:
+        alphas = [np.float32(x) for x in (1.0, 0.5, 2.0, 0.25)]
+
+    def pack(arrs, pad=256):
+        one = max(x.size for x in arrs)
+        stride = (one + pad + 15) // 16 * 16
+        buf = np.full(G * stride, 0x5A, dtype=np.uint8)
+        for g, x in enumerate(arrs):
+            buf[g * stride:g * stride + x.size] = np.ascontiguousarray(x).view(np.uint8).ravel()
+        return P.dev(buf), stride
+
+    B, sB = pack([b for b, _, _ in bs])
+    SFB, sSFB = pack([f for _, f, _ in bs])
+    A, SFA = P.dev(a), P.dev(sfa)
+    alpha_dev = torch.tensor(np.array(alphas, dtype=np.float32), device="cuda")
+    gi = torch.from_numpy(gidx).cuda()
+    D = torch.full((M * N,), 0x7BAD, dtype=torch.int16, device="cuda")
+    residual = "BSG_FORCE_SPLITS" in env
+    C = Cvals = None
+    if residual:
+        cbits, Cvals = P.synth_residual(M, N, "bf16", seed=77)
+        C = P.dev(cbits.view(np.int16)).view(torch.int16)
+    bias_bits, bias_vals = synth.bias(N, out="bf16")
+    bias = P.dev(bias_bits.view(np.int16)).view(torch.int16)
+    silu = kind == "nvfp4"
+    flags = (bsg.BSG_F_GROUPED | bsg.BSG_F_ALPHA_DEVICE | bsg.BSG_F_BIAS | (bsg.BSG_F_SILU if silu else 0) |
+             (bsg.BSG_F_C if residual else 0))
+    with bsg.Plan(P.KIND[kind], P.OUT["bf16"], M, N, K, A, B, SFA, SFB, D, flags=flags, bias=bias,
+                  alpha_dev=alpha_dev, C=C, beta=0.75, L=G, strides=dict(stride_B=sB, stride_SFB=sSFB),
+                  group_index=gi) as plan:
+        variant = plan.variant
+        plan.run()
+        plan.check_status()
+    torch.cuda.synchronize()
+    assert "pair" not in variant, variant
+    bits = D.cpu().numpy().view(np.uint16).reshape(M, N)
+    got = R.out_from_bits(bits, "bf16")
+    stored = np.zeros(M, dtype=bool)
+    for g in range(G):
+        if not grows[g]:
+            continue
+        b, sfb, _ = bs[g]
+        prob = dict(kind=kind, M=M, N=N, K=K, A=a, B=b, SFA=sfa, SFB=sfb, alpha=alphas[g])
+        epi = dict(C=Cvals, beta=0.75) if residual else None
+        P.assert_parity(got, prob, "bf16", bias_vals, silu, rows=grows[g], epi=epi)
+        stored[grows[g]] = True
+    assert np.all(bits[~stored] == 0x7BAD), "rows of no stored group were written (%s)" % variant
