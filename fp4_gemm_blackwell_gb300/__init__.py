@@ -13,7 +13,7 @@ import os
 __all__ = [
     "BSG_MXFP8", "BSG_NVFP4", "BSG_OUT_F16", "BSG_OUT_BF16", "BSG_F_BIAS", "BSG_F_SILU",
     "BSG_F_ALPHA_DEVICE", "BSG_F_C", "BSG_F_ALPHA_ROW", "BSG_F_ALPHA_COL", "BSG_F_GROUPED", "BsgError", "lib", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_plan_create",
-    "bsg_plan_run", "bsg_plan_destroy", "bsg_plan_check_status", "bsg_plan_variant",
+    "bsg_plan_run", "bsg_plan_run_operands", "bsg_plan_destroy", "bsg_plan_check_status", "bsg_plan_variant",
     "bsg_plan_debug_set", "mxfp8_gemm", "nvfp4_gemm", "bsg_cache_clear", "bsg_last_error",
     "bsg_version", "Plan", "bsg_gemm_noalloc",
 ]
@@ -54,6 +54,11 @@ class BsgDesc(ctypes.Structure):
     ]
 
 
+class BsgOperands(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in
+                ("A", "B", "SFA", "SFB", "D", "bias", "alpha_dev", "C", "alpha_row", "alpha_col", "group_index")]
+
+
 _lib = None
 
 
@@ -70,6 +75,7 @@ def lib():
     sig = {
         "bsg_plan_create": (st, [ctypes.POINTER(vp), ctypes.POINTER(BsgDesc)]),
         "bsg_plan_run": (st, [vp, vp]),
+        "bsg_plan_run_operands": (st, [vp, ctypes.POINTER(BsgOperands), vp]),
         "bsg_plan_destroy": (st, [vp]),
         "bsg_plan_check_status": (st, [vp]),
         "bsg_plan_variant": (ctypes.c_char_p, [vp]),
@@ -156,6 +162,13 @@ def bsg_plan_run(plan, stream=None):
     _check(lib().bsg_plan_run(plan, _stream(stream)))
 
 
+def bsg_plan_run_operands(plan, A, B, SFA, SFB, D, bias=None, alpha_dev=None, C=None, alpha_row=None,
+                          alpha_col=None, group_index=None, stream=None):
+    ops = BsgOperands(*(_ptr(x) for x in (A, B, SFA, SFB, D, bias, alpha_dev, C, alpha_row, alpha_col,
+                                          group_index)))
+    _check(lib().bsg_plan_run_operands(plan, ctypes.byref(ops), _stream(stream)))
+
+
 def bsg_plan_destroy(plan):
     _check(lib().bsg_plan_destroy(plan))
 
@@ -202,6 +215,9 @@ class Plan:
 
     def run(self, stream=None):
         bsg_plan_run(self.handle, stream)
+
+    def run_operands(self, *args, **kwargs):
+        bsg_plan_run_operands(self.handle, *args, **kwargs)
 
     def check_status(self):
         bsg_plan_check_status(self.handle)

@@ -66,6 +66,12 @@ struct GemmParams {
                            // below (1 when grouped)
   int b_entries;           // entries of B and SFB: L when batched, the G groups when grouped, else 1
   const int* group_index;  // grouped (F_GROUPED): the group of each of the M rows, -1 = no group
+  // Pointer-agnostic runs (EXT instantiations): when map_slots is set, each CTA's code producer
+  // copies tmap_a / tmap_b into its two 128-byte global slots (map_slots + 2 * blockIdx.x),
+  // replaces their global addresses by remap_a / remap_b and loads through the copies.
+  CUtensorMap* map_slots;
+  const void* remap_a;
+  const void* remap_b;
   int units_per_batch;     // num_m_groups * num_n_groups * splits
   long long sfa_batch, sfb_batch;  // bytes between the scale buffers of consecutive entries (groups)
   long long d_batch, c_batch;      // 16-bit elements between consecutive D (C) matrices
@@ -120,6 +126,8 @@ bool gemm_pair_kernel_info_nv_ext(int out, GemmKernelInfo* info);
 // The kernel of variant (pair, bn, kc) for a problem's format, output type, epilogue flags and
 // batch count.
 bool find_kernel(int kind, int out, unsigned flags, int batches, bool pair, int bn, int kc, GemmKernelInfo* info);
+// The same with the instantiation named: EXT (ext) or plain.
+bool find_kernel_variant(int kind, int out, bool ext, bool pair, int bn, int kc, GemmKernelInfo* info);
 
 // Quantisers (stream-ordered).  See bsg_quantize / bsg_quantize_bf16 in include/bsgemm.h; the
 // uint16_t forms read BF16 bit patterns.

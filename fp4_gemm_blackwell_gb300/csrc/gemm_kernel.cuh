@@ -593,6 +593,15 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer: code tiles
       if (lane == 0) {
+        const CUtensorMap* tma = &p.tmap_a;
+        const CUtensorMap* tmb = &p.tmap_b;
+        if (EXT && p.map_slots != nullptr) {  // pointer-agnostic run: this CTA's own copies
+          CUtensorMap* slot = p.map_slots + 2 * blockIdx.x;
+          tmap_remap(slot, &p.tmap_a, p.remap_a);
+          tmap_remap(slot + 1, &p.tmap_b, p.remap_b);
+          tma = slot;
+          tmb = slot + 1;
+        }
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -619,29 +628,29 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
                   // into the same stage of every CTA that shares the m-tile
                   const int rows = C::BM / p.cmn;
                   if (EXT && p.batches > 1)
-                    tma_load_3d_mc(sa + rn * rows * C::BK_BYTES, &p.tmap_a, fb, x, c.m_blk * C::BM + rn * rows, c.batch,
+                    tma_load_3d_mc(sa + rn * rows * C::BK_BYTES, tma, fb, x, c.m_blk * C::BM + rn * rows, c.batch,
                                    amask);
                   else
-                    tma_load_2d_mc(sa + rn * rows * C::BK_BYTES, &p.tmap_a, fb, x, c.m_blk * C::BM + rn * rows, amask);
+                    tma_load_2d_mc(sa + rn * rows * C::BK_BYTES, tma, fb, x, c.m_blk * C::BM + rn * rows, amask);
                 } else {
                   if (EXT && p.batches > 1)
-                    tma_load_3d(sa, &p.tmap_a, fb, x, c.m_blk * C::BM, c.batch);
+                    tma_load_3d(sa, tma, fb, x, c.m_blk * C::BM, c.batch);
                   else
-                    tma_load_2d(sa, &p.tmap_a, fb, x, c.m_blk * C::BM);
+                    tma_load_2d(sa, tma, fb, x, c.m_blk * C::BM);
                 }
                 if (p.cmm > 1) {
                   // likewise a BN/cmm-row slice of the B tile for every CTA that shares the n-tile
                   const int rows = BN / p.cmm;
                   if (EXT && p.b_entries > 1)
-                    tma_load_3d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, c.bsel,
+                    tma_load_3d_mc(sb + rm * rows * C::BK_BYTES, tmb, fb, x, c.n_blk * BN + rm * rows, c.bsel,
                                    bmask);
                   else
-                    tma_load_2d_mc(sb + rm * rows * C::BK_BYTES, &p.tmap_b, fb, x, c.n_blk * BN + rm * rows, bmask);
+                    tma_load_2d_mc(sb + rm * rows * C::BK_BYTES, tmb, fb, x, c.n_blk * BN + rm * rows, bmask);
                 } else {
                   if (EXT && p.b_entries > 1)
-                    tma_load_3d(sb, &p.tmap_b, fb, x, c.n_blk * BN, c.bsel);
+                    tma_load_3d(sb, tmb, fb, x, c.n_blk * BN, c.bsel);
                   else
-                    tma_load_2d(sb, &p.tmap_b, fb, x, c.n_blk * BN);
+                    tma_load_2d(sb, tmb, fb, x, c.n_blk * BN);
                 }
               }
             }

@@ -81,6 +81,8 @@ struct PairCfg {
   static_assert(TMEM_USED <= TMEM_COLS, "tensor memory");
 };
 
+// Grouped problems never run here (a 256-row pair tile could span two groups); the host plans
+// them on 1-SM tiles.
 template <int KIND, int KC, int OUT, bool EXT>
 __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   using C = PairCfg<KIND, KC>;
@@ -159,6 +161,15 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer (each CTA)
       if (lane == 0) {
+        const CUtensorMap* tma = &p.tmap_a;
+        const CUtensorMap* tmb = &p.tmap_b;
+        if (EXT && p.map_slots != nullptr) {  // pointer-agnostic run: this CTA's own copies
+          CUtensorMap* slot = p.map_slots + 2 * blockIdx.x;
+          tmap_remap(slot, &p.tmap_a, p.remap_a);
+          tmap_remap(slot + 1, &p.tmap_b, p.remap_b);
+          tma = slot;
+          tmb = slot + 1;
+        }
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -182,13 +193,13 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
                 const int x = (kt * KC + j) * C::BK_BYTES;
                 const int yb = c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128;
                 if (EXT && p.batches > 1)
-                  tma_load_3d_pair(stage_a(stage) + j * C::SLAB_A, &p.tmap_a, fb, x, m_blk * C::BM, c.batch);
+                  tma_load_3d_pair(stage_a(stage) + j * C::SLAB_A, tma, fb, x, m_blk * C::BM, c.batch);
                 else
-                  tma_load_2d_pair(stage_a(stage) + j * C::SLAB_A, &p.tmap_a, fb, x, m_blk * C::BM);
+                  tma_load_2d_pair(stage_a(stage) + j * C::SLAB_A, tma, fb, x, m_blk * C::BM);
                 if (EXT && p.b_entries > 1)
-                  tma_load_3d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x, yb, c.bsel);
+                  tma_load_3d_pair(stage_b(stage) + j * C::SLAB_B, tmb, fb, x, yb, c.bsel);
                 else
-                  tma_load_2d_pair(stage_b(stage) + j * C::SLAB_B, &p.tmap_b, fb, x, yb);
+                  tma_load_2d_pair(stage_b(stage) + j * C::SLAB_B, tmb, fb, x, yb);
               }
             }
             first = false;

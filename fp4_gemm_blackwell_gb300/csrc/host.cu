@@ -233,6 +233,8 @@ struct bsg_plan_s {
   bsg_desc desc;
   bsg::GemmParams params;
   bsg::GemmKernelInfo info;
+  const void* fn_ext;        // the EXT instantiation of the same variant (bsg_plan_run_operands)
+  CUtensorMap* map_slots;    // two 128-byte tensor-map slots per CTA of the grid, in the workspace
   int device;
   int grid;
   int cluster;
@@ -430,17 +432,19 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   return v;
 }
 
-// Workspace layout: [status word | per-tile counters | split-K partials (workspace mode)].
+// Workspace layout: [status word | per-tile counters | split-K partials (workspace mode) |
+// tensor-map slots (pointer-agnostic runs: two 128-byte maps per CTA of a grid of `grid`)].
 struct WorkspaceLayout {
-  size_t cnt_off, part_off, part_bytes, total;
+  size_t cnt_off, part_off, part_bytes, slot_off, total;
 };
 
-WorkspaceLayout workspace_layout(const Variant& v, int num_tiles) {
+WorkspaceLayout workspace_layout(const Variant& v, int num_tiles, int grid) {
   WorkspaceLayout w;
   w.cnt_off = 256;
   w.part_off = w.cnt_off + (static_cast<size_t>(num_tiles) * 4 + 255) / 256 * 256;
   w.part_bytes = v.mode == bsg::SPLIT_WORKSPACE ? static_cast<size_t>(v.splits) * num_tiles * 128 * v.bn * 4 : 0;
-  w.total = w.part_off + w.part_bytes;
+  w.slot_off = (w.part_off + w.part_bytes + 255) / 256 * 256;
+  w.total = w.slot_off + static_cast<size_t>(grid) * 2 * sizeof(CUtensorMap);
   return w;
 }
 
@@ -588,6 +592,9 @@ bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, 
 namespace bsg {
 bool find_kernel(int kind, int out, unsigned flags, int batches, bool pair, int bn, int kc, GemmKernelInfo* info) {
   const bool ext = (flags & (BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL | BSG_F_GROUPED)) != 0 || batches > 1;
+  return find_kernel_variant(kind, out, ext, pair, bn, kc, info);
+}
+bool find_kernel_variant(int kind, int out, bool ext, bool pair, int bn, int kc, GemmKernelInfo* info) {
   if (pair) {
     if (kind == KIND_MX) return ext ? gemm_pair_kernel_info_mx_ext(out, info) : gemm_pair_kernel_info_mx(out, info);
     return ext ? gemm_pair_kernel_info_nv_ext(out, info) : gemm_pair_kernel_info_nv(out, info);
@@ -618,6 +625,11 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
                                       v.pair, v.bn, v.kc, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
+  bsg::GemmKernelInfo info_ext{};
+  if (!bsg::find_kernel_variant(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, true, v.pair, v.bn, v.kc,
+                                &info_ext))
+    return fail(BSG_ERR_DTYPE, "no extended kernel for this format / output type");
+  if ((s = ensure_smem_attr(info_ext, dev)) != BSG_OK) return s;
   int resident = di.sms;
   if ((s = resident_ctas(info, v.cmn * v.cmm, di.sms, dev, &resident)) != BSG_OK) return s;
 
@@ -626,6 +638,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   p->magic = kPlanMagic;
   p->desc = *d;
   p->info = info;
+  p->fn_ext = info_ext.fn;
   p->device = dev;
   p->workspace = nullptr;
   p->cluster = v.cluster;
@@ -634,7 +647,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
     delete p;
     return s;
   }
-  const WorkspaceLayout w = workspace_layout(v, g.num_tiles);
+  const WorkspaceLayout w = workspace_layout(v, g.num_tiles, p->grid);
   cudaError_t e = cudaMalloc(&p->workspace, w.total);
   if (e != cudaSuccess) {
     delete p;
@@ -651,6 +664,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   g.status = reinterpret_cast<unsigned*>(ws);
   g.counters = reinterpret_cast<unsigned*>(ws + w.cnt_off);
   g.partial = w.part_bytes ? reinterpret_cast<float*>(ws + w.part_off) : nullptr;
+  p->map_slots = reinterpret_cast<CUtensorMap*>(ws + w.slot_off);
   static const char* kModeName[] = {"", "w", "c"};
   if (v.pair) {
     std::snprintf(p->variant, sizeof(p->variant), "%s_pair256_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
@@ -692,6 +706,43 @@ BSG_API bsg_status bsg_plan_create(bsg_plan_t* plan, const bsg_desc* d) { return
 BSG_API bsg_status bsg_plan_run(bsg_plan_t plan, bsg_stream_t stream) {
   if (!plan_ok(plan)) return fail(BSG_ERR_INVALID_ARG, "invalid plan handle");
   return plan_launch(plan, plan->params, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BSG_API bsg_status bsg_plan_run_operands(bsg_plan_t plan, const bsg_operands* ops, bsg_stream_t stream) {
+  if (!plan_ok(plan)) return fail(BSG_ERR_INVALID_ARG, "invalid plan handle");
+  if (ops == nullptr) return fail(BSG_ERR_INVALID_ARG, "operands are null");
+  bsg_desc d = plan->desc;
+  d.A = ops->A;
+  d.B = ops->B;
+  d.SFA = ops->SFA;
+  d.SFB = ops->SFB;
+  d.D = ops->D;
+  d.bias = ops->bias;
+  d.alpha_dev = ops->alpha_dev;
+  d.C = ops->C;
+  d.alpha_row = ops->alpha_row;
+  d.alpha_col = ops->alpha_col;
+  d.group_index = ops->group_index;
+  bsg_status s = validate_desc(&d);
+  if (s != BSG_OK) return s;
+  if ((s = validate_ranges(&d)) != BSG_OK) return s;
+  bsg::GemmParams g = plan->params;
+  g.sfa = static_cast<const uint8_t*>(d.SFA);
+  g.sfb = static_cast<const uint8_t*>(d.SFB);
+  g.bias = d.bias;
+  g.d = d.D;
+  g.alpha_dev = d.alpha_dev;
+  g.c = (d.flags & BSG_F_C) ? d.C : nullptr;
+  g.alpha_row = (d.flags & BSG_F_ALPHA_ROW) ? d.alpha_row : nullptr;
+  g.alpha_col = (d.flags & BSG_F_ALPHA_COL) ? d.alpha_col : nullptr;
+  g.group_index = (d.flags & BSG_F_GROUPED) ? d.group_index : nullptr;
+  const bool d32 = (reinterpret_cast<uintptr_t>(d.D) & 31u) == 0 &&
+                   (!(d.flags & BSG_F_C) || (reinterpret_cast<uintptr_t>(d.C) & 31u) == 0);
+  g.flags = (g.flags & ~bsg::F_D32) | (d32 ? bsg::F_D32 : 0u);
+  g.map_slots = plan->map_slots;
+  g.remap_a = d.A;
+  g.remap_b = d.B;
+  return launch_with(&plan->cfg, plan->fn_ext, g, reinterpret_cast<cudaStream_t>(stream));
 }
 
 BSG_API bsg_status bsg_plan_destroy(bsg_plan_t plan) {
@@ -950,7 +1001,7 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
   const int num_tiles =
       ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn) * (d->L > 1 && !(d->flags & BSG_F_GROUPED) ? d->L : 1);
-  const WorkspaceLayout w = workspace_layout(v, num_tiles);
+  const WorkspaceLayout w = workspace_layout(v, num_tiles, 0);
   if (w.total > kNoAllocScratchBytes)
     return fail(BSG_ERR_SHAPE,
                 "this problem needs %zu bytes of scratch (split-K %d over %d tiles); the allocation-free "

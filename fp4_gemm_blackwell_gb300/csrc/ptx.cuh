@@ -133,6 +133,22 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// A copy of the tensor map `src` (kernel parameter space) in the 128-byte aligned global slot
+// `dst`, with its global address replaced by `addr`, made visible to the tensor-map proxy of the
+// calling thread's later TMA copies: plain stores of the 128 bytes, tensormap.replace of the
+// address field, then a release and an acquire fence between the generic and tensor-map proxies.
+// The calling thread alone uses the slot; no other copy may be in flight through it.
+__device__ __forceinline__ void tmap_remap(CUtensorMap* dst, const CUtensorMap* src, const void* addr) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d[i] = s[i];
+  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(addr)
+               : "memory");
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(dst) : "memory");
+}
+
 // 1-D bulk load global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {

@@ -151,6 +151,33 @@ bsg_status bsg_plan_create(bsg_plan_t* plan, const bsg_desc* d);
  * shared between its launches). */
 bsg_status bsg_plan_run(bsg_plan_t plan, bsg_stream_t stream);
 
+/* The buffers of one run of a plan on operands other than those it was created with
+ * (fields as in bsg_desc; those the plan's flags do not read are ignored). */
+typedef struct {
+  const void* A;
+  const void* B;
+  const void* SFA;
+  const void* SFB;
+  void* D;
+  const void* bias;
+  const float* alpha_dev;
+  const void* C;
+  const float* alpha_row;
+  const float* alpha_col;
+  const int* group_index;
+} bsg_operands;
+
+/* Pointer-agnostic run: enqueue the plan's GEMM on `ops`' buffers, which must have the
+ * plan's shapes, strides and alignment (checked here as at plan creation, each buffer
+ * against its allocation).  Nothing is re-encoded on the host: the new pointers travel as
+ * kernel parameters.  Each CTA copies the plan's two TMA tensor maps into its own slot of
+ * the plan's workspace and replaces their global addresses on the device (tensormap.replace,
+ * the device-side form of re-encoding a tensor map that the launch-overhead page profiles
+ * on the host), so a captured graph node of this call can be re-pointed by updating its
+ * kernel parameters alone.  The plan's own buffers are untouched; bsg_plan_run still uses
+ * them.  Same stream rule as bsg_plan_run. */
+bsg_status bsg_plan_run_operands(bsg_plan_t plan, const bsg_operands* ops, bsg_stream_t stream);
+
 /* Free the plan and its workspace.  Call after its last launch has completed. */
 bsg_status bsg_plan_destroy(bsg_plan_t plan);
 

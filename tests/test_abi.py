@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for want in ["bsg_plan_create", "bsg_plan_run", "bsg_plan_destroy", "bsg_plan_check_status",
-                 "mxfp8_gemm", "nvfp4_gemm", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_last_error"]:
+                 "mxfp8_gemm", "nvfp4_gemm", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_last_error",
+                 "bsg_plan_run_operands"]:
         assert want in names
 
 
@@ -91,6 +92,7 @@ def test_invalid_descriptors_are_rejected_before_device_work(L, kw, status):
 def test_null_handles(L):
     assert L.bsg_plan_create(None, None) == 1
     assert L.bsg_plan_run(None, None) == 1
+    assert L.bsg_plan_run_operands(None, None, None) == 1
     assert L.bsg_plan_destroy(None) == 1
     assert L.bsg_plan_check_status(None) == 1
     assert L.bsg_plan_variant(None) == b""

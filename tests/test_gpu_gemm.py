@@ -348,13 +348,16 @@ def test_batched(kind, env, monkeypatch):
     alphas = [float(p["alpha"]) for p in probs]
     # alpha is shared by the batch: give every entry the same one by scaling with entry 0's
     alpha = alphas[0]
+    D2 = torch.full_like(D, 0x7BAD)
     with bsg.Plan(P.KIND[kind], P.OUT["bf16"], M, N, K, A, B, SFA, SFB, D, alpha=alpha, flags=flags, bias=bias,
                   C=C, beta=0.5, L=L, strides=strides) as plan:
         variant = plan.variant
         plan.run()
+        plan.run_operands(A, B, SFA, SFB, D2, bias=bias, C=C)  # 3-D maps rewritten on the device
         plan.check_status()
     torch.cuda.synchronize()
     dall = D.cpu().numpy().view(np.uint16)
+    assert np.array_equal(D2.cpu().numpy().view(np.uint16), dall), variant
     sD = strides["stride_D"] // 2
     for l, p in enumerate(probs):
         got = R.out_from_bits(dall[l * sD:l * sD + M * N].reshape(M, N), "bf16")
@@ -434,13 +437,16 @@ def test_grouped(kind, env, monkeypatch):
     silu = kind == "nvfp4"
     flags = (bsg.BSG_F_GROUPED | bsg.BSG_F_ALPHA_DEVICE | bsg.BSG_F_BIAS | (bsg.BSG_F_SILU if silu else 0) |
              (bsg.BSG_F_C if residual else 0))
+    D2 = torch.full_like(D, 0x7BAD)
     with bsg.Plan(P.KIND[kind], P.OUT["bf16"], M, N, K, A, B, SFA, SFB, D, flags=flags, bias=bias,
                   alpha_dev=alpha_dev, C=C, beta=0.75, L=G, strides=dict(stride_B=sB, stride_SFB=sSFB),
                   group_index=gi) as plan:
         variant = plan.variant
         plan.run()
+        plan.run_operands(A, B, SFA, SFB, D2, bias=bias, alpha_dev=alpha_dev, C=C, group_index=gi)
         plan.check_status()
     torch.cuda.synchronize()
+    assert np.array_equal(D2.cpu().numpy(), D.cpu().numpy()), variant
     assert "pair" not in variant, variant
     bits = D.cpu().numpy().view(np.uint16).reshape(M, N)
     got = R.out_from_bits(bits, "bf16")
@@ -454,3 +460,45 @@ def test_grouped(kind, env, monkeypatch):
         P.assert_parity(got, prob, "bf16", bias_vals, silu, rows=grows[g], epi=epi)
         stored[grows[g]] = True
     assert np.all(bits[~stored] == 0x7BAD), "rows of no stored group were written (%s)" % variant
+
+
+@pytest.mark.parametrize("env", [{}, {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 32},
+                                 {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2},
+                                 {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3}, {"BSG_FORCE_BN": 32, "BSG_FORCE_CM": 4}])
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_run_operands(kind, env, monkeypatch):
+    # Pointer-agnostic runs: one plan, made on problem 1's buffers, runs on problem 2's (its
+    # tensor maps rewritten on the device), then plainly on its own, then on problem 2's again;
+    # every kernel family (CTA pair, one and two accumulators, split-K in a cluster and through
+    # the workspace, multicast).  Each result against its own oracle; the other D untouched.
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    silu = kind == "nvfp4"
+    p1 = P.make_problem(kind, 300, 272, 2048, seed_a=3, seed_b=4)
+    p2 = P.make_problem(kind, 300, 272, 2048, seed_a=5, seed_b=6)
+    d1 = P.DeviceProblem(p1, bias=True, silu=silu, residual="separate", beta=0.5)
+    d2 = P.DeviceProblem(p2, bias=True, silu=silu, residual="separate", beta=0.5)
+    a1 = torch.tensor([float(p1["alpha"])], dtype=torch.float32, device="cuda")
+    a2 = torch.tensor([float(p2["alpha"])], dtype=torch.float32, device="cuda")
+
+    def run2(plan):
+        plan.run_operands(d2.A, d2.B, d2.SFA, d2.SFB, d2.D, bias=d2.bias, alpha_dev=a2, C=d2.C)
+
+    with d1.plan(alpha_dev=a1) as plan:
+        variant = plan.variant
+        run2(plan)
+        plan.check_status()
+        got2 = d2.result()
+        assert np.all(d1.Dbuf.cpu().numpy().view(np.uint16) == d1.CANARY), "the plan's own D was written"
+        plan.run()
+        plan.check_status()
+        got1 = d1.result()
+        d2.Dbuf.fill_(d2.CANARY)
+        run2(plan)
+        plan.check_status()
+        got2b = d2.result()
+    P.assert_parity(got2, p2, "bf16", d2.bias_vals, silu, epi=d2.epi_kwargs())
+    P.assert_parity(got1, p1, "bf16", d1.bias_vals, silu, epi=d1.epi_kwargs())
+    assert np.array_equal(got2, got2b), variant
+    if "BSG_FORCE_PAIR" in env:
+        assert "pair" in variant, variant
