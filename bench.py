@@ -496,6 +496,39 @@ def grouped_config(bsg, peaks, steps=200, warmup=10):
     return r
 
 
+class _OperandsRun:
+    """plan.run_operands on one fixed buffer set, with the run(stream) method graph_time calls."""
+
+    def __init__(self, plan, a, b, bias, d, alpha_dev):
+        self.plan, self.args = plan, (a.codes, b.codes, a.sf, b.sf, d)
+        self.kw = dict(bias=bias, alpha_dev=alpha_dev)
+
+    def run(self, stream=None):
+        self.plan.run_operands(*self.args, stream=stream, **self.kw)
+
+
+def remap_config(bsg, peaks, steps=400, warmup=10):
+    """The headline workload with ONE plan run on every input copy by bsg_plan_run_operands (its
+    tensor maps rewritten on the device each launch), against one plan per copy."""
+    p1 = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=1)
+    cp = copies_to_exceed_l2(p1.algorithmic_bytes())
+    p1.close()
+    prob = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=cp)
+    ms_plain, _ = graph_time(prob.plans, steps, warmup)
+    ad = torch.tensor([prob.alpha], dtype=torch.float32, device="cuda")
+    k = bsg.BSG_NVFP4
+    a0, b0, bt0, d0 = prob.sets[0]
+    one = bsg.Plan(k, bsg.BSG_OUT_BF16, M1, N1, K1, a0.codes, b0.codes, a0.sf, b0.sf, d0,
+                   flags=prob.flags | bsg.BSG_F_ALPHA_DEVICE, bias=bt0, alpha_dev=ad)
+    runs = [_OperandsRun(one, a, b, bt, d, ad) for (a, b, bt, d) in prob.sets]
+    ms_remap, _ = graph_time(runs, steps, warmup)
+    r = {"kernel_us_remap": round(ms_remap * 1e3 / steps, 3), "kernel_us_plans": round(ms_plain * 1e3 / steps, 3),
+         "copies": cp, "variant": one.variant}
+    one.close()
+    prob.close()
+    return r
+
+
 def small_config(bsg, peaks, steps=2000, warmup=20):
     prob = Problem(bsg, "mxfp8", 256, 256, 256, copies=64)
     ms, _ = graph_time(prob.plans, steps, warmup)
@@ -808,6 +841,7 @@ def main():
             for L in (2, 8):
                 extras["nvfp4_batched_l%d_m128_n4096_k4096" % L] = batched_config(bsg, peaks, L)
             extras["nvfp4_grouped_8x4096x4096_moe"] = grouped_config(bsg, peaks)
+            extras["nvfp4_m128_pointer_agnostic"] = remap_config(bsg, peaks)
             extras["launch_loop_1000"] = launch_loop(bsg)
             for kind in ("mxfp8", "nvfp4"):
                 for bf in (False, True):

@@ -68,7 +68,8 @@ struct GemmParams {
   const int* group_index;  // grouped (F_GROUPED): the group of each of the M rows, -1 = no group
   // Pointer-agnostic runs (EXT instantiations): when map_slots is set, each CTA's code producer
   // copies tmap_a / tmap_b into its two 128-byte global slots (map_slots + 2 * blockIdx.x),
-  // replaces their global addresses by remap_a / remap_b and loads through the copies.
+  // replaces their global addresses by remap_a / remap_b and loads through the copies.  The
+  // host alternates between two slot sets from one such launch of a plan to the next.
   CUtensorMap* map_slots;
   const void* remap_a;
   const void* remap_b;

@@ -580,6 +580,19 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
   const uint16_t cmask = static_cast<uint16_t>(row_mask | col_mask);
   const uint32_t tmem_base = *tmem_slot;
   const int nst = p.ring_stages;  // ring stages in use (fewer than STAGES with a split-K cluster)
+  // Pointer-agnostic run: the code producer's own copies of the tensor maps, written before the
+  // wait below (they read only this launch's parameters, and the slot set is not the one the
+  // plan's previous launch, which may still run, uses), so that their fences overlap it.
+  const CUtensorMap* tma = &p.tmap_a;
+  const CUtensorMap* tmb = &p.tmap_b;
+  if (EXT && p.map_slots != nullptr) {
+    CUtensorMap* slot = p.map_slots + 2 * blockIdx.x;
+    if (warp == 0 && lane == 0) {
+      tmap_remap2(slot, &p.tmap_a, &p.tmap_b, p.remap_a, p.remap_b);
+    }
+    tma = slot;
+    tmb = slot + 1;
+  }
   // Everything above touched only this CTA's own resources; from here on global memory is
   // read and written, so wait for the preceding grid in the stream (programmatic dependent
   // launch), and let the next grid start its launch while this one runs.
@@ -593,15 +606,6 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer: code tiles
       if (lane == 0) {
-        const CUtensorMap* tma = &p.tmap_a;
-        const CUtensorMap* tmb = &p.tmap_b;
-        if (EXT && p.map_slots != nullptr) {  // pointer-agnostic run: this CTA's own copies
-          CUtensorMap* slot = p.map_slots + 2 * blockIdx.x;
-          tmap_remap(slot, &p.tmap_a, p.remap_a);
-          tmap_remap(slot + 1, &p.tmap_b, p.remap_b);
-          tma = slot;
-          tmb = slot + 1;
-        }
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;

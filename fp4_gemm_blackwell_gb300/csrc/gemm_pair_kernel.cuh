@@ -150,6 +150,18 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
   cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Pointer-agnostic run: the code producer's own copies of the tensor maps, written before the
+  // wait (see the 1-SM kernel)
+  const CUtensorMap* tma = &p.tmap_a;
+  const CUtensorMap* tmb = &p.tmap_b;
+  if (EXT && p.map_slots != nullptr) {
+    CUtensorMap* slot = p.map_slots + 2 * blockIdx.x;
+    if (warp == 0 && lane == 0) {
+      tmap_remap2(slot, &p.tmap_a, &p.tmap_b, p.remap_a, p.remap_b);
+    }
+    tma = slot;
+    tmb = slot + 1;
+  }
   griddep_wait();
   griddep_launch_dependents();
 
@@ -161,15 +173,6 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer (each CTA)
       if (lane == 0) {
-        const CUtensorMap* tma = &p.tmap_a;
-        const CUtensorMap* tmb = &p.tmap_b;
-        if (EXT && p.map_slots != nullptr) {  // pointer-agnostic run: this CTA's own copies
-          CUtensorMap* slot = p.map_slots + 2 * blockIdx.x;
-          tmap_remap(slot, &p.tmap_a, p.remap_a);
-          tmap_remap(slot + 1, &p.tmap_b, p.remap_b);
-          tma = slot;
-          tmb = slot + 1;
-        }
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;

@@ -234,7 +234,8 @@ struct bsg_plan_s {
   bsg::GemmParams params;
   bsg::GemmKernelInfo info;
   const void* fn_ext;        // the EXT instantiation of the same variant (bsg_plan_run_operands)
-  CUtensorMap* map_slots;    // two 128-byte tensor-map slots per CTA of the grid, in the workspace
+  CUtensorMap* map_slots;    // two sets of two 128-byte tensor-map slots per CTA, in the workspace
+  unsigned remap_runs;       // pointer-agnostic launches so far (their parity picks the slot set)
   int device;
   int grid;
   int cluster;
@@ -433,7 +434,8 @@ Variant choose_variant(const bsg_desc* d, int sms) {
 }
 
 // Workspace layout: [status word | per-tile counters | split-K partials (workspace mode) |
-// tensor-map slots (pointer-agnostic runs: two 128-byte maps per CTA of a grid of `grid`)].
+// tensor-map slots (pointer-agnostic runs: two sets of two 128-byte maps per CTA of a grid of
+// `grid`)].
 struct WorkspaceLayout {
   size_t cnt_off, part_off, part_bytes, slot_off, total;
 };
@@ -444,7 +446,7 @@ WorkspaceLayout workspace_layout(const Variant& v, int num_tiles, int grid) {
   w.part_off = w.cnt_off + (static_cast<size_t>(num_tiles) * 4 + 255) / 256 * 256;
   w.part_bytes = v.mode == bsg::SPLIT_WORKSPACE ? static_cast<size_t>(v.splits) * num_tiles * 128 * v.bn * 4 : 0;
   w.slot_off = (w.part_off + w.part_bytes + 255) / 256 * 256;
-  w.total = w.slot_off + static_cast<size_t>(grid) * 2 * sizeof(CUtensorMap);
+  w.total = w.slot_off + static_cast<size_t>(grid) * 4 * sizeof(CUtensorMap);
   return w;
 }
 
@@ -639,6 +641,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   p->desc = *d;
   p->info = info;
   p->fn_ext = info_ext.fn;
+  p->remap_runs = 0;
   p->device = dev;
   p->workspace = nullptr;
   p->cluster = v.cluster;
@@ -739,7 +742,9 @@ BSG_API bsg_status bsg_plan_run_operands(bsg_plan_t plan, const bsg_operands* op
   const bool d32 = (reinterpret_cast<uintptr_t>(d.D) & 31u) == 0 &&
                    (!(d.flags & BSG_F_C) || (reinterpret_cast<uintptr_t>(d.C) & 31u) == 0);
   g.flags = (g.flags & ~bsg::F_D32) | (d32 ? bsg::F_D32 : 0u);
-  g.map_slots = plan->map_slots;
+  // The kernel writes its slots before its programmatic-launch wait, while the plan's previous
+  // launch may still run: consecutive pointer-agnostic launches take alternate slot sets.
+  g.map_slots = plan->map_slots + static_cast<size_t>(plan->remap_runs++ & 1u) * 2 * plan->grid;
   g.remap_a = d.A;
   g.remap_b = d.B;
   return launch_with(&plan->cfg, plan->fn_ext, g, reinterpret_cast<cudaStream_t>(stream));

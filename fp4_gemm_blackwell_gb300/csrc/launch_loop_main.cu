@@ -3,7 +3,10 @@
 // {(4096, 4096), (14336, 4096), (4096, 14336)}, BF16 output, cached plans.  Prints one JSON
 // line: host enqueue time per call on a stream, wall time per call, device time per call of
 // the same calls replayed from a captured CUDA graph, and host time per call of that replay.
-// Operands are quantised on the device by bsg_quantize from a deterministic pattern.
+// Then one plan of the 128 x 4096 x 4096 shape: host time per call of bsg_plan_run, and of
+// bsg_plan_run_operands alternating between two buffer sets (the pointer-agnostic run, which
+// checks every buffer against its allocation).  Operands are quantised on the device by
+// bsg_quantize from a deterministic pattern.
 #include <cuda_runtime.h>
 
 #include <chrono>
@@ -107,12 +110,57 @@ int main() {
   cudaStreamSynchronize(stream);
   float ms = 0.0f;
   cudaEventElapsedTime(&ms, e0, e1);
+  // one plan, two buffer sets of the 128 x 4096 x 4096 shape
+  const Call* c0 = nullptr;
+  for (const Call& c : cl)
+    if (c.s.M == 128 && c.s.N == 4096 && c.s.K == 4096) c0 = &c;
+  Operand a2, b2;
+  void* d2 = nullptr;
+  if (c0 == nullptr || !make_operand(128, 4096, 91, xbuf, gs, &a2) || !make_operand(4096, 4096, 92, xbuf, gs, &b2) ||
+      cudaMalloc(&d2, 128 * 4096 * 2) != cudaSuccess) {
+    std::printf("{\"error\": \"second operand set\"}\n");
+    return 1;
+  }
+  bsg_desc d{};
+  d.kind = BSG_NVFP4;
+  d.out = BSG_OUT_BF16;
+  d.M = 128;
+  d.N = 4096;
+  d.K = 4096;
+  d.A = c0->a.codes;
+  d.B = c0->b.codes;
+  d.SFA = c0->a.sf;
+  d.SFB = c0->b.sf;
+  d.D = c0->d;
+  d.alpha = c0->alpha;
+  bsg_plan_t plan = nullptr;
+  if (bsg_plan_create(&plan, &d) != BSG_OK) {
+    std::printf("{\"error\": \"%s\"}\n", bsg_last_error());
+    return 1;
+  }
+  bsg_operands ops[2] = {{c0->a.codes, c0->b.codes, c0->a.sf, c0->b.sf, c0->d},
+                         {a2.codes, b2.codes, a2.sf, b2.sf, d2}};
+  const bsg_stream_t st = reinterpret_cast<bsg_stream_t>(stream);
+  for (int i = 0; i < 20; ++i) bsg_plan_run_operands(plan, &ops[i & 1], st);
+  cudaStreamSynchronize(stream);
+  const double r0 = now_us();
+  for (int i = 0; i < calls; ++i) bsg_plan_run(plan, st);
+  const double r1 = now_us();
+  cudaStreamSynchronize(stream);
+  const double o0 = now_us();
+  int bad = 0;
+  for (int i = 0; i < calls; ++i) bad += bsg_plan_run_operands(plan, &ops[i & 1], st) != BSG_OK;
+  const double o1 = now_us();
+  cudaStreamSynchronize(stream);
+  bsg_plan_destroy(plan);
   const cudaError_t err = cudaGetLastError();
   const double kernel_us = ms * 1000.0 / calls;
   std::printf("{\"calls\": %d, \"shapes\": %d, \"host_us_per_call\": %.3f, \"wall_us_per_call\": %.3f, "
               "\"kernel_us_per_call\": %.3f, \"graph_host_us_per_call\": %.4f, \"host_over_kernel\": %.4f, "
+              "\"plan_run_host_us\": %.3f, \"plan_run_operands_host_us\": %.3f, \"operands_errors\": %d, "
               "\"cuda\": \"%s\"}\n",
               calls, static_cast<int>(cl.size()), (t1 - t0) / calls, (t2 - t0) / calls, kernel_us,
-              (g1 - g0) / calls, (t1 - t0) / calls / kernel_us, cudaGetErrorString(err));
+              (g1 - g0) / calls, (t1 - t0) / calls / kernel_us, (r1 - r0) / calls, (o1 - o0) / calls, bad,
+              cudaGetErrorString(err));
   return err == cudaSuccess ? 0 : 1;
 }

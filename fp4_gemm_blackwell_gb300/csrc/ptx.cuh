@@ -133,20 +133,29 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// A copy of the tensor map `src` (kernel parameter space) in the 128-byte aligned global slot
-// `dst`, with its global address replaced by `addr`, made visible to the tensor-map proxy of the
-// calling thread's later TMA copies: plain stores of the 128 bytes, tensormap.replace of the
-// address field, then a release and an acquire fence between the generic and tensor-map proxies.
-// The calling thread alone uses the slot; no other copy may be in flight through it.
-__device__ __forceinline__ void tmap_remap(CUtensorMap* dst, const CUtensorMap* src, const void* addr) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
+// Copies of the tensor maps `src[0..1]` (kernel parameter space) in the 128-byte aligned global
+// slots `dst[0..1]`, their global addresses replaced by `addr[0..1]`, made visible to the
+// tensor-map proxy of the calling thread's later TMA copies: plain stores of the 2 x 128 bytes,
+// tensormap.replace of each address field, one release fence and an acquire fence per map
+// between the generic and tensor-map proxies.  The calling thread alone uses the slots; no
+// copy may be in flight through them.
+__device__ __forceinline__ void tmap_remap2(CUtensorMap* dst, const CUtensorMap* src0, const CUtensorMap* src1,
+                                            const void* addr0, const void* addr1) {
+  const uint4* s0 = reinterpret_cast<const uint4*>(src0);
+  const uint4* s1 = reinterpret_cast<const uint4*>(src1);
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) d[i] = s[i];
-  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(addr)
+  for (int i = 0; i < 8; ++i) {
+    d[i] = s0[i];
+    d[8 + i] = s1[i];
+  }
+  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(addr0)
+               : "memory");
+  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst + 1), "l"(addr1)
                : "memory");
   asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(dst) : "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(dst + 1) : "memory");
 }
 
 // 1-D bulk load global -> shared (16-byte aligned addresses, size a multiple of 16).
