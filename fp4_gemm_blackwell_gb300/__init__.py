@@ -11,7 +11,7 @@ import ctypes
 import os
 
 __all__ = [
-    "BSG_MXFP8", "BSG_NVFP4", "BSG_OUT_F16", "BSG_OUT_BF16", "BSG_F_BIAS", "BSG_F_SILU",
+    "BSG_MXFP8", "BSG_NVFP4", "BSG_OUT_F16", "BSG_OUT_BF16", "BSG_OUT_NVFP4", "BSG_F_BIAS", "BSG_F_SILU",
     "BSG_F_ALPHA_DEVICE", "BSG_F_C", "BSG_F_ALPHA_ROW", "BSG_F_ALPHA_COL", "BSG_F_GROUPED", "BsgError", "lib", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_plan_create",
     "bsg_plan_run", "bsg_plan_run_operands", "bsg_plan_destroy", "bsg_plan_check_status", "bsg_plan_variant",
     "bsg_plan_debug_set", "mxfp8_gemm", "nvfp4_gemm", "bsg_cache_clear", "bsg_last_error",
@@ -19,7 +19,7 @@ __all__ = [
 ]
 
 BSG_MXFP8, BSG_NVFP4 = 0, 1
-BSG_OUT_F16, BSG_OUT_BF16 = 0, 1
+BSG_OUT_F16, BSG_OUT_BF16, BSG_OUT_NVFP4 = 0, 1, 2
 BSG_F_BIAS, BSG_F_SILU, BSG_F_ALPHA_DEVICE = 1, 2, 4
 BSG_F_C, BSG_F_ALPHA_ROW, BSG_F_ALPHA_COL, BSG_F_GROUPED = 8, 16, 32, 64
 
@@ -50,13 +50,14 @@ class BsgDesc(ctypes.Structure):
         ("alpha_col", ctypes.c_void_p), ("L", ctypes.c_int),
         ("stride_A", ctypes.c_longlong), ("stride_B", ctypes.c_longlong), ("stride_SFA", ctypes.c_longlong),
         ("stride_SFB", ctypes.c_longlong), ("stride_D", ctypes.c_longlong), ("stride_C", ctypes.c_longlong),
-        ("group_index", ctypes.c_void_p),
+        ("group_index", ctypes.c_void_p), ("SFD", ctypes.c_void_p), ("d_scale", ctypes.c_void_p),
     ]
 
 
 class BsgOperands(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in
-                ("A", "B", "SFA", "SFB", "D", "bias", "alpha_dev", "C", "alpha_row", "alpha_col", "group_index")]
+                ("A", "B", "SFA", "SFB", "D", "bias", "alpha_dev", "C", "alpha_row", "alpha_col", "group_index",
+                 "SFD", "d_scale")]
 
 
 _lib = None
@@ -144,15 +145,17 @@ def bsg_quantize_bf16(kind, x, rows, K, codes, sf, global_scale=None, stream=Non
 
 
 def bsg_plan_create(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None,
-                    C=None, beta=0.0, alpha_row=None, alpha_col=None, L=0, strides=None, group_index=None):
+                    C=None, beta=0.0, alpha_row=None, alpha_col=None, L=0, strides=None, group_index=None,
+                    SFD=None, d_scale=None):
     """strides (batched, L >= 2; grouped, stride_B and stride_SFB): dict of byte strides
     stride_A, stride_B, stride_SFA, stride_SFB, stride_D and stride_C between consecutive
-    entries.  group_index (grouped, with BSG_F_GROUPED and L groups): M int32 on the device."""
+    entries.  group_index (grouped, with BSG_F_GROUPED and L groups): M int32 on the device.
+    SFD, d_scale (out = BSG_OUT_NVFP4): the output scales and the device global scale."""
     st = strides or {}
     d = BsgDesc(kind, out, flags, M, N, K, _ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(bias), _ptr(D),
                 alpha, _ptr(alpha_dev), _ptr(C), beta, _ptr(alpha_row), _ptr(alpha_col), L,
                 *(st.get(k, 0) for k in ("stride_A", "stride_B", "stride_SFA", "stride_SFB", "stride_D", "stride_C")),
-                _ptr(group_index))
+                _ptr(group_index), _ptr(SFD), _ptr(d_scale))
     h = ctypes.c_void_p()
     _check(lib().bsg_plan_create(ctypes.byref(h), ctypes.byref(d)))
     return h.value
@@ -163,9 +166,9 @@ def bsg_plan_run(plan, stream=None):
 
 
 def bsg_plan_run_operands(plan, A, B, SFA, SFB, D, bias=None, alpha_dev=None, C=None, alpha_row=None,
-                          alpha_col=None, group_index=None, stream=None):
+                          alpha_col=None, group_index=None, SFD=None, d_scale=None, stream=None):
     ops = BsgOperands(*(_ptr(x) for x in (A, B, SFA, SFB, D, bias, alpha_dev, C, alpha_row, alpha_col,
-                                          group_index)))
+                                          group_index, SFD, d_scale)))
     _check(lib().bsg_plan_run_operands(plan, ctypes.byref(ops), _stream(stream)))
 
 

@@ -9,7 +9,7 @@
 namespace bsg {
 
 enum : int { KIND_MX = 0, KIND_NV = 1 };
-enum : int { OUT_F16 = 0, OUT_BF16 = 1 };
+enum : int { OUT_F16 = 0, OUT_BF16 = 1, OUT_NV4 = 2 };  // OUT_NV4: NVFP4 codes + scales
 enum : unsigned {
   F_BIAS = 1u,
   F_SILU = 2u,
@@ -48,6 +48,9 @@ struct GemmParams {
   const float* alpha_row;  // M factors (flags & F_ALPHA_ROW)
   const float* alpha_col;  // N factors (flags & F_ALPHA_COL)
   const float* alpha_dev;
+  uint8_t* sfd;            // NVFP4 output: swizzled UE4M3 scales of D (M x N/16, padded)
+  const float* d_scale;    // NVFP4 output: the global scale s of D (device memory)
+  int sfd_cols4;           // NVFP4 output: padded scale columns / 4
   float* partial;      // split-K partial tiles (splits x tiles x 128 x BN floats)
   unsigned* counters;  // split-K arrival counter per tile (0 between launches)
   unsigned* status;    // device status word

@@ -25,6 +25,7 @@
 #include <cuda_fp16.h>
 
 #include "bsg_internal.h"
+#include "nvfp4_codec.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
@@ -201,23 +202,25 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
   return r != 0;
 }
 
+// Two values rounded to the 16-bit output type and packed (BF16 for OUT_BF16, and for OUT_NV4,
+// whose bias and C are BF16).
 template <int OUT>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
-  if constexpr (OUT == OUT_BF16) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  if constexpr (OUT == OUT_F16) {
+    __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   } else {
-    __half2 h = __floats2half2_rn(a, b);
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
 }
 
 template <int OUT>
 __device__ __forceinline__ float out_to_float(uint16_t bits) {
-  if constexpr (OUT == OUT_BF16) {
-    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
-  } else {
+  if constexpr (OUT == OUT_F16) {
     return __half2float(__ushort_as_half(bits));
+  } else {
+    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
   }
 }
 
@@ -271,9 +274,8 @@ __device__ __forceinline__ void load_bias(const GemmParams& p, int n, float (&b)
 // Columns at or beyond N read no bias.  The path of every problem without C or per-column
 // factors (epi_pack_ext covers those).
 template <int OUT, int W>
-__device__ __forceinline__ void epi_pack(const GemmParams& p, int n, const float* v, float alpha, uint32_t* out) {
+__device__ __forceinline__ void epi_vals(const GemmParams& p, int n, const float* v, float alpha, float* y) {
   static_assert(W == 4 || W == 8, "group width");
-  float y[W];
   if ((p.flags & F_BIAS) && n < p.N) {
     float b[W];
     load_bias<OUT, W>(p, n, b);
@@ -283,7 +285,12 @@ __device__ __forceinline__ void epi_pack(const GemmParams& p, int n, const float
 #pragma unroll
     for (int i = 0; i < W; ++i) y[i] = __fmul_rn(alpha, v[i]);
   }
-  if (p.flags & F_SILU) silu_inplace(y);
+  if (p.flags & F_SILU) silu_inplace(reinterpret_cast<float(&)[W]>(*y));
+}
+template <int OUT, int W>
+__device__ __forceinline__ void epi_pack(const GemmParams& p, int n, const float* v, float alpha, uint32_t* out) {
+  float y[W];
+  epi_vals<OUT, W>(p, n, v, alpha, y);
 #pragma unroll
   for (int i = 0; i < W / 2; ++i) out[i] = pack2<OUT>(y[2 * i], y[2 * i + 1]);
 }
@@ -293,11 +300,11 @@ __device__ __forceinline__ void epi_pack(const GemmParams& p, int n, const float
 // alpha_m = row_alpha(alpha, m); c = the W values of C[m, n..] already loaded (cw: W/2 words of
 // two output-type values), read only with F_C.  Columns at or beyond N read nothing.
 template <int OUT, int W>
-__device__ __forceinline__ void epi_pack_ext(const GemmParams& p, int n, const float* v, float alpha_m,
-                                             const uint32_t* cw, uint32_t* out) {
+__device__ __forceinline__ void epi_vals_ext(const GemmParams& p, int n, const float* v, float alpha_m,
+                                             const uint32_t* cw, float* y) {
   static_assert(W == 4 || W == 8, "group width");
   const bool in = n < p.N;
-  float a[W], y[W];
+  float a[W];
 #pragma unroll
   for (int i = 0; i < W; ++i)
     a[i] = ((p.flags & F_ALPHA_COL) && in) ? __fmul_rn(alpha_m, __ldg(p.alpha_col + n + i)) : alpha_m;
@@ -315,7 +322,13 @@ __device__ __forceinline__ void epi_pack_ext(const GemmParams& p, int n, const f
 #pragma unroll
     for (int i = 0; i < W; ++i) y[i] = __fmaf_rn(p.beta, out_to_float<OUT>(c[i]), y[i]);
   }
-  if (p.flags & F_SILU) silu_inplace(y);
+  if (p.flags & F_SILU) silu_inplace(reinterpret_cast<float(&)[W]>(*y));
+}
+template <int OUT, int W>
+__device__ __forceinline__ void epi_pack_ext(const GemmParams& p, int n, const float* v, float alpha_m,
+                                             const uint32_t* cw, uint32_t* out) {
+  float y[W];
+  epi_vals_ext<OUT, W>(p, n, v, alpha_m, cw, y);
 #pragma unroll
   for (int i = 0; i < W / 2; ++i) out[i] = pack2<OUT>(y[2 * i], y[2 * i + 1]);
 }
@@ -338,13 +351,84 @@ __device__ __forceinline__ void load_c16(const GemmParams& p, int b, int m, int 
   }
 }
 
+// NVFP4 output (OUT_NV4): a row segment of 16*G accumulator values r (row m, columns n0.., n0 a
+// multiple of 16) through the epilogue (bias and C in BF16) and the NVFP4 block encoding with the
+// global scale *d_scale: 8 code bytes per 16 columns into D (row-major, N/2 bytes a row) and one
+// scale byte into SFD.  Every scale byte of the padded layout that the segment covers is written,
+// 0 for rows at or beyond M and columns at or beyond N, and the thread holding the row's last
+// block also zeroes the padding columns after its segment, so that the scale buffer is complete
+// for a GEMM that reads it.  Rows past M rounded up to 128 (a pair tile's) touch nothing.
+template <int G, bool EXT>
+__device__ __forceinline__ void epilogue_row_nv4(const GemmParams& p, int m, bool row_in, int n0, const uint32_t* r,
+                                                 float alpha) {
+  if (m >= ((p.M + 127) & ~127)) return;
+  const float s = __ldg(p.d_scale);
+  const float d = __fmul_rn(6.0f, s);
+  const int cols_pad = p.sfd_cols4 * 4;
+  uint8_t* drow = static_cast<uint8_t*>(p.d) + static_cast<size_t>(m) * (p.N >> 1);
+  const bool ext = EXT && (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW));
+  const float alpha_m = ext ? row_alpha(p, alpha, m) : alpha;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int n = n0 + 16 * g;
+    const int c = n >> 4;
+    uint32_t sc = 0;
+    if (row_in && n < p.N) {
+      float y[16];
+      const float* v = reinterpret_cast<const float*>(r + 16 * g);
+      if (ext) {
+        uint32_t cw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (p.flags & F_C) load_c16(p, 0, m, n, (p.flags & F_D32) != 0, cw);
+        epi_vals_ext<OUT_NV4, 8>(p, n, v, alpha_m, cw, y);
+        epi_vals_ext<OUT_NV4, 8>(p, n + 8, v + 8, alpha_m, cw + 4, y + 8);
+      } else {
+        epi_vals<OUT_NV4, 8>(p, n, v, alpha, y);
+        epi_vals<OUT_NV4, 8>(p, n + 8, v + 8, alpha, y + 8);
+      }
+      uint32_t lo, hi;
+      sc = nv_encode_block16(y, s, d, lo, hi);
+      *reinterpret_cast<uint2*>(drow + (n >> 1)) = make_uint2(lo, hi);
+    }
+    if (c < cols_pad) p.sfd[sf_swizzle_offset(m, c, p.sfd_cols4)] = static_cast<uint8_t>(sc);
+  }
+  const int last = (p.N >> 4) - 1;
+  if (last >= (n0 >> 4) && last < (n0 >> 4) + G)
+    for (int c = (n0 >> 4) + G; c < cols_pad; ++c) p.sfd[sf_swizzle_offset(m, c, p.sfd_cols4)] = 0;
+}
+
+// NVFP4 output of a thread's HC-column row segment straight from TMEM (t, its first column):
+// 32-column chunks (16 when HC is 16) loaded, encoded and stored one after another, so that few
+// values are live at once.  The caller releases the accumulator afterwards.
+template <int HC, bool EXT>
+__device__ __forceinline__ void nv4_segment(const GemmParams& p, uint32_t t, int m, bool row_in, int n0,
+                                            float alpha) {
+  if constexpr (HC < 32) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(t, r);
+    tmem_ld_wait();
+    epilogue_row_nv4<1, EXT>(p, m, row_in, n0, r, alpha);
+  } else {
+#pragma unroll 1
+    for (int ch = 0; ch < HC / 32; ++ch) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t + ch * 32, r);
+      tmem_ld_wait();
+      epilogue_row_nv4<2, EXT>(p, m, row_in, n0 + ch * 32, r, alpha);
+    }
+  }
+}
+
 // A row segment of 16*G accumulator values r (row m, columns n0.., n0 a multiple of 16) through
-// the epilogue into D: the plain path, or (C / per-column factors) the extended one, which loads
+// the epilogue into D: the NVFP4 output above, the plain path, or (C / per-column factors) the extended one, which loads
 // C one group of 16 columns ahead of the arithmetic.  The row is stored only if row_in
 // (row_live), and columns at or beyond N never.
 template <int OUT, int G, bool EXT>
 __device__ __forceinline__ void epilogue_row(const GemmParams& p, int b, int m, bool row_in, int n0,
                                              const uint32_t* r, float alpha) {
+  if constexpr (OUT == OUT_NV4) {
+    epilogue_row_nv4<G, EXT>(p, m, row_in, n0, r, alpha);
+    return;
+  }
   uint16_t* drow = d_row(p, b, m);
   const bool wide = p.flags & F_D32;
   if (!EXT || !(p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW))) {
@@ -891,7 +975,12 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
       const int nbase = c.n_blk * BN;
       if (p.split_mode == SPLIT_NONE) {
         uint16_t* drow = d_row(p, c.batch, m);
-        if constexpr (C::NACC == 1) {
+        if constexpr (OUT == OUT_NV4) {
+          nv4_segment<HC, EXT>(p, t_row + col0, m, row_in, nbase + col0, alpha);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty(acc));
+        } else if constexpr (C::NACC == 1) {
           // One accumulator: the whole row segment comes out of TMEM before any arithmetic and
           // the accumulator is released at once, since the next tile's MMAs need all of it.
           uint32_t r[HC];
@@ -953,7 +1042,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
             if (row_in && n < p.N) st_out16(drow + n, reinterpret_cast<const uint32_t(&)[8]>(packed[8 * g]), wide);
           }
         }
-      } else if constexpr (BN >= 64) {  // split-K is planned for tiles 64 columns wide or more
+      } else if constexpr (BN >= 64 && OUT != OUT_NV4) {  // split-K: tiles 64 wide or more, 16-bit out
         if (p.split_mode == SPLIT_CLUSTER) {
           // Split-K through the cluster (one unit per CTA).  Row `row` of the tile belongs to
           // split owner = lane / (32/S), so every warp holds rows of every owner.  Each thread

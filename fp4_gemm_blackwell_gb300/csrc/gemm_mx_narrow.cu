@@ -16,6 +16,9 @@ bool BSG_INST_NAME(gemm_kernel_info_mx_narrow)(int bn, int out, GemmKernelInfo* 
   if (bn == 32 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 32, 1, OUT_BF16, BSG_INST_EXT>(info);
   if (bn == 64 && out == OUT_F16) return fill_kernel_info<KIND_MX, 64, 1, OUT_F16, BSG_INST_EXT>(info);
   if (bn == 64 && out == OUT_BF16) return fill_kernel_info<KIND_MX, 64, 1, OUT_BF16, BSG_INST_EXT>(info);
+#ifdef BSG_INST_NV4
+  if (bn == 32 && out == OUT_NV4) return fill_kernel_info<KIND_MX, 32, 1, OUT_NV4, true>(info);
+#endif
   return false;
 }
 

@@ -1,7 +1,5 @@
 // NVFP4 (E2M1 elements, UE4M3 per-16 scales) instantiations of the block-scaled GEMM kernel.
-#include <cstdlib>
-
-#include "gemm_pair_kernel.cuh"
+#include "gemm_kernel.cuh"
 
 // Instantiated twice: here without the residual / factor epilogue and batch entries, and by the
 // _ext twin of this file (which defines these two macros and includes it) with them.
@@ -19,16 +17,9 @@ bool BSG_INST_NAME(gemm_kernel_info_nv)(int bn, int out, int kc, GemmKernelInfo*
   if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 128, 1, OUT_BF16, BSG_INST_EXT>(info);
   if (bn == 256 && out == OUT_F16) return fill_kernel_info<KIND_NV, 256, 1, OUT_F16, BSG_INST_EXT>(info);
   if (bn == 256 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 256, 1, OUT_BF16, BSG_INST_EXT>(info);
-  return false;
-}
-
-bool BSG_INST_NAME(gemm_pair_kernel_info_nv)(int out, GemmKernelInfo* info) {
-  const char* e = std::getenv("BSG_PAIR_KC");
-  const int kc = (e != nullptr && std::atoi(e) == 1) ? 1 : 2;  // two k-slabs per stage unless forced
-  if (kc == 2 && out == OUT_F16) return fill_pair_kernel_info<KIND_NV, 2, OUT_F16, BSG_INST_EXT>(info);
-  if (kc == 2 && out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, 2, OUT_BF16, BSG_INST_EXT>(info);
-  if (out == OUT_F16) return fill_pair_kernel_info<KIND_NV, 1, OUT_F16, BSG_INST_EXT>(info);
-  if (out == OUT_BF16) return fill_pair_kernel_info<KIND_NV, 1, OUT_BF16, BSG_INST_EXT>(info);
+#ifdef BSG_INST_NV4
+  if (bn == 256 && out == OUT_NV4) return fill_kernel_info<KIND_NV, 256, 1, OUT_NV4, true>(info);
+#endif
   return false;
 }
 

@@ -16,6 +16,10 @@ bool BSG_INST_NAME(gemm_kernel_info_nv_kc2)(int bn, int out, GemmKernelInfo* inf
   if (bn == 64 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 64, 2, OUT_BF16, BSG_INST_EXT>(info);
   if (bn == 128 && out == OUT_F16) return fill_kernel_info<KIND_NV, 128, 2, OUT_F16, BSG_INST_EXT>(info);
   if (bn == 128 && out == OUT_BF16) return fill_kernel_info<KIND_NV, 128, 2, OUT_BF16, BSG_INST_EXT>(info);
+#ifdef BSG_INST_NV4
+  if (bn == 64 && out == OUT_NV4) return fill_kernel_info<KIND_NV, 64, 2, OUT_NV4, true>(info);
+  if (bn == 128 && out == OUT_NV4) return fill_kernel_info<KIND_NV, 128, 2, OUT_NV4, true>(info);
+#endif
   return false;
 }
 

@@ -457,20 +457,28 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
       // The whole row segment comes out of TMEM before any arithmetic and the accumulator is
       // released at once: the next tile's MMAs need all of it, and holding it through the
       // epilogue math stalled them for longer than the math itself takes.
-      uint32_t r[HC];
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (is_leader)
+            mbar_arrive(bar_tempty);
+          else
+            tc_commit_pair_mc(bar_tempty, leader_mask);
+        }
+      };
+      if constexpr (OUT == OUT_NV4) {  // NVFP4 output: chunk by chunk from TMEM, then the release
+        nv4_segment<HC, EXT>(p, t_row + col0, m, m < p.M, nbase + col0, alpha);
+        release();
+      } else {
+        uint32_t r[HC];
 #pragma unroll
-      for (int ch = 0; ch < HC / 32; ++ch)
-        tmem_ld_32x32b_x32(t_row + col0 + ch * 32, reinterpret_cast<uint32_t(&)[32]>(r[32 * ch]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (is_leader)
-          mbar_arrive(bar_tempty);
-        else
-          tc_commit_pair_mc(bar_tempty, leader_mask);
+        for (int ch = 0; ch < HC / 32; ++ch)
+          tmem_ld_32x32b_x32(t_row + col0 + ch * 32, reinterpret_cast<uint32_t(&)[32]>(r[32 * ch]));
+        tmem_ld_wait();
+        release();
+        epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, m < p.M, nbase + col0, r, alpha);
       }
-      epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, m < p.M, nbase + col0, r, alpha);
       acc_phase ^= 1u;
     }
   }

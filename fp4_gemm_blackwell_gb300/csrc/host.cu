@@ -125,11 +125,22 @@ size_t sf_bytes_of(int kind, int rows, int K) {
 
 size_t code_row_bytes(int kind, int K) { return kind == bsg::KIND_MX ? K : K / 2; }
 
+int out_type(int out) {
+  return out == BSG_OUT_BF16 ? bsg::OUT_BF16 : (out == BSG_OUT_NVFP4 ? bsg::OUT_NV4 : bsg::OUT_F16);
+}
+
 bsg_status validate_desc(const bsg_desc* d) {
   if (d == nullptr) return fail(BSG_ERR_INVALID_ARG, "descriptor is null");
   if (d->kind != BSG_MXFP8 && d->kind != BSG_NVFP4) return fail(BSG_ERR_INVALID_ARG, "unknown kind %d", d->kind);
-  if (d->out != BSG_OUT_F16 && d->out != BSG_OUT_BF16)
-    return fail(BSG_ERR_DTYPE, "unsupported output type %d (FP16 or BF16 only)", d->out);
+  if (d->out != BSG_OUT_F16 && d->out != BSG_OUT_BF16 && d->out != BSG_OUT_NVFP4)
+    return fail(BSG_ERR_DTYPE, "unsupported output type %d (FP16, BF16 or NVFP4)", d->out);
+  if (d->out == BSG_OUT_NVFP4) {
+    if (!d->SFD || !d->d_scale) return fail(BSG_ERR_INVALID_ARG, "NVFP4 output needs SFD and d_scale");
+    if (!aligned16(d->SFD) || (reinterpret_cast<uintptr_t>(d->d_scale) & 3u))
+      return fail(BSG_ERR_ALIGNMENT, "SFD must be 16-byte and d_scale 4-byte aligned");
+    if (d->L > 1 || (d->flags & BSG_F_GROUPED))
+      return fail(BSG_ERR_SHAPE, "NVFP4 output is for single problems (no batches or groups)");
+  }
   if (d->flags &
       ~(BSG_F_BIAS | BSG_F_SILU | BSG_F_ALPHA_DEVICE | BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL | BSG_F_GROUPED))
     return fail(BSG_ERR_INVALID_ARG, "unknown flag bits 0x%x", d->flags);
@@ -203,7 +214,11 @@ bsg_status validate_ranges(const bsg_desc* d) {
   if ((s = check_range(d->SFB, span(d->stride_SFB, sf_bytes_of(d->kind, d->N, d->K)), BSG_ERR_SCALE_LAYOUT, "SFB")) !=
       BSG_OK)
     return s;
-  if ((s = check_range(d->D, span_a(d->stride_D, static_cast<size_t>(d->M) * d->N * 2), BSG_ERR_SHAPE, "D")) != BSG_OK)
+  const size_t d_bytes = static_cast<size_t>(d->M) * d->N * (d->out == BSG_OUT_NVFP4 ? 1 : 4) / 2;
+  if ((s = check_range(d->D, span_a(d->stride_D, d_bytes), BSG_ERR_SHAPE, "D")) != BSG_OK) return s;
+  if (d->out == BSG_OUT_NVFP4 &&
+      ((s = check_range(d->SFD, sf_bytes_of(bsg::KIND_NV, d->M, d->N), BSG_ERR_SCALE_LAYOUT, "SFD")) != BSG_OK ||
+       (s = check_range(d->d_scale, 4, BSG_ERR_SHAPE, "d_scale")) != BSG_OK))
     return s;
   if ((d->flags & BSG_F_BIAS) && (s = check_range(d->bias, static_cast<size_t>(d->N) * 2, BSG_ERR_SHAPE, "bias")) != BSG_OK)
     return s;
@@ -374,6 +389,12 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   }
   if (fs >= 1) s = std::min(fs, nkt);
   if (b < 64) s = 1;  // 32-wide tiles never split K
+  if (d->out == BSG_OUT_NVFP4 && s > 1) {
+    // the NVFP4 output is encoded by the row-segment epilogues only: no split-K, and 32-wide
+    // tiles in its place (the most tiles for few rows)
+    s = 1;
+    if (fb == 0) b = 32;
+  }
   // Two 128-byte k-slabs per ring stage halve the per-stage control (one barrier wait, one
   // commit, one scale staging per 8 MMAs) where the ring keeps three stages of the doubled size:
   // 64-wide tiles, and 128-wide tiles without a split-K receive area (measured: 128x4096x4096
@@ -502,9 +523,14 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->M = d->M;
   g->N = d->N;
   g->K = d->K;
-  // 32-byte stores (and loads of C) when D and, if read, C are 32-byte aligned
-  const bool d32 = (reinterpret_cast<uintptr_t>(d->D) & 31u) == 0 &&
+  // 32-byte stores (and loads of C) when D (16-bit output) and, if read, C are 32-byte aligned
+  const bool d32 = (d->out == BSG_OUT_NVFP4 || (reinterpret_cast<uintptr_t>(d->D) & 31u) == 0) &&
                    (!(d->flags & BSG_F_C) || (reinterpret_cast<uintptr_t>(d->C) & 31u) == 0);
+  if (d->out == BSG_OUT_NVFP4) {
+    g->sfd = static_cast<uint8_t*>(d->SFD);
+    g->d_scale = d->d_scale;
+    g->sfd_cols4 = (d->N / 16 + 3) / 4;
+  }
   g->flags = d->flags | (d32 ? bsg::F_D32 : 0u);
   g->c = (d->flags & BSG_F_C) ? d->C : nullptr;
   g->beta = d->beta;
@@ -593,7 +619,8 @@ bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, 
 
 namespace bsg {
 bool find_kernel(int kind, int out, unsigned flags, int batches, bool pair, int bn, int kc, GemmKernelInfo* info) {
-  const bool ext = (flags & (BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL | BSG_F_GROUPED)) != 0 || batches > 1;
+  const bool ext =
+      (flags & (BSG_F_C | BSG_F_ALPHA_ROW | BSG_F_ALPHA_COL | BSG_F_GROUPED)) != 0 || batches > 1 || out == OUT_NV4;
   return find_kernel_variant(kind, out, ext, pair, bn, kc, info);
 }
 bool find_kernel_variant(int kind, int out, bool ext, bool pair, int bn, int kc, GemmKernelInfo* info) {
@@ -622,10 +649,10 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
 
   const Variant v = choose_variant(d, di.sms);
   bsg::GemmKernelInfo info{};
-  const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
+  const int out_t = out_type(d->out);
   const bool found = bsg::find_kernel(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, d->flags, d->L,
                                       v.pair, v.bn, v.kc, &info);
-  if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
+  if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type / variant");
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
   bsg::GemmKernelInfo info_ext{};
   if (!bsg::find_kernel_variant(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, true, v.pair, v.bn, v.kc,
@@ -700,7 +727,8 @@ BSG_API const char* bsg_last_error(void) { return g_err.c_str(); }
 BSG_API const char* bsg_version(void) { return "bsgemm 0.1 (sm_103a)"; }
 
 BSG_API size_t bsg_sf_bytes(bsg_kind kind, int rows, int K) {
-  if ((kind != BSG_MXFP8 && kind != BSG_NVFP4) || rows < 1 || K < 32 || K % 32) return 0;
+  const int blk = kind == BSG_MXFP8 ? 32 : 16;
+  if ((kind != BSG_MXFP8 && kind != BSG_NVFP4) || rows < 1 || K < blk || K % blk) return 0;
   return sf_bytes_of(kind, rows, K);
 }
 
@@ -726,6 +754,8 @@ BSG_API bsg_status bsg_plan_run_operands(bsg_plan_t plan, const bsg_operands* op
   d.alpha_row = ops->alpha_row;
   d.alpha_col = ops->alpha_col;
   d.group_index = ops->group_index;
+  d.SFD = ops->SFD;
+  d.d_scale = ops->d_scale;
   bsg_status s = validate_desc(&d);
   if (s != BSG_OK) return s;
   if ((s = validate_ranges(&d)) != BSG_OK) return s;
@@ -739,9 +769,13 @@ BSG_API bsg_status bsg_plan_run_operands(bsg_plan_t plan, const bsg_operands* op
   g.alpha_row = (d.flags & BSG_F_ALPHA_ROW) ? d.alpha_row : nullptr;
   g.alpha_col = (d.flags & BSG_F_ALPHA_COL) ? d.alpha_col : nullptr;
   g.group_index = (d.flags & BSG_F_GROUPED) ? d.group_index : nullptr;
-  const bool d32 = (reinterpret_cast<uintptr_t>(d.D) & 31u) == 0 &&
+  const bool d32 = (d.out == BSG_OUT_NVFP4 || (reinterpret_cast<uintptr_t>(d.D) & 31u) == 0) &&
                    (!(d.flags & BSG_F_C) || (reinterpret_cast<uintptr_t>(d.C) & 31u) == 0);
   g.flags = (g.flags & ~bsg::F_D32) | (d32 ? bsg::F_D32 : 0u);
+  if (d.out == BSG_OUT_NVFP4) {
+    g.sfd = static_cast<uint8_t*>(d.SFD);
+    g.d_scale = d.d_scale;
+  }
   // The kernel writes its slots before its programmatic-launch wait, while the plan's previous
   // launch may still run: consecutive pointer-agnostic launches take alternate slot sets.
   g.map_slots = plan->map_slots + static_cast<size_t>(plan->remap_runs++ & 1u) * 2 * plan->grid;
@@ -1000,7 +1034,7 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
 
   const Variant v = choose_variant(d, di.sms);
   bsg::GemmKernelInfo info{};
-  const int out_t = d->out == BSG_OUT_BF16 ? bsg::OUT_BF16 : bsg::OUT_F16;
+  const int out_t = out_type(d->out);
   const bool found = bsg::find_kernel(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, d->flags, d->L,
                                       v.pair, v.bn, v.kc, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");

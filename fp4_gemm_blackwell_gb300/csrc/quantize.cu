@@ -15,15 +15,10 @@
 #include <cstdint>
 
 #include "bsg_internal.h"
+#include "nvfp4_codec.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
-
-// Byte offset of scale (r, c) in the swizzled buffer (cols4 = padded scale columns / 4).
-__device__ __forceinline__ size_t sf_swizzle_offset(int r, int c, int cols4) {
-  const size_t atom = static_cast<size_t>(r >> 7) * cols4 + (c >> 2);
-  return atom * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
-}
 
 // e = least integer with a <= 448 * 2^e, clamped to [-127, 127], for finite a >= 0.
 // With a = (1 + f) 2^(E-127) (E the biased exponent field) and 448 = 1.75 * 2^8:
@@ -134,13 +129,6 @@ __global__ void __launch_bounds__(256) amax_kernel(const T* __restrict__ x, long
   }
 }
 
-// E4M3 code with the sign bit clear -> exact float value.
-__device__ __forceinline__ float ue4m3_value(uint32_t code) {
-  const uint32_t e = (code >> 3) & 0xFu, m = code & 7u;
-  if (e == 0) return static_cast<float>(m) * 0x1p-9f;
-  return __uint_as_float(((e + 120u) << 23) | (m << 20));
-}
-
 template <typename T>
 __global__ void __launch_bounds__(256) quantize_nv_kernel(const T* __restrict__ x, int rows, int K,
                                                           uint8_t* __restrict__ codes,
@@ -161,37 +149,8 @@ __global__ void __launch_bounds__(256) quantize_nv_kernel(const T* __restrict__ 
     if (r < rows && c < nblk) {
       float v[16];
       load_f32(x + static_cast<size_t>(r) * K + c * 16, v);
-      float bmax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(v[j]));
-      const float t = (d != 0.0f) ? __fdiv_rn(bmax, d) : 0.0f;
-      const uint32_t sc = cvt_e4m3x2(t, 0.0f) & 0x7Fu;
-      const float den = __fmul_rn(ue4m3_value(sc), s);
-      // Element = E2M1(RN(x / den)), reached without a division per element: p = RN(x * RN(1/den))
-      // is within 2^-22.4 of x/den relative (and so of RN(x/den)), and E2M1 rounding is monotone,
-      // so when p (1 - 2^-21) and p (1 + 2^-21) round to the same code, that is the code of
-      // RN(x/den).  Pairs that straddle a rounding threshold, and blocks whose den or 1/den is
-      // not a normal float32, take the IEEE division.
-      const bool fast = den >= 0x1p-126f && den <= 0x1p126f;
-      const float inv = fast ? __frcp_rn(den) : 0.0f;
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t byte = 0;
-        if (den != 0.0f) {
-          bool exact = !fast;
-          if (fast) {
-            const float p0 = __fmul_rn(v[2 * j], inv), p1 = __fmul_rn(v[2 * j + 1], inv);
-            const uint32_t below = cvt_e2m1x2(__fmul_rn(p0, 1.0f - 0x1p-21f), __fmul_rn(p1, 1.0f - 0x1p-21f)) & 0xFFu;
-            const uint32_t above = cvt_e2m1x2(__fmul_rn(p0, 1.0f + 0x1p-21f), __fmul_rn(p1, 1.0f + 0x1p-21f)) & 0xFFu;
-            byte = below;
-            exact = below != above;
-          }
-          if (exact) byte = cvt_e2m1x2(__fdiv_rn(v[2 * j], den), __fdiv_rn(v[2 * j + 1], den)) & 0xFFu;
-        }
-        if (j < 4) lo |= byte << (8 * j);
-        else hi |= byte << (8 * (j - 4));
-      }
+      uint32_t lo, hi;
+      const uint32_t sc = nv_encode_block16(v, s, d, lo, hi);
       *reinterpret_cast<uint2*>(codes + static_cast<size_t>(r) * (K / 2) + c * 8) = make_uint2(lo, hi);
       code = static_cast<uint8_t>(sc);
     }

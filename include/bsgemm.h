@@ -65,7 +65,12 @@ typedef enum {
 } bsg_status;
 
 typedef enum { BSG_MXFP8 = 0, BSG_NVFP4 = 1 } bsg_kind;
-typedef enum { BSG_OUT_F16 = 0, BSG_OUT_BF16 = 1 } bsg_out;
+/* NVFP4: D holds packed E2M1 codes (M x N/2 bytes, row-major, element 2j in the low nibble
+ * of byte j) and SFD its UE4M3 block scales (one per 16 columns) in the swizzled 128x4 layout of
+ * the scale operands (bsg_sf_bytes(BSG_NVFP4, M, N) bytes, padding written as zeros), quantised
+ * with the global scale *d_scale by the recipe of bsg_quantize: ready to be the A operand of an
+ * NVFP4 GEMM whose K is this N (its alpha then carries *d_scale). */
+typedef enum { BSG_OUT_F16 = 0, BSG_OUT_BF16 = 1, BSG_OUT_NVFP4 = 2 } bsg_out;
 
 /* Epilogue flags.  BIAS and SILU are the kEnableBias / kEnableSilu switches of
  * runNvfp4Gemm; ALPHA_DEVICE reads alpha from device memory at run time, the
@@ -114,7 +119,12 @@ typedef struct bsg_plan_s* bsg_plan_t;
  * outside 0..L-1) is skipped whole, and a row whose group differs from its block's is not
  * stored.  So each group's rows start on a multiple of 128 and are padded with -1 rows to the
  * next one.  stride_A, stride_SFA, stride_D and stride_C are ignored.  Grouped problems run on
- * 128-row tiles (no CTA pairs). */
+ * 128-row tiles (no CTA pairs).
+ * NVFP4 output (out = BSG_OUT_NVFP4, single problems only): SFD (16-byte aligned) and d_scale
+ * (one float, device memory, 4-byte aligned) are required; bias and C are BF16.  Each
+ * 16-column block of y (the value before the output rounding above) is quantised in float32:
+ * scale = UE4M3(amax / (6 s)), elements E2M1(y / (scale s)), s = *d_scale.  Such a problem is
+ * never split along K. */
 typedef struct {
   bsg_kind kind;
   bsg_out out;
@@ -135,6 +145,8 @@ typedef struct {
   int L;
   long long stride_A, stride_B, stride_SFA, stride_SFB, stride_D, stride_C;
   const int* group_index;
+  void* SFD;
+  const float* d_scale;
 } bsg_desc;
 
 /* Validate d, choose the kernel variant (tile shape, split-K), encode the TMA tensor
@@ -165,6 +177,8 @@ typedef struct {
   const float* alpha_row;
   const float* alpha_col;
   const int* group_index;
+  void* SFD;
+  const float* d_scale;
 } bsg_operands;
 
 /* Pointer-agnostic run: enqueue the plan's GEMM on `ops`' buffers, which must have the
@@ -219,7 +233,8 @@ bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream);
 bsg_status bsg_cache_clear(void);
 
 /* Bytes of the swizzled scale buffer of a rows x K operand: 128*ceil(rows/128) *
- * 4*ceil((K/blk)/4), blk = 32 (MXFP8) or 16 (NVFP4).  0 for invalid arguments. */
+ * 4*ceil((K/blk)/4), blk = 32 (MXFP8) or 16 (NVFP4).  K must be a multiple of blk (so an
+ * NVFP4 output's N, a multiple of 16, is accepted).  0 for invalid arguments. */
 size_t bsg_sf_bytes(bsg_kind kind, int rows, int K);
 
 /* Quantise a row-major float32 matrix x (rows x K, device) on `stream`:

@@ -27,13 +27,19 @@ with C kept separate; their order is this library's documented reading.
 
 The scales are read from the swizzled buffers through ``layout.unswizzle`` so
 that the byte map of the scale layout is exercised end to end.
+
+NVFP4 output (the output half of the activation-quantiser step that the MXFP8
+page's test performs before each GEMM): instead of rounding y to a 16-bit type,
+each 16-column block of a row goes through the NVFP4 recipe of ``quantize`` with
+a given global scale s, on y taken in float32 (the precision the recipe states);
+``quantize_output_nvfp4``.
 """
 
 import numpy as np
 
 from . import formats as F
 from . import layout as L
-from .quantize import MX_BLOCK, NV_BLOCK, unpack_e2m1
+from .quantize import MX_BLOCK, NV_BLOCK, quantize_nvfp4, unpack_e2m1
 
 MXFP8 = "mxfp8"
 NVFP4 = "nvfp4"
@@ -151,3 +157,11 @@ def gemm_naive(kind, A, B, SFA, SFB, M, N, K, alpha=1.0, bias=None, silu=False, 
                 t += float(Ahat[m, k]) * float(Bhat[n, k])
             acc[m, n] = t
     return epilogue(acc, alpha, bias, silu, C, beta, alpha_row, alpha_col)
+
+
+def quantize_output_nvfp4(y, s):
+    """NVFP4 output of the epilogue: y (float64 [M, N], the values before output rounding) in
+    float32, then per 16-column block of a row the NVFP4 recipe with global scale s.
+    Returns (packed E2M1 codes uint8 [M, N/2], UE4M3 scale codes uint8 [M, N/16])."""
+    codes, scales, _ = quantize_nvfp4(np.asarray(y, dtype=np.float64).astype(np.float32), np.float32(s))
+    return codes, scales

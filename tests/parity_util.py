@@ -10,6 +10,7 @@ import torch
 
 import fp4_gemm_blackwell_gb300 as bsg
 from fp4_gemm_blackwell_gb300 import synth
+from oracle import formats as F
 from oracle import gemm as R
 from oracle import layout as L
 from oracle import quantize as Q
@@ -141,3 +142,57 @@ def assert_parity(got, prob, out, bias_vals=None, silu=False, rows=None, epi=Non
         detail = ", ".join("(%d,%d) got %r ref %r tol %.3g" % (i, j, got[i, j], ref[i, j], tol[i, j]) for i, j in idx)
         raise AssertionError("%d of %d outputs outside tolerance: %s" % (bad.sum(), bad.size, detail))
     return float(np.max(err / np.maximum(tol, 1e-300)))
+
+
+def check_nvfp4_output(codes, sfbuf, prob, bias_vals, silu, s, epi=None, min_agree=0.99):
+    """NVFP4 output of a GEMM (codes: M x N/2 bytes; sfbuf: the whole swizzled scale buffer)
+    against the oracle's pre-rounding y, whose GPU counterpart differs from it by the
+    accumulation error:
+    (1) every scale code is one the recipe gives for a block amax within the tolerance (r11,
+        without the output rounding) of the oracle's, and, given the GPU's scale, every element
+        code one it gives for a value within the tolerance of the oracle's y;
+    (2) at least `min_agree` of the scale codes and of the element codes equal the oracle's
+        quantisation of its own y (only values near a rounding threshold can differ);
+    (3) the padding of the scale layout (rows past M, scale columns past N/16) is zero.
+    Returns the two agreement fractions."""
+    p = prob
+    M, N, K = p["M"], p["N"], p["K"]
+    nb = N // 16
+    ep = epi or {}
+    _, y = R.reference(p["kind"], p["A"], p["B"], p["SFA"], p["SFB"], M, N, K, alpha=p["alpha"], bias=bias_vals,
+                       silu=silu, out="bf16", **ep)
+    abs_sum = R.abs_product_sum(p["kind"], p["A"], p["B"], p["SFA"], p["SFB"], M, N, K)
+    alpha = p["alpha"]
+    if ep.get("alpha_row") is not None or ep.get("alpha_col") is not None:
+        alpha = np.broadcast_to(R.effective_alpha(alpha, ep.get("alpha_row"), ep.get("alpha_col")), y.shape)
+    tol = R.tolerance(y, y, abs_sum, alpha, silu, "bf16")
+    s32 = np.float32(s)
+    d = np.float32(np.float32(6.0) * s32)
+    sc_gpu = L.unswizzle(sfbuf, M, nb)
+    el_gpu = Q.unpack_e2m1(np.asarray(codes).reshape(M, N // 2), N)
+    q_codes, q_sc = R.quantize_output_nvfp4(y, s32)
+    agree_sc = float(np.mean(sc_gpu == q_sc))
+    agree_el = float(np.mean(el_gpu == Q.unpack_e2m1(q_codes, N)))
+    assert agree_sc >= min_agree and agree_el >= min_agree, (agree_sc, agree_el)
+    # (1) intervals, widened by 2^-20 relative for the float32 steps of the bounds themselves
+    w = 2.0 ** -20
+    yb, tb = y.reshape(M, nb, 16), tol.reshape(M, nb, 16)
+    lo = np.maximum(np.abs(yb) - tb, 0.0).max(axis=2) * (1 - w)
+    hi = (np.abs(yb) + tb).max(axis=2) * (1 + w)
+    c_lo = F.encode_ue4m3((lo / np.float64(d)).astype(np.float32))
+    c_hi = F.encode_ue4m3((hi / np.float64(d)).astype(np.float32))
+    bad = (sc_gpu < c_lo) | (sc_gpu > c_hi)
+    assert not bad.any(), "scale codes outside their intervals at %s" % np.argwhere(bad)[:5].tolist()
+    den = (F.decode_ue4m3(sc_gpu).astype(np.float32) * s32).astype(np.float64)
+    den16 = np.repeat(den, 16, axis=1)
+    safe = np.where(den16 > 0, den16, 1.0)
+    v_lo = F.decode_e2m1(F.encode_e2m1(((y - tol) / safe) * (1 - w * np.sign(y - tol))))
+    v_hi = F.decode_e2m1(F.encode_e2m1(((y + tol) / safe) * (1 + w * np.sign(y + tol))))
+    v_gpu = F.decode_e2m1(el_gpu)
+    bad = np.where(den16 > 0, (v_gpu < v_lo) | (v_gpu > v_hi), v_gpu != 0)
+    assert not bad.any(), "element codes outside their intervals at %s" % np.argwhere(bad)[:5].tolist()
+    # (3) padding
+    rp, cp = (M + 127) // 128 * 128, (nb + 3) // 4 * 4
+    full = L.unswizzle(sfbuf, rp, cp)
+    assert not full[M:].any() and not full[:, nb:].any(), "scale padding not zero"
+    return agree_sc, agree_el

@@ -49,6 +49,8 @@ def test_version_and_sf_bytes(L):
     assert bsg.bsg_sf_bytes(bsg.BSG_MXFP8, 1, 160) == 128 * 8
     assert bsg.bsg_sf_bytes(bsg.BSG_MXFP8, 0, 32) == 0
     assert bsg.bsg_sf_bytes(bsg.BSG_MXFP8, 4, 48) == 0
+    assert bsg.bsg_sf_bytes(bsg.BSG_NVFP4, 300, 272) == 384 * 20   # an NVFP4 output's N: 17 blocks
+    assert bsg.bsg_sf_bytes(bsg.BSG_NVFP4, 4, 40) == 0
     assert bsg.bsg_sf_bytes(7, 4, 64) == 0
 
 

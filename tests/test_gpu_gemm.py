@@ -502,3 +502,65 @@ def test_run_operands(kind, env, monkeypatch):
     assert np.array_equal(got2, got2b), variant
     if "BSG_FORCE_PAIR" in env:
         assert "pair" in variant, variant
+
+
+@pytest.mark.parametrize("env", [{}, {"BSG_FORCE_BN": 64}, {"BSG_FORCE_BN": 128}, {"BSG_FORCE_BN": 256},
+                                 {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 32, "BSG_FORCE_CM": 4},
+                                 {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2}])
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_nvfp4_output(kind, env, monkeypatch):
+    # D written as NVFP4 (E2M1 codes + swizzled UE4M3 scales, global scale from the device) by
+    # every kernel family; M and N ragged (N/16 = 17 scale columns: 3 of padding), bias (+ SiLU),
+    # and with some families the residual and both factor vectors.  Checked by intervals and
+    # agreement against the oracle's quantisation of its own result, the scale padding zero, the
+    # buffers' margins untouched; a forced split-K does not apply; a pointer-agnostic run into
+    # second buffers gives the same bytes.
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    M, N, K = 300, 272, 1024
+    silu = kind == "nvfp4"
+    prob = P.make_problem(kind, M, N, K, seed_a=7, seed_b=8)
+    extra = env.get("BSG_FORCE_BN") in (64, 256)
+    bias_bits, bias_vals = synth.bias(N, out="bf16")
+    bias = P.dev(bias_bits.view(np.int16)).view(torch.int16)
+    epi, C, ar, ac = None, None, None, None
+    if extra:
+        cbits, cvals = P.synth_residual(M, N, "bf16", seed=11)
+        rng = np.random.default_rng(12)
+        arv = rng.uniform(0.5, 2.0, M).astype(np.float32)
+        acv = rng.uniform(0.5, 2.0, N).astype(np.float32)
+        C = P.dev(cbits.view(np.int16)).view(torch.int16)
+        ar, ac = P.dev(arv).view(torch.float32), P.dev(acv).view(torch.float32)
+        epi = dict(C=cvals, beta=0.5, alpha_row=arv, alpha_col=acv)
+    _, y = R.reference(kind, prob["A"], prob["B"], prob["SFA"], prob["SFB"], M, N, K, alpha=prob["alpha"],
+                       bias=bias_vals, silu=silu, out="bf16", **(epi or {}))
+    s = np.float32(np.float32(np.max(np.abs(y))) / np.float32(2688.0))   # the recipe's tensor scale
+    d_scale = torch.tensor([float(s)], dtype=torch.float32, device="cuda")
+    nsf = bsg.bsg_sf_bytes(bsg.BSG_NVFP4, M, N)
+    assert nsf == 384 * 20
+    pad = 256
+
+    def buffers():
+        dbuf = torch.full((M * N // 2 + 2 * pad,), 0xCD, dtype=torch.uint8, device="cuda")
+        sbuf = torch.full((nsf + 2 * pad,), 0xAB, dtype=torch.uint8, device="cuda")
+        return dbuf, sbuf, dbuf[pad:pad + M * N // 2], sbuf[pad:pad + nsf]
+
+    dbuf, sbuf, D, SFD = buffers()
+    dbuf2, sbuf2, D2, SFD2 = buffers()
+    A, B, SFA, SFB = P.dev(prob["A"]), P.dev(prob["B"]), P.dev(prob["SFA"]), P.dev(prob["SFB"])
+    flags = bsg.BSG_F_BIAS | (bsg.BSG_F_SILU if silu else 0)
+    if extra:
+        flags |= bsg.BSG_F_C | bsg.BSG_F_ALPHA_ROW | bsg.BSG_F_ALPHA_COL
+    with bsg.Plan(P.KIND[kind], bsg.BSG_OUT_NVFP4, M, N, K, A, B, SFA, SFB, D, alpha=float(prob["alpha"]),
+                  flags=flags, bias=bias, C=C, beta=0.5, alpha_row=ar, alpha_col=ac, SFD=SFD, d_scale=d_scale) as plan:
+        variant = plan.variant
+        plan.run()
+        plan.run_operands(A, B, SFA, SFB, D2, bias=bias, C=C, alpha_row=ar, alpha_col=ac, SFD=SFD2, d_scale=d_scale)
+        plan.check_status()
+    torch.cuda.synchronize()
+    assert "_s1" in variant or "pair" in variant, variant
+    db, sb = dbuf.cpu().numpy(), sbuf.cpu().numpy()
+    assert np.all(db[:pad] == 0xCD) and np.all(db[-pad:] == 0xCD), "D margins written (%s)" % variant
+    assert np.all(sb[:pad] == 0xAB) and np.all(sb[-pad:] == 0xAB), "SFD margins written (%s)" % variant
+    P.check_nvfp4_output(db[pad:-pad], sb[pad:-pad], prob, bias_vals, silu, s, epi=epi)
+    assert np.array_equal(dbuf2.cpu().numpy(), db) and np.array_equal(sbuf2.cpu().numpy(), sb), variant

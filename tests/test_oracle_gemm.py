@@ -209,3 +209,56 @@ def test_naive_loop_matches_with_residual_and_factors():
     _, y = R.reference(R.NVFP4, ap, bp, L.swizzle(sfa), L.swizzle(sfb), M, N, K, **kw)
     y2 = R.gemm_naive(R.NVFP4, ap, bp, L.swizzle(sfa), L.swizzle(sfb), M, N, K, **kw)
     assert np.allclose(y, y2, rtol=1e-13, atol=1e-15)
+
+
+def test_nvfp4_output_closed_form():
+    # The NVFP4 output of the epilogue with s = 1 (d = 6): a block whose largest magnitude is 6
+    # has scale UE4M3(1) = 0x38 and elements E2M1(y) directly; a block twice as large has scale
+    # 0x40 (2) and elements E2M1(y / 2), its 12.000000001 taken as float32 12; a zero block has
+    # scale and codes 0; and s = 0 zeroes everything.
+    idx = {v: i for i, v in enumerate(E2M1_LIST)}
+    vals = [6, 0.5, -1, 1.5, 2, -3, 4, 0.25, 0, 1, -0.5, 3, -6, 2, 1.5, -4]
+    # 0.25, the tie between 0 and 0.5, goes to the even code 0
+    want = [(idx[abs(v)] | (8 if v < 0 else 0)) if abs(v) != 0.25 else 0 for v in vals]
+    y = np.zeros((1, 48))
+    y[0, :16] = vals
+    y[0, 16:32] = 2 * np.array(vals, dtype=np.float64)
+    y[0, 16] = 12.000000001
+    codes, scales = R.quantize_output_nvfp4(y, 1.0)
+    assert scales.tolist() == [[0x38, 0x40, 0x00]]
+    packed = [want[2 * j] | (want[2 * j + 1] << 4) for j in range(8)]
+    assert codes[0, :8].tolist() == packed
+    assert codes[0, 8:16].tolist() == packed
+    assert codes[0, 16:].tolist() == [0] * 8
+    codes0, scales0 = R.quantize_output_nvfp4(y, 0.0)
+    assert not codes0.any() and not scales0.any()
+
+
+def test_nvfp4_output_checker_catches_planted_mistakes():
+    # The NVFP4-output parity check of the GPU tests, run on the oracle's own output (it must
+    # pass, agreeing everywhere) and on that output with a mistake planted: every byte's nibbles
+    # swapped, every block scale one code up (both caught by the agreement test), one element
+    # code pushed to +-6 where the oracle has 0 (caught by its interval), a nonzero padding
+    # byte past M.  Each must fail.
+    import parity_util as P
+    M, N, K = 130, 48, 64
+    prob = P.make_problem("nvfp4", M, N, K, seed_a=7, seed_b=8)
+    bias = np.zeros(N)
+    _, y = R.reference("nvfp4", prob["A"], prob["B"], prob["SFA"], prob["SFB"], M, N, K, alpha=prob["alpha"],
+                       bias=bias, silu=True, out="bf16")
+    s = np.float32(np.float32(np.max(np.abs(y))) / np.float32(2688.0))
+    codes, scales = R.quantize_output_nvfp4(y, s)
+    buf = L.swizzle(scales)
+    assert P.check_nvfp4_output(codes.ravel(), buf, prob, bias, True, s) == (1.0, 1.0)
+    swapped = ((codes & 0xF) << 4) | (codes >> 4)
+    planted = [(swapped.ravel(), buf), (codes.ravel(), L.swizzle(scales + 1))]
+    c = codes.copy()
+    j = int(np.flatnonzero((c & 0xF) == 0)[0])               # an element (low nibble) coded 0
+    c.flat[j] = (c.flat[j] & 0xF0) | 0x7
+    planted.append((c.ravel(), buf))
+    b2 = buf.copy()
+    b2[L.sf_offset(np.array([M + 1]), np.array([0]), N // 16)] = 0x38   # a row past M
+    planted.append((codes.ravel(), b2))
+    for cd, sb in planted:
+        with pytest.raises(AssertionError):
+            P.check_nvfp4_output(cd, sb, prob, bias, True, s)
