@@ -529,6 +529,40 @@ def remap_config(bsg, peaks, steps=400, warmup=10):
     return r
 
 
+def nvfp4_out_config(bsg, peaks, M, N, K, steps, warmup=5):
+    """NVFP4 GEMM M x N x K with bias + SiLU whose output is NVFP4 (codes + swizzled scales, a
+    device global scale): the form in which one layer's GEMM feeds the next.  Inputs rotate
+    over enough copies to exceed L2; bytes count the NVFP4 output instead of a 16-bit one."""
+    from fp4_gemm_blackwell_gb300 import synth
+    k = bsg.BSG_NVFP4
+    sfd_bytes = bsg.bsg_sf_bytes(k, M, N)
+    one = M * K // 2 + N * K // 2 + bsg.bsg_sf_bytes(k, M, K) + bsg.bsg_sf_bytes(k, N, K) + M * N // 2 + sfd_bytes
+    cp = copies_to_exceed_l2(one)
+    bits, _ = synth.bias(N, out="bf16")
+    bias_t = torch.from_numpy(bits.view(np.int16)).cuda()
+    d_scale = torch.tensor([0.05], dtype=torch.float32, device="cuda")
+    plans, keep = [], []
+    for i in range(cp):
+        a = Operands(bsg, "nvfp4", M, K, 30 + i)
+        b = Operands(bsg, "nvfp4", N, K, 60 + i)
+        d = torch.empty(M * N // 2, dtype=torch.uint8, device="cuda")
+        sfd = torch.empty(sfd_bytes, dtype=torch.uint8, device="cuda")
+        keep += [a, b, d, sfd]
+        alpha = float(np.float32(np.float32(a.s) * np.float32(b.s)))
+        plans.append(bsg.Plan(k, bsg.BSG_OUT_NVFP4, M, N, K, a.codes, b.codes, a.sf, b.sf, d, alpha=alpha,
+                              flags=bsg.BSG_F_BIAS | bsg.BSG_F_SILU, bias=bias_t, SFD=sfd, d_scale=d_scale))
+    ms, _ = graph_time(plans, steps, warmup)
+    us = ms * 1e3 / steps
+    tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+    gbs = (one + 2 * N) / (us * 1e-6) / 1e9
+    r = {"us": round(us, 3), "tflops": round(tf, 1), "frac_of_fp4_peak": round(tf / tensor_peak(peaks, "nvfp4"), 4),
+         "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": one + 2 * N,
+         "variant": plans[0].variant, "copies": cp}
+    for pl in plans:
+        pl.close()
+    return r
+
+
 def small_config(bsg, peaks, steps=2000, warmup=20):
     prob = Problem(bsg, "mxfp8", 256, 256, 256, copies=64)
     ms, _ = graph_time(prob.plans, steps, warmup)
@@ -842,6 +876,8 @@ def main():
                 extras["nvfp4_batched_l%d_m128_n4096_k4096" % L] = batched_config(bsg, peaks, L)
             extras["nvfp4_grouped_8x4096x4096_moe"] = grouped_config(bsg, peaks)
             extras["nvfp4_m128_pointer_agnostic"] = remap_config(bsg, peaks)
+            extras["nvfp4_m128_nvfp4_out"] = nvfp4_out_config(bsg, peaks, M1, N1, K1, steps=400)
+            extras["nvfp4_8192_nvfp4_out"] = nvfp4_out_config(bsg, peaks, 8192, 8192, 8192, steps=20)
             extras["launch_loop_1000"] = launch_loop(bsg)
             for kind in ("mxfp8", "nvfp4"):
                 for bf in (False, True):
