@@ -975,7 +975,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
       const int nbase = c.n_blk * BN;
       if (p.split_mode == SPLIT_NONE) {
         uint16_t* drow = d_row(p, c.batch, m);
-        if constexpr (OUT == OUT_NV4) {
+        if constexpr (OUT == OUT_NV4 && C::NACC == 2) {
+          // NVFP4 output beside a second accumulator: chunk by chunk from TMEM, then the release
+          // (with one accumulator the path below drains, releases, then encodes, so that the next
+          // tile's MMAs do not wait for the encoding)
           nv4_segment<HC, EXT>(p, t_row + col0, m, row_in, nbase + col0, alpha);
           tc_fence_before();
           __syncwarp();

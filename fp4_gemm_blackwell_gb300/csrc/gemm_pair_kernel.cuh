@@ -467,18 +467,15 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
             tc_commit_pair_mc(bar_tempty, leader_mask);
         }
       };
-      if constexpr (OUT == OUT_NV4) {  // NVFP4 output: chunk by chunk from TMEM, then the release
-        nv4_segment<HC, EXT>(p, t_row + col0, m, m < p.M, nbase + col0, alpha);
-        release();
-      } else {
-        uint32_t r[HC];
+      // (the NVFP4 output too: holding the only accumulator through its encoding stalled the next
+      // tile's MMAs, 8192^3 315 us against 180 us with a 16-bit output)
+      uint32_t r[HC];
 #pragma unroll
-        for (int ch = 0; ch < HC / 32; ++ch)
-          tmem_ld_32x32b_x32(t_row + col0 + ch * 32, reinterpret_cast<uint32_t(&)[32]>(r[32 * ch]));
-        tmem_ld_wait();
-        release();
-        epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, m < p.M, nbase + col0, r, alpha);
-      }
+      for (int ch = 0; ch < HC / 32; ++ch)
+        tmem_ld_32x32b_x32(t_row + col0 + ch * 32, reinterpret_cast<uint32_t(&)[32]>(r[32 * ch]));
+      tmem_ld_wait();
+      release();
+      epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, m < p.M, nbase + col0, r, alpha);
       acc_phase ^= 1u;
     }
   }
