@@ -57,12 +57,12 @@ def test_version_and_sf_bytes(L):
 def _plan_status(L, **kw):
     base = dict(kind=0, out=1, flags=0, M=128, N=128, K=128, A=16, B=32, SFA=48, SFB=64, bias=None,
                 D=80, alpha=1.0, alpha_dev=None, C=None, beta=0.0, alpha_row=None, alpha_col=None, batches=0,
-                strides=(0, 0, 0, 0, 0, 0), group_index=None)
+                strides=(0, 0, 0, 0, 0, 0), group_index=None, SFD=None, d_scale=None)
     base.update(kw)
     d = bsg.BsgDesc(base["kind"], base["out"], base["flags"], base["M"], base["N"], base["K"], base["A"],
                     base["B"], base["SFA"], base["SFB"], base["bias"], base["D"], base["alpha"], base["alpha_dev"],
                     base["C"], base["beta"], base["alpha_row"], base["alpha_col"], base["batches"], *base["strides"],
-                    base["group_index"])
+                    base["group_index"], base["SFD"], base["d_scale"])
     h = ctypes.c_void_p()
     st = L.bsg_plan_create(ctypes.byref(h), ctypes.byref(d))
     assert h.value is None
@@ -85,6 +85,12 @@ def _plan_status(L, **kw):
     (dict(flags=64), 2), (dict(flags=64, batches=4), 1), (dict(flags=64, batches=4, group_index=6), 3),
     (dict(flags=64, batches=4, group_index=256, strides=(0, 16384 - 16, 0, 2048, 0, 0)), 2),
     (dict(flags=64, batches=4, group_index=256, strides=(0, 16384, 0, 512 - 16, 0, 0)), 2),
+    # NVFP4 output: an unknown output type; no SFD or d_scale; a misaligned SFD or d_scale;
+    # batches or groups with it
+    (dict(out=3), 5), (dict(out=2), 1), (dict(out=2, SFD=96), 1), (dict(out=2, d_scale=100), 1),
+    (dict(out=2, SFD=104, d_scale=100), 3), (dict(out=2, SFD=96, d_scale=102), 3),
+    (dict(out=2, SFD=96, d_scale=100, batches=2, strides=(16384, 16384, 512, 512, 16384, 0)), 2),
+    (dict(out=2, SFD=96, d_scale=100, flags=64, batches=2, group_index=256, strides=(0, 16384, 0, 512, 0, 0)), 2),
 ])
 def test_invalid_descriptors_are_rejected_before_device_work(L, kw, status):
     assert _plan_status(L, **kw) == status
