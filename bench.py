@@ -563,6 +563,18 @@ def nvfp4_out_config(bsg, peaks, M, N, K, steps, warmup=5):
     return r
 
 
+def l2_warm_config(bsg, peaks, steps=2000, warmup=20):
+    """The headline workload with ONE input set, so that after the first launch its operands
+    are L2-resident: the L2-warm number, reported beside the HBM-cold headline as context."""
+    prob = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=1)
+    ms, _ = graph_time(prob.plans, steps, warmup)
+    us = ms * 1e3 / steps
+    r = {"us": round(us, 3), "tflops": round(prob.flops() / (us * 1e-6) / 1e12, 1), "l2": "warm (one input set)",
+         "variant": prob.variant}
+    prob.close()
+    return r
+
+
 def small_config(bsg, peaks, steps=2000, warmup=20):
     prob = Problem(bsg, "mxfp8", 256, 256, 256, copies=64)
     ms, _ = graph_time(prob.plans, steps, warmup)
@@ -864,6 +876,7 @@ def main():
         e2e_r = e2e(bsg, min(200, args.steps))
         if not args.quick:
             extras["mxfp8_256_bf16"] = small_config(bsg, peaks)
+            extras["nvfp4_m128_l2_warm"] = l2_warm_config(bsg, peaks)
             extras["mxfp8_8192_bf16"] = big_config(bsg, peaks, "mxfp8", 8192, 8192, 8192, "bf16", False, False)
             extras["mxfp8_8192_f16"] = big_config(bsg, peaks, "mxfp8", 8192, 8192, 8192, "f16", False, False)
             extras["nvfp4_8192_bias_silu_bf16"] = big_config(bsg, peaks, "nvfp4", 8192, 8192, 8192, "bf16", True, True)

@@ -5,7 +5,10 @@
 // the same calls replayed from a captured CUDA graph, and host time per call of that replay.
 // Then one plan of the 128 x 4096 x 4096 shape: host time per call of bsg_plan_run, and of
 // bsg_plan_run_operands alternating between two buffer sets (the pointer-agnostic run, which
-// checks every buffer against its allocation).  Operands are quantised on the device by
+// checks every buffer against its allocation).  Then, as context, the per-call host path that the
+// launch-overhead page profiles: bsg_gemm_noalloc, which validates, chooses the variant and
+// encodes both tensor maps on every call, and the same with a driver entry-point lookup of
+// cuTensorMapEncodeTiled before every call.  Operands are quantised on the device by
 // bsg_quantize from a deterministic pattern.
 #include <cuda_runtime.h>
 
@@ -153,14 +156,29 @@ int main() {
   const double o1 = now_us();
   cudaStreamSynchronize(stream);
   bsg_plan_destroy(plan);
+  for (int i = 0; i < 20; ++i) bad += bsg_gemm_noalloc(&d, st) != BSG_OK;  // first call finds the scratch
+  cudaStreamSynchronize(stream);
+  const double n0 = now_us();
+  for (int i = 0; i < calls; ++i) bad += bsg_gemm_noalloc(&d, st) != BSG_OK;
+  const double n1 = now_us();
+  cudaStreamSynchronize(stream);
+  const double x0 = now_us();
+  for (int i = 0; i < calls; ++i) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    bad += bsg_gemm_noalloc(&d, st) != BSG_OK;
+  }
+  const double x1 = now_us();
+  cudaStreamSynchronize(stream);
   const cudaError_t err = cudaGetLastError();
   const double kernel_us = ms * 1000.0 / calls;
   std::printf("{\"calls\": %d, \"shapes\": %d, \"host_us_per_call\": %.3f, \"wall_us_per_call\": %.3f, "
               "\"kernel_us_per_call\": %.3f, \"graph_host_us_per_call\": %.4f, \"host_over_kernel\": %.4f, "
-              "\"plan_run_host_us\": %.3f, \"plan_run_operands_host_us\": %.3f, \"operands_errors\": %d, "
-              "\"cuda\": \"%s\"}\n",
+              "\"plan_run_host_us\": %.3f, \"plan_run_operands_host_us\": %.3f, \"reencode_host_us\": %.3f, "
+              "\"reencode_and_lookup_host_us\": %.3f, \"errors\": %d, \"cuda\": \"%s\"}\n",
               calls, static_cast<int>(cl.size()), (t1 - t0) / calls, (t2 - t0) / calls, kernel_us,
-              (g1 - g0) / calls, (t1 - t0) / calls / kernel_us, (r1 - r0) / calls, (o1 - o0) / calls, bad,
-              cudaGetErrorString(err));
+              (g1 - g0) / calls, (t1 - t0) / calls / kernel_us, (r1 - r0) / calls, (o1 - o0) / calls,
+              (n1 - n0) / calls, (x1 - x0) / calls, bad, cudaGetErrorString(err));
   return err == cudaSuccess ? 0 : 1;
 }
