@@ -384,6 +384,17 @@ def dist_setup(n_gpus):
     return 0, 1, 0, None
 
 
+def whole_job(ms_local, flops_per_step, steps, world, dist=None, device="cuda"):
+    """The timed region's maximum over ranks (ms) and the whole-job throughput in TFLOPS: every
+    rank's `steps` steps of `flops_per_step`, over that maximum."""
+    ms_max = ms_local
+    if dist is not None:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, flops_per_step * steps * world / (ms_max * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- the other workloads
 def tensor_peak(peaks, kind):
     return peaks["bf16_tflops"] * NOMINAL_RATIO["fp8" if kind == "mxfp8" else "fp4"]
@@ -861,13 +872,7 @@ def main():
     h = headline(bsg, args.steps, args.warmup, barrier)
     clocks = sampler.stop() if rank == 0 else None
     prob = h["problem"]
-    ms_max = h["ms"]
-    if dist:
-        t = torch.tensor([h["ms"]], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    total_flops = prob.flops() * args.steps * world
-    value = total_flops / (ms_max * 1e-3) / 1e12
+    ms_max, value = whole_job(h["ms"], prob.flops(), args.steps, world, dist)
     kernel_us = h["ms"] * 1e3 / args.steps
     achieved = prob.algorithmic_bytes() / (kernel_us * 1e-6) / 1e9
     result = None
