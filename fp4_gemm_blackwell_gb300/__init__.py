@@ -199,10 +199,15 @@ def nvfp4_gemm(D, A, B, SFA, SFB, bias, alpha, flags, M, N, K, out, stream=None)
 
 
 def bsg_gemm_noalloc(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None,
-                     stream=None, C=None, beta=0.0, alpha_row=None, alpha_col=None):
-    """Allocation-free GEMM (no device allocation; shares one static scratch array per GPU)."""
+                     stream=None, C=None, beta=0.0, alpha_row=None, alpha_col=None, L=0, strides=None,
+                     group_index=None, SFD=None, d_scale=None):
+    """Allocation-free GEMM (no device allocation; shares one static scratch array per GPU).
+    The descriptor fields are those of bsg_plan_create."""
+    st = strides or {}
     d = BsgDesc(kind, out, flags, M, N, K, _ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(bias), _ptr(D),
-                alpha, _ptr(alpha_dev), _ptr(C), beta, _ptr(alpha_row), _ptr(alpha_col))
+                alpha, _ptr(alpha_dev), _ptr(C), beta, _ptr(alpha_row), _ptr(alpha_col), L,
+                *(st.get(k, 0) for k in ("stride_A", "stride_B", "stride_SFA", "stride_SFB", "stride_D", "stride_C")),
+                _ptr(group_index), _ptr(SFD), _ptr(d_scale))
     _check(lib().bsg_gemm_noalloc(ctypes.byref(d), _stream(stream)))
 
 
