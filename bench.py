@@ -159,6 +159,23 @@ class Operands:
         return c
 
 
+def algorithmic_bytes(kind, M, N, K, bias=False, residual=False, factors=False, L=1):
+    """Bytes one launch must move at least: codes + padded scales of A and B, the 16-bit output,
+    and the bias, C and factor vectors when used (L entries of everything but the bias and
+    factors, which the entries share)."""
+    cb = 1 if kind == "mxfp8" else 0.5
+    blk = 32 if kind == "mxfp8" else 16
+    sf = lambda rows: ((rows + 127) // 128 * 128) * ((K // blk + 3) // 4 * 4)
+    b = L * (M * K * cb + N * K * cb + sf(M) + sf(N) + M * N * 2)
+    if bias:
+        b += N * 2
+    if residual:
+        b += L * M * N * 2
+    if factors:
+        b += (M + N) * 4
+    return int(b)
+
+
 class Problem:
     """R device copies of one GEMM problem (operands, bias, output) with a plan per copy."""
 
@@ -215,19 +232,8 @@ class Problem:
         return 2.0 * self.M * self.N * self.K * self.L
 
     def algorithmic_bytes(self):
-        """Bytes one launch must move at least: codes + scales of A and B, bias, output (of all
-        L entries; bias and factors are shared by the entries)."""
-        cb = 1 if self.kind == "mxfp8" else 0.5
-        blk = 32 if self.kind == "mxfp8" else 16
-        sf = lambda rows: ((rows + 127) // 128 * 128) * ((self.K // blk + 3) // 4 * 4)
-        b = self.L * (self.M * self.K * cb + self.N * self.K * cb + sf(self.M) + sf(self.N) + self.M * self.N * 2)
-        if self.flags & 1:
-            b += self.N * 2
-        if self.residual:
-            b += self.L * self.M * self.N * 2
-        if self.factors:
-            b += (self.M + self.N) * 4
-        return int(b)
+        return algorithmic_bytes(self.kind, self.M, self.N, self.K, bias=bool(self.flags & 1),
+                                 residual=self.residual, factors=self.factors, L=self.L)
 
     def close(self):
         for p in self.plans:

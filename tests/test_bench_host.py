@@ -58,3 +58,27 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
     import bench
     monkeypatch.setenv("RANK", "1")
     assert bench.reference_arm(argparse.Namespace(steps=1, warmup=3, gpus=2)) == 0
+
+
+def test_algorithmic_bytes_of_the_measured_configurations():
+    # the per-launch byte counts the rooflines divide by, against the sums spelled out term by
+    # term: codes of A and B, their padded scales, the bias and the 16-bit output
+    sys.path.insert(0, ROOT)
+    import bench
+    # NVFP4 128 x 4096 x 4096 + bias: 262,144 + 32,768 + 8,388,608 + 1,048,576 + 8,192 + 1,048,576
+    assert bench.algorithmic_bytes("nvfp4", 128, 4096, 4096, bias=True) == 10_788_864
+    # MXFP8 256^3: 65,536 + 2,048 + 65,536 + 2,048 + 131,072
+    assert bench.algorithmic_bytes("mxfp8", 256, 256, 256) == 266_240
+    # MXFP8 8192^3: two 64 MiB code matrices, two 2 MiB scale buffers, a 128 MiB output
+    assert bench.algorithmic_bytes("mxfp8", 8192, 8192, 8192) == 2 * 67_108_864 + 2 * 2_097_152 + 134_217_728
+    # NVFP4 8192^3 + bias
+    assert bench.algorithmic_bytes("nvfp4", 8192, 8192, 8192, bias=True) == \
+        2 * 33_554_432 + 2 * 4_194_304 + 16_384 + 134_217_728
+    # ragged M: A's scales padded to 8064 rows
+    assert bench.algorithmic_bytes("nvfp4", 8000, 8192, 8192) == \
+        8000 * 4096 + 8192 * 4096 + 8064 * 512 + 8192 * 512 + 8000 * 8192 * 2
+    # residual and factors; L entries
+    base = bench.algorithmic_bytes("nvfp4", 128, 4096, 4096, bias=True)
+    assert bench.algorithmic_bytes("nvfp4", 128, 4096, 4096, bias=True, residual=True, factors=True) == \
+        base + 128 * 4096 * 2 + (128 + 4096) * 4
+    assert bench.algorithmic_bytes("nvfp4", 128, 4096, 4096, bias=True, L=8) == 8 * (base - 8192) + 8192
