@@ -127,3 +127,34 @@ def test_one_shot_validation(L):
     # N not a multiple of 16 and a device alpha through the host-alpha call are refused
     assert L.mxfp8_gemm(16, 32, 48, 64, 80, ctypes.c_float(1.0), 128, 120, 128, 1, None) == 2
     assert L.nvfp4_gemm(16, 32, 48, 64, 80, None, ctypes.c_float(1.0), 4, 128, 128, 128, 1, None) == 1
+
+
+def test_python_structures_match_the_header_layout():
+    # bsg_desc and bsg_operands as the C compiler lays them out from include/bsgemm.h (a probe
+    # built with gcc under the git-ignored _build/) against the ctypes structures of the binding:
+    # the same size and every field at the same offset, so that appended fields cannot drift.
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = os.path.join(root, "_build", "abi_layout")
+    os.makedirs(out, exist_ok=True)
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "bsgemm.h"', "int main(void) {"]
+    for cname, py in (("bsg_desc", bsg.BsgDesc), ("bsg_operands", bsg.BsgOperands)):
+        lines.append('  printf("%s %%zu\\n", sizeof(%s));' % (cname, cname))
+        for field, _ in py._fields_:
+            lines.append('  printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (cname, field, cname, field))
+    lines += ["  return 0;", "}"]
+    src = os.path.join(out, "layout.c")
+    exe = os.path.join(out, "layout")
+    with open(src, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    subprocess.run([gcc, "-std=c11", "-I", os.path.join(root, "include"), src, "-o", exe], check=True)
+    got = dict(line.split() for line in subprocess.run([exe], check=True, capture_output=True,
+                                                       text=True).stdout.splitlines())
+    for cname, py in (("bsg_desc", bsg.BsgDesc), ("bsg_operands", bsg.BsgOperands)):
+        assert int(got[cname]) == ctypes.sizeof(py), cname
+        for field, _ in py._fields_:
+            assert int(got["%s.%s" % (cname, field)]) == getattr(py, field).offset, (cname, field)
