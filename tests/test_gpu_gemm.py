@@ -564,3 +564,30 @@ def test_nvfp4_output(kind, env, monkeypatch):
     assert np.all(sb[:pad] == 0xAB) and np.all(sb[-pad:] == 0xAB), "SFD margins written (%s)" % variant
     P.check_nvfp4_output(db[pad:-pad], sb[pad:-pad], prob, bias_vals, silu, s, epi=epi)
     assert np.array_equal(dbuf2.cpu().numpy(), db) and np.array_equal(sbuf2.cpu().numpy(), sb), variant
+
+
+@pytest.mark.parametrize("env", [{}, {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2}, {"BSG_FORCE_PAIR": 1}])
+def test_batched_device_alpha_per_entry(env, monkeypatch):
+    # L = 3 NVFP4 problems whose global factors differ (each entry's s_A * s_B): with
+    # BSG_F_ALPHA_DEVICE, alpha_dev holds one alpha per entry, and each entry matches its own
+    # oracle result with its own alpha
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    L, M, N, K = 3, 300, 144, 1024
+    probs, A, B, SFA, SFB, D, _, _, strides = _batched_buffers("nvfp4", L, M, N, K)
+    alphas = np.array([p["alpha"] for p in probs], dtype=np.float32)
+    assert len(set(alphas.tolist())) == L
+    ad = torch.from_numpy(alphas).cuda()
+    with bsg.Plan(bsg.BSG_NVFP4, bsg.BSG_OUT_BF16, M, N, K, A, B, SFA, SFB, D, flags=bsg.BSG_F_ALPHA_DEVICE,
+                  alpha_dev=ad, L=L, strides=strides) as plan:
+        variant = plan.variant
+        plan.run()
+        plan.check_status()
+    torch.cuda.synchronize()
+    dall = D.cpu().numpy().view(np.uint16)
+    sD = strides["stride_D"] // 2
+    for l, p in enumerate(probs):
+        got = R.out_from_bits(dall[l * sD:l * sD + M * N].reshape(M, N), "bf16")
+        P.assert_parity(got, p, "bf16")
+    if "BSG_FORCE_PAIR" in env:
+        assert "pair" in variant, variant
