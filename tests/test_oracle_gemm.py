@@ -262,3 +262,39 @@ def test_nvfp4_output_checker_catches_planted_mistakes():
     for cd, sb in planted:
         with pytest.raises(AssertionError):
             P.check_nvfp4_output(cd, sb, prob, bias, True, s)
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_parity_tolerance_catches_plausible_mistakes(kind):
+    # The element-wise tolerance of the GPU parity tests (r11) must not hide a real mistake: the
+    # oracle's own output passes, and that output computed with a mistake planted fails: B's
+    # rows in the wrong order, alpha doubled, SiLU left out, the result transposed.  A bias
+    # shifted by one column is caught where the accumulation term of the bound vanishes (A all
+    # zero: D = round(silu(bias)) up to one output ulp); next to a full accumulation, a bias of
+    # N(0, 0.1) sits below 2^-7 sum|a b| and a shift is not visible.
+    import parity_util as P
+    M, N, K = 64, 64, 256
+    prob = P.make_problem(kind, M, N, K, seed_a=21, seed_b=22)
+    bias_bits, bias_vals = synth.bias(N, out="bf16")
+    silu = True
+    ref, _ = P.reference(prob, "bf16", bias_vals, silu)
+    P.assert_parity(ref, prob, "bf16", bias_vals, silu)
+
+    def out(p, **kw):
+        q = dict(p)
+        q.update(kw.pop("prob", {}))
+        return P.reference(q, "bf16", kw.get("bias", bias_vals), kw.get("silu", silu))[0]
+
+    perm = np.roll(np.arange(N), 1)
+    sfb_lin = L.unswizzle(prob["SFB"], N, K // (32 if kind == "mxfp8" else 16))
+    wrong_b = dict(B=prob["B"][perm], SFB=L.swizzle(sfb_lin[perm]))
+    planted = [out(prob, prob=wrong_b), out(prob, prob=dict(alpha=np.float32(2 * prob["alpha"]))),
+               out(prob, silu=False), ref.T.copy()]
+    for got in planted:
+        with pytest.raises(AssertionError):
+            P.assert_parity(got, prob, "bf16", bias_vals, silu)
+    zero = dict(prob, A=np.zeros_like(prob["A"]))
+    zref = out(zero)
+    P.assert_parity(zref, zero, "bf16", bias_vals, silu)
+    with pytest.raises(AssertionError):
+        P.assert_parity(out(zero, bias=np.roll(bias_vals, 1)), zero, "bf16", bias_vals, silu)
