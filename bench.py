@@ -2,19 +2,20 @@
 
 Headline workload (one step = one GEMM through the library's plan, operands already
 quantised and resident in HBM):
-    NVFP4 GEMM M=128, N=4096, K=4096, BF16 bias + SiLU, BF16 out (skinny M, HBM-bound).
-Metric: block-scaled GEMM TFLOPS (2*M*N*K per step); extras in the same JSON line give
-the roofline of the dominant kernel, the host microseconds per call against the kernel
-time, the end-to-end number through the C ABI with host buffers, the other workloads
-(MXFP8 256^3, MXFP8 8192^3 FP16/BF16, NVFP4 8192^3 and 8000x8192x8192, the launch loop)
-and the CPU oracle timed on this machine's host cores.
+    NVFP4 GEMM M=N=K=8192, BF16 bias + SiLU, BF16 out (tensor-bound: the configuration the
+    pages' "% of dense block-scaled tensor peak" target is stated at).
+Metric: block-scaled GEMM TFLOPS (2*M*N*K per step) and its fraction of the FP4 tensor peak;
+the same JSON line gives the host microseconds per call against the kernel time, the end-to-end
+number through the C ABI with host buffers, the other workloads (the skinny-M HBM-bound NVFP4
+128x4096x4096 with its HBM roofline, MXFP8 256^3, MXFP8 8192^3 FP16/BF16, NVFP4
+8000x8192x8192, the launch loop, ...) and the CPU oracle timed on this machine's host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--quick]
 
-Inputs rotate over enough copies that the operands of a step are not in L2 from the
-previous use (the copies together exceed the 129 MB L2).  Timed regions are bracketed by
-torch.cuda.synchronize (and a barrier with N > 1) and measured with CUDA events on the
-stream the kernels are launched on.
+Inputs rotate over copies whose bytes together exceed the 129 MB L2 (for the headline: two
+copies of 75 MB of operands and a 134 MB output each), so a step's operands are not in L2 from
+the previous use.  Timed regions are bracketed by torch.cuda.synchronize (and a barrier with
+N > 1) and measured with CUDA events on the stream the kernels are launched on.
 """
 
 import argparse
@@ -33,7 +34,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-M1, N1, K1 = 128, 4096, 4096          # the headline workload
+MH, NH, KH = 8192, 8192, 8192         # the headline workload (NVFP4, bias + SiLU, BF16 out)
+M1, N1, K1 = 128, 4096, 4096          # the skinny-M workload (HBM-bound)
 L2_BYTES = 129 * 1024 * 1024
 SM_COUNT_DEFAULT = 152
 
@@ -117,7 +119,7 @@ class ClockSampler:
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp4_gemm_blackwell_gb300", "csrc")
-    for name in ("gemm_kernel.cuh", "ptx.cuh", "bsg_internal.h"):
+    for name in ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "nvfp4_codec.cuh", "ptx.cuh", "bsg_internal.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -300,26 +302,48 @@ def stream_time(plans, steps, warmup):
 
 # ---------------------------------------------------------------- the headline step
 def headline(bsg, steps, warmup, barrier):
+    """The headline GEMM, two operand / output copies (420 MB together, above the L2) in turn."""
+    prob = Problem(bsg, "nvfp4", MH, NH, KH, bias=True, silu=True, copies=2)
+    ms, launches = graph_time(prob.plans, steps, warmup, barrier)
+    stream_ms, host_us = stream_time(prob.plans, min(steps, 1000), warmup)
+    return dict(problem=prob, ms=ms, launches=launches, copies=2, per_copy=prob.algorithmic_bytes(),
+                stream_kernel_us=stream_ms * 1e3 / min(steps, 1000), host_us_per_run=host_us)
+
+
+def skinny_headline(bsg, peaks, steps=400, warmup=10):
+    """NVFP4 128 x 4096 x 4096 with bias + SiLU (skinny M, HBM-bound), inputs rotated over enough
+    copies to exceed L2: kernel time, host time per plan run and the HBM roofline."""
     probe = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=1)
     per_copy = probe.algorithmic_bytes()
     probe.close()
     copies = copies_to_exceed_l2(per_copy)
     prob = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=copies)
-    ms, launches = graph_time(prob.plans, steps, warmup, barrier)
+    ms, _ = graph_time(prob.plans, steps, warmup)
     stream_ms, host_us = stream_time(prob.plans, min(steps, 1000), warmup)
-    out = dict(problem=prob, ms=ms, launches=launches, copies=copies, per_copy=per_copy,
-               stream_kernel_us=stream_ms * 1e3 / min(steps, 1000), host_us_per_run=host_us)
-    return out
+    us = ms * 1e3 / steps
+    gbs = per_copy / (us * 1e-6) / 1e9
+    r = {"us": round(us, 3), "tflops": round(prob.flops() / (us * 1e-6) / 1e12, 1), "variant": prob.variant,
+         "l2": "inputs rotate over %d copies (%.0f MB > 129 MB L2)" % (copies, copies * per_copy / 2 ** 20),
+         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": round(gbs / peaks["hbm_gbs"], 4),
+                      "traffic": recorded_traffic("bsg_gemm_kernel<nvfp4,%s>" % prob.variant.split("_")[1],
+                                                  "nvfp4_m128_n4096_k4096"),
+                      "algorithmic_bytes_per_launch": per_copy,
+                      "peak_source": peaks["source"] + " hbm_gbs (burst copy)"},
+         "host_us_per_plan_run": round(host_us, 3), "kernel_us_stream_back_to_back": round(stream_ms * 1e3 / min(
+             steps, 1000), 3)}
+    prob.close()
+    return r
 
 
-def e2e(bsg, steps):
-    """Same workload through the one-shot C-ABI call, host buffers in and out every step: each
+def e2e(bsg, steps, M=MH, N=NH, K=KH):
+    """The workload through the one-shot C-ABI call, host buffers in and out every step: each
     step copies its A, SFA, B, SFB and bias from pinned host memory (one copy: the five inputs
     sit at 256-byte-aligned offsets of one block), runs nvfp4_gemm and copies D back to pinned
     host memory.  Steps are pipelined the way a serving loop would run them: two device buffer
     sets, the copy in (copy stream), the GEMM (compute stream) and the copy out (a third stream)
     of consecutive steps overlap; every copy of every step is inside the timed region."""
-    prob = Problem(bsg, "nvfp4", M1, N1, K1, bias=True, silu=True, copies=1)
+    prob = Problem(bsg, "nvfp4", M, N, K, bias=True, silu=True, copies=1)
     a0, b0, bias0, d0 = prob.sets[0]
     parts = [a0.codes, a0.sf, b0.codes, b0.sf, bias0]
     offs, total = [], 0
@@ -354,7 +378,7 @@ def e2e(bsg, steps):
         s_comp.wait_event(ev[i]["in"])
         s_comp.wait_event(ev[i]["out"])          # this set's previous result has left the GPU
         st = L.nvfp4_gemm(d.data_ptr(), base + offs[0], base + offs[2], base + offs[1], base + offs[3],
-                          base + offs[4], alpha, flags, M1, N1, K1, bsg.BSG_OUT_BF16, s_comp.cuda_stream)
+                          base + offs[4], alpha, flags, M, N, K, bsg.BSG_OUT_BF16, s_comp.cuda_stream)
         if st != 0:
             raise bsg.BsgError(st, bsg.bsg_last_error())
         ev[i]["comp"].record(s_comp)
@@ -372,7 +396,7 @@ def e2e(bsg, steps):
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     bsg.bsg_cache_clear()
-    tflops = 2.0 * M1 * N1 * K1 * steps / dt / 1e12
+    tflops = 2.0 * M * N * K * steps / dt / 1e12
     return {"value": round(tflops, 4), "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3 / steps, 4), "steps": steps,
             "h2d_gbs": round(h2d * steps / dt / 1e9, 1),
@@ -728,71 +752,70 @@ def native_launch_loop():
 
 
 # ---------------------------------------------------------------- the CPU oracle
-def oracle_problem():
-    """The headline problem's operands quantised by the CPU oracle (setup, untimed)."""
+def oracle_sample(rows, cols):
+    """Operands of a rows x cols block of the headline problem's output, quantised by the CPU
+    oracle (setup, untimed): the first `rows` rows of A and `cols` rows of B over the full K, each
+    with the NVFP4 tensor scale of its whole 8192 x 8192 matrix (the oracle's own function)."""
     from fp4_gemm_blackwell_gb300 import synth
     from oracle import layout as OL
     from oracle import quantize as OQ
-    xa = synth.normal_rowscaled(M1, K1, synth.SEED_A)
-    xb = synth.normal_rowscaled(N1, K1, synth.SEED_B)
-    a, sfa, sa = OQ.quantize_nvfp4(xa)
-    b, sfb, sb = OQ.quantize_nvfp4(xb)
-    _, bias = synth.bias(N1)
-    return dict(A=a, B=b, sfa=sfa, sfb=sfb, SFA=OL.swizzle(sfa), SFB=OL.swizzle(sfb),
-                alpha=np.float32(np.float32(sa) * np.float32(sb)), bias=bias)
+    xa = synth.normal_rowscaled(MH, KH, synth.SEED_A)
+    xb = synth.normal_rowscaled(NH, KH, synth.SEED_B)
+    sa, sb = OQ.nvfp4_global_scale(xa), OQ.nvfp4_global_scale(xb)
+    a, sfa, _ = OQ.quantize_nvfp4(xa[:rows], sa)
+    b, sfb, _ = OQ.quantize_nvfp4(xb[:cols], sb)
+    _, bias = synth.bias(NH)
+    return dict(A=a, B=b, SFA=OL.swizzle(sfa), SFB=OL.swizzle(sfb), rows=rows, cols=cols,
+                alpha=np.float32(np.float32(sa) * np.float32(sb)), bias=bias[:cols])
+
+
+def oracle_block(p):
+    """One evaluation of the oracle (table decode, float64 GEMM, bias, SiLU, BF16 rounding) on a
+    sample block; returns its FLOPs."""
+    from oracle import gemm as OG
+    OG.reference(OG.NVFP4, p["A"], p["B"], p["SFA"], p["SFB"], p["rows"], p["cols"], KH, alpha=p["alpha"],
+                 bias=p["bias"], silu=True, out=OG.BF16)
+    return 2.0 * p["rows"] * p["cols"] * KH
 
 
 def cpu_baseline(budget_s=10.0):
-    """The oracle as it stands (decode through its tables, FP64 GEMM, epilogue, rounding) on the
-    whole headline problem, repeated until about `budget_s` seconds of CPU work."""
-    from oracle import gemm as OG
-    p = oracle_problem()
-    reps, t0 = 0, time.perf_counter()
+    """The oracle as it stands on a bounded sample of the headline workload: a 64 x 256 block of
+    the 8192^3 output over the full K, repeated until about `budget_s` seconds of CPU work."""
+    p = oracle_sample(64, 256)
+    reps, flops, t0 = 0, 0.0, time.perf_counter()
     while True:
-        OG.reference(OG.NVFP4, p["A"], p["B"], p["SFA"], p["SFB"], M1, N1, K1, alpha=p["alpha"],
-                     bias=p["bias"], silu=True, out=OG.BF16)
+        flops += oracle_block(p)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s:
             break
-    tf = reps * 2.0 * M1 * N1 * K1 / dt / 1e12
+    tf = flops / dt / 1e12
     return {"value": round(tf, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "%d full NVFP4 M=128 N=4096 K=4096 problems (table decode, float64 numpy matmul, bias, "
-                      "SiLU, BF16 rounding) in %.1f s; numpy's BLAS uses all %d host threads"
-                      % (reps, dt, os.cpu_count())}
+            "sample": "%d evaluations of a 64 x 256 output block of NVFP4 8192^3 (full K = 8192; table decode, "
+                      "float64 numpy matmul, bias, SiLU, BF16 rounding) in %.1f s; numpy's BLAS uses all %d host "
+                      "threads" % (reps, dt, os.cpu_count())}
 
 
 def reference_arm(args):
-    """--impl reference: the CPU oracle is the reference implementation on this workload.  A step
-    is a bounded sample: a 128 x 16 block of the output over the full K."""
-    from oracle import gemm as OG
-    from oracle import layout as OL
+    """--impl reference: the CPU oracle is the reference implementation of this workload.  A step
+    is a bounded sample of it: a 32 x 64 block of the 8192^3 output over the full K."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    p = oracle_problem()
-    cols = 16
-    B = p["B"][:cols]
-    SFB = OL.swizzle(p["sfb"][:cols])
-    bias = p["bias"][:cols]
-
-    def step():
-        OG.reference(OG.NVFP4, p["A"], B, p["SFA"], SFB, M1, cols, K1, alpha=p["alpha"], bias=bias, silu=True,
-                     out=OG.BF16)
-
+    p = oracle_sample(32, 64)
     for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
+        oracle_block(p)
+    flops, t0 = 0.0, time.perf_counter()
     for _ in range(args.steps):
-        step()
+        flops += oracle_block(p)
     dt = time.perf_counter() - t0
-    flops = 2.0 * M1 * cols * K1 * args.steps
     tf = flops / dt / 1e12
-    sample = "per step a 128 x %d output block of NVFP4 M=128 N=4096 K=4096 (bias+SiLU, BF16) by the float64 oracle" % cols
+    sample = ("per step a 32 x 64 output block of NVFP4 8192^3 (full K, bias + SiLU, BF16) by the float64 "
+              "oracle on %d host cores" % os.cpu_count())
     line = {"impl": "reference", "metric": METRIC, "value": round(tf, 6), "unit": "TFLOPS", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "M": M1, "N": N1, "K": K1},
+            "data": "synthetic", "config": headline_config(),
             "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(tf, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -846,7 +869,13 @@ def case_arm(args):
 
 
 METRIC = "block-scaled GEMM TFLOPS & % tensor peak (MXFP8, NVFP4); host µs/call vs kernel"
-WORKLOAD = "nvfp4_gemm M=128 N=4096 K=4096, bf16 bias + SiLU, bf16 out"
+WORKLOAD = "nvfp4_gemm M=N=K=8192, bf16 bias + SiLU, bf16 out"
+
+
+def headline_config():
+    """The headline's `config`, the same in both arms."""
+    return {"workload": WORKLOAD, "M": MH, "N": NH, "K": KH,
+            "l2": "operands and output rotate over 2 copies (420 MB > 129 MB L2)"}
 
 
 def main():
@@ -883,17 +912,18 @@ def main():
     prob = h["problem"]
     ms_max, value = whole_job(h["ms"], prob.flops(), args.steps, world, dist)
     kernel_us = h["ms"] * 1e3 / args.steps
-    achieved = prob.algorithmic_bytes() / (kernel_us * 1e-6) / 1e9
+    achieved = prob.flops() / (kernel_us * 1e-6) / 1e12          # TFLOP/s of the one kernel per step
+    peak = tensor_peak(peaks, "nvfp4")
     result = None
     if rank == 0:
         extras = {}
         e2e_r = e2e(bsg, min(200, args.steps))
         if not args.quick:
+            extras["nvfp4_m128_n4096_k4096_bias_silu"] = skinny_headline(bsg, peaks)
             extras["mxfp8_256_bf16"] = small_config(bsg, peaks)
             extras["nvfp4_m128_l2_warm"] = l2_warm_config(bsg, peaks)
             extras["mxfp8_8192_bf16"] = big_config(bsg, peaks, "mxfp8", 8192, 8192, 8192, "bf16", False, False)
             extras["mxfp8_8192_f16"] = big_config(bsg, peaks, "mxfp8", 8192, 8192, 8192, "f16", False, False)
-            extras["nvfp4_8192_bias_silu_bf16"] = big_config(bsg, peaks, "nvfp4", 8192, 8192, 8192, "bf16", True, True)
             extras["nvfp4_8000x8192x8192_bias_silu_bf16"] = big_config(bsg, peaks, "nvfp4", 8000, 8192, 8192, "bf16",
                                                                        True, True)
             extras["nvfp4_8192_bias_silu_residual_factors_bf16"] = big_config(
@@ -915,16 +945,17 @@ def main():
             "metric": METRIC, "value": round(value, 4), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 6), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32 accumulate", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M1, "N": N1, "K": K1, "variant": prob.variant,
-                       "l2": "inputs rotate over %d copies (%.0f MB > 129 MB L2)" % (h["copies"], h["copies"] * h["per_copy"] / 2 ** 20),
-                       "timing": "CUDA events around one CUDA-graph replay of the K plan launches",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": recorded_traffic("bsg_gemm_kernel<nvfp4,%s>" % prob.variant.split("_")[1],
-                                                     "nvfp4_m128_n4096_k4096"),
-                         "algorithmic_bytes_per_launch": prob.algorithmic_bytes(),
-                         "kernel_us": round(kernel_us, 3), "peak_source": peaks["source"] + " hbm_gbs (burst copy)"},
+            "config": headline_config(),
+            "variant": prob.variant,
+            "timing": "CUDA events around one CUDA-graph replay of the K plan launches",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": recorded_traffic("bsg_gemm_pair_kernel<nvfp4>", "nvfp4_8192_bias_silu"),
+                         "flops_per_launch": prob.flops(), "algorithmic_bytes_per_launch": prob.algorithmic_bytes(),
+                         "kernel_us": round(kernel_us, 3),
+                         "peak_source": "%s bf16_tflops %.1f (burst cuBLAS GEMM) x 6, the nominal dense FP4 / BF16 "
+                                        "ratio 13.5 / 2.25" % (peaks["source"], peaks["bf16_tflops"])},
             "host_us_per_call": {"plan_run_stream": round(h["host_us_per_run"], 3),
                                  "kernel_us_stream_back_to_back": round(h["stream_kernel_us"], 3)},
             "clocks": clocks, "e2e": e2e_r, "gpu_launches": h["launches"], "cpu_baseline": cpu, "extras": extras,

@@ -15,7 +15,7 @@ __all__ = [
     "BSG_F_ALPHA_DEVICE", "BSG_F_C", "BSG_F_ALPHA_ROW", "BSG_F_ALPHA_COL", "BSG_F_GROUPED", "BsgError", "lib", "bsg_sf_bytes", "bsg_quantize", "bsg_quantize_bf16", "bsg_plan_create",
     "bsg_plan_run", "bsg_plan_run_operands", "bsg_plan_destroy", "bsg_plan_check_status", "bsg_plan_variant",
     "bsg_plan_debug_set", "mxfp8_gemm", "nvfp4_gemm", "bsg_cache_clear", "bsg_last_error",
-    "bsg_version", "Plan", "bsg_gemm_noalloc",
+    "bsg_version", "Plan", "bsg_gemm_noalloc", "bsg_noalloc_check_status",
 ]
 
 BSG_MXFP8, BSG_NVFP4 = 0, 1
@@ -85,6 +85,7 @@ def lib():
         "nvfp4_gemm": (st, [vp, vp, vp, vp, vp, vp, f, u, i, i, i, i, vp]),
         "bsg_cache_clear": (st, []),
         "bsg_gemm_noalloc": (st, [ctypes.POINTER(BsgDesc), vp]),
+        "bsg_noalloc_check_status": (st, [vp]),
         "bsg_sf_bytes": (ctypes.c_size_t, [i, i, i]),
         "bsg_quantize": (st, [i, vp, i, i, vp, vp, vp, vp]),
         "bsg_quantize_bf16": (st, [i, vp, i, i, vp, vp, vp, vp]),
@@ -209,6 +210,12 @@ def bsg_gemm_noalloc(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, 
                 *(st.get(k, 0) for k in ("stride_A", "stride_B", "stride_SFA", "stride_SFB", "stride_D", "stride_C")),
                 _ptr(group_index), _ptr(SFD), _ptr(d_scale))
     _check(lib().bsg_gemm_noalloc(ctypes.byref(d), _stream(stream)))
+
+
+def bsg_noalloc_check_status(stream=None):
+    """Raises BsgError (BSG_ERR_DEVICE_TIMEOUT) if an allocation-free launch on the current
+    device gave up a wait since the last check; synchronises `stream` first."""
+    _check(lib().bsg_noalloc_check_status(_stream(stream)))
 
 
 def bsg_cache_clear():

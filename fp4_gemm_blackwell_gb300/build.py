@@ -19,6 +19,9 @@ LIB = os.path.join(PKG, "libbsgemm.so")
 # Programs built beside the library (csrc/*_main.cu, linked against it): the native
 # launch-overhead loop that bench.py runs.
 LAUNCH_LOOP = os.path.join(PKG, "bsg_launch_loop")
+# Test-only probe kernels (tests/csrc/*.cu), each built into its own shared library beside its
+# source; only the GPU tests load them.
+TEST_CSRC = os.path.join(ROOT, "tests", "csrc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-I" + INCLUDE, "-I" + CSRC,
           "-Xcompiler", "-fPIC,-fvisibility=hidden"]
@@ -82,6 +85,16 @@ def build(verbose=False, force=False):
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("launch loop build failed:\n" + r.stdout.decode(errors="replace"))
+    for src in sorted(glob.glob(os.path.join(TEST_CSRC, "*.cu"))):
+        so = os.path.join(TEST_CSRC, "lib" + os.path.basename(src)[:-3] + ".so")
+        if not force and os.path.exists(so) and os.path.getmtime(so) >= max(os.path.getmtime(src), hdr_time):
+            continue
+        cmd = [nvcc] + ARCH + CFLAGS + ["-shared", "-o", so, src]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+        if r.returncode != 0:
+            raise RuntimeError("test probe build failed:\n" + r.stdout.decode(errors="replace"))
     return LIB
 
 

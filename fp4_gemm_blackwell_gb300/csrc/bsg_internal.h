@@ -76,7 +76,7 @@ struct GemmParams {
   CUtensorMap* map_slots;
   const void* remap_a;
   const void* remap_b;
-  int units_per_batch;     // num_m_groups * num_n_groups * splits
+  int units_per_batch;     // num_m_tiles * num_n_tiles * splits
   long long sfa_batch, sfb_batch;  // bytes between the scale buffers of consecutive entries (groups)
   long long d_batch, c_batch;      // 16-bit elements between consecutive D (C) matrices
   int splits;              // split-K factor (every split owns >= 1 k-tile)
@@ -86,11 +86,6 @@ struct GemmParams {
   int group_m;             // tile rasterisation: m-blocks per group
   int ring_stages;         // shared-memory ring stages in use (the kernel's maximum, or fewer to
                            // make room for split-K receive slots)
-  // Multicast clusters: cm = cmn x cmm CTAs (1 = none) take a block of cmm m-tiles x cmn n-tiles;
-  // the cmn CTAs of one m-tile share (multicast) its A tile, the cmm CTAs of one n-tile its B tile.
-  int cm, cmn, cmm;
-  int num_m_groups;        // ceil(num_m_tiles / cmm)
-  int num_n_groups;        // ceil(num_n_tiles / cmn)
   int debug_skip_first_load;  // test hook: the producer never loads its first stage
 };
 

@@ -11,7 +11,6 @@
 //                warps 8..11 the first half of the columns, warps 12..15 the second half),
 //                alpha, bias, SiLU, FP16/BF16 rounding and stores; with split-K, FP32 partial
 //                tiles reduced inside a thread-block cluster or through the workspace.
-// Optional multicast clusters share the A tile across n-tiles and the B tile across m-tiles.
 // Tile 128 x BN x (128 bytes of K): MXFP8 = 128 E4M3 per row per stage (four K=32 MMAs, one
 // UE8M0 scale each), NVFP4 = 256 E2M1 per row per stage (four K=64 MMAs, four UE4M3 each).
 //
@@ -103,13 +102,12 @@ struct UnitCoord {
 };
 
 // Unit u (a tile, or one split of a tile, of batch entry u / units_per_batch) -> tile
-// coordinates and k range.  With a multicast cluster, u numbers blocks of cmm x cmn tiles and
-// `rank` (the CTA's rank in its cluster, rn + cmn * rm) picks the tile of the block.  `tile` is
-// the tile's index over all entries (the workspace's).  Batch entries and groups exist only in
-// the EXT instantiations; elsewhere c.batch and c.bsel are the constant 0 and every entry offset
-// folds away.  Grouped (1-SM tiles, no multicast), the tile's group is that of its first row.
+// coordinates and k range.  `tile` is the tile's index over all entries (the workspace's).
+// Batch entries and groups exist only in the EXT instantiations; elsewhere c.batch and c.bsel
+// are the constant 0 and every entry offset folds away.  Grouped (1-SM tiles), the tile's group
+// is that of its first row.
 template <bool EXT>
-__device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u, int rank) {
+__device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u) {
   UnitCoord c;
   c.batch = 0;
   int tile0 = 0;  // tiles of the entries before this one
@@ -121,13 +119,13 @@ __device__ __forceinline__ UnitCoord decode_unit(const GemmParams& p, int u, int
   c.split = u % p.splits;
   const int t = u / p.splits;
   c.tile = tile0 + t;
-  const int per_group = p.group_m * p.num_n_groups;
+  const int per_group = p.group_m * p.num_n_tiles;
   const int g = t / per_group;
   const int first_m = g * p.group_m;
-  const int gm = min(p.num_m_groups - first_m, p.group_m);
+  const int gm = min(p.num_m_tiles - first_m, p.group_m);
   const int r = t - g * per_group;
-  c.m_blk = (first_m + r % gm) * p.cmm + rank / p.cmn;
-  c.n_blk = (r / gm) * p.cmn + rank % p.cmn;
+  c.m_blk = first_m + r % gm;
+  c.n_blk = r / gm;
   c.kt0 = c.split * p.k_tiles_per_split;
   c.kt1 = min(c.kt0 + p.k_tiles_per_split, p.num_k_tiles);
   c.bsel = c.batch;
@@ -620,7 +618,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
       // the code producer (with its bytes) and the four scale warps once the stage's scales are
       // in TMEM: one wait per k-tile for the MMA issuer
       mbar_init(bar_full(s), 1 + 4);
-      mbar_init(bar_empty(s), p.cmn + p.cmm - 1);  // one release per CTA this stage's copies reach
+      mbar_init(bar_empty(s), 1);  // the MMA issuer's commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
@@ -649,19 +647,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
   // first remote store, or at teardown.
   bool cluster_waited = false;  // this thread has completed the start-up cluster barrier
   if (p.split_mode == SPLIT_CLUSTER) cluster_arrive_relaxed();
-  // Multicast cluster: no CTA may write into a peer's ring or arrive on its barriers before the
-  // peer has initialised them.
-  if (p.cm > 1) cluster_sync();
-  const int crank = p.cm > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int rn = crank % p.cmn, rm = crank / p.cmn;      // position in the cmm x cmn block
-  const int u0 = static_cast<int>(blockIdx.x) / p.cm;   // first unit of this CTA (or cluster)
-  const int ustep = static_cast<int>(gridDim.x) / p.cm;  // CTAs (clusters) of the grid
-  // CTAs sharing this CTA's A tile (same m-tile) and B tile (same n-tile)
-  uint32_t row_mask = 0, col_mask = 0;
-  for (int i = 0; i < p.cmn; ++i) row_mask |= 1u << (rm * p.cmn + i);
-  for (int i = 0; i < p.cmm; ++i) col_mask |= 1u << (rn + i * p.cmn);
-  const uint16_t amask = static_cast<uint16_t>(row_mask), bmask = static_cast<uint16_t>(col_mask);
-  const uint16_t cmask = static_cast<uint16_t>(row_mask | col_mask);
+  const int u0 = static_cast<int>(blockIdx.x);     // first unit of this CTA
+  const int ustep = static_cast<int>(gridDim.x);  // CTAs of the grid
   const uint32_t tmem_base = *tmem_slot;
   const int nst = p.ring_stages;  // ring stages in use (fewer than STAGES with a split-K cluster)
   // Pointer-agnostic run: the code producer's own copies of the tensor maps, written before the
@@ -695,7 +682,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         bool ok = true;
         bool first = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit<EXT>(p, u, crank);
+          const UnitCoord c = decode_unit<EXT>(p, u);
           if (EXT && c.skip) continue;
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
             if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
@@ -711,49 +698,17 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
               for (int j = 0; j < KC; ++j) {  // k-slabs past K read as zeros (their MMAs are skipped)
                 const int x = (kt * KC + j) * C::BK_BYTES;
                 const uint32_t sa = stage_a(stage) + j * C::SLAB_A, sb = stage_b(stage) + j * C::SLAB_B;
-                if (p.cmn > 1) {
-                  // this CTA's slice of the A tile (the tensor map's box is 128/cmn rows), written
-                  // into the same stage of every CTA that shares the m-tile
-                  const int rows = C::BM / p.cmn;
-                  if (EXT && p.batches > 1)
-                    tma_load_3d_mc(sa + rn * rows * C::BK_BYTES, tma, fb, x, c.m_blk * C::BM + rn * rows, c.batch,
-                                   amask);
-                  else
-                    tma_load_2d_mc(sa + rn * rows * C::BK_BYTES, tma, fb, x, c.m_blk * C::BM + rn * rows, amask);
-                } else {
-                  if (EXT && p.batches > 1)
-                    tma_load_3d(sa, tma, fb, x, c.m_blk * C::BM, c.batch);
-                  else
-                    tma_load_2d(sa, tma, fb, x, c.m_blk * C::BM);
-                }
-                if (p.cmm > 1) {
-                  // likewise a BN/cmm-row slice of the B tile for every CTA that shares the n-tile
-                  const int rows = BN / p.cmm;
-                  if (EXT && p.b_entries > 1)
-                    tma_load_3d_mc(sb + rm * rows * C::BK_BYTES, tmb, fb, x, c.n_blk * BN + rm * rows, c.bsel,
-                                   bmask);
-                  else
-                    tma_load_2d_mc(sb + rm * rows * C::BK_BYTES, tmb, fb, x, c.n_blk * BN + rm * rows, bmask);
-                } else {
-                  if (EXT && p.b_entries > 1)
-                    tma_load_3d(sb, tmb, fb, x, c.n_blk * BN, c.bsel);
-                  else
-                    tma_load_2d(sb, tmb, fb, x, c.n_blk * BN);
-                }
+                if (EXT && p.batches > 1)
+                  tma_load_3d(sa, tma, fb, x, c.m_blk * C::BM, c.batch);
+                else
+                  tma_load_2d(sa, tma, fb, x, c.m_blk * C::BM);
+                if (EXT && p.b_entries > 1)
+                  tma_load_3d(sb, tmb, fb, x, c.n_blk * BN, c.bsel);
+                else
+                  tma_load_2d(sb, tmb, fb, x, c.n_blk * BN);
               }
             }
             first = false;
-            if (++stage == nst) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-        if (ok && p.cm > 1) {
-          // Wait until every consumer of the cluster has released the last fill of each stage:
-          // no peer's release may arrive at this CTA's barriers after it has exited.
-          for (int i = 0; i < nst; ++i) {
-            if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) break;
             if (++stage == nst) {
               stage = 0;
               phase ^= 1u;
@@ -773,7 +728,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         bool ok = true;
         bool first = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit<EXT>(p, u, crank);
+          const UnitCoord c = decode_unit<EXT>(p, u);
           if (EXT && c.skip) continue;
           const int band0 = c.n_blk * BN / 128;    // first scale band of the B tile
           const bool a_band = c.m_blk < p.sfa_bands;  // false only for a cluster's m-tile beyond M
@@ -825,7 +780,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit<EXT>(p, u, crank);
+          const UnitCoord c = decode_unit<EXT>(p, u);
           if (EXT && c.skip) continue;
           if (!wait_bounded(bar_tempty(acc), acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
             ok = false;
@@ -863,10 +818,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
                             sfb_t + 4 * C::NB * j, (kt > c.kt0 || j > 0) ? 1u : 0u);
               }
             }
-            if (p.cm > 1)
-              tc_commit_mc(bar_empty(stage), cmask);  // every CTA whose copies reach this stage
-            else
-              tc_commit(bar_empty(stage));
+            tc_commit(bar_empty(stage));
             if (++stage == nst) {
               stage = 0;
               phase ^= 1u;
@@ -908,7 +860,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     uint32_t phase = 0;
     bool ok = true;
     for (int u = u0; ok && u < p.num_units; u += ustep) {
-      const UnitCoord c = decode_unit<EXT>(p, u, crank);
+      const UnitCoord c = decode_unit<EXT>(p, u);
       if (EXT && c.skip) continue;
       const int jq = BN < 128 ? (c.n_blk * BN % 128) / 32 : 0;
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
@@ -961,7 +913,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = u0; u < p.num_units; u += ustep) {
-      const UnitCoord c = decode_unit<EXT>(p, u, crank);
+      const UnitCoord c = decode_unit<EXT>(p, u);
       if (EXT && c.skip) continue;
       const float alpha = unit_alpha<EXT>(p, c, alpha0);
       bool ok = wait_bounded(bar_tfull(acc), acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
@@ -1178,10 +1130,6 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     // CTA needs to outlive another: a CTA leaves after its receive barrier saw every byte sent
     // to it, and what it sent came from registers.
     if (!cluster_waited) cluster_wait();
-  } else if (p.cm > 1) {
-    // multicast cluster: leave together, once no CTA issues further copies into the others
-    __syncwarp();
-    cluster_sync();
   }
 
   // ------------------------------------------------------------ teardown

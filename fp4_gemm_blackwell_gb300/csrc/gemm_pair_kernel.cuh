@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         bool ok = true;
         bool first = true;
         for (int u = pair0; ok && u < p.num_units; u += pairs) {
-          const UnitCoord c = decode_unit<EXT>(p, u, 0);
+          const UnitCoord c = decode_unit<EXT>(p, u);
           const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
           for (int kt = c.kt0; kt < c.kt1; ++kt) {
             if (!wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         bool ok = true;
         bool first = true;
         for (int u = pair0; ok && u < p.num_units; u += pairs) {
-          const UnitCoord c = decode_unit<EXT>(p, u, 0);
+          const UnitCoord c = decode_unit<EXT>(p, u);
           const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
           const bool a_band = m_blk < p.sfa_bands;  // false for the pair's second m-tile past M
           int bands = 0;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int u = pair0; ok && u < p.num_units; u += pairs) {
-          const UnitCoord c = decode_unit<EXT>(p, u, 0);
+          const UnitCoord c = decode_unit<EXT>(p, u);
           if (!wait_bounded_cluster(bar_tempty, acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
             ok = false;
             break;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     uint32_t ph_old = 0;
     bool ok = true;
     for (int u = pair0; ok && u < p.num_units; u += pairs) {
-      const UnitCoord c = decode_unit<EXT>(p, u, 0);
+      const UnitCoord c = decode_unit<EXT>(p, u);
       for (int kt = c.kt0; kt < c.kt1; ++kt) {
         ok = __all_sync(0xffffffffu, wait_bounded(bar_sf_full(stage), phase, abort_flag, p, ST_TIMEOUT_SCALES));
         if (!ok) break;
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
     uint32_t acc_phase = 0;
     for (int u = pair0; u < p.num_units; u += pairs) {
-      const UnitCoord c = decode_unit<EXT>(p, u, 0);
+      const UnitCoord c = decode_unit<EXT>(p, u);
       const float alpha = unit_alpha<EXT>(p, c, alpha0);
       bool ok = wait_bounded_cluster(bar_tfull, acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE);
       ok = named_bar_and(1, C::EPI_THREADS, ok);

@@ -31,6 +31,12 @@ constexpr int kMaxDim = 1 << 20;
 
 thread_local std::string g_err;
 
+// State of the allocation-free entry point (bsg_gemm_noalloc): the lock of its per-device
+// scratch lookup, and its test hook (bsg_plan_debug_set with a null plan).
+std::mutex g_noalloc_mutex;
+int g_noalloc_skip_first_load = 0;
+unsigned long long g_noalloc_wait_limit_ns = kDefaultWaitLimitNs;
+
 bsg_status fail(bsg_status s, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -276,43 +282,6 @@ bsg_status ensure_smem_attr(const bsg::GemmKernelInfo& info, int device) {
   return BSG_OK;
 }
 
-// CTAs of `info`'s kernel that can be resident at once when launched in clusters of `cluster`
-// (the SM count for cluster <= 1; clusters must fit in a GPC, which can leave SMs over).
-std::mutex g_occ_mutex;
-std::unordered_map<std::string, int> g_occ_cache;
-
-bsg_status resident_ctas(const bsg::GemmKernelInfo& info, int cluster, int sms, int device, int* out) {
-  *out = sms;
-  if (cluster <= 1) return BSG_OK;
-  char key[96];
-  std::snprintf(key, sizeof(key), "%p/%d/%d", info.fn, cluster, device);
-  std::lock_guard<std::mutex> lk(g_occ_mutex);
-  auto it = g_occ_cache.find(key);
-  if (it != g_occ_cache.end()) {
-    *out = it->second;
-    return BSG_OK;
-  }
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = static_cast<unsigned>(cluster);
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(cluster * sms), 1, 1);
-  cfg.blockDim = dim3(static_cast<unsigned>(info.threads), 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(info.smem_bytes);
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  const cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, info.fn, &cfg);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
-  if (clusters < 1) return fail(BSG_ERR_CUDA, "no cluster of %d CTAs of this kernel fits on the device", cluster);
-  *out = std::min(sms, clusters * cluster);
-  g_occ_cache[key] = *out;
-  return BSG_OK;
-}
-
 int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (v == nullptr || *v == 0) return dflt;
@@ -328,11 +297,10 @@ int env_int(const char* name, int dflt) {
 //    128-wide tiles with K split so that tiles x splits fills at most one wave (2, 4 or 8
 //    splits reduce inside a thread-block cluster; other factors, only reachable by forcing,
 //    go through the plan's global workspace).
-// Multicast clusters (A shared along n, B along m) are available by forcing but never won a
-// measurement: the 1-SM tile is bound by shared-memory traffic, which multicast leaves as is.
+// Every TMA copy of these kernels lands in the shared memory of the CTA that issues it; a
+// cluster exists only for split-K reductions (DSMEM) and CTA pairs.
 struct Variant {
   int bn, splits, kps, mode, cluster;
-  int cmn, cmm;  // multicast cluster: cmm m-tiles x cmn n-tiles (A shared along n, B along m)
   int kc;        // 128-byte k-slabs per ring stage (1-SM kernel; kps counts ring stages)
   bool pair;     // CTA-pair kernel: 256 x 256 tiles over 2-CTA clusters
 };
@@ -406,8 +374,6 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   int k = (nst + s - 1) / s;
   s = (nst + k - 1) / k;
   Variant v;
-  v.cmn = 1;
-  v.cmm = 1;
   v.kc = kc;
   v.pair = pair && env_int("BSG_FORCE_SPLITS", 0) == 0;
   const int fp = env_int("BSG_FORCE_PAIR", -1);
@@ -425,25 +391,6 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   v.bn = b;
   v.splits = s;
   v.kps = k;
-  // multicast cluster (split-K off): A shared by cmn n-tiles, B by cmm m-tiles; each at most the
-  // number of such tiles (power of two), and the cluster at most 8 CTAs
-  int cmn = 1, cmm = 1;
-  const int fc = env_int("BSG_FORCE_CM", 0);
-  if (fc == 1 || fc == 2 || fc == 4 || fc == 8) cmn = fc;
-  const int fm = env_int("BSG_FORCE_CMM", 0);
-  if (fm == 1 || fm == 2 || fm == 4 || fm == 8) cmm = fm;
-  if (s > 1 || grouped) cmn = cmm = 1;  // grouped: the m-tiles sharing a B tile could differ in group
-  const long long nt = (d->N + b - 1) / b;
-  while (cmn > 1 && cmn > nt) cmn /= 2;
-  while (cmm > 1 && cmm > mt) cmm /= 2;
-  while (cmn * cmm > 8) (cmn >= cmm ? cmn : cmm) /= 2;
-  if (cmn * cmm > 1) {
-    v.cmn = cmn;
-    v.cmm = cmm;
-    v.mode = bsg::SPLIT_NONE;
-    v.cluster = cmn * cmm;
-    return v;
-  }
   // A cluster split keeps 128 x (bn + 4) floats of partial rows in shared memory next to the
   // ring, which leaves 64- and 128-wide tiles enough stages and a 256-wide tile too few.
   const bool cluster_ok = (s == 2 || s == 4 || s == 8) && (b == 64 || b == 128);
@@ -492,17 +439,16 @@ bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, u
 // workspace pointers.  Grid: persistent (<= #SMs) unless the splits form clusters, in which
 // case every unit is its own CTA.
 bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, const bsg::GemmKernelInfo& info,
-                       int sms, int resident_ctas, int* grid) {
+                       int sms, int* grid) {
   std::memset(g, 0, sizeof(*g));
   const size_t rb = code_row_bytes(d->kind, d->K);
   bsg_status s;
   const bool grouped = (d->flags & BSG_F_GROUPED) != 0;
   const int LB = d->L > 1 ? d->L : 1;  // entries of B and SFB (batch entries or groups)
   const int L = grouped ? 1 : LB;      // entries of A, SFA, D and C
-  if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, static_cast<uint32_t>(128 / v.cmn), L, d->stride_A, "A")) !=
-          BSG_OK ||
-      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn / v.cmm), LB,
-                          d->stride_B, "B")) != BSG_OK)
+  if ((s = encode_operand(&g->tmap_a, d->A, rb, d->M, 128u, L, d->stride_A, "A")) != BSG_OK ||
+      (s = encode_operand(&g->tmap_b, d->B, rb, d->N, static_cast<uint32_t>(v.pair ? 128 : v.bn), LB, d->stride_B,
+                          "B")) != BSG_OK)
     return s;
   g->batches = L;
   g->b_entries = LB;
@@ -547,12 +493,7 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->splits = v.splits;
   g->split_mode = v.mode;
   g->k_tiles_per_split = v.pair ? g->num_k_tiles : v.kps;  // in ring stages
-  g->cmn = v.cmn;
-  g->cmm = v.cmm;
-  g->cm = v.cmn * v.cmm;
-  g->num_m_groups = (g->num_m_tiles + v.cmm - 1) / v.cmm;
-  g->num_n_groups = (g->num_n_tiles + v.cmn - 1) / v.cmn;
-  g->units_per_batch = g->num_m_groups * g->num_n_groups * v.splits;
+  g->units_per_batch = g->num_m_tiles * g->num_n_tiles * v.splits;
   g->num_units = g->units_per_batch * L;
   g->group_m = 16;
   g->debug_skip_first_load = 0;
@@ -569,7 +510,6 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
       return fail(BSG_ERR_SHAPE, "split-K cluster staging does not fit the ring");
   }
   if (v.pair) *grid = 2 * std::min(g->num_units, sms / 2);
-  else if (g->cm > 1) *grid = g->cm * std::min(g->num_units, resident_ctas / g->cm);
   else *grid = v.mode == bsg::SPLIT_CLUSTER ? g->num_units : std::min(g->num_units, sms);
   return BSG_OK;
 }
@@ -659,8 +599,6 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
                                 &info_ext))
     return fail(BSG_ERR_DTYPE, "no extended kernel for this format / output type");
   if ((s = ensure_smem_attr(info_ext, dev)) != BSG_OK) return s;
-  int resident = di.sms;
-  if ((s = resident_ctas(info, v.cmn * v.cmm, di.sms, dev, &resident)) != BSG_OK) return s;
 
   bsg_plan_s* p = new (std::nothrow) bsg_plan_s();
   if (p == nullptr) return fail(BSG_ERR_NOMEM, "host allocation of the plan failed");
@@ -673,7 +611,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   p->workspace = nullptr;
   p->cluster = v.cluster;
   bsg::GemmParams& g = p->params;
-  if ((s = fill_params(&g, d, v, info, di.sms, resident, &p->grid)) != BSG_OK) {
+  if ((s = fill_params(&g, d, v, info, di.sms, &p->grid)) != BSG_OK) {
     delete p;
     return s;
   }
@@ -700,10 +638,8 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
     std::snprintf(p->variant, sizeof(p->variant), "%s_pair256_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
                   info.stages, p->grid);
   } else {
-    char mc[24] = "";
-    if (v.cmn * v.cmm > 1) std::snprintf(mc, sizeof(mc), v.cmm > 1 ? "_mc%dx%d" : "_mc%d", v.cmn, v.cmm);
-    std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s%s%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
-                  v.bn, v.splits, kModeName[v.mode], mc, v.kc == 2 ? "_kc2" : "", g.ring_stages, p->grid);
+    std::snprintf(p->variant, sizeof(p->variant), "%s_bn%d_s%d%s%s_st%d_g%d", d->kind == BSG_MXFP8 ? "mxfp8" : "nvfp4",
+                  v.bn, v.splits, kModeName[v.mode], v.kc == 2 ? "_kc2" : "", g.ring_stages, p->grid);
   }
   make_launch_config(&p->cfg, p->attrs, p->grid, info.threads, info.smem_bytes, p->cluster);
   if (env_int("BSG_LOG", 0))
@@ -819,6 +755,12 @@ BSG_API const char* bsg_plan_variant(bsg_plan_t plan) {
 }
 
 BSG_API bsg_status bsg_plan_debug_set(bsg_plan_t plan, int skip_first_load, unsigned long long wait_limit_ns) {
+  if (plan == nullptr) {  // the allocation-free path's setting (process-wide)
+    std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+    g_noalloc_skip_first_load = skip_first_load ? 1 : 0;
+    g_noalloc_wait_limit_ns = wait_limit_ns ? wait_limit_ns : kDefaultWaitLimitNs;
+    return BSG_OK;
+  }
   if (!plan_ok(plan)) return fail(BSG_ERR_INVALID_ARG, "invalid plan handle");
   plan->params.debug_skip_first_load = skip_first_load ? 1 : 0;
   plan->params.wait_limit_ns = wait_limit_ns ? wait_limit_ns : kDefaultWaitLimitNs;
@@ -993,6 +935,8 @@ BSG_API bsg_status bsg_quantize_bf16(bsg_kind kind, const void* x, int rows, int
 // the same kernel as bsg_plan_run, but its status word, split-K counters and split-K partial
 // tiles live in the file-scope device array below (kNoAllocScratchBytes per GPU that loads
 // this library, held until the process exits) instead of a plan's cudaMalloc'ed workspace.
+// The status word (offset 0) is cleared only by bsg_noalloc_check_status, so that a wait a
+// kernel gave up stays visible until it is read; every call clears the split-K counters.
 
 namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
@@ -1003,7 +947,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 
-std::mutex g_noalloc_mutex;
 unsigned char* g_noalloc_ptr[kNoAllocMaxDevices] = {};
 
 // Device address of the scratch array on `dev` (current device); looked up once per device.
@@ -1038,31 +981,51 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
   const bool found = bsg::find_kernel(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, d->flags, d->L,
                                       v.pair, v.bn, v.kc, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
-  const int num_tiles =
-      ((d->M + 127) / 128) * ((d->N + v.bn - 1) / v.bn) * (d->L > 1 && !(d->flags & BSG_F_GROUPED) ? d->L : 1);
-  const WorkspaceLayout w = workspace_layout(v, num_tiles, 0);
+  bsg::GemmParams g;
+  int grid = 0;
+  if ((s = fill_params(&g, d, v, info, di.sms, &grid)) != BSG_OK) return s;
+  // the same layout a plan's workspace has for this variant and tile count (no map slots)
+  const WorkspaceLayout w = workspace_layout(v, g.num_tiles, 0);
   if (w.total > kNoAllocScratchBytes)
     return fail(BSG_ERR_SHAPE,
                 "this problem needs %zu bytes of scratch (split-K %d over %d tiles); the allocation-free "
                 "entry point has %zu; use a plan",
-                w.total, v.splits, num_tiles, kNoAllocScratchBytes);
+                w.total, v.splits, g.num_tiles, kNoAllocScratchBytes);
   unsigned char* scratch = nullptr;
   if ((s = noalloc_scratch(dev, &scratch)) != BSG_OK) return s;
   if ((s = ensure_smem_attr(info, dev)) != BSG_OK) return s;
-  int resident = di.sms;
-  if ((s = resident_ctas(info, v.cmn * v.cmm, di.sms, dev, &resident)) != BSG_OK) return s;
-
-  bsg::GemmParams g;
-  int grid = 0;
-  if ((s = fill_params(&g, d, v, info, di.sms, resident, &grid)) != BSG_OK) return s;
   g.status = reinterpret_cast<unsigned*>(scratch);
   g.counters = reinterpret_cast<unsigned*>(scratch + w.cnt_off);
   g.partial = w.part_bytes ? reinterpret_cast<float*>(scratch + w.part_off) : nullptr;
+  g.debug_skip_first_load = g_noalloc_skip_first_load;
+  g.wait_limit_ns = g_noalloc_wait_limit_ns;
 
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the status word and the split-K counters must start at zero; the partial tiles are
-  // written whole by their split before they are read
-  const cudaError_t e = cudaMemsetAsync(scratch, 0, w.part_off, st);
+  // the split-K counters must start at zero (a launch that gave up a wait can leave them
+  // set); the partial tiles are written whole by their split before they are read
+  const cudaError_t e = cudaMemsetAsync(scratch + w.cnt_off, 0, w.part_off - w.cnt_off, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(allocation-free scratch)");
   return launch_gemm(info.fn, g, grid, info.threads, info.smem_bytes, v.cluster, st);
+}
+
+BSG_API bsg_status bsg_noalloc_check_status(bsg_stream_t stream) {
+  int dev = 0;
+  DeviceInfo di;
+  bsg_status s = current_device(&dev, &di);
+  if (s != BSG_OK) return s;
+  unsigned char* scratch = nullptr;
+  if ((s = noalloc_scratch(dev, &scratch)) != BSG_OK) return s;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != 0) e = cudaMemset(scratch, 0, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the allocation-free status word");
+  if (word != 0)
+    return fail(BSG_ERR_DEVICE_TIMEOUT,
+                "an allocation-free launch on this device gave up a wait (status 0x%x:%s%s%s%s%s)", word,
+                (word & bsg::ST_TIMEOUT_PRODUCER) ? " producer" : "", (word & bsg::ST_TIMEOUT_MMA) ? " mma" : "",
+                (word & bsg::ST_TIMEOUT_EPILOGUE) ? " epilogue" : "", (word & bsg::ST_TIMEOUT_DRAIN) ? " drain" : "",
+                (word & bsg::ST_TIMEOUT_SCALES) ? " scales" : "");
+  return BSG_OK;
 }

@@ -78,16 +78,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// The same box delivered to every CTA of the cluster named in cta_mask, at this CTA's shared
-// memory offset `dst`, each completing on its own barrier at offset `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
-                                               int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
 // Tiled load for CTA pairs: the destination is this CTA's shared memory, the completion may
 // be counted on the pair leader's barrier (`bar` a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
@@ -106,7 +96,7 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&v)[8]) 
                : "memory");
 }
 
-// 3-D forms of the three tiled loads above: (x, y) within one matrix of a batch, z the batch
+// 3-D forms of the two tiled loads above: (x, y) within one matrix of a batch, z the batch
 // index (tensor maps of batched operands are 3-D: K bytes, rows, batch).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y,
                                             int32_t z) {
@@ -114,14 +104,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y,
-                                               int32_t z, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
@@ -400,16 +382,9 @@ __device__ __forceinline__ void tc_cp_sf_atom_pair(uint32_t taddr, uint64_t sdes
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-// Arrive once on the barrier at the same smem offset in every CTA of `cta_mask` when the pair's
-// tensor-core operations issued so far by this thread complete.
-// Arrive on the barrier at offset `bar` of every CTA in cta_mask once this CTA's earlier
-// tensor-core operations have completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
+// Arrive once on the barrier at offset `bar` of every CTA in cta_mask (the two CTAs of a pair, or
+// the leader alone) when the pair's tensor-core operations issued so far by this thread complete.
+// A barrier arrive, not a data copy: nothing is loaded from global memory.
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),

@@ -216,18 +216,29 @@ bsg_status nvfp4_gemm(void* D, const void* A, const void* B, const void* SFA, co
  * cannot allocate device memory when they run a GEMM -- code running inside an allocator or
  * memory-pool callback, engines that forbid device allocation after start-up to keep a fixed
  * memory budget, hosts whose CUDA allocator belongs to someone else.  It computes exactly what
- * bsg_plan_create + bsg_plan_run compute for `d` (same validation, same kernel), but allocates
- * no device memory: no cudaMalloc, no cudaFree, no allocating library routine.  Its status
- * word, split-K counters and split-K partial tiles live in one static device array of
- * 16 MiB that every GPU loading this library holds until the process exits; a problem whose
- * split-K partials would not fit is rejected with BSG_ERR_SHAPE (use a plan instead).
- * The first call on a device looks up that array's device address (once per device, with
- * that device current); make that first call before any stream capture.  Every call clears
- * the counters and status word at its start on `stream`; all calls share the one array, so
- * calls that overlap on the GPU (different streams, or concurrent host threads) race.
- * A kernel that gives up a wait is not reported by this call (there is no plan to query).
- * Each call encodes its tensor maps on the host, so it costs more host time than a plan. */
+ * bsg_plan_create + bsg_plan_run compute for `d` (same validation, same kernel), but makes no
+ * cudaMalloc, no cudaFree and no call to an allocating library routine.  Its status word,
+ * split-K counters and split-K partial tiles live in one static device array of 16 MiB that
+ * every GPU loading this library holds until the process exits; a problem whose split-K
+ * partials would not fit is rejected with BSG_ERR_SHAPE (use a plan instead).
+ * First use: the first call on a device looks up that array's device address (once per
+ * device, with that device current), and the first call that runs a given kernel variant sets
+ * its shared-memory attribute.  With CUDA's default lazy module loading, these first uses load
+ * the library's device code and the array itself, which the driver does by allocating device
+ * memory.  So make one call of each problem shape you will use outside the restricted context
+ * and before any stream capture (or set CUDA_MODULE_LOADING=EAGER); calls after that allocate
+ * nothing.  Every call clears the split-K counters at its start on `stream`; all calls share
+ * the one array, so calls that overlap on the GPU (different streams, or concurrent host
+ * threads) race.  A kernel that gives up a bounded wait records it in the array's status word,
+ * which stays set until bsg_noalloc_check_status reads it.  Each call encodes its tensor maps
+ * on the host, so it costs more host time than a plan's run. */
 bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream);
+
+/* Status of the allocation-free calls on the current device: synchronise `stream` (the
+ * stream of those calls), read the status word of the device's scratch array and clear it.
+ * BSG_OK, or BSG_ERR_DEVICE_TIMEOUT if a bsg_gemm_noalloc launch on this device abandoned a
+ * bounded wait since the last check (its output is then incomplete).  Allocates nothing. */
+bsg_status bsg_noalloc_check_status(bsg_stream_t stream);
 
 /* Drop every plan of the one-shot cache (after the work using them has completed). */
 bsg_status bsg_cache_clear(void);
@@ -272,7 +283,9 @@ const char* bsg_version(void);
  * Set the plan's bounded-wait limit (nanoseconds, 0 keeps the default of 2 s) and, with
  * skip_first_load != 0, make the producer of every CTA leave its first ring stage unfilled,
  * so that the tensor-core warp's wait runs out, the kernel flags BSG_ERR_DEVICE_TIMEOUT in
- * the plan's status word and returns cleanly.  For tests of the failure path only. */
+ * the plan's status word and returns cleanly.  With plan == NULL the setting applies to every
+ * later bsg_gemm_noalloc call of the process (read back with bsg_noalloc_check_status).  For
+ * tests of the failure path only. */
 bsg_status bsg_plan_debug_set(bsg_plan_t plan, int skip_first_load, unsigned long long wait_limit_ns);
 
 #ifdef __cplusplus

@@ -25,3 +25,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The largest accumulation error the GPU parity checks saw (tests/parity_util.py)."""
+    mod = sys.modules.get("parity_util")
+    rec = getattr(mod, "RECORD", None)
+    if rec:
+        terminalreporter.write_line(
+            "parity: %d checks, largest accumulation error %.4g x |alpha| sum|a b| (secondary bound %s)"
+            % (len(rec), max(rec), mod.SECONDARY_REL))

@@ -102,25 +102,19 @@ def test_cluster_split_ragged_rows(kind, monkeypatch):
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("bn", [32, 64])
-@pytest.mark.parametrize("cm", [1, 2, 4, 8])
-def test_narrow_tiles_multicast(kind, bn, cm, monkeypatch):
-    # 32- and 64-wide tiles (B scales taken from a quarter / half of each 128-row band), the A
-    # tile multicast over clusters of cm CTAs; N = 400 leaves the last tile half full and the
-    # last cluster with n-tiles wholly beyond N, M = 200 a ragged second m-tile
-    v = run_case(kind, 200, 400, 1792, env={"BSG_FORCE_BN": bn, "BSG_FORCE_CM": cm}, monkeypatch=monkeypatch,
-                 bias=True, silu=True)
-    nt = -(-400 // bn)
-    while cm > nt:  # a cluster never has more CTAs than there are n-tiles
-        cm //= 2
-    assert "_bn%d_s1%s_" % (bn, "" if cm == 1 else "_mc%d" % cm) in v
+def test_narrow_tiles(kind, bn, monkeypatch):
+    # 32- and 64-wide tiles (B scales taken from a quarter / half of each 128-row band); N = 400
+    # leaves the last tile half full, M = 200 a ragged second m-tile
+    v = run_case(kind, 200, 400, 1792, env={"BSG_FORCE_BN": bn}, monkeypatch=monkeypatch, bias=True, silu=True)
+    assert "_bn%d_s1_" % bn in v
 
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
-def test_narrow_tiles_persistent_clusters(kind, monkeypatch):
-    # 8 x 128 tiles of 128 x 32 in clusters of 4: more cluster units than resident clusters
-    v = run_case(kind, 1024, 4096, 512, env={"BSG_FORCE_BN": 32, "BSG_FORCE_CM": 4}, monkeypatch=monkeypatch,
+def test_narrow_tiles_persistent(kind, monkeypatch):
+    # 8 x 128 tiles of 128 x 32 on a persistent grid: every CTA runs several tiles
+    v = run_case(kind, 1024, 4096, 512, env={"BSG_FORCE_BN": 32}, monkeypatch=monkeypatch,
                  out="f16", rows=np.arange(0, 1024, 7))
-    assert "_bn32_s1_mc4_" in v
+    assert "_bn32_s1_" in v
 
 
 @pytest.mark.parametrize("M,N,K,expect", [
@@ -139,13 +133,12 @@ def test_default_variants(M, N, K, expect):
         P.assert_parity(dp.result(), prob, "bf16", dp.bias_vals, True, rows=np.arange(0, M, max(1, M // 96)))
 
 
-def test_multicast_wait_timeout_reports_status(monkeypatch):
+def test_narrow_wait_timeout_reports_status(monkeypatch):
     monkeypatch.setenv("BSG_FORCE_BN", "32")
-    monkeypatch.setenv("BSG_FORCE_CM", "4")
     prob = P.make_problem("nvfp4", 256, 1024, 1024)
     dp = P.DeviceProblem(prob)
     with dp.plan() as plan:
-        assert "_mc4_" in plan.variant
+        assert "_bn32_s1_" in plan.variant
         bsg.bsg_plan_debug_set(plan.handle, 1, 50_000_000)
         plan.run()
         with pytest.raises(bsg.BsgError) as e:
@@ -332,7 +325,7 @@ def _batched_buffers(kind, L, M, N, K, pad=256, residual=False):
 
 @pytest.mark.parametrize("env", [{}, {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 128},
                                  {"BSG_FORCE_BN": 32}, {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2},
-                                 {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3}, {"BSG_FORCE_BN": 32, "BSG_FORCE_CM": 4}])
+                                 {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3}])
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 def test_batched(kind, env, monkeypatch):
     # L = 3 problems of one shape in one launch (the L of the {m, n, k, l} problem shape), every
@@ -385,15 +378,15 @@ def _grouped_layout(sizes, tail):
 @pytest.mark.parametrize("env", [{}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 128}, {"BSG_FORCE_BN": 32},
                                  {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2},
                                  {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3},
-                                 {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_CM": 4}])
+                                 {"BSG_FORCE_PAIR": 1}])
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 def test_grouped(kind, env, monkeypatch):
     # Grouped GEMM (expert GEMMs of a mixture-of-experts layer): 4 groups of 200, 0, 37 and 128
     # rows with their own B and alpha, in the 128-row-aligned layout; then a block whose first
     # row names group 99 (skipped whole) and a ragged tail of no group.  One row inside group
     # 3's block is marked group 2: it is not stored.  Each group against its own oracle result;
-    # every row of no stored group keeps the canary.  A forced CTA pair or multicast cluster
-    # must not apply to a grouped problem.
+    # every row of no stored group keeps the canary.  A forced CTA pair must not apply to a
+    # grouped problem.
     for k, v in env.items():
         monkeypatch.setenv(k, str(v))
     G, N, K = 4, 144, 1536
@@ -464,13 +457,13 @@ def test_grouped(kind, env, monkeypatch):
 
 @pytest.mark.parametrize("env", [{}, {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 256}, {"BSG_FORCE_BN": 32},
                                  {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2},
-                                 {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3}, {"BSG_FORCE_BN": 32, "BSG_FORCE_CM": 4}])
+                                 {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 3}])
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 def test_run_operands(kind, env, monkeypatch):
     # Pointer-agnostic runs: one plan, made on problem 1's buffers, runs on problem 2's (its
     # tensor maps rewritten on the device), then plainly on its own, then on problem 2's again;
     # every kernel family (CTA pair, one and two accumulators, split-K in a cluster and through
-    # the workspace, multicast).  Each result against its own oracle; the other D untouched.
+    # the workspace).  Each result against its own oracle; the other D untouched.
     for k, v in env.items():
         monkeypatch.setenv(k, str(v))
     silu = kind == "nvfp4"
@@ -505,7 +498,7 @@ def test_run_operands(kind, env, monkeypatch):
 
 
 @pytest.mark.parametrize("env", [{}, {"BSG_FORCE_BN": 64}, {"BSG_FORCE_BN": 128}, {"BSG_FORCE_BN": 256},
-                                 {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 32, "BSG_FORCE_CM": 4},
+                                 {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 32},
                                  {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2}])
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 def test_nvfp4_output(kind, env, monkeypatch):
@@ -591,3 +584,39 @@ def test_batched_device_alpha_per_entry(env, monkeypatch):
         P.assert_parity(got, p, "bf16")
     if "BSG_FORCE_PAIR" in env:
         assert "pair" in variant, variant
+
+
+@pytest.mark.parametrize("env", EPI_FAMILIES)
+@pytest.mark.parametrize("kind,residual", [("nvfp4", None), ("mxfp8", None), ("nvfp4", "separate"),
+                                           ("mxfp8", "inplace")])
+def test_additive_terms_where_rows_of_a_are_zero(env, kind, residual, monkeypatch):
+    # Rows of A that are all zero have an accumulation term of exactly 0, so there the output is
+    # the epilogue's additive terms alone: D[m, n] = round(silu(bias[n] + beta * C[m, n])) to one
+    # output ulp, a bound too tight for a bias or C taken from a neighbouring column or row.  The
+    # zero rows are scattered over lanes, warps and tiles; the other rows check the accumulation
+    # in the same launch.  Every kernel family, the plain instantiation (bias + SiLU) and the
+    # extended one (with C).
+    for k, v in env.items():
+        monkeypatch.setenv(k, str(v))
+    M, N, K = 300, 272, 2048
+    zero = (np.arange(M) // 7) % 3 == 0
+    prob = P.make_problem(kind, M, N, K, zero_rows=zero)
+    assert not prob["A"][zero].any()
+    dp = P.DeviceProblem(prob, out="bf16", bias=True, silu=True, residual=residual, beta=0.75)
+    with dp.plan() as plan:
+        variant = plan.variant
+        plan.run()
+        plan.check_status()
+        got = dp.result()
+    P.assert_parity(got, prob, "bf16", dp.bias_vals, True, epi=dp.epi_kwargs())
+    # the closed form of the zero rows, written out here rather than taken from the oracle
+    y = np.broadcast_to(dp.bias_vals[None, :], (M, N)).astype(np.float64)
+    if residual is not None:
+        y = y + np.float64(np.float32(0.75)) * dp.C_vals
+    y = y / (1.0 + np.exp(-y))
+    want = R.round_out(y, "bf16")[zero]
+    g = got[zero]
+    ulp = R.ulp_out(np.maximum(np.abs(want), np.abs(g)), "bf16")
+    bad = np.abs(g - want) > ulp
+    assert not bad.any(), "%s: %d zero-row outputs off by more than one ulp, first at %s" % (
+        variant, bad.sum(), np.argwhere(bad)[:3].tolist())

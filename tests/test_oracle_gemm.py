@@ -266,7 +266,8 @@ def test_nvfp4_output_checker_catches_planted_mistakes():
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 def test_parity_tolerance_catches_plausible_mistakes(kind):
-    # The element-wise tolerance of the GPU parity tests (r11) must not hide a real mistake: the
+    # The element-wise tolerance of the GPU parity tests (|alpha| 2^-7 sum|a b|, x 1.1 with SiLU,
+    # + 1 output ulp) must not hide a real mistake: the
     # oracle's own output passes, and that output computed with a mistake planted fails: B's
     # rows in the wrong order, alpha doubled, SiLU left out, the result transposed.  A bias
     # shifted by one column is caught where the accumulation term of the bound vanishes (A all
@@ -292,9 +293,38 @@ def test_parity_tolerance_catches_plausible_mistakes(kind):
                out(prob, silu=False), ref.T.copy()]
     for got in planted:
         with pytest.raises(AssertionError):
-            P.assert_parity(got, prob, "bf16", bias_vals, silu)
+            P.assert_parity(got, prob, "bf16", bias_vals, silu, record=False)
     zero = dict(prob, A=np.zeros_like(prob["A"]))
     zref = out(zero)
     P.assert_parity(zref, zero, "bf16", bias_vals, silu)
     with pytest.raises(AssertionError):
-        P.assert_parity(out(zero, bias=np.roll(bias_vals, 1)), zero, "bf16", bias_vals, silu)
+        P.assert_parity(out(zero, bias=np.roll(bias_vals, 1)), zero, "bf16", bias_vals, silu, record=False)
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_secondary_bound_catches_small_mistakes(kind):
+    # Mistakes that the stated bar misses, or catches in a few elements only, at K = 4096 must
+    # exceed the secondary bound of the GPU parity checks (an accumulation error of at most
+    # 2^-13 sum|a b| beyond one output ulp): the oracle's result computed with one block scale of
+    # A one code too large (within the stated bar everywhere), and with one k-tile of the kernels
+    # (128 E4M3 / 256 E2M1 values) left out of every dot product.  The oracle's own result
+    # measures 0.
+    import parity_util as P
+    bound = 2.0 ** -13
+    M, N, K = 128, 128, 4096
+    blk = 32 if kind == "mxfp8" else 16
+    prob = P.make_problem(kind, M, N, K, seed_a=31, seed_b=32)
+    ref, abs_sum = P.reference(prob, "bf16")
+    alpha = prob["alpha"]
+    assert P.accumulation_ratio(ref, ref, abs_sum, alpha, False, "bf16") == 0.0
+    sfa = L.unswizzle(prob["SFA"], M, K // blk).copy()
+    sfa[37, 11] += 1
+    bumped = P.reference(dict(prob, SFA=L.swizzle(sfa)), "bf16")[0]
+    P.assert_parity(bumped, prob, "bf16", record=False)
+    assert P.accumulation_ratio(bumped, ref, abs_sum, alpha, False, "bf16") > bound
+    # one k-tile dropped: its scales set to code 0 decode to 2^-127 (MXFP8) or 0 (NVFP4)
+    kt = 128 if kind == "mxfp8" else 256
+    sfa = L.unswizzle(prob["SFA"], M, K // blk).copy()
+    sfa[:, 5 * kt // blk:6 * kt // blk] = 0
+    dropped = P.reference(dict(prob, SFA=L.swizzle(sfa)), "bf16")[0]
+    assert P.accumulation_ratio(dropped, ref, abs_sum, alpha, False, "bf16") > bound

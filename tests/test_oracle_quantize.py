@@ -178,3 +178,29 @@ def test_bf16_quantisers_quantise_the_widened_values():
     p0, t0, g0 = Q.quantize_nvfp4_bf16(bits)
     p1, t1, g1 = Q.quantize_nvfp4(wide)
     assert np.array_equal(p0, p1) and np.array_equal(t0, t1) and g0 == g1
+
+
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_row_chunked_quantisation_equals_whole_matrix(kind):
+    # the large GPU parity cases quantise their operands in row chunks in worker processes:
+    # the bytes must be those of one oracle call on the whole matrix (NVFP4: the chunks take
+    # the whole matrix's tensor scale); rows = 300 gives chunks of unequal size
+    import oracle_pool
+    from oracle import layout as L
+    x = synth.normal_rowscaled(300, 256, seed=9)
+    x[17] *= 40.0                        # the tensor amax sits in one chunk only
+    if kind == "mxfp8":
+        want_c, want_s = Q.quantize_mxfp8(x)
+        want_g = None
+    else:
+        want_c, want_s, want_g = Q.quantize_nvfp4(x)
+    for parts in (1, 7):
+        c, s, g = oracle_pool.quantize_rows(kind, x, parts=parts)
+        assert np.array_equal(c, want_c) and np.array_equal(s, want_s) and g == want_g
+    pool = oracle_pool.spawn_pool(2)
+    try:
+        c, sw, g = oracle_pool.operand(kind, x, pool)
+    finally:
+        pool.close()
+        pool.join()
+    assert np.array_equal(c, want_c) and np.array_equal(sw, L.swizzle(want_s)) and g == want_g
