@@ -133,8 +133,12 @@ def reference(prob, out, bias_vals=None, silu=False, rows=None, epi=None):
 # the accumulation error as a fraction of sum|a b| once output rounding and the fast SiLU's
 # float32 error are taken out, and asserts r <= SECONDARY_REL.  Where sum|a b| is 0 (rows of A
 # all zero) the output must be within one ulp plus the SiLU term.  The largest r of a run is
-# printed at the end of the session (tests/conftest.py).
-SECONDARY_REL = None
+# printed at the end of the session (tests/conftest.py).  On GB300 the 296 checks of the GPU
+# suite (every kernel family, K up to 14336, the 8192^3 configurations) measured r <= 2.1e-8
+# (about 2^-25.5: the tensor cores' FP32 accumulation); the bound leaves a factor of 500 above
+# that and is still far below the error of one block scale off by one code (> 2^-13 at K = 4096,
+# tests/test_oracle_gemm.py).
+SECONDARY_REL = 2.0 ** -16
 RECORD = []
 
 

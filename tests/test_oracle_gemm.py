@@ -304,13 +304,13 @@ def test_parity_tolerance_catches_plausible_mistakes(kind):
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 def test_secondary_bound_catches_small_mistakes(kind):
     # Mistakes that the stated bar misses, or catches in a few elements only, at K = 4096 must
-    # exceed the secondary bound of the GPU parity checks (an accumulation error of at most
-    # 2^-13 sum|a b| beyond one output ulp): the oracle's result computed with one block scale of
-    # A one code too large (within the stated bar everywhere), and with one k-tile of the kernels
-    # (128 E4M3 / 256 E2M1 values) left out of every dot product.  The oracle's own result
-    # measures 0.
+    # exceed 2^-13 sum|a b| beyond one output ulp, eight times the secondary bound of the GPU
+    # parity checks: the oracle's result computed with one block scale of A one code too large
+    # (within the stated bar everywhere), and with one k-tile of the kernels (128 E4M3 / 256 E2M1
+    # values) left out of every dot product.  The oracle's own result measures 0.
     import parity_util as P
     bound = 2.0 ** -13
+    assert P.SECONDARY_REL <= bound / 8
     M, N, K = 128, 128, 4096
     blk = 32 if kind == "mxfp8" else 16
     prob = P.make_problem(kind, M, N, K, seed_a=31, seed_b=32)
