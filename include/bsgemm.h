@@ -203,8 +203,9 @@ bsg_status bsg_plan_check_status(bsg_plan_t plan);
 const char* bsg_plan_variant(bsg_plan_t plan);
 
 /* One-shot calls: look the problem up in a process-wide plan cache (keyed on every
- * argument and the device), create the plan on a miss, and run it.  After the first call
- * with given arguments, a call costs a hash lookup and one launch. */
+ * argument but alpha, and the device), create the plan on a miss, and run it.  After the first
+ * call with given arguments, a call costs a lookup (lock-free when the calling thread used the
+ * same arguments recently) and one launch. */
 bsg_status mxfp8_gemm(void* D, const void* A, const void* B, const void* SFA, const void* SFB,
                       float alpha, int M, int N, int K, bsg_out out, bsg_stream_t stream);
 
@@ -240,7 +241,8 @@ bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream);
  * bounded wait since the last check (its output is then incomplete).  Allocates nothing. */
 bsg_status bsg_noalloc_check_status(bsg_stream_t stream);
 
-/* Drop every plan of the one-shot cache (after the work using them has completed). */
+/* Drop every plan of the one-shot cache.  Call it after the work using them has completed and
+ * while no other thread is inside a one-shot call. */
 bsg_status bsg_cache_clear(void);
 
 /* Bytes of the swizzled scale buffer of a rows x K operand: 128*ceil(rows/128) *
