@@ -485,13 +485,16 @@ __device__ __forceinline__ void store_chunk32(const GemmParams& p, int b, int m,
 }
 
 // The epilogue on 4 accumulator values of row m, columns n..n+3, with the bias preloaded
-// (braw); packed two per word.  EXT: the residual and per-column factors too (alpha_m is then
-// row_alpha(alpha, m)); without it, the plain path's arithmetic exactly.
+// (braw), into y before the output rounding.  EXT: the residual and per-column factors too
+// (alpha_m is then row_alpha(alpha, m)); without it, the plain path's arithmetic exactly.
 template <int OUT, bool EXT>
-__device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, int b, int m, int n, const float4& a,
-                                                uint2 braw, float alpha_m) {
+__device__ __forceinline__ void epi4_values(const GemmParams& p, int b, int m, int n, const float4& a, uint2 braw,
+                                            float alpha_m, float (&y)[4]) {
   const uint16_t* bv = reinterpret_cast<const uint16_t*>(&braw);
-  float y[4] = {a.x, a.y, a.z, a.w};
+  y[0] = a.x;
+  y[1] = a.y;
+  y[2] = a.z;
+  y[3] = a.w;
   const bool has_bias = (p.flags & F_BIAS) != 0;
   if (!EXT || !(p.flags & F_ALPHA_COL)) {
 #pragma unroll
@@ -511,7 +514,45 @@ __device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, int b, int 
     for (int i = 0; i < 4; ++i) y[i] = __fmaf_rn(p.beta, out_to_float<OUT>(c[i]), y[i]);
   }
   if (p.flags & F_SILU) silu_inplace(y);
+}
+
+// The same, rounded to the output type and packed two per word.
+template <int OUT, bool EXT>
+__device__ __forceinline__ uint2 epi4_with_bias(const GemmParams& p, int b, int m, int n, const float4& a,
+                                                uint2 braw, float alpha_m) {
+  float y[4];
+  epi4_values<OUT, EXT>(p, b, m, n, a, braw, alpha_m, y);
   return make_uint2(pack2<OUT>(y[0], y[1]), pack2<OUT>(y[2], y[3]));
+}
+
+// NVFP4 output (OUT_NV4) of 4 reduced accumulator values a of row m, columns n..n+3: a quarter
+// of a 16-column block whose other quarters are in the three neighbouring lanes (lanes 4k ..
+// 4k+3 of the warp, all calling this for the same row and block).  The epilogue in float32 (bias
+// and C in BF16), then the quantiser's block encoding with the global scale *d_scale, the
+// block's amax taken across the four lanes: 2 code bytes into D (row-major, N/2 bytes a row),
+// and the scale byte from the block's first lane.  A row outside the problem stores no codes and
+// a zero scale; a block past N (N % 16 == 0: blocks are whole) inside the padded scale columns
+// a zero scale.
+template <bool EXT>
+__device__ __forceinline__ void nv4_quarter(const GemmParams& p, const UnitCoord& c, int m, int n, const float4& a,
+                                            uint2 braw, float alpha) {
+  const int blk = n >> 4;
+  const bool first = (n & 15) == 0;
+  if (n >= p.N) {
+    if (first && blk < p.sfd_cols4 * 4) p.sfd[sf_swizzle_offset(m, blk, p.sfd_cols4)] = 0;
+    return;
+  }
+  uint32_t sc = 0;
+  if (row_live<EXT>(p, c, m)) {
+    float y[4];
+    epi4_values<OUT_NV4, EXT>(p, c.batch, m, n, a, braw, EXT ? row_alpha(p, alpha, m) : alpha, y);
+    const float s = __ldg(p.d_scale);
+    uint32_t codes;
+    sc = nv_encode_quad(y, s, __fmul_rn(6.0f, s), codes);
+    *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(p.d) + static_cast<size_t>(m) * (p.N >> 1) + (n >> 1)) =
+        static_cast<uint16_t>(codes);
+  }
+  if (first) p.sfd[sf_swizzle_offset(m, blk, p.sfd_cols4)] = static_cast<uint8_t>(sc);
 }
 
 // Split-K through a cluster, owner side: the S partial slabs of this CTA's 128/S rows are in
@@ -552,9 +593,13 @@ __device__ __forceinline__ void cluster_reduce_s(const GemmParams& p, const floa
     // slab row rl holds tile row (rl / LPO) * 32 + split * LPO + rl % LPO, LPO = 32 / S
     const int row = (rl / (32 / S)) * 32 + c.split * (32 / S) + rl % (32 / S);
     const int m = c.m_blk * 128 + row;
-    if (row_live<EXT>(p, c, m) && n < p.N)  // N % 16 == 0: groups of 4 are whole
+    if constexpr (OUT == OUT_NV4) {
+      // four consecutive column groups (lanes 4k .. 4k+3: C4 is a multiple of 16) make a block
+      nv4_quarter<EXT>(p, c, m, n, acc, braw, alpha);
+    } else if (row_live<EXT>(p, c, m) && n < p.N) {  // N % 16 == 0: groups of 4 are whole
       *reinterpret_cast<uint2*>(d_row(p, c.batch, m) + n) =
           epi4_with_bias<OUT, EXT>(p, c.batch, m, n, acc, braw, EXT ? row_alpha(p, alpha, m) : alpha);
+    }
   }
 }
 
@@ -997,7 +1042,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
             if (row_in && n < p.N) st_out16(drow + n, reinterpret_cast<const uint32_t(&)[8]>(packed[8 * g]), wide);
           }
         }
-      } else if constexpr (BN >= 64 && OUT != OUT_NV4) {  // split-K: tiles 64 wide or more, 16-bit out
+      } else if constexpr (BN >= 64) {  // split-K: tiles 64 wide or more
         if (p.split_mode == SPLIT_CLUSTER) {
           // Split-K through the cluster (one unit per CTA).  Row `row` of the tile belongs to
           // split owner = lane / (32/S), so every warp holds rows of every owner.  Each thread
@@ -1109,7 +1154,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
                   v[4 * g + 3] += t.w;
                 }
               }
-              store_chunk32<OUT, EXT>(p, c.batch, m, row_in, nbase + ch * 32, v, alpha);
+              if constexpr (OUT == OUT_NV4)
+                epilogue_row_nv4<2, EXT>(p, m, row_in, nbase + ch * 32, reinterpret_cast<const uint32_t*>(v), alpha);
+              else
+                store_chunk32<OUT, EXT>(p, c.batch, m, row_in, nbase + ch * 32, v, alpha);
             }
           }
           named_bar_sync(1, C::EPI_THREADS);

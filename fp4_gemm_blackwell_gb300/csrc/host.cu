@@ -355,6 +355,8 @@ Variant choose_variant(const bsg_desc* d, int sms) {
     // of a 128 x bn FP32 tile), which moves ~5x slower than TMA fills.
     double best = 1e30;
     for (int cb : {128, 64}) {
+      // the NVFP4-output kernels that reduce split-K partials are the 64-wide ones
+      if (d->out == BSG_OUT_NVFP4 && cb != 64) continue;
       const long long tiles = mt * ((d->N + cb - 1) / cb) * L;
       const long long want = std::min<long long>(std::min<long long>(nkt, 8), std::max<long long>(1, sms / tiles));
       int cs = 1;
@@ -378,12 +380,7 @@ Variant choose_variant(const bsg_desc* d, int sms) {
   }
   if (fs >= 1) s = std::min(fs, nkt);
   if (b < 64) s = 1;  // 32-wide tiles never split K
-  if (d->out == BSG_OUT_NVFP4 && s > 1) {
-    // the NVFP4 output is encoded by the row-segment epilogues only: no split-K, and 32-wide
-    // tiles in its place (the most tiles for few rows)
-    s = 1;
-    if (fb == 0) b = 32;
-  }
+  if (d->out == BSG_OUT_NVFP4 && s > 1 && b != 64) s = 1;  // a forced other width runs unsplit
   // Two 128-byte k-slabs per ring stage halve the per-stage control (one barrier wait, one
   // commit, one scale staging per 8 MMAs) where the ring keeps three stages of the doubled size:
   // 64-wide tiles, and 128-wide tiles without a split-K receive area (measured: 128x4096x4096

@@ -35,6 +35,40 @@ static __device__ __noinline__ uint32_t e2m1_pair_div(float a, float b, float de
   return cvt_e2m1x2(__fdiv_rn(a, den), __fdiv_rn(b, den)) & 0xFFu;
 }
 
+// The scale of one block from its amax, and what its elements' encoding needs.
+struct NvBlockScale {
+  uint32_t sc;  // UE4M3 scale code
+  float den;    // RN(value(sc) * s)
+  float inv;    // RN(1 / den) when fast
+  bool fast;    // den and 1 / den are normal float32 values
+};
+
+__device__ __forceinline__ NvBlockScale nv_block_scale(float bmax, float s, float d) {
+  NvBlockScale b;
+  const float t = (d != 0.0f) ? __fdiv_rn(bmax, d) : 0.0f;
+  b.sc = cvt_e4m3x2(t, 0.0f) & 0x7Fu;
+  b.den = __fmul_rn(ue4m3_value(b.sc), s);
+  b.fast = b.den >= 0x1p-126f && b.den <= 0x1p126f;
+  b.inv = b.fast ? __frcp_rn(b.den) : 0.0f;
+  return b;
+}
+
+// E2M1 codes of RN(x0 / den) and RN(x1 / den) in one byte (x0 in the low nibble), reached without
+// a division per element: p = RN(x * RN(1/den)) is within 2^-22.4 of x/den relative (and so of
+// RN(x/den)), and E2M1 rounding is monotone, so when p (1 - 2^-21) and p (1 + 2^-21) round to the
+// same code, that is the code of RN(x/den).  Pairs that straddle a rounding threshold, and blocks
+// whose den or 1/den is not a normal float32, take the IEEE division.
+__device__ __forceinline__ uint32_t nv_pair_code(float x0, float x1, const NvBlockScale& b) {
+  if (b.den == 0.0f) return 0u;
+  if (b.fast) {
+    const float p0 = __fmul_rn(x0, b.inv), p1 = __fmul_rn(x1, b.inv);
+    const uint32_t below = cvt_e2m1x2(__fmul_rn(p0, 1.0f - 0x1p-21f), __fmul_rn(p1, 1.0f - 0x1p-21f)) & 0xFFu;
+    const uint32_t above = cvt_e2m1x2(__fmul_rn(p0, 1.0f + 0x1p-21f), __fmul_rn(p1, 1.0f + 0x1p-21f)) & 0xFFu;
+    if (below == above) return below;
+  }
+  return e2m1_pair_div(x0, x1, b.den);
+}
+
 // One block of 16 values v -> its UE4M3 scale code (returned) and 16 E2M1 codes packed two per
 // byte, element 2j in the low nibble of byte j (lo: bytes 0..3, hi: bytes 4..7).
 __device__ __forceinline__ uint32_t nv_encode_block16(const float (&v)[16], float s, float d, uint32_t& lo,
@@ -42,36 +76,30 @@ __device__ __forceinline__ uint32_t nv_encode_block16(const float (&v)[16], floa
   float bmax = 0.0f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(v[j]));
-  const float t = (d != 0.0f) ? __fdiv_rn(bmax, d) : 0.0f;
-  const uint32_t sc = cvt_e4m3x2(t, 0.0f) & 0x7Fu;
-  const float den = __fmul_rn(ue4m3_value(sc), s);
-  // Element = E2M1(RN(x / den)), reached without a division per element: p = RN(x * RN(1/den)) is
-  // within 2^-22.4 of x/den relative (and so of RN(x/den)), and E2M1 rounding is monotone, so
-  // when p (1 - 2^-21) and p (1 + 2^-21) round to the same code, that is the code of RN(x/den).
-  // Pairs that straddle a rounding threshold, and blocks whose den or 1/den is not a normal
-  // float32, take the IEEE division.
-  const bool fast = den >= 0x1p-126f && den <= 0x1p126f;
-  const float inv = fast ? __frcp_rn(den) : 0.0f;
+  const NvBlockScale b = nv_block_scale(bmax, s, d);
   lo = 0;
   hi = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    uint32_t byte = 0;
-    if (den != 0.0f) {
-      bool exact = !fast;
-      if (fast) {
-        const float p0 = __fmul_rn(v[2 * j], inv), p1 = __fmul_rn(v[2 * j + 1], inv);
-        const uint32_t below = cvt_e2m1x2(__fmul_rn(p0, 1.0f - 0x1p-21f), __fmul_rn(p1, 1.0f - 0x1p-21f)) & 0xFFu;
-        const uint32_t above = cvt_e2m1x2(__fmul_rn(p0, 1.0f + 0x1p-21f), __fmul_rn(p1, 1.0f + 0x1p-21f)) & 0xFFu;
-        byte = below;
-        exact = below != above;
-      }
-      if (exact) byte = e2m1_pair_div(v[2 * j], v[2 * j + 1], den);
-    }
+    const uint32_t byte = nv_pair_code(v[2 * j], v[2 * j + 1], b);
     if (j < 4) lo |= byte << (8 * j);
     else hi |= byte << (8 * (j - 4));
   }
-  return sc;
+  return b.sc;
+}
+
+// The same encoding with the block's 16 values spread over four neighbouring lanes of a warp
+// (lanes 4k .. 4k+3, all calling this together), four each: v holds elements 4q .. 4q+3 of the
+// block, q = lane % 4.  Every lane gets the block's scale code (returned, from the amax of all 16)
+// and its own four E2M1 codes in `codes` (16 bits: element 4q in the low nibble).
+__device__ __forceinline__ uint32_t nv_encode_quad(const float (&v)[4], float s, float d, uint32_t& codes) {
+  const unsigned mask = 0xFu << (threadIdx.x & 28u);
+  float bmax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  bmax = fmaxf(bmax, __shfl_xor_sync(mask, bmax, 1));
+  bmax = fmaxf(bmax, __shfl_xor_sync(mask, bmax, 2));
+  const NvBlockScale b = nv_block_scale(bmax, s, d);
+  codes = nv_pair_code(v[0], v[1], b) | (nv_pair_code(v[2], v[3], b) << 8);
+  return b.sc;
 }
 
 }  // namespace bsg

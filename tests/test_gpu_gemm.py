@@ -497,23 +497,13 @@ def test_run_operands(kind, env, monkeypatch):
         assert "pair" in variant, variant
 
 
-@pytest.mark.parametrize("env", [{}, {"BSG_FORCE_BN": 64}, {"BSG_FORCE_BN": 128}, {"BSG_FORCE_BN": 256},
-                                 {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 32},
-                                 {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2}])
-@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
-def test_nvfp4_output(kind, env, monkeypatch):
-    # D written as NVFP4 (E2M1 codes + swizzled UE4M3 scales, global scale from the device) by
-    # every kernel family; M and N ragged (N/16 = 17 scale columns: 3 of padding), bias (+ SiLU),
-    # and with some families the residual and both factor vectors.  Checked by intervals and
-    # agreement against the oracle's quantisation of its own result, the scale padding zero, the
-    # buffers' margins untouched; a forced split-K does not apply; a pointer-agnostic run into
-    # second buffers gives the same bytes.
+def _nvfp4_output_case(kind, env, M, N, K, extra, monkeypatch):
+    """One GEMM with NVFP4 output under `env`, checked against the oracle (see test_nvfp4_output);
+    returns the plan's variant."""
     for k, v in env.items():
         monkeypatch.setenv(k, str(v))
-    M, N, K = 300, 272, 1024
     silu = kind == "nvfp4"
     prob = P.make_problem(kind, M, N, K, seed_a=7, seed_b=8)
-    extra = env.get("BSG_FORCE_BN") in (64, 256)
     bias_bits, bias_vals = synth.bias(N, out="bf16")
     bias = P.dev(bias_bits.view(np.int16)).view(torch.int16)
     epi, C, ar, ac = None, None, None, None
@@ -530,7 +520,6 @@ def test_nvfp4_output(kind, env, monkeypatch):
     s = np.float32(np.float32(np.max(np.abs(y))) / np.float32(2688.0))   # the recipe's tensor scale
     d_scale = torch.tensor([float(s)], dtype=torch.float32, device="cuda")
     nsf = bsg.bsg_sf_bytes(bsg.BSG_NVFP4, M, N)
-    assert nsf == 384 * 20
     pad = 256
 
     def buffers():
@@ -551,12 +540,52 @@ def test_nvfp4_output(kind, env, monkeypatch):
         plan.run_operands(A, B, SFA, SFB, D2, bias=bias, C=C, alpha_row=ar, alpha_col=ac, SFD=SFD2, d_scale=d_scale)
         plan.check_status()
     torch.cuda.synchronize()
-    assert "_s1" in variant or "pair" in variant, variant
     db, sb = dbuf.cpu().numpy(), sbuf.cpu().numpy()
     assert np.all(db[:pad] == 0xCD) and np.all(db[-pad:] == 0xCD), "D margins written (%s)" % variant
     assert np.all(sb[:pad] == 0xAB) and np.all(sb[-pad:] == 0xAB), "SFD margins written (%s)" % variant
     P.check_nvfp4_output(db[pad:-pad], sb[pad:-pad], prob, bias_vals, silu, s, epi=epi)
     assert np.array_equal(dbuf2.cpu().numpy(), db) and np.array_equal(sbuf2.cpu().numpy(), sb), variant
+    return variant
+
+
+@pytest.mark.parametrize("env", [{}, {"BSG_FORCE_BN": 64}, {"BSG_FORCE_BN": 128}, {"BSG_FORCE_BN": 256},
+                                 {"BSG_FORCE_PAIR": 1}, {"BSG_FORCE_BN": 32}, {"BSG_FORCE_BN": 128, "BSG_FORCE_SPLITS": 2}])
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_nvfp4_output(kind, env, monkeypatch):
+    # D written as NVFP4 (E2M1 codes + swizzled UE4M3 scales, global scale from the device) by
+    # every unsplit kernel family (and the default choice); M and N ragged (N/16 = 17 scale columns: 3 of padding), bias
+    # (+ SiLU), and with some families the residual and both factor vectors.  Checked by intervals
+    # and agreement against the oracle's quantisation of its own result, the scale padding zero,
+    # the buffers' margins untouched; a split forced on 128-wide tiles does not apply (the
+    # split-K reductions encode NVFP4 on 64-wide tiles); a pointer-agnostic run into second
+    # buffers gives the same bytes.
+    variant = _nvfp4_output_case(kind, env, 300, 272, 1024, env.get("BSG_FORCE_BN") in (64, 256), monkeypatch)
+    if env:
+        assert "_s1" in variant or "pair" in variant, variant
+
+
+@pytest.mark.parametrize("env,extra", [
+    ({"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2}, False),      # cluster reduction, 2 splits
+    ({"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 4}, True),       # cluster reduction, 4, residual + factors
+    ({"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 3}, True),       # through the workspace (3 splits)
+    ({"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2, "BSG_SPLIT_WORKSPACE": 1}, False),
+])
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_nvfp4_output_split_k(kind, env, extra, monkeypatch):
+    # NVFP4 output from the split-K reductions: in a cluster each block of 16 columns is encoded
+    # by four lanes that share its amax, through the workspace by the last split's row segments.
+    # M = 300 leaves rows of the last tile without a problem row (their scales zero), N = 272 puts
+    # scale columns 17..19 (padding) in the last 64-wide tile.
+    variant = _nvfp4_output_case(kind, env, 300, 272, 4096, extra, monkeypatch)
+    want = "_s%d%s_" % (env["BSG_FORCE_SPLITS"],
+                        "w" if ("BSG_SPLIT_WORKSPACE" in env or env["BSG_FORCE_SPLITS"] == 3) else "c")
+    assert "_bn64" in variant and want in variant, variant
+
+
+def test_nvfp4_output_skinny_default_splits(monkeypatch):
+    # the skinny shape with NVFP4 output takes the split-K variant of its 16-bit-output twin
+    variant = _nvfp4_output_case("nvfp4", {}, 128, 4096, 4096, False, monkeypatch)
+    assert "_bn64_s2c_" in variant, variant
 
 
 @pytest.mark.parametrize("env", [{}, {"BSG_FORCE_BN": 64, "BSG_FORCE_SPLITS": 2}, {"BSG_FORCE_PAIR": 1}])
