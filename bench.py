@@ -630,7 +630,7 @@ def small_config(bsg, peaks, steps=2000, warmup=20):
     return r
 
 
-def quantiser(bsg, peaks, kind, rows, K, bf16, steps=50, warmup=5):
+def quantiser(bsg, peaks, kind, rows, K, bf16, steps=50, warmup=5, scaled=False):
     """bsg_quantize / bsg_quantize_bf16 on a rows x K activation (float32 or BF16), timed as one
     CUDA-graph replay of `steps` calls.  Algorithmic bytes: the input once, the codes, the
     swizzled scale buffer (and the 4-byte global scale); NVFP4 reads its input twice (tensor
@@ -646,6 +646,10 @@ def quantiser(bsg, peaks, kind, rows, K, bf16, steps=50, warmup=5):
     sf = torch.empty(sf_bytes, dtype=torch.uint8, device="cuda")
     gs = torch.empty(1, dtype=torch.float32, device="cuda")
     fn = bsg.bsg_quantize_bf16 if bf16 else bsg.bsg_quantize
+    if scaled:   # NVFP4 with the global scale given (the tensor's own, from one bsg_quantize call)
+        (bsg.bsg_quantize_bf16 if bf16 else bsg.bsg_quantize)(k, xd, rows, K, codes, sf, gs)
+        torch.cuda.synchronize()
+        fn = lambda k_, x_, r_, K_, c_, s_, g_, st_: bsg.bsg_quantize_nvfp4_scaled(x_, r_, K_, c_, s_, g_, bf16, st_)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -670,7 +674,8 @@ def quantiser(bsg, peaks, kind, rows, K, bf16, steps=50, warmup=5):
     del g
     return {"us": round(us, 2), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
             "algorithmic_bytes": nbytes, "input": "bf16" if bf16 else "f32", "shape": [rows, K],
-            "launches_per_call": 1 if kind == "mxfp8" else 3}
+            "launches_per_call": 1 if kind == "mxfp8" or scaled else 3,
+            "global_scale": "given" if scaled else ("per tensor (amax pass)" if kind == "nvfp4" else None)}
 
 
 def launch_loop(bsg, calls=1000):
@@ -940,6 +945,9 @@ def main():
                 for bf in (False, True):
                     extras["quantize_%s_%s_8192x8192" % (kind, "bf16" if bf else "f32")] = quantiser(
                         bsg, peaks, kind, 8192, 8192, bf)
+            for bf in (False, True):
+                extras["quantize_nvfp4_given_scale_%s_8192x8192" % ("bf16" if bf else "f32")] = quantiser(
+                    bsg, peaks, "nvfp4", 8192, 8192, bf, scaled=True)
         cpu = cpu_baseline() if not args.quick else None
         result = {
             "metric": METRIC, "value": round(value, 4), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,

@@ -16,6 +16,7 @@ __all__ = [
     "bsg_plan_run", "bsg_plan_run_operands", "bsg_plan_destroy", "bsg_plan_check_status", "bsg_plan_variant",
     "bsg_plan_debug_set", "mxfp8_gemm", "nvfp4_gemm", "bsg_cache_clear", "bsg_last_error",
     "bsg_version", "Plan", "bsg_gemm_noalloc", "bsg_noalloc_check_status",
+    "bsg_quantize_nvfp4_scaled",
 ]
 
 BSG_MXFP8, BSG_NVFP4 = 0, 1
@@ -89,6 +90,7 @@ def lib():
         "bsg_sf_bytes": (ctypes.c_size_t, [i, i, i]),
         "bsg_quantize": (st, [i, vp, i, i, vp, vp, vp, vp]),
         "bsg_quantize_bf16": (st, [i, vp, i, i, vp, vp, vp, vp]),
+        "bsg_quantize_nvfp4_scaled": (st, [vp, i, i, i, vp, vp, vp, vp]),
         "bsg_last_error": (ctypes.c_char_p, []),
         "bsg_version": (ctypes.c_char_p, []),
     }
@@ -143,6 +145,12 @@ def bsg_quantize_bf16(kind, x, rows, K, codes, sf, global_scale=None, stream=Non
     """x: rows x K BF16 values (a torch.bfloat16 tensor or 16-bit integer bit patterns)."""
     _check(lib().bsg_quantize_bf16(kind, _ptr(x), rows, K, _ptr(codes), _ptr(sf), _ptr(global_scale),
                                    _stream(stream)))
+
+
+def bsg_quantize_nvfp4_scaled(x, rows, K, codes, sf, global_scale, bf16_input=False, stream=None):
+    """NVFP4 quantisation with the global scale given (device float), one pass; x float32 or BF16."""
+    _check(lib().bsg_quantize_nvfp4_scaled(_ptr(x), 1 if bf16_input else 0, rows, K, _ptr(codes), _ptr(sf),
+                                           _ptr(global_scale), _stream(stream)))
 
 
 def bsg_plan_create(kind, out, M, N, K, A, B, SFA, SFB, D, alpha=1.0, flags=0, bias=None, alpha_dev=None,

@@ -138,5 +138,10 @@ cudaError_t launch_quantize_nv(const float* x, int rows, int K, uint8_t* codes, 
                                float* global_scale, cudaStream_t s);
 cudaError_t launch_quantize_nv(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
                                float* global_scale, cudaStream_t s);
+// NVFP4 with the global scale given in device memory (one pass, no amax).
+cudaError_t launch_quantize_nv_scaled(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                                      const float* global_scale, cudaStream_t s);
+cudaError_t launch_quantize_nv_scaled(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                                      const float* global_scale, cudaStream_t s);
 
 }  // namespace bsg

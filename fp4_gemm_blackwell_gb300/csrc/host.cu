@@ -1004,6 +1004,34 @@ BSG_API bsg_status bsg_quantize_bf16(bsg_kind kind, const void* x, int rows, int
   return quantize_entry(kind, static_cast<const uint16_t*>(x), rows, K, codes, sf, global_scale, stream);
 }
 
+BSG_API bsg_status bsg_quantize_nvfp4_scaled(const void* x, int bf16_input, int rows, int K, void* codes, void* sf,
+                                             const float* global_scale, bsg_stream_t stream) {
+  if (rows < 1 || K < 32 || K % 32 || rows > kMaxDim || K > kMaxDim)
+    return fail(BSG_ERR_SHAPE, "quantise shape rows=%d K=%d (rows>=1, K>=32, K%%32==0, each <= 2^20)", rows, K);
+  if (!x || !codes || !sf || !global_scale) return fail(BSG_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf) || (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return fail(BSG_ERR_ALIGNMENT, "x, codes and sf must be 16-byte aligned, global_scale 4-byte aligned");
+  int dev = 0;
+  DeviceInfo di;
+  bsg_status s = current_device(&dev, &di);
+  if (s != BSG_OK) return s;
+  load_driver_entry_points();
+  const size_t elem = bf16_input ? 2 : 4;
+  if ((s = check_range(x, static_cast<size_t>(rows) * K * elem, BSG_ERR_SHAPE, "x")) != BSG_OK ||
+      (s = check_range(codes, code_row_bytes(BSG_NVFP4, K) * rows, BSG_ERR_SHAPE, "codes")) != BSG_OK ||
+      (s = check_range(sf, sf_bytes_of(BSG_NVFP4, rows, K), BSG_ERR_SCALE_LAYOUT, "sf")) != BSG_OK ||
+      (s = check_range(global_scale, 4, BSG_ERR_SHAPE, "global_scale")) != BSG_OK)
+    return s;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      bf16_input ? bsg::launch_quantize_nv_scaled(static_cast<const uint16_t*>(x), rows, K, static_cast<uint8_t*>(codes),
+                                                  static_cast<uint8_t*>(sf), global_scale, st)
+                 : bsg::launch_quantize_nv_scaled(static_cast<const float*>(x), rows, K, static_cast<uint8_t*>(codes),
+                                                  static_cast<uint8_t*>(sf), global_scale, st);
+  if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
+  return BSG_OK;
+}
+
 // ==================================================================== allocation-free GEMM
 // Some callers cannot allocate device memory at the point where they run a GEMM: code that
 // runs inside a custom allocator or memory-pool callback, an engine that forbids device

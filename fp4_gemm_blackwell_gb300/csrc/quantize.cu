@@ -66,16 +66,19 @@ __device__ __forceinline__ void load_f32(const uint16_t* p, float (&v)[N]) {
   }
 }
 
-template <typename T>
+// I: the index type of the (row, block) loop, 32-bit unsigned whenever the padded scale matrix has
+// fewer than 2^32 entries (a 64-bit division per block costs about as much as the block's
+// arithmetic).
+template <typename T, typename I>
 __global__ void __launch_bounds__(256) quantize_mx_kernel(const T* __restrict__ x, int rows, int K,
                                                           uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ sf, int rows_pad,
                                                           int cols4) {
   const int nblk = K / 32;
-  const int cols_pad = cols4 * 4;
-  const long long total = static_cast<long long>(rows_pad) * cols_pad;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+  const I cols_pad = static_cast<I>(cols4) * 4;
+  const I total = static_cast<I>(rows_pad) * cols_pad;
+  for (I i = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<I>(gridDim.x) * blockDim.x) {
     const int r = static_cast<int>(i / cols_pad);
     const int c = static_cast<int>(i % cols_pad);
     uint8_t code = 0;
@@ -110,8 +113,19 @@ __global__ void __launch_bounds__(256) amax_kernel(const T* __restrict__ x, long
                                                    unsigned* __restrict__ amax_bits) {
   float m = 0.0f;
   const long long n8 = n / 8;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  // four groups of eight per thread in flight at once, then the remainder one group at a time
+  for (; i + 3 * step < n8; i += 4 * step) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load_f32(x + (i + u * step) * 8, v[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[u][j]));
+  }
+  for (; i < n8; i += step) {
     float v[8];
     load_f32(x + i * 8, v);
 #pragma unroll
@@ -129,20 +143,24 @@ __global__ void __launch_bounds__(256) amax_kernel(const T* __restrict__ x, long
   }
 }
 
-template <typename T>
+// The (row, block) entries are visited from the end of the matrix backwards: the amax pass that
+// precedes this one read the matrix from the start, so its last rows are the ones still in L2.
+// SCALED: the global scale s is given (*scale_in, a float) instead of derived from the amax
+// pass's result (*scale_in holding the amax's bits).
+template <typename T, typename I, bool SCALED>
 __global__ void __launch_bounds__(256) quantize_nv_kernel(const T* __restrict__ x, int rows, int K,
                                                           uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ sf, int rows_pad,
                                                           int cols4,
-                                                          const unsigned* __restrict__ amax_bits) {
-  const float amax = __uint_as_float(*amax_bits);
-  const float s = __fdiv_rn(amax, 2688.0f);
+                                                          const unsigned* __restrict__ scale_in) {
+  const float s = SCALED ? __uint_as_float(*scale_in) : __fdiv_rn(__uint_as_float(*scale_in), 2688.0f);
   const float d = __fmul_rn(6.0f, s);
   const int nblk = K / 16;
-  const int cols_pad = cols4 * 4;
-  const long long total = static_cast<long long>(rows_pad) * cols_pad;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+  const I cols_pad = static_cast<I>(cols4) * 4;
+  const I total = static_cast<I>(rows_pad) * cols_pad;
+  for (I j = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; j < total;
+       j += static_cast<I>(gridDim.x) * blockDim.x) {
+    const I i = total - 1 - j;
     const int r = static_cast<int>(i / cols_pad);
     const int c = static_cast<int>(i % cols_pad);
     uint8_t code = 0;
@@ -175,7 +193,11 @@ cudaError_t quantize_mx(const T* x, int rows, int K, uint8_t* codes, uint8_t* sf
   const int rows_pad = (rows + 127) / 128 * 128;
   const int cols4 = (K / 32 + 3) / 4;
   const long long total = static_cast<long long>(rows_pad) * cols4 * 4;
-  quantize_mx_kernel<T><<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4);
+  if (total < (1LL << 32))
+    quantize_mx_kernel<T, uint32_t><<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4);
+  else
+    quantize_mx_kernel<T, unsigned long long><<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad,
+                                                                                     cols4);
   return cudaGetLastError();
 }
 
@@ -191,12 +213,42 @@ cudaError_t quantize_nv(const T* x, int rows, int K, uint8_t* codes, uint8_t* sf
   amax_kernel<T><<<grid_for(n / 8, 256), 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(global_scale));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  quantize_nv_kernel<T><<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad, cols4,
-                                                             reinterpret_cast<unsigned*>(global_scale));
+  if (total < (1LL << 32))
+    quantize_nv_kernel<T, uint32_t, false><<<grid_for(total, 256), 256, 0, s>>>(
+        x, rows, K, codes, sf, rows_pad, cols4, reinterpret_cast<unsigned*>(global_scale));
+  else
+    quantize_nv_kernel<T, unsigned long long, false><<<grid_for(total, 256), 256, 0, s>>>(
+        x, rows, K, codes, sf, rows_pad, cols4, reinterpret_cast<unsigned*>(global_scale));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   nv_finalize_kernel<<<1, 1, 0, s>>>(global_scale);
   return cudaGetLastError();
+}
+
+// NVFP4 with the global scale given: one pass, no amax.
+template <typename T>
+cudaError_t quantize_nv_scaled(const T* x, int rows, int K, uint8_t* codes, uint8_t* sf, const float* global_scale,
+                               cudaStream_t s) {
+  const int rows_pad = (rows + 127) / 128 * 128;
+  const int cols4 = (K / 16 + 3) / 4;
+  const long long total = static_cast<long long>(rows_pad) * cols4 * 4;
+  const unsigned* sc = reinterpret_cast<const unsigned*>(global_scale);
+  if (total < (1LL << 32))
+    quantize_nv_kernel<T, uint32_t, true><<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf, rows_pad,
+                                                                               cols4, sc);
+  else
+    quantize_nv_kernel<T, unsigned long long, true><<<grid_for(total, 256), 256, 0, s>>>(x, rows, K, codes, sf,
+                                                                                         rows_pad, cols4, sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_nv_scaled(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                                      const float* global_scale, cudaStream_t s) {
+  return quantize_nv_scaled(x, rows, K, codes, sf, global_scale, s);
+}
+cudaError_t launch_quantize_nv_scaled(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+                                      const float* global_scale, cudaStream_t s) {
+  return quantize_nv_scaled(x, rows, K, codes, sf, global_scale, s);
 }
 
 cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,

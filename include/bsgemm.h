@@ -275,6 +275,19 @@ bsg_status bsg_quantize(bsg_kind kind, const float* x, int rows, int K, void* co
 bsg_status bsg_quantize_bf16(bsg_kind kind, const void* x, int rows, int K, void* codes, void* sf,
                              float* global_scale, bsg_stream_t stream);
 
+/* NVFP4 quantisation with the global scale s given by the caller: *global_scale (a device float,
+ * read when the call runs, not written) takes the place of amax(|x|) / 2688, and steps 2-3 of the
+ * NVFP4 recipe above run unchanged in one pass over x, with no amax pass: block scale =
+ * UE4M3(amax_block / (6 s)), saturating at 448; element = E2M1(x / (scale * s)), saturating at 6;
+ * s = 0 gives all-zero codes and scales.  The recipe's own s reproduces bsg_quantize's bytes.  This
+ * is the quantiser in front of a GEMM whose activation scale is calibrated or carried over from the
+ * previous step (as the NVFP4-output epilogue takes its s), the way the "[QST] Performance
+ * overhead ..." page's Nvf4 GEMM receives a precomputed global alpha.  x holds rows x K float32
+ * values (bf16_input = 0) or BF16 values (bf16_input != 0), 16-byte aligned; codes, sf as for
+ * bsg_quantize.  Errors as bsg_quantize. */
+bsg_status bsg_quantize_nvfp4_scaled(const void* x, int bf16_input, int rows, int K, void* codes, void* sf,
+                                     const float* global_scale, bsg_stream_t stream);
+
 /* Last error message of the calling thread ("" if none). */
 const char* bsg_last_error(void);
 

@@ -170,3 +170,37 @@ def test_nv_elements_at_rounding_thresholds():
     _, _, s = Q.quantize_nvfp4(x)
     assert s == np.float32(1.0)
     check("nvfp4", x)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("rows,K,scale_factor", [(200, 96, 1.0), (1000, 512, 1.0), (256, 4096, 0.25),
+                                                  (129, 160, 3.0), (128, 256, 0.0)])
+def test_nvfp4_given_scale(rows, K, scale_factor, bf16):
+    # bsg_quantize_nvfp4_scaled: the recipe's steps 2-3 with the caller's global scale, one pass.
+    # Against the oracle's quantize_nvfp4(x, s) bit for bit: the tensor's own s (then also the
+    # bytes of bsg_quantize), a quarter of it (many blocks saturate at scale 448 and elements at
+    # +-6), three times it (small scales), and 0 (everything zero).
+    x = synth.normal_rowscaled(rows, K, seed=rows * 3 + K)
+    if bf16:
+        bits = synth.as_bf16_bits(x)
+        vals = F.decode_bf16(bits).astype(np.float32)
+        xd = torch.from_numpy(bits.view(np.int16)).cuda()
+    else:
+        vals = x
+        xd = torch.from_numpy(x).cuda()
+    s = np.float32(Q.nvfp4_global_scale(vals) * np.float32(scale_factor))
+    sd = torch.tensor([float(s)], dtype=torch.float32, device="cuda")
+    codes = torch.full((rows * K // 2,), 0xCD, dtype=torch.uint8, device="cuda")
+    sf = torch.full((bsg.bsg_sf_bytes(bsg.BSG_NVFP4, rows, K),), 0xAB, dtype=torch.uint8, device="cuda")
+    bsg.bsg_quantize_nvfp4_scaled(xd, rows, K, codes, sf, sd, bf16_input=bf16)
+    torch.cuda.synchronize()
+    oc, osf, _ = Q.quantize_nvfp4(vals, s)
+    assert np.array_equal(codes.cpu().numpy(), oc.ravel())
+    assert np.array_equal(sf.cpu().numpy(), L.swizzle(osf))
+    assert float(sd.item()) == float(s), "the global scale is read, not written"
+    if scale_factor == 1.0:
+        c2, sf2, _ = (gpu_quantize_bf16 if bf16 else gpu_quantize)("nvfp4", bits if bf16 else x)
+        assert np.array_equal(codes.cpu().numpy(), c2) and np.array_equal(sf.cpu().numpy(), sf2)
+    if scale_factor == 0.25:
+        sat = ((oc & 0x7) == 0x7) | (((oc >> 4) & 0x7) == 0x7)
+        assert (osf == 0x7E).any() and sat.any()   # saturation reached on both levels
