@@ -513,7 +513,7 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->k_tiles_per_split = v.pair ? g->num_k_tiles : v.kps;  // in ring stages
   g->units_per_batch = g->num_m_tiles * g->num_n_tiles * v.splits;
   g->num_units = g->units_per_batch * L;
-  g->group_m = 16;
+  g->group_m = std::max(1, env_int("BSG_GROUP_M", 16));  // m-tiles per rasterisation group
   g->debug_skip_first_load = 0;
   g->ring_stages = info.stages;
   if (v.mode == bsg::SPLIT_CLUSTER) {

@@ -123,6 +123,19 @@ def test_quantize_validation(L, args, status):
     assert L.bsg_quantize_bf16(kind, x, rows, K, codes, sf, gs, None) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    ((None, 0, 128, 256, 32, 48, 64), 1),      # null x
+    ((16, 0, 128, 256, 32, 48, None), 1),      # null global scale
+    ((16, 1, 0, 256, 32, 48, 64), 2),          # rows < 1
+    ((16, 0, 128, 48, 32, 48, 64), 2),         # K not a multiple of 32
+    ((24, 0, 128, 256, 32, 48, 64), 3),        # x not 16-byte aligned
+    ((16, 1, 128, 256, 32, 48, 66), 3),        # global scale not 4-byte aligned
+])
+def test_quantize_given_scale_validation(L, args, status):
+    x, bf16, rows, K, codes, sf, gs = args
+    assert L.bsg_quantize_nvfp4_scaled(x, bf16, rows, K, codes, sf, gs, None) == status
+
+
 def test_one_shot_validation(L):
     # N not a multiple of 16 and a device alpha through the host-alpha call are refused
     assert L.mxfp8_gemm(16, 32, 48, 64, 80, ctypes.c_float(1.0), 128, 120, 128, 1, None) == 2
@@ -158,3 +171,14 @@ def test_python_structures_match_the_header_layout():
         assert int(got[cname]) == ctypes.sizeof(py), cname
         for field, _ in py._fields_:
             assert int(got["%s.%s" % (cname, field)]) == getattr(py, field).offset, (cname, field)
+
+
+def test_allocation_free_entry_points_validate_before_device_work(L):
+    # a bad descriptor is refused by the allocation-free call as by plan creation; without a GPU
+    # the status query reports a CUDA error instead of crashing
+    d = bsg.BsgDesc(0, 1, 0, 128, 120, 128, 16, 32, 48, 64, None, 80, 1.0, None, None, 0.0, None, None, 0,
+                    0, 0, 0, 0, 0, 0, None, None, None)
+    assert L.bsg_gemm_noalloc(ctypes.byref(d), None) == 2          # N not a multiple of 16
+    assert L.bsg_gemm_noalloc(None, None) == 1
+    st = L.bsg_noalloc_check_status(None)
+    assert st in (0, 6, 7)                                          # OK / not sm_103 / CUDA error
