@@ -897,9 +897,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     // Per stage, each warp writes its TMEM lane quarter of the stage's scale slot with the layout
     // a 32x128b.warpx4 copy of the atoms produces: lane i, column 4j + k holds the four scales
     // (one 32-bit word of the atom's row i) of A row 32k + i of atom j, and column
-    // 4*NB*j + 4b + k those of B row 128b + 32k + i.  A tile narrower than its 128-row band uses
-    // words jq.. of each B atom row, jq = its first 32-row quarter of the band: they are rotated
-    // to the front.
+    // 4*NB*j + 4b + k those of B row 128b + 32k + i.  Of A's four columns the MMA reads, in lane
+    // quarter q, only column 4j + q (the scales of its own rows 32q + i), so each warp writes only
+    // that one.  A tile narrower than its 128-row band uses words jq.. of each B atom row, jq =
+    // its first 32-row quarter of the band: they are rotated to the front.
     const int q = warp & 3;
     int stage = 0;
     uint32_t phase = 0;
@@ -917,14 +918,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
         constexpr int GA = NA < 4 ? NA : 4;
 #pragma unroll
         for (int g0 = 0; g0 < NA; g0 += GA) {
-          uint32_t a[4 * GA], b[4 * C::NB * GA];
+          uint32_t a[GA], b[4 * C::NB * GA];
 #pragma unroll
           for (int t = 0; t < GA; ++t) {
-            const uint4 v = lds_u4(stage_sfa(stage) + 512 * (g0 + t) + 16 * lane);
-            a[4 * t] = v.x;
-            a[4 * t + 1] = v.y;
-            a[4 * t + 2] = v.z;
-            a[4 * t + 3] = v.w;
+            a[t] = lds_u32(stage_sfa(stage) + 512 * (g0 + t) + 16 * lane + 4 * q);  // this quarter's word
 #pragma unroll
             for (int rb = 0; rb < C::NB; ++rb) {
               const uint4 w = rotate_words(lds_u4(stage_sfb(stage) + rb * NA * 512 + 512 * (g0 + t) + 16 * lane), jq);
@@ -934,7 +931,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
               b[(C::NB * t + rb) * 4 + 3] = w.w;
             }
           }
-          tmem_st_cols(slot + 4 * g0, a);
+#pragma unroll
+          for (int t = 0; t < GA; ++t) tmem_st_32x32b_x1(slot + 4 * (g0 + t) + q, a[t]);
           tmem_st_cols(slot + C::SFA_COLS + 4 * C::NB * g0, b);
         }
         tmem_st_wait();

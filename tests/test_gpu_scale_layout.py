@@ -9,9 +9,10 @@ Two checks tie that reading to something outside this library:
 1. the hardware: ``tcgen05.cp`` with the 32x128b.warpx4 shape, the tensor cores' own way to load
    a scale atom, places shared-memory row i (16 bytes) of an atom into lane i of every 32-lane
    quarter of tensor memory as four 32-bit columns.  The probe copies an atom of random bytes
-   and reads the lanes back; the scale warps of the GEMM kernels write exactly that placement
-   (lane i, column k = word k of atom row i, in every quarter), so with the GEMM parity tests,
-   whose per-block scales vary, the oracle's byte order is the one the tensor cores consume;
+   and reads the lanes back; the scale warps of the GEMM kernels write that placement (lane i,
+   column k = word k of atom row i; for B in every quarter, for A only the column the MMA reads
+   in each quarter, k = q), so with the GEMM parity tests, whose per-block scales vary, the
+   oracle's byte order is the one the tensor cores consume;
 2. cuBLAS through ``torch._scaled_mm`` (where the installed PyTorch supports block-scaled
    operands on this GPU): the same codes and scale bytes, given to a second implementation of
    the published layout, must give the oracle's result; with the atom's row groups read in the
