@@ -385,12 +385,6 @@ __device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d, uint64_t adesc, uin
       : "memory");
 }
 
-// Pair copy of one 512-byte scale atom: each CTA of the pair copies the atom at `sdesc` in its
-// own shared memory into its own TMEM at `taddr` (issued once, by the leader).
-__device__ __forceinline__ void tc_cp_sf_atom_pair(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Arrive once on the barrier at offset `bar` of every CTA in cta_mask (the two CTAs of a pair, or
 // the leader alone) when the pair's tensor-core operations issued so far by this thread complete.
 // A barrier arrive, not a data copy: nothing is loaded from global memory.
@@ -399,11 +393,6 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mas
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
       : "memory");
-}
-
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // ---------------------------------------------------------------- launch / cluster
@@ -418,7 +407,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // Shared memory of this CTA -> shared memory of a CTA of the cluster (dst and bar both in that
@@ -432,18 +420,7 @@ __device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// 16 bytes from registers into the shared memory of a CTA of the cluster (shared::cluster address
-// `dst`), counted as complete-tx bytes on that CTA's mbarrier `bar` (shared::cluster address).
-__device__ __forceinline__ void st_async_v4(uint32_t dst, float a, float b, float c, float d, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
-               "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
-               : "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -464,16 +441,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-
-// volatile keeps it after the cluster barrier that publishes the data; without a memory
-// clobber several loads can be issued before their results are used.
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-      : "r"(addr));
-  return v;
 }
 
 // ---------------------------------------------------------------- conversions
