@@ -37,9 +37,17 @@ enum : unsigned {
 
 // Kernel parameters, passed by value as a __grid_constant__ (the tensor maps must live in
 // parameter space for the TMA instructions).
+// Tensor-map slots per CTA of a pointer-agnostic run.
+constexpr int MAP_SLOTS_PER_CTA = 4;
+
 struct GemmParams {
   CUtensorMap tmap_a;  // A codes: bytes, dims {K bytes, M, batches}, box {128, 128, 1}, 128-byte swizzle
   CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N, b_entries}, box {128, BN, 1}, 128-byte swizzle
+  // Scale atoms of A and B for the CTA-pair kernel (zeroed for the others): 32-bit words, dims
+  // {128 (one 512-byte atom), bands x atoms per band, entries}, box {128, atoms per ring stage, 1},
+  // no swizzle; rows past the buffer read as zeros.
+  CUtensorMap tmap_sfa;
+  CUtensorMap tmap_sfb;
   const uint8_t* sfa;  // swizzled 128x4 scale atoms of A
   const uint8_t* sfb;
   const void* bias;    // N values of the output type (flags & F_BIAS)
@@ -69,13 +77,16 @@ struct GemmParams {
                            // below (1 when grouped)
   int b_entries;           // entries of B and SFB: L when batched, the G groups when grouped, else 1
   const int* group_index;  // grouped (F_GROUPED): the group of each of the M rows, -1 = no group
-  // Pointer-agnostic runs (EXT instantiations): when map_slots is set, each CTA's code producer
-  // copies tmap_a / tmap_b into its two 128-byte global slots (map_slots + 2 * blockIdx.x),
-  // replaces their global addresses by remap_a / remap_b and loads through the copies.  The
-  // host alternates between two slot sets from one such launch of a plan to the next.
+  // Pointer-agnostic runs (EXT instantiations): when map_slots is set, each CTA copies its tensor
+  // maps (tmap_a, tmap_b, and in the CTA-pair kernel tmap_sfa, tmap_sfb) into its 128-byte global
+  // slots (map_slots + MAP_SLOTS_PER_CTA * blockIdx.x), replaces their global addresses by
+  // remap_a, remap_b (remap_sfa, remap_sfb) and loads through the copies.  The host alternates
+  // between two slot sets from one such launch of a plan to the next.
   CUtensorMap* map_slots;
   const void* remap_a;
   const void* remap_b;
+  const void* remap_sfa;
+  const void* remap_sfb;
   int units_per_batch;     // num_m_tiles * num_n_tiles * splits
   long long sfa_batch, sfb_batch;  // bytes between the scale buffers of consecutive entries (groups)
   long long d_batch, c_batch;      // 16-bit elements between consecutive D (C) matrices

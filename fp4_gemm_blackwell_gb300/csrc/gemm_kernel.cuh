@@ -186,6 +186,28 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t pari
   }
 }
 
+// The same wait performed by a whole warp, which leaves it together: every lane polls (each
+// acquiring the barrier's phase for itself), and the loop's exit is decided by warp votes, so the
+// warp stays converged and values computed after the wait stay warp-uniform.
+__device__ __forceinline__ bool wait_bounded_cluster_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                          const GemmParams& p, unsigned who) {
+  if (__all_sync(0xffffffffu, mbar_try_wait_cluster(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_cluster(bar, parity))) return true;
+    const bool aborted = *abort_flag != 0;
+    const bool late = globaltimer_ns() - t0 > p.wait_limit_ns;
+    if (__any_sync(0xffffffffu, aborted || late)) {
+      if ((threadIdx.x & 31) == 0 && !aborted) {
+        *abort_flag = 1;
+        atomicOr(p.status, who);
+      }
+      __syncwarp();
+      return false;
+    }
+  }
+}
+
 // Named-barrier AND over `nthreads` threads: every participant gets the same answer.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
   uint32_t r;
@@ -702,7 +724,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
   const CUtensorMap* tma = &p.tmap_a;
   const CUtensorMap* tmb = &p.tmap_b;
   if (EXT && p.map_slots != nullptr) {
-    CUtensorMap* slot = p.map_slots + 2 * blockIdx.x;
+    CUtensorMap* slot = p.map_slots + MAP_SLOTS_PER_CTA * blockIdx.x;
     if (warp == 0 && lane == 0) {
       tmap_remap2(slot, &p.tmap_a, &p.tmap_b, p.remap_a, p.remap_b);
     }

@@ -16,13 +16,14 @@ namespace bsg {
 
 bool BSG_INST_NAME(gemm_pair_kernel_info_mx)(int out, GemmKernelInfo* info) {
   const char* e = std::getenv("BSG_PAIR_KC");
-  const int kc = (e != nullptr && std::atoi(e) == 1) ? 1 : 2;  // two k-tiles per stage unless forced
+  const int kc = (e != nullptr && std::atoi(e) == 2) ? 2 : 1;  // one k-slab per stage unless forced (more, smaller stages)
   if (kc == 2 && out == OUT_F16) return fill_pair_kernel_info<KIND_MX, 2, OUT_F16, BSG_INST_EXT>(info);
   if (kc == 2 && out == OUT_BF16) return fill_pair_kernel_info<KIND_MX, 2, OUT_BF16, BSG_INST_EXT>(info);
   if (out == OUT_F16) return fill_pair_kernel_info<KIND_MX, 1, OUT_F16, BSG_INST_EXT>(info);
   if (out == OUT_BF16) return fill_pair_kernel_info<KIND_MX, 1, OUT_BF16, BSG_INST_EXT>(info);
 #ifdef BSG_INST_NV4
-  if (kc == 2 && out == OUT_NV4) return fill_pair_kernel_info<KIND_MX, 2, OUT_NV4, true>(info);
+  if (out == OUT_NV4) return kc == 2 ? fill_pair_kernel_info<KIND_MX, 2, OUT_NV4, true>(info)
+                                     : fill_pair_kernel_info<KIND_MX, 1, OUT_NV4, true>(info);
 #endif
   return false;
 }

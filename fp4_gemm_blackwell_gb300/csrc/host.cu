@@ -275,7 +275,7 @@ struct bsg_plan_s {
   bsg::GemmParams params;
   bsg::GemmKernelInfo info;
   const void* fn_ext;        // the EXT instantiation of the same variant (bsg_plan_run_operands)
-  CUtensorMap* map_slots;    // two sets of two 128-byte tensor-map slots per CTA, in the workspace
+  CUtensorMap* map_slots;    // two sets of MAP_SLOTS_PER_CTA 128-byte tensor-map slots per CTA, in the workspace
   unsigned remap_runs;       // pointer-agnostic launches so far (their parity picks the slot set)
   int device;
   int grid;
@@ -420,8 +420,8 @@ Variant choose_variant(const bsg_desc* d, int sms) {
 }
 
 // Workspace layout: [status word | per-tile counters | split-K partials (workspace mode) |
-// tensor-map slots (pointer-agnostic runs: two sets of two 128-byte maps per CTA of a grid of
-// `grid`)].
+// tensor-map slots (pointer-agnostic runs: two sets of MAP_SLOTS_PER_CTA 128-byte maps per CTA
+// of a grid of `grid`)].
 struct WorkspaceLayout {
   size_t cnt_off, part_off, part_bytes, slot_off, total;
 };
@@ -432,7 +432,7 @@ WorkspaceLayout workspace_layout(const Variant& v, int num_tiles, int grid) {
   w.part_off = w.cnt_off + (static_cast<size_t>(num_tiles) * 4 + 255) / 256 * 256;
   w.part_bytes = v.mode == bsg::SPLIT_WORKSPACE ? static_cast<size_t>(v.splits) * num_tiles * 128 * v.bn * 4 : 0;
   w.slot_off = (w.part_off + w.part_bytes + 255) / 256 * 256;
-  w.total = w.slot_off + static_cast<size_t>(grid) * 4 * sizeof(CUtensorMap);
+  w.total = w.slot_off + static_cast<size_t>(grid) * 2 * bsg::MAP_SLOTS_PER_CTA * sizeof(CUtensorMap);
   return w;
 }
 
@@ -447,6 +447,24 @@ bsg_status encode_operand(CUtensorMap* m, const void* ptr, uint64_t row_bytes, u
   const cuuint32_t rank = batches > 1 ? 3 : 2;
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(ptr), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(BSG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with driver error %d", name, static_cast<int>(r));
+  return BSG_OK;
+}
+
+// Tiled map of the scale atoms of one operand for the CTA-pair kernel: 512-byte atoms as rows of
+// 128 32-bit words, `rows` atoms per entry, `entries` entries `entry_bytes` apart; a box is the
+// `box_atoms` consecutive atoms of one ring stage of one 128-row band.
+bsg_status encode_scales(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t box_atoms, uint64_t entries,
+                         uint64_t entry_bytes, const char* name) {
+  cuuint64_t dims[3] = {128, rows, entries};
+  cuuint64_t strides[2] = {512, entry_bytes};
+  cuuint32_t box[3] = {128, box_atoms, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t rank = entries > 1 ? 3 : 2;
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<void*>(ptr), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(BSG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with driver error %d", name, static_cast<int>(r));
@@ -504,6 +522,17 @@ bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, 
   g->sfb_atoms_per_band = g->sfa_atoms_per_band;
   g->sfb_bands = (d->N + 127) / 128;
   g->sfa_bands = (d->M + 127) / 128;
+  if (v.pair) {
+    // the pair kernel loads its scale atoms with the pair form of the tiled copy, so that both
+    // CTAs' atoms complete on the leader's barrier
+    const uint32_t box_atoms = static_cast<uint32_t>(info.kc * (d->kind == BSG_MXFP8 ? 1 : 4));
+    const uint64_t apb = static_cast<uint64_t>(g->sfa_atoms_per_band);
+    if ((s = encode_scales(&g->tmap_sfa, d->SFA, g->sfa_bands * apb, box_atoms, L,
+                           L > 1 ? static_cast<uint64_t>(d->stride_SFA) : g->sfa_bands * apb * 512, "SFA")) != BSG_OK ||
+        (s = encode_scales(&g->tmap_sfb, d->SFB, g->sfb_bands * apb, box_atoms, LB,
+                           LB > 1 ? static_cast<uint64_t>(d->stride_SFB) : g->sfb_bands * apb * 512, "SFB")) != BSG_OK)
+      return s;
+  }
   g->num_m_tiles = v.pair ? (d->M + 255) / 256 : (d->M + 127) / 128;
   g->num_n_tiles = (d->N + v.bn - 1) / v.bn;
   g->num_k_tiles = (d->K + k_tile * info.kc - 1) / (k_tile * info.kc);  // ring stages of K
@@ -763,9 +792,11 @@ BSG_API bsg_status bsg_plan_run_operands(bsg_plan_t plan, const bsg_operands* op
   }
   // The kernel writes its slots before its programmatic-launch wait, while the plan's previous
   // launch may still run: consecutive pointer-agnostic launches take alternate slot sets.
-  g.map_slots = plan->map_slots + static_cast<size_t>(plan->remap_runs++ & 1u) * 2 * plan->grid;
+  g.map_slots = plan->map_slots + static_cast<size_t>(plan->remap_runs++ & 1u) * bsg::MAP_SLOTS_PER_CTA * plan->grid;
   g.remap_a = d.A;
   g.remap_b = d.B;
+  g.remap_sfa = d.SFA;
+  g.remap_sfb = d.SFB;
   return launch_with(&plan->lc, plan->fn_ext, plan->cu_fn_ext, g, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -395,6 +395,55 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mas
       : "memory");
 }
 
+// The same pair operations issued by a whole converged warp, one elected lane performing each
+// (elect.sync over the full warp elects the same lane every time, so the commit below tracks the
+// copies and MMAs that lane issued).  Issued this way, with warp-uniform operands, the tensor
+// pipe takes a scale-atom copy every ~22 cycles and overlaps copies with MMAs; from one lane
+// of a diverged warp each tcgen05 instruction held the issuing thread ~55-90 cycles.
+__device__ __forceinline__ void tc_cp_sf_atom_pair_warp(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf8_pair_warp(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                      uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_nvf4_pair_warp(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                      uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_mc_warp(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Arrive (release, cluster scope) on a barrier of another CTA of the cluster (shared::cluster
+// address, from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // ---------------------------------------------------------------- launch / cluster
 // Programmatic dependent launch: wait for the preceding grid in the stream to complete (its
 // memory visible); allow the next grid in the stream to begin launching.
