@@ -842,34 +842,78 @@ CASES = {
 def case_arm(args):
     """--case NAME: one workload, `steps` plain stream launches of its plan after `warmup`
     (for profiler captures and quick timing); prints one JSON line."""
+    if args.case in CUBLAS_CASES:
+        return cublas_case(args)
     import __graft_entry__
     import fp4_gemm_blackwell_gb300 as bsg
     __graft_entry__.build()
     torch.cuda.set_device(0)
     kind, M, N, K, out, bias, silu, *batch = CASES[args.case]
     prob = Problem(bsg, kind, M, N, K, out=out, bias=bias, silu=silu, copies=1, L=batch[0] if batch else 1)
-    stream = torch.cuda.Stream()
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            prob.plans[0].run(stream)
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(0)
-    clocks.start()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(args.steps):
-            prob.plans[0].run(stream)
-        end.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    us = start.elapsed_time(end) * 1e3 / args.steps
+    us, clk = time_launches(lambda stream: prob.plans[0].run(stream), args.steps, args.warmup)
     prob.plans[0].check_status()
     print(json.dumps({"case": args.case, "variant": prob.variant, "us_per_launch": round(us, 3),
                       "tflops": round(prob.flops() / (us * 1e-6) / 1e12, 2),
                       "gbs": round(prob.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
                       "clocks": clk}), flush=True)
     prob.close()
+    return 0
+
+
+def time_launches(launch, steps, warmup):
+    """`steps` launches of launch(stream) after `warmup`, with the clock sampler running: the
+    sampler starts first (its start-up is not in the timed region) and the launches queue
+    behind a device-side sleep, so the events measure back-to-back execution.  Returns
+    (us per launch, clock record)."""
+    stream = torch.cuda.Stream()
+    clocks = ClockSampler(0)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            launch(stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(2e6))
+        start.record(stream)
+        for _ in range(steps):
+            launch(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    return start.elapsed_time(end) * 1e3 / steps, clk
+
+
+# cuBLAS's block-scaled GEMM (through torch._scaled_mm) on the shapes of the 8192^3 workloads, for
+# a vendor-library figure beside the kernels' (no bias or SiLU: a plain GEMM with BF16 output).
+# Random code bytes and scale bytes of one binade; the result is not checked (the GPU tests pin the
+# scale layout against the same call).
+CUBLAS_CASES = {"cublas_nvfp4_8192": "nvfp4", "cublas_mxfp8_8192": "mxfp8"}
+
+
+def cublas_case(args):
+    torch.cuda.set_device(0)
+    kind = CUBLAS_CASES[args.case]
+    M = N = K = 8192
+    g = torch.Generator(device="cuda").manual_seed(1)
+
+    def operand(rows):
+        if kind == "nvfp4":
+            codes = torch.randint(0, 256, (rows, K // 2), dtype=torch.uint8, device="cuda", generator=g)
+            sf = torch.randint(0x30, 0x40, (rows * (K // 16),), dtype=torch.uint8, device="cuda", generator=g)
+            return codes.view(torch.float4_e2m1fn_x2), sf.view(torch.float8_e4m3fn)
+        codes = torch.randint(0, 256, (rows, K), dtype=torch.uint8, device="cuda", generator=g)
+        codes[(codes & 0x7F) == 0x7F] = 0  # no NaN codes
+        sf = torch.randint(120, 134, (rows * (K // 32),), dtype=torch.uint8, device="cuda", generator=g)
+        return codes.view(torch.float8_e4m3fn), sf.view(torch.float8_e8m0fnu)
+
+    (a, sa), (b, sb) = operand(M), operand(N)
+    us, clk = time_launches(lambda stream: torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb,
+                                                             out_dtype=torch.bfloat16),
+                            args.steps, args.warmup)
+    print(json.dumps({"case": args.case, "library": "cuBLAS via torch._scaled_mm " + torch.__version__,
+                      "us_per_launch": round(us, 3), "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1),
+                      "clocks": clk}), flush=True)
     return 0
 
 
@@ -890,7 +934,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only (no other workloads, no CPU baseline)")
-    ap.add_argument("--case", choices=sorted(CASES), help="time one workload with plain launches and exit")
+    ap.add_argument("--case", choices=sorted(CASES) + sorted(CUBLAS_CASES),
+                    help="time one workload with plain launches and exit")
     args = ap.parse_args()
     if args.case:
         return case_arm(args)
