@@ -154,8 +154,14 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
   const CUtensorMap* tmsb = &p.tmap_sfb;
   if (EXT && p.map_slots != nullptr) {
     CUtensorMap* slot = p.map_slots + MAP_SLOTS_PER_CTA * blockIdx.x;
+    // (written by lane 0; every lane of the producer warp acquires them, as the lane that issues
+    // its copies is an elected one)
     if (warp == 0 && lane == 0) tmap_remap2(slot, &p.tmap_a, &p.tmap_b, p.remap_a, p.remap_b);
     if (warp == 2 && lane == 0) tmap_remap2(slot + 2, &p.tmap_sfa, &p.tmap_sfb, p.remap_sfa, p.remap_sfb);
+    if (warp == 0 || warp == 2) {
+      __syncwarp();
+      tmap_acquire2(warp == 0 ? slot : slot + 2);
+    }
     tma = slot;
     tmb = slot + 1;
     tmsa = slot + 2;
@@ -171,91 +177,84 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
     setmaxnreg_dec<C::REGS_CTRL>();
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer (each CTA)
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        bool first = true;
-        for (int u = pair0; ok && u < p.num_units; u += pairs) {
-          const UnitCoord c = decode_unit<EXT>(p, u);
-          const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
-          for (int kt = c.kt0; kt < c.kt1; ++kt) {
-            if (!wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
-              ok = false;
-              break;
-            }
-            if (first && p.debug_skip_first_load) {
-              // test hook: leave this stage unfilled so that the waits downstream run out
-            } else {
-              // code tiles of both CTAs: one transaction on the leader's barrier
-              const uint32_t fb = mapa_shared(bar_full(stage), leader);
-              if (is_leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (C::A_BYTES + C::B_BYTES));
+      // The whole warp runs the loop; one elected lane issues each copy.
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool first = true;
+      for (int u = pair0; ok && u < p.num_units; u += pairs) {
+        const UnitCoord c = decode_unit<EXT>(p, u);
+        const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          ok = wait_bounded_cluster_warp(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER);
+          if (!ok) break;
+          if (first && p.debug_skip_first_load) {
+            // test hook: leave this stage unfilled so that the waits downstream run out
+          } else {
+            // code tiles of both CTAs: one transaction on the leader's barrier
+            const uint32_t fb = mapa_shared(bar_full(stage), leader);
+            if (is_leader) mbar_arrive_expect_tx_warp(bar_full(stage), 2 * (C::A_BYTES + C::B_BYTES));
 #pragma unroll
-              for (int j = 0; j < KC; ++j) {  // slabs past K read as zeros (their MMAs are skipped)
-                const int x = (kt * KC + j) * C::BK_BYTES;
-                const int yb = c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128;
-                if (EXT && p.batches > 1)
-                  tma_load_3d_pair(stage_a(stage) + j * C::SLAB_A, tma, fb, x, m_blk * C::BM, c.batch);
-                else
-                  tma_load_2d_pair(stage_a(stage) + j * C::SLAB_A, tma, fb, x, m_blk * C::BM);
-                if (EXT && p.b_entries > 1)
-                  tma_load_3d_pair(stage_b(stage) + j * C::SLAB_B, tmb, fb, x, yb, c.bsel);
-                else
-                  tma_load_2d_pair(stage_b(stage) + j * C::SLAB_B, tmb, fb, x, yb);
-              }
+            for (int j = 0; j < KC; ++j) {  // slabs past K read as zeros (their MMAs are skipped)
+              const int x = (kt * KC + j) * C::BK_BYTES;
+              const int yb = c.n_blk * C::BN + static_cast<int>(rank & 1u) * 128;
+              if (EXT && p.batches > 1)
+                tma_load_3d_pair_warp(stage_a(stage) + j * C::SLAB_A, tma, fb, x, m_blk * C::BM, c.batch);
+              else
+                tma_load_2d_pair_warp(stage_a(stage) + j * C::SLAB_A, tma, fb, x, m_blk * C::BM);
+              if (EXT && p.b_entries > 1)
+                tma_load_3d_pair_warp(stage_b(stage) + j * C::SLAB_B, tmb, fb, x, yb, c.bsel);
+              else
+                tma_load_2d_pair_warp(stage_b(stage) + j * C::SLAB_B, tmb, fb, x, yb);
             }
-            first = false;
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          }
+          first = false;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
       }
     } else if (warp == 2) {
       // ---------------------------------------------------------- TMA producer: scale atoms
-      // A second issuing thread (each copy instruction holds its thread for a hundred-odd
-      // cycles): this CTA's scale atoms of the stage, in the pair form of the tiled copy on the
-      // leader's `full`.  Whole boxes always (atoms past the buffer read as zeros), so the byte
-      // count is fixed: A's band of this CTA and both bands of B, for each CTA.
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        bool first = true;
-        for (int u = pair0; ok && u < p.num_units; u += pairs) {
-          const UnitCoord c = decode_unit<EXT>(p, u);
-          const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
-          for (int kt = c.kt0; kt < c.kt1; ++kt) {
-            if (!wait_bounded_cluster(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
-              ok = false;
-              break;
-            }
-            if (first && p.debug_skip_first_load) {
-              // test hook (see the code producer)
-            } else {
-              const uint32_t fb = mapa_shared(bar_full(stage), leader);
-              if (is_leader) mbar_arrive_expect_tx(bar_full(stage), 2 * (C::SFA_BYTES + C::SFB_BYTES));
-              const int row = kt * C::SF_ATOMS;
-              const int ya = m_blk * p.sfa_atoms_per_band + row;
-              if (EXT && p.batches > 1)
-                tma_load_3d_pair(stage_sfa(stage), tmsa, fb, 0, ya, c.batch);
-              else
-                tma_load_2d_pair(stage_sfa(stage), tmsa, fb, 0, ya);
+      // This CTA's scale atoms of the stage, in the pair form of the tiled copy on the leader's
+      // `full` (the whole warp runs the loop, one elected lane issues).  Whole boxes always (atoms
+      // past the buffer read as zeros), so the byte count is fixed: A's band of this CTA and both
+      // bands of B, for each CTA.
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool first = true;
+      for (int u = pair0; ok && u < p.num_units; u += pairs) {
+        const UnitCoord c = decode_unit<EXT>(p, u);
+        const int m_blk = c.m_blk * 2 + static_cast<int>(rank & 1u);
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          ok = wait_bounded_cluster_warp(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER);
+          if (!ok) break;
+          if (first && p.debug_skip_first_load) {
+            // test hook (see the code producer)
+          } else {
+            const uint32_t fb = mapa_shared(bar_full(stage), leader);
+            if (is_leader) mbar_arrive_expect_tx_warp(bar_full(stage), 2 * (C::SFA_BYTES + C::SFB_BYTES));
+            const int row = kt * C::SF_ATOMS;
+            const int ya = m_blk * p.sfa_atoms_per_band + row;
+            if (EXT && p.batches > 1)
+              tma_load_3d_pair_warp(stage_sfa(stage), tmsa, fb, 0, ya, c.batch);
+            else
+              tma_load_2d_pair_warp(stage_sfa(stage), tmsa, fb, 0, ya);
 #pragma unroll
-              for (int rb = 0; rb < 2; ++rb) {
-                const int yb = (c.n_blk * 2 + rb) * p.sfb_atoms_per_band + row;
-                if (EXT && p.b_entries > 1)
-                  tma_load_3d_pair(stage_sfb(stage) + rb * C::SF_ATOMS * 512, tmsb, fb, 0, yb, c.bsel);
-                else
-                  tma_load_2d_pair(stage_sfb(stage) + rb * C::SF_ATOMS * 512, tmsb, fb, 0, yb);
-              }
+            for (int rb = 0; rb < 2; ++rb) {
+              const int yb = (c.n_blk * 2 + rb) * p.sfb_atoms_per_band + row;
+              if (EXT && p.b_entries > 1)
+                tma_load_3d_pair_warp(stage_sfb(stage) + rb * C::SF_ATOMS * 512, tmsb, fb, 0, yb, c.bsel);
+              else
+                tma_load_2d_pair_warp(stage_sfb(stage) + rb * C::SF_ATOMS * 512, tmsb, fb, 0, yb);
             }
-            first = false;
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          }
+          first = false;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
       }

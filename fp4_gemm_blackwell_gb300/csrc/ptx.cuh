@@ -115,6 +115,41 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// The pair-form tiled loads and the expect-tx arrive issued by a whole converged warp, one
+// elected lane performing each (the same lane every time): with warp-uniform operands the issue
+// does not hold a diverged lane for a hundred-odd cycles per copy.
+__device__ __forceinline__ void tma_load_2d_pair_warp(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
+                                                      int32_t y) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_warp(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
+                                                      int32_t y, int32_t z) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_warp(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+// Acquire, for the calling thread's later TMA copies, two tensor maps that another thread of
+// the warp wrote (tmap_remap2, then __syncwarp).
+__device__ __forceinline__ void tmap_acquire2(const CUtensorMap* m) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m) : "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m + 1) : "memory");
+}
+
 // Copies of the tensor maps `src[0..1]` (kernel parameter space) in the 128-byte aligned global
 // slots `dst[0..1]`, their global addresses replaced by `addr[0..1]`, made visible to the
 // tensor-map proxy of the calling thread's later TMA copies: plain stores of the 2 x 128 bytes,

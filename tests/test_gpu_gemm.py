@@ -198,7 +198,11 @@ def test_output_only_16_byte_aligned(kind, env, monkeypatch):
 
 @pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("M,N,K,out", [(256, 256, 512, "bf16"), (300, 272, 1024, "f16"), (2048, 2560, 512, "bf16"),
-                                       (640, 768, 4096, "bf16")])
+                                       (640, 768, 4096, "bf16"),
+                                       # K past the last whole stage (NVFP4 stages take 256 of K,
+                                       # MXFP8 128): a last stage of 1 or 3 MMAs, its scale boxes
+                                       # reaching past K
+                                       (512, 512, 1056, "bf16"), (320, 512, 1184, "bf16")])
 def test_pair_kernel(kind, M, N, K, out, monkeypatch):
     # CTA-pair kernel (256 x 256 tiles on 2-CTA clusters): ragged M and N, both outputs,
     # more pair tiles than SM pairs (persistent loop)
