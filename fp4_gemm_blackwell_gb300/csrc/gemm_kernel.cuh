@@ -208,6 +208,26 @@ __device__ __forceinline__ bool wait_bounded_cluster_warp(uint32_t bar, uint32_t
   }
 }
 
+// The same at CTA scope (barriers only this CTA's threads and copies arrive on).
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  const GemmParams& p, unsigned who) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const bool aborted = *abort_flag != 0;
+    const bool late = globaltimer_ns() - t0 > p.wait_limit_ns;
+    if (__any_sync(0xffffffffu, aborted || late)) {
+      if ((threadIdx.x & 31) == 0 && !aborted) {
+        *abort_flag = 1;
+        atomicOr(p.status, who);
+      }
+      __syncwarp();
+      return false;
+    }
+  }
+}
+
 // Named-barrier AND over `nthreads` threads: every participant gets the same answer.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
   uint32_t r;
@@ -728,6 +748,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     if (warp == 0 && lane == 0) {
       tmap_remap2(slot, &p.tmap_a, &p.tmap_b, p.remap_a, p.remap_b);
     }
+    if (warp == 0) {  // every lane acquires them: the lane that issues the copies is elected
+      __syncwarp();
+      tmap_acquire2(slot);
+    }
     tma = slot;
     tmb = slot + 1;
   }
@@ -743,166 +767,160 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
     setmaxnreg_dec<C::REGS_CTRL>();
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer: code tiles
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        bool first = true;
-        for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit<EXT>(p, u);
-          if (EXT && c.skip) continue;
-          for (int kt = c.kt0; kt < c.kt1; ++kt) {
-            if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
-              ok = false;
-              break;
-            }
-            if (first && p.debug_skip_first_load) {
-              // test hook: leave this stage unfilled so that the MMA warp's wait runs out
-            } else {
-              const uint32_t fb = bar_full(stage);
-              mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+      // The whole warp runs the loop with warp-uniform values; one elected lane issues each copy
+      // (a diverged lane was held ~100 cycles per copy).
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool first = true;
+      for (int u = u0; ok && u < p.num_units; u += ustep) {
+        const UnitCoord c = decode_unit<EXT>(p, u);
+        if (EXT && c.skip) continue;
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          ok = wait_bounded_warp(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER);
+          if (!ok) break;
+          if (first && p.debug_skip_first_load) {
+            // test hook: leave this stage unfilled so that the MMA warp's wait runs out
+          } else {
+            const uint32_t fb = bar_full(stage);
+            mbar_arrive_expect_tx_warp(fb, C::A_BYTES + C::B_BYTES);
 #pragma unroll
-              for (int j = 0; j < KC; ++j) {  // k-slabs past K read as zeros (their MMAs are skipped)
-                const int x = (kt * KC + j) * C::BK_BYTES;
-                const uint32_t sa = stage_a(stage) + j * C::SLAB_A, sb = stage_b(stage) + j * C::SLAB_B;
-                if (EXT && p.batches > 1)
-                  tma_load_3d(sa, tma, fb, x, c.m_blk * C::BM, c.batch);
-                else
-                  tma_load_2d(sa, tma, fb, x, c.m_blk * C::BM);
-                if (EXT && p.b_entries > 1)
-                  tma_load_3d(sb, tmb, fb, x, c.n_blk * BN, c.bsel);
-                else
-                  tma_load_2d(sb, tmb, fb, x, c.n_blk * BN);
-              }
+            for (int j = 0; j < KC; ++j) {  // k-slabs past K read as zeros (their MMAs are skipped)
+              const int x = (kt * KC + j) * C::BK_BYTES;
+              const uint32_t sa = stage_a(stage) + j * C::SLAB_A, sb = stage_b(stage) + j * C::SLAB_B;
+              if (EXT && p.batches > 1)
+                tma_load_3d_warp(sa, tma, fb, x, c.m_blk * C::BM, c.batch);
+              else
+                tma_load_2d_warp(sa, tma, fb, x, c.m_blk * C::BM);
+              if (EXT && p.b_entries > 1)
+                tma_load_3d_warp(sb, tmb, fb, x, c.n_blk * BN, c.bsel);
+              else
+                tma_load_2d_warp(sb, tmb, fb, x, c.n_blk * BN);
             }
-            first = false;
-            if (++stage == nst) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          }
+          first = false;
+          if (++stage == nst) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
       }
     } else if (warp == 2) {
       // ------------------------------------------------------------ TMA producer: scale atoms
-      // A second issuing thread: each copy instruction holds its thread for a hundred-odd cycles,
-      // so the scale copies run beside the code-tile copies, into the same stage, completing on
-      // the stage's `sf_full` barrier, which the scale warps wait for; they in turn arrive on
-      // the stage's `full` barrier, so the MMA issuer waits once per k-tile.
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        bool first = true;
-        for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit<EXT>(p, u);
-          if (EXT && c.skip) continue;
-          const int band0 = c.n_blk * BN / 128;    // first scale band of the B tile
-          const bool a_band = c.m_blk < p.sfa_bands;  // false only for a cluster's m-tile beyond M
-          int bands = 0;
+      // A second issuing warp, so that the scale copies run beside the code-tile copies, into the
+      // same stage, completing on the stage's `sf_full` barrier, which the scale warps wait for;
+      // they in turn arrive on the stage's `full` barrier, so the MMA issuer waits once per
+      // k-tile.  Whole-warp loop, one elected lane per copy.
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool first = true;
+      for (int u = u0; ok && u < p.num_units; u += ustep) {
+        const UnitCoord c = decode_unit<EXT>(p, u);
+        if (EXT && c.skip) continue;
+        const int band0 = c.n_blk * BN / 128;    // first scale band of the B tile
+        const bool a_band = c.m_blk < p.sfa_bands;  // false only for a cluster's m-tile beyond M
+        int bands = 0;
 #pragma unroll
-          for (int rb = 0; rb < C::NB; ++rb) bands += (band0 + rb < p.sfb_bands) ? 1 : 0;
-          for (int kt = c.kt0; kt < c.kt1; ++kt) {
-            if (!wait_bounded(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER)) {
-              ok = false;
-              break;
+        for (int rb = 0; rb < C::NB; ++rb) bands += (band0 + rb < p.sfb_bands) ? 1 : 0;
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          ok = wait_bounded_warp(bar_empty(stage), phase ^ 1u, abort_flag, p, ST_TIMEOUT_PRODUCER);
+          if (!ok) break;
+          const int k_rem = p.K - kt * C::K_TILE;
+          const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
+          const int sf_atoms = KIND == KIND_MX ? (steps + 3) / 4 : steps;  // atoms K still covers
+          if (first && p.debug_skip_first_load) {
+            // test hook (see the code producer)
+          } else {
+            const uint32_t fb = bar_sf_full(stage);
+            mbar_arrive_expect_tx_warp(fb, static_cast<uint32_t>(((a_band ? 1 : 0) + bands) * sf_atoms * 512));
+            if (a_band) {
+              const uint8_t* sa = p.sfa + c.batch * p.sfa_batch + (static_cast<size_t>(c.m_blk) * p.sfa_atoms_per_band +
+                                           static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
+              bulk_load_warp(stage_sfa(stage), sa, sf_atoms * 512, fb);
             }
-            const int k_rem = p.K - kt * C::K_TILE;
-            const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
-            const int sf_atoms = KIND == KIND_MX ? (steps + 3) / 4 : steps;  // atoms K still covers
-            if (first && p.debug_skip_first_load) {
-              // test hook (see the code producer)
-            } else {
-              const uint32_t fb = bar_sf_full(stage);
-              mbar_arrive_expect_tx(fb, static_cast<uint32_t>(((a_band ? 1 : 0) + bands) * sf_atoms * 512));
-              if (a_band) {
-                const uint8_t* sa = p.sfa + c.batch * p.sfa_batch + (static_cast<size_t>(c.m_blk) * p.sfa_atoms_per_band +
+#pragma unroll
+            for (int rb = 0; rb < C::NB; ++rb) {
+              const int band = band0 + rb;
+              if (band < p.sfb_bands) {
+                const uint8_t* sb = p.sfb + c.bsel * p.sfb_batch + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
                                              static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
-                bulk_load(stage_sfa(stage), sa, sf_atoms * 512, fb);
-              }
-#pragma unroll
-              for (int rb = 0; rb < C::NB; ++rb) {
-                const int band = band0 + rb;
-                if (band < p.sfb_bands) {
-                  const uint8_t* sb = p.sfb + c.bsel * p.sfb_batch + (static_cast<size_t>(band) * p.sfb_atoms_per_band +
-                                               static_cast<size_t>(kt) * C::SF_ATOMS) * 512;
-                  bulk_load(stage_sfb(stage) + rb * C::SF_ATOMS * 512, sb, sf_atoms * 512, fb);
-                }
+                bulk_load_warp(stage_sfb(stage) + rb * C::SF_ATOMS * 512, sb, sf_atoms * 512, fb);
               }
             }
-            first = false;
-            if (++stage == nst) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          }
+          first = false;
+          if (++stage == nst) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        bool ok = true;
-        for (int u = u0; ok && u < p.num_units; u += ustep) {
-          const UnitCoord c = decode_unit<EXT>(p, u);
-          if (EXT && c.skip) continue;
-          if (!wait_bounded(bar_tempty(acc), acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int kt = c.kt0; kt < c.kt1; ++kt) {
-            if (!wait_bounded(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const int k_rem = p.K - kt * C::K_TILE;
-            const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
-            // the scale warps have put this stage's scales in its TMEM slot
-            const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS;
-            const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-            const uint32_t sa = stage_a(stage), sb = stage_b(stage);
-            // MMA j reads 32 bytes of K at offset 32 (j % 4) of k-slab j / 4; its scales are in
-            // atom j / 4 (MXFP8, byte j % 4 of each word) or atom j (NVFP4)
-            if constexpr (KIND == KIND_MX) {
-              for (int j = 0; j < steps; ++j) {
-                const uint32_t jj = static_cast<uint32_t>(j & 3), slab = static_cast<uint32_t>(j >> 2);
-                const uint32_t idesc = C::IDESC | (jj << 4) | (jj << 29);
-                tc_mma_mxf8(d_t, sdesc_kmajor_sw128(sa + slab * C::SLAB_A + 32 * jj),
-                            sdesc_kmajor_sw128(sb + slab * C::SLAB_B + 32 * jj), idesc, sfa_t + 4 * slab,
-                            sfb_t + 4 * C::NB * slab, (kt > c.kt0 || j > 0) ? 1u : 0u);
-              }
-            } else {
-              for (int j = 0; j < steps; ++j) {
-                const uint32_t jj = static_cast<uint32_t>(j & 3), slab = static_cast<uint32_t>(j >> 2);
-                tc_mma_nvf4(d_t, sdesc_kmajor_sw128(sa + slab * C::SLAB_A + 32 * jj),
-                            sdesc_kmajor_sw128(sb + slab * C::SLAB_B + 32 * jj), C::IDESC, sfa_t + 4 * j,
-                            sfb_t + 4 * C::NB * j, (kt > c.kt0 || j > 0) ? 1u : 0u);
-              }
-            }
-            tc_commit(bar_empty(stage));
-            if (++stage == nst) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
+      // The whole warp runs the loop with warp-uniform values; one elected lane issues each MMA
+      // and commit.
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = u0; ok && u < p.num_units; u += ustep) {
+        const UnitCoord c = decode_unit<EXT>(p, u);
+        if (EXT && c.skip) continue;
+        ok = wait_bounded_warp(bar_tempty(acc), acc_phase ^ 1u, abort_flag, p, ST_TIMEOUT_MMA);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          ok = wait_bounded_warp(bar_full(stage), phase, abort_flag, p, ST_TIMEOUT_MMA);
           if (!ok) break;
-          tc_commit(bar_tfull(acc));
-          if (C::NACC == 2) {
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+          tc_fence_after();
+          const int k_rem = p.K - kt * C::K_TILE;
+          const int steps = min(C::STEPS, (k_rem + C::MMA_K - 1) / C::MMA_K);
+          // the scale warps have put this stage's scales in its TMEM slot
+          const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_SLOT_COLS;
+          const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+          const uint32_t sa = stage_a(stage), sb = stage_b(stage);
+          const uint32_t acc0 = kt > c.kt0 ? 1u : 0u;
+          // MMA j reads 32 bytes of K at offset 32 (j % 4) of k-slab j / 4; its scales are in
+          // atom j / 4 (MXFP8, byte j % 4 of each word) or atom j (NVFP4)
+          auto mma = [&](int j, uint32_t accumulate) {
+            const uint32_t jj = static_cast<uint32_t>(j & 3), slab = static_cast<uint32_t>(j >> 2);
+            if constexpr (KIND == KIND_MX)
+              tc_mma_mxf8_warp(d_t, sdesc_kmajor_sw128(sa + slab * C::SLAB_A + 32 * jj),
+                               sdesc_kmajor_sw128(sb + slab * C::SLAB_B + 32 * jj), C::IDESC | (jj << 4) | (jj << 29),
+                               sfa_t + 4 * slab, sfb_t + 4 * C::NB * slab, accumulate);
+            else
+              tc_mma_nvf4_warp(d_t, sdesc_kmajor_sw128(sa + slab * C::SLAB_A + 32 * jj),
+                               sdesc_kmajor_sw128(sb + slab * C::SLAB_B + 32 * jj), C::IDESC, sfa_t + 4 * j,
+                               sfb_t + 4 * C::NB * j, accumulate);
+          };
+          if (steps == C::STEPS) {
+#pragma unroll
+            for (int j = 0; j < C::STEPS; ++j) mma(j, j == 0 ? acc0 : 1u);  // straight-line issue
           } else {
-            acc_phase ^= 1u;
+            for (int j = 0; j < steps; ++j) mma(j, j == 0 ? acc0 : 1u);  // the last, partial k-tile
+          }
+          tc_commit_warp(bar_empty(stage));
+          if (++stage == nst) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        if (!ok) {
-          // let every tensor-core operation issued so far finish before TMEM is released
-          tc_commit(bar_drain);
+        if (!ok) break;
+        tc_commit_warp(bar_tfull(acc));
+        if (C::NACC == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // let every tensor-core operation issued so far finish before TMEM is released
+        tc_commit_warp(bar_drain);
+        if (lane == 0) {
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(bar_drain, 0)) {
             if (globaltimer_ns() - t0 > 10000000ull) {
@@ -911,6 +929,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN, KC>::THREADS, 1) bsg_gemm_ke
             }
           }
         }
+        __syncwarp();
       }
     }
   } else if (warp < C::EPI_WARP0) {
