@@ -1,7 +1,6 @@
 // Internal declarations shared by the host side and the kernels of the block-scaled GEMM.
 #pragma once
 
-#include <cstddef>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,11 +42,6 @@ constexpr int MAP_SLOTS_PER_CTA = 4;
 struct GemmParams {
   CUtensorMap tmap_a;  // A codes: bytes, dims {K bytes, M, batches}, box {128, 128, 1}, 128-byte swizzle
   CUtensorMap tmap_b;  // B codes: bytes, dims {K bytes, N, b_entries}, box {128, BN, 1}, 128-byte swizzle
-  // Scale atoms of A and B for the CTA-pair kernel (zeroed for the others): 32-bit words, dims
-  // {128 (one 512-byte atom), bands x atoms per band, entries}, box {128, atoms per ring stage, 1},
-  // no swizzle; rows past the buffer read as zeros.
-  CUtensorMap tmap_sfa;
-  CUtensorMap tmap_sfb;
   const uint8_t* sfa;  // swizzled 128x4 scale atoms of A
   const uint8_t* sfb;
   const void* bias;    // N values of the output type (flags & F_BIAS)
@@ -78,7 +72,7 @@ struct GemmParams {
   int b_entries;           // entries of B and SFB: L when batched, the G groups when grouped, else 1
   const int* group_index;  // grouped (F_GROUPED): the group of each of the M rows, -1 = no group
   // Pointer-agnostic runs (EXT instantiations): when map_slots is set, each CTA copies its tensor
-  // maps (tmap_a, tmap_b, and in the CTA-pair kernel tmap_sfa, tmap_sfb) into its 128-byte global
+  // maps (tmap_a, tmap_b, and in the CTA-pair kernel PairParams::tmap_sfa, tmap_sfb) into its 128-byte global
   // slots (map_slots + MAP_SLOTS_PER_CTA * blockIdx.x), replaces their global addresses by
   // remap_a, remap_b (remap_sfa, remap_sfb) and loads through the copies.  The host alternates
   // between two slot sets from one such launch of a plan to the next.
@@ -99,6 +93,20 @@ struct GemmParams {
                            // make room for split-K receive slots)
   int debug_skip_first_load;  // test hook: the producer never loads its first stage
 };
+// The CTA-pair kernel's parameters: GemmParams, then the tiled maps of the scale atoms of A and B
+// (32-bit words, dims {128 (one 512-byte atom), bands x atoms per band, entries}, box {128, atoms
+// per ring stage, 1}, no swizzle; rows past the buffer read as zeros).  The host builds this
+// superset for every plan; a 1-SM kernel, whose parameter is GemmParams, is launched with the
+// same block and receives its first sizeof(GemmParams) bytes (the launch copies as many bytes
+// as the kernel's parameter holds): 640 bytes instead of 896, a shorter launch (host time per
+// launch of an empty cluster kernel: 1.47 us with 512 bytes of parameters, 1.56 with 768).
+struct PairParams : GemmParams {
+  CUtensorMap tmap_sfa;
+  CUtensorMap tmap_sfb;
+};
+static_assert(sizeof(GemmParams) % 64 == 0 && sizeof(PairParams) == sizeof(GemmParams) + 2 * sizeof(CUtensorMap),
+              "the pair kernel's parameter block extends the 1-SM one");
+
 
 struct GemmKernelInfo {
   const void* fn;

@@ -82,7 +82,7 @@ struct PairCfg {
 // Grouped problems never run here (a 256-row pair tile could span two groups); the host plans
 // them on 1-SM tiles.
 template <int KIND, int KC, int OUT, bool EXT>
-__global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_kernel(const __grid_constant__ PairParams p) {
   using C = PairCfg<KIND, KC>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);

@@ -272,7 +272,7 @@ struct LaunchCfg {
 struct bsg_plan_s {
   uint32_t magic;
   bsg_desc desc;
-  bsg::GemmParams params;
+  bsg::PairParams params;
   bsg::GemmKernelInfo info;
   const void* fn_ext;        // the EXT instantiation of the same variant (bsg_plan_run_operands)
   CUtensorMap* map_slots;    // two sets of MAP_SLOTS_PER_CTA 128-byte tensor-map slots per CTA, in the workspace
@@ -474,7 +474,7 @@ bsg_status encode_scales(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_
 // Kernel parameters of problem d under variant v (tensor maps encoded here), except the
 // workspace pointers.  Grid: persistent (<= #SMs) unless the splits form clusters, in which
 // case every unit is its own CTA.
-bsg_status fill_params(bsg::GemmParams* g, const bsg_desc* d, const Variant& v, const bsg::GemmKernelInfo& info,
+bsg_status fill_params(bsg::PairParams* g, const bsg_desc* d, const Variant& v, const bsg::GemmKernelInfo& info,
                        int sms, int* grid) {
   std::memset(g, 0, sizeof(*g));
   const size_t rb = code_row_bytes(d->kind, d->K);
@@ -605,9 +605,9 @@ void make_launch_config(LaunchCfg* lc, int grid, int threads, int smem, int clus
 }
 
 // One launch of `fn` (its driver handle `cu`, or null) with `params` on `stream`.
-bsg_status launch_with(LaunchCfg* lc, const void* fn, CUfunction cu, const bsg::GemmParams& params,
+bsg_status launch_with(LaunchCfg* lc, const void* fn, CUfunction cu, const bsg::PairParams& params,
                        cudaStream_t stream) {
-  void* args[] = {const_cast<bsg::GemmParams*>(&params)};
+  void* args[] = {const_cast<bsg::PairParams*>(&params)};
   if (cu != nullptr && g_launch != nullptr) {
     lc->drv.hStream = reinterpret_cast<CUstream>(stream);
     if (g_launch(&lc->drv, cu, args, nullptr) == CUDA_SUCCESS) return BSG_OK;
@@ -618,7 +618,7 @@ bsg_status launch_with(LaunchCfg* lc, const void* fn, CUfunction cu, const bsg::
   return BSG_OK;
 }
 
-bsg_status launch_gemm(const void* fn, const bsg::GemmParams& params, int grid, int threads, int smem,
+bsg_status launch_gemm(const void* fn, const bsg::PairParams& params, int grid, int threads, int smem,
                        int cluster, cudaStream_t stream) {
   LaunchCfg lc;
   make_launch_config(&lc, grid, threads, smem, cluster);
@@ -690,7 +690,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
   p->device = dev;
   p->workspace = nullptr;
   p->cluster = v.cluster;
-  bsg::GemmParams& g = p->params;
+  bsg::PairParams& g = p->params;
   if ((s = fill_params(&g, d, v, info, di.sms, &p->grid)) != BSG_OK) {
     delete p;
     return s;
@@ -732,7 +732,7 @@ bsg_status plan_create(bsg_plan_t* out, const bsg_desc* d) {
 
 bool plan_ok(bsg_plan_t p) { return p != nullptr && p->magic == kPlanMagic; }
 
-bsg_status plan_launch(bsg_plan_t p, const bsg::GemmParams& params, cudaStream_t stream) {
+bsg_status plan_launch(bsg_plan_t p, const bsg::PairParams& params, cudaStream_t stream) {
   return launch_with(&p->lc, p->info.fn, p->cu_fn, params, stream);
 }
 
@@ -777,7 +777,7 @@ BSG_API bsg_status bsg_plan_run_operands(bsg_plan_t plan, const bsg_operands* op
   bsg_status s = validate_desc(&d);
   if (s != BSG_OK) return s;
   if ((s = validate_ranges(&d)) != BSG_OK) return s;
-  bsg::GemmParams g = plan->params;
+  bsg::PairParams g = plan->params;
   g.sfa = static_cast<const uint8_t*>(d.SFA);
   g.sfb = static_cast<const uint8_t*>(d.SFB);
   g.bias = d.bias;
@@ -934,7 +934,7 @@ bsg_status cached_run(const bsg_desc& d, cudaStream_t stream) {
     te.gen = g_cache_gen.load(std::memory_order_relaxed);
   }
   if (plan->params.alpha == d.alpha) return plan_launch(plan, plan->params, stream);
-  bsg::GemmParams params = plan->params;  // alpha is not part of the key
+  bsg::PairParams params = plan->params;  // alpha is not part of the key
   params.alpha = d.alpha;
   return plan_launch(plan, params, stream);
 }
@@ -1121,7 +1121,7 @@ BSG_API bsg_status bsg_gemm_noalloc(const bsg_desc* d, bsg_stream_t stream) {
   const bool found = bsg::find_kernel(d->kind == BSG_MXFP8 ? bsg::KIND_MX : bsg::KIND_NV, out_t, d->flags, d->L,
                                       v.pair, v.bn, v.kc, &info);
   if (!found) return fail(BSG_ERR_DTYPE, "no kernel for this format / output type");
-  bsg::GemmParams g;
+  bsg::PairParams g;
   int grid = 0;
   if ((s = fill_params(&g, d, v, info, di.sms, &grid)) != BSG_OK) return s;
   // the same layout a plan's workspace has for this variant and tile count (no map slots)
