@@ -11,7 +11,7 @@
 //
 // Each ring stage holds a k-tile of both operands' codes and their scale atoms (A's 128 rows,
 // both 128-row bands of B).  Sixteen warps per CTA in four warpgroups (register budgets set
-// with setmaxnreg):
+// with setmaxnreg: 56 for the control warps, 152 for the epilogue's):
 //   warp 0       TMA producer of the A / B code tiles with the pair form of the copy,
 //                completing on the leader's `full` barrier (the leader posts both CTAs' bytes);
 //   warp 1       TMEM owner; on the leader, the whole warp issues the pair's MMAs, one elected
@@ -22,14 +22,16 @@
 //                from shared memory into the stage's TMEM slot (tcgen05.cp, each CTA's atoms into
 //                its own TMEM) and commits to `sf_ready`; issued from a warp of their own, the
 //                copies overlap the MMAs on the tensor pipe;
-//   warps 4..7   unused (their registers go to the epilogue);
-//   warps 8..15  epilogue of the CTA's 128 rows; each warp arrives on the leader's
-//                `tmem_empty` once per tile (the peer's through a multicast tcgen05.commit).
+//   warps 4..15  epilogue of the CTA's 128 rows, three warps per TMEM lane quarter (64, 96 and 96
+//                of a row's 256 columns); each warp arrives on the leader's `tmem_empty` once
+//                per tile (the peer's through a multicast tcgen05.commit).
 // The leader's tcgen05.commit is multicast to both CTAs' `empty` and `tmem_full` barriers.
 // TMEM: one 256-column accumulator, then one scale slot per ring stage, so a slot is free
 // again exactly when its stage is (the producer refills a stage only after the MMAs that read
 // its slot have completed).
 #pragma once
+
+#include <type_traits>
 
 #include "gemm_kernel.cuh"
 
@@ -64,13 +66,16 @@ struct PairCfg {
   static constexpr int SF_COL0 = BN;             // one 256-column accumulator first
   static constexpr int TMEM_USED = SF_COL0 + STAGES * SF_SLOT_COLS;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int IDLE_WARP0 = 4;
-  static constexpr int EPI_WARP0 = 8;
-  static constexpr int EPI_WARPS = 8;
+  // Epilogue: warps 4..15, three per TMEM lane quarter; of a row's 256 columns the first warp of
+  // a quarter takes 64, the other two 96 each (TMEM loads of 32 columns, output blocks of 16).
+  static constexpr int EPI_WARP0 = 4;
+  static constexpr int EPI_WARPS = 12;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = 32 * EPI_WARP0 + EPI_THREADS;
-  static constexpr int REGS_CTRL = 56, REGS_IDLE = 56, REGS_EPI = 184;
-  static_assert(REGS_CTRL + REGS_IDLE + 2 * REGS_EPI <= 512, "register split");
+  static constexpr int EPI_COLS_FIRST = 64, EPI_COLS = 96;
+  static_assert(EPI_COLS_FIRST + 2 * EPI_COLS == BN, "epilogue column split");
+  static constexpr int REGS_CTRL = 56, REGS_EPI = 152;
+  static_assert(REGS_CTRL + 3 * REGS_EPI <= 512, "register split");
   static_assert(THREADS == 512, "warpgroup layout");
   static constexpr uint32_t IDESC =
       (KIND == KIND_MX ? ((0u << 7) | (0u << 10) | (1u << 23)) : ((1u << 7) | (1u << 10) | (0u << 23))) |
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
   const int pair0 = blockIdx.x >> 1;
   const int pairs = gridDim.x >> 1;
 
-  if (warp < C::IDLE_WARP0) {
+  if (warp < C::EPI_WARP0) {
     setmaxnreg_dec<C::REGS_CTRL>();
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer (each CTA)
@@ -376,31 +381,37 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
         }
       }
     }
-  } else if (warp < C::EPI_WARP0) {
-    setmaxnreg_dec<C::REGS_IDLE>();
   } else {
     setmaxnreg_inc<C::REGS_EPI>();
-    // ------------------------------------------------------------ epilogue (each CTA, 8 warps)
+    // ------------------------------------------------------------ epilogue (each CTA, 12 warps)
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    constexpr int HC = C::BN / 2;
-    const int col0 = ((warp - C::EPI_WARP0) >> 2) * HC;
+    const int part = (warp - C::EPI_WARP0) >> 2;  // 0: columns 0..63, 1: 64..159, 2: 160..255
+    const int col0 = part == 0 ? 0 : C::EPI_COLS_FIRST + (part - 1) * C::EPI_COLS;
     const float alpha0 = (p.flags & F_ALPHA_DEVICE) ? __ldg(p.alpha_dev) : p.alpha;
     const uint16_t leader_mask = static_cast<uint16_t>(1u << leader);
     uint32_t acc_phase = 0;
-    for (int u = pair0; u < p.num_units; u += pairs) {
-      const UnitCoord c = decode_unit<EXT>(p, u);
-      const float alpha = unit_alpha<EXT>(p, c, alpha0);
-      // each warp on its own: a warp that gives up leaves the loop, and none waits for another
-      if (!wait_bounded_cluster(bar_tfull, acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE)) break;
-      tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      const int m = (c.m_blk * 2 + static_cast<int>(rank & 1u)) * C::BM + row;
-      const int nbase = c.n_blk * C::BN;
-      // The whole row segment comes out of TMEM before any arithmetic and the accumulator is
-      // released at once: the next tile's MMAs need all of it, and holding it through the
-      // epilogue math stalled them for longer than the math itself takes.
-      auto release = [&]() {
+    // The whole row segment comes out of TMEM before any arithmetic and the accumulator is
+    // released at once: the next tile's MMAs need all of it, and holding it through the epilogue
+    // math stalled them for longer than the math itself takes (the NVFP4 output too: holding
+    // the only accumulator through its encoding, 8192^3 took 315 us against 180 us with a 16-bit
+    // output).
+    auto tile = [&](auto cols_tag) {
+      constexpr int COLS = decltype(cols_tag)::value;
+      for (int u = pair0; u < p.num_units; u += pairs) {
+        const UnitCoord c = decode_unit<EXT>(p, u);
+        const float alpha = unit_alpha<EXT>(p, c, alpha0);
+        // each warp on its own: a warp that gives up leaves the loop, and none waits for another
+        if (!wait_bounded_cluster(bar_tfull, acc_phase, abort_flag, p, ST_TIMEOUT_EPILOGUE)) break;
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const int m = (c.m_blk * 2 + static_cast<int>(rank & 1u)) * C::BM + row;
+        const int nbase = c.n_blk * C::BN;
+        uint32_t r[COLS];
+#pragma unroll
+        for (int ch = 0; ch < COLS / 32; ++ch)
+          tmem_ld_32x32b_x32(t_row + col0 + ch * 32, reinterpret_cast<uint32_t(&)[32]>(r[32 * ch]));
+        tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -409,18 +420,14 @@ __global__ void __launch_bounds__(PairCfg<KIND, KC>::THREADS, 1) bsg_gemm_pair_k
           else
             tc_commit_pair_mc(bar_tempty, leader_mask);
         }
-      };
-      // (the NVFP4 output too: holding the only accumulator through its encoding stalled the next
-      // tile's MMAs, 8192^3 315 us against 180 us with a 16-bit output)
-      uint32_t r[HC];
-#pragma unroll
-      for (int ch = 0; ch < HC / 32; ++ch)
-        tmem_ld_32x32b_x32(t_row + col0 + ch * 32, reinterpret_cast<uint32_t(&)[32]>(r[32 * ch]));
-      tmem_ld_wait();
-      release();
-      epilogue_row<OUT, HC / 16, EXT>(p, c.batch, m, m < p.M, nbase + col0, r, alpha);
-      acc_phase ^= 1u;
-    }
+        epilogue_row<OUT, COLS / 16, EXT>(p, c.batch, m, m < p.M, nbase + col0, r, alpha);
+        acc_phase ^= 1u;
+      }
+    };
+    if (part == 0)
+      tile(std::integral_constant<int, C::EPI_COLS_FIRST>{});
+    else
+      tile(std::integral_constant<int, C::EPI_COLS>{});
   }
 
   // ------------------------------------------------------------ teardown
