@@ -148,19 +148,19 @@ bool find_kernel(int kind, int out, unsigned flags, int batches, bool pair, int 
 bool find_kernel_variant(int kind, int out, bool ext, bool pair, int bn, int kc, GemmKernelInfo* info);
 
 // Quantisers (stream-ordered).  See bsg_quantize / bsg_quantize_bf16 in include/bsgemm.h; the
-// uint16_t forms read BF16 bit patterns.
-cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+// uint16_t forms read BF16 bit patterns; sms: the device's SM count (the grids are persistent).
+cudaError_t launch_quantize_mx(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf, int sms,
                                cudaStream_t s);
-cudaError_t launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
+cudaError_t launch_quantize_mx(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf, int sms,
                                cudaStream_t s);
 cudaError_t launch_quantize_nv(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
-                               float* global_scale, cudaStream_t s);
+                               float* global_scale, int sms, cudaStream_t s);
 cudaError_t launch_quantize_nv(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
-                               float* global_scale, cudaStream_t s);
+                               float* global_scale, int sms, cudaStream_t s);
 // NVFP4 with the global scale given in device memory (one pass, no amax).
 cudaError_t launch_quantize_nv_scaled(const float* x, int rows, int K, uint8_t* codes, uint8_t* sf,
-                                      const float* global_scale, cudaStream_t s);
+                                      const float* global_scale, int sms, cudaStream_t s);
 cudaError_t launch_quantize_nv_scaled(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* sf,
-                                      const float* global_scale, cudaStream_t s);
+                                      const float* global_scale, int sms, cudaStream_t s);
 
 }  // namespace bsg

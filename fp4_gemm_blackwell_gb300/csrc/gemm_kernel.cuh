@@ -402,8 +402,7 @@ template <int G, bool EXT>
 __device__ __forceinline__ void epilogue_row_nv4(const GemmParams& p, int m, bool row_in, int n0, const uint32_t* r,
                                                  float alpha) {
   if (m >= ((p.M + 127) & ~127)) return;
-  const float s = __ldg(p.d_scale);
-  const float d = __fmul_rn(6.0f, s);
+  const NvTensorScale ts = nv_tensor_scale(__ldg(p.d_scale));
   const int cols_pad = p.sfd_cols4 * 4;
   uint8_t* drow = static_cast<uint8_t*>(p.d) + static_cast<size_t>(m) * (p.N >> 1);
   const bool ext = EXT && (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW));
@@ -426,7 +425,7 @@ __device__ __forceinline__ void epilogue_row_nv4(const GemmParams& p, int m, boo
         epi_vals<OUT_NV4, 8>(p, n + 8, v + 8, alpha, y + 8);
       }
       uint32_t lo, hi;
-      sc = nv_encode_block16(y, s, d, lo, hi);
+      sc = nv_encode_block16(y, ts, lo, hi);
       *reinterpret_cast<uint2*>(drow + (n >> 1)) = make_uint2(lo, hi);
     }
     if (c < cols_pad) p.sfd[sf_swizzle_offset(m, c, p.sfd_cols4)] = static_cast<uint8_t>(sc);
@@ -588,9 +587,8 @@ __device__ __forceinline__ void nv4_quarter(const GemmParams& p, const UnitCoord
   if (row_live<EXT>(p, c, m)) {
     float y[4];
     epi4_values<OUT_NV4, EXT>(p, c.batch, m, n, a, braw, EXT ? row_alpha(p, alpha, m) : alpha, y);
-    const float s = __ldg(p.d_scale);
     uint32_t codes;
-    sc = nv_encode_quad(y, s, __fmul_rn(6.0f, s), codes);
+    sc = nv_encode_quad(y, nv_tensor_scale(__ldg(p.d_scale)), codes);
     *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(p.d) + static_cast<size_t>(m) * (p.N >> 1) + (n >> 1)) =
         static_cast<uint16_t>(codes);
   }

@@ -1022,9 +1022,10 @@ static bsg_status quantize_entry(bsg_kind kind, const T* x, int rows, int K, voi
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e =
       kind == BSG_MXFP8
-          ? bsg::launch_quantize_mx(x, rows, K, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(sf), st)
+          ? bsg::launch_quantize_mx(x, rows, K, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(sf), di.sms,
+                                    st)
           : bsg::launch_quantize_nv(x, rows, K, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(sf),
-                                    global_scale, st);
+                                    global_scale, di.sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
   return BSG_OK;
 }
@@ -1060,9 +1061,9 @@ BSG_API bsg_status bsg_quantize_nvfp4_scaled(const void* x, int bf16_input, int 
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e =
       bf16_input ? bsg::launch_quantize_nv_scaled(static_cast<const uint16_t*>(x), rows, K, static_cast<uint8_t*>(codes),
-                                                  static_cast<uint8_t*>(sf), global_scale, st)
+                                                  static_cast<uint8_t*>(sf), global_scale, di.sms, st)
                  : bsg::launch_quantize_nv_scaled(static_cast<const float*>(x), rows, K, static_cast<uint8_t*>(codes),
-                                                  static_cast<uint8_t*>(sf), global_scale, st);
+                                                  static_cast<uint8_t*>(sf), global_scale, di.sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
   return BSG_OK;
 }
