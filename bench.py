@@ -844,6 +844,8 @@ def case_arm(args):
     (for profiler captures and quick timing); prints one JSON line."""
     if args.case in CUBLAS_CASES:
         return cublas_case(args)
+    if args.case in QUANT_CASES:
+        return quant_case(args)
     import __graft_entry__
     import fp4_gemm_blackwell_gb300 as bsg
     __graft_entry__.build()
@@ -917,6 +919,25 @@ def cublas_case(args):
     return 0
 
 
+# The quantisers on an 8192 x 8192 activation: (kind, BF16 input, global scale given).
+QUANT_CASES = {"quantize_mxfp8_f32": ("mxfp8", False, False), "quantize_mxfp8_bf16": ("mxfp8", True, False),
+               "quantize_nvfp4_f32": ("nvfp4", False, False), "quantize_nvfp4_bf16": ("nvfp4", True, False),
+               "quantize_nvfp4_given_f32": ("nvfp4", False, True),
+               "quantize_nvfp4_given_bf16": ("nvfp4", True, True)}
+
+
+def quant_case(args):
+    """--case quantize_*: `steps` quantiser calls replayed as one CUDA graph after `warmup`."""
+    import __graft_entry__
+    import fp4_gemm_blackwell_gb300 as bsg
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    kind, bf16, given = QUANT_CASES[args.case]
+    r = quantiser(bsg, load_peaks(), kind, 8192, 8192, bf16, steps=args.steps, warmup=args.warmup, scaled=given)
+    print(json.dumps(dict({"case": args.case}, **r)), flush=True)
+    return 0
+
+
 METRIC = "block-scaled GEMM TFLOPS & % tensor peak (MXFP8, NVFP4); host µs/call vs kernel"
 WORKLOAD = "nvfp4_gemm M=N=K=8192, bf16 bias + SiLU, bf16 out"
 
@@ -934,7 +955,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only (no other workloads, no CPU baseline)")
-    ap.add_argument("--case", choices=sorted(CASES) + sorted(CUBLAS_CASES),
+    ap.add_argument("--case", choices=sorted(CASES) + sorted(CUBLAS_CASES) + sorted(QUANT_CASES),
                     help="time one workload with plain launches and exit")
     args = ap.parse_args()
     if args.case:

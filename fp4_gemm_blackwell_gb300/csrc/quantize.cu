@@ -299,13 +299,6 @@ __global__ void nv_finalize_kernel(float* global_scale) {
   *global_scale = __fdiv_rn(amax, 2688.0f);
 }
 
-static int grid_for(long long n, int threads) {
-  long long b = (n + threads - 1) / threads;
-  if (b < 1) b = 1;
-  if (b > 152 * 16) b = 152 * 16;
-  return static_cast<int>(b);
-}
-
 // CTAs of 256 threads of KERNEL resident on one SM, asked of the runtime once per kernel.
 template <auto KERNEL>
 static int resident_ctas() {
@@ -367,7 +360,8 @@ cudaError_t quantize_nv(const T* x, int rows, int K, uint8_t* codes, uint8_t* sf
   cudaError_t e = cudaMemsetAsync(global_scale, 0, sizeof(float), s);
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(rows) * K;
-  amax_kernel<T><<<grid_for(n / 8, 256), 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(global_scale));
+  amax_kernel<T><<<persistent_grid<amax_kernel<T>>(n / 32, sms), 256, 0, s>>>(x, n,
+                                                                                reinterpret_cast<unsigned*>(global_scale));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_nv<T, false>(x, rows, K, codes, sf, reinterpret_cast<unsigned*>(global_scale), sms, s);
