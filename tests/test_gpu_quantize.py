@@ -135,6 +135,19 @@ def test_bf16_full_size_operand():
     check("mxfp8", synth.as_bf16_bits(synth.normal(8000, 8192, seed=0)), bf16=True)
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("kind", ["mxfp8", "nvfp4"])
+def test_grid_stride_crosses_row_ends(kind, bf16):
+    # 20000 x 1120: 35 MXFP8 or 70 NVFP4 blocks a row and more blocks than either quantiser's
+    # grid has threads, so every thread visits several blocks a grid stride apart, and the stride
+    # (a multiple of 256 threads) is no multiple of the blocks per row: a thread's next block
+    # lies in another column of a later row.  The smaller cases give each thread one block, and
+    # the 8192-wide ones a stride that keeps the column.
+    gen = synth.normal if kind == "mxfp8" else synth.normal_rowscaled
+    x = gen(20000, 1120, seed=7)
+    check(kind, synth.as_bf16_bits(x) if bf16 else x, bf16=bf16)
+
+
 def test_nv_elements_at_rounding_thresholds():
     # One element of 2688 makes s = 1, so a block whose largest magnitude is 6 v (v a UE4M3 value)
     # gets den = v exactly.  With v not a power of two, x / den and x * (1 / den) can round
