@@ -39,30 +39,34 @@ static __device__ __noinline__ uint32_t e2m1_pair_div(float a, float b, float de
 // Packed float32 pairs, each lane exactly the scalar operation: (a0 b0, a1 b1) rounded to
 // nearest even, and (a0 b0 + c0, a1 b1 + c1) with one rounding, to nearest even (rn) or toward
 // minus infinity (rm).
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
   uint64_t v;
   asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
   return v;
 }
-__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
 __device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
   uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pack2(a0, a1)), "l"(pack2(b0, b1)));
-  unpack2(r, r0, r1);
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f32x2_pack(a0, a1)), "l"(f32x2_pack(b0, b1)));
+  f32x2_unpack(r, r0, r1);
 }
 __device__ __forceinline__ void ffma2_rn(float a0, float a1, float b0, float b1, float c0, float c1, float& r0,
                                          float& r1) {
   uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pack2(a0, a1)), "l"(pack2(b0, b1)), "l"(pack2(c0, c1)));
-  unpack2(r, r0, r1);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(f32x2_pack(a0, a1)), "l"(f32x2_pack(b0, b1)), "l"(f32x2_pack(c0, c1)));
+  f32x2_unpack(r, r0, r1);
 }
 __device__ __forceinline__ void ffma2_rm(float a0, float a1, float b0, float b1, float c0, float c1, float& r0,
                                          float& r1) {
   uint64_t r;
-  asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pack2(a0, a1)), "l"(pack2(b0, b1)), "l"(pack2(c0, c1)));
-  unpack2(r, r0, r1);
+  asm("fma.rm.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(f32x2_pack(a0, a1)), "l"(f32x2_pack(b0, b1)), "l"(f32x2_pack(c0, c1)));
+  f32x2_unpack(r, r0, r1);
 }
 
 // Quotients without a division, by Markstein's correction step (P. Markstein, "Computation of

@@ -299,7 +299,9 @@ __global__ void nv_finalize_kernel(float* global_scale) {
   *global_scale = __fdiv_rn(amax, 2688.0f);
 }
 
-// CTAs of 256 threads of KERNEL resident on one SM, asked of the runtime once per kernel.
+// CTAs of 256 threads of KERNEL resident on one SM, asked of the runtime once per kernel (a
+// failed query gives 1 and is asked again next time; its error is cleared so that the launch
+// reports its own).
 template <auto KERNEL>
 static int resident_ctas() {
   static std::atomic<int> cached{0};
@@ -307,7 +309,7 @@ static int resident_ctas() {
   if (n == 0) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, KERNEL, 256, 0) != cudaSuccess || n < 1) {
       (void)cudaGetLastError();
-      n = 1;
+      return 1;
     }
     cached.store(n, std::memory_order_relaxed);
   }
@@ -360,8 +362,8 @@ cudaError_t quantize_nv(const T* x, int rows, int K, uint8_t* codes, uint8_t* sf
   cudaError_t e = cudaMemsetAsync(global_scale, 0, sizeof(float), s);
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(rows) * K;
-  amax_kernel<T><<<persistent_grid<amax_kernel<T>>(n / 32, sms), 256, 0, s>>>(x, n,
-                                                                                reinterpret_cast<unsigned*>(global_scale));
+  const int grid = persistent_grid<amax_kernel<T>>(n / 32, sms);  // 32 elements a thread an iteration
+  amax_kernel<T><<<grid, 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(global_scale));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_nv<T, false>(x, rows, K, codes, sf, reinterpret_cast<unsigned*>(global_scale), sms, s);
