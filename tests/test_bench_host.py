@@ -82,3 +82,15 @@ def test_algorithmic_bytes_of_the_measured_configurations():
     assert bench.algorithmic_bytes("nvfp4", 128, 4096, 4096, bias=True, residual=True, factors=True) == \
         base + 128 * 4096 * 2 + (128 + 4096) * 4
     assert bench.algorithmic_bytes("nvfp4", 128, 4096, 4096, bias=True, L=8) == 8 * (base - 8192) + 8192
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    # The traffic records in profiles/traffic.json are keyed by this hash: a comment edit keeps
+    # them, any code edit drops them.
+    sys.path.insert(0, ROOT)
+    import bench
+    code = "int f(int x) {  // one\n  /* two\n     lines */ return x + 1;\n}\n"
+    assert bench.strip_comments(code) == "int f(int x) {\n   return x + 1;\n}"
+    assert bench.strip_comments(code.replace("// one", "// changed")) == bench.strip_comments(code)
+    assert bench.strip_comments(code.replace("x + 1", "x + 2")) != bench.strip_comments(code)
+    assert bench.recorded_traffic("bsg_gemm_pair_kernel<nvfp4>", "nvfp4_8192_bias_silu") is not None
