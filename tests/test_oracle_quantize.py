@@ -4,7 +4,10 @@ MXFP8: the scale exponent is the least e with amax <= 448 * 2**e (checked with
 exact fractions), and every element is the nearest E4M3 value of x / 2**e
 (exhaustive search).  NVFP4: hand-chosen inputs where every float32 step is
 exact, so the codes are known in closed form; the general case is checked
-element by element against an exhaustive nearest-value search of x / den.
+element by element against an exhaustive nearest-value search of x / den; and
+elements within a few ulps of every E2M1 threshold against E2M1(RN(x / den))
+computed with exact rationals (no float32 division: an oracle that multiplied by
+a rounded reciprocal instead fails this pin and passes the brute-force one).
 """
 
 from fractions import Fraction
@@ -119,6 +122,72 @@ def test_nv_quantiser_against_brute_force():
                 q = float(np.float32(blk[j] / den))
                 want = _nearest_brute(q, F.E2M1_VALUES, 6.0, 8) | (0x8 if np.signbit(q) else 0)
                 assert codes[r, 16 * b + j] == want
+
+
+def _rn_float32(q):
+    """The float32 nearest to the non-negative rational q, ties to the even significand (normal
+    and subnormal range; these tests stay far from overflow)."""
+    if q == 0:
+        return Fraction(0)
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1
+    e = max(e, -126)                                  # below 2^-126 the spacing stays 2^-149
+    scaled = q * Fraction(2) ** (23 - e)              # significand in units of the last place
+    n, rem = divmod(scaled.numerator, scaled.denominator)
+    twice = 2 * rem
+    if twice > scaled.denominator or (twice == scaled.denominator and n % 2 == 1):
+        n += 1
+    return Fraction(n) * Fraction(2) ** (e - 23)
+
+
+def _e2m1_code_exact(v):
+    """E2M1 code of the float32 value v (a Fraction, any sign): the nearest magnitude of the
+    value set, ties to the even code, saturating at 6, sign bit 0x8."""
+    mag = min(abs(v), Fraction(6))
+    vals = [Fraction(x) for x in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    best = min(range(8), key=lambda c: (abs(mag - vals[c]), c % 2))
+    return best | (0x8 if v < 0 else 0)
+
+
+def test_nv_elements_near_thresholds_match_exact_rationals():
+    # Dividends RN(T * den) and up to 4 float32 ulps either side of every E2M1 rounding threshold
+    # T, for block scales den = value(code) * s with s = amax / 2688 of a tensor whose amax has a
+    # long significand: the oracle's element codes against E2M1(RN(x / den)) computed with exact
+    # rationals, where numpy's float32 division is not used at all.
+    rng = np.random.default_rng(11)
+    thresholds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for amax in (np.float32(10.3125), np.float32(2688.0), np.float32(rng.uniform(1, 100))):
+        s = np.float32(amax / np.float32(2688.0))
+        for code in (0x30, 0x35, 0x3B, 0x41, 0x4E, 0x57):
+            den = np.float32(np.float32(F.E4M3_VALUES[code]) * s)
+            cand = []
+            for T in thresholds:
+                base = np.float32(np.float32(T) * den)
+                for k in range(-4, 5):
+                    v = np.float32(base)
+                    step = np.float32(np.inf) if k > 0 else np.float32(0)
+                    for _ in range(abs(k)):
+                        v = np.nextafter(v, step)
+                    cand.append(v)
+            cand = np.array(cand, dtype=np.float32)
+            cand[1::2] *= -1
+            for i in range(0, len(cand), 15):
+                blk = np.zeros(16, dtype=np.float32)
+                blk[0] = np.float32(np.float32(6.0) * den)     # block amax: its scale is `code`
+                chunk = cand[i:i + 15]
+                blk[1:1 + len(chunk)] = chunk
+                x = np.stack([blk, np.r_[amax, np.zeros(15, dtype=np.float32)].astype(np.float32)])
+                packed, sc, s_out = Q.quantize_nvfp4(x)
+                assert s_out == s and sc[0, 0] == code
+                codes = Q.unpack_e2m1(packed, 16)[0]
+                den_q = Fraction(float(den))
+                for j in range(16):
+                    q = _rn_float32(abs(Fraction(float(blk[j])) / den_q))
+                    want = _e2m1_code_exact(-q if np.signbit(blk[j]) else q)
+                    if q == 0 and np.signbit(blk[j]):
+                        want = 0x8
+                    assert codes[j] == want, (float(blk[j]), float(den), codes[j], want)
 
 
 def test_nv_tensor_amax_block_gets_max_scale():
