@@ -7,7 +7,8 @@ exact, so the codes are known in closed form; the general case is checked
 element by element against an exhaustive nearest-value search of x / den; and
 elements within a few ulps of every E2M1 threshold against E2M1(RN(x / den))
 computed with exact rationals (no float32 division: an oracle that multiplied by
-a rounded reciprocal instead fails this pin and passes the brute-force one).
+a rounded reciprocal instead fails this pin and passes the brute-force one); block
+amaxes near every E4M3 midpoint likewise for the scale step.
 """
 
 from fractions import Fraction
@@ -188,6 +189,37 @@ def test_nv_elements_near_thresholds_match_exact_rationals():
                     if q == 0 and np.signbit(blk[j]):
                         want = 0x8
                     assert codes[j] == want, (float(blk[j]), float(den), codes[j], want)
+
+
+def test_nv_block_scales_near_midpoints_match_exact_rationals():
+    # Block amaxes RN(m * d) and up to 3 float32 ulps either side of every midpoint m between two
+    # neighbouring E4M3 values (and past the largest), for given global scales with long
+    # significands: the oracle's scale codes against UE4M3(RN(amax / d)) computed with exact
+    # rationals (no float32 division).
+    pos = [c for c in range(0x7F) if np.isfinite(F.E4M3_VALUES[c])]
+    vals = [Fraction(float(F.E4M3_VALUES[c])) for c in pos]
+    mids = [(vals[i] + vals[i + 1]) / 2 for i in range(len(vals) - 1)] + [Fraction(464)]
+    for s in (np.float32(np.float32(10.3125) / np.float32(2688.0)), np.float32(0.0123456789),
+              np.float32(3.3333333)):
+        d = np.float32(np.float32(6.0) * s)
+        d_q = Fraction(float(d))
+        amaxes = []
+        for m in mids:
+            base = np.float32(float(m * d_q))
+            for k in range(-3, 4):
+                v = base
+                for _ in range(abs(k)):
+                    v = np.nextafter(v, np.float32(np.inf) if k > 0 else np.float32(0))
+                amaxes.append(v)
+        x = np.zeros((len(amaxes), 16), dtype=np.float32)
+        x[:, 0] = amaxes
+        _, sc, s_out = Q.quantize_nvfp4(x, s)
+        assert s_out == s
+        for r, a in enumerate(amaxes):
+            t = _rn_float32(Fraction(float(a)) / d_q)
+            mag = min(t, Fraction(448))
+            want = pos[min(range(len(pos)), key=lambda i: (abs(mag - vals[i]), pos[i] % 2))]
+            assert sc[r, 0] == want, (float(a), float(d), sc[r, 0], want)
 
 
 def test_nv_tensor_amax_block_gets_max_scale():
