@@ -217,3 +217,54 @@ def test_nvfp4_given_scale(rows, K, scale_factor, bf16):
     if scale_factor == 0.25:
         sat = ((oc & 0x7) == 0x7) | (((oc >> 4) & 0x7) == 0x7)
         assert (osf == 0x7E).any() and sat.any()   # saturation reached on both levels
+
+
+def test_nvfp4_given_scale_near_rounding_midpoints():
+    # bsg_quantize_nvfp4_scaled against the oracle on the inputs its exact-rational pins use: block
+    # amaxes within 3 ulps of every midpoint between neighbouring E4M3 values, and elements within
+    # 4 ulps of every E2M1 threshold, for global scales with long significands (both quotients
+    # x / den and amax / d land within a rounding of a code boundary).
+    e4 = [float(F.E4M3_VALUES[c]) for c in range(0x7F) if np.isfinite(F.E4M3_VALUES[c])]
+    mids = [(e4[i] + e4[i + 1]) / 2 for i in range(len(e4) - 1)] + [464.0]
+    for s in (np.float32(np.float32(10.3125) / np.float32(2688.0)), np.float32(0.0123456789)):
+        d = np.float32(np.float32(6.0) * s)
+        rows = []
+        for m in mids:                                           # block-scale midpoints
+            base = np.float32(np.float64(m) * np.float64(d))
+            for k in range(-3, 4):
+                v = base
+                for _ in range(abs(k)):
+                    v = np.nextafter(v, np.float32(np.inf) if k > 0 else np.float32(0))
+                blk = np.zeros(16, dtype=np.float32)
+                blk[0] = v
+                rows.append(blk)
+        for code in (0x30, 0x35, 0x3B, 0x41, 0x4E, 0x57):       # element thresholds
+            den = np.float32(np.float32(F.E4M3_VALUES[code]) * s)
+            cand = []
+            for T in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0):
+                base = np.float32(np.float32(T) * den)
+                for k in range(-4, 5):
+                    v = base
+                    for _ in range(abs(k)):
+                        v = np.nextafter(v, np.float32(np.inf) if k > 0 else np.float32(0))
+                    cand.append(v)
+            cand = np.array(cand, dtype=np.float32)
+            cand[1::2] *= -1
+            for i in range(0, len(cand), 15):
+                blk = np.zeros(16, dtype=np.float32)
+                blk[0] = np.float32(np.float32(6.0) * den)
+                chunk = cand[i:i + 15]
+                blk[1:1 + len(chunk)] = chunk
+                rows.append(blk)
+        if len(rows) % 2:
+            rows.append(np.zeros(16, dtype=np.float32))
+        x = np.stack(rows).reshape(-1, 32)
+        nrows, K = x.shape
+        sd = torch.tensor([float(s)], dtype=torch.float32, device="cuda")
+        codes = torch.full((nrows * K // 2,), 0xCD, dtype=torch.uint8, device="cuda")
+        sf = torch.full((bsg.bsg_sf_bytes(bsg.BSG_NVFP4, nrows, K),), 0xAB, dtype=torch.uint8, device="cuda")
+        bsg.bsg_quantize_nvfp4_scaled(torch.from_numpy(x).cuda(), nrows, K, codes, sf, sd, bf16_input=False)
+        torch.cuda.synchronize()
+        oc, osf, _ = Q.quantize_nvfp4(x, s)
+        assert np.array_equal(codes.cpu().numpy(), oc.ravel())
+        assert np.array_equal(sf.cpu().numpy(), L.swizzle(osf))
